@@ -1,0 +1,16 @@
+"""CPU oracle for W4A16 RTN quantization and GEMM.  Test infrastructure only:
+see ``w4a16_oracle`` for what it computes and which passages it follows."""
+
+from .w4a16_oracle import (  # noqa: F401
+    GROUP,
+    QMAX,
+    QMIN,
+    bf16_bits_to_f32,
+    dequantize,
+    gemm,
+    pack_codes,
+    quantize,
+    quantize_f32,
+    scales_f32,
+    unpack_codes,
+)
