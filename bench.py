@@ -1,0 +1,421 @@
+#!/usr/bin/env python3
+"""Benchmark of the W4A16 hot path on GB300.
+
+One step = one pass of the whole path over one batch of synthetic inputs:
+for every projection of the workload, RTN quantize/pack of its bf16 weight
+(w4a16_quantize) followed by the W4A16 GEMM (w4a16_gemm).  Default workload:
+the action-expert projections at M = 50 tokens, (N, K) = (2048, 1024),
+(1024, 1024), (8192, 1024), (1024, 4096), seeds 1..4.
+
+Timing: W untimed warm-up steps, then exactly K timed steps between CUDA
+events on the launching stream, with a device synchronize (and, for N > 1,
+a barrier) on both sides; the max over ranks is reported.  Every step reads
+a different copy of all inputs and the copies together exceed 3x the L2
+size, so each step streams its inputs from HBM.  Kernel durations for the
+roofline come from CUDA events recorded around each launch on the same
+stream during the timed steps.
+
+`value` is whole-job algorithmic HBM bytes per second (GB/s): for each
+quantize 2.515625 * N * K bytes (bf16 read, codes and scales written), for
+each GEMM 0.515625 * N * K + 2 * M * K bytes (packed weight, scales and
+activations read).  GEMM TFLOP/s and weight-stream GB/s are reported per
+kernel alongside.
+
+--impl reference times the CPU oracle (test infrastructure, never the
+product path) on a bounded sample of the same workload.
+Multi-GPU: the path is replicated (each rank runs the whole workload on its
+own GPU); there is no collective on the data path.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+L2_BYTES = 129 * 1024 * 1024
+METRIC = "W4A16 GEMM TFLOPS & weight-stream GB/s vs roofline (M=1..8192), 1×GB300"
+
+
+# ----------------------------------------------------------------- helpers
+def quant_bytes(N, K):
+    return 2.515625 * N * K
+
+
+def gemm_bytes(M, N, K):
+    return 0.515625 * N * K + 2.0 * M * K
+
+
+def gemm_flops(M, N, K):
+    return 2.0 * M * N * K
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=float(d["hbm_gbs"]), bf16_tflops=float(d["bf16_tflops"]),
+                    bf16_tflops_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "weight_only_int4_rtn_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()[:12]
+
+
+def dram_traffic(kernel: str, workload: str):
+    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if it
+    was taken on the current kernel sources; else None."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    cur = kernel_source_hash()
+    with open(p) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 4 and not line.startswith("#"):
+                k, w, b, src = parts[:4]
+                if k == kernel and w == workload and src == cur:
+                    return float(b)
+    return None
+
+
+class ClockSampler:
+    """Samples nvidia-smi SM clocks and throttle reasons every 200 ms."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.samples = []
+        self._stop = threading.Event()
+        self._t = None
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                out = subprocess.run(
+                    ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                     "--format=csv,noheader,nounits"], capture_output=True, text=True, timeout=5)
+                if out.returncode == 0 and out.stdout.strip():
+                    self.samples.append([x.strip() for x in out.stdout.strip().split(",")])
+            except Exception:
+                pass
+            self._stop.wait(0.2)
+
+    def __enter__(self):
+        self._t = threading.Thread(target=self._run, daemon=True)
+        self._t.start()
+        return self
+
+    def __exit__(self, *exc):
+        self._stop.set()
+        if self._t is not None:
+            self._t.join(timeout=10)
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(s[0]) for s in self.samples if s[0].replace(".", "").isdigit()]
+        mx = [float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for s in self.samples:
+            for name, v in zip(names, s[4:8]):
+                if v.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(self.samples)}
+
+
+# ------------------------------------------------------------- GPU arm
+def run_gpu(args, rank, world):
+    import numpy as np
+    import torch
+
+    import weight_only_int4_rtn_gb300 as w4
+    from weight_only_int4_rtn_gb300 import synthetic
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    cases = synthetic.WORKLOADS[args.workload]
+    if args.tune:
+        for c in cases:
+            w4.w4a16_tune(c.M, c.N, c.K)
+
+    # one set of inputs per copy; the copies rotate step by step
+    per_copy = sum(2 * c.N * c.K + c.N * c.K // 2 + 2 * c.N * c.K // 128 + 2 * c.M * c.K +
+                   2 * c.M * c.N for c in cases)
+    copies = max(1, min(64, -(-3 * L2_BYTES // per_copy)))
+    host_sets = [synthetic.draw(c) for c in cases]
+    sets = []
+    for r in range(copies):
+        s = []
+        for c, (W, A, b) in zip(cases, host_sets):
+            Wd = W.to(dev) if r == 0 else sets[0][len(s)]["W"].clone()
+            Ad = A.to(dev) if r == 0 else sets[0][len(s)]["A"].clone()
+            s.append(dict(W=Wd, A=Ad,
+                          packed=torch.empty(c.N, c.K // 2, dtype=torch.uint8, device=dev),
+                          scales=torch.empty(c.K // 128, c.N, dtype=torch.float16, device=dev),
+                          Y=torch.empty(c.M, c.N, dtype=torch.bfloat16, device=dev)))
+        sets.append(s)
+    ws_bytes = max(w4.w4a16_gemm_workspace_bytes_max(c.M, c.N, c.K) for c in cases)
+    ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    n_k = 2 * len(cases)
+    def step(r, evs=None):
+        for j, c in enumerate(cases):
+            s = sets[r % copies][j]
+            if evs is not None:
+                evs[2 * j][0].record(stream)
+            w4.w4a16_quantize(s["W"], packed=s["packed"], scales=s["scales"])
+            if evs is not None:
+                evs[2 * j][1].record(stream)
+                evs[2 * j + 1][0].record(stream)
+            w4.w4a16_gemm(s["A"], s["packed"], s["scales"], Y=s["Y"], workspace=ws)
+            if evs is not None:
+                evs[2 * j + 1][1].record(stream)
+
+    for r in range(args.warmup):
+        step(r)
+    torch.cuda.synchronize(dev)
+    if w4.w4a16_get_device_error() != w4.W4A16_OK:
+        raise RuntimeError("device error during warm-up")
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    # --- timed region: whole steps, back to back
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = w4.w4a16_launch_count()
+    barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index) as clk:
+        start.record(stream)
+        for r in range(args.steps):
+            step(args.warmup + r)
+        end.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier()
+    launches = w4.w4a16_launch_count() - launches0
+    elapsed_ms = start.elapsed_time(end)
+
+    # --- per-kernel durations (separate pass with events around each launch)
+    kev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_k)]
+           for _ in range(args.steps)]
+    torch.cuda.synchronize(dev)
+    for r in range(args.steps):
+        step(args.warmup + args.steps + r, kev[r])
+    torch.cuda.synchronize(dev)
+    if w4.w4a16_get_device_error() != w4.W4A16_OK:
+        raise RuntimeError("device error during timing")
+    kern_ms = [statistics.mean(kev[r][k][0].elapsed_time(kev[r][k][1]) for r in range(args.steps))
+               for k in range(n_k)]
+
+    # --- e2e: pinned host inputs -> device, the path, result -> host
+    pinned = [(W.pin_memory(), A.pin_memory()) for (W, A, b) in host_sets]
+    yh = [torch.empty(c.M, c.N, dtype=torch.bfloat16).pin_memory() for c in cases]
+    h2d = sum(W.numel() * 2 + A.numel() * 2 for W, A in pinned)
+    d2h = sum(c.M * c.N * 2 for c in cases)
+    s0 = sets[0]
+    for _ in range(2):
+        for j, c in enumerate(cases):
+            s0[j]["W"].copy_(pinned[j][0], non_blocking=True)
+            s0[j]["A"].copy_(pinned[j][1], non_blocking=True)
+            w4.w4a16_quantize(s0[j]["W"], packed=s0[j]["packed"], scales=s0[j]["scales"])
+            w4.w4a16_gemm(s0[j]["A"], s0[j]["packed"], s0[j]["scales"], Y=s0[j]["Y"], workspace=ws)
+            yh[j].copy_(s0[j]["Y"], non_blocking=True)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    e0.record(stream)
+    for _ in range(args.steps):
+        for j, c in enumerate(cases):
+            s0[j]["W"].copy_(pinned[j][0], non_blocking=True)
+            s0[j]["A"].copy_(pinned[j][1], non_blocking=True)
+            w4.w4a16_quantize(s0[j]["W"], packed=s0[j]["packed"], scales=s0[j]["scales"])
+            w4.w4a16_gemm(s0[j]["A"], s0[j]["packed"], s0[j]["scales"], Y=s0[j]["Y"], workspace=ws)
+            yh[j].copy_(s0[j]["Y"], non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1)
+
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([elapsed_ms, e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms, e2e_ms = float(t[0]), float(t[1])
+
+    bytes_step = sum(quant_bytes(c.N, c.K) + gemm_bytes(c.M, c.N, c.K) for c in cases)
+    flops_step = sum(gemm_flops(c.M, c.N, c.K) for c in cases)
+    ms_step = elapsed_ms / args.steps
+    value = world * bytes_step * args.steps / (elapsed_ms * 1e-3) / 1e9
+    e2e_value = world * bytes_step * args.steps / (e2e_ms * 1e-3) / 1e9
+
+    peaks = load_peaks()
+    kernels = []
+    for j, c in enumerate(cases):
+        tq, tg = kern_ms[2 * j], kern_ms[2 * j + 1]
+        kernels.append(dict(kernel="rtn_quantize", shape=[c.N, c.K], us=round(tq * 1e3, 3),
+                            gbs=round(quant_bytes(c.N, c.K) / (tq * 1e-3) / 1e9, 1)))
+        kernels.append(dict(kernel="w4a16_gemm_tc", shape=[c.M, c.N, c.K], us=round(tg * 1e3, 3),
+                            variant=w4.w4a16_variant_name(w4.w4a16_select_variant(c.M, c.N, c.K)),
+                            tflops=round(gemm_flops(c.M, c.N, c.K) / (tg * 1e-3) / 1e12, 2),
+                            weight_gbs=round(0.515625 * c.N * c.K / (tg * 1e-3) / 1e9, 1),
+                            gbs=round(gemm_bytes(c.M, c.N, c.K) / (tg * 1e-3) / 1e9, 1)))
+    # dominant kernel: the kind with the larger share of kernel time
+    t_q = sum(kern_ms[0::2])
+    t_g = sum(kern_ms[1::2])
+    if t_q >= t_g:
+        dom, dom_bytes = "rtn_quantize", sum(quant_bytes(c.N, c.K) for c in cases)
+        dom_ms, launches_dom = t_q, len(cases)
+        bound, achieved, peak, unit = "hbm", None, peaks["hbm_gbs"], "GB/s"
+        achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+    else:
+        dom_ms, launches_dom = t_g, len(cases)
+        big = max(cases, key=lambda c: gemm_flops(c.M, c.N, c.K) / max(gemm_bytes(c.M, c.N, c.K), 1))
+        ai = gemm_flops(big.M, big.N, big.K) / gemm_bytes(big.M, big.N, big.K)
+        tensor_bound = ai > peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+        dom = "w4a16_gemm_tc"
+        if tensor_bound:
+            bound, peak, unit = "tensor", peaks["bf16_tflops"], "TFLOP/s"
+            achieved = sum(gemm_flops(c.M, c.N, c.K) for c in cases) / (dom_ms * 1e-3) / 1e12
+        else:
+            bound, peak, unit = "hbm", peaks["hbm_gbs"], "GB/s"
+            achieved = sum(gemm_bytes(c.M, c.N, c.K) for c in cases) / (dom_ms * 1e-3) / 1e9
+    traffic = dram_traffic(dom, args.workload)
+    roofline = dict(bound=bound, achieved=round(achieved, 2), peak=peak, unit=unit,
+                    frac=round(achieved / peak, 4),
+                    traffic=None if traffic is None else traffic,
+                    kernel=dom, launches_per_step=launches_dom, peak_source=peaks["source"])
+
+    out = dict(metric=METRIC, value=round(value, 2), unit="GB/s", n_gpus=world, steps=args.steps,
+               warmup=args.warmup, ms_per_step=round(ms_step, 5), higher_is_better=True,
+               scaling="weak", vs_baseline=None, dtype="bf16", data="synthetic",
+               config=dict(workload=args.workload,
+                           shapes=[[c.M, c.N, c.K] for c in cases],
+                           step="rtn_quantize + w4a16_gemm per projection",
+                           l2="inputs rotate over %d copies (%.0f MB > 3x L2)" % (copies, copies * per_copy / 2**20),
+                           parallelism=f"replicas x{world}"),
+               gemm=dict(tflops=round(flops_step * args.steps * world / (elapsed_ms * 1e-3) / 1e12, 3)),
+               kernels=kernels, roofline=roofline, clocks=clk.summary(),
+               gpu_launches=int(launches),
+               e2e=dict(value=round(e2e_value, 2), unit="GB/s", h2d_bytes_per_step=int(h2d),
+                        d2h_bytes_per_step=int(d2h)))
+    return out
+
+
+# ------------------------------------------------------------- CPU oracle
+def time_oracle(workload: str, budget_s: float):
+    """The oracle as it stands, on the host cores, over whole passes of the
+    workload (quantize + GEMM per projection) until `budget_s` is used."""
+    import numpy as np
+
+    import oracle
+    from weight_only_int4_rtn_gb300 import synthetic
+
+    cases = synthetic.WORKLOADS[workload]
+    inputs = []
+    for c in cases:
+        W, A, b = synthetic.draw(c)
+        inputs.append((synthetic.bits(W), synthetic.bits(A)))
+    # bounded sample: for very large workloads only the first rows of A
+    sample_rows = [min(c.M, 64) for c in cases]
+    done_bytes = 0.0
+    passes = 0
+    t0 = time.perf_counter()
+    while True:
+        for c, (wb, ab), mr in zip(cases, inputs, sample_rows):
+            p, s = oracle.quantize(wb)
+            oracle.gemm(ab[:mr], p, s)
+            done_bytes += quant_bytes(c.N, c.K) + gemm_bytes(mr, c.N, c.K)
+        passes += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    sample = (f"{passes} pass(es) of {workload}: oracle quantize + FP32 GEMM per projection"
+              + ("" if all(mr == c.M for mr, c in zip(sample_rows, cases)) else
+                 ", GEMM on the first 64 rows of A"))
+    return dict(value=round(done_bytes / dt / 1e9, 4), unit="GB/s", cores=cores, kind="oracle",
+                sample=sample, seconds=round(dt, 2))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="expert_m50",
+                    choices=["tiny", "expert_m50", "prefix_m816", "sweep", "large"])
+    ap.add_argument("--tune", action="store_true", help="tune the variant table first")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        t_budget = max(5.0, min(60.0, args.cpu_budget * (args.steps + args.warmup) / 10))
+        cb = time_oracle(args.workload, t_budget)
+        line = dict(metric=METRIC, value=cb["value"], unit="GB/s", n_gpus=world, steps=args.steps,
+                    warmup=args.warmup, ms_per_step=None, higher_is_better=True, scaling="weak",
+                    vs_baseline=None, dtype="f32", data="synthetic", impl="reference",
+                    config=dict(workload=args.workload), cpu_baseline=cb,
+                    e2e=dict(value=cb["value"], unit="GB/s", h2d_bytes_per_step=0,
+                             d2h_bytes_per_step=0))
+        print(json.dumps(line), flush=True)
+        return 0
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist.init_process_group("nccl")
+
+    from __graft_entry__ import build
+    build()
+    out = run_gpu(args, rank, world)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = time_oracle(args.workload, args.cpu_budget)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,195 @@
+/*
+ * w4a16.h - C ABI of the GB300 (sm_103a) weight-only INT4 round-to-nearest
+ * library: quantize/pack of bf16 weights and the W4A16 GEMM.
+ *
+ * The operation.  "Kernel dispatch and Humming quantization in PhyAI",
+ * section "Humming makes the separation useful": weights are post-training
+ * quantized at load by round-to-nearest; attention and MLP projections are
+ * stored as INT4 with group size 128 while activations stay BF16 (or FP16),
+ * and the quantized layers execute through a kernel that understands the
+ * packed layout (a plain BF16 GEMM cannot execute it).  The method
+ * specification fixes the rest: symmetric codes in [-8, 7], one fp16 scale
+ * per group of 128 consecutive K values equal to fp32 absmax / 7, round half
+ * to even, and scale 1 for an all-zero group.
+ *
+ * Data layout (all row-major, all device memory, all owned by the caller):
+ *   W       [N, K]     bf16   weight to quantize (K contiguous)
+ *   packed  [N, K/2]   uint8  code of k = 2j in the low nibble of byte j,
+ *                             code of k = 2j+1 in the high nibble, two's
+ *                             complement
+ *   scales  [K/128, N] fp16   scale of group g of row n at scales[g * N + n]
+ *   A       [M, K]     bf16   activations
+ *   bias    [N]        bf16   optional
+ *   Y       [M, N]     bf16   Y = bf16(A . dequant(W)^T + bias), fp32
+ *                             accumulation, bias added in fp32 before the one
+ *                             final rounding ("Piper Kernels", section "NVFP4
+ *                             construction": scales and bias are applied in
+ *                             FP32 before the final output conversion)
+ *
+ * Calling conventions ("Piper Kernels", section "Validation contract"):
+ *   - Arguments are checked from metadata only (sizes, alignment, group):
+ *     no tensor contents are read, no synchronisation, no allocation, no
+ *     extra launch.  Contents are caller preconditions: finite values and
+ *     |w| small enough that absmax / 7 fits fp16.  Inputs and outputs must
+ *     not alias.
+ *   - w4a16_quantize and w4a16_gemm are asynchronous on `stream` (a
+ *     cudaStream_t; NULL = the legacy default stream) and can be captured
+ *     into a CUDA graph.  They launch on the current CUDA device.
+ *   - Argument errors are returned before anything is launched.  A launch
+ *     failure returns W4A16_ERR_CUDA.  A kernel whose internal wait ran
+ *     out of time records W4A16_ERR_TIMEOUT in a device word that
+ *     w4a16_get_device_error reports.
+ *   - There is no CPU fallback: every call runs on the GPU or fails.
+ *
+ * Shape limits: group == 128; K % 128 == 0; K >= 128; N % 8 == 0; N >= 8;
+ * M >= 1; all of M, N, K < 2^31 and M*N, N*K < 2^40.  Every pointer must be
+ * 16-byte aligned.
+ */
+#ifndef W4A16_H_
+#define W4A16_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  W4A16_OK = 0,
+  W4A16_ERR_INVALID_ARG = 1,  /* null pointer, size out of range          */
+  W4A16_ERR_UNSUPPORTED = 2,  /* group != 128, K % 128, N % 8, bad variant */
+  W4A16_ERR_ALIGNMENT = 3,    /* a pointer is not 16-byte aligned          */
+  W4A16_ERR_WORKSPACE = 4,    /* workspace missing or too small            */
+  W4A16_ERR_NO_VARIANT = 5,   /* no GEMM variant is usable for the shape   */
+  W4A16_ERR_CUDA = 6,         /* a CUDA runtime/driver call failed         */
+  W4A16_ERR_TIMEOUT = 7       /* a device-side bounded wait expired        */
+} w4a16_status;
+
+/* Human-readable name of a status code.  Never NULL. */
+const char* w4a16_status_string(int status);
+
+/* Bytes of the packed code array for an [N, K] weight: N * K / 2. */
+size_t w4a16_packed_bytes(int64_t N, int64_t K);
+
+/* Bytes of the scale array: (K / group) * N * 2.  0 if group != 128. */
+size_t w4a16_scales_bytes(int64_t N, int64_t K, int group);
+
+/*
+ * RTN quantize/pack ("Kernel dispatch and Humming quantization in PhyAI",
+ * section "Humming makes the separation useful": round-to-nearest at load,
+ * INT4, group 128).  For each row n and group g:
+ *   amax = max |W[n, k]| (fp32);  s = fp16_rn(amax / 7.0f);  s = 1 if s == 0;
+ *   q = clamp(rint_even(W[n, k] / s), -8, 7)   (IEEE fp32 division)
+ * writes the codes to packed_out and s to scales_out[g * N + n].
+ * W: [N, K] bf16 (read);  packed_out: N*K/2 bytes;  scales_out: (K/128)*N
+ * fp16 (both written).  One kernel launch on `stream`.
+ */
+int w4a16_quantize(const void* W_bf16, int64_t N, int64_t K, int group, void* packed_out,
+                   void* scales_out, void* stream);
+
+/*
+ * Workspace the GEMM needs for this shape with the variant the library's
+ * table selects (split-K partial sums and per-tile arrival counters).  May
+ * be 0.  The workspace must be zero-filled before its first use
+ * (w4a16_workspace_init does that); every successful call leaves it
+ * reusable.  One workspace must not be used by two GEMMs that can run at
+ * the same time.
+ */
+size_t w4a16_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+/* Upper bound of w4a16_gemm_workspace_bytes over every variant of the
+ * catalogue for this shape. */
+size_t w4a16_gemm_workspace_bytes_max(int64_t M, int64_t N, int64_t K);
+
+/* Zero `bytes` of a workspace asynchronously on `stream` (cudaMemsetAsync). */
+int w4a16_workspace_init(void* workspace, size_t bytes, void* stream);
+
+/*
+ * W4A16 GEMM: Y[M, N] = bf16( A[M, K] . dequant(packed, scales)^T + bias ),
+ * dequant(q, s) = q * s, fp32 accumulation on the tcgen05 tensor cores.
+ * bias_bf16_or_null may be NULL.  workspace may be NULL when
+ * w4a16_gemm_workspace_bytes(M, N, K) is 0.  The variant comes from the
+ * library's per-shape table (w4a16_select_variant).  1 launch on `stream`.
+ */
+int w4a16_gemm(const void* A_bf16, int64_t M, int64_t N, int64_t K, const void* packed,
+               const void* scales, int group, const void* bias_bf16_or_null, void* Y_bf16,
+               void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------- variants
+ * The GEMM catalogue holds several kernel configurations (activation-tile
+ * width, scaling mode, schedule).  The table maps a shape to one of them; it
+ * is filled by measurement (w4a16_tune), in the spirit of the memoized,
+ * autotuned kernel choice of "Kernel dispatch and Humming quantization in
+ * PhyAI", section "Keep selection work out of repeated inference".  A shape
+ * with no entry uses a fixed rule; both only ever choose GPU variants. */
+
+/* Number of variants in the catalogue; ids are 0 .. count-1. */
+int w4a16_variant_count(void);
+
+/* Short name of a variant ("tc_a64_grp_sk" ...), or NULL for a bad id. */
+const char* w4a16_variant_name(int variant);
+
+/* 1 if `variant` can run this shape, else 0. */
+int w4a16_variant_eligible(int variant, int64_t M, int64_t N, int64_t K);
+
+/* Workspace bytes `variant` needs for this shape. */
+size_t w4a16_variant_workspace_bytes(int variant, int64_t M, int64_t N, int64_t K);
+
+/* The variant w4a16_gemm uses for this shape (table entry, else the rule). */
+int w4a16_select_variant(int64_t M, int64_t N, int64_t K);
+
+/* w4a16_gemm with an explicit variant (tests, tuning).  Same contract. */
+int w4a16_gemm_variant(int variant, const void* A_bf16, int64_t M, int64_t N, int64_t K,
+                       const void* packed, const void* scales, int group,
+                       const void* bias_bf16_or_null, void* Y_bf16, void* workspace,
+                       size_t workspace_bytes, void* stream);
+
+/*
+ * Time every eligible variant on synthetic device buffers of this shape
+ * and store the fastest in the table.  Allocates, synchronises and
+ * launches many kernels: call it at set-up, never inside graph capture.
+ * If out_variant is not NULL it receives the chosen id.
+ */
+int w4a16_tune(int64_t M, int64_t N, int64_t K, void* stream, int* out_variant);
+
+/* Put an entry in the table by hand (variant must be eligible). */
+int w4a16_table_set(int64_t M, int64_t N, int64_t K, int variant);
+
+/* Forget every table entry. */
+void w4a16_table_clear(void);
+
+/* Write / read the table as text lines "M N K variant_name". */
+int w4a16_table_save(const char* path);
+int w4a16_table_load(const char* path);
+
+/* ------------------------------------------------------------ diagnostics */
+
+/*
+ * Synchronise `stream`, then return and clear the device error word of the
+ * current device: W4A16_OK, or W4A16_ERR_TIMEOUT if a kernel's bounded wait
+ * expired since the last call (that kernel's output is then undefined and a
+ * workspace it used must be re-initialised).
+ */
+int w4a16_get_device_error(void* stream);
+
+/* Set the time a kernel-internal wait may take before it gives up and
+ * records W4A16_ERR_TIMEOUT (default 2 s).  Applies to later launches. */
+void w4a16_set_wait_timeout_ns(uint64_t ns);
+
+/*
+ * Failure-detection self test: launch one small kernel whose thread waits on
+ * an mbarrier that nothing ever arrives at, with a limit of `timeout_ns`;
+ * the wait runs out, the kernel records W4A16_ERR_TIMEOUT and returns.
+ * Nothing faults or hangs.  Read the result with w4a16_get_device_error.
+ */
+int w4a16_selftest_wait_timeout(uint64_t timeout_ns, void* stream);
+
+/* Number of kernel launches this library has made in this process. */
+uint64_t w4a16_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4A16_H_ */

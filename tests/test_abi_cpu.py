@@ -1,0 +1,123 @@
+"""The C ABI loads, exports what include/w4a16.h declares, and rejects bad
+arguments from metadata alone (no GPU needed: nothing here launches)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import weight_only_int4_rtn_gb300 as w4
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "w4a16.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(w4a16_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("w4a16_quantize", "w4a16_gemm", "w4a16_tune", "w4a16_get_device_error",
+                     "w4a16_status_string", "w4a16_packed_bytes", "w4a16_scales_bytes",
+                     "w4a16_gemm_workspace_bytes"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(built_lib):
+    handle = ctypes.CDLL(built_lib)
+    missing = [n for n in declared_functions() if not hasattr(handle, n)]
+    assert not missing, missing
+
+
+def test_binding_covers_every_declared_symbol():
+    bound = {name for name, _, _ in w4.SIGNATURES}
+    assert set(declared_functions()) == bound
+
+
+def test_sizes(built_lib):
+    assert w4.w4a16_packed_bytes(256, 512) == 256 * 256
+    assert w4.w4a16_scales_bytes(256, 512) == 4 * 256 * 2
+    assert w4.w4a16_scales_bytes(256, 512, 64) == 0
+
+
+def test_status_strings(built_lib):
+    for st in range(8):
+        assert w4.status_string(st).startswith("W4A16_")
+    assert "unknown" in w4.status_string(99)
+
+
+def _gemm(L, **kw):
+    args = dict(A=16, M=4, N=256, K=512, packed=16, scales=16, group=128, bias=None, Y=16,
+                ws=None, ws_bytes=0, stream=None)
+    args.update(kw)
+    return L.w4a16_gemm(args["A"], args["M"], args["N"], args["K"], args["packed"], args["scales"],
+                        args["group"], args["bias"], args["Y"], args["ws"], args["ws_bytes"],
+                        args["stream"])
+
+
+def test_gemm_argument_errors_before_any_launch(built_lib):
+    L = w4.lib()
+    assert _gemm(L, A=None) == w4.W4A16_ERR_INVALID_ARG
+    assert _gemm(L, Y=None) == w4.W4A16_ERR_INVALID_ARG
+    assert _gemm(L, M=0) == w4.W4A16_ERR_INVALID_ARG
+    assert _gemm(L, group=64) == w4.W4A16_ERR_UNSUPPORTED
+    assert _gemm(L, K=500) == w4.W4A16_ERR_UNSUPPORTED
+    assert _gemm(L, N=250) == w4.W4A16_ERR_UNSUPPORTED
+    assert _gemm(L, A=18) == w4.W4A16_ERR_ALIGNMENT
+    assert _gemm(L, packed=8) == w4.W4A16_ERR_ALIGNMENT
+    assert _gemm(L, bias=4) == w4.W4A16_ERR_ALIGNMENT
+    assert _gemm(L, Y=2) == w4.W4A16_ERR_ALIGNMENT
+
+
+def test_quantize_argument_errors_before_any_launch(built_lib):
+    L = w4.lib()
+    assert L.w4a16_quantize(None, 256, 512, 128, 16, 16, None) == w4.W4A16_ERR_INVALID_ARG
+    assert L.w4a16_quantize(16, 256, 512, 32, 16, 16, None) == w4.W4A16_ERR_UNSUPPORTED
+    assert L.w4a16_quantize(16, 256, 130, 128, 16, 16, None) == w4.W4A16_ERR_UNSUPPORTED
+    assert L.w4a16_quantize(16, 12, 512, 128, 16, 16, None) == w4.W4A16_ERR_UNSUPPORTED
+    assert L.w4a16_quantize(17, 256, 512, 128, 16, 16, None) == w4.W4A16_ERR_ALIGNMENT
+    assert L.w4a16_quantize(16, 256, 512, 128, 16, 24, None) == w4.W4A16_ERR_ALIGNMENT
+
+
+def test_variant_catalogue_is_host_only(built_lib):
+    n = w4.w4a16_variant_count()
+    assert n >= 4
+    names = [w4.w4a16_variant_name(i) for i in range(n)]
+    assert len(set(names)) == n and all(names)
+    assert w4.w4a16_variant_name(n) is None
+    for i in range(n):
+        assert w4.w4a16_variant_eligible(i, 16, 256, 512)
+        assert not w4.w4a16_variant_eligible(i, 16, 256, 500)
+    for M in (1, 4, 16, 50, 64, 816, 8192):
+        v = w4.w4a16_select_variant(M, 8192, 8192)
+        assert 0 <= v < n
+
+
+def test_table_roundtrip(built_lib, tmp_path):
+    w4.w4a16_table_clear()
+    rule = w4.w4a16_select_variant(50, 2048, 1024)
+    v = w4.variant_id("tc_a16_grp_sk")
+    assert v != rule
+    w4.w4a16_table_set(50, 2048, 1024, v)
+    assert w4.w4a16_select_variant(50, 2048, 1024) == v
+    p = str(tmp_path / "table.txt")
+    w4.w4a16_table_save(p)
+    w4.w4a16_table_clear()
+    assert w4.w4a16_select_variant(50, 2048, 1024) == rule
+    w4.w4a16_table_load(p)
+    assert w4.w4a16_select_variant(50, 2048, 1024) == v
+    with open(p, "a") as f:
+        f.write("16 256 512 no_such_variant\n")
+    with pytest.raises(w4.W4A16Error):
+        w4.w4a16_table_load(p)
+    w4.w4a16_table_clear()
+
+
+def test_binding_rejects_cpu_tensors(built_lib):
+    import torch
+    W = torch.zeros(256, 512, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        w4.w4a16_quantize(W)

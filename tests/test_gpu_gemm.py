@@ -1,0 +1,142 @@
+"""W4A16 GEMM on the GPU against the oracle's FP32 GEMM on identical packed
+operands: |y - y_ref| <= 1e-2 |y_ref| + 1e-2 rms(y_ref) element by element."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import pins
+from gpu_helpers import bits, check_gemm_close, guarded, oracle_quantize
+from weight_only_int4_rtn_gb300 import synthetic
+
+pytestmark = pytest.mark.gpu
+
+NAN_BF16 = 0x7FC1
+
+
+def make_operands(w4, case):
+    W, A, b = synthetic.draw(case)
+    packed, scales = w4.w4a16_quantize(W.cuda())
+    return W, A, b, packed, scales
+
+
+def reference(A, packed, scales, b, rows=None):
+    p = packed.cpu().numpy()
+    s = scales.cpu().view(torch.int16).numpy().view(np.uint16)
+    return oracle.gemm(bits(A), p, s, None if b is None else bits(b), rows=rows)
+
+
+SHAPES = [
+    synthetic.Case("tiny", 16, 256, 512, 0),
+    synthetic.Case("m1_ragged_n", 1, 264, 384, 11, bias=True),
+    synthetic.Case("m50_ragged", 50, 520, 640, 12, "t4", bias=True),
+    synthetic.Case("m129", 129, 256, 256, 13),
+    synthetic.Case("m300_multi_tile", 300, 384, 1024, 14, bias=True),
+    synthetic.Case("m17_long_k", 17, 136, 4096, 15),
+]
+
+
+def variant_ids(w4):
+    return list(range(w4.w4a16_variant_count()))
+
+
+@pytest.mark.parametrize("case", SHAPES, ids=[c.name for c in SHAPES])
+def test_every_variant(w4, case):
+    W, A, b, packed, scales = make_operands(w4, case)
+    y_ref = reference(A, packed, scales, b)
+    Ad = A.cuda()
+    bd = None if b is None else b.cuda()
+    for v in variant_ids(w4):
+        if not w4.w4a16_variant_eligible(v, case.M, case.N, case.K):
+            continue
+        Y, ok = guarded((case.M, case.N), torch.bfloat16, Ad.device, NAN_BF16)
+        w4.w4a16_gemm(Ad, packed, scales, bias=bd, Y=Y, variant=v)
+        torch.cuda.synchronize()
+        assert ok(), f"variant {w4.w4a16_variant_name(v)} wrote outside Y"
+        check_gemm_close(Y, y_ref, what=w4.w4a16_variant_name(v))
+    assert w4.w4a16_get_device_error() == w4.W4A16_OK
+
+
+def test_default_selection_and_determinism(w4):
+    case = synthetic.Case("det", 64, 2048, 2048, 21, bias=True)
+    W, A, b, packed, scales = make_operands(w4, case)
+    Ad, bd = A.cuda(), b.cuda()
+    y1 = w4.w4a16_gemm(Ad, packed, scales, bias=bd).clone()
+    y2 = w4.w4a16_gemm(Ad, packed, scales, bias=bd).clone()
+    torch.cuda.synchronize()
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+    check_gemm_close(y1, reference(A, packed, scales, b))
+
+
+def test_hand_worked_example(w4):
+    # A = ones(1, 128); W rows r0..r3 (and zero rows up to N = 8):
+    # Y = 6, 0, 3 * 0.142822265625, -14 -> bf16 6, 0, 0.427734375, -14
+    rows, _ = pins.load_golden()
+    x = np.zeros((8, 128), np.float32)
+    for i, n in enumerate(["r0", "r1", "r2", "r3"]):
+        x[i] = pins.golden_row_values(rows[n])
+    W = synthetic.to_bf16(x).cuda()
+    packed, scales = w4.w4a16_quantize(W)
+    A = torch.ones(1, 128, dtype=torch.bfloat16, device="cuda")
+    for v in variant_ids(w4):
+        Y = w4.w4a16_gemm(A, packed, scales, variant=v)
+        torch.cuda.synchronize()
+        got = Y.float().cpu().numpy()[0]
+        assert got[0] == 6.0 and got[1] == 0.0 and got[3] == -14.0, (w4.w4a16_variant_name(v), got)
+        assert got[2] == np.float32(0.427734375), (w4.w4a16_variant_name(v), got)
+        assert not got[4:].any()
+
+
+def test_integer_exact(w4):
+    # power-of-two scales and small-integer activations: every partial sum is
+    # exact in fp32 and the results are integers below 256, exact in bf16
+    rng = np.random.default_rng(31)
+    M, N, K = 40, 256, 512
+    codes = rng.integers(-3, 4, size=(N, K))
+    codes[:, ::128] = 7
+    e = rng.integers(-3, 0, size=(N, K // 128))
+    x = (codes * np.repeat(2.0 ** e, 128, axis=1)).astype(np.float32)
+    a = rng.integers(-1, 2, size=(M, K)).astype(np.float32)
+    W = synthetic.to_bf16(x).cuda()
+    A = synthetic.to_bf16(a)
+    packed, scales = w4.w4a16_quantize(W)
+    exact = a.astype(np.float64) @ x.astype(np.float64).T
+    assert np.all(exact == np.round(exact * 8) / 8) and np.abs(exact).max() < 256
+    for v in variant_ids(w4):
+        Y = w4.w4a16_gemm(A.cuda(), packed, scales, variant=v)
+        torch.cuda.synchronize()
+        assert np.array_equal(Y.float().cpu().numpy().astype(np.float64), exact), w4.w4a16_variant_name(v)
+
+
+def test_workspace_too_small_is_an_error(w4):
+    M, N, K = 16, 2048, 2048
+    v = w4.variant_id("tc_a16_grp_sk")
+    need = w4.w4a16_variant_workspace_bytes(v, M, N, K)
+    assert need > 0
+    A = torch.zeros(M, K, dtype=torch.bfloat16, device="cuda")
+    packed = torch.zeros(N, K // 2, dtype=torch.uint8, device="cuda")
+    scales = torch.ones(K // 128, N, dtype=torch.float16, device="cuda")
+    ws = torch.zeros(need - 256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(w4.W4A16Error) as ei:
+        w4.w4a16_gemm(A, packed, scales, workspace=ws, variant=v)
+    assert ei.value.status == w4.W4A16_ERR_WORKSPACE
+
+
+FULL = [c for name in ("tiny", "expert_m50", "prefix_m816", "sweep", "large")
+        for c in synthetic.WORKLOADS[name]]
+
+
+@pytest.mark.parametrize("case", FULL, ids=[c.name for c in FULL])
+def test_workloads_full_size_sampled(w4, case):
+    """Full-size workloads through the default (table/rule) variant, which is
+    the launch configuration the benchmark times; rows sampled for the
+    oracle (all rows when M <= 64)."""
+    W, A, b, packed, scales = make_operands(w4, case)
+    Y = w4.w4a16_gemm(A.cuda(), packed, scales)
+    torch.cuda.synchronize()
+    M = case.M
+    rows = np.arange(M) if M <= 64 else np.unique(np.r_[0, 1, M // 2, M - 2, M - 1,
+                                                       np.random.default_rng(0).integers(0, M, 11)])
+    y_ref = reference(A, packed, scales, b, rows=rows)
+    check_gemm_close(Y[torch.as_tensor(rows, device=Y.device)], y_ref, what=case.name)

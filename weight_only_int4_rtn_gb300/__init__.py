@@ -1,0 +1,297 @@
+"""GB300 (sm_103a) weight-only INT4 round-to-nearest quantization and W4A16 GEMM.
+
+A thin ctypes binding over the C ABI in ``include/w4a16.h`` (the in-tree
+library ``libw4a16.so``).  Every function here only marshals arguments:
+shapes, dtypes and devices are checked from metadata, device buffers come
+from PyTorch, and each call is one launch of the library's CUDA kernels on
+the current PyTorch stream.  There is no CPU path: a missing library or a
+non-CUDA tensor raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libw4a16.so")
+GROUP = 128
+
+W4A16_OK = 0
+W4A16_ERR_INVALID_ARG = 1
+W4A16_ERR_UNSUPPORTED = 2
+W4A16_ERR_ALIGNMENT = 3
+W4A16_ERR_WORKSPACE = 4
+W4A16_ERR_NO_VARIANT = 5
+W4A16_ERR_CUDA = 6
+W4A16_ERR_TIMEOUT = 7
+
+# (name, restype, argtypes) of every symbol the C header declares.
+_c_int64, _c_size, _vp = ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p
+SIGNATURES = [
+    ("w4a16_status_string", ctypes.c_char_p, [ctypes.c_int]),
+    ("w4a16_packed_bytes", _c_size, [_c_int64, _c_int64]),
+    ("w4a16_scales_bytes", _c_size, [_c_int64, _c_int64, ctypes.c_int]),
+    ("w4a16_quantize", ctypes.c_int, [_vp, _c_int64, _c_int64, ctypes.c_int, _vp, _vp, _vp]),
+    ("w4a16_gemm_workspace_bytes", _c_size, [_c_int64, _c_int64, _c_int64]),
+    ("w4a16_gemm_workspace_bytes_max", _c_size, [_c_int64, _c_int64, _c_int64]),
+    ("w4a16_workspace_init", ctypes.c_int, [_vp, _c_size, _vp]),
+    ("w4a16_gemm", ctypes.c_int,
+     [_vp, _c_int64, _c_int64, _c_int64, _vp, _vp, ctypes.c_int, _vp, _vp, _vp, _c_size, _vp]),
+    ("w4a16_variant_count", ctypes.c_int, []),
+    ("w4a16_variant_name", ctypes.c_char_p, [ctypes.c_int]),
+    ("w4a16_variant_eligible", ctypes.c_int, [ctypes.c_int, _c_int64, _c_int64, _c_int64]),
+    ("w4a16_variant_workspace_bytes", _c_size, [ctypes.c_int, _c_int64, _c_int64, _c_int64]),
+    ("w4a16_select_variant", ctypes.c_int, [_c_int64, _c_int64, _c_int64]),
+    ("w4a16_gemm_variant", ctypes.c_int,
+     [ctypes.c_int, _vp, _c_int64, _c_int64, _c_int64, _vp, _vp, ctypes.c_int, _vp, _vp, _vp,
+      _c_size, _vp]),
+    ("w4a16_tune", ctypes.c_int, [_c_int64, _c_int64, _c_int64, _vp, ctypes.POINTER(ctypes.c_int)]),
+    ("w4a16_table_set", ctypes.c_int, [_c_int64, _c_int64, _c_int64, ctypes.c_int]),
+    ("w4a16_table_clear", None, []),
+    ("w4a16_table_save", ctypes.c_int, [ctypes.c_char_p]),
+    ("w4a16_table_load", ctypes.c_int, [ctypes.c_char_p]),
+    ("w4a16_get_device_error", ctypes.c_int, [_vp]),
+    ("w4a16_set_wait_timeout_ns", None, [ctypes.c_uint64]),
+    ("w4a16_selftest_wait_timeout", ctypes.c_int, [ctypes.c_uint64, _vp]),
+    ("w4a16_launch_count", ctypes.c_uint64, []),
+]
+
+_lib = None
+_lib_lock = threading.Lock()
+
+
+class W4A16Error(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)}")
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        with _lib_lock:
+            if _lib is None:
+                if not os.path.exists(LIB_PATH):
+                    raise RuntimeError(
+                        f"{LIB_PATH} is not built; run `python -c \"import __graft_entry__ as g; g.build()\"`")
+                handle = ctypes.CDLL(LIB_PATH)
+                for name, res, args in SIGNATURES:
+                    fn = getattr(handle, name)
+                    fn.restype = res
+                    fn.argtypes = args
+                _lib = handle
+    return _lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return lib().w4a16_status_string(status).decode()
+    except Exception:   # library missing: still give a readable message
+        return f"status {status}"
+
+
+def _check(status: int, what: str) -> None:
+    if status != W4A16_OK:
+        raise W4A16Error(status, what)
+
+
+def _stream_handle(device: torch.device, stream=None) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return int(stream.cuda_stream)
+
+
+def _require_cuda(t: torch.Tensor, name: str, dtype: torch.dtype) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor (no CPU path), got {t.device}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+# ------------------------------------------------------------------ sizes
+def w4a16_packed_bytes(N: int, K: int) -> int:
+    return lib().w4a16_packed_bytes(N, K)
+
+
+def w4a16_scales_bytes(N: int, K: int, group: int = GROUP) -> int:
+    return lib().w4a16_scales_bytes(N, K, group)
+
+
+def w4a16_gemm_workspace_bytes(M: int, N: int, K: int) -> int:
+    return lib().w4a16_gemm_workspace_bytes(M, N, K)
+
+
+def w4a16_gemm_workspace_bytes_max(M: int, N: int, K: int) -> int:
+    return lib().w4a16_gemm_workspace_bytes_max(M, N, K)
+
+
+# --------------------------------------------------------------- quantize
+def w4a16_quantize(W: torch.Tensor, group: int = GROUP, packed: torch.Tensor | None = None,
+                   scales: torch.Tensor | None = None, stream=None):
+    """RTN-quantize ``W[N, K]`` (bf16, CUDA).  Returns ``(packed uint8 [N, K/2],
+    scales fp16 [K/128, N])``; outputs are allocated when not given."""
+    _require_cuda(W, "W", torch.bfloat16)
+    if W.dim() != 2:
+        raise ValueError("W must be [N, K]")
+    N, K = W.shape
+    if packed is None:
+        packed = torch.empty((N, K // 2), dtype=torch.uint8, device=W.device)
+    if scales is None:
+        scales = torch.empty((max(K // group, 0), N), dtype=torch.float16, device=W.device)
+    _require_cuda(packed, "packed", torch.uint8)
+    _require_cuda(scales, "scales", torch.float16)
+    if packed.numel() * 2 != N * K or scales.numel() * group != N * K:
+        raise ValueError("output buffers have the wrong size")
+    st = lib().w4a16_quantize(W.data_ptr(), N, K, group, packed.data_ptr(), scales.data_ptr(),
+                              _stream_handle(W.device, stream))
+    _check(st, "w4a16_quantize")
+    return packed, scales
+
+
+# ------------------------------------------------------------------- GEMM
+class Workspace:
+    """A zero-initialised device workspace that grows on demand.  One per
+    (device, stream): GEMMs that may run concurrently need separate ones."""
+
+    def __init__(self):
+        self._buf: dict = {}
+
+    def get(self, device: torch.device, stream_handle: int, nbytes: int) -> torch.Tensor | None:
+        if nbytes == 0:
+            return None
+        key = (device.index, stream_handle)
+        buf = self._buf.get(key)
+        if buf is None or buf.numel() < nbytes:
+            buf = torch.zeros(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
+            self._buf[key] = buf
+        return buf
+
+
+_default_ws = Workspace()
+
+
+def w4a16_gemm(A: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor,
+               bias: torch.Tensor | None = None, Y: torch.Tensor | None = None,
+               workspace: torch.Tensor | None = None, group: int = GROUP, stream=None,
+               variant: int | None = None) -> torch.Tensor:
+    """``Y[M, N] = bf16(A[M, K] @ dequant(packed, scales)^T + bias)`` on the GPU.
+
+    ``variant`` forces one entry of the kernel catalogue (tests, tuning);
+    otherwise the library's per-shape table chooses."""
+    _require_cuda(A, "A", torch.bfloat16)
+    _require_cuda(packed, "packed", torch.uint8)
+    _require_cuda(scales, "scales", torch.float16)
+    if A.dim() != 2 or packed.dim() != 2 or scales.dim() != 2:
+        raise ValueError("A, packed and scales must be 2-D")
+    M, K = A.shape
+    N = packed.shape[0]
+    if packed.shape[1] * 2 != K or scales.shape != (K // group, N):
+        raise ValueError("packed must be [N, K/2] and scales [K/128, N]")
+    if bias is not None:
+        _require_cuda(bias, "bias", torch.bfloat16)
+        if bias.numel() != N:
+            raise ValueError("bias must have N elements")
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    _require_cuda(Y, "Y", torch.bfloat16)
+    if Y.shape != (M, N):
+        raise ValueError("Y must be [M, N]")
+    sh = _stream_handle(A.device, stream)
+    L = lib()
+    need = (L.w4a16_gemm_workspace_bytes(M, N, K) if variant is None
+            else L.w4a16_variant_workspace_bytes(variant, M, N, K))
+    if workspace is None:
+        workspace = _default_ws.get(A.device, sh, need)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    bias_ptr = bias.data_ptr() if bias is not None else None
+    if variant is None:
+        st = L.w4a16_gemm(A.data_ptr(), M, N, K, packed.data_ptr(), scales.data_ptr(), group,
+                          bias_ptr, Y.data_ptr(), ws_ptr, ws_bytes, sh)
+    else:
+        st = L.w4a16_gemm_variant(variant, A.data_ptr(), M, N, K, packed.data_ptr(),
+                                  scales.data_ptr(), group, bias_ptr, Y.data_ptr(), ws_ptr,
+                                  ws_bytes, sh)
+    _check(st, "w4a16_gemm")
+    return Y
+
+
+# --------------------------------------------------------------- variants
+def w4a16_variant_count() -> int:
+    return lib().w4a16_variant_count()
+
+
+def w4a16_variant_name(variant: int) -> str | None:
+    n = lib().w4a16_variant_name(variant)
+    return None if n is None else n.decode()
+
+
+def w4a16_variant_eligible(variant: int, M: int, N: int, K: int) -> bool:
+    return bool(lib().w4a16_variant_eligible(variant, M, N, K))
+
+
+def w4a16_variant_workspace_bytes(variant: int, M: int, N: int, K: int) -> int:
+    return lib().w4a16_variant_workspace_bytes(variant, M, N, K)
+
+
+def w4a16_select_variant(M: int, N: int, K: int) -> int:
+    return lib().w4a16_select_variant(M, N, K)
+
+
+def variant_id(name: str) -> int:
+    for i in range(w4a16_variant_count()):
+        if w4a16_variant_name(i) == name:
+            return i
+    raise KeyError(name)
+
+
+def w4a16_tune(M: int, N: int, K: int, stream=None, device=None) -> int:
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    out = ctypes.c_int(-1)
+    _check(lib().w4a16_tune(M, N, K, _stream_handle(dev, stream), ctypes.byref(out)), "w4a16_tune")
+    return out.value
+
+
+def w4a16_table_set(M: int, N: int, K: int, variant: int) -> None:
+    _check(lib().w4a16_table_set(M, N, K, variant), "w4a16_table_set")
+
+
+def w4a16_table_clear() -> None:
+    lib().w4a16_table_clear()
+
+
+def w4a16_table_save(path: str) -> None:
+    _check(lib().w4a16_table_save(path.encode()), "w4a16_table_save")
+
+
+def w4a16_table_load(path: str) -> None:
+    _check(lib().w4a16_table_load(path.encode()), "w4a16_table_load")
+
+
+# ------------------------------------------------------------ diagnostics
+def w4a16_get_device_error(stream=None, device=None) -> int:
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    return lib().w4a16_get_device_error(_stream_handle(dev, stream))
+
+
+def w4a16_set_wait_timeout_ns(ns: int) -> None:
+    lib().w4a16_set_wait_timeout_ns(ns)
+
+
+def w4a16_selftest_wait_timeout(timeout_ns: int, stream=None, device=None) -> None:
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    _check(lib().w4a16_selftest_wait_timeout(timeout_ns, _stream_handle(dev, stream)),
+           "w4a16_selftest_wait_timeout")
+
+
+def w4a16_launch_count() -> int:
+    return lib().w4a16_launch_count()

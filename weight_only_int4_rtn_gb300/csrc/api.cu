@@ -1,0 +1,567 @@
+// C ABI of the W4A16 library: argument checks (metadata only), the GEMM
+// variant catalogue and its per-shape table, tuning by measurement, the
+// device error word and the TMA descriptor encoder.
+//
+// The per-shape table mirrors the cached, frozen, optionally autotuned kernel
+// choice of "Kernel dispatch and Humming quantization in PhyAI", sections
+// "Keep selection work out of repeated inference" (prepared selections are
+// memoized and reused) and "Put deployment choices in a policy" (an error,
+// never a silent fallback, when no implementation is usable).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <fstream>
+#include <map>
+#include <mutex>
+#include <sstream>
+#include <string>
+#include <tuple>
+#include <vector>
+
+#include "../../include/w4a16.h"
+#include "kernels.h"
+
+namespace w4a16 {
+
+// Device error word: bit 0 = a bounded wait ran out.  One per device that
+// loads this library.
+__device__ uint32_t g_error_word;
+
+namespace {
+
+std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+std::atomic<uint64_t> g_launches{0};
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool ready = false;
+  int num_sms = 0;
+  uint32_t* error_word = nullptr;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mutex;
+
+// Current device's SM count and error-word address (looked up once).
+bool device_info(DeviceInfo& out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return false;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return false;
+    d.num_sms = sms;
+    d.error_word = static_cast<uint32_t*>(p);
+    d.ready = true;
+  }
+  out = d;
+  return true;
+}
+
+// ------------------------------------------------------------ catalogue
+struct Variant {
+  const char* name;
+  GemmKernelConfig cfg;
+  bool stream_k;   // false: whole tiles only (data parallel)
+};
+
+const Variant kVariants[] = {
+    {"tc_a16_grp_sk", {16, 2, true, 16}, true},
+    {"tc_a32_grp_sk", {32, 2, true, 12}, true},
+    {"tc_a64_grp_sk", {64, 2, true, 8}, true},
+    {"tc_a64_deq_sk", {64, 2, false, 8}, true},
+    {"tc_a128_grp_sk", {128, 2, true, 5}, true},
+    {"tc_a128_deq_sk", {128, 2, false, 5}, true},
+    {"tc_a256_deq_sk", {256, 2, false, 3}, true},
+    {"tc_a16_grp_dp", {16, 2, true, 16}, false},
+    {"tc_a64_grp_dp", {64, 2, true, 8}, false},
+    {"tc_a128_deq_dp", {128, 2, false, 5}, false},
+    {"tc_a256_deq_dp", {256, 2, false, 3}, false},
+};
+constexpr int kNumVariants = static_cast<int>(sizeof(kVariants) / sizeof(kVariants[0]));
+
+int variant_by_name(const std::string& n) {
+  for (int i = 0; i < kNumVariants; ++i)
+    if (n == kVariants[i].name) return i;
+  return -1;
+}
+
+bool shape_ok(int64_t M, int64_t N, int64_t K) {
+  return M >= 1 && N >= 8 && K >= 128 && (K % kGroup) == 0 && (N % 8) == 0 &&
+         M < (1ll << 31) && N < (1ll << 31) && K < (1ll << 31) && M * N < (1ll << 40) &&
+         N * K < (1ll << 40);
+}
+
+GemmSchedule make_schedule(const Variant& v, int64_t M, int64_t N, int64_t K, int num_sms) {
+  GemmSchedule s{};
+  const int64_t tiles = gemm_tiles(v.cfg, M, N);
+  const int64_t KB = K / kGroup;
+  const int64_t units = tiles * KB;
+  if (!v.stream_k) {
+    s.grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
+    s.dp_tiles = static_cast<int>(tiles);
+    s.sk_units = 0;
+    return s;
+  }
+  if (tiles >= num_sms) {
+    s.grid = num_sms;
+    const int64_t rem = tiles % num_sms;
+    if (rem != 0 && rem * KB >= num_sms) {
+      s.dp_tiles = static_cast<int>(tiles - rem);
+      s.sk_units = rem * KB;
+    } else {
+      s.dp_tiles = static_cast<int>(tiles);
+      s.sk_units = 0;
+    }
+  } else {
+    s.grid = static_cast<int>(units < num_sms ? units : num_sms);
+    s.dp_tiles = 0;
+    s.sk_units = units;
+  }
+  return s;
+}
+
+bool variant_eligible(int id, int64_t M, int64_t N, int64_t K) {
+  if (id < 0 || id >= kNumVariants) return false;
+  if (!shape_ok(M, N, K)) return false;
+  const Variant& v = kVariants[id];
+  if (!gemm_config_available(v.cfg)) return false;
+  const int64_t tiles = gemm_tiles(v.cfg, M, N);
+  if (tiles * (K / kGroup) >= (1ll << 31)) return false;
+  return true;
+}
+
+// Fixed rule for shapes without a table entry.
+int rule_variant(int64_t M, int64_t N, int64_t K) {
+  (void)N;
+  (void)K;
+  if (M <= 16) return variant_by_name("tc_a16_grp_sk");
+  if (M <= 32) return variant_by_name("tc_a32_grp_sk");
+  if (M <= 64) return variant_by_name("tc_a64_grp_sk");
+  if (M <= 128) return variant_by_name("tc_a128_grp_sk");
+  return variant_by_name("tc_a256_deq_sk");
+}
+
+// ---------------------------------------------------------------- table
+std::mutex g_table_mutex;
+std::map<std::tuple<int64_t, int64_t, int64_t>, int> g_table;
+bool g_table_env_loaded = false;
+
+int load_table_locked(const char* path) {
+  std::ifstream f(path);
+  if (!f) return W4A16_ERR_INVALID_ARG;
+  std::string line;
+  while (std::getline(f, line)) {
+    if (line.empty() || line[0] == '#') continue;
+    std::istringstream ss(line);
+    int64_t M, N, K;
+    std::string name;
+    if (!(ss >> M >> N >> K >> name)) return W4A16_ERR_INVALID_ARG;
+    const int id = variant_by_name(name);
+    if (id < 0 || !variant_eligible(id, M, N, K)) return W4A16_ERR_NO_VARIANT;
+    g_table[{M, N, K}] = id;
+  }
+  return W4A16_OK;
+}
+
+void maybe_load_env_table_locked() {
+  if (g_table_env_loaded) return;
+  g_table_env_loaded = true;
+  const char* p = std::getenv("W4A16_VARIANT_TABLE");
+  if (p != nullptr && p[0] != '\0') {
+    const int st = load_table_locked(p);
+    if (st != W4A16_OK) std::fprintf(stderr, "w4a16: could not load variant table %s (%d)\n", p, st);
+  }
+}
+
+bool log_enabled() {
+  static const bool on = [] {
+    const char* p = std::getenv("W4A16_LOG");
+    return p != nullptr && p[0] == '1';
+  }();
+  return on;
+}
+
+int select_variant(int64_t M, int64_t N, int64_t K) {
+  int id = -1;
+  {
+    std::lock_guard<std::mutex> lock(g_table_mutex);
+    maybe_load_env_table_locked();
+    auto it = g_table.find({M, N, K});
+    if (it != g_table.end()) id = it->second;
+  }
+  if (id < 0) id = rule_variant(M, N, K);
+  if (!variant_eligible(id, M, N, K)) return -1;
+  return id;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_gemm_args(const void* A, int64_t M, int64_t N, int64_t K, const void* packed,
+                    const void* scales, int group, const void* bias, void* Y) {
+  if (A == nullptr || packed == nullptr || scales == nullptr || Y == nullptr)
+    return W4A16_ERR_INVALID_ARG;
+  if (M < 1 || N < 1 || K < 1) return W4A16_ERR_INVALID_ARG;
+  if (group != kGroup) return W4A16_ERR_UNSUPPORTED;
+  if (!shape_ok(M, N, K)) return W4A16_ERR_UNSUPPORTED;
+  if (!aligned16(A) || !aligned16(packed) || !aligned16(scales) || !aligned16(Y) ||
+      (bias != nullptr && !aligned16(bias)))
+    return W4A16_ERR_ALIGNMENT;
+  return W4A16_OK;
+}
+
+int run_gemm(int id, const void* A, int64_t M, int64_t N, int64_t K, const void* packed,
+             const void* scales, const void* bias, void* Y, void* ws, size_t ws_bytes,
+             cudaStream_t stream) {
+  DeviceInfo dev;
+  if (!device_info(dev)) return W4A16_ERR_CUDA;
+  const Variant& v = kVariants[id];
+  const GemmSchedule s = make_schedule(v, M, N, K, dev.num_sms);
+  const size_t need = gemm_workspace_bytes(v.cfg, s, M, N, K);
+  if (need > 0) {
+    if (ws == nullptr || ws_bytes < need) return W4A16_ERR_WORKSPACE;
+    if (!aligned16(ws)) return W4A16_ERR_ALIGNMENT;
+  }
+  GemmProblem p{};
+  p.A = A;
+  p.packed = packed;
+  p.scales = scales;
+  p.bias = bias;
+  p.Y = Y;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.workspace = ws;
+  p.workspace_bytes = ws_bytes;
+  p.error_word = dev.error_word;
+  p.timeout_ns = g_timeout_ns.load();
+  if (log_enabled())
+    std::fprintf(stderr, "w4a16: gemm M=%lld N=%lld K=%lld variant=%s grid=%d dp_tiles=%d sk_units=%lld\n",
+                 static_cast<long long>(M), static_cast<long long>(N), static_cast<long long>(K),
+                 v.name, s.grid, s.dp_tiles, static_cast<long long>(s.sk_units));
+  const cudaError_t e = launch_gemm_tc(v.cfg, s, p, /*use_pdl=*/true, stream);
+  if (e != cudaSuccess) return W4A16_ERR_CUDA;
+  g_launches.fetch_add(1);
+  return W4A16_OK;
+}
+
+size_t variant_ws(int id, int64_t M, int64_t N, int64_t K) {
+  DeviceInfo dev;
+  int sms = 148;
+  if (device_info(dev)) sms = dev.num_sms;
+  const Variant& v = kVariants[id];
+  return gemm_workspace_bytes(v.cfg, make_schedule(v, M, N, K, sms), M, N, K);
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ TMA
+CUresult encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                        uint64_t inner, uint64_t outer, uint64_t outer_stride_bytes,
+                        uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle) {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }();
+  if (fn == nullptr) return CUDA_ERROR_NOT_FOUND;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {outer_stride_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+}  // namespace w4a16
+
+using namespace w4a16;
+
+extern "C" {
+
+const char* w4a16_status_string(int status) {
+  switch (status) {
+    case W4A16_OK: return "W4A16_OK";
+    case W4A16_ERR_INVALID_ARG: return "W4A16_ERR_INVALID_ARG: null pointer or size out of range";
+    case W4A16_ERR_UNSUPPORTED: return "W4A16_ERR_UNSUPPORTED: group must be 128, K % 128 == 0, N % 8 == 0";
+    case W4A16_ERR_ALIGNMENT: return "W4A16_ERR_ALIGNMENT: pointers must be 16-byte aligned";
+    case W4A16_ERR_WORKSPACE: return "W4A16_ERR_WORKSPACE: workspace missing or too small";
+    case W4A16_ERR_NO_VARIANT: return "W4A16_ERR_NO_VARIANT: no GEMM variant is usable for this shape";
+    case W4A16_ERR_CUDA: return "W4A16_ERR_CUDA: a CUDA call failed";
+    case W4A16_ERR_TIMEOUT: return "W4A16_ERR_TIMEOUT: a device-side bounded wait expired";
+    default: return "W4A16: unknown status";
+  }
+}
+
+size_t w4a16_packed_bytes(int64_t N, int64_t K) {
+  if (N < 0 || K < 0) return 0;
+  return static_cast<size_t>(N) * static_cast<size_t>(K) / 2;
+}
+
+size_t w4a16_scales_bytes(int64_t N, int64_t K, int group) {
+  if (group != kGroup || N < 0 || K < 0) return 0;
+  return static_cast<size_t>(K / group) * static_cast<size_t>(N) * 2;
+}
+
+int w4a16_quantize(const void* W_bf16, int64_t N, int64_t K, int group, void* packed_out,
+                   void* scales_out, void* stream) {
+  if (W_bf16 == nullptr || packed_out == nullptr || scales_out == nullptr)
+    return W4A16_ERR_INVALID_ARG;
+  if (N < 1 || K < 1) return W4A16_ERR_INVALID_ARG;
+  if (group != kGroup) return W4A16_ERR_UNSUPPORTED;
+  if (K % kGroup != 0 || N % 8 != 0) return W4A16_ERR_UNSUPPORTED;
+  if (N >= (1ll << 31) || K >= (1ll << 31) || N * K >= (1ll << 40)) return W4A16_ERR_UNSUPPORTED;
+  if (!aligned16(W_bf16) || !aligned16(packed_out) || !aligned16(scales_out))
+    return W4A16_ERR_ALIGNMENT;
+  DeviceInfo dev;
+  if (!device_info(dev)) return W4A16_ERR_CUDA;
+  const cudaError_t e = launch_rtn_quantize(W_bf16, N, K, packed_out, scales_out, dev.num_sms,
+                                            static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return W4A16_ERR_CUDA;
+  g_launches.fetch_add(1);
+  return W4A16_OK;
+}
+
+size_t w4a16_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  const int id = select_variant(M, N, K);
+  if (id < 0) return 0;
+  return variant_ws(id, M, N, K);
+}
+
+size_t w4a16_gemm_workspace_bytes_max(int64_t M, int64_t N, int64_t K) {
+  size_t m = 0;
+  for (int id = 0; id < kNumVariants; ++id) {
+    if (!variant_eligible(id, M, N, K)) continue;
+    const size_t b = variant_ws(id, M, N, K);
+    if (b > m) m = b;
+  }
+  return m;
+}
+
+int w4a16_workspace_init(void* workspace, size_t bytes, void* stream) {
+  if (bytes == 0) return W4A16_OK;
+  if (workspace == nullptr) return W4A16_ERR_INVALID_ARG;
+  if (cudaMemsetAsync(workspace, 0, bytes, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return W4A16_ERR_CUDA;
+  return W4A16_OK;
+}
+
+int w4a16_gemm(const void* A_bf16, int64_t M, int64_t N, int64_t K, const void* packed,
+               const void* scales, int group, const void* bias_bf16_or_null, void* Y_bf16,
+               void* workspace, size_t workspace_bytes, void* stream) {
+  const int st = check_gemm_args(A_bf16, M, N, K, packed, scales, group, bias_bf16_or_null, Y_bf16);
+  if (st != W4A16_OK) return st;
+  const int id = select_variant(M, N, K);
+  if (id < 0) return W4A16_ERR_NO_VARIANT;
+  return run_gemm(id, A_bf16, M, N, K, packed, scales, bias_bf16_or_null, Y_bf16, workspace,
+                  workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+int w4a16_variant_count(void) { return kNumVariants; }
+
+const char* w4a16_variant_name(int variant) {
+  if (variant < 0 || variant >= kNumVariants) return nullptr;
+  return kVariants[variant].name;
+}
+
+int w4a16_variant_eligible(int variant, int64_t M, int64_t N, int64_t K) {
+  return variant_eligible(variant, M, N, K) ? 1 : 0;
+}
+
+size_t w4a16_variant_workspace_bytes(int variant, int64_t M, int64_t N, int64_t K) {
+  if (!variant_eligible(variant, M, N, K)) return 0;
+  return variant_ws(variant, M, N, K);
+}
+
+int w4a16_select_variant(int64_t M, int64_t N, int64_t K) { return select_variant(M, N, K); }
+
+int w4a16_gemm_variant(int variant, const void* A_bf16, int64_t M, int64_t N, int64_t K,
+                       const void* packed, const void* scales, int group,
+                       const void* bias_bf16_or_null, void* Y_bf16, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  const int st = check_gemm_args(A_bf16, M, N, K, packed, scales, group, bias_bf16_or_null, Y_bf16);
+  if (st != W4A16_OK) return st;
+  if (variant < 0 || variant >= kNumVariants) return W4A16_ERR_UNSUPPORTED;
+  if (!variant_eligible(variant, M, N, K)) return W4A16_ERR_NO_VARIANT;
+  return run_gemm(variant, A_bf16, M, N, K, packed, scales, bias_bf16_or_null, Y_bf16, workspace,
+                  workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+int w4a16_table_set(int64_t M, int64_t N, int64_t K, int variant) {
+  if (!variant_eligible(variant, M, N, K)) return W4A16_ERR_NO_VARIANT;
+  std::lock_guard<std::mutex> lock(g_table_mutex);
+  maybe_load_env_table_locked();
+  g_table[{M, N, K}] = variant;
+  return W4A16_OK;
+}
+
+void w4a16_table_clear(void) {
+  std::lock_guard<std::mutex> lock(g_table_mutex);
+  g_table_env_loaded = true;
+  g_table.clear();
+}
+
+int w4a16_table_save(const char* path) {
+  if (path == nullptr) return W4A16_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_table_mutex);
+  std::ofstream f(path);
+  if (!f) return W4A16_ERR_INVALID_ARG;
+  f << "# M N K variant\n";
+  for (const auto& kv : g_table)
+    f << std::get<0>(kv.first) << ' ' << std::get<1>(kv.first) << ' ' << std::get<2>(kv.first)
+      << ' ' << kVariants[kv.second].name << '\n';
+  return f ? W4A16_OK : W4A16_ERR_INVALID_ARG;
+}
+
+int w4a16_table_load(const char* path) {
+  if (path == nullptr) return W4A16_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_table_mutex);
+  g_table_env_loaded = true;
+  return load_table_locked(path);
+}
+
+int w4a16_tune(int64_t M, int64_t N, int64_t K, void* stream_v, int* out_variant) {
+  if (!shape_ok(M, N, K)) return W4A16_ERR_UNSUPPORTED;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone)
+    return W4A16_ERR_INVALID_ARG;
+
+  // Synthetic operands; enough weight copies that the timed launches stream
+  // them from HBM rather than L2.
+  const size_t wbytes = w4a16_packed_bytes(N, K);
+  const size_t sbytes = w4a16_scales_bytes(N, K, kGroup);
+  const size_t abytes = static_cast<size_t>(M) * K * 2;
+  const size_t ybytes = static_cast<size_t>(M) * N * 2;
+  const size_t wsbytes = w4a16_gemm_workspace_bytes_max(M, N, K);
+  const size_t per_copy = wbytes + sbytes + 4096;
+  int copies = static_cast<int>((512ull << 20) / per_copy) + 1;
+  if (copies > 16) copies = 16;
+  if (copies < 1) copies = 1;
+
+  std::vector<void*> bufs;
+  auto alloc = [&](size_t b) -> void* {
+    void* p = nullptr;
+    if (cudaMalloc(&p, b < 256 ? 256 : b) != cudaSuccess) return nullptr;
+    bufs.push_back(p);
+    return p;
+  };
+  auto release = [&]() {
+    for (void* p : bufs) cudaFree(p);
+    bufs.clear();
+  };
+  void* A = alloc(abytes);
+  void* Y = alloc(ybytes);
+  void* ws = wsbytes ? alloc(wsbytes) : nullptr;
+  std::vector<void*> Wp(copies), Sc(copies);
+  bool ok = A && Y && (wsbytes == 0 || ws);
+  for (int c = 0; ok && c < copies; ++c) {
+    Wp[c] = alloc(wbytes);
+    Sc[c] = alloc(sbytes);
+    ok = Wp[c] && Sc[c];
+  }
+  if (!ok) {
+    release();
+    return W4A16_ERR_CUDA;
+  }
+  cudaMemsetAsync(A, 0x3C, abytes, stream);
+  for (int c = 0; c < copies; ++c) {
+    cudaMemsetAsync(Wp[c], 0x5A, wbytes, stream);
+    cudaMemsetAsync(Sc[c], 0x1C, sbytes, stream);
+  }
+  if (ws) cudaMemsetAsync(ws, 0, wsbytes, stream);
+
+  cudaEvent_t e0, e1;
+  cudaEventCreate(&e0);
+  cudaEventCreate(&e1);
+  float best_ms = 0.0f;
+  int best = -1;
+  constexpr int kIters = 20;
+  for (int id = 0; id < kNumVariants; ++id) {
+    if (!variant_eligible(id, M, N, K)) continue;
+    bool fine = true;
+    for (int it = 0; it < 3 && fine; ++it)
+      fine = run_gemm(id, A, M, N, K, Wp[it % copies], Sc[it % copies], nullptr, Y, ws, wsbytes,
+                      stream) == W4A16_OK;
+    if (!fine) continue;
+    cudaEventRecord(e0, stream);
+    for (int it = 0; it < kIters; ++it)
+      run_gemm(id, A, M, N, K, Wp[it % copies], Sc[it % copies], nullptr, Y, ws, wsbytes, stream);
+    cudaEventRecord(e1, stream);
+    if (cudaEventSynchronize(e1) != cudaSuccess) {
+      ok = false;
+      break;
+    }
+    float ms = 0.0f;
+    cudaEventElapsedTime(&ms, e0, e1);
+    if (best < 0 || ms < best_ms) {
+      best_ms = ms;
+      best = id;
+    }
+  }
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  const int dev_err = w4a16_get_device_error(stream);
+  release();
+  if (!ok) return W4A16_ERR_CUDA;
+  if (dev_err != W4A16_OK) return dev_err;
+  if (best < 0) return W4A16_ERR_NO_VARIANT;
+  {
+    std::lock_guard<std::mutex> lock(g_table_mutex);
+    maybe_load_env_table_locked();
+    g_table[{M, N, K}] = best;
+  }
+  if (out_variant) *out_variant = best;
+  if (log_enabled())
+    std::fprintf(stderr, "w4a16: tuned M=%lld N=%lld K=%lld -> %s (%.3f us)\n",
+                 static_cast<long long>(M), static_cast<long long>(N), static_cast<long long>(K),
+                 kVariants[best].name, 1000.0 * best_ms / kIters);
+  return W4A16_OK;
+}
+
+int w4a16_get_device_error(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return W4A16_ERR_CUDA;
+  DeviceInfo dev;
+  if (!device_info(dev)) return W4A16_ERR_CUDA;
+  uint32_t word = 0;
+  if (cudaMemcpy(&word, dev.error_word, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return W4A16_ERR_CUDA;
+  if (word != 0) {
+    const uint32_t zero = 0;
+    if (cudaMemcpy(dev.error_word, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+      return W4A16_ERR_CUDA;
+    return W4A16_ERR_TIMEOUT;
+  }
+  return W4A16_OK;
+}
+
+void w4a16_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns == 0 ? 1 : ns); }
+
+int w4a16_selftest_wait_timeout(uint64_t timeout_ns, void* stream) {
+  DeviceInfo dev;
+  if (!device_info(dev)) return W4A16_ERR_CUDA;
+  if (launch_wait_timeout_selftest(dev.error_word, timeout_ns,
+                                   static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return W4A16_ERR_CUDA;
+  g_launches.fetch_add(1);
+  return W4A16_OK;
+}
+
+uint64_t w4a16_launch_count(void) { return g_launches.load(); }
+
+}  // extern "C"

@@ -1,0 +1,78 @@
+// Internal launch interface between the C ABI (api.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+namespace w4a16 {
+
+constexpr int kGroup = 128;     // quantization group along K
+constexpr int kTileW = 128;     // weight rows per GEMM tile (tcgen05 M)
+
+// RTN quantize/pack; one launch.
+cudaError_t launch_rtn_quantize(const void* W, int64_t N, int64_t K, void* packed, void* scales,
+                                int num_sms, cudaStream_t stream);
+
+// One configuration of the tcgen05 GEMM kernel.
+struct GemmKernelConfig {
+  int act_tile;      // activation rows per tile (tcgen05 N): 16..256
+  int worker_wgs;    // dequant/epilogue warpgroups: 1 or 2
+  bool group_scale;  // true: per-group fp32 scaling of integer-code partial sums
+                     // false: weights dequantized to bf16(q*s) before the MMA
+  int stages;        // shared-memory pipeline depth
+};
+
+// The schedule of one launch.
+struct GemmSchedule {
+  int grid;          // CTAs (one per SM at most)
+  int dp_tiles;      // tiles 0..dp_tiles-1 run whole, tile t on CTA t % grid
+  int64_t sk_units;  // the remaining tiles' (tile, k-block) units, split in
+                     // contiguous balanced ranges over all CTAs
+};
+
+struct GemmProblem {
+  const void* A;       // [M, K] bf16
+  const void* packed;  // [N, K/2] u8
+  const void* scales;  // [K/128, N] fp16
+  const void* bias;    // [N] bf16 or null
+  void* Y;             // [M, N] bf16
+  int64_t M, N, K;
+  void* workspace;
+  size_t workspace_bytes;
+  uint32_t* error_word;
+  uint64_t timeout_ns;
+};
+
+// Number of tiles of a problem under a configuration.
+inline int64_t gemm_tiles(const GemmKernelConfig& c, int64_t M, int64_t N) {
+  return ((N + kTileW - 1) / kTileW) * ((M + c.act_tile - 1) / c.act_tile);
+}
+
+// Workspace layout: [grid][2][act_tile][128] fp32 partial slots, then one
+// uint32 arrival counter per stream-K tile.
+size_t gemm_workspace_bytes(const GemmKernelConfig& c, const GemmSchedule& s, int64_t M,
+                            int64_t N, int64_t K);
+
+// Shared memory bytes of a configuration (for eligibility checks).
+size_t gemm_smem_bytes(const GemmKernelConfig& c);
+
+// True if the kernel for `c` is compiled in.
+bool gemm_config_available(const GemmKernelConfig& c);
+
+cudaError_t launch_gemm_tc(const GemmKernelConfig& c, const GemmSchedule& s,
+                           const GemmProblem& p, bool use_pdl, cudaStream_t stream);
+
+// Failure-detection self test: one thread waits on an mbarrier nobody
+// arrives at, with a bounded wait; records a timeout in *error_word.
+cudaError_t launch_wait_timeout_selftest(uint32_t* error_word, uint64_t timeout_ns,
+                                         cudaStream_t stream);
+
+// Encoders for the TMA descriptors (driver entry point, resolved once).
+CUresult encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                        uint64_t inner, uint64_t outer, uint64_t outer_stride_bytes,
+                        uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle);
+
+}  // namespace w4a16
