@@ -7,13 +7,17 @@ for every projection of the workload, RTN quantize/pack of its bf16 weight
 the action-expert projections at M = 50 tokens, (N, K) = (2048, 1024),
 (1024, 1024), (8192, 1024), (1024, 4096), seeds 1..4.
 
-Timing: W untimed warm-up steps, then exactly K timed steps between CUDA
+Timing: the steps are captured into CUDA graphs (the library's calls are
+capture-safe), so no host launch overhead sits between kernels.  W untimed
+warm-up steps replay first, then exactly K timed steps replay between CUDA
 events on the launching stream, with a device synchronize (and, for N > 1,
 a barrier) on both sides; the max over ranks is reported.  Every step reads
 a different copy of all inputs and the copies together exceed 3x the L2
 size, so each step streams its inputs from HBM.  Kernel durations for the
-roofline come from CUDA events recorded around each launch on the same
-stream during the timed steps.
+roofline come from a second replay of the same K steps with CUDA events
+recorded around each launch on the same stream.  The e2e figure is the
+eager public API (no graph) with pinned host inputs copied in and results
+copied out every step.
 
 `value` is whole-job algorithmic HBM bytes per second (GB/s): for each
 quantize 2.515625 * N * K bytes (bf16 read, codes and scales written), for
@@ -176,7 +180,8 @@ def run_gpu(args, rank, world):
             Wd = W.to(dev) if r == 0 else sets[0][len(s)]["W"].clone()
             Ad = A.to(dev) if r == 0 else sets[0][len(s)]["A"].clone()
             s.append(dict(W=Wd, A=Ad,
-                          packed=torch.empty(c.N, c.K // 2, dtype=torch.uint8, device=dev),
+                          packed=torch.empty(w4.w4a16_packed_bytes(c.N, c.K), dtype=torch.uint8,
+                                             device=dev),
                           scales=torch.empty(c.K // 128, c.N, dtype=torch.float16, device=dev),
                           Y=torch.empty(c.M, c.N, dtype=torch.bfloat16, device=dev)))
         sets.append(s)
@@ -185,6 +190,7 @@ def run_gpu(args, rank, world):
     stream = torch.cuda.current_stream(dev)
 
     n_k = 2 * len(cases)
+
     def step(r, evs=None):
         for j, c in enumerate(cases):
             s = sets[r % copies][j]
@@ -198,43 +204,99 @@ def run_gpu(args, rank, world):
             if evs is not None:
                 evs[2 * j + 1][1].record(stream)
 
-    for r in range(args.warmup):
+    # eager warm-up (also sets kernel attributes outside any capture)
+    for r in range(min(args.warmup, copies)):
         step(r)
     torch.cuda.synchronize(dev)
     if w4.w4a16_get_device_error() != w4.W4A16_OK:
         raise RuntimeError("device error during warm-up")
+
+    # The timed steps run as one CUDA graph (no host launch overhead between
+    # kernels): graph A holds warm-up + timed steps back to back; graph B is
+    # the same steps with timing events around every kernel.
+    def capture(n_steps, first, with_events):
+        evs = None
+        if with_events:
+            evs = [[[torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
+                    for _ in range(n_k)] for _ in range(n_steps)]
+        g = torch.cuda.CUDAGraph()
+        cap_stream = torch.cuda.Stream(dev)
+        cap_stream.wait_stream(torch.cuda.current_stream(dev))
+        l0 = w4.w4a16_launch_count()
+        with torch.cuda.stream(cap_stream):
+            with torch.cuda.graph(g, stream=cap_stream):
+                for r in range(n_steps):
+                    step_on(first + r, cap_stream, None if evs is None else evs[r])
+        torch.cuda.current_stream(dev).wait_stream(cap_stream)
+        return g, evs, w4.w4a16_launch_count() - l0
+
+    def step_on(r, st, evs):
+        for j, c in enumerate(cases):
+            s = sets[r % copies][j]
+            if evs is not None:
+                evs[2 * j][0].record(st)
+            w4.w4a16_quantize(s["W"], packed=s["packed"], scales=s["scales"], stream=st)
+            if evs is not None:
+                evs[2 * j][1].record(st)
+                evs[2 * j + 1][0].record(st)
+            w4.w4a16_gemm(s["A"], s["packed"], s["scales"], Y=s["Y"], workspace=ws, stream=st)
+            if evs is not None:
+                evs[2 * j + 1][1].record(st)
+
+    g_warm, _, _ = capture(args.warmup, 0, False)
+    g_timed, _, launches_per_replay = capture(args.steps, args.warmup, False)
+    try:
+        g_ev, kev, _ = capture(args.steps, args.warmup, True)
+    except TypeError:
+        g_ev, kev = None, None
 
     def barrier():
         if world > 1:
             import torch.distributed as dist
             dist.barrier()
 
-    # --- timed region: whole steps, back to back
+    # --- timed region
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    launches0 = w4.w4a16_launch_count()
+    g_warm.replay()
     barrier()
     torch.cuda.synchronize(dev)
     with ClockSampler(dev.index) as clk:
         start.record(stream)
-        for r in range(args.steps):
-            step(args.warmup + r)
+        g_timed.replay()
         end.record(stream)
         torch.cuda.synchronize(dev)
     barrier()
-    launches = w4.w4a16_launch_count() - launches0
+    launches = launches_per_replay
     elapsed_ms = start.elapsed_time(end)
 
-    # --- per-kernel durations (separate pass with events around each launch)
-    kev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_k)]
-           for _ in range(args.steps)]
-    torch.cuda.synchronize(dev)
-    for r in range(args.steps):
-        step(args.warmup + args.steps + r, kev[r])
-    torch.cuda.synchronize(dev)
+    # --- per-kernel durations: the same steps with events around each kernel
+    if g_ev is not None:
+        g_warm.replay()
+        g_ev.replay()
+        torch.cuda.synchronize(dev)
+        kern_ms = [statistics.mean(kev[r][k][0].elapsed_time(kev[r][k][1]) for r in range(args.steps))
+                   for k in range(n_k)]
+    else:
+        kern_ms = []
+        for k in range(n_k):
+            gk = torch.cuda.CUDAGraph()
+            j, is_gemm = divmod(k, 2)
+            with torch.cuda.graph(gk):
+                for r in range(args.steps):
+                    s = sets[(args.warmup + r) % copies][j]
+                    if is_gemm:
+                        w4.w4a16_gemm(s["A"], s["packed"], s["scales"], Y=s["Y"], workspace=ws)
+                    else:
+                        w4.w4a16_quantize(s["W"], packed=s["packed"], scales=s["scales"])
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            gk.replay()
+            e0.record(stream)
+            gk.replay()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            kern_ms.append(e0.elapsed_time(e1) / args.steps)
     if w4.w4a16_get_device_error() != w4.W4A16_OK:
         raise RuntimeError("device error during timing")
-    kern_ms = [statistics.mean(kev[r][k][0].elapsed_time(kev[r][k][1]) for r in range(args.steps))
-               for k in range(n_k)]
 
     # --- e2e: pinned host inputs -> device, the path, result -> host
     pinned = [(W.pin_memory(), A.pin_memory()) for (W, A, b) in host_sets]

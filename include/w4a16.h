@@ -14,9 +14,20 @@
  *
  * Data layout (all row-major, all device memory, all owned by the caller):
  *   W       [N, K]     bf16   weight to quantize (K contiguous)
- *   packed  [N, K/2]   uint8  code of k = 2j in the low nibble of byte j,
- *                             code of k = 2j+1 in the high nibble, two's
- *                             complement
+ *   packed  tiles      uint8  tiled storage of the codes: row n, byte j
+ *                             of the row-major [N, K/2] code array (code of
+ *                             k = 2j in the low nibble, k = 2j+1 in the high
+ *                             nibble, two's complement) is stored at offset
+ *                             ((n / 128) * (K / 128) + j / 64) * 8192
+ *                             + (n % 128) * 64 + j % 64.  Each 128 x 128
+ *                             tile is one contiguous 8 KiB block; rows past N
+ *                             (to the next multiple of 128) hold zeros.  Size
+ *                             w4a16_packed_bytes(N, K).  The layout belongs
+ *                             to this library's GEMM ("Kernel dispatch and
+ *                             Humming quantization in PhyAI", section
+ *                             "Humming makes the separation useful": the
+ *                             packed layout is executed only by its
+ *                             matching kernel).
  *   scales  [K/128, N] fp16   scale of group g of row n at scales[g * N + n]
  *   A       [M, K]     bf16   activations
  *   bias    [N]        bf16   optional
@@ -69,7 +80,8 @@ typedef enum {
 /* Human-readable name of a status code.  Never NULL. */
 const char* w4a16_status_string(int status);
 
-/* Bytes of the packed code array for an [N, K] weight: N * K / 2. */
+/* Bytes of the tiled code storage of an [N, K] weight:
+ * ceil(N / 128) * 128 * K / 2. */
 size_t w4a16_packed_bytes(int64_t N, int64_t K);
 
 /* Bytes of the scale array: (K / group) * N * 2.  0 if group != 128. */
@@ -81,9 +93,10 @@ size_t w4a16_scales_bytes(int64_t N, int64_t K, int group);
  * INT4, group 128).  For each row n and group g:
  *   amax = max |W[n, k]| (fp32);  s = fp16_rn(amax / 7.0f);  s = 1 if s == 0;
  *   q = clamp(rint_even(W[n, k] / s), -8, 7)   (IEEE fp32 division)
- * writes the codes to packed_out and s to scales_out[g * N + n].
- * W: [N, K] bf16 (read);  packed_out: N*K/2 bytes;  scales_out: (K/128)*N
- * fp16 (both written).  One kernel launch on `stream`.
+ * writes the codes to packed_out (tiled storage, padding rows zero) and s
+ * to scales_out[g * N + n].  W: [N, K] bf16 (read);  packed_out:
+ * w4a16_packed_bytes(N, K) bytes;  scales_out: (K/128)*N fp16 (both
+ * written).  One kernel launch on `stream`.
  */
 int w4a16_quantize(const void* W_bf16, int64_t N, int64_t K, int group, void* packed_out,
                    void* scales_out, void* stream);
@@ -187,6 +200,11 @@ int w4a16_selftest_wait_timeout(uint64_t timeout_ns, void* stream);
 
 /* Number of kernel launches this library has made in this process. */
 uint64_t w4a16_launch_count(void);
+
+/* Text of the last CUDA failure that made a call of this thread return
+ * W4A16_ERR_CUDA ("" if none).  The library clears the CUDA runtime's
+ * per-thread last error when it reports such a failure. */
+const char* w4a16_last_error_detail(void);
 
 #ifdef __cplusplus
 }

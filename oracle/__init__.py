@@ -3,14 +3,19 @@ see ``w4a16_oracle`` for what it computes and which passages it follows."""
 
 from .w4a16_oracle import (  # noqa: F401
     GROUP,
+    TILE_BYTES,
+    TILE_ROWS,
     QMAX,
     QMIN,
     bf16_bits_to_f32,
     dequantize,
+    from_tile_layout,
     gemm,
     pack_codes,
     quantize,
     quantize_f32,
     scales_f32,
+    tiled_bytes,
+    to_tile_layout,
     unpack_codes,
 )

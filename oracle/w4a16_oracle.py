@@ -33,9 +33,13 @@ reason in the design notes of the repository):
    fp16 (all-zero group, or an absmax so small that absmax/7 underflows) is
    replaced by 1.0.
 4. fp16 subnormal scales are kept (no flush to zero).
-5. Packed layout: ``packed[N, K/2]`` bytes, byte j of a row holds code 2j in
-   its low nibble and code 2j+1 in its high nibble, two's complement.
-   ``scales[K/128, N]`` fp16, group-major.
+5. Packed layout: within a row, byte j holds code 2j in its low nibble and
+   code 2j+1 in its high nibble, two's complement (``pack_codes`` gives the
+   plain row-major ``[N, K/2]`` array).  The library stores those bytes in
+   tiles of 128 rows x 128 K values (8 KiB, row-major inside the tile), tile
+   (tn, g) at byte offset (tn * K/128 + g) * 8192, rows past N zero
+   (``to_tile_layout`` / ``from_tile_layout``): a pure permutation of the
+   row-major bytes.  ``scales[K/128, N]`` fp16, group-major.
 6. Groups are contiguous runs of 128 along K, starting at k = 0, per row n.
 7. Dequantized weight = float(code) * float(scale), exact in fp32.
 8. GEMM: ``Y = A @ dequant(W)^T (+ bias)`` accumulated in FP32, bias added in
@@ -128,6 +132,40 @@ def unpack_codes(packed: np.ndarray) -> np.ndarray:
     codes[:, 0::2] = lo
     codes[:, 1::2] = hi
     return codes
+
+
+TILE_ROWS = 128      # rows of a storage tile
+TILE_BYTES = TILE_ROWS * GROUP // 2
+
+
+def tiled_bytes(n_rows: int, k_cols: int) -> int:
+    """Bytes of the tiled storage of an [N, K] weight (rows padded to 128)."""
+    return -(-n_rows // TILE_ROWS) * TILE_ROWS * k_cols // 2
+
+
+def to_tile_layout(packed: np.ndarray) -> np.ndarray:
+    """Row-major packed bytes [N, K/2] -> tiled storage (1-D uint8).
+    Byte (n, j) goes to offset ((n // 128) * (K/128) + j // 64) * 8192 +
+    (n % 128) * 64 + j % 64; padding rows are zero."""
+    p = np.ascontiguousarray(packed, dtype=np.uint8)
+    n_rows, half = p.shape
+    n_groups = half // (GROUP // 2)
+    n_tiles = -(-n_rows // TILE_ROWS)
+    padded = np.zeros((n_tiles * TILE_ROWS, half), dtype=np.uint8)
+    padded[:n_rows] = p
+    t = padded.reshape(n_tiles, TILE_ROWS, n_groups, GROUP // 2)   # [tn, r, g, byte]
+    return np.ascontiguousarray(t.transpose(0, 2, 1, 3)).reshape(-1)
+
+
+def from_tile_layout(tiled: np.ndarray, n_rows: int, k_cols: int) -> np.ndarray:
+    """Inverse of :func:`to_tile_layout`: tiled storage -> [N, K/2] bytes."""
+    b = np.ascontiguousarray(tiled, dtype=np.uint8).reshape(-1)
+    n_tiles = -(-n_rows // TILE_ROWS)
+    n_groups = k_cols // GROUP
+    if b.size != n_tiles * TILE_ROWS * k_cols // 2:
+        raise ValueError("tiled buffer has the wrong size")
+    t = b.reshape(n_tiles, n_groups, TILE_ROWS, GROUP // 2).transpose(0, 2, 1, 3)
+    return np.ascontiguousarray(t.reshape(n_tiles * TILE_ROWS, k_cols // 2)[:n_rows])
 
 
 def scales_f32(scale_bits: np.ndarray) -> np.ndarray:

@@ -20,8 +20,9 @@ def oracle_quantize(W: torch.Tensor):
 
 
 def check_quantize_exact(W: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor):
-    p_ref, s_ref = oracle_quantize(W)
-    p = packed.cpu().numpy()
+    p_rm, s_ref = oracle_quantize(W)
+    p_ref = oracle.to_tile_layout(p_rm)
+    p = packed.cpu().numpy().reshape(-1)
     s = scales.cpu().view(torch.int16).numpy().view(np.uint16)
     assert p.shape == p_ref.shape and s.shape == s_ref.shape
     bad_s = np.argwhere(s != s_ref)

@@ -39,6 +39,7 @@ def test_binding_covers_every_declared_symbol():
 
 def test_sizes(built_lib):
     assert w4.w4a16_packed_bytes(256, 512) == 256 * 256
+    assert w4.w4a16_packed_bytes(264, 512) == 384 * 256     # rows padded to whole 128-row tiles
     assert w4.w4a16_scales_bytes(256, 512) == 4 * 256 * 2
     assert w4.w4a16_scales_bytes(256, 512, 64) == 0
 

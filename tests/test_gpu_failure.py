@@ -29,7 +29,7 @@ def test_graph_capture(w4):
     case = synthetic.Case("graph", 50, 1024, 1024, 8, bias=True)
     W, A, b, _, _ = make_operands(w4, case)
     Wd, Ad, bd = W.cuda(), A.cuda(), b.cuda()
-    packed = torch.empty(1024, 512, dtype=torch.uint8, device="cuda")
+    packed = torch.empty(w4.w4a16_packed_bytes(1024, 1024), dtype=torch.uint8, device="cuda")
     scales = torch.empty(8, 1024, dtype=torch.float16, device="cuda")
     Y = torch.empty(50, 1024, dtype=torch.bfloat16, device="cuda")
     ws = torch.zeros(max(w4.w4a16_gemm_workspace_bytes(50, 1024, 1024), 16), dtype=torch.uint8,

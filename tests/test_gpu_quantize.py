@@ -55,7 +55,7 @@ def test_small_and_ragged_shapes(w4, N, K):
 def test_outputs_stay_in_bounds(w4):
     N, K = 40, 640
     W = synthetic.draw_weight_only(3, N, K).cuda()
-    packed, p_ok = guarded((N, K // 2), torch.uint8, W.device, 0xA5)
+    packed, p_ok = guarded((w4.w4a16_packed_bytes(N, K),), torch.uint8, W.device, 0xA5)
     scales, s_ok = guarded((K // 128, N), torch.float16, W.device, 0x7E00)
     w4.w4a16_quantize(W, packed=packed, scales=scales)
     torch.cuda.synchronize()

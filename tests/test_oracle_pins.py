@@ -86,3 +86,25 @@ def test_rejects_bad_shapes():
         oracle.quantize_f32(np.zeros((2, 100), np.float32))
     with pytest.raises(ValueError):
         oracle.quantize_f32(np.zeros((2, 256), np.float32), group=64)
+
+
+def test_tile_layout_closed_form():
+    # every byte lands at the offset the layout formula gives, by brute force
+    rng = np.random.default_rng(13)
+    N, K = 136, 384
+    p = rng.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    t = oracle.to_tile_layout(p)
+    assert t.size == oracle.tiled_bytes(N, K) == 256 * K // 2
+    G = K // 128
+    for n in range(N):
+        for j in range(K // 2):
+            off = ((n // 128) * G + j // 64) * 8192 + (n % 128) * 64 + j % 64
+            assert t[off] == p[n, j]
+    # padding rows are zero, and the inverse recovers the row-major bytes
+    pad = np.ones(t.size, bool)
+    for n in range(N):
+        for g in range(G):
+            base = ((n // 128) * G + g) * 8192 + (n % 128) * 64
+            pad[base:base + 64] = False
+    assert not t[pad].any()
+    assert (oracle.from_tile_layout(t, N, K) == p).all()

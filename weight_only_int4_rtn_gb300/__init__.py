@@ -58,6 +58,7 @@ SIGNATURES = [
     ("w4a16_set_wait_timeout_ns", None, [ctypes.c_uint64]),
     ("w4a16_selftest_wait_timeout", ctypes.c_int, [ctypes.c_uint64, _vp]),
     ("w4a16_launch_count", ctypes.c_uint64, []),
+    ("w4a16_last_error_detail", ctypes.c_char_p, []),
 ]
 
 _lib = None
@@ -97,6 +98,8 @@ def status_string(status: int) -> str:
 
 def _check(status: int, what: str) -> None:
     if status != W4A16_OK:
+        if status == W4A16_ERR_CUDA:
+            what = f"{what} [{lib().w4a16_last_error_detail().decode()}]"
         raise W4A16Error(status, what)
 
 
@@ -137,19 +140,22 @@ def w4a16_gemm_workspace_bytes_max(M: int, N: int, K: int) -> int:
 # --------------------------------------------------------------- quantize
 def w4a16_quantize(W: torch.Tensor, group: int = GROUP, packed: torch.Tensor | None = None,
                    scales: torch.Tensor | None = None, stream=None):
-    """RTN-quantize ``W[N, K]`` (bf16, CUDA).  Returns ``(packed uint8 [N, K/2],
-    scales fp16 [K/128, N])``; outputs are allocated when not given."""
+    """RTN-quantize ``W[N, K]`` (bf16, CUDA).  Returns ``(packed, scales)``:
+    ``packed`` is the 1-D uint8 tiled code storage of w4a16_packed_bytes(N, K)
+    bytes, ``scales`` fp16 ``[K/128, N]``; outputs are allocated when not
+    given."""
     _require_cuda(W, "W", torch.bfloat16)
     if W.dim() != 2:
         raise ValueError("W must be [N, K]")
     N, K = W.shape
+    nbytes = lib().w4a16_packed_bytes(N, K)
     if packed is None:
-        packed = torch.empty((N, K // 2), dtype=torch.uint8, device=W.device)
+        packed = torch.empty(nbytes, dtype=torch.uint8, device=W.device)
     if scales is None:
         scales = torch.empty((max(K // group, 0), N), dtype=torch.float16, device=W.device)
     _require_cuda(packed, "packed", torch.uint8)
     _require_cuda(scales, "scales", torch.float16)
-    if packed.numel() * 2 != N * K or scales.numel() * group != N * K:
+    if packed.numel() != nbytes or scales.numel() * group != N * K:
         raise ValueError("output buffers have the wrong size")
     st = lib().w4a16_quantize(W.data_ptr(), N, K, group, packed.data_ptr(), scales.data_ptr(),
                               _stream_handle(W.device, stream))
@@ -190,12 +196,14 @@ def w4a16_gemm(A: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor,
     _require_cuda(A, "A", torch.bfloat16)
     _require_cuda(packed, "packed", torch.uint8)
     _require_cuda(scales, "scales", torch.float16)
-    if A.dim() != 2 or packed.dim() != 2 or scales.dim() != 2:
-        raise ValueError("A, packed and scales must be 2-D")
+    if A.dim() != 2 or scales.dim() != 2:
+        raise ValueError("A and scales must be 2-D")
     M, K = A.shape
-    N = packed.shape[0]
-    if packed.shape[1] * 2 != K or scales.shape != (K // group, N):
-        raise ValueError("packed must be [N, K/2] and scales [K/128, N]")
+    N = scales.shape[1]
+    if scales.shape[0] * group != K:
+        raise ValueError("scales must be [K/128, N]")
+    if packed.numel() != lib().w4a16_packed_bytes(N, K):
+        raise ValueError("packed must hold w4a16_packed_bytes(N, K) bytes of tiled codes")
     if bias is not None:
         _require_cuda(bias, "bias", torch.bfloat16)
         if bias.numel() != N:

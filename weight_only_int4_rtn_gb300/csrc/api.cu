@@ -35,6 +35,18 @@ __device__ uint32_t g_error_word;
 namespace {
 
 std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+thread_local char g_error_detail[256] = "";
+
+// Record a failed CUDA call for w4a16_last_error_detail and clear the
+// runtime's per-thread last error, so that it does not surface in an
+// unrelated later call of this library or of the caller.
+int cuda_failure(cudaError_t e, const char* where) {
+  std::snprintf(g_error_detail, sizeof(g_error_detail), "%s: %s (%d)", where,
+                cudaGetErrorString(e), static_cast<int>(e));
+  (void)cudaGetLastError();
+  if (std::getenv("W4A16_LOG") != nullptr) std::fprintf(stderr, "w4a16: %s\n", g_error_detail);
+  return W4A16_ERR_CUDA;
+}
 std::atomic<uint64_t> g_launches{0};
 
 constexpr int kMaxDevices = 64;
@@ -75,17 +87,16 @@ struct Variant {
 };
 
 const Variant kVariants[] = {
-    {"tc_a16_grp_sk", {16, 2, true, 16}, true},
-    {"tc_a32_grp_sk", {32, 2, true, 12}, true},
-    {"tc_a64_grp_sk", {64, 2, true, 8}, true},
-    {"tc_a64_deq_sk", {64, 2, false, 8}, true},
-    {"tc_a128_grp_sk", {128, 2, true, 5}, true},
-    {"tc_a128_deq_sk", {128, 2, false, 5}, true},
-    {"tc_a256_deq_sk", {256, 2, false, 3}, true},
-    {"tc_a16_grp_dp", {16, 2, true, 16}, false},
-    {"tc_a64_grp_dp", {64, 2, true, 8}, false},
-    {"tc_a128_deq_dp", {128, 2, false, 5}, false},
-    {"tc_a256_deq_dp", {256, 2, false, 3}, false},
+    {"tc_a16_grp_sk", {16, 2, true, 16, 1}, true},
+    {"tc_a32_grp_sk", {32, 2, true, 12, 1}, true},
+    {"tc_a64_grp_sk", {64, 2, true, 8, 1}, true},
+    {"tc_a64_deq_sk", {64, 2, false, 8, 1}, true},
+    {"tc_a128_deq_sk", {128, 2, false, 5, 1}, true},
+    {"tc_a256_deq_sk", {256, 2, false, 3, 1}, true},
+    {"tc_a16_grp_dp", {16, 2, true, 16, 1}, false},
+    {"tc_a64_grp_dp", {64, 2, true, 8, 1}, false},
+    {"tc_a128_deq_dp", {128, 2, false, 5, 1}, false},
+    {"tc_a256_deq_dp", {256, 2, false, 3, 1}, false},
 };
 constexpr int kNumVariants = static_cast<int>(sizeof(kVariants) / sizeof(kVariants[0]));
 
@@ -103,6 +114,7 @@ bool shape_ok(int64_t M, int64_t N, int64_t K) {
 
 GemmSchedule make_schedule(const Variant& v, int64_t M, int64_t N, int64_t K, int num_sms) {
   GemmSchedule s{};
+  if (num_sms > kMaxGrid) num_sms = kMaxGrid;
   const int64_t tiles = gemm_tiles(v.cfg, M, N);
   const int64_t KB = K / kGroup;
   const int64_t units = tiles * KB;
@@ -147,7 +159,7 @@ int rule_variant(int64_t M, int64_t N, int64_t K) {
   if (M <= 16) return variant_by_name("tc_a16_grp_sk");
   if (M <= 32) return variant_by_name("tc_a32_grp_sk");
   if (M <= 64) return variant_by_name("tc_a64_grp_sk");
-  if (M <= 128) return variant_by_name("tc_a128_grp_sk");
+  if (M <= 128) return variant_by_name("tc_a128_deq_sk");
   return variant_by_name("tc_a256_deq_sk");
 }
 
@@ -249,7 +261,7 @@ int run_gemm(int id, const void* A, int64_t M, int64_t N, int64_t K, const void*
                  static_cast<long long>(M), static_cast<long long>(N), static_cast<long long>(K),
                  v.name, s.grid, s.dp_tiles, static_cast<long long>(s.sk_units));
   const cudaError_t e = launch_gemm_tc(v.cfg, s, p, /*use_pdl=*/true, stream);
-  if (e != cudaSuccess) return W4A16_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_failure(e, v.name);
   g_launches.fetch_add(1);
   return W4A16_OK;
 }
@@ -265,9 +277,8 @@ size_t variant_ws(int id, int64_t M, int64_t N, int64_t K) {
 }  // namespace
 
 // ------------------------------------------------------------------ TMA
-CUresult encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
-                        uint64_t inner, uint64_t outer, uint64_t outer_stride_bytes,
-                        uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle) {
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
     void* f = nullptr;
     cudaDriverEntryPointQueryResult q{};
@@ -277,12 +288,35 @@ CUresult encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void*
       f = nullptr;
     return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
   }();
+  return fn;
+}
+}  // namespace
+
+CUresult encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                        uint64_t inner, uint64_t outer, uint64_t outer_stride_bytes,
+                        uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle) {
+  const auto fn = tmap_encoder();
   if (fn == nullptr) return CUDA_ERROR_NOT_FOUND;
   const cuuint64_t dims[2] = {inner, outer};
   const cuuint64_t strides[1] = {outer_stride_bytes};
   const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t estr[2] = {1, 1};
   return fn(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+CUresult encode_tmap_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                        uint64_t d0, uint64_t d1, uint64_t d2, uint64_t stride1_bytes,
+                        uint64_t stride2_bytes, uint32_t box0, uint32_t box1, uint32_t box2,
+                        CUtensorMapSwizzle swizzle) {
+  const auto fn = tmap_encoder();
+  if (fn == nullptr) return CUDA_ERROR_NOT_FOUND;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+  const cuuint32_t box[3] = {box0, box1, box2};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, dtype, 3, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
@@ -309,7 +343,8 @@ const char* w4a16_status_string(int status) {
 
 size_t w4a16_packed_bytes(int64_t N, int64_t K) {
   if (N < 0 || K < 0) return 0;
-  return static_cast<size_t>(N) * static_cast<size_t>(K) / 2;
+  const int64_t n_pad = (N + kTileW - 1) / kTileW * kTileW;
+  return static_cast<size_t>(n_pad) * static_cast<size_t>(K) / 2;
 }
 
 size_t w4a16_scales_bytes(int64_t N, int64_t K, int group) {
@@ -329,9 +364,10 @@ int w4a16_quantize(const void* W_bf16, int64_t N, int64_t K, int group, void* pa
     return W4A16_ERR_ALIGNMENT;
   DeviceInfo dev;
   if (!device_info(dev)) return W4A16_ERR_CUDA;
-  const cudaError_t e = launch_rtn_quantize(W_bf16, N, K, packed_out, scales_out, dev.num_sms,
-                                            static_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return W4A16_ERR_CUDA;
+  const cudaError_t e =
+      launch_rtn_quantize(W_bf16, N, K, packed_out, scales_out, dev.num_sms, dev.error_word,
+                          g_timeout_ns.load(), static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_failure(e, "rtn_quantize");
   g_launches.fetch_add(1);
   return W4A16_OK;
 }
@@ -555,13 +591,15 @@ void w4a16_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns == 0 ? 1 : n
 int w4a16_selftest_wait_timeout(uint64_t timeout_ns, void* stream) {
   DeviceInfo dev;
   if (!device_info(dev)) return W4A16_ERR_CUDA;
-  if (launch_wait_timeout_selftest(dev.error_word, timeout_ns,
-                                   static_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return W4A16_ERR_CUDA;
+  const cudaError_t e =
+      launch_wait_timeout_selftest(dev.error_word, timeout_ns, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_failure(e, "wait_timeout_selftest");
   g_launches.fetch_add(1);
   return W4A16_OK;
 }
 
 uint64_t w4a16_launch_count(void) { return g_launches.load(); }
+
+const char* w4a16_last_error_detail(void) { return g_error_detail; }
 
 }  // extern "C"

@@ -18,15 +18,17 @@
 //     128-byte-swizzled K-major layout and described by a shared-memory
 //     descriptor (the MMA's B operand).
 //   * Each K block (128 values = one quantization group) is one pipeline
-//     unit: TMA brings the packed codes (128 rows x 64 B), the 128 scales of
-//     that group and the activation slice; the workers convert; one thread
-//     issues 8 MMAs of K = 16.
+//     unit: TMA brings the packed codes (one contiguous 8 KiB tile of the
+//     tiled storage: 128 rows x 64 B), the 128 scales of that group and the
+//     activation slice; the dequant warps convert; one thread issues 8 MMAs
+//     of K = 16.  (Row-major codes would make every unit 128 separate 64-byte
+//     pieces K/2 bytes apart, which TMA streams several times slower.)
 //
 // Two scaling modes:
 //   group_scale = true:  the weight operand holds the integer codes (exact in
 //     bf16); each unit's MMA result D_g is the integer-code partial sum of one
-//     group, which the workers read back and accumulate as acc += s[g, n] *
-//     D_g in fp32 registers.  Cheapest conversion; used for small act_tile.
+//     group, which the readout warps accumulate as acc += s[g, n] * D_g in
+//     fp32 registers.  Cheapest conversion; used for small act_tile.
 //   group_scale = false: the weight operand is bf16_rn(q * s), computed
 //     exactly as fma(q, s_hi, q * s_lo) with s = s_hi + s_lo split into two
 //     bf16 values; D accumulates the whole K range in TMEM.
@@ -40,12 +42,17 @@
 // (deterministic), adds the bias and stores Y, then resets the counter.
 // Nothing ever waits on another CTA.
 //
-// Warp roles (blockDim = 64 + 128 * worker_wgs):
-//   warp 0      TMA producer (one lane)
+// Warp roles (blockDim = 224 + 128 * dequant_wgs):
+//   warps 0, 2  TMA producers (one lane each; even and odd units, because one
+//               thread can only complete a few mbarrier phases per
+//               microsecond, fewer than the weight stream needs)
 //   warp 1      TMEM allocator; MMA issuer (one lane)
-//   warps 2..   workers: dequant into TMEM, read accumulators, epilogue.
-//               A warp may only touch TMEM lanes 32 * (warp % 4) .. + 31, so
-//               each worker thread owns weight row 32 * (warp % 4) + lane.
+//   warps 3-6   readout: accumulator -> registers / output, stream-K fixup
+//   warps 7..   dequant: packed codes (shared memory) -> weight operand (TMEM)
+// A warp may only touch TMEM lanes 32 * (warp % 4) .. + 31, so each readout
+// and dequant thread owns weight row 32 * (warp % 4) + lane.  The dequant
+// warps never wait on accumulators: they run up to four units ahead of the
+// MMA, which runs up to DB units ahead of the readout.
 //
 // Every wait on an mbarrier is bounded by a time limit; on expiry the kernel
 // records an error word, lets every role leave its loop, waits (bounded) for
@@ -58,24 +65,51 @@
 
 #include "kernels.h"
 #include "ptx.cuh"
+#include "waits.cuh"
 
 namespace w4a16 {
 
+#ifdef W4A16_TRACE
+// Timestamp probes for profiling builds only (never in the default build).
+__device__ unsigned long long* g_trace = nullptr;
+__device__ unsigned long long* g_trace_units = nullptr;
+#define W4A16_TRACE_POINT(id)                                                           \
+  do {                                                                                  \
+    if (trace_cta != nullptr) trace_cta[blockIdx.x * 16 + (id)] = ptx::globaltimer_ns(); \
+  } while (0)
+#define W4A16_TRACE_UNIT(role, i)                                                       \
+  do {                                                                                  \
+    if (trace_unit != nullptr && (i) < 64)                                             \
+      trace_unit[(role) * 64 + (i)] = static_cast<unsigned long long>(clock64());     \
+  } while (0)
+#else
+#define W4A16_TRACE_POINT(id) \
+  do {                        \
+  } while (0)
+#define W4A16_TRACE_UNIT(role, i) \
+  do {                            \
+  } while (0)
+#endif
+
 namespace {
 
-constexpr int kUnitK = 128;               // K values per unit (one group)
+constexpr int kUnitK = 128;                    // K values per unit (one group)
 constexpr int kWBytes = kTileW * kUnitK / 2;   // packed codes per unit: 8 KiB
 constexpr int kSBytes = kTileW * 2;            // scales per unit: 256 B
 constexpr int kAStages = 4;                    // weight-operand stages in TMEM
 constexpr int kAStageCols = kUnitK / 2;        // 64 TMEM columns per stage
 constexpr int kDCol = kAStages * kAStageCols;  // accumulators start at column 256
+constexpr int kDCols = 512 - kDCol;            // 256 accumulator columns
 constexpr uint32_t kTmemCols = 512;
+constexpr int kReadoutWarp0 = 3;
+constexpr int kDequantWarp0 = 7;
 
 struct Args {
   int M, N, K, KB;
   int n_tiles;
   int dp_tiles;
   int sk_units;
+  int act_3d;                  // activation map is 3-D: both 64-k halves in one copy
   const __nv_bfloat16* bias;
   __nv_bfloat16* Y;
   float* ws;
@@ -137,6 +171,65 @@ struct Sched {
   }
 };
 
+// Walks this CTA's units in order, one at a time, with no division per unit
+// (the issuing threads are on the critical path of the pipeline).
+struct UnitIter {
+  int C, KB, ndp, u0, u1, dp_tiles;
+  int i, tile, kb, u, tl, first_tl;
+
+  __device__ void init(const Sched& s) {
+    C = s.C;
+    KB = s.KB;
+    ndp = s.dp_iters * s.KB;
+    u0 = s.u0;
+    u1 = s.u1;
+    dp_tiles = s.dp_tiles;
+    i = 0;
+    tile = s.c;
+    kb = 0;
+    if (ndp == 0) start_sk();
+  }
+  __device__ void start_sk() {
+    u = u0;
+    tl = u0 / KB;
+    first_tl = tl;
+    kb = u0 - tl * KB;
+    tile = dp_tiles + tl;
+  }
+  __device__ Unit next() {
+    Unit r;
+    r.tile = tile;
+    r.kb = kb;
+    if (i < ndp) {
+      r.seg_first = (kb == 0);
+      r.seg_last = (kb == KB - 1);
+      r.whole = true;
+      r.slot = 0;
+      r.sk_tile = -1;
+      ++i;
+      if (++kb == KB) {
+        kb = 0;
+        tile += C;
+      }
+      if (i == ndp) start_sk();
+    } else {
+      r.seg_first = (kb == 0) || (u == u0);
+      r.seg_last = (kb == KB - 1) || (u == u1 - 1);
+      r.whole = (tl * KB >= u0) && ((tl + 1) * KB <= u1);
+      r.slot = (tl == first_tl) ? 0 : 1;
+      r.sk_tile = tl;
+      ++i;
+      ++u;
+      if (++kb == KB) {
+        kb = 0;
+        ++tl;
+        ++tile;
+      }
+    }
+    return r;
+  }
+};
+
 // CTA that owns stream-K unit u under the balanced split.
 __device__ __forceinline__ int sk_owner(int u, int C, int sk_units) {
   return static_cast<int>(((static_cast<int64_t>(u) + 1) * C - 1) / sk_units);
@@ -147,62 +240,15 @@ struct Shared {
   uint64_t empty[16];
   uint64_t afull[kAStages];
   uint64_t aempty[kAStages];
-  uint64_t dfull[2];
-  uint64_t dempty[2];
+  uint64_t dfull[4];
+  uint64_t dempty[4];
+  uint64_t unit_done[16];     // ring: phase completes when a unit's MMAs completed
   uint64_t mma_done;
-  uint64_t wsync;             // worker-only barrier (bounded waits, unlike bar.sync)
+  uint64_t wsync;             // readout-only barrier (bounded waits, unlike bar.sync)
   uint32_t tmem_base;
   int abort_flag;
   int fixup_last;
 };
-
-// ------------------------------------------------------------- bounded waits
-__device__ __forceinline__ void record_timeout(const Args& a, Shared* sh) {
-  *reinterpret_cast<volatile int*>(&sh->abort_flag) = 1;
-  atomicOr(a.err, 1u);
-}
-
-// Single-thread wait.  false = gave up (timeout, or another role gave up).
-__device__ bool wait_one(uint64_t* bar, uint32_t parity, const Args& a, Shared* sh) {
-  if (ptx::mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = ptx::globaltimer_ns();
-  for (uint32_t spin = 1;; ++spin) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
-    if ((spin & 31) == 0) {
-      if (*reinterpret_cast<volatile int*>(&sh->abort_flag)) return false;
-      if (ptx::globaltimer_ns() - t0 > a.timeout_ns) {
-        record_timeout(a, sh);
-        return false;
-      }
-    }
-  }
-}
-
-// Warp-uniform wait: every lane observes the phase; the give-up decision is
-// lane 0's and is shared, so the warp stays converged for .sync.aligned ops.
-__device__ bool wait_warp(uint64_t* bar, uint32_t parity, const Args& a, Shared* sh) {
-  const int lane = threadIdx.x & 31;
-  uint64_t t0 = 0;
-  for (uint32_t spin = 0;; ++spin) {
-    const bool ok = ptx::mbar_try_wait(bar, parity);
-    if (__all_sync(0xffffffffu, ok)) return true;
-    if ((spin & 31) == 31) {
-      int give_up = 0;
-      if (lane == 0) {
-        const uint64_t now = ptx::globaltimer_ns();
-        if (t0 == 0) t0 = now;
-        if (*reinterpret_cast<volatile int*>(&sh->abort_flag)) {
-          give_up = 1;
-        } else if (now - t0 > a.timeout_ns) {
-          record_timeout(a, sh);
-          give_up = 1;
-        }
-      }
-      give_up = __shfl_sync(0xffffffffu, give_up, 0);
-      if (give_up) return false;
-    }
-  }
-}
 
 // ------------------------------------------------------- code -> bf16 pairs
 // Eight 4-bit codes (one 32-bit word, code k in nibble k) to four bf16x2
@@ -232,23 +278,30 @@ __device__ __forceinline__ uint32_t scale_pair(uint32_t q, uint32_t s_hi2, uint3
   return bf16x2_fma(q, s_hi2, lo);
 }
 
-__device__ __forceinline__ float bits_f32(uint32_t u) { return __uint_as_float(u); }
-
-template <int BA, int NWG, bool GRP, int STAGES>
+template <int BA, int NWG, bool GRP, int STAGES, int NACC>
 struct Cfg {
   static constexpr int kActBox = BA * 128;                        // bytes per 64-k box
   static constexpr int kStageRaw = 2 * kActBox + kWBytes + kSBytes;
   static constexpr int kStage = (kStageRaw + 1023) / 1024 * 1024;
-  static constexpr int kThreads = 64 + 128 * NWG;
-  static constexpr int kColsPerWg = BA / NWG;                     // D columns per worker WG
+  static constexpr int kThreads = 32 * kDequantWarp0 + 128 * NWG;   // 15 warps: <= 128 registers
   static constexpr int kDequantCols = kAStageCols / NWG;          // A-stage columns per WG
-  static constexpr int kChunk = kColsPerWg < 32 ? kColsPerWg : 32;
+  static constexpr int kWords = 16 / NWG;                         // code words per thread per unit
+  // Each accumulator buffer holds NACC partial accumulators of BA columns:
+  // k-step kk of a unit goes to partial kk % NACC, so NACC independent MMA
+  // dependency chains overlap in the tensor pipe (with a small N a single
+  // chain is bound by the MMA latency, not its throughput); the readout sums
+  // the partials.
+  static constexpr int kBufCols = BA * NACC;
+  static constexpr int kDB = (kDCols / kBufCols) < 4 ? (kDCols / kBufCols) : 4;
+  static constexpr int kChunk = BA < (GRP ? 16 : 32) ? BA : (GRP ? 16 : 32);
   static constexpr size_t kSmem = static_cast<size_t>(STAGES) * kStage + 1024 + sizeof(Shared);
   static constexpr uint32_t kTx = 2 * kActBox + kWBytes + kSBytes;
   static_assert(BA % 16 == 0 && BA >= 16 && BA <= 256, "tcgen05 N for M=128");
-  static_assert(GRP ? (2 * BA <= 256) : (BA <= 256), "accumulators fit in TMEM");
+  static_assert(kDB >= 1, "accumulators fit in TMEM");
+  static_assert(NACC == 1 || NACC == 2 || NACC == 4, "partial accumulators divide the 8 k-steps");
+  static_assert(!GRP || BA <= 64, "group mode keeps BA fp32 accumulators per thread");
   static_assert(STAGES <= 16, "barrier arrays");
-  static_assert(kColsPerWg >= 8, "at least 8 accumulator columns per worker warpgroup");
+  static_assert(NWG == 1 || NWG == 2, "dequant warpgroups");
 };
 
 template <int N>
@@ -263,8 +316,24 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t* r) {
   }
 }
 
-// Write `cnt` accumulator columns [col0, col0 + cnt) of this thread's weight
-// row either to Y (whole tile) or to this CTA's partial slot.
+// CNT accumulator columns of this thread's lane, summed over the NACC
+// partial accumulators (BA columns apart).
+template <int CNT, int NACC, int BA>
+__device__ __forceinline__ void load_partials(uint32_t taddr, float (&v)[CNT]) {
+  uint32_t r[CNT];
+  tmem_ld_cols<CNT>(taddr, r);
+#pragma unroll
+  for (int j = 0; j < CNT; ++j) v[j] = __uint_as_float(r[j]);
+#pragma unroll
+  for (int p = 1; p < NACC; ++p) {
+    tmem_ld_cols<CNT>(taddr + p * BA, r);
+#pragma unroll
+    for (int j = 0; j < CNT; ++j) v[j] += __uint_as_float(r[j]);
+  }
+}
+
+// Write accumulator columns [col0, col0 + CNT) of this thread's weight row
+// either to Y (whole tile) or to this CTA's partial slot.
 template <int BA, int CNT>
 __device__ __forceinline__ void emit_cols(const Args& a, const Unit& u, int row, int col0,
                                           const float (&v)[CNT], float bias_n) {
@@ -280,70 +349,90 @@ __device__ __forceinline__ void emit_cols(const Args& a, const Unit& u, int row,
       }
     }
   } else {
-    float* slot = a.ws + (static_cast<int64_t>(blockIdx.x) * 2 + u.slot) * (BA * kTileW);
+    // partial slot, row-major: this thread's row holds BA contiguous floats
+    float* slot = a.ws + (static_cast<int64_t>(blockIdx.x) * 2 + u.slot) * (BA * kTileW) +
+                  row * BA + col0;
 #pragma unroll
-    for (int j = 0; j < CNT; ++j) slot[(col0 + j) * kTileW + row] = v[j];
+    for (int j = 0; j < CNT; j += 4)
+      *reinterpret_cast<float4*>(slot + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
   }
 }
 
-// Barrier among the worker warps built on an mbarrier, so that a worker warp
-// that gave up after a timeout cannot leave the others blocked forever.
-__device__ bool worker_sync(Shared* sh, uint32_t& nsync, const Args& a) {
+// Barrier among the readout warps built on an mbarrier, so that a warp that
+// gave up after a timeout cannot leave the others blocked forever.
+__device__ bool readout_sync(Shared* sh, uint32_t& nsync, const WaitCtx& wc) {
   __syncwarp();
   if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(&sh->wsync);
-  const bool ok = wait_warp(&sh->wsync, nsync & 1, a, sh);
+  const bool ok = wait_warp(&sh->wsync, nsync & 1, wc);
   ++nsync;
   return ok;
 }
 
 // After this CTA wrote a partial tile: count the arrival; the CTA that
 // completes the count sums every partial of the tile in k order and stores Y.
-template <int BA, int NWG>
-__device__ bool stream_k_fixup(const Args& a, const Unit& u, Shared* sh, int row, int wg,
-                               uint32_t& nsync) {
-  constexpr int kCols = BA / NWG;
+template <int BA>
+__device__ bool stream_k_fixup(const Args& a, const Unit& u, Shared* sh, int row, float bias_n,
+                               uint32_t& nsync, const WaitCtx& wc) {
+  constexpr int kSub = BA < 16 ? BA : 16;   // columns summed together
   const int C = gridDim.x;
   __threadfence();
-  if (!worker_sync(sh, nsync, a)) return false;
+  if (!readout_sync(sh, nsync, wc)) return false;
   const int KB = a.KB;
   const int c_lo = sk_owner(u.sk_tile * KB, C, a.sk_units);
   const int c_hi = sk_owner(u.sk_tile * KB + KB - 1, C, a.sk_units);
-  if (threadIdx.x == 64) {
+  if (threadIdx.x == 32 * kReadoutWarp0) {
     const uint32_t old = atomicAdd(&a.counters[u.sk_tile], 1u);
     const bool last = (old == static_cast<uint32_t>(c_hi - c_lo));
     if (last) atomicExch(&a.counters[u.sk_tile], 0u);
     sh->fixup_last = last ? 1 : 0;
   }
-  if (!worker_sync(sh, nsync, a)) return false;
+  if (!readout_sync(sh, nsync, wc)) return false;
   if (!sh->fixup_last) return true;
   __threadfence();
   const int n0 = (u.tile % a.n_tiles) * kTileW;
   const int m0 = (u.tile / a.n_tiles) * BA;
   const int n = n0 + row;
-  const float bias_n = (a.bias != nullptr && n < a.N) ? __bfloat162float(a.bias[n]) : 0.0f;
-  const int col_begin = wg * kCols;
-  for (int j = 0; j < kCols; ++j) {
-    const int col = col_begin + j;
-    float acc = 0.0f;
+  const float* base = a.ws + row * BA;
+  for (int c0 = 0; c0 < BA; c0 += kSub) {
+    float acc[kSub];
+#pragma unroll
+    for (int j = 0; j < kSub; ++j) acc[j] = 0.0f;
+#pragma unroll 4
     for (int cc = c_lo; cc <= c_hi; ++cc) {
-      const int first_tile_of_cc =
-          static_cast<int>((static_cast<int64_t>(cc) * a.sk_units) / C) / KB;
-      const int slot = (u.sk_tile == first_tile_of_cc) ? 0 : 1;
-      const float* src = a.ws + (static_cast<int64_t>(cc) * 2 + slot) * (BA * kTileW);
-      acc += __ldcg(src + col * kTileW + row);
+      // slot 0 when the tile is the first stream-K tile of CTA cc, else 1
+      const int first_tile = static_cast<int>((static_cast<int64_t>(cc) * a.sk_units) / C) / KB;
+      const int slot = (u.sk_tile == first_tile) ? 0 : 1;
+      const float4* src = reinterpret_cast<const float4*>(
+          base + (static_cast<int64_t>(cc) * 2 + slot) * (BA * kTileW) + c0);
+      float4 v[kSub / 4];
+#pragma unroll
+      for (int j = 0; j < kSub / 4; ++j) v[j] = __ldcg(src + j);
+#pragma unroll
+      for (int j = 0; j < kSub / 4; ++j) {
+        acc[4 * j] += v[j].x;
+        acc[4 * j + 1] += v[j].y;
+        acc[4 * j + 2] += v[j].z;
+        acc[4 * j + 3] += v[j].w;
+      }
     }
-    const int m = m0 + col;
-    if (n < a.N && m < a.M) a.Y[static_cast<int64_t>(m) * a.N + n] = __float2bfloat16_rn(acc + bias_n);
+    if (n < a.N) {
+#pragma unroll
+      for (int j = 0; j < kSub; ++j) {
+        const int m = m0 + c0 + j;
+        if (m < a.M) a.Y[static_cast<int64_t>(m) * a.N + n] = __float2bfloat16_rn(acc[j] + bias_n);
+      }
+    }
   }
   return true;
 }
 
-template <int BA, int NWG, bool GRP, int STAGES>
-__global__ void __launch_bounds__(Cfg<BA, NWG, GRP, STAGES>::kThreads, 1)
+template <int BA, int NWG, bool GRP, int STAGES, int NACC>
+__global__ void __launch_bounds__(Cfg<BA, NWG, GRP, STAGES, NACC>::kThreads, 1)
     w4a16_gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_act,
                          const __grid_constant__ CUtensorMap tm_w,
                          const __grid_constant__ CUtensorMap tm_s, const Args a) {
-  using C = Cfg<BA, NWG, GRP, STAGES>;
+  using C = Cfg<BA, NWG, GRP, STAGES, NACC>;
+  constexpr int DB = C::kDB;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -360,21 +449,33 @@ __global__ void __launch_bounds__(Cfg<BA, NWG, GRP, STAGES>::kThreads, 1)
   };
 
   // ---------------------------------------------------------------- set-up
+#ifdef W4A16_TRACE
+  unsigned long long* const trace_cta = g_trace;
+  unsigned long long* const trace_unit = blockIdx.x == 0 ? g_trace_units : nullptr;
+#endif
+  // Barriers.  full[s]: a stage's copies landed.  unit_done[i % R]: all MMAs
+  // of unit i completed (one tcgen05.commit per unit); it frees the TMEM
+  // weight stage of unit i, tells the group-mode readout that the unit's
+  // partial sum is ready, and (dequant mode) frees the shared-memory stage.
+  // empty[s] (group mode): the readout has read the stage's scales, the last
+  // use of the stage.  afull: the weight operand is in TMEM.  dempty: the
+  // readout drained an accumulator buffer.  dfull (dequant mode): a run on a
+  // tile is fully accumulated.
+  constexpr int R = STAGES > kAStages ? STAGES : kAStages;
+  if (threadIdx.x == 0) W4A16_TRACE_POINT(0);
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       ptx::mbar_init(&sh->full[s], 1);
-      ptx::mbar_init(&sh->empty[s], 1);
+      ptx::mbar_init(&sh->empty[s], 4);
     }
-    for (int s = 0; s < kAStages; ++s) {
-      ptx::mbar_init(&sh->afull[s], 4 * NWG);
-      ptx::mbar_init(&sh->aempty[s], 1);
-    }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < R; ++s) ptx::mbar_init(&sh->unit_done[s], 1);
+    for (int s = 0; s < kAStages; ++s) ptx::mbar_init(&sh->afull[s], 4 * NWG);
+    for (int s = 0; s < DB; ++s) {
       ptx::mbar_init(&sh->dfull[s], 1);
-      ptx::mbar_init(&sh->dempty[s], 4 * NWG);
+      ptx::mbar_init(&sh->dempty[s], 4);
     }
     ptx::mbar_init(&sh->mma_done, 1);
-    ptx::mbar_init(&sh->wsync, 4 * NWG);
+    ptx::mbar_init(&sh->wsync, 4);
     sh->abort_flag = 0;
     sh->fixup_last = 0;
     ptx::fence_mbar_init();
@@ -390,36 +491,55 @@ __global__ void __launch_bounds__(Cfg<BA, NWG, GRP, STAGES>::kThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = sh->tmem_base;
+  const WaitCtx wc{a.err, a.timeout_ns, &sh->abort_flag};
 
+  if (threadIdx.x == 0) W4A16_TRACE_POINT(1);
   // Inputs may be produced by the previous kernel on the stream.
   ptx::grid_dependency_wait();
   ptx::grid_launch_dependents();
+  if (threadIdx.x == 0) W4A16_TRACE_POINT(2);
 
   Sched sched;
   sched.init(a);
+  UnitIter it;
+  it.init(sched);
+  const int total = sched.total;
 
-  if (warp == 0) {
-    // ------------------------------------------------------ TMA producer
+  if (warp == 0 || warp == 2) {
+    // ----------------------------------------------------- TMA producers
     if (lane == 0) {
-      int issued = 0;
-      for (int i = 0; i < sched.total; ++i) {
+      const int mine = warp == 0 ? 0 : 1;
+      int issued = -1;
+      for (int i = 0; i < total; ++i) {
+        const Unit u = it.next();
+        if ((i & 1) != mine) continue;
         const int stage = i % STAGES;
-        const uint32_t ph = (i / STAGES) & 1;
-        if (!wait_one(&sh->empty[stage], ph ^ 1, a, sh)) break;
-        const Unit u = sched.get(i);
-        const int n0 = (u.tile % a.n_tiles) * kTileW;
+        if (i >= STAGES) {
+          const int j = i - STAGES;   // the unit that last used this stage
+          const bool ok = GRP ? wait_one(&sh->empty[stage], (j / STAGES) & 1, wc)
+                              : wait_one(&sh->unit_done[j % R], (j / R) & 1, wc);
+          if (!ok) break;
+        }
         const int m0 = (u.tile / a.n_tiles) * BA;
         ptx::mbar_arrive_expect_tx(&sh->full[stage], C::kTx);
-        ptx::tma_load_2d(act_box(stage, 0), &tm_act, &sh->full[stage], u.kb * kUnitK, m0);
-        ptx::tma_load_2d(act_box(stage, 1), &tm_act, &sh->full[stage], u.kb * kUnitK + 64, m0);
-        ptx::tma_load_2d(w_tile(stage), &tm_w, &sh->full[stage], u.kb * (kUnitK / 2), n0);
-        ptx::tma_load_2d(s_tile(stage), &tm_s, &sh->full[stage], n0, u.kb);
-        issued = i + 1;
+        if (a.act_3d) {
+          ptx::tma_load_3d(act_box(stage, 0), &tm_act, &sh->full[stage], 0, m0, u.kb * 2);
+        } else {
+          ptx::tma_load_2d(act_box(stage, 0), &tm_act, &sh->full[stage], u.kb * kUnitK, m0);
+          ptx::tma_load_2d(act_box(stage, 1), &tm_act, &sh->full[stage], u.kb * kUnitK + 64, m0);
+        }
+        // the unit's codes: one contiguous 8 KiB tile of the tiled storage
+        ptx::tma_load_2d(w_tile(stage), &tm_w, &sh->full[stage], 0,
+                         ((u.tile % a.n_tiles) * a.KB + u.kb) * kTileW);
+        ptx::tma_load_2d(s_tile(stage), &tm_s, &sh->full[stage], (u.tile % a.n_tiles) * kTileW,
+                         u.kb);
+        if (i <= 1) W4A16_TRACE_POINT(3);
+        W4A16_TRACE_UNIT(0, i);
+        issued = i;
       }
       if (*reinterpret_cast<volatile int*>(&sh->abort_flag)) {
-        // let the copies still in flight land before the CTA exits
-        const int first = issued > STAGES ? issued - STAGES : 0;
-        for (int i = first; i < issued; ++i) {
+        // let this producer's copies still in flight land before the CTA exits
+        for (int i = issued; i >= 0 && i > issued - STAGES; i -= 2) {
           const uint64_t t0 = ptx::globaltimer_ns();
           while (!ptx::mbar_try_wait(&sh->full[i % STAGES], (i / STAGES) & 1)) {
             if (ptx::globaltimer_ns() - t0 > a.timeout_ns) break;
@@ -431,130 +551,144 @@ __global__ void __launch_bounds__(Cfg<BA, NWG, GRP, STAGES>::kThreads, 1)
     // -------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = ptx::idesc_bf16_f32(kTileW, BA);
+      const uint32_t smem0 = ptx::smem_u32(smem);
       int seg = 0;
-      for (int i = 0; i < sched.total; ++i) {
+      int db = 0;
+      for (int i = 0; i < total; ++i) {
+        const Unit u = it.next();
         const int stage = i % STAGES;
         const int as = i % kAStages;
-        const Unit u = sched.get(i);
-        if (!wait_one(&sh->full[stage], (i / STAGES) & 1, a, sh)) break;
-        if (!wait_one(&sh->afull[as], (i / kAStages) & 1, a, sh)) break;
-        int db = 0;
+        W4A16_TRACE_UNIT(8, i);
+        if (!wait_one(&sh->full[stage], (i / STAGES) & 1, wc)) break;
+        W4A16_TRACE_UNIT(9, i);
+        if (!wait_one(&sh->afull[as], (i / kAStages) & 1, wc)) break;
+        W4A16_TRACE_UNIT(10, i);
         bool fresh;
-        if (GRP) {
-          db = i & 1;
-          if (!wait_one(&sh->dempty[db], ((i >> 1) & 1) ^ 1, a, sh)) break;
+        if constexpr (GRP) {
+          db = i % DB;
+          if (i >= DB && !wait_one(&sh->dempty[db], ((i / DB) - 1) & 1, wc)) break;
           fresh = true;
         } else {
           fresh = u.seg_first;
-          if (u.seg_first && !wait_one(&sh->dempty[0], (seg & 1) ^ 1, a, sh)) break;
+          if (u.seg_first) {
+            db = seg % DB;
+            if (seg >= DB && !wait_one(&sh->dempty[db], ((seg / DB) - 1) & 1, wc)) break;
+          }
         }
         ptx::tc_fence_after();
-        const uint32_t d_tmem = tmem + kDCol + db * BA;
+        if (i == 0) W4A16_TRACE_POINT(4);
+        if (i == total - 1) W4A16_TRACE_POINT(5);
+        W4A16_TRACE_UNIT(4, i);
+        const uint32_t d_tmem = tmem + kDCol + db * C::kBufCols;
         const uint32_t a_tmem = tmem + as * kAStageCols;
-        const uint32_t b0 = ptx::smem_u32(act_box(stage, 0));
-        const uint32_t b1 = ptx::smem_u32(act_box(stage, 1));
+        const uint32_t b0 = smem0 + stage * C::kStage;
 #pragma unroll
         for (int kk = 0; kk < kUnitK / 16; ++kk) {
-          const uint32_t baddr = (kk < 4 ? b0 : b1) + (kk & 3) * 32;
-          ptx::mma_bf16_tmem_a(d_tmem, a_tmem + kk * 8, ptx::smem_desc_sw128(baddr), idesc,
-                               (kk > 0 || !fresh) ? 1u : 0u);
+          const uint32_t baddr = b0 + (kk >> 2) * C::kActBox + (kk & 3) * 32;
+          ptx::mma_bf16_tmem_a(d_tmem + (kk % NACC) * BA, a_tmem + kk * 8,
+                               ptx::smem_desc_sw128(baddr), idesc,
+                               (kk >= NACC || !fresh) ? 1u : 0u);
         }
-        ptx::mma_commit(&sh->empty[stage]);
-        ptx::mma_commit(&sh->aempty[as]);
-        if (GRP) {
-          ptx::mma_commit(&sh->dfull[db]);
-        } else if (u.seg_last) {
-          ptx::mma_commit(&sh->dfull[0]);
-          ++seg;
+        W4A16_TRACE_UNIT(11, i);
+        ptx::mma_commit(&sh->unit_done[i % R]);
+        if constexpr (!GRP) {
+          if (u.seg_last) {
+            ptx::mma_commit(&sh->dfull[db]);
+            ++seg;
+          }
         }
+        W4A16_TRACE_UNIT(5, i);
       }
       // all MMAs of this CTA complete before TMEM is freed
       ptx::mma_commit(&sh->mma_done);
       const uint64_t t0 = ptx::globaltimer_ns();
       while (!ptx::mbar_try_wait(&sh->mma_done, 0)) {
         if (ptx::globaltimer_ns() - t0 > a.timeout_ns) {
-          record_timeout(a, sh);
+          wait_record_timeout(wc);
           break;
         }
       }
     }
-  } else {
-    // ------------------------------------------------------------ workers
-    const int wg = (warp - 2) >> 2;
+  } else if (warp < kDequantWarp0) {
+    // ------------------------------------------------------------ readout
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    constexpr int kWords = 16 / NWG;                 // 32-bit code words per thread per unit
-    constexpr int kCols = C::kColsPerWg;
-
-    float acc[GRP ? kCols : 1];
-    struct Pending {
-      bool valid;
-      Unit u;
-      int i;
-      int seg;
-      float scale;
-    } pend;
-    pend.valid = false;
-    int seg = 0;
     uint32_t nsync = 0;
-    bool ok = true;
-
-    // D -> acc (group mode) or D -> output (dequant mode) for a finished unit.
-    auto finish = [&](const Pending& p) -> bool {
-      const int n = (p.u.tile % a.n_tiles) * kTileW + row;
-      const float bias_n =
-          (a.bias != nullptr && n < a.N) ? __bfloat162float(a.bias[n]) : 0.0f;
+    float acc[GRP ? BA : 1];
+    float bias_n = 0.0f;
+    int seg = 0;
+    for (int i = 0; i < total; ++i) {
+      const Unit u = it.next();
+      const int n = (u.tile % a.n_tiles) * kTileW + row;
+      if (u.seg_first)
+        bias_n = (a.bias != nullptr && n < a.N) ? __bfloat162float(a.bias[n]) : 0.0f;
       if constexpr (GRP) {
-        const int db = p.i & 1;
-        if (!wait_warp(&sh->dfull[db], (p.i >> 1) & 1, a, sh)) return false;
+        const int stage = i % STAGES;
+        const int db = i % DB;
+        // the unit's MMAs are complete: its partial sum is in TMEM and the
+        // stage's other contents are consumed; the scales are read last
+        if (!wait_warp(&sh->unit_done[i % R], (i / R) & 1, wc)) break;
+        if (!wait_warp(&sh->full[stage], (i / STAGES) & 1, wc)) break;
+        if (threadIdx.x == 32 * kReadoutWarp0 && i == 0) W4A16_TRACE_POINT(8);
+        if (threadIdx.x == 32 * kReadoutWarp0 && i == total - 1) W4A16_TRACE_POINT(9);
+        if (threadIdx.x == 32 * kReadoutWarp0) W4A16_TRACE_UNIT(6, i);
+        const float scale = __half2float(s_tile(stage)[row]);
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&sh->empty[stage]);
         ptx::tc_fence_after();
 #pragma unroll
-        for (int c0 = 0; c0 < kCols; c0 += C::kChunk) {
-          uint32_t r[C::kChunk];
-          tmem_ld_cols<C::kChunk>(lane_base + kDCol + db * BA + wg * kCols + c0, r);
+        for (int c0 = 0; c0 < BA; c0 += C::kChunk) {
+          float d[C::kChunk];
+          load_partials<C::kChunk, NACC, BA>(lane_base + kDCol + db * C::kBufCols + c0, d);
 #pragma unroll
-          for (int j = 0; j < C::kChunk; ++j) {
-            const float d = bits_f32(r[j]);
-            acc[c0 + j] = p.u.seg_first ? p.scale * d : fmaf(p.scale, d, acc[c0 + j]);
-          }
+          for (int j = 0; j < C::kChunk; ++j)
+            acc[c0 + j] = u.seg_first ? scale * d[j] : fmaf(scale, d[j], acc[c0 + j]);
         }
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&sh->dempty[db]);
-        if (p.u.seg_last) {
-          emit_cols<BA, kCols>(a, p.u, row, wg * kCols, acc, bias_n);
-          if (!p.u.whole && !stream_k_fixup<BA, NWG>(a, p.u, sh, row, wg, nsync)) return false;
+        if (threadIdx.x == 32 * kReadoutWarp0) W4A16_TRACE_UNIT(7, i);
+        if (u.seg_last) {
+          emit_cols<BA, BA>(a, u, row, 0, acc, bias_n);
+          if (!u.whole && !stream_k_fixup<BA>(a, u, sh, row, bias_n, nsync, wc)) break;
         }
       } else {
-        if (!wait_warp(&sh->dfull[0], p.seg & 1, a, sh)) return false;
+        if (!u.seg_last) continue;
+        const int db = seg % DB;
+        if (!wait_warp(&sh->dfull[db], (seg / DB) & 1, wc)) break;
+        ++seg;
         ptx::tc_fence_after();
 #pragma unroll 1
-        for (int c0 = 0; c0 < kCols; c0 += C::kChunk) {
-          uint32_t r[C::kChunk];
+        for (int c0 = 0; c0 < BA; c0 += C::kChunk) {
           float v[C::kChunk];
-          tmem_ld_cols<C::kChunk>(lane_base + kDCol + wg * kCols + c0, r);
-#pragma unroll
-          for (int j = 0; j < C::kChunk; ++j) v[j] = bits_f32(r[j]);
-          emit_cols<BA, C::kChunk>(a, p.u, row, wg * kCols + c0, v, bias_n);
+          load_partials<C::kChunk, NACC, BA>(lane_base + kDCol + db * C::kBufCols + c0, v);
+          emit_cols<BA, C::kChunk>(a, u, row, c0, v, bias_n);
         }
         ptx::tc_fence_before();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&sh->dempty[0]);
-        if (!p.u.whole && !stream_k_fixup<BA, NWG>(a, p.u, sh, row, wg, nsync)) return false;
+        if (lane == 0) ptx::mbar_arrive(&sh->dempty[db]);
+        if (!u.whole && !stream_k_fixup<BA>(a, u, sh, row, bias_n, nsync, wc)) break;
       }
-      return true;
-    };
-
-    for (int i = 0; i < sched.total && ok; ++i) {
+    }
+  } else {
+    // ------------------------------------------------------------ dequant
+    const int wg = (warp - kDequantWarp0) >> 2;
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    constexpr int kWords = C::kWords;
+    const uint32_t wrow0 = ptx::smem_u32(w_tile(0)) + row * 64;
+    for (int i = 0; i < total; ++i) {
       const int stage = i % STAGES;
       const int as = i % kAStages;
-      const Unit u = sched.get(i);
-      if (!wait_warp(&sh->full[stage], (i / STAGES) & 1, a, sh)) { ok = false; break; }
+      if (!wait_warp(&sh->full[stage], (i / STAGES) & 1, wc)) break;
+      if (i == 0 && threadIdx.x == 32 * kDequantWarp0) W4A16_TRACE_POINT(6);
+      if (threadIdx.x == 32 * kDequantWarp0) W4A16_TRACE_UNIT(1, i);
 
-      // this thread's 64 B of packed codes, stored with the 64-byte swizzle:
-      // 16-byte chunk c of row r sits at chunk position c ^ ((r >> 1) & 3)
-      const uint32_t wrow = ptx::smem_u32(w_tile(stage)) + row * 64;
+      // this thread's share of its row's 64 B of packed codes, stored with the
+      // 64-byte swizzle: 16-byte chunk c of row r sits at c ^ ((r >> 1) & 3)
+      const uint32_t wrow = wrow0 + stage * C::kStage;
       uint32_t words[kWords];
 #pragma unroll
       for (int q = 0; q < kWords / 4; ++q) {
@@ -565,12 +699,11 @@ __global__ void __launch_bounds__(Cfg<BA, NWG, GRP, STAGES>::kThreads, 1)
         words[4 * q + 2] = v.z;
         words[4 * q + 3] = v.w;
       }
-      const float scale = __half2float(s_tile(stage)[row]);
-
       uint32_t opnd[4 * kWords];
 #pragma unroll
       for (int q = 0; q < kWords; ++q) codes_to_bf16(words[q], &opnd[4 * q]);
       if constexpr (!GRP) {
+        const float scale = __half2float(s_tile(stage)[row]);
         const __nv_bfloat16 hi = __float2bfloat16_rn(scale);
         const float lo_f = scale - __bfloat162float(hi);        // exact
         const __nv_bfloat16 lo = __float2bfloat16_rn(lo_f);     // exact
@@ -582,7 +715,12 @@ __global__ void __launch_bounds__(Cfg<BA, NWG, GRP, STAGES>::kThreads, 1)
         for (int q = 0; q < 4 * kWords; ++q) opnd[q] = scale_pair(opnd[q], s_hi2, s_lo2);
       }
 
-      if (!wait_warp(&sh->aempty[as], ((i / kAStages) & 1) ^ 1, a, sh)) { ok = false; break; }
+      // the TMEM stage is free once the MMAs of the unit that used it completed
+      if (i >= kAStages) {
+        const int j = i - kAStages;
+        if (!wait_warp(&sh->unit_done[j % R], (j / R) & 1, wc)) break;
+      }
+      if (threadIdx.x == 32 * kDequantWarp0) W4A16_TRACE_UNIT(2, i);
       ptx::tc_fence_after();
       const uint32_t a_addr = lane_base + as * kAStageCols + wg * C::kDequantCols;
 #pragma unroll
@@ -591,51 +729,39 @@ __global__ void __launch_bounds__(Cfg<BA, NWG, GRP, STAGES>::kThreads, 1)
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&sh->afull[as]);
-
-      if (pend.valid) {
-        if (!finish(pend)) { ok = false; break; }
-        pend.valid = false;
-      }
-      if (GRP || u.seg_last) {
-        pend.valid = true;
-        pend.u = u;
-        pend.i = i;
-        pend.seg = seg;
-        pend.scale = scale;
-      }
-      if (!GRP && u.seg_last) ++seg;
+      if (threadIdx.x == 32 * kDequantWarp0) W4A16_TRACE_UNIT(3, i);
+      if (i == total - 1 && threadIdx.x == 32 * kDequantWarp0) W4A16_TRACE_POINT(7);
     }
-    if (ok && pend.valid) finish(pend);
   }
 
   // ------------------------------------------------------------- teardown
+  if (threadIdx.x == 32 * kReadoutWarp0) W4A16_TRACE_POINT(10);
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
   if (warp == 1) ptx::tmem_dealloc(tmem, kTmemCols);
+  if (threadIdx.x == 32) W4A16_TRACE_POINT(11);
 }
 
 // One-thread kernel whose wait can never complete: exercises the bounded
 // wait and the error word without faulting or hanging the GPU.
 __global__ void wait_timeout_selftest_kernel(uint32_t* err, uint64_t timeout_ns) {
   __shared__ uint64_t bar;
-  __shared__ Shared sh;
+  __shared__ int abort_flag;
   if (threadIdx.x == 0) {
     ptx::mbar_init(&bar, 1);
     ptx::fence_mbar_init();
-    sh.abort_flag = 0;
-    Args a{};
-    a.err = err;
-    a.timeout_ns = timeout_ns;
-    (void)wait_one(&bar, 0, a, &sh);   // nobody arrives: times out
+    abort_flag = 0;
+    const WaitCtx wc{err, timeout_ns, &abort_flag};
+    (void)wait_one(&bar, 0, wc);   // nobody arrives: times out
   }
 }
 
-template <int BA, int NWG, bool GRP, int STAGES>
+template <int BA, int NWG, bool GRP, int STAGES, int NACC>
 cudaError_t launch_instance(const GemmSchedule& s, const GemmProblem& p, bool use_pdl,
                             cudaStream_t stream) {
-  using C = Cfg<BA, NWG, GRP, STAGES>;
-  auto kernel = w4a16_gemm_tc_kernel<BA, NWG, GRP, STAGES>;
+  using C = Cfg<BA, NWG, GRP, STAGES, NACC>;
+  auto kernel = w4a16_gemm_tc_kernel<BA, NWG, GRP, STAGES, NACC>;
 
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -650,11 +776,21 @@ cudaError_t launch_instance(const GemmSchedule& s, const GemmProblem& p, bool us
   }
 
   CUtensorMap tm_act, tm_w, tm_s;
-  if (encode_tmap_2d(&tm_act, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.A, p.K, p.M, p.K * 2, 64, BA,
-                     CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
-    return cudaErrorInvalidValue;
-  if (encode_tmap_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.packed, p.K / 2, p.N, p.K / 2, 64,
-                     kTileW, CU_TENSOR_MAP_SWIZZLE_64B) != CUDA_SUCCESS)
+  // Activations as [K/64][M][64]: one box {64, BA, 2} brings both 64-wide K
+  // halves of a unit, in the same shared-memory order as two 2-D boxes.
+  int act_3d = 1;
+  if (encode_tmap_3d(&tm_act, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.A, 64, p.M, p.K / 64, p.K * 2, 128,
+                     64, BA, 2, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS) {
+    act_3d = 0;
+    if (encode_tmap_2d(&tm_act, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.A, p.K, p.M, p.K * 2, 64, BA,
+                       CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  // tiled code storage viewed as rows of 64 bytes: tile (tn, g) is rows
+  // (tn * K/128 + g) * 128 .. + 127
+  const uint64_t w_rows = static_cast<uint64_t>((p.N + kTileW - 1) / kTileW) * (p.K / kUnitK) * kTileW;
+  if (encode_tmap_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.packed, 64, w_rows, 64, 64, kTileW,
+                     CU_TENSOR_MAP_SWIZZLE_64B) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
   if (encode_tmap_2d(&tm_s, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.scales, p.N, p.K / kGroup, p.N * 2,
                      kTileW, 1, CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
@@ -668,12 +804,11 @@ cudaError_t launch_instance(const GemmSchedule& s, const GemmProblem& p, bool us
   a.n_tiles = static_cast<int>((p.N + kTileW - 1) / kTileW);
   a.dp_tiles = s.dp_tiles;
   a.sk_units = static_cast<int>(s.sk_units);
+  a.act_3d = act_3d;
   a.bias = static_cast<const __nv_bfloat16*>(p.bias);
   a.Y = static_cast<__nv_bfloat16*>(p.Y);
-  a.ws = static_cast<float*>(p.workspace);
-  a.counters = reinterpret_cast<uint32_t*>(
-      static_cast<uint8_t*>(p.workspace) +
-      static_cast<size_t>(s.grid) * 2 * BA * kTileW * sizeof(float));
+  a.counters = static_cast<uint32_t*>(p.workspace);
+  a.ws = reinterpret_cast<float*>(static_cast<uint8_t*>(p.workspace) + kCounterBytes);
   a.err = p.error_word;
   a.timeout_ns = p.timeout_ns;
 
@@ -690,22 +825,23 @@ cudaError_t launch_instance(const GemmSchedule& s, const GemmProblem& p, bool us
   return cudaLaunchKernelEx(&cfg, kernel, tm_act, tm_w, tm_s, a);
 }
 
-// The compiled configurations: {act_tile, worker_wgs, group_scale, stages}.
+// The compiled configurations:
+//   {act_tile, dequant_wgs, group_scale, stages, partial accumulators}.
 #define W4A16_GEMM_INSTANCES(X) \
-  X(16, 2, true, 16)            \
-  X(32, 2, true, 12)            \
-  X(64, 2, true, 8)             \
-  X(64, 2, false, 8)            \
-  X(128, 2, true, 5)            \
-  X(128, 2, false, 5)           \
-  X(256, 2, false, 3)
+  X(16, 2, true, 16, 1)         \
+  X(32, 2, true, 12, 1)         \
+  X(64, 2, true, 8, 1)          \
+  X(64, 2, false, 8, 1)         \
+  X(128, 2, false, 5, 1)        \
+  X(256, 2, false, 3, 1)
 
 }  // namespace
 
 size_t gemm_smem_bytes(const GemmKernelConfig& c) {
-#define W4A16_SMEM_CASE(BA, NWG, GRP, ST)                                                      \
-  if (c.act_tile == BA && c.worker_wgs == NWG && c.group_scale == GRP && c.stages == ST) \
-    return Cfg<BA, NWG, GRP, ST>::kSmem;
+#define W4A16_SMEM_CASE(BA, NWG, GRP, ST, NA)                                            \
+  if (c.act_tile == BA && c.worker_wgs == NWG && c.group_scale == GRP && c.stages == ST && \
+      c.accumulators == NA)                                                                \
+    return Cfg<BA, NWG, GRP, ST, NA>::kSmem;
   W4A16_GEMM_INSTANCES(W4A16_SMEM_CASE)
 #undef W4A16_SMEM_CASE
   return 0;
@@ -715,29 +851,40 @@ bool gemm_config_available(const GemmKernelConfig& c) { return gemm_smem_bytes(c
 
 size_t gemm_workspace_bytes(const GemmKernelConfig& c, const GemmSchedule& s, int64_t M,
                             int64_t N, int64_t K) {
+  (void)M;
+  (void)N;
   (void)K;
   if (s.sk_units == 0) return 0;
-  const int64_t tiles = gemm_tiles(c, M, N);
-  const int64_t sk_tiles = tiles - s.dp_tiles;
-  const size_t slots = static_cast<size_t>(s.grid) * 2 * c.act_tile * kTileW * sizeof(float);
-  const size_t counters = static_cast<size_t>(sk_tiles) * sizeof(uint32_t);
-  return slots + ((counters + 255) / 256) * 256;
+  return kCounterBytes + static_cast<size_t>(s.grid) * 2 * c.act_tile * kTileW * sizeof(float);
 }
 
 cudaError_t launch_gemm_tc(const GemmKernelConfig& c, const GemmSchedule& s,
                            const GemmProblem& p, bool use_pdl, cudaStream_t stream) {
-#define W4A16_LAUNCH_CASE(BA, NWG, GRP, ST)                                                    \
-  if (c.act_tile == BA && c.worker_wgs == NWG && c.group_scale == GRP && c.stages == ST) \
-    return launch_instance<BA, NWG, GRP, ST>(s, p, use_pdl, stream);
+#define W4A16_LAUNCH_CASE(BA, NWG, GRP, ST, NA)                                          \
+  if (c.act_tile == BA && c.worker_wgs == NWG && c.group_scale == GRP && c.stages == ST && \
+      c.accumulators == NA)                                                                \
+    return launch_instance<BA, NWG, GRP, ST, NA>(s, p, use_pdl, stream);
   W4A16_GEMM_INSTANCES(W4A16_LAUNCH_CASE)
 #undef W4A16_LAUNCH_CASE
   return cudaErrorInvalidConfiguration;
 }
 
+#ifdef W4A16_TRACE
+extern "C" int w4a16_debug_set_trace(unsigned long long* buf) {
+  return cudaMemcpyToSymbol(g_trace, &buf, sizeof(buf)) == cudaSuccess ? 0 : 1;
+}
+extern "C" int w4a16_debug_set_trace_units(unsigned long long* buf) {
+  return cudaMemcpyToSymbol(g_trace_units, &buf, sizeof(buf)) == cudaSuccess ? 0 : 1;
+}
+#endif
+
 cudaError_t launch_wait_timeout_selftest(uint32_t* error_word, uint64_t timeout_ns,
                                          cudaStream_t stream) {
-  wait_timeout_selftest_kernel<<<1, 32, 0, stream>>>(error_word, timeout_ns);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(32);
+  cfg.stream = stream;
+  return cudaLaunchKernelEx(&cfg, wait_timeout_selftest_kernel, error_word, timeout_ns);
 }
 
 }  // namespace w4a16

@@ -14,15 +14,17 @@ constexpr int kTileW = 128;     // weight rows per GEMM tile (tcgen05 M)
 
 // RTN quantize/pack; one launch.
 cudaError_t launch_rtn_quantize(const void* W, int64_t N, int64_t K, void* packed, void* scales,
-                                int num_sms, cudaStream_t stream);
+                                int num_sms, uint32_t* error_word, uint64_t timeout_ns,
+                                cudaStream_t stream);
 
 // One configuration of the tcgen05 GEMM kernel.
 struct GemmKernelConfig {
   int act_tile;      // activation rows per tile (tcgen05 N): 16..256
-  int worker_wgs;    // dequant/epilogue warpgroups: 1 or 2
+  int worker_wgs;    // dequant warpgroups: 1 or 2
   bool group_scale;  // true: per-group fp32 scaling of integer-code partial sums
                      // false: weights dequantized to bf16(q*s) before the MMA
   int stages;        // shared-memory pipeline depth
+  int accumulators;  // partial accumulators per buffer (independent MMA chains)
 };
 
 // The schedule of one launch.
@@ -51,8 +53,12 @@ inline int64_t gemm_tiles(const GemmKernelConfig& c, int64_t M, int64_t N) {
   return ((N + kTileW - 1) / kTileW) * ((M + c.act_tile - 1) / c.act_tile);
 }
 
-// Workspace layout: [grid][2][act_tile][128] fp32 partial slots, then one
-// uint32 arrival counter per stream-K tile.
+// Workspace layout: kCounterBytes of uint32 arrival counters (one per
+// stream-K tile; there are never more stream-K tiles than CTAs, so the
+// region has a fixed size and every variant finds its counters at the same
+// place), then [grid][2][act_tile][128] fp32 partial slots.
+constexpr size_t kCounterBytes = 4096;
+constexpr int kMaxGrid = static_cast<int>(kCounterBytes / 4);
 size_t gemm_workspace_bytes(const GemmKernelConfig& c, const GemmSchedule& s, int64_t M,
                             int64_t N, int64_t K);
 
@@ -74,5 +80,9 @@ cudaError_t launch_wait_timeout_selftest(uint32_t* error_word, uint64_t timeout_
 CUresult encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
                         uint64_t inner, uint64_t outer, uint64_t outer_stride_bytes,
                         uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle);
+CUresult encode_tmap_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                        uint64_t d0, uint64_t d1, uint64_t d2, uint64_t stride1_bytes,
+                        uint64_t stride2_bytes, uint32_t box0, uint32_t box1, uint32_t box2,
+                        CUtensorMapSwizzle swizzle);
 
 }  // namespace w4a16
