@@ -206,6 +206,31 @@ uint64_t w4a16_launch_count(void);
  * per-thread last error when it reports such a failure. */
 const char* w4a16_last_error_detail(void);
 
+/*
+ * W4A16 GEMM without a caller-provided workspace.  The paper has no
+ * counterpart: this is an addition for callers that cannot allocate device
+ * memory themselves, e.g. code whose device memory is owned by another
+ * allocator (a framework's caching pool or a fixed arena, where an extra
+ * cudaMalloc would bypass its accounting), real-time control loops that
+ * forbid allocation after start-up (cudaMalloc can synchronise the device and
+ * has unbounded latency), or C callers with no workspace management.
+ * Same operation and argument contract as w4a16_gemm.  The split-K scratch
+ * is a 16 MiB array in static device storage of this library; every GPU that
+ * loads the library holds it until the process exits.  A shape whose variant
+ * needs more scratch than that returns W4A16_ERR_WORKSPACE (the reason is in
+ * w4a16_last_error_detail) before anything is launched.  The first call on a
+ * device looks up the array's device address (cudaGetSymbolAddress); make
+ * that first call before any stream capture on that device.  Each call
+ * clears the scratch's arrival counters with a cudaMemsetAsync on `stream`,
+ * then launches the GEMM; it calls no cudaMalloc, cudaFree or other
+ * allocating routine.  All calls on one device share that device's array, so
+ * calls that can overlap on the GPU (for example on two streams) race: the
+ * caller must serialise them.
+ */
+int w4a16_gemm_noalloc(const void* A_bf16, int64_t M, int64_t N, int64_t K, const void* packed,
+                       const void* scales, int group, const void* bias_bf16_or_null, void* Y_bf16,
+                       void* stream);
+
 #ifdef __cplusplus
 }
 #endif

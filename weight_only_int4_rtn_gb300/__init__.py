@@ -59,6 +59,8 @@ SIGNATURES = [
     ("w4a16_selftest_wait_timeout", ctypes.c_int, [ctypes.c_uint64, _vp]),
     ("w4a16_launch_count", ctypes.c_uint64, []),
     ("w4a16_last_error_detail", ctypes.c_char_p, []),
+    ("w4a16_gemm_noalloc", ctypes.c_int,
+     [_vp, _c_int64, _c_int64, _c_int64, _vp, _vp, ctypes.c_int, _vp, _vp, _vp]),
 ]
 
 _lib = None

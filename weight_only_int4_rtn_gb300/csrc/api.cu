@@ -323,6 +323,40 @@ CUresult encode_tmap_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void*
 
 }  // namespace w4a16
 
+namespace w4a16 {
+namespace {
+
+// Scratch for w4a16_gemm_noalloc: a file-scope device array, so that callers
+// that must not allocate device memory can still run the stream-K GEMM.  Every
+// GPU that loads this library holds it until the process exits.
+constexpr size_t kNoAllocScratchBytes = 16u << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device.  In host code
+// the array's name is only a host-side stand-in, so the address is looked up
+// with cudaGetSymbolAddress, once per device, with that device current.
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  const cudaError_t e0 = cudaGetDevice(&dev);
+  if (e0 != cudaSuccess) return cuda_failure(e0, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return W4A16_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_failure(e, "cudaGetSymbolAddress(noalloc scratch)");
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return W4A16_OK;
+}
+
+}  // namespace
+}  // namespace w4a16
+
 using namespace w4a16;
 
 extern "C" {
@@ -601,5 +635,33 @@ int w4a16_selftest_wait_timeout(uint64_t timeout_ns, void* stream) {
 uint64_t w4a16_launch_count(void) { return g_launches.load(); }
 
 const char* w4a16_last_error_detail(void) { return g_error_detail; }
+
+int w4a16_gemm_noalloc(const void* A_bf16, int64_t M, int64_t N, int64_t K, const void* packed,
+                       const void* scales, int group, const void* bias_bf16_or_null, void* Y_bf16,
+                       void* stream) {
+  const int st = check_gemm_args(A_bf16, M, N, K, packed, scales, group, bias_bf16_or_null, Y_bf16);
+  if (st != W4A16_OK) return st;
+  const int id = select_variant(M, N, K);
+  if (id < 0) return W4A16_ERR_NO_VARIANT;
+  const size_t need = variant_ws(id, M, N, K);
+  if (need > kNoAllocScratchBytes) {
+    std::snprintf(g_error_detail, sizeof(g_error_detail),
+                  "w4a16_gemm_noalloc: variant %s needs %zu scratch bytes, the static array holds %zu",
+                  kVariants[id].name, need, kNoAllocScratchBytes);
+    return W4A16_ERR_WORKSPACE;
+  }
+  void* scratch = nullptr;
+  const int sst = noalloc_scratch(&scratch);
+  if (sst != W4A16_OK) return sst;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (need > 0) {
+    // the arrival counters must start at zero (a call that timed out could
+    // have left them set); clearing them is a memset, not an allocation
+    const cudaError_t e = cudaMemsetAsync(scratch, 0, kCounterBytes, s);
+    if (e != cudaSuccess) return cuda_failure(e, "cudaMemsetAsync(noalloc counters)");
+  }
+  return run_gemm(id, A_bf16, M, N, K, packed, scales, bias_bf16_or_null, Y_bf16,
+                  need > 0 ? scratch : nullptr, need > 0 ? kNoAllocScratchBytes : 0, s);
+}
 
 }  // extern "C"
