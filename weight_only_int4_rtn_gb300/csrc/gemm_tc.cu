@@ -110,6 +110,7 @@ struct Args {
   int dp_tiles;
   int sk_units;
   int act_3d;                  // activation map is 3-D: both 64-k halves in one copy
+  const __half* scales;        // [K/128, N]; the group-mode readout reads its scales here
   const __nv_bfloat16* bias;
   __nv_bfloat16* Y;
   float* ws;
@@ -284,8 +285,7 @@ struct Cfg {
   static constexpr int kStageRaw = 2 * kActBox + kWBytes + kSBytes;
   static constexpr int kStage = (kStageRaw + 1023) / 1024 * 1024;
   static constexpr int kThreads = 32 * kDequantWarp0 + 128 * NWG;   // 15 warps: <= 128 registers
-  static constexpr int kDequantCols = kAStageCols / NWG;          // A-stage columns per WG
-  static constexpr int kWords = 16 / NWG;                         // code words per thread per unit
+  static constexpr int kWords = 16;                               // code words per thread per unit
   // Each accumulator buffer holds NACC partial accumulators of BA columns:
   // k-step kk of a unit goes to partial kk % NACC, so NACC independent MMA
   // dependency chains overlap in the tensor pipe (with a small N a single
@@ -454,13 +454,14 @@ __global__ void __launch_bounds__(Cfg<BA, NWG, GRP, STAGES, NACC>::kThreads, 1)
   unsigned long long* const trace_unit = blockIdx.x == 0 ? g_trace_units : nullptr;
 #endif
   // Barriers.  full[s]: a stage's copies landed.  unit_done[i % R]: all MMAs
-  // of unit i completed (one tcgen05.commit per unit); it frees the TMEM
-  // weight stage of unit i, tells the group-mode readout that the unit's
-  // partial sum is ready, and (dequant mode) frees the shared-memory stage.
-  // empty[s] (group mode): the readout has read the stage's scales, the last
-  // use of the stage.  afull: the weight operand is in TMEM.  dempty: the
-  // readout drained an accumulator buffer.  dfull (dequant mode): a run on a
-  // tile is fully accumulated.
+  // of unit i completed (one tcgen05.commit per unit); it frees the
+  // shared-memory stage and the TMEM weight stage of unit i and tells the
+  // group-mode readout that the unit's partial sum is ready.  afull: the
+  // weight operand is in TMEM (the dequant warps waited on full before, so
+  // the MMA thread need not).  dempty: the readout drained an accumulator
+  // buffer.  dfull (dequant mode): a run on a tile is fully accumulated.
+  // Each mbarrier check costs about a hundred cycles even when the phase is
+  // already complete, so the single MMA thread makes as few as it can.
   constexpr int R = STAGES > kAStages ? STAGES : kAStages;
   if (threadIdx.x == 0) W4A16_TRACE_POINT(0);
   if (threadIdx.x == 0) {
@@ -469,7 +470,7 @@ __global__ void __launch_bounds__(Cfg<BA, NWG, GRP, STAGES, NACC>::kThreads, 1)
       ptx::mbar_init(&sh->empty[s], 4);
     }
     for (int s = 0; s < R; ++s) ptx::mbar_init(&sh->unit_done[s], 1);
-    for (int s = 0; s < kAStages; ++s) ptx::mbar_init(&sh->afull[s], 4 * NWG);
+    for (int s = 0; s < kAStages; ++s) ptx::mbar_init(&sh->afull[s], 4);
     for (int s = 0; s < DB; ++s) {
       ptx::mbar_init(&sh->dfull[s], 1);
       ptx::mbar_init(&sh->dempty[s], 4);
@@ -516,9 +517,7 @@ __global__ void __launch_bounds__(Cfg<BA, NWG, GRP, STAGES, NACC>::kThreads, 1)
         const int stage = i % STAGES;
         if (i >= STAGES) {
           const int j = i - STAGES;   // the unit that last used this stage
-          const bool ok = GRP ? wait_one(&sh->empty[stage], (j / STAGES) & 1, wc)
-                              : wait_one(&sh->unit_done[j % R], (j / R) & 1, wc);
-          if (!ok) break;
+          if (!wait_one(&sh->unit_done[j % R], (j / R) & 1, wc)) break;
         }
         const int m0 = (u.tile / a.n_tiles) * BA;
         ptx::mbar_arrive_expect_tx(&sh->full[stage], C::kTx);
@@ -559,14 +558,14 @@ __global__ void __launch_bounds__(Cfg<BA, NWG, GRP, STAGES, NACC>::kThreads, 1)
         const int stage = i % STAGES;
         const int as = i % kAStages;
         W4A16_TRACE_UNIT(8, i);
-        if (!wait_one(&sh->full[stage], (i / STAGES) & 1, wc)) break;
-        W4A16_TRACE_UNIT(9, i);
         if (!wait_one(&sh->afull[as], (i / kAStages) & 1, wc)) break;
         W4A16_TRACE_UNIT(10, i);
         bool fresh;
         if constexpr (GRP) {
           db = i % DB;
-          if (i >= DB && !wait_one(&sh->dempty[db], ((i / DB) - 1) & 1, wc)) break;
+          // the readout frees buffers in unit order: once unit i-1 is read
+          // out, the buffers of units i .. i+DB-1 are all free
+          if (db == 0 && i >= DB && !wait_one(&sh->dempty[DB - 1], ((i / DB) - 1) & 1, wc)) break;
           fresh = true;
         } else {
           fresh = u.seg_first;
@@ -618,24 +617,34 @@ __global__ void __launch_bounds__(Cfg<BA, NWG, GRP, STAGES, NACC>::kThreads, 1)
     float acc[GRP ? BA : 1];
     float bias_n = 0.0f;
     int seg = 0;
+    // group mode: the unit's scales come from global memory (L2: the TMA just
+    // brought them), fetched two units ahead
+    UnitIter ahead = it;
+    float s_next = 0.0f, s_next2 = 0.0f;
+    auto fetch_scale = [&](int j) -> float {
+      if (j >= total) return 0.0f;
+      const Unit v = ahead.next();
+      const int nn = (v.tile % a.n_tiles) * kTileW + row;
+      return nn < a.N ? __half2float(a.scales[static_cast<int64_t>(v.kb) * a.N + nn]) : 0.0f;
+    };
+    if constexpr (GRP) {
+      s_next = fetch_scale(0);
+      s_next2 = fetch_scale(1);
+    }
     for (int i = 0; i < total; ++i) {
       const Unit u = it.next();
       const int n = (u.tile % a.n_tiles) * kTileW + row;
       if (u.seg_first)
         bias_n = (a.bias != nullptr && n < a.N) ? __bfloat162float(a.bias[n]) : 0.0f;
       if constexpr (GRP) {
-        const int stage = i % STAGES;
         const int db = i % DB;
-        // the unit's MMAs are complete: its partial sum is in TMEM and the
-        // stage's other contents are consumed; the scales are read last
+        const float scale = s_next;
+        s_next = s_next2;
+        s_next2 = fetch_scale(i + 2);
         if (!wait_warp(&sh->unit_done[i % R], (i / R) & 1, wc)) break;
-        if (!wait_warp(&sh->full[stage], (i / STAGES) & 1, wc)) break;
         if (threadIdx.x == 32 * kReadoutWarp0 && i == 0) W4A16_TRACE_POINT(8);
         if (threadIdx.x == 32 * kReadoutWarp0 && i == total - 1) W4A16_TRACE_POINT(9);
         if (threadIdx.x == 32 * kReadoutWarp0) W4A16_TRACE_UNIT(6, i);
-        const float scale = __half2float(s_tile(stage)[row]);
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&sh->empty[stage]);
         ptx::tc_fence_after();
 #pragma unroll
         for (int c0 = 0; c0 < BA; c0 += C::kChunk) {
@@ -647,7 +656,7 @@ __global__ void __launch_bounds__(Cfg<BA, NWG, GRP, STAGES, NACC>::kThreads, 1)
         }
         ptx::tc_fence_before();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&sh->dempty[db]);
+        if (lane == 0 && db == DB - 1) ptx::mbar_arrive(&sh->dempty[DB - 1]);
         if (threadIdx.x == 32 * kReadoutWarp0) W4A16_TRACE_UNIT(7, i);
         if (u.seg_last) {
           emit_cols<BA, BA>(a, u, row, 0, acc, bias_n);
@@ -673,47 +682,35 @@ __global__ void __launch_bounds__(Cfg<BA, NWG, GRP, STAGES, NACC>::kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ dequant
+    // warpgroup wg converts units wg, wg + NWG, ...: every thread its whole
+    // row of 128 codes per unit
     const int wg = (warp - kDequantWarp0) >> 2;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    constexpr int kWords = C::kWords;
     const uint32_t wrow0 = ptx::smem_u32(w_tile(0)) + row * 64;
-    for (int i = 0; i < total; ++i) {
+    const uint32_t swz = (row >> 1) & 3;
+    for (int i = wg; i < total; i += NWG) {
       const int stage = i % STAGES;
       const int as = i % kAStages;
       if (!wait_warp(&sh->full[stage], (i / STAGES) & 1, wc)) break;
       if (i == 0 && threadIdx.x == 32 * kDequantWarp0) W4A16_TRACE_POINT(6);
       if (threadIdx.x == 32 * kDequantWarp0) W4A16_TRACE_UNIT(1, i);
 
-      // this thread's share of its row's 64 B of packed codes, stored with the
-      // 64-byte swizzle: 16-byte chunk c of row r sits at c ^ ((r >> 1) & 3)
+      // the row's 64 B of packed codes, stored with the 64-byte swizzle:
+      // 16-byte chunk c of row r sits at chunk position c ^ ((r >> 1) & 3)
       const uint32_t wrow = wrow0 + stage * C::kStage;
-      uint32_t words[kWords];
+      uint32_t words[16];
 #pragma unroll
-      for (int q = 0; q < kWords / 4; ++q) {
-        const int chunk = wg * (kWords / 4) + q;
-        const uint4 v = ptx::lds128(wrow + ((chunk ^ ((row >> 1) & 3)) << 4));
+      for (int q = 0; q < 4; ++q) {
+        const uint4 v = ptx::lds128(wrow + ((q ^ swz) << 4));
         words[4 * q + 0] = v.x;
         words[4 * q + 1] = v.y;
         words[4 * q + 2] = v.z;
         words[4 * q + 3] = v.w;
       }
-      uint32_t opnd[4 * kWords];
-#pragma unroll
-      for (int q = 0; q < kWords; ++q) codes_to_bf16(words[q], &opnd[4 * q]);
-      if constexpr (!GRP) {
-        const float scale = __half2float(s_tile(stage)[row]);
-        const __nv_bfloat16 hi = __float2bfloat16_rn(scale);
-        const float lo_f = scale - __bfloat162float(hi);        // exact
-        const __nv_bfloat16 lo = __float2bfloat16_rn(lo_f);     // exact
-        const uint32_t hi_bits = static_cast<uint32_t>(__bfloat16_as_ushort(hi));
-        const uint32_t lo_bits = static_cast<uint32_t>(__bfloat16_as_ushort(lo));
-        const uint32_t s_hi2 = hi_bits | (hi_bits << 16);
-        const uint32_t s_lo2 = lo_bits | (lo_bits << 16);
-#pragma unroll
-        for (int q = 0; q < 4 * kWords; ++q) opnd[q] = scale_pair(opnd[q], s_hi2, s_lo2);
-      }
+      float scale = 0.0f;
+      if constexpr (!GRP) scale = __half2float(s_tile(stage)[row]);
 
       // the TMEM stage is free once the MMAs of the unit that used it completed
       if (i >= kAStages) {
@@ -722,15 +719,35 @@ __global__ void __launch_bounds__(Cfg<BA, NWG, GRP, STAGES, NACC>::kThreads, 1)
       }
       if (threadIdx.x == 32 * kDequantWarp0) W4A16_TRACE_UNIT(2, i);
       ptx::tc_fence_after();
-      const uint32_t a_addr = lane_base + as * kAStageCols + wg * C::kDequantCols;
+      const uint32_t a_addr = lane_base + as * kAStageCols;
+      uint32_t s_hi2 = 0, s_lo2 = 0;
+      if constexpr (!GRP) {
+        const __nv_bfloat16 hi = __float2bfloat16_rn(scale);
+        const float lo_f = scale - __bfloat162float(hi);        // exact
+        const __nv_bfloat16 lo = __float2bfloat16_rn(lo_f);     // exact
+        const uint32_t hi_bits = static_cast<uint32_t>(__bfloat16_as_ushort(hi));
+        const uint32_t lo_bits = static_cast<uint32_t>(__bfloat16_as_ushort(lo));
+        s_hi2 = hi_bits | (hi_bits << 16);
+        s_lo2 = lo_bits | (lo_bits << 16);
+      }
+      // convert and store 16 columns (4 code words) at a time
 #pragma unroll
-      for (int q = 0; q < (4 * kWords) / 16; ++q) ptx::tmem_st_x16(a_addr + 16 * q, &opnd[16 * q]);
+      for (int q = 0; q < 4; ++q) {
+        uint32_t opnd[16];
+#pragma unroll
+        for (int w = 0; w < 4; ++w) codes_to_bf16(words[4 * q + w], &opnd[4 * w]);
+        if constexpr (!GRP) {
+#pragma unroll
+          for (int c = 0; c < 16; ++c) opnd[c] = scale_pair(opnd[c], s_hi2, s_lo2);
+        }
+        ptx::tmem_st_x16(a_addr + 16 * q, opnd);
+      }
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&sh->afull[as]);
       if (threadIdx.x == 32 * kDequantWarp0) W4A16_TRACE_UNIT(3, i);
-      if (i == total - 1 && threadIdx.x == 32 * kDequantWarp0) W4A16_TRACE_POINT(7);
+      if (i >= total - NWG && threadIdx.x == 32 * kDequantWarp0) W4A16_TRACE_POINT(7);
     }
   }
 
@@ -805,6 +822,7 @@ cudaError_t launch_instance(const GemmSchedule& s, const GemmProblem& p, bool us
   a.dp_tiles = s.dp_tiles;
   a.sk_units = static_cast<int>(s.sk_units);
   a.act_3d = act_3d;
+  a.scales = static_cast<const __half*>(p.scales);
   a.bias = static_cast<const __nv_bfloat16*>(p.bias);
   a.Y = static_cast<__nv_bfloat16*>(p.Y);
   a.counters = static_cast<uint32_t*>(p.workspace);
