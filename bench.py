@@ -64,6 +64,26 @@ def gemm_flops(M, N, K):
     return 2.0 * M * N * K
 
 
+def max_over_ranks(values, world, device=None):
+    """Element-wise max of per-rank floats over all ranks (identity at N=1).
+    Uses the process group already initialised: NCCL reduces on `device`,
+    gloo on the CPU."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+    dev = device if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
+def job_rate(units_per_rank_step, steps, elapsed_ms, world):
+    """Whole-job throughput: every rank processes `units_per_rank_step` per
+    step (replicas), the job takes the slowest rank's `elapsed_ms`."""
+    return world * units_per_rank_step * steps / (elapsed_ms * 1e-3)
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -327,17 +347,13 @@ def run_gpu(args, rank, world):
     barrier()
     e2e_ms = e0.elapsed_time(e1)
 
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([elapsed_ms, e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms, e2e_ms = float(t[0]), float(t[1])
+    elapsed_ms, e2e_ms = max_over_ranks([elapsed_ms, e2e_ms], world, dev)
 
     bytes_step = sum(quant_bytes(c.N, c.K) + gemm_bytes(c.M, c.N, c.K) for c in cases)
     flops_step = sum(gemm_flops(c.M, c.N, c.K) for c in cases)
     ms_step = elapsed_ms / args.steps
-    value = world * bytes_step * args.steps / (elapsed_ms * 1e-3) / 1e9
-    e2e_value = world * bytes_step * args.steps / (e2e_ms * 1e-3) / 1e9
+    value = job_rate(bytes_step, args.steps, elapsed_ms, world) / 1e9
+    e2e_value = job_rate(bytes_step, args.steps, e2e_ms, world) / 1e9
 
     peaks = load_peaks()
     kernels = []
@@ -384,7 +400,7 @@ def run_gpu(args, rank, world):
                            step="rtn_quantize + w4a16_gemm per projection",
                            l2="inputs rotate over %d copies (%.0f MB > 3x L2)" % (copies, copies * per_copy / 2**20),
                            parallelism=f"replicas x{world}"),
-               gemm=dict(tflops=round(flops_step * args.steps * world / (elapsed_ms * 1e-3) / 1e12, 3)),
+               gemm=dict(tflops=round(job_rate(flops_step, args.steps, elapsed_ms, world) / 1e12, 3)),
                kernels=kernels, roofline=roofline, clocks=clk.summary(),
                gpu_launches=int(launches),
                e2e=dict(value=round(e2e_value, 2), unit="GB/s", h2d_bytes_per_step=int(h2d),
