@@ -59,6 +59,28 @@ def test_every_variant(w4, case):
     assert w4.w4a16_get_device_error() == w4.W4A16_OK
 
 
+def test_every_variant_long_pipelines(w4):
+    """Long runs through every variant's stage rings (K = 16384: 128 units
+    per tile, up to 128 units per CTA), each launch on a fresh workspace whose
+    partial slots hold NaN, three launches per variant: a stage reused before
+    its copy landed, or a partial tile read before it was written, shows up
+    as a wrong or non-finite output."""
+    case = synthetic.Case("m300_k16384", 300, 256, 16384, 16, bias=True)
+    W, A, b, packed, scales = make_operands(w4, case)
+    y_ref = reference(A, packed, scales, b)
+    Ad, bd = A.cuda(), b.cuda()
+    for v in variant_ids(w4):
+        if not w4.w4a16_variant_eligible(v, case.M, case.N, case.K):
+            continue
+        need = w4.w4a16_variant_workspace_bytes(v, case.M, case.N, case.K)
+        for _ in range(3):
+            ws = torch.zeros(max(need, 4096), dtype=torch.uint8, device=Ad.device)
+            ws[4096:].fill_(0xFF)
+            Y = w4.w4a16_gemm(Ad, packed, scales, bias=bd, workspace=ws, variant=v)
+            assert w4.w4a16_get_device_error() == w4.W4A16_OK, w4.w4a16_variant_name(v)
+            check_gemm_close(Y, y_ref, what=w4.w4a16_variant_name(v))
+
+
 def test_default_selection_and_determinism(w4):
     case = synthetic.Case("det", 64, 2048, 2048, 21, bias=True)
     W, A, b, packed, scales = make_operands(w4, case)
@@ -137,7 +159,7 @@ def test_workloads_full_size_sampled(w4, case):
     oracle (all rows when M <= 64)."""
     W, A, b, packed, scales = make_operands(w4, case)
     Y = w4.w4a16_gemm(A.cuda(), packed, scales)
-    torch.cuda.synchronize()
+    assert w4.w4a16_get_device_error() == w4.W4A16_OK
     M = case.M
     rows = np.arange(M) if M <= 64 else np.unique(np.r_[0, 1, M // 2, M - 2, M - 1,
                                                        np.random.default_rng(0).integers(0, M, 11)])

@@ -87,16 +87,16 @@ struct Variant {
 };
 
 const Variant kVariants[] = {
-    {"tc_a16_grp_sk", {16, 2, true, 16, 1}, true},
-    {"tc_a32_grp_sk", {32, 2, true, 12, 1}, true},
-    {"tc_a64_grp_sk", {64, 2, true, 8, 1}, true},
-    {"tc_a64_deq_sk", {64, 2, false, 8, 1}, true},
-    {"tc_a128_deq_sk", {128, 2, false, 5, 1}, true},
-    {"tc_a256_deq_sk", {256, 2, false, 3, 1}, true},
-    {"tc_a16_grp_dp", {16, 2, true, 16, 1}, false},
-    {"tc_a64_grp_dp", {64, 2, true, 8, 1}, false},
-    {"tc_a128_deq_dp", {128, 2, false, 5, 1}, false},
-    {"tc_a256_deq_dp", {256, 2, false, 3, 1}, false},
+    {"tc_a16_grp_sk", {16, 2, true, 16}, true},
+    {"tc_a32_grp_sk", {32, 2, true, 12}, true},
+    {"tc_a64_grp_sk", {64, 2, true, 8}, true},
+    {"tc_a64_deq_sk", {64, 1, false, 8}, true},
+    {"tc_a128_deq_sk", {128, 1, false, 5}, true},
+    {"tc_a256_deq_sk", {256, 1, false, 3}, true},
+    {"tc_a16_grp_dp", {16, 2, true, 16}, false},
+    {"tc_a64_grp_dp", {64, 2, true, 8}, false},
+    {"tc_a128_deq_dp", {128, 1, false, 5}, false},
+    {"tc_a256_deq_dp", {256, 1, false, 3}, false},
 };
 constexpr int kNumVariants = static_cast<int>(sizeof(kVariants) / sizeof(kVariants[0]));
 

@@ -37,22 +37,33 @@
 // fastest.  Tiles 0 .. dp_tiles-1 run whole on CTA t % grid.  The units of
 // the remaining tiles are split into contiguous, balanced ranges over all
 // CTAs (stream-K).  A range that covers only part of a tile writes an fp32
-// partial tile to the workspace and increments that tile's counter; the CTA
-// whose increment completes the count sums the partials in k order
-// (deterministic), adds the bias and stores Y, then resets the counter.
-// Nothing ever waits on another CTA.
+// partial tile to the workspace.  When every CTA is done, one grid-wide
+// barrier; then all CTAs together sum each split tile's partials in k order
+// (deterministic), add the bias and store Y.  The grid is at most one CTA
+// per SM and a CTA needs more than half an SM's shared memory, so all CTAs
+// are resident at once and the barrier cannot wait on an unscheduled CTA.
 //
-// Warp roles (blockDim = 224 + 128 * dequant_wgs):
+// Lanes.  One thread issuing tcgen05.mma with a small N (16..64) is limited
+// by its own issue rate (about 47 cycles per MMA), well below the tensor
+// pipe; two issuing threads reach the pipe's rate.  So the group-scale
+// variants run two lanes: even units and odd units each have their own
+// producer, dequant warpgroup and MMA issuer, their own shared-memory stages,
+// TMEM weight stages, accumulators and barrier rings; only the readout
+// visits all units, in order.
+//
+// Warp roles (16 warps):
 //   warps 0, 2  TMA producers (one lane each; even and odd units, because one
 //               thread can only complete a few mbarrier phases per
 //               microsecond, fewer than the weight stream needs)
-//   warp 1      TMEM allocator; MMA issuer (one lane)
-//   warps 3-6   readout: accumulator -> registers / output, stream-K fixup
-//   warps 7..   dequant: packed codes (shared memory) -> weight operand (TMEM)
+//   warp 1      TMEM allocator; MMA issuer of lane 0 (of all units with one lane)
+//   warp 15     MMA issuer of lane 1
+//   warps 3-6   readout: accumulator -> registers -> Y or partial tile
+//   warps 7-14  dequant, two warpgroups (even / odd units): packed codes
+//               (shared memory) -> weight operand (TMEM)
 // A warp may only touch TMEM lanes 32 * (warp % 4) .. + 31, so each readout
 // and dequant thread owns weight row 32 * (warp % 4) + lane.  The dequant
 // warps never wait on accumulators: they run up to four units ahead of the
-// MMA, which runs up to DB units ahead of the readout.
+// MMA, which runs up to the accumulator count ahead of the readout.
 //
 // Every wait on an mbarrier is bounded by a time limit; on expiry the kernel
 // records an error word, lets every role leave its loop, waits (bounded) for
@@ -101,8 +112,10 @@ constexpr int kAStageCols = kUnitK / 2;        // 64 TMEM columns per stage
 constexpr int kDCol = kAStages * kAStageCols;  // accumulators start at column 256
 constexpr int kDCols = 512 - kDCol;            // 256 accumulator columns
 constexpr uint32_t kTmemCols = 512;
+constexpr int kWarps = 16;
 constexpr int kReadoutWarp0 = 3;
 constexpr int kDequantWarp0 = 7;
+constexpr int kMmaWarp2 = 15;                  // second MMA issuer (two lanes)
 
 struct Args {
   int M, N, K, KB;
@@ -141,34 +154,6 @@ struct Sched {
     u0 = static_cast<int>((static_cast<int64_t>(c) * a.sk_units) / C);
     u1 = static_cast<int>((static_cast<int64_t>(c + 1) * a.sk_units) / C);
     total = dp_iters * KB + (u1 - u0);
-  }
-
-  __device__ Unit get(int i) const {
-    Unit r;
-    const int ndp = dp_iters * KB;
-    if (i < ndp) {
-      const int it = i / KB;
-      r.tile = it * C + c;
-      r.kb = i - it * KB;
-      r.seg_first = (r.kb == 0);
-      r.seg_last = (r.kb == KB - 1);
-      r.whole = true;
-      r.slot = 0;
-      r.sk_tile = -1;
-    } else {
-      const int u = u0 + (i - ndp);
-      const int tl = u / KB;
-      r.tile = dp_tiles + tl;
-      r.kb = u - tl * KB;
-      const int seg_lo = max(u0, tl * KB);
-      const int seg_hi = min(u1, (tl + 1) * KB);   // exclusive
-      r.seg_first = (u == seg_lo);
-      r.seg_last = (u == seg_hi - 1);
-      r.whole = (seg_lo == tl * KB) && (seg_hi == (tl + 1) * KB);
-      r.slot = (tl == u0 / KB) ? 0 : 1;
-      r.sk_tile = tl;
-    }
-    return r;
   }
 };
 
@@ -237,18 +222,15 @@ __device__ __forceinline__ int sk_owner(int u, int C, int sk_units) {
 }
 
 struct Shared {
-  uint64_t full[16];
-  uint64_t empty[16];
-  uint64_t afull[kAStages];
-  uint64_t aempty[kAStages];
-  uint64_t dfull[4];
-  uint64_t dempty[4];
-  uint64_t unit_done[16];     // ring: phase completes when a unit's MMAs completed
-  uint64_t mma_done;
-  uint64_t wsync;             // readout-only barrier (bounded waits, unlike bar.sync)
+  uint64_t full[16];          // a shared-memory stage's copies landed
+  uint64_t afull[kAStages];   // a TMEM weight stage is written
+  uint64_t unit_done[32];     // per lane a ring: a unit's MMAs completed
+  uint64_t dfull[8];          // dequant mode: a run on a tile is accumulated
+  uint64_t dempty[8];         // the readout drained accumulator buffer(s)
+  uint64_t mma_done[2];
   uint32_t tmem_base;
   int abort_flag;
-  int fixup_last;
+  int reduce_ok;
 };
 
 // ------------------------------------------------------- code -> bf16 pairs
@@ -279,30 +261,44 @@ __device__ __forceinline__ uint32_t scale_pair(uint32_t q, uint32_t s_hi2, uint3
   return bf16x2_fma(q, s_hi2, lo);
 }
 
-template <int BA, int NWG, bool GRP, int STAGES, int NACC>
+template <int BA, int L, bool GRP, int STAGES>
 struct Cfg {
   static constexpr int kActBox = BA * 128;                        // bytes per 64-k box
   static constexpr int kStageRaw = 2 * kActBox + kWBytes + kSBytes;
   static constexpr int kStage = (kStageRaw + 1023) / 1024 * 1024;
-  static constexpr int kThreads = 32 * kDequantWarp0 + 128 * NWG;   // 15 warps: <= 128 registers
-  static constexpr int kWords = 16;                               // code words per thread per unit
-  // Each accumulator buffer holds NACC partial accumulators of BA columns:
-  // k-step kk of a unit goes to partial kk % NACC, so NACC independent MMA
-  // dependency chains overlap in the tensor pipe (with a small N a single
-  // chain is bound by the MMA latency, not its throughput); the readout sums
-  // the partials.
-  static constexpr int kBufCols = BA * NACC;
-  static constexpr int kDB = (kDCols / kBufCols) < 4 ? (kDCols / kBufCols) : 4;
+  static constexpr int kThreads = 32 * kWarps;                    // 16 warps: <= 128 registers
+  static constexpr int kSL = STAGES / L;                          // shared-memory stages per lane
+  static constexpr int kAL = kAStages / L;                        // TMEM weight stages per lane
+  static constexpr int kDBfit = kDCols / BA;                      // accumulators that fit
+  static constexpr int kDB = kDBfit < (GRP ? 8 : 4) ? kDBfit : (GRP ? 8 : 4);
+  static constexpr int kDL = kDB / L;                             // accumulator buffers per lane
+  static constexpr int kRL = kSL > kAL ? kSL : kAL;               // unit_done ring per lane
   static constexpr int kChunk = BA < (GRP ? 16 : 32) ? BA : (GRP ? 16 : 32);
   static constexpr size_t kSmem = static_cast<size_t>(STAGES) * kStage + 1024 + sizeof(Shared);
   static constexpr uint32_t kTx = 2 * kActBox + kWBytes + kSBytes;
   static_assert(BA % 16 == 0 && BA >= 16 && BA <= 256, "tcgen05 N for M=128");
-  static_assert(kDB >= 1, "accumulators fit in TMEM");
-  static_assert(NACC == 1 || NACC == 2 || NACC == 4, "partial accumulators divide the 8 k-steps");
+  static_assert(L == 1 || L == 2, "lanes");
+  static_assert(GRP || L == 1, "dequant mode accumulates a tile run in one lane");
+  static_assert(STAGES % L == 0 && STAGES <= 16, "stages split over the lanes");
+  static_assert(kDB % L == 0 && kDL >= 1, "accumulators split over the lanes");
+  // a unit_done phase may only be reused once every waiter saw the previous
+  // one: the readout is at most kDL units of a lane behind its MMAs
+  static_assert(kRL >= kDL, "unit_done ring covers the accumulator buffers");
+  static_assert(L * kRL <= 32, "barrier arrays");
   static_assert(!GRP || BA <= 64, "group mode keeps BA fp32 accumulators per thread");
-  static_assert(STAGES <= 16, "barrier arrays");
-  static_assert(NWG == 1 || NWG == 2, "dequant warpgroups");
 };
+
+// Lane of unit i and its index within the lane.
+template <int L>
+__device__ __forceinline__ void lane_split(int i, int& p, int& j) {
+  if constexpr (L == 1) {
+    p = 0;
+    j = i;
+  } else {
+    p = i & 1;
+    j = i >> 1;
+  }
+}
 
 template <int N>
 __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t* r) {
@@ -316,24 +312,17 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t* r) {
   }
 }
 
-// CNT accumulator columns of this thread's lane, summed over the NACC
-// partial accumulators (BA columns apart).
-template <int CNT, int NACC, int BA>
-__device__ __forceinline__ void load_partials(uint32_t taddr, float (&v)[CNT]) {
+template <int CNT>
+__device__ __forceinline__ void load_cols(uint32_t taddr, float (&v)[CNT]) {
   uint32_t r[CNT];
   tmem_ld_cols<CNT>(taddr, r);
 #pragma unroll
   for (int j = 0; j < CNT; ++j) v[j] = __uint_as_float(r[j]);
-#pragma unroll
-  for (int p = 1; p < NACC; ++p) {
-    tmem_ld_cols<CNT>(taddr + p * BA, r);
-#pragma unroll
-    for (int j = 0; j < CNT; ++j) v[j] += __uint_as_float(r[j]);
-  }
 }
 
 // Write accumulator columns [col0, col0 + CNT) of this thread's weight row
-// either to Y (whole tile) or to this CTA's partial slot.
+// either to Y (whole tile: bias added, one rounding to bf16) or to this CTA's
+// partial slot (fp32, no bias; column m of the slot holds 128 rows).
 template <int BA, int CNT>
 __device__ __forceinline__ void emit_cols(const Args& a, const Unit& u, int row, int col0,
                                           const float (&v)[CNT], float bias_n) {
@@ -349,90 +338,100 @@ __device__ __forceinline__ void emit_cols(const Args& a, const Unit& u, int row,
       }
     }
   } else {
-    // partial slot, row-major: this thread's row holds BA contiguous floats
-    float* slot = a.ws + (static_cast<int64_t>(blockIdx.x) * 2 + u.slot) * (BA * kTileW) +
-                  row * BA + col0;
+    float* slot = a.ws + (static_cast<int64_t>(blockIdx.x) * 2 + u.slot) * (BA * kTileW) + row;
 #pragma unroll
-    for (int j = 0; j < CNT; j += 4)
-      *reinterpret_cast<float4*>(slot + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+    for (int j = 0; j < CNT; ++j) {
+      if (m0 + col0 + j < a.M) slot[(col0 + j) * kTileW] = v[j];
+    }
   }
 }
 
-// Barrier among the readout warps built on an mbarrier, so that a warp that
-// gave up after a timeout cannot leave the others blocked forever.
-__device__ bool readout_sync(Shared* sh, uint32_t& nsync, const WaitCtx& wc) {
-  __syncwarp();
-  if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(&sh->wsync);
-  const bool ok = wait_warp(&sh->wsync, nsync & 1, wc);
-  ++nsync;
-  return ok;
-}
-
-// After this CTA wrote a partial tile: count the arrival; the CTA that
-// completes the count sums every partial of the tile in k order and stores Y.
-template <int BA>
-__device__ bool stream_k_fixup(const Args& a, const Unit& u, Shared* sh, int row, float bias_n,
-                               uint32_t& nsync, const WaitCtx& wc) {
-  constexpr int kSub = BA < 16 ? BA : 16;   // columns summed together
-  const int C = gridDim.x;
+// Grid-wide barrier after every CTA wrote its partial tiles (one thread per
+// CTA).  The grid never exceeds one CTA per SM and each CTA needs more than
+// half an SM's shared memory, so all CTAs are resident together; the wait is
+// bounded all the same.  Self-resetting: the last arrival clears the count
+// and bumps the generation the others wait on.
+__device__ bool grid_barrier(const Args& a, const WaitCtx& wc) {
+  if (*reinterpret_cast<volatile int*>(wc.abort_flag)) return false;
+  uint32_t* count = a.counters;
+  uint32_t* gen = a.counters + 1;
+  const uint32_t g0 = ptx::ld_acquire_gpu(gen);
   __threadfence();
-  if (!readout_sync(sh, nsync, wc)) return false;
-  const int KB = a.KB;
-  const int c_lo = sk_owner(u.sk_tile * KB, C, a.sk_units);
-  const int c_hi = sk_owner(u.sk_tile * KB + KB - 1, C, a.sk_units);
-  if (threadIdx.x == 32 * kReadoutWarp0) {
-    const uint32_t old = atomicAdd(&a.counters[u.sk_tile], 1u);
-    const bool last = (old == static_cast<uint32_t>(c_hi - c_lo));
-    if (last) atomicExch(&a.counters[u.sk_tile], 0u);
-    sh->fixup_last = last ? 1 : 0;
+  const uint32_t old = atomicAdd(count, 1u);
+  if (old == gridDim.x - 1) {
+    atomicExch(count, 0u);
+    __threadfence();
+    atomicAdd(gen, 1u);
+    return true;
   }
-  if (!readout_sync(sh, nsync, wc)) return false;
-  if (!sh->fixup_last) return true;
-  __threadfence();
-  const int n0 = (u.tile % a.n_tiles) * kTileW;
-  const int m0 = (u.tile / a.n_tiles) * BA;
-  const int n = n0 + row;
-  const float* base = a.ws + row * BA;
-  for (int c0 = 0; c0 < BA; c0 += kSub) {
-    float acc[kSub];
-#pragma unroll
-    for (int j = 0; j < kSub; ++j) acc[j] = 0.0f;
-#pragma unroll 4
-    for (int cc = c_lo; cc <= c_hi; ++cc) {
-      // slot 0 when the tile is the first stream-K tile of CTA cc, else 1
-      const int first_tile = static_cast<int>((static_cast<int64_t>(cc) * a.sk_units) / C) / KB;
-      const int slot = (u.sk_tile == first_tile) ? 0 : 1;
-      const float4* src = reinterpret_cast<const float4*>(
-          base + (static_cast<int64_t>(cc) * 2 + slot) * (BA * kTileW) + c0);
-      float4 v[kSub / 4];
-#pragma unroll
-      for (int j = 0; j < kSub / 4; ++j) v[j] = __ldcg(src + j);
-#pragma unroll
-      for (int j = 0; j < kSub / 4; ++j) {
-        acc[4 * j] += v[j].x;
-        acc[4 * j + 1] += v[j].y;
-        acc[4 * j + 2] += v[j].z;
-        acc[4 * j + 3] += v[j].w;
-      }
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (ptx::ld_acquire_gpu(gen) == g0) {
+    if (ptx::globaltimer_ns() - t0 > a.timeout_ns) {
+      wait_record_timeout(wc);
+      return false;
     }
-    if (n < a.N) {
-#pragma unroll
-      for (int j = 0; j < kSub; ++j) {
-        const int m = m0 + c0 + j;
-        if (m < a.M) a.Y[static_cast<int64_t>(m) * a.N + n] = __float2bfloat16_rn(acc[j] + bias_n);
-      }
-    }
+    ptx::nanosleep(32);
   }
   return true;
 }
 
-template <int BA, int NWG, bool GRP, int STAGES, int NACC>
-__global__ void __launch_bounds__(Cfg<BA, NWG, GRP, STAGES, NACC>::kThreads, 1)
+// Second phase of stream-K: every element of every split tile is the sum of
+// its contributors' partials in k order (deterministic), plus the bias,
+// rounded once to bf16.  The elements are spread evenly over all CTAs and
+// all threads; consecutive threads take consecutive weight rows, so partial
+// reads and Y stores are coalesced.
+template <int BA>
+__device__ void stream_k_reduce(const Args& a) {
+  constexpr int kTileElems = BA * kTileW;
+  const int C = gridDim.x;
+  const int KB = a.KB;
+  const int S = a.sk_units;
+  const int64_t E = static_cast<int64_t>(S / KB) * kTileElems;
+  const int64_t e_lo = static_cast<int64_t>(blockIdx.x) * E / C;
+  const int64_t e_hi = static_cast<int64_t>(blockIdx.x + 1) * E / C;
+  int cached = -1, c_lo = 0, c_hi = 0, slot_lo = 0, m0 = 0, n0 = 0;
+  for (int64_t e = e_lo + threadIdx.x; e < e_hi; e += blockDim.x) {
+    const int tl = static_cast<int>(e / kTileElems);
+    const int rem = static_cast<int>(e - static_cast<int64_t>(tl) * kTileElems);
+    const int m = rem >> 7;
+    const int row = rem & (kTileW - 1);
+    if (tl != cached) {
+      cached = tl;
+      c_lo = sk_owner(tl * KB, C, S);
+      c_hi = sk_owner(tl * KB + KB - 1, C, S);
+      // the CTA holding the tile's first k-block keeps it in slot 0 only if
+      // its range starts exactly there; every later contributor's range
+      // starts inside the tile (slot 0)
+      const int u0_lo = static_cast<int>(static_cast<int64_t>(c_lo) * S / C);
+      slot_lo = (u0_lo == tl * KB) ? 0 : 1;
+      const int tile = a.dp_tiles + tl;
+      m0 = (tile / a.n_tiles) * BA;
+      n0 = (tile % a.n_tiles) * kTileW;
+    }
+    if (c_lo == c_hi) continue;   // one CTA ran the whole tile and stored Y
+    const int mm = m0 + m;
+    const int n = n0 + row;
+    if (mm >= a.M || n >= a.N) continue;
+    const float* col = a.ws + static_cast<int64_t>(m) * kTileW + row;
+    float sum = __ldcg(col + (static_cast<int64_t>(c_lo) * 2 + slot_lo) * kTileElems);
+#pragma unroll 4
+    for (int c = c_lo + 1; c <= c_hi; ++c) sum += __ldcg(col + static_cast<int64_t>(c) * 2 * kTileElems);
+    const float b = a.bias != nullptr ? __bfloat162float(a.bias[n]) : 0.0f;
+    a.Y[static_cast<int64_t>(mm) * a.N + n] = __float2bfloat16_rn(sum + b);
+  }
+}
+
+template <int BA, int L, bool GRP, int STAGES>
+__global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES>::kThreads, 1)
     w4a16_gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_act,
                          const __grid_constant__ CUtensorMap tm_w,
                          const __grid_constant__ CUtensorMap tm_s, const Args a) {
-  using C = Cfg<BA, NWG, GRP, STAGES, NACC>;
+  using C = Cfg<BA, L, GRP, STAGES>;
   constexpr int DB = C::kDB;
+  constexpr int SL = C::kSL;
+  constexpr int AL = C::kAL;
+  constexpr int DL = C::kDL;
+  constexpr int RL = C::kRL;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -447,38 +446,47 @@ __global__ void __launch_bounds__(Cfg<BA, NWG, GRP, STAGES, NACC>::kThreads, 1)
   auto s_tile = [&](int stage) -> __half* {
     return reinterpret_cast<__half*>(smem + stage * C::kStage + 2 * C::kActBox + kWBytes);
   };
+  // Resources of unit i (lane p, index j in the lane): the lanes own
+  // interleaved shared-memory stages, TMEM weight stages and accumulators.
+  auto stage_of = [&](int i) -> int {
+    int p, j;
+    lane_split<L>(i, p, j);
+    return p + L * (j % SL);
+  };
+  auto astage_of = [&](int i) -> int {
+    int p, j;
+    lane_split<L>(i, p, j);
+    return p + L * (j % AL);
+  };
+  auto done_bar = [&](int i) -> uint64_t* {
+    int p, j;
+    lane_split<L>(i, p, j);
+    return &sh->unit_done[p * RL + j % RL];
+  };
+  auto done_parity = [&](int i) -> uint32_t {
+    int p, j;
+    lane_split<L>(i, p, j);
+    return static_cast<uint32_t>((j / RL) & 1);
+  };
 
   // ---------------------------------------------------------------- set-up
 #ifdef W4A16_TRACE
   unsigned long long* const trace_cta = g_trace;
   unsigned long long* const trace_unit = blockIdx.x == 0 ? g_trace_units : nullptr;
 #endif
-  // Barriers.  full[s]: a stage's copies landed.  unit_done[i % R]: all MMAs
-  // of unit i completed (one tcgen05.commit per unit); it frees the
-  // shared-memory stage and the TMEM weight stage of unit i and tells the
-  // group-mode readout that the unit's partial sum is ready.  afull: the
-  // weight operand is in TMEM (the dequant warps waited on full before, so
-  // the MMA thread need not).  dempty: the readout drained an accumulator
-  // buffer.  dfull (dequant mode): a run on a tile is fully accumulated.
-  // Each mbarrier check costs about a hundred cycles even when the phase is
-  // already complete, so the single MMA thread makes as few as it can.
-  constexpr int R = STAGES > kAStages ? STAGES : kAStages;
   if (threadIdx.x == 0) W4A16_TRACE_POINT(0);
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      ptx::mbar_init(&sh->full[s], 1);
-      ptx::mbar_init(&sh->empty[s], 4);
-    }
-    for (int s = 0; s < R; ++s) ptx::mbar_init(&sh->unit_done[s], 1);
+    for (int s = 0; s < STAGES; ++s) ptx::mbar_init(&sh->full[s], 1);
+    for (int s = 0; s < L * RL; ++s) ptx::mbar_init(&sh->unit_done[s], 1);
     for (int s = 0; s < kAStages; ++s) ptx::mbar_init(&sh->afull[s], 4);
     for (int s = 0; s < DB; ++s) {
       ptx::mbar_init(&sh->dfull[s], 1);
       ptx::mbar_init(&sh->dempty[s], 4);
     }
-    ptx::mbar_init(&sh->mma_done, 1);
-    ptx::mbar_init(&sh->wsync, 4);
+    ptx::mbar_init(&sh->mma_done[0], 1);
+    ptx::mbar_init(&sh->mma_done[1], 1);
     sh->abort_flag = 0;
-    sh->fixup_last = 0;
+    sh->reduce_ok = 0;
     ptx::fence_mbar_init();
     ptx::prefetch_tmap(&tm_act);
     ptx::prefetch_tmap(&tm_w);
@@ -508,17 +516,17 @@ __global__ void __launch_bounds__(Cfg<BA, NWG, GRP, STAGES, NACC>::kThreads, 1)
 
   if (warp == 0 || warp == 2) {
     // ----------------------------------------------------- TMA producers
+    // Even units from warp 0, odd units from warp 2 (with two lanes: one
+    // producer per lane).
     if (lane == 0) {
       const int mine = warp == 0 ? 0 : 1;
       int issued = -1;
       for (int i = 0; i < total; ++i) {
         const Unit u = it.next();
         if ((i & 1) != mine) continue;
-        const int stage = i % STAGES;
-        if (i >= STAGES) {
-          const int j = i - STAGES;   // the unit that last used this stage
-          if (!wait_one(&sh->unit_done[j % R], (j / R) & 1, wc)) break;
-        }
+        const int stage = stage_of(i);
+        // the unit that last used this stage is i - STAGES (same lane)
+        if (i >= STAGES && !wait_one(done_bar(i - STAGES), done_parity(i - STAGES), wc)) break;
         const int m0 = (u.tile / a.n_tiles) * BA;
         ptx::mbar_arrive_expect_tx(&sh->full[stage], C::kTx);
         if (a.act_3d) {
@@ -539,33 +547,42 @@ __global__ void __launch_bounds__(Cfg<BA, NWG, GRP, STAGES, NACC>::kThreads, 1)
       if (*reinterpret_cast<volatile int*>(&sh->abort_flag)) {
         // let this producer's copies still in flight land before the CTA exits
         for (int i = issued; i >= 0 && i > issued - STAGES; i -= 2) {
+          int p, j;
+          lane_split<L>(i, p, j);
           const uint64_t t0 = ptx::globaltimer_ns();
-          while (!ptx::mbar_try_wait(&sh->full[i % STAGES], (i / STAGES) & 1)) {
+          while (!ptx::mbar_try_wait(&sh->full[stage_of(i)], (j / SL) & 1)) {
             if (ptx::globaltimer_ns() - t0 > a.timeout_ns) break;
           }
         }
       }
     }
-  } else if (warp == 1) {
-    // -------------------------------------------------------- MMA issuer
+  } else if (warp == 1 || (L == 2 && warp == kMmaWarp2)) {
+    // ------------------------------------------------------- MMA issuers
+    // One thread per lane: one thread alone cannot issue small-N MMAs as
+    // fast as the tensor pipe runs them.
     if (lane == 0) {
+      const int mine = warp == 1 ? 0 : 1;
       constexpr uint32_t idesc = ptx::idesc_bf16_f32(kTileW, BA);
       const uint32_t smem0 = ptx::smem_u32(smem);
       int seg = 0;
       int db = 0;
       for (int i = 0; i < total; ++i) {
         const Unit u = it.next();
-        const int stage = i % STAGES;
-        const int as = i % kAStages;
+        if (L == 2 && (i & 1) != mine) continue;
+        int p, j;
+        lane_split<L>(i, p, j);
+        const int stage = stage_of(i);
+        const int as = astage_of(i);
         W4A16_TRACE_UNIT(8, i);
-        if (!wait_one(&sh->afull[as], (i / kAStages) & 1, wc)) break;
+        if (!wait_one(&sh->afull[as], (j / AL) & 1, wc)) break;
         W4A16_TRACE_UNIT(10, i);
         bool fresh;
         if constexpr (GRP) {
-          db = i % DB;
-          // the readout frees buffers in unit order: once unit i-1 is read
-          // out, the buffers of units i .. i+DB-1 are all free
-          if (db == 0 && i >= DB && !wait_one(&sh->dempty[DB - 1], ((i / DB) - 1) & 1, wc)) break;
+          const int dl = j % DL;
+          db = p + L * dl;
+          // the readout frees a lane's buffers in order: once it read the
+          // lane's unit j-1, buffers of units j .. j+DL-1 are free
+          if (dl == 0 && j >= DL && !wait_one(&sh->dempty[p], ((j / DL) - 1) & 1, wc)) break;
           fresh = true;
         } else {
           fresh = u.seg_first;
@@ -578,18 +595,17 @@ __global__ void __launch_bounds__(Cfg<BA, NWG, GRP, STAGES, NACC>::kThreads, 1)
         if (i == 0) W4A16_TRACE_POINT(4);
         if (i == total - 1) W4A16_TRACE_POINT(5);
         W4A16_TRACE_UNIT(4, i);
-        const uint32_t d_tmem = tmem + kDCol + db * C::kBufCols;
+        const uint32_t d_tmem = tmem + kDCol + db * BA;
         const uint32_t a_tmem = tmem + as * kAStageCols;
         const uint32_t b0 = smem0 + stage * C::kStage;
 #pragma unroll
         for (int kk = 0; kk < kUnitK / 16; ++kk) {
           const uint32_t baddr = b0 + (kk >> 2) * C::kActBox + (kk & 3) * 32;
-          ptx::mma_bf16_tmem_a(d_tmem + (kk % NACC) * BA, a_tmem + kk * 8,
-                               ptx::smem_desc_sw128(baddr), idesc,
-                               (kk >= NACC || !fresh) ? 1u : 0u);
+          ptx::mma_bf16_tmem_a(d_tmem, a_tmem + kk * 8, ptx::smem_desc_sw128(baddr), idesc,
+                               (kk > 0 || !fresh) ? 1u : 0u);
         }
         W4A16_TRACE_UNIT(11, i);
-        ptx::mma_commit(&sh->unit_done[i % R]);
+        ptx::mma_commit(done_bar(i));
         if constexpr (!GRP) {
           if (u.seg_last) {
             ptx::mma_commit(&sh->dfull[db]);
@@ -598,22 +614,21 @@ __global__ void __launch_bounds__(Cfg<BA, NWG, GRP, STAGES, NACC>::kThreads, 1)
         }
         W4A16_TRACE_UNIT(5, i);
       }
-      // all MMAs of this CTA complete before TMEM is freed
-      ptx::mma_commit(&sh->mma_done);
+      // all MMAs of this thread complete before TMEM is freed
+      ptx::mma_commit(&sh->mma_done[mine]);
       const uint64_t t0 = ptx::globaltimer_ns();
-      while (!ptx::mbar_try_wait(&sh->mma_done, 0)) {
+      while (!ptx::mbar_try_wait(&sh->mma_done[mine], 0)) {
         if (ptx::globaltimer_ns() - t0 > a.timeout_ns) {
           wait_record_timeout(wc);
           break;
         }
       }
     }
-  } else if (warp < kDequantWarp0) {
+  } else if (warp >= kReadoutWarp0 && warp < kReadoutWarp0 + 4) {
     // ------------------------------------------------------------ readout
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    uint32_t nsync = 0;
     float acc[GRP ? BA : 1];
     float bias_n = 0.0f;
     int seg = 0;
@@ -621,8 +636,8 @@ __global__ void __launch_bounds__(Cfg<BA, NWG, GRP, STAGES, NACC>::kThreads, 1)
     // brought them), fetched two units ahead
     UnitIter ahead = it;
     float s_next = 0.0f, s_next2 = 0.0f;
-    auto fetch_scale = [&](int j) -> float {
-      if (j >= total) return 0.0f;
+    auto fetch_scale = [&](int jj) -> float {
+      if (jj >= total) return 0.0f;
       const Unit v = ahead.next();
       const int nn = (v.tile % a.n_tiles) * kTileW + row;
       return nn < a.N ? __half2float(a.scales[static_cast<int64_t>(v.kb) * a.N + nn]) : 0.0f;
@@ -637,11 +652,14 @@ __global__ void __launch_bounds__(Cfg<BA, NWG, GRP, STAGES, NACC>::kThreads, 1)
       if (u.seg_first)
         bias_n = (a.bias != nullptr && n < a.N) ? __bfloat162float(a.bias[n]) : 0.0f;
       if constexpr (GRP) {
-        const int db = i % DB;
+        int p, j;
+        lane_split<L>(i, p, j);
+        const int dl = j % DL;
+        const int db = p + L * dl;
         const float scale = s_next;
         s_next = s_next2;
         s_next2 = fetch_scale(i + 2);
-        if (!wait_warp(&sh->unit_done[i % R], (i / R) & 1, wc)) break;
+        if (!wait_warp(done_bar(i), done_parity(i), wc)) break;
         if (threadIdx.x == 32 * kReadoutWarp0 && i == 0) W4A16_TRACE_POINT(8);
         if (threadIdx.x == 32 * kReadoutWarp0 && i == total - 1) W4A16_TRACE_POINT(9);
         if (threadIdx.x == 32 * kReadoutWarp0) W4A16_TRACE_UNIT(6, i);
@@ -649,19 +667,16 @@ __global__ void __launch_bounds__(Cfg<BA, NWG, GRP, STAGES, NACC>::kThreads, 1)
 #pragma unroll
         for (int c0 = 0; c0 < BA; c0 += C::kChunk) {
           float d[C::kChunk];
-          load_partials<C::kChunk, NACC, BA>(lane_base + kDCol + db * C::kBufCols + c0, d);
+          load_cols<C::kChunk>(lane_base + kDCol + db * BA + c0, d);
 #pragma unroll
-          for (int j = 0; j < C::kChunk; ++j)
-            acc[c0 + j] = u.seg_first ? scale * d[j] : fmaf(scale, d[j], acc[c0 + j]);
+          for (int jj = 0; jj < C::kChunk; ++jj)
+            acc[c0 + jj] = u.seg_first ? scale * d[jj] : fmaf(scale, d[jj], acc[c0 + jj]);
         }
         ptx::tc_fence_before();
         __syncwarp();
-        if (lane == 0 && db == DB - 1) ptx::mbar_arrive(&sh->dempty[DB - 1]);
+        if (lane == 0 && dl == DL - 1) ptx::mbar_arrive(&sh->dempty[p]);
         if (threadIdx.x == 32 * kReadoutWarp0) W4A16_TRACE_UNIT(7, i);
-        if (u.seg_last) {
-          emit_cols<BA, BA>(a, u, row, 0, acc, bias_n);
-          if (!u.whole && !stream_k_fixup<BA>(a, u, sh, row, bias_n, nsync, wc)) break;
-        }
+        if (u.seg_last) emit_cols<BA, BA>(a, u, row, 0, acc, bias_n);
       } else {
         if (!u.seg_last) continue;
         const int db = seg % DB;
@@ -671,29 +686,39 @@ __global__ void __launch_bounds__(Cfg<BA, NWG, GRP, STAGES, NACC>::kThreads, 1)
 #pragma unroll 1
         for (int c0 = 0; c0 < BA; c0 += C::kChunk) {
           float v[C::kChunk];
-          load_partials<C::kChunk, NACC, BA>(lane_base + kDCol + db * C::kBufCols + c0, v);
+          load_cols<C::kChunk>(lane_base + kDCol + db * BA + c0, v);
           emit_cols<BA, C::kChunk>(a, u, row, c0, v, bias_n);
         }
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&sh->dempty[db]);
-        if (!u.whole && !stream_k_fixup<BA>(a, u, sh, row, bias_n, nsync, wc)) break;
       }
     }
-  } else {
+  } else if (warp >= kDequantWarp0 && warp < kDequantWarp0 + 8) {
     // ------------------------------------------------------------ dequant
-    // warpgroup wg converts units wg, wg + NWG, ...: every thread its whole
-    // row of 128 codes per unit
+    // warpgroup wg converts units wg, wg + 2, ... (with two lanes: lane wg's
+    // units): every thread its whole row of 128 codes per unit
     const int wg = (warp - kDequantWarp0) >> 2;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const uint32_t wrow0 = ptx::smem_u32(w_tile(0)) + row * 64;
     const uint32_t swz = (row >> 1) & 3;
-    for (int i = wg; i < total; i += NWG) {
-      const int stage = i % STAGES;
-      const int as = i % kAStages;
-      if (!wait_warp(&sh->full[stage], (i / STAGES) & 1, wc)) break;
+    for (int i = wg; i < total; i += 2) {
+      int p, j;
+      lane_split<L>(i, p, j);
+      const int stage = stage_of(i);
+      const int as = astage_of(i);
+      if constexpr (L == 1 && (STAGES & 1) != 0) {
+        // With an odd stage count the uses of one stage alternate between
+        // the two warpgroups, so this warpgroup did not see the stage's
+        // previous phase (unit i - STAGES, the other warpgroup's), and a
+        // parity wait cannot tell that phase from this unit's.  The producer
+        // refills the stage only after the MMAs of unit i - STAGES completed,
+        // so waiting for those first proves the previous phase complete.
+        if (i >= STAGES && !wait_warp(done_bar(i - STAGES), done_parity(i - STAGES), wc)) break;
+      }
+      if (!wait_warp(&sh->full[stage], (j / SL) & 1, wc)) break;
       if (i == 0 && threadIdx.x == 32 * kDequantWarp0) W4A16_TRACE_POINT(6);
       if (threadIdx.x == 32 * kDequantWarp0) W4A16_TRACE_UNIT(1, i);
 
@@ -712,11 +737,9 @@ __global__ void __launch_bounds__(Cfg<BA, NWG, GRP, STAGES, NACC>::kThreads, 1)
       float scale = 0.0f;
       if constexpr (!GRP) scale = __half2float(s_tile(stage)[row]);
 
-      // the TMEM stage is free once the MMAs of the unit that used it completed
-      if (i >= kAStages) {
-        const int j = i - kAStages;
-        if (!wait_warp(&sh->unit_done[j % R], (j / R) & 1, wc)) break;
-      }
+      // the TMEM stage is free once the MMAs of the unit that used it
+      // (i - kAStages, same lane) completed
+      if (i >= kAStages && !wait_warp(done_bar(i - kAStages), done_parity(i - kAStages), wc)) break;
       if (threadIdx.x == 32 * kDequantWarp0) W4A16_TRACE_UNIT(2, i);
       ptx::tc_fence_after();
       const uint32_t a_addr = lane_base + as * kAStageCols;
@@ -747,7 +770,7 @@ __global__ void __launch_bounds__(Cfg<BA, NWG, GRP, STAGES, NACC>::kThreads, 1)
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&sh->afull[as]);
       if (threadIdx.x == 32 * kDequantWarp0) W4A16_TRACE_UNIT(3, i);
-      if (i >= total - NWG && threadIdx.x == 32 * kDequantWarp0) W4A16_TRACE_POINT(7);
+      if (i >= total - 2 && threadIdx.x == 32 * kDequantWarp0) W4A16_TRACE_POINT(7);
     }
   }
 
@@ -757,6 +780,13 @@ __global__ void __launch_bounds__(Cfg<BA, NWG, GRP, STAGES, NACC>::kThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   if (warp == 1) ptx::tmem_dealloc(tmem, kTmemCols);
+  if (a.sk_units > 0) {
+    // split tiles: every CTA wrote its partials; after the grid barrier all
+    // CTAs reduce them together
+    if (threadIdx.x == 0) sh->reduce_ok = grid_barrier(a, wc) ? 1 : 0;
+    __syncthreads();
+    if (sh->reduce_ok) stream_k_reduce<BA>(a);
+  }
   if (threadIdx.x == 32) W4A16_TRACE_POINT(11);
 }
 
@@ -774,11 +804,11 @@ __global__ void wait_timeout_selftest_kernel(uint32_t* err, uint64_t timeout_ns)
   }
 }
 
-template <int BA, int NWG, bool GRP, int STAGES, int NACC>
+template <int BA, int L, bool GRP, int STAGES>
 cudaError_t launch_instance(const GemmSchedule& s, const GemmProblem& p, bool use_pdl,
                             cudaStream_t stream) {
-  using C = Cfg<BA, NWG, GRP, STAGES, NACC>;
-  auto kernel = w4a16_gemm_tc_kernel<BA, NWG, GRP, STAGES, NACC>;
+  using C = Cfg<BA, L, GRP, STAGES>;
+  auto kernel = w4a16_gemm_tc_kernel<BA, L, GRP, STAGES>;
 
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -843,23 +873,21 @@ cudaError_t launch_instance(const GemmSchedule& s, const GemmProblem& p, bool us
   return cudaLaunchKernelEx(&cfg, kernel, tm_act, tm_w, tm_s, a);
 }
 
-// The compiled configurations:
-//   {act_tile, dequant_wgs, group_scale, stages, partial accumulators}.
+// The compiled configurations: {act_tile, lanes, group_scale, stages}.
 #define W4A16_GEMM_INSTANCES(X) \
-  X(16, 2, true, 16, 1)         \
-  X(32, 2, true, 12, 1)         \
-  X(64, 2, true, 8, 1)          \
-  X(64, 2, false, 8, 1)         \
-  X(128, 2, false, 5, 1)        \
-  X(256, 2, false, 3, 1)
+  X(16, 2, true, 16)            \
+  X(32, 2, true, 12)            \
+  X(64, 2, true, 8)             \
+  X(64, 1, false, 8)            \
+  X(128, 1, false, 5)           \
+  X(256, 1, false, 3)
 
 }  // namespace
 
 size_t gemm_smem_bytes(const GemmKernelConfig& c) {
-#define W4A16_SMEM_CASE(BA, NWG, GRP, ST, NA)                                            \
-  if (c.act_tile == BA && c.worker_wgs == NWG && c.group_scale == GRP && c.stages == ST && \
-      c.accumulators == NA)                                                                \
-    return Cfg<BA, NWG, GRP, ST, NA>::kSmem;
+#define W4A16_SMEM_CASE(BA, L, GRP, ST) \
+  if (c.act_tile == BA && c.lanes == L && c.group_scale == GRP && c.stages == ST) \
+    return Cfg<BA, L, GRP, ST>::kSmem;
   W4A16_GEMM_INSTANCES(W4A16_SMEM_CASE)
 #undef W4A16_SMEM_CASE
   return 0;
@@ -878,10 +906,9 @@ size_t gemm_workspace_bytes(const GemmKernelConfig& c, const GemmSchedule& s, in
 
 cudaError_t launch_gemm_tc(const GemmKernelConfig& c, const GemmSchedule& s,
                            const GemmProblem& p, bool use_pdl, cudaStream_t stream) {
-#define W4A16_LAUNCH_CASE(BA, NWG, GRP, ST, NA)                                          \
-  if (c.act_tile == BA && c.worker_wgs == NWG && c.group_scale == GRP && c.stages == ST && \
-      c.accumulators == NA)                                                                \
-    return launch_instance<BA, NWG, GRP, ST, NA>(s, p, use_pdl, stream);
+#define W4A16_LAUNCH_CASE(BA, L, GRP, ST) \
+  if (c.act_tile == BA && c.lanes == L && c.group_scale == GRP && c.stages == ST) \
+    return launch_instance<BA, L, GRP, ST>(s, p, use_pdl, stream);
   W4A16_GEMM_INSTANCES(W4A16_LAUNCH_CASE)
 #undef W4A16_LAUNCH_CASE
   return cudaErrorInvalidConfiguration;

@@ -20,11 +20,11 @@ cudaError_t launch_rtn_quantize(const void* W, int64_t N, int64_t K, void* packe
 // One configuration of the tcgen05 GEMM kernel.
 struct GemmKernelConfig {
   int act_tile;      // activation rows per tile (tcgen05 N): 16..256
-  int worker_wgs;    // dequant warpgroups: 1 or 2
+  int lanes;         // independent pipelines (1 or 2), each with its own MMA
+                     // issuing thread; units alternate between them
   bool group_scale;  // true: per-group fp32 scaling of integer-code partial sums
                      // false: weights dequantized to bf16(q*s) before the MMA
-  int stages;        // shared-memory pipeline depth
-  int accumulators;  // partial accumulators per buffer (independent MMA chains)
+  int stages;        // shared-memory pipeline depth (all lanes together)
 };
 
 // The schedule of one launch.
@@ -53,10 +53,12 @@ inline int64_t gemm_tiles(const GemmKernelConfig& c, int64_t M, int64_t N) {
   return ((N + kTileW - 1) / kTileW) * ((M + c.act_tile - 1) / c.act_tile);
 }
 
-// Workspace layout: kCounterBytes of uint32 arrival counters (one per
-// stream-K tile; there are never more stream-K tiles than CTAs, so the
-// region has a fixed size and every variant finds its counters at the same
-// place), then [grid][2][act_tile][128] fp32 partial slots.
+// Workspace layout: kCounterBytes of uint32 counters (words 0 and 1: the
+// grid barrier's arrival count and generation; the region has a fixed size so
+// every variant finds them at the same place), then [grid][2][act_tile][128]
+// fp32 partial slots (slot 0: the first stream-K tile of a CTA's range,
+// slot 1: its last; inside a slot, column m of the tile is 128 contiguous
+// weight rows).
 constexpr size_t kCounterBytes = 4096;
 constexpr int kMaxGrid = static_cast<int>(kCounterBytes / 4);
 size_t gemm_workspace_bytes(const GemmKernelConfig& c, const GemmSchedule& s, int64_t M,
