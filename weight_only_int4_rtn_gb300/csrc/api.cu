@@ -51,6 +51,10 @@ std::atomic<uint64_t> g_launches{0};
 
 constexpr int kMaxDevices = 64;
 
+// SM count assumed by host-only queries when no CUDA device is visible
+// (GB300: 152 SMs); launches always use the device's own count.
+constexpr int kDefaultSms = 152;
+
 struct DeviceInfo {
   bool ready = false;
   int num_sms = 0;
@@ -84,19 +88,28 @@ struct Variant {
   const char* name;
   GemmKernelConfig cfg;
   bool stream_k;   // false: whole tiles only (data parallel)
+  int min_units;   // stream-K: at least this many units per CTA (fewer CTAs and
+                   // fewer split tiles on small problems)
+  double unit_us;  // measured time of one unit (128 weight rows x one group)
+                   // in steady state on GB300, for the selection rule
 };
 
 const Variant kVariants[] = {
-    {"tc_a16_grp_sk", {16, 2, true, 16}, true},
-    {"tc_a32_grp_sk", {32, 2, true, 12}, true},
-    {"tc_a64_grp_sk", {64, 2, true, 8}, true},
-    {"tc_a64_deq_sk", {64, 1, false, 8}, true},
-    {"tc_a128_deq_sk", {128, 1, false, 5}, true},
-    {"tc_a256_deq_sk", {256, 1, false, 3}, true},
-    {"tc_a16_grp_dp", {16, 2, true, 16}, false},
-    {"tc_a64_grp_dp", {64, 2, true, 8}, false},
-    {"tc_a128_deq_dp", {128, 1, false, 5}, false},
-    {"tc_a256_deq_dp", {256, 1, false, 3}, false},
+    {"tc_a16_grp_sk", {16, 2, true, 16}, true, 1, 0.44},
+    {"tc_a32_grp_sk", {32, 2, true, 12}, true, 1, 0.57},
+    {"tc_a64_grp_sk", {64, 2, true, 8}, true, 1, 1.30},
+    {"tc_a64_deq_sk", {64, 1, false, 8}, true, 1, 0.71},
+    {"tc_a128_deq_sk", {128, 1, false, 5}, true, 1, 0.80},
+    {"tc_a256_deq_sk", {256, 1, false, 3}, true, 1, 1.08},
+    {"tc_a16_grp_dp", {16, 2, true, 16}, false, 1, 0.44},
+    {"tc_a64_grp_dp", {64, 2, true, 8}, false, 1, 1.30},
+    {"tc_a128_deq_dp", {128, 1, false, 5}, false, 1, 0.80},
+    {"tc_a256_deq_dp", {256, 1, false, 3}, false, 1, 1.08},
+    {"tc_a16_grp_sk4", {16, 2, true, 16}, true, 4, 0.44},
+    {"tc_a16_grp_sk8", {16, 2, true, 16}, true, 8, 0.44},
+    {"tc_a32_grp_sk4", {32, 2, true, 12}, true, 4, 0.57},
+    {"tc_a64_grp_sk4", {64, 2, true, 8}, true, 4, 1.30},
+    {"tc_a64_grp_sk8", {64, 2, true, 8}, true, 8, 1.30},
 };
 constexpr int kNumVariants = static_cast<int>(sizeof(kVariants) / sizeof(kVariants[0]));
 
@@ -135,7 +148,8 @@ GemmSchedule make_schedule(const Variant& v, int64_t M, int64_t N, int64_t K, in
       s.sk_units = 0;
     }
   } else {
-    s.grid = static_cast<int>(units < num_sms ? units : num_sms);
+    const int64_t want = (units + v.min_units - 1) / v.min_units;
+    s.grid = static_cast<int>(want < num_sms ? want : num_sms);
     s.dp_tiles = 0;
     s.sk_units = units;
   }
@@ -152,15 +166,38 @@ bool variant_eligible(int id, int64_t M, int64_t N, int64_t K) {
   return true;
 }
 
-// Fixed rule for shapes without a table entry.
-int rule_variant(int64_t M, int64_t N, int64_t K) {
-  (void)N;
-  (void)K;
-  if (M <= 16) return variant_by_name("tc_a16_grp_sk");
-  if (M <= 32) return variant_by_name("tc_a32_grp_sk");
-  if (M <= 64) return variant_by_name("tc_a64_grp_sk");
-  if (M <= 128) return variant_by_name("tc_a128_deq_sk");
-  return variant_by_name("tc_a256_deq_sk");
+// Rule for shapes without a table entry: a cost model fitted to GB300
+// measurements.  A launch pays a fixed head (launch, set-up, pipeline fill);
+// each CTA then runs its units at the variant's per-unit time; a schedule
+// that splits tiles over CTAs adds the grid-wide barrier and the reduction
+// of the partial tiles (more for wider activation tiles).  The variant with
+// the smallest estimate wins.
+constexpr double kHeadUs = 3.0;
+constexpr double kSplitUs = 4.0;
+constexpr double kSplitUsPerCol = 0.02;
+
+double estimate_us(const Variant& v, int64_t M, int64_t N, int64_t K, int num_sms) {
+  const GemmSchedule s = make_schedule(v, M, N, K, num_sms);
+  const int64_t KB = K / kGroup;
+  const int64_t dp_per_cta = (s.dp_tiles + s.grid - 1) / s.grid;
+  const int64_t sk_per_cta = (s.sk_units + s.grid - 1) / s.grid;
+  double t = kHeadUs + static_cast<double>(dp_per_cta * KB + sk_per_cta) * v.unit_us;
+  if (s.sk_units > 0) t += kSplitUs + kSplitUsPerCol * v.cfg.act_tile;
+  return t;
+}
+
+int rule_variant(int64_t M, int64_t N, int64_t K, int num_sms) {
+  int best = -1;
+  double best_t = 0.0;
+  for (int id = 0; id < kNumVariants; ++id) {
+    if (!variant_eligible(id, M, N, K)) continue;
+    const double t = estimate_us(kVariants[id], M, N, K, num_sms);
+    if (best < 0 || t < best_t) {
+      best = id;
+      best_t = t;
+    }
+  }
+  return best;
 }
 
 // ---------------------------------------------------------------- table
@@ -211,7 +248,11 @@ int select_variant(int64_t M, int64_t N, int64_t K) {
     auto it = g_table.find({M, N, K});
     if (it != g_table.end()) id = it->second;
   }
-  if (id < 0) id = rule_variant(M, N, K);
+  if (id < 0) {
+    DeviceInfo dev;
+    const int sms = device_info(dev) ? dev.num_sms : kDefaultSms;
+    id = rule_variant(M, N, K, sms);
+  }
   if (!variant_eligible(id, M, N, K)) return -1;
   return id;
 }
@@ -268,7 +309,7 @@ int run_gemm(int id, const void* A, int64_t M, int64_t N, int64_t K, const void*
 
 size_t variant_ws(int id, int64_t M, int64_t N, int64_t K) {
   DeviceInfo dev;
-  int sms = 148;
+  int sms = kDefaultSms;
   if (device_info(dev)) sms = dev.num_sms;
   const Variant& v = kVariants[id];
   return gemm_workspace_bytes(v.cfg, make_schedule(v, M, N, K, sms), M, N, K);
@@ -555,39 +596,70 @@ int w4a16_tune(int64_t M, int64_t N, int64_t K, void* stream_v, int* out_variant
   }
   if (ws) cudaMemsetAsync(ws, 0, wsbytes, stream);
 
+  // Each variant is timed as one CUDA graph of kIters launches (so host
+  // launch overhead does not hide short kernels), on a private stream.
   cudaEvent_t e0, e1;
   cudaEventCreate(&e0);
   cudaEventCreate(&e1);
+  cudaStream_t cs = nullptr;
+  if (cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess) ok = false;
+  if (ok && cudaStreamSynchronize(stream) != cudaSuccess) ok = false;
   float best_ms = 0.0f;
   int best = -1;
   constexpr int kIters = 20;
-  for (int id = 0; id < kNumVariants; ++id) {
+  for (int id = 0; ok && id < kNumVariants; ++id) {
     if (!variant_eligible(id, M, N, K)) continue;
     bool fine = true;
     for (int it = 0; it < 3 && fine; ++it)
       fine = run_gemm(id, A, M, N, K, Wp[it % copies], Sc[it % copies], nullptr, Y, ws, wsbytes,
-                      stream) == W4A16_OK;
+                      cs) == W4A16_OK;
     if (!fine) continue;
-    cudaEventRecord(e0, stream);
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t exec = nullptr;
+    if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+      ok = false;
+      break;
+    }
     for (int it = 0; it < kIters; ++it)
-      run_gemm(id, A, M, N, K, Wp[it % copies], Sc[it % copies], nullptr, Y, ws, wsbytes, stream);
-    cudaEventRecord(e1, stream);
-    if (cudaEventSynchronize(e1) != cudaSuccess) {
+      run_gemm(id, A, M, N, K, Wp[it % copies], Sc[it % copies], nullptr, Y, ws, wsbytes, cs);
+    if (cudaStreamEndCapture(cs, &graph) != cudaSuccess ||
+        cudaGraphInstantiate(&exec, graph, 0) != cudaSuccess) {
+      if (graph) cudaGraphDestroy(graph);
+      ok = false;
+      break;
+    }
+    cudaGraphLaunch(exec, cs);   // warm
+    cudaEventRecord(e0, cs);
+    cudaGraphLaunch(exec, cs);
+    cudaEventRecord(e1, cs);
+    const bool synced = cudaEventSynchronize(e1) == cudaSuccess;
+    cudaGraphExecDestroy(exec);
+    cudaGraphDestroy(graph);
+    if (!synced) {
       ok = false;
       break;
     }
     float ms = 0.0f;
     cudaEventElapsedTime(&ms, e0, e1);
+    if (log_enabled())
+      std::fprintf(stderr, "w4a16: tune M=%lld N=%lld K=%lld %s %.3f us\n",
+                   static_cast<long long>(M), static_cast<long long>(N), static_cast<long long>(K),
+                   kVariants[id].name, 1000.0 * ms / kIters);
     if (best < 0 || ms < best_ms) {
       best_ms = ms;
       best = id;
     }
   }
+  if (cs) {
+    cudaStreamSynchronize(cs);
+    cudaStreamDestroy(cs);
+  }
   cudaEventDestroy(e0);
   cudaEventDestroy(e1);
+  cudaGetLastError();   // a failed capture leaves no sticky error behind
   const int dev_err = w4a16_get_device_error(stream);
   release();
-  if (!ok) return W4A16_ERR_CUDA;
+  if (!ok) return cuda_failure(cudaErrorUnknown, "w4a16_tune: graph timing failed");
   if (dev_err != W4A16_OK) return dev_err;
   if (best < 0) return W4A16_ERR_NO_VARIANT;
   {

@@ -90,7 +90,7 @@ __device__ unsigned long long* g_trace_units = nullptr;
   } while (0)
 #define W4A16_TRACE_UNIT(role, i)                                                       \
   do {                                                                                  \
-    if (trace_unit != nullptr && (i) < 64)                                             \
+    if (trace_unit != nullptr && (i) < 64)                                              \
       trace_unit[(role) * 64 + (i)] = static_cast<unsigned long long>(clock64());     \
   } while (0)
 #else
@@ -116,6 +116,9 @@ constexpr int kWarps = 16;
 constexpr int kReadoutWarp0 = 3;
 constexpr int kDequantWarp0 = 7;
 constexpr int kMmaWarp2 = 15;                  // second MMA issuer (two lanes)
+constexpr int kScaleRing = 8;                  // group mode: units of scales in shared memory
+constexpr int kScaleAhead = 2;                 // ... copied this many unit pairs ahead
+constexpr int kPairRing = 8;                   // group mode: pair_done barriers
 
 struct Args {
   int M, N, K, KB;
@@ -216,6 +219,50 @@ struct UnitIter {
   }
 };
 
+// Walks this CTA's runs ("segments": consecutive units on one tile) in
+// order.  For the readout, which needs tile-level facts only at the ends of
+// runs.
+struct SegCursor {
+  int C, KB, dp_left, tile, u, u1, first_sk;
+  __device__ void init(const Sched& s) {
+    C = s.C;
+    KB = s.KB;
+    dp_left = s.dp_iters;
+    tile = s.c;
+    u = s.u0;
+    u1 = s.u1;
+    first_sk = 1;
+  }
+  // Next run: its tile, first k-block, length, and whether it is the whole
+  // tile (else: the partial slot it writes).
+  __device__ void next(Unit& r, int& kb0, int& len, int dp_tiles) {
+    if (dp_left > 0) {
+      --dp_left;
+      r.tile = tile;
+      tile += C;
+      kb0 = 0;
+      len = KB;
+      r.whole = true;
+      r.slot = 0;
+      r.sk_tile = -1;
+    } else {
+      const int tl = u / KB;
+      kb0 = u - tl * KB;
+      const int end = min(u1, (tl + 1) * KB);
+      len = end - u;
+      r.tile = dp_tiles + tl;
+      r.whole = (kb0 == 0) && (len == KB);
+      r.slot = first_sk ? 0 : 1;
+      r.sk_tile = tl;
+      first_sk = 0;
+      u = end;
+    }
+    r.kb = kb0;
+    r.seg_first = true;
+    r.seg_last = true;
+  }
+};
+
 // CTA that owns stream-K unit u under the balanced split.
 __device__ __forceinline__ int sk_owner(int u, int C, int sk_units) {
   return static_cast<int>(((static_cast<int64_t>(u) + 1) * C - 1) / sk_units);
@@ -227,6 +274,7 @@ struct Shared {
   uint64_t unit_done[32];     // per lane a ring: a unit's MMAs completed
   uint64_t dfull[8];          // dequant mode: a run on a tile is accumulated
   uint64_t dempty[8];         // the readout drained accumulator buffer(s)
+  uint64_t pair_done[8];       // group mode: both lanes' units of a pair completed
   uint64_t mma_done[2];
   uint32_t tmem_base;
   int abort_flag;
@@ -274,7 +322,8 @@ struct Cfg {
   static constexpr int kDL = kDB / L;                             // accumulator buffers per lane
   static constexpr int kRL = kSL > kAL ? kSL : kAL;               // unit_done ring per lane
   static constexpr int kChunk = BA < (GRP ? 16 : 32) ? BA : (GRP ? 16 : 32);
-  static constexpr size_t kSmem = static_cast<size_t>(STAGES) * kStage + 1024 + sizeof(Shared);
+  static constexpr size_t kSmem = static_cast<size_t>(STAGES) * kStage + 1024 + sizeof(Shared) +
+                                  (GRP ? kScaleRing * kTileW * 2 : 0);
   static constexpr uint32_t kTx = 2 * kActBox + kWBytes + kSBytes;
   static_assert(BA % 16 == 0 && BA >= 16 && BA <= 256, "tcgen05 N for M=128");
   static_assert(L == 1 || L == 2, "lanes");
@@ -286,6 +335,11 @@ struct Cfg {
   static_assert(kRL >= kDL, "unit_done ring covers the accumulator buffers");
   static_assert(L * kRL <= 32, "barrier arrays");
   static_assert(!GRP || BA <= 64, "group mode keeps BA fp32 accumulators per thread");
+  static_assert(!GRP || L == 2, "group mode runs two lanes (the readout takes units in pairs)");
+  // group mode: the pair ring replaces the unit ring for every waiter, so
+  // it must be as deep as the stage rings and the accumulator buffers
+  static_assert(!GRP || (kDL <= kPairRing && kSL <= kPairRing && kAL <= kPairRing),
+                "pair ring covers the stage rings and the accumulator buffers");
 };
 
 // Lane of unit i and its index within the lane.
@@ -356,21 +410,22 @@ __device__ bool grid_barrier(const Args& a, const WaitCtx& wc) {
   uint32_t* count = a.counters;
   uint32_t* gen = a.counters + 1;
   const uint32_t g0 = ptx::ld_acquire_gpu(gen);
-  __threadfence();
-  const uint32_t old = atomicAdd(count, 1u);
+  // acquire-release: the last arrival observes every other CTA's partials
+  const uint32_t old = ptx::atom_add_acq_rel_gpu(count, 1u);
   if (old == gridDim.x - 1) {
     atomicExch(count, 0u);
-    __threadfence();
-    atomicAdd(gen, 1u);
+    ptx::atom_add_release_gpu(gen, 1u);   // publishes all partials
     return true;
   }
   const uint64_t t0 = ptx::globaltimer_ns();
-  while (ptx::ld_acquire_gpu(gen) == g0) {
-    if (ptx::globaltimer_ns() - t0 > a.timeout_ns) {
-      wait_record_timeout(wc);
-      return false;
+  for (uint32_t spin = 0; ptx::ld_acquire_gpu(gen) == g0; ++spin) {
+    if ((spin & 15) == 15) {
+      if (ptx::globaltimer_ns() - t0 > a.timeout_ns) {
+        wait_record_timeout(wc);
+        return false;
+      }
+      ptx::nanosleep(32);
     }
-    ptx::nanosleep(32);
   }
   return true;
 }
@@ -458,14 +513,19 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES>::kThreads, 1)
     lane_split<L>(i, p, j);
     return p + L * (j % AL);
   };
+  // Completion of unit i's MMAs.  Group mode: the pair ring (lane 0's and
+  // lane 1's j-th units complete together, one arrival each); one lane:
+  // the unit ring.
   auto done_bar = [&](int i) -> uint64_t* {
     int p, j;
     lane_split<L>(i, p, j);
+    if constexpr (GRP) return &sh->pair_done[j % kPairRing];
     return &sh->unit_done[p * RL + j % RL];
   };
   auto done_parity = [&](int i) -> uint32_t {
     int p, j;
     lane_split<L>(i, p, j);
+    if constexpr (GRP) return static_cast<uint32_t>((j / kPairRing) & 1);
     return static_cast<uint32_t>((j / RL) & 1);
   };
 
@@ -483,6 +543,7 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES>::kThreads, 1)
       ptx::mbar_init(&sh->dfull[s], 1);
       ptx::mbar_init(&sh->dempty[s], 4);
     }
+    for (int s = 0; s < kPairRing; ++s) ptx::mbar_init(&sh->pair_done[s], 2);
     ptx::mbar_init(&sh->mma_done[0], 1);
     ptx::mbar_init(&sh->mma_done[1], 1);
     sh->abort_flag = 0;
@@ -564,55 +625,75 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES>::kThreads, 1)
       const int mine = warp == 1 ? 0 : 1;
       constexpr uint32_t idesc = ptx::idesc_bf16_f32(kTileW, BA);
       const uint32_t smem0 = ptx::smem_u32(smem);
-      int seg = 0;
-      int db = 0;
-      for (int i = 0; i < total; ++i) {
-        const Unit u = it.next();
-        if (L == 2 && (i & 1) != mine) continue;
-        int p, j;
-        lane_split<L>(i, p, j);
-        const int stage = stage_of(i);
-        const int as = astage_of(i);
-        W4A16_TRACE_UNIT(8, i);
-        if (!wait_one(&sh->afull[as], (j / AL) & 1, wc)) break;
-        W4A16_TRACE_UNIT(10, i);
-        bool fresh;
-        if constexpr (GRP) {
+      if constexpr (GRP) {
+        // this lane's units j = 0, 1, ...: unit i = 2 j + mine; every unit
+        // starts a fresh accumulator (the readout applies the group scale)
+        const int nj = (total - mine + 1) >> 1;
+        for (int j = 0; j < nj; ++j) {
+          const int stage = mine + 2 * (j % SL);
+          const int as = mine + 2 * (j % AL);
           const int dl = j % DL;
-          db = p + L * dl;
+          if (!wait_one(&sh->afull[as], (j / AL) & 1, wc)) break;
           // the readout frees a lane's buffers in order: once it read the
           // lane's unit j-1, buffers of units j .. j+DL-1 are free
-          if (dl == 0 && j >= DL && !wait_one(&sh->dempty[p], ((j / DL) - 1) & 1, wc)) break;
-          fresh = true;
-        } else {
-          fresh = u.seg_first;
+          if (dl == 0 && j >= DL && !wait_one(&sh->dempty[mine], ((j / DL) - 1) & 1, wc)) break;
+          ptx::tc_fence_after();
+          if (j == 0) W4A16_TRACE_POINT(4);
+          W4A16_TRACE_UNIT(4, 2 * j + mine);
+          const uint32_t d_tmem = tmem + kDCol + (mine + 2 * dl) * BA;
+          const uint32_t a_tmem = tmem + as * kAStageCols;
+          const uint32_t b0 = smem0 + stage * C::kStage;
+#pragma unroll
+          for (int kk = 0; kk < kUnitK / 16; ++kk) {
+            const uint32_t baddr = b0 + (kk >> 2) * C::kActBox + (kk & 3) * 32;
+            ptx::mma_bf16_tmem_a(d_tmem, a_tmem + kk * 8, ptx::smem_desc_sw128(baddr), idesc,
+                                 kk > 0 ? 1u : 0u);
+          }
+          // one arrival per lane on the pair's barrier; an unpaired last
+          // unit (lane 0) arrives for both
+          ptx::mma_commit(&sh->pair_done[j % kPairRing]);
+          if (mine == 0 && 2 * j == total - 1) ptx::mma_commit(&sh->pair_done[j % kPairRing]);
+          W4A16_TRACE_UNIT(5, 2 * j + mine);
+        }
+        if (nj > 0) W4A16_TRACE_POINT(5);
+      } else {
+        int seg = 0;
+        int db = 0;
+        for (int i = 0; i < total; ++i) {
+          const Unit u = it.next();
+          int p, j;
+          lane_split<L>(i, p, j);
+          const int stage = stage_of(i);
+          const int as = astage_of(i);
+          W4A16_TRACE_UNIT(8, i);
+          if (!wait_one(&sh->afull[as], (j / AL) & 1, wc)) break;
+          W4A16_TRACE_UNIT(10, i);
+          const bool fresh = u.seg_first;
           if (u.seg_first) {
             db = seg % DB;
             if (seg >= DB && !wait_one(&sh->dempty[db], ((seg / DB) - 1) & 1, wc)) break;
           }
-        }
-        ptx::tc_fence_after();
-        if (i == 0) W4A16_TRACE_POINT(4);
-        if (i == total - 1) W4A16_TRACE_POINT(5);
-        W4A16_TRACE_UNIT(4, i);
-        const uint32_t d_tmem = tmem + kDCol + db * BA;
-        const uint32_t a_tmem = tmem + as * kAStageCols;
-        const uint32_t b0 = smem0 + stage * C::kStage;
-#pragma unroll
-        for (int kk = 0; kk < kUnitK / 16; ++kk) {
-          const uint32_t baddr = b0 + (kk >> 2) * C::kActBox + (kk & 3) * 32;
-          ptx::mma_bf16_tmem_a(d_tmem, a_tmem + kk * 8, ptx::smem_desc_sw128(baddr), idesc,
-                               (kk > 0 || !fresh) ? 1u : 0u);
-        }
-        W4A16_TRACE_UNIT(11, i);
-        ptx::mma_commit(done_bar(i));
-        if constexpr (!GRP) {
+          ptx::tc_fence_after();
+          if (i == 0) W4A16_TRACE_POINT(4);
+          if (i == total - 1) W4A16_TRACE_POINT(5);
+          W4A16_TRACE_UNIT(4, i);
+          const uint32_t d_tmem = tmem + kDCol + db * BA;
+          const uint32_t a_tmem = tmem + as * kAStageCols;
+          const uint32_t b0 = smem0 + stage * C::kStage;
+  #pragma unroll
+          for (int kk = 0; kk < kUnitK / 16; ++kk) {
+            const uint32_t baddr = b0 + (kk >> 2) * C::kActBox + (kk & 3) * 32;
+            ptx::mma_bf16_tmem_a(d_tmem, a_tmem + kk * 8, ptx::smem_desc_sw128(baddr), idesc,
+                                 (kk > 0 || !fresh) ? 1u : 0u);
+          }
+          W4A16_TRACE_UNIT(11, i);
+          ptx::mma_commit(done_bar(i));
           if (u.seg_last) {
             ptx::mma_commit(&sh->dfull[db]);
             ++seg;
           }
+          W4A16_TRACE_UNIT(5, i);
         }
-        W4A16_TRACE_UNIT(5, i);
       }
       // all MMAs of this thread complete before TMEM is freed
       ptx::mma_commit(&sh->mma_done[mine]);
@@ -629,55 +710,139 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES>::kThreads, 1)
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    float acc[GRP ? BA : 1];
-    float bias_n = 0.0f;
-    int seg = 0;
-    // group mode: the unit's scales come from global memory (L2: the TMA just
-    // brought them), fetched two units ahead
-    UnitIter ahead = it;
-    float s_next = 0.0f, s_next2 = 0.0f;
-    auto fetch_scale = [&](int jj) -> float {
-      if (jj >= total) return 0.0f;
-      const Unit v = ahead.next();
-      const int nn = (v.tile % a.n_tiles) * kTileW + row;
-      return nn < a.N ? __half2float(a.scales[static_cast<int64_t>(v.kb) * a.N + nn]) : 0.0f;
-    };
     if constexpr (GRP) {
-      s_next = fetch_scale(0);
-      s_next2 = fetch_scale(1);
-    }
-    for (int i = 0; i < total; ++i) {
-      const Unit u = it.next();
-      const int n = (u.tile % a.n_tiles) * kTileW + row;
-      if (u.seg_first)
-        bias_n = (a.bias != nullptr && n < a.N) ? __bfloat162float(a.bias[n]) : 0.0f;
-      if constexpr (GRP) {
-        int p, j;
-        lane_split<L>(i, p, j);
-        const int dl = j % DL;
-        const int db = p + L * dl;
-        const float scale = s_next;
-        s_next = s_next2;
-        s_next2 = fetch_scale(i + 2);
-        if (!wait_warp(done_bar(i), done_parity(i), wc)) break;
-        if (threadIdx.x == 32 * kReadoutWarp0 && i == 0) W4A16_TRACE_POINT(8);
-        if (threadIdx.x == 32 * kReadoutWarp0 && i == total - 1) W4A16_TRACE_POINT(9);
-        if (threadIdx.x == 32 * kReadoutWarp0) W4A16_TRACE_UNIT(6, i);
-        ptx::tc_fence_after();
-#pragma unroll
-        for (int c0 = 0; c0 < BA; c0 += C::kChunk) {
-          float d[C::kChunk];
-          load_cols<C::kChunk>(lane_base + kDCol + db * BA + c0, d);
-#pragma unroll
-          for (int jj = 0; jj < C::kChunk; ++jj)
-            acc[c0 + jj] = u.seg_first ? scale * d[jj] : fmaf(scale, d[jj], acc[c0 + jj]);
+      // Units come in pairs (lane 0's j-th unit, lane 1's j-th unit), behind
+      // one barrier that both lanes' MMA threads arrive on.  Per pair: one
+      // wait, both accumulators loaded, then acc += s * D for each unit in
+      // order.  Per unit only a countdown; tile, row and scale addresses are
+      // computed once per run ("segment") of the CTA.
+      float acc[BA];
+      // Scales: copied from global memory into a ring in shared memory
+      // kScaleAhead pairs before they are needed (per-thread asynchronous
+      // copies; each even lane copies its row's and the next row's scale).
+      uint16_t* const sring =
+          reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(sh) + sizeof(Shared));
+      SegCursor pf_cur;
+      pf_cur.init(sched);
+      int pf_left = 0;
+      const __half* pf_ptr = a.scales;
+      bool pf_ok = false;
+      auto prefetch_unit = [&](int jj) {
+        if (jj >= total) return;
+        if (pf_left == 0) {
+          Unit v;
+          int kb0;
+          pf_cur.next(v, kb0, pf_left, a.dp_tiles);
+          const int nn = (v.tile % a.n_tiles) * kTileW + row;
+          pf_ok = nn < a.N;   // N % 8 == 0: row nn + 1 exists too
+          pf_ptr = a.scales + static_cast<int64_t>(kb0) * a.N + nn;
+        } else {
+          pf_ptr += a.N;
         }
-        ptx::tc_fence_before();
+        --pf_left;
+        if ((lane & 1) == 0 && pf_ok)
+          ptx::cp_async_4(ptx::smem_u32(sring + (jj % kScaleRing) * kTileW + row), pf_ptr);
+      };
+#pragma unroll
+      for (int q = 0; q < kScaleAhead; ++q) {
+        prefetch_unit(2 * q);
+        prefetch_unit(2 * q + 1);
+        ptx::cp_async_commit();
+      }
+      // the current run
+      SegCursor cur;
+      cur.init(sched);
+      Unit seg;
+      int seg_left = 0;
+      bool first = true;
+      float bias_f = 0.0f;
+      auto open_run = [&]() {
+        int kb0;
+        cur.next(seg, kb0, seg_left, a.dp_tiles);
+        const int n = (seg.tile % a.n_tiles) * kTileW + row;
+        bias_f = (a.bias != nullptr && n < a.N) ? __bfloat162float(a.bias[n]) : 0.0f;
+        first = true;
+      };
+      if (total > 0) open_run();
+      // acc (+)= scale * D for one unit, 16 columns at a time; emits at the
+      // end of a run
+      auto accumulate = [&](float scale, const uint32_t* d, int c0) {
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          acc[c0 + c] = first ? scale * __uint_as_float(d[c]) : fmaf(scale, __uint_as_float(d[c]), acc[c0 + c]);
+      };
+      auto finish_unit = [&](int i) {
+        first = false;
+        if (--seg_left == 0) {
+          emit_cols<BA, BA>(a, seg, row, 0, acc, bias_f);
+          if (i + 1 < total) open_run();
+        }
+      };
+      const int pairs = (total + 1) >> 1;
+      for (int q = 0; q < pairs; ++q) {
+        const int i0 = 2 * q;
+        const bool has1 = i0 + 1 < total;
+        const int dl = q % DL;
+        prefetch_unit(2 * (q + kScaleAhead));
+        prefetch_unit(2 * (q + kScaleAhead) + 1);
+        ptx::cp_async_commit();
+        ptx::cp_async_wait<kScaleAhead>();   // this pair's copies landed
         __syncwarp();
-        if (lane == 0 && dl == DL - 1) ptx::mbar_arrive(&sh->dempty[p]);
-        if (threadIdx.x == 32 * kReadoutWarp0) W4A16_TRACE_UNIT(7, i);
-        if (u.seg_last) emit_cols<BA, BA>(a, u, row, 0, acc, bias_n);
-      } else {
+        const float s0 = __half2float(__ushort_as_half(sring[(i0 % kScaleRing) * kTileW + row]));
+        const float s1 = __half2float(__ushort_as_half(sring[((i0 + 1) % kScaleRing) * kTileW + row]));
+        if (threadIdx.x == 32 * kReadoutWarp0) W4A16_TRACE_UNIT(12, i0);
+        if (!wait_warp(&sh->pair_done[q % kPairRing], (q / kPairRing) & 1, wc)) break;
+        if (threadIdx.x == 32 * kReadoutWarp0 && q == 0) W4A16_TRACE_POINT(8);
+        if (threadIdx.x == 32 * kReadoutWarp0 && q == pairs - 1) W4A16_TRACE_POINT(9);
+        if (threadIdx.x == 32 * kReadoutWarp0) W4A16_TRACE_UNIT(6, i0);
+        ptx::tc_fence_after();
+        const uint32_t d0 = lane_base + kDCol + (0 + 2 * dl) * BA;
+        const uint32_t d1 = lane_base + kDCol + (1 + 2 * dl) * BA;
+        auto release = [&]() {
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0 && dl == DL - 1) {
+            ptx::mbar_arrive(&sh->dempty[0]);
+            if (has1) ptx::mbar_arrive(&sh->dempty[1]);
+          }
+          if (threadIdx.x == 32 * kReadoutWarp0) W4A16_TRACE_UNIT(7, i0);
+        };
+        if constexpr (BA == 16) {
+          // both accumulators with one TMEM wait
+          uint32_t r0[16], r1[16];
+          ptx::tmem_ld2_x16_sync(d0, d1, r0, r1);
+          release();
+          accumulate(s0, r0, 0);
+          finish_unit(i0);
+          if (has1) {
+            accumulate(s1, r1, 0);
+            finish_unit(i0 + 1);
+          }
+        } else {
+          // one unit at a time, 16 columns per TMEM load
+#pragma unroll 1
+          for (int h = 0; h <= (has1 ? 1 : 0); ++h) {
+#pragma unroll
+            for (int c0 = 0; c0 < BA; c0 += 16) {
+              uint32_t r[16];
+              ptx::tmem_ld_x16_sync((h ? d1 : d0) + c0, r);
+              accumulate(h ? s1 : s0, r, c0);
+            }
+            if (h == (has1 ? 1 : 0)) release();
+            finish_unit(i0 + h);
+          }
+        }
+      }
+      ptx::cp_async_wait<0>();   // no copy may land after exit
+    } else {
+      uint16_t bias_raw = 0;
+      int seg = 0;
+      for (int i = 0; i < total; ++i) {
+        const Unit u = it.next();
+        if (u.seg_first) {
+          const int n = (u.tile % a.n_tiles) * kTileW + row;
+          bias_raw = (a.bias != nullptr && n < a.N) ? __bfloat16_as_ushort(a.bias[n]) : 0;
+        }
         if (!u.seg_last) continue;
         const int db = seg % DB;
         if (!wait_warp(&sh->dfull[db], (seg / DB) & 1, wc)) break;
@@ -687,7 +852,7 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES>::kThreads, 1)
         for (int c0 = 0; c0 < BA; c0 += C::kChunk) {
           float v[C::kChunk];
           load_cols<C::kChunk>(lane_base + kDCol + db * BA + c0, v);
-          emit_cols<BA, C::kChunk>(a, u, row, c0, v, bias_n);
+          emit_cols<BA, C::kChunk>(a, u, row, c0, v, __bfloat162float(__ushort_as_bfloat16(bias_raw)));
         }
         ptx::tc_fence_before();
         __syncwarp();
