@@ -10,35 +10,35 @@
 // 8 KiB tile, tile (tn, g) at (tn * K/128 + g) * 8192, row-major inside; rows
 // past N (up to the next multiple of 128) get zero codes.
 //
-// Work split.  A tile is 64 consecutive rows x one group (64 x 256 B).  A
-// producer thread streams tiles with 2-D TMA loads into a ring of shared-
-// memory stages (up to 96 KiB in flight per CTA, two CTAs per SM); eight
-// consumer warps quantize from shared memory.  One half-warp handles one
-// (row, group): each lane reads 16 bytes (8 bf16) of the row's 256, the
-// group absmax is a 4-step xor-shuffle max inside the half-warp, and each
-// lane writes one 32-bit word of codes (64 contiguous bytes per group).
-// Tiles are numbered row-block fastest, so a CTA's 64 scale stores of one
-// group are contiguous, and its 64 rows of codes are one contiguous 4 KiB
-// run of the tiled layout.  Rows past N arrive zero-filled; their (zero)
-// codes are stored, their scales are not.
+// Work split.  A work tile is exactly one storage tile: 128 consecutive rows
+// x one group (32 KiB of bf16 in, 8 KiB of codes and 256 B of scales out).
+// A producer thread streams tiles with TMA into a ring of shared-memory
+// stages, as two boxes of 128 rows x 64 values with the 128-byte swizzle (so
+// that the per-row reads below hit 32 different banks).  Two teams of eight
+// consumer warps take alternate tiles; in a team a pair of threads owns one
+// row of the tile, i.e. one (row, group), each thread 64 of its values:
+//   pass 1: absmax (packed bf16x2 max of |w|), combined across the pair,
+//           then the scale, once per group;
+//   pass 2: the codes, 8 packed 32-bit words per thread, stored as two
+//           16-byte stores (the tile's 8 KiB are written by its 256 threads).
+// Tiles are numbered group fastest within a 128-row block, so neighbouring
+// CTAs read neighbouring 256-byte pieces of the same rows and write
+// neighbouring 8 KiB blocks.
 //
 // Division.  The codes must equal rint(fl32(w / s)) bit for bit.  All 128
-// elements of a group share s, so the kernel multiplies by r = fl32(1/s)
-// (__frcp_rn) where that provably gives the same integer:
-//  * Let w = X * 2^a (|X| < 2^8: w is bf16) and s = S * 2^b with a normal
-//    fp16 significand 2^10 <= S < 2^11.  If w/s is not itself a half-integer
-//    h, then |w/s - h| = |X 2^(a+1) - (2k+1) S 2^b| / (2 s) is either at
-//    least 2^-12 (when a + 1 >= b) or |w/s| < 1/8 (when a + 1 < b).
-//  * w/s = h exactly needs (2k+1) * (odd part of S) < 2^8, i.e. the odd
-//    part of S below 2^8, i.e. S divisible by 8.
-//  * |w/s| <= amax/s <= 7 / (1 - 2^-11) < 7.5 for a normal scale, so no
-//    clamp is ever active, and |w*r - w/s| <= |w/s| 2^-24 < 2^-21.
-// So for a normal scale whose significand is not a multiple of 8, w*r and
-// fl32(w/s) lie strictly on the same side of every half-integer and round to
-// the same integer; w*r + 1.5 * 2^23 (one fused multiply-add) rounds it, and
-// the low 4 bits of that float are the two's-complement nibble.  Every
-// other group (significand a multiple of 8, subnormal scale, or the zero
-// rule) takes the IEEE division __fdiv_rn and the clamp element by element.
+// values of a group share s, so pass 2 multiplies by r = fl32(1/s) and
+// rounds with one fused multiply-add, y = w * r + 1.5 * 2^23, whose low four
+// bits are the two's-complement nibble of q = y - 1.5 * 2^23.  w * r differs
+// from w / s by at most |w/s| 2^-23, so q is the correct integer unless w / s
+// lies within that distance of a half-integer (a tie included).  Each value
+// checks its own case exactly: e = w - q * s is computed without rounding by
+// one fused multiply-add (w has 8 significant bits, q * s at most 15, and
+// |e| <= s/2 + |w| 2^-22, so the exact difference fits in 24 bits), and
+// |e| < s/2 holds exactly when q is the unique nearest integer to w / s.  A
+// group in which any value fails the check, or whose scale is not a normal
+// fp16 number (where |w / s| may exceed the code range), is recomputed with
+// the IEEE division __fdiv_rn, the clamp and round-half-to-even, value by
+// value.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -55,7 +55,71 @@ namespace {
 
 constexpr float kRoundMagic = 12582912.0f;        // 1.5 * 2^23
 
-__device__ __forceinline__ void unpack_bf16x8(const uint4& v, float (&f)[8]) {
+constexpr int kQRows = 128;                       // rows per tile (one storage tile)
+constexpr int kQBoxBytes = kQRows * 128;          // one box: 128 rows x 64 bf16
+constexpr int kQTileBytes = 2 * kQBoxBytes;       // 32 KiB
+constexpr int kQStages = 6;                       // even: each stage feeds one tile team
+constexpr int kQTeamWarps = 8;                    // a team: 256 threads, two per row
+constexpr int kQConsumerWarps = 2 * kQTeamWarps;  // two teams, alternate tiles
+constexpr int kQThreads = 32 * (kQConsumerWarps + 1);
+
+struct QShared {
+  uint64_t full[kQStages];
+  uint64_t empty[kQStages];
+  uint64_t team_bar[2];          // per team: all 8 warps reached a step (bounded waits)
+  int exact_rows[2][kQTeamWarps];  // per team and warp: rows that need the exact path
+  uint16_t perm[2][kQRows];      // per team: row processed in pass-2 slot j
+  uint16_t sbits[2][kQRows];     // per team: scale of that row (fp16 bits)
+  int abort_flag;
+};
+
+// 16-byte chunk c (0..7) of row r of a 128-byte-swizzled box.
+__device__ __forceinline__ uint32_t chunk_addr(uint32_t box, int r, int c) {
+  return box + r * 128 + ((c ^ (r & 7)) << 4);
+}
+
+// Nibbles of 8 rounded values (float bit patterns, code in the low 4 bits)
+// into one word, code i in nibble i.
+__device__ __forceinline__ uint32_t pack8(const uint32_t (&y)[8]) {
+  uint32_t p[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) p[i] = (y[2 * i] & 0xFu) | ((y[2 * i + 1] << 4) & ~0xFu);
+  const uint32_t lo = ptx::prmt(p[0], p[1], 0x0040);
+  const uint32_t hi = ptx::prmt(p[2], p[3], 0x0040);
+  return ptx::prmt(lo, hi, 0x5410);
+}
+
+// Codes of 8 values when the reciprocal alone is not enough (a normal scale
+// whose significand is a multiple of 8: w / s may be exactly a half-integer).
+// The quotient is corrected to the correctly rounded fl32(w / s) by one
+// remainder step (Markstein: with r the correctly rounded reciprocal, the
+// remainder w - q1 s is exact and q1 + (w - q1 s) r rounds to fl32(w / s)),
+// then rounded half to even.  |w / s| < 7.5, so no clamp is active.
+__device__ __forceinline__ uint32_t codes_corrected(const float (&f)[8], float s, float r) {
+  uint32_t y[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float q1 = __fmul_rn(f[i], r);
+    const float e = fmaf(-q1, s, f[i]);
+    const float q2 = fmaf(e, r, q1);
+    y[i] = __float_as_uint(__fadd_rn(q2, kRoundMagic));
+  }
+  return pack8(y);
+}
+
+// Codes of 8 values for a subnormal scale: IEEE quotient, clamp (|w / s|
+// may exceed the code range), round half to even.
+__device__ __forceinline__ uint32_t codes_exact(const float (&f)[8], float s) {
+  uint32_t y[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float tc = fminf(fmaxf(__fdiv_rn(f[i], s), -8.0f), 7.0f);
+    y[i] = __float_as_uint(__fadd_rn(tc, kRoundMagic));
+  }
+  return pack8(y);
+}
+
+__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -64,51 +128,20 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4& v, float (&f)[8]) {
   }
 }
 
-// Codes of 8 elements from their exact fp32 quotients w / s: clamp, round to
-// nearest even (fp32 addition of 1.5 * 2^23 rounds to an integer), keep the
-// low nibble.
-__device__ __forceinline__ uint32_t codes_exact(const float (&f)[8], float s) {
-  uint32_t word = 0;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float tc = fminf(fmaxf(__fdiv_rn(f[i], s), -8.0f), 7.0f);
-    const float tm = tc + kRoundMagic;
-    word |= (__float_as_uint(tm) & 0xFu) << (4 * i);
-  }
-  return word;
+__device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t acc, uint32_t w) {
+  const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&acc);
+  const __nv_bfloat162 b = __habs2(*reinterpret_cast<const __nv_bfloat162*>(&w));
+  const __nv_bfloat162 m = __hmax2(a, b);
+  return *reinterpret_cast<const uint32_t*>(&m);
 }
 
-// Same codes through the reciprocal (valid when no tie and no clamp can occur;
-// see the derivation at the top of this file).
-__device__ __forceinline__ uint32_t codes_fast(const float (&f)[8], float r) {
-  uint32_t word = 0;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float tm = fmaf(f[i], r, kRoundMagic);
-    word |= (__float_as_uint(tm) & 0xFu) << (4 * i);
-  }
-  return word;
-}
-
-constexpr int kQRows = 64;                  // rows per tile
-constexpr int kQStages = 6;                 // shared-memory ring depth
-constexpr int kQTileBytes = kQRows * 256;   // 64 rows x 128 bf16
-constexpr int kQConsumerWarps = 8;
-constexpr int kQThreads = 32 * (kQConsumerWarps + 1);
-
-struct QShared {
-  uint64_t full[kQStages];
-  uint64_t empty[kQStages];
-  int abort_flag;
-};
-
-__global__ void __launch_bounds__(kQThreads, 2)
-    rtn_quantize_kernel(const __grid_constant__ CUtensorMap tm_w, int N, int K,
+__global__ void __launch_bounds__(kQThreads, 1)
+    rtn_quantize_kernel(const __grid_constant__ CUtensorMap tm_w, int N, int G,
                         uint32_t* __restrict__ packed, __half* __restrict__ scales, int tiles,
-                        int row_blocks, uint32_t* err, uint64_t timeout_ns) {
-  extern __shared__ __align__(128) uint8_t q_smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(q_smem_raw) + 127) &
-                                             ~static_cast<uintptr_t>(127));
+                        uint32_t* err, uint64_t timeout_ns) {
+  extern __shared__ __align__(1024) uint8_t q_smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(q_smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
   QShared* sh = reinterpret_cast<QShared*>(smem + kQStages * kQTileBytes);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -116,8 +149,10 @@ __global__ void __launch_bounds__(kQThreads, 2)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kQStages; ++s) {
       ptx::mbar_init(&sh->full[s], 1);
-      ptx::mbar_init(&sh->empty[s], kQConsumerWarps);
+      ptx::mbar_init(&sh->empty[s], kQTeamWarps);
     }
+    ptx::mbar_init(&sh->team_bar[0], kQTeamWarps);
+    ptx::mbar_init(&sh->team_bar[1], kQTeamWarps);
     sh->abort_flag = 0;
     ptx::fence_mbar_init();
     ptx::prefetch_tmap(&tm_w);
@@ -137,14 +172,16 @@ __global__ void __launch_bounds__(kQThreads, 2)
         const int stage = i % kQStages;
         if (!wait_one(&sh->empty[stage], ((i / kQStages) & 1) ^ 1, wc)) break;
         const int t = static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
-        const int g = t / row_blocks;
-        const int rb = t - g * row_blocks;
+        const int tn = t / G;
+        const int g = t - tn * G;
+        uint8_t* dst = smem + stage * kQTileBytes;
         ptx::mbar_arrive_expect_tx(&sh->full[stage], kQTileBytes);
-        ptx::tma_load_2d(smem + stage * kQTileBytes, &tm_w, &sh->full[stage], g * kGroup,
-                         rb * kQRows);
+        ptx::tma_load_2d(dst, &tm_w, &sh->full[stage], g * kGroup, tn * kQRows);
+        ptx::tma_load_2d(dst + kQBoxBytes, &tm_w, &sh->full[stage], g * kGroup + 64, tn * kQRows);
         issued = i + 1;
       }
       if (*reinterpret_cast<volatile int*>(&sh->abort_flag)) {
+        // let the copies in flight land before the CTA exits
         const int first = issued > kQStages ? issued - kQStages : 0;
         for (int i = first; i < issued; ++i) {
           const uint64_t t0 = ptx::globaltimer_ns();
@@ -157,48 +194,117 @@ __global__ void __launch_bounds__(kQThreads, 2)
   }
 
   // -------------------------------------------------------------- consumers
-  const int hw = warp * 2 + (lane >> 4);          // half-warp 0..15
-  const int lane16 = lane & 15;
-  const uint32_t half_mask = (lane & 16) ? 0xFFFF0000u : 0x0000FFFFu;
-  const int n_groups = K / kGroup;
-  for (int i = 0; i < n_local; ++i) {
+  // Team `team` takes tiles team, team + 2, ...  Pass 1: thread pair
+  // (2 row, 2 row + 1) owns row `row`, half h = box h = values 64 h .. 64 h + 63
+  // (the two halves read their chunks in different orders, so one instruction
+  // never hits the same bank in both boxes).  Rows whose scale needs more
+  // than the reciprocal (about one in eight) are then moved to the last pass-2
+  // slots, so that all but one or two warps run the one-instruction path
+  // without divergence.
+  const int team = warp / kQTeamWarps;
+  const int tw = warp % kQTeamWarps;
+  const int tt = tw * 32 + lane;   // 0..255
+  const int row = tt >> 1;
+  const int h = tt & 1;
+  uint32_t team_phase = 0;
+  auto team_sync = [&]() -> bool {
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(&sh->team_bar[team]);
+    const bool ok = wait_warp(&sh->team_bar[team], team_phase & 1, wc);
+    ++team_phase;
+    return ok;
+  };
+  for (int i = team; i < n_local; i += 2) {
     const int stage = i % kQStages;
     if (!wait_warp(&sh->full[stage], (i / kQStages) & 1, wc)) break;
     const int t = static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
-    const int g = t / row_blocks;
-    const int rb = t - g * row_blocks;
+    const int tn = t / G;
+    const int g = t - tn * G;
     const uint32_t tile = ptx::smem_u32(smem + stage * kQTileBytes);
-#pragma unroll
-    for (int j = 0; j < kQRows / 16; ++j) {
-      const int r = hw + 16 * j;
-      const uint4 v = ptx::lds128(tile + r * 256 + lane16 * 16);
-      float f[8];
-      unpack_bf16x8(v, f);
-      float amax = 0.0f;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(f[e]));
-#pragma unroll
-      for (int off = 8; off >= 1; off >>= 1)
-        amax = fmaxf(amax, __shfl_xor_sync(half_mask, amax, off, 16));
 
-      __half sh16 = __float2half_rn(__fdiv_rn(amax, 7.0f));
-      if (__half_as_ushort(sh16) == 0) sh16 = __ushort_as_half(0x3C00);   // zero rule: 1.0
-      const float s = __half2float(sh16);
-      const uint32_t sbits = __half_as_ushort(sh16);
-      const bool normal = (sbits & 0x7C00u) != 0;
-      uint32_t word;
-      if (normal && (sbits & 7u) != 0) {
-        word = codes_fast(f, __frcp_rn(s));     // significand not a multiple of 8
-      } else {
-        word = codes_exact(f, s);
+    // pass 1: absmax of the row's 128 values (two independent chains per
+    // thread, then across the pair), and the scale
+    {
+      const uint32_t box = tile + h * kQBoxBytes;
+      uint32_t ma = 0, mb = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint4 v = ptx::lds128(chunk_addr(box, row, (j + 4 * h) & 7));
+        ma = bf16x2_absmax(ma, v.x);
+        mb = bf16x2_absmax(mb, v.y);
+        ma = bf16x2_absmax(ma, v.z);
+        mb = bf16x2_absmax(mb, v.w);
       }
-      const int n = rb * kQRows + r;
-      // tiled storage: ((tn * G + g) * 128 + n % 128) rows of 16 words
-      packed[((static_cast<int64_t>(n >> 7) * n_groups + g) * 128 + (n & 127)) * 16 + lane16] = word;
-      if (lane16 == 0 && n < N) scales[static_cast<int64_t>(g) * N + n] = sh16;
+      ma = bf16x2_absmax(ma, mb);
+      float amax = fmaxf(__uint_as_float(ma << 16), __uint_as_float(ma & 0xFFFF0000u));
+      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+      uint32_t sb = __half_as_ushort(__float2half_rn(__fdiv_rn(amax, 7.0f)));
+      if (sb == 0) sb = 0x3C00u;   // zero rule: 1.0
+      // the reciprocal alone is exact only for a normal scale whose
+      // significand is not a multiple of 8
+      const bool slow = ((sb & 0x7C00u) == 0) || ((sb & 7u) == 0);
+      const uint32_t ball = __ballot_sync(0xFFFFFFFFu, h == 0 && slow);
+      if (lane == 0) sh->exact_rows[team][tw] = __popc(ball);
+      if (!team_sync()) break;
+      int before = __popc(ball & ((1u << lane) - 1u)), total = 0;
+#pragma unroll
+      for (int w = 0; w < kQTeamWarps; ++w) {
+        const int c = sh->exact_rows[team][w];
+        total += c;
+        if (w < tw) before += c;
+      }
+      if (h == 0) {
+        const int slot = slow ? (kQRows - total) + before : row - before;
+        sh->perm[team][slot] = static_cast<uint16_t>(row);
+        sh->sbits[team][slot] = static_cast<uint16_t>(sb);
+      }
+      if (!team_sync()) break;
+    }
+
+    // pass 2: slot `row` of the permutation
+    const int prow = sh->perm[team][row];
+    const uint32_t sb = sh->sbits[team][row];
+    const float s = __half2float(__ushort_as_half(static_cast<unsigned short>(sb)));
+    const float r = __frcp_rn(s);
+    const uint32_t box = tile + h * kQBoxBytes;
+    // this half-row's 32 bytes of codes: row `prow` of storage tile (tn, g),
+    // words 8 h .. 8 h + 7
+    uint32_t* const dst = packed + ((static_cast<int64_t>(tn) * G + g) * kQRows + prow) * 16 + 8 * h;
+    const bool normal = (sb & 0x7C00u) != 0;
+    if (normal && (sb & 7u) != 0) {
+      uint32_t words[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        float f[8];
+        unpack8(ptx::lds128(chunk_addr(box, prow, (j + 4 * h) & 7)), f);
+        uint32_t y[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) y[e] = __float_as_uint(fmaf(f[e], r, kRoundMagic));
+        words[j] = pack8(y);   // chunk (j + 4 h) mod 8
+      }
+      const uint4 w0 = make_uint4(words[0], words[1], words[2], words[3]);
+      const uint4 w1 = make_uint4(words[4], words[5], words[6], words[7]);
+      reinterpret_cast<uint4*>(dst)[0] = h ? w1 : w0;
+      reinterpret_cast<uint4*>(dst)[1] = h ? w0 : w1;
+    } else if (normal) {
+#pragma unroll 1
+      for (int c = 0; c < 8; ++c) {
+        float f[8];
+        unpack8(ptx::lds128(chunk_addr(box, prow, c)), f);
+        dst[c] = codes_corrected(f, s, r);
+      }
+    } else {
+#pragma unroll 1
+      for (int c = 0; c < 8; ++c) {
+        float f[8];
+        unpack8(ptx::lds128(chunk_addr(box, prow, c)), f);
+        dst[c] = codes_exact(f, s);
+      }
     }
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(&sh->empty[stage]);
+    const int n = tn * kQRows + prow;
+    if (h == 0 && n < N) scales[static_cast<int64_t>(g) * N + n] = __ushort_as_half(static_cast<unsigned short>(sb));
   }
 }
 
@@ -207,15 +313,16 @@ __global__ void __launch_bounds__(kQThreads, 2)
 cudaError_t launch_rtn_quantize(const void* W, int64_t N, int64_t K, void* packed, void* scales,
                                 int num_sms, uint32_t* error_word, uint64_t timeout_ns,
                                 cudaStream_t stream) {
+  // the weight as [N][K] bf16; boxes of 128 rows x 64 values, 128-byte
+  // swizzle; rows past N read as zeros
   CUtensorMap tm_w;
   if (encode_tmap_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, static_cast<uint64_t>(K),
-                     static_cast<uint64_t>(N), static_cast<uint64_t>(K) * 2, kGroup, kQRows,
-                     CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
+                     static_cast<uint64_t>(N), static_cast<uint64_t>(K) * 2, 64, kQRows,
+                     CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
-  // row blocks cover the rows padded to a multiple of 128 (tile height)
-  const int row_blocks = static_cast<int>((N + 127) / 128) * (128 / kQRows);
-  const int tiles = row_blocks * static_cast<int>(K / kGroup);
-  constexpr size_t smem = static_cast<size_t>(kQStages) * kQTileBytes + sizeof(QShared) + 128;
+  const int G = static_cast<int>(K / kGroup);
+  const int tiles = static_cast<int>((N + kQRows - 1) / kQRows) * G;
+  constexpr size_t smem = static_cast<size_t>(kQStages) * kQTileBytes + sizeof(QShared) + 1024;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -227,17 +334,16 @@ cudaError_t launch_rtn_quantize(const void* W, int64_t N, int64_t K, void* packe
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  int grid = 2 * num_sms;
+  int grid = num_sms;
   if (grid > tiles) grid = tiles;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(kQThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  return cudaLaunchKernelEx(&cfg, rtn_quantize_kernel, tm_w, static_cast<int>(N),
-                            static_cast<int>(K), static_cast<uint32_t*>(packed),
-                            static_cast<__half*>(scales), tiles, row_blocks, error_word,
-                            timeout_ns);
+  return cudaLaunchKernelEx(&cfg, rtn_quantize_kernel, tm_w, static_cast<int>(N), G,
+                            static_cast<uint32_t*>(packed), static_cast<__half*>(scales), tiles,
+                            error_word, timeout_ns);
 }
 
 }  // namespace w4a16
