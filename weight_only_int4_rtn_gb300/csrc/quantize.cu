@@ -159,7 +159,11 @@ __global__ void __launch_bounds__(kQThreads, 1)
   }
   __syncthreads();
   const WaitCtx wc{err, timeout_ns, &sh->abort_flag};
+  // The weight may be written by the previous kernel on the stream; the next
+  // kernel may start its own set-up now (it waits for this grid to complete
+  // before it reads anything this kernel writes).
   ptx::grid_dependency_wait();
+  ptx::grid_launch_dependents();
 
   const int n_local = (tiles - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
                       static_cast<int>(gridDim.x);
@@ -341,6 +345,12 @@ cudaError_t launch_rtn_quantize(const void* W, int64_t N, int64_t K, void* packe
   cfg.blockDim = dim3(kQThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
+  // programmatic dependent launch: set-up overlaps the previous kernel's tail
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, rtn_quantize_kernel, tm_w, static_cast<int>(N), G,
                             static_cast<uint32_t*>(packed), static_cast<__half*>(scales), tiles,
                             error_word, timeout_ns);
