@@ -62,8 +62,9 @@
 //               (shared memory) -> weight operand (TMEM)
 // A warp may only touch TMEM lanes 32 * (warp % 4) .. + 31, so each readout
 // and dequant thread owns weight row 32 * (warp % 4) + lane.  The dequant
-// warps never wait on accumulators: they run up to four units ahead of the
-// MMA, which runs up to the accumulator count ahead of the readout.
+// warps never wait on accumulators: they run up to the TMEM weight-stage
+// count ahead of the MMA, which runs up to the accumulator count ahead of the
+// readout.
 //
 // Every wait on an mbarrier is bounded by a time limit; on expiry the kernel
 // records an error word, lets every role leave its loop, waits (bounded) for
@@ -107,10 +108,8 @@ namespace {
 constexpr int kUnitK = 128;                    // K values per unit (one group)
 constexpr int kWBytes = kTileW * kUnitK / 2;   // packed codes per unit: 8 KiB
 constexpr int kSBytes = kTileW * 2;            // scales per unit: 256 B
-constexpr int kAStages = 4;                    // weight-operand stages in TMEM
+constexpr int kMaxAStages = 6;                 // weight-operand stages in TMEM (at most)
 constexpr int kAStageCols = kUnitK / 2;        // 64 TMEM columns per stage
-constexpr int kDCol = kAStages * kAStageCols;  // accumulators start at column 256
-constexpr int kDCols = 512 - kDCol;            // 256 accumulator columns
 constexpr uint32_t kTmemCols = 512;
 constexpr int kWarps = 16;
 constexpr int kReadoutWarp0 = 3;
@@ -270,7 +269,7 @@ __device__ __forceinline__ int sk_owner(int u, int C, int sk_units) {
 
 struct Shared {
   uint64_t full[16];          // a shared-memory stage's copies landed
-  uint64_t afull[kAStages];   // a TMEM weight stage is written
+  uint64_t afull[kMaxAStages];   // a TMEM weight stage is written
   uint64_t unit_done[32];     // per lane a ring: a unit's MMAs completed
   uint64_t dfull[8];          // dequant mode: a run on a tile is accumulated
   uint64_t dempty[8];         // the readout drained accumulator buffer(s)
@@ -316,7 +315,13 @@ struct Cfg {
   static constexpr int kStage = (kStageRaw + 1023) / 1024 * 1024;
   static constexpr int kThreads = 32 * kWarps;                    // 16 warps: <= 128 registers
   static constexpr int kSL = STAGES / L;                          // shared-memory stages per lane
-  static constexpr int kAL = kAStages / L;                        // TMEM weight stages per lane
+  // TMEM: kAS weight stages of 64 columns, then the accumulators.  The
+  // narrowest group-mode tile needs few accumulator columns, so it takes
+  // three weight stages per lane (the dequant runs further ahead).
+  static constexpr int kAS = (GRP && BA == 16) ? 6 : 4;
+  static constexpr int kDCol = kAS * kAStageCols;
+  static constexpr int kDCols = 512 - kDCol;
+  static constexpr int kAL = kAS / L;                             // TMEM weight stages per lane
   static constexpr int kDBfit = kDCols / BA;                      // accumulators that fit
   static constexpr int kDB = kDBfit < (GRP ? 8 : 4) ? kDBfit : (GRP ? 8 : 4);
   static constexpr int kDL = kDB / L;                             // accumulator buffers per lane
@@ -535,10 +540,11 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES>::kThreads, 1)
   unsigned long long* const trace_unit = blockIdx.x == 0 ? g_trace_units : nullptr;
 #endif
   if (threadIdx.x == 0) W4A16_TRACE_POINT(0);
+  if (threadIdx.x == 0) W4A16_TRACE_UNIT(9, 0);
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) ptx::mbar_init(&sh->full[s], 1);
     for (int s = 0; s < L * RL; ++s) ptx::mbar_init(&sh->unit_done[s], 1);
-    for (int s = 0; s < kAStages; ++s) ptx::mbar_init(&sh->afull[s], 4);
+    for (int s = 0; s < C::kAS; ++s) ptx::mbar_init(&sh->afull[s], 4);
     for (int s = 0; s < DB; ++s) {
       ptx::mbar_init(&sh->dfull[s], 1);
       ptx::mbar_init(&sh->dempty[s], 4);
@@ -564,16 +570,19 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES>::kThreads, 1)
   const WaitCtx wc{a.err, a.timeout_ns, &sh->abort_flag};
 
   if (threadIdx.x == 0) W4A16_TRACE_POINT(1);
-  // Inputs may be produced by the previous kernel on the stream.
-  ptx::grid_dependency_wait();
-  ptx::grid_launch_dependents();
-  if (threadIdx.x == 0) W4A16_TRACE_POINT(2);
-
+  if (threadIdx.x == 0) W4A16_TRACE_UNIT(9, 1);
+  // The schedule depends on the launch only, so it is worked out while the
+  // previous kernel on the stream may still run; the inputs may be that
+  // kernel's outputs, so nothing is read before the dependency wait.
   Sched sched;
   sched.init(a);
   UnitIter it;
   it.init(sched);
   const int total = sched.total;
+  ptx::grid_dependency_wait();
+  ptx::grid_launch_dependents();
+  if (threadIdx.x == 0) W4A16_TRACE_POINT(2);
+  if (threadIdx.x == 0) W4A16_TRACE_UNIT(9, 2);
 
   if (warp == 0 || warp == 2) {
     // ----------------------------------------------------- TMA producers
@@ -588,19 +597,24 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES>::kThreads, 1)
         const int stage = stage_of(i);
         // the unit that last used this stage is i - STAGES (same lane)
         if (i >= STAGES && !wait_one(done_bar(i - STAGES), done_parity(i - STAGES), wc)) break;
+        if (i == 0) W4A16_TRACE_UNIT(9, 3);
         const int m0 = (u.tile / a.n_tiles) * BA;
         ptx::mbar_arrive_expect_tx(&sh->full[stage], C::kTx);
+        if (i == 0) W4A16_TRACE_UNIT(9, 4);
         if (a.act_3d) {
           ptx::tma_load_3d(act_box(stage, 0), &tm_act, &sh->full[stage], 0, m0, u.kb * 2);
         } else {
           ptx::tma_load_2d(act_box(stage, 0), &tm_act, &sh->full[stage], u.kb * kUnitK, m0);
           ptx::tma_load_2d(act_box(stage, 1), &tm_act, &sh->full[stage], u.kb * kUnitK + 64, m0);
         }
+        if (i == 0) W4A16_TRACE_UNIT(9, 5);
         // the unit's codes: one contiguous 8 KiB tile of the tiled storage
         ptx::tma_load_2d(w_tile(stage), &tm_w, &sh->full[stage], 0,
                          ((u.tile % a.n_tiles) * a.KB + u.kb) * kTileW);
+        if (i == 0) W4A16_TRACE_UNIT(9, 6);
         ptx::tma_load_2d(s_tile(stage), &tm_s, &sh->full[stage], (u.tile % a.n_tiles) * kTileW,
                          u.kb);
+        if (i == 0) W4A16_TRACE_UNIT(9, 7);
         if (i <= 1) W4A16_TRACE_POINT(3);
         W4A16_TRACE_UNIT(0, i);
         issued = i;
@@ -640,7 +654,7 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES>::kThreads, 1)
           ptx::tc_fence_after();
           if (j == 0) W4A16_TRACE_POINT(4);
           W4A16_TRACE_UNIT(4, 2 * j + mine);
-          const uint32_t d_tmem = tmem + kDCol + (mine + 2 * dl) * BA;
+          const uint32_t d_tmem = tmem + C::kDCol + (mine + 2 * dl) * BA;
           const uint32_t a_tmem = tmem + as * kAStageCols;
           const uint32_t b0 = smem0 + stage * C::kStage;
 #pragma unroll
@@ -677,7 +691,7 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES>::kThreads, 1)
           if (i == 0) W4A16_TRACE_POINT(4);
           if (i == total - 1) W4A16_TRACE_POINT(5);
           W4A16_TRACE_UNIT(4, i);
-          const uint32_t d_tmem = tmem + kDCol + db * BA;
+          const uint32_t d_tmem = tmem + C::kDCol + db * BA;
           const uint32_t a_tmem = tmem + as * kAStageCols;
           const uint32_t b0 = smem0 + stage * C::kStage;
   #pragma unroll
@@ -796,8 +810,8 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES>::kThreads, 1)
         if (threadIdx.x == 32 * kReadoutWarp0 && q == pairs - 1) W4A16_TRACE_POINT(9);
         if (threadIdx.x == 32 * kReadoutWarp0) W4A16_TRACE_UNIT(6, i0);
         ptx::tc_fence_after();
-        const uint32_t d0 = lane_base + kDCol + (0 + 2 * dl) * BA;
-        const uint32_t d1 = lane_base + kDCol + (1 + 2 * dl) * BA;
+        const uint32_t d0 = lane_base + C::kDCol + (0 + 2 * dl) * BA;
+        const uint32_t d1 = lane_base + C::kDCol + (1 + 2 * dl) * BA;
         auto release = [&]() {
           ptx::tc_fence_before();
           __syncwarp();
@@ -851,7 +865,7 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES>::kThreads, 1)
 #pragma unroll 1
         for (int c0 = 0; c0 < BA; c0 += C::kChunk) {
           float v[C::kChunk];
-          load_cols<C::kChunk>(lane_base + kDCol + db * BA + c0, v);
+          load_cols<C::kChunk>(lane_base + C::kDCol + db * BA + c0, v);
           emit_cols<BA, C::kChunk>(a, u, row, c0, v, __bfloat162float(__ushort_as_bfloat16(bias_raw)));
         }
         ptx::tc_fence_before();
@@ -903,8 +917,8 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES>::kThreads, 1)
       if constexpr (!GRP) scale = __half2float(s_tile(stage)[row]);
 
       // the TMEM stage is free once the MMAs of the unit that used it
-      // (i - kAStages, same lane) completed
-      if (i >= kAStages && !wait_warp(done_bar(i - kAStages), done_parity(i - kAStages), wc)) break;
+      // (i - kAS, same lane) completed
+      if (i >= C::kAS && !wait_warp(done_bar(i - C::kAS), done_parity(i - C::kAS), wc)) break;
       if (threadIdx.x == 32 * kDequantWarp0) W4A16_TRACE_UNIT(2, i);
       ptx::tc_fence_after();
       const uint32_t a_addr = lane_base + as * kAStageCols;
