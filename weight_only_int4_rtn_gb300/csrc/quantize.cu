@@ -25,20 +25,16 @@
 // CTAs read neighbouring 256-byte pieces of the same rows and write
 // neighbouring 8 KiB blocks.
 //
-// Division.  The codes must equal rint(fl32(w / s)) bit for bit.  All 128
-// values of a group share s, so pass 2 multiplies by r = fl32(1/s) and
-// rounds with one fused multiply-add, y = w * r + 1.5 * 2^23, whose low four
-// bits are the two's-complement nibble of q = y - 1.5 * 2^23.  w * r differs
-// from w / s by at most |w/s| 2^-23, so q is the correct integer unless w / s
-// lies within that distance of a half-integer (a tie included).  Each value
-// checks its own case exactly: e = w - q * s is computed without rounding by
-// one fused multiply-add (w has 8 significant bits, q * s at most 15, and
-// |e| <= s/2 + |w| 2^-22, so the exact difference fits in 24 bits), and
-// |e| < s/2 holds exactly when q is the unique nearest integer to w / s.  A
-// group in which any value fails the check, or whose scale is not a normal
-// fp16 number (where |w / s| may exceed the code range), is recomputed with
-// the IEEE division __fdiv_rn, the clamp and round-half-to-even, value by
-// value.
+// Division.  The codes must equal rint_even(fl32(w / s)) bit for bit.  All
+// 128 values of a group share s, so r = fl32(1/s) is computed once, and per
+// value the quotient is q1 = fl32(w r), the remainder e = w - q1 s (exact:
+// one fused multiply-add) and q2 = fl32(q1 + e r).  With r the correctly
+// rounded reciprocal this one correction gives the correctly rounded quotient
+// q2 = fl32(w / s) (Markstein's theorem), which a fused add of 1.5 * 2^23
+// rounds half to even; the low four bits of that float are the code's
+// two's-complement nibble.  For a normal scale |w / s| <= 7 (1 + 2^-11) < 7.5,
+// so no clamp can be active.  A subnormal scale (rare) takes the IEEE
+// division __fdiv_rn and the clamp value by value.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -66,10 +62,6 @@ constexpr int kQThreads = 32 * (kQConsumerWarps + 1);
 struct QShared {
   uint64_t full[kQStages];
   uint64_t empty[kQStages];
-  uint64_t team_bar[2];          // per team: all 8 warps reached a step (bounded waits)
-  int exact_rows[2][kQTeamWarps];  // per team and warp: rows that need the exact path
-  uint16_t perm[2][kQRows];      // per team: row processed in pass-2 slot j
-  uint16_t sbits[2][kQRows];     // per team: scale of that row (fp16 bits)
   int abort_flag;
 };
 
@@ -89,12 +81,11 @@ __device__ __forceinline__ uint32_t pack8(const uint32_t (&y)[8]) {
   return ptx::prmt(lo, hi, 0x5410);
 }
 
-// Codes of 8 values when the reciprocal alone is not enough (a normal scale
-// whose significand is a multiple of 8: w / s may be exactly a half-integer).
-// The quotient is corrected to the correctly rounded fl32(w / s) by one
-// remainder step (Markstein: with r the correctly rounded reciprocal, the
-// remainder w - q1 s is exact and q1 + (w - q1 s) r rounds to fl32(w / s)),
-// then rounded half to even.  |w / s| < 7.5, so no clamp is active.
+// Codes of 8 values for a normal scale: the quotient corrected to the
+// correctly rounded fl32(w / s) by one remainder step (Markstein: with r the
+// correctly rounded reciprocal, the remainder w - q1 s is exact and
+// q1 + (w - q1 s) r rounds to fl32(w / s)), then rounded half to even.
+// |w / s| < 7.5, so no clamp is active.
 __device__ __forceinline__ uint32_t codes_corrected(const float (&f)[8], float s, float r) {
   uint32_t y[8];
 #pragma unroll
@@ -151,8 +142,6 @@ __global__ void __launch_bounds__(kQThreads, 1)
       ptx::mbar_init(&sh->full[s], 1);
       ptx::mbar_init(&sh->empty[s], kQTeamWarps);
     }
-    ptx::mbar_init(&sh->team_bar[0], kQTeamWarps);
-    ptx::mbar_init(&sh->team_bar[1], kQTeamWarps);
     sh->abort_flag = 0;
     ptx::fence_mbar_init();
     ptx::prefetch_tmap(&tm_w);
@@ -198,117 +187,69 @@ __global__ void __launch_bounds__(kQThreads, 1)
   }
 
   // -------------------------------------------------------------- consumers
-  // Team `team` takes tiles team, team + 2, ...  Pass 1: thread pair
-  // (2 row, 2 row + 1) owns row `row`, half h = box h = values 64 h .. 64 h + 63
-  // (the two halves read their chunks in different orders, so one instruction
-  // never hits the same bank in both boxes).  Rows whose scale needs more
-  // than the reciprocal (about one in eight) are then moved to the last pass-2
-  // slots, so that all but one or two warps run the one-instruction path
-  // without divergence.
+  // Team `team` takes tiles team, team + 2, ...  Thread pair (2 row, 2 row + 1)
+  // owns row `row`: half h = box h = values 64 h .. 64 h + 63 (the two halves
+  // read their chunks in different orders, so one instruction never hits the
+  // same bank in both boxes).
   const int team = warp / kQTeamWarps;
-  const int tw = warp % kQTeamWarps;
-  const int tt = tw * 32 + lane;   // 0..255
+  const int tt = (warp % kQTeamWarps) * 32 + lane;   // 0..255
   const int row = tt >> 1;
   const int h = tt & 1;
-  uint32_t team_phase = 0;
-  auto team_sync = [&]() -> bool {
-    __syncwarp();
-    if (lane == 0) ptx::mbar_arrive(&sh->team_bar[team]);
-    const bool ok = wait_warp(&sh->team_bar[team], team_phase & 1, wc);
-    ++team_phase;
-    return ok;
-  };
   for (int i = team; i < n_local; i += 2) {
     const int stage = i % kQStages;
     if (!wait_warp(&sh->full[stage], (i / kQStages) & 1, wc)) break;
     const int t = static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
     const int tn = t / G;
     const int g = t - tn * G;
-    const uint32_t tile = ptx::smem_u32(smem + stage * kQTileBytes);
+    const uint32_t box = ptx::smem_u32(smem + stage * kQTileBytes) + h * kQBoxBytes;
 
     // pass 1: absmax of the row's 128 values (two independent chains per
     // thread, then across the pair), and the scale
-    {
-      const uint32_t box = tile + h * kQBoxBytes;
-      uint32_t ma = 0, mb = 0;
+    uint32_t ma = 0, mb = 0;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const uint4 v = ptx::lds128(chunk_addr(box, row, (j + 4 * h) & 7));
-        ma = bf16x2_absmax(ma, v.x);
-        mb = bf16x2_absmax(mb, v.y);
-        ma = bf16x2_absmax(ma, v.z);
-        mb = bf16x2_absmax(mb, v.w);
-      }
-      ma = bf16x2_absmax(ma, mb);
-      float amax = fmaxf(__uint_as_float(ma << 16), __uint_as_float(ma & 0xFFFF0000u));
-      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-      uint32_t sb = __half_as_ushort(__float2half_rn(__fdiv_rn(amax, 7.0f)));
-      if (sb == 0) sb = 0x3C00u;   // zero rule: 1.0
-      // the reciprocal alone is exact only for a normal scale whose
-      // significand is not a multiple of 8
-      const bool slow = ((sb & 0x7C00u) == 0) || ((sb & 7u) == 0);
-      const uint32_t ball = __ballot_sync(0xFFFFFFFFu, h == 0 && slow);
-      if (lane == 0) sh->exact_rows[team][tw] = __popc(ball);
-      if (!team_sync()) break;
-      int before = __popc(ball & ((1u << lane) - 1u)), total = 0;
-#pragma unroll
-      for (int w = 0; w < kQTeamWarps; ++w) {
-        const int c = sh->exact_rows[team][w];
-        total += c;
-        if (w < tw) before += c;
-      }
-      if (h == 0) {
-        const int slot = slow ? (kQRows - total) + before : row - before;
-        sh->perm[team][slot] = static_cast<uint16_t>(row);
-        sh->sbits[team][slot] = static_cast<uint16_t>(sb);
-      }
-      if (!team_sync()) break;
+    for (int j = 0; j < 8; ++j) {
+      const uint4 v = ptx::lds128(chunk_addr(box, row, (j + 4 * h) & 7));
+      ma = bf16x2_absmax(ma, v.x);
+      mb = bf16x2_absmax(mb, v.y);
+      ma = bf16x2_absmax(ma, v.z);
+      mb = bf16x2_absmax(mb, v.w);
     }
-
-    // pass 2: slot `row` of the permutation
-    const int prow = sh->perm[team][row];
-    const uint32_t sb = sh->sbits[team][row];
-    const float s = __half2float(__ushort_as_half(static_cast<unsigned short>(sb)));
+    ma = bf16x2_absmax(ma, mb);
+    float amax = fmaxf(__uint_as_float(ma << 16), __uint_as_float(ma & 0xFFFF0000u));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+    __half s16 = __float2half_rn(__fdiv_rn(amax, 7.0f));
+    if (__half_as_ushort(s16) == 0) s16 = __ushort_as_half(0x3C00);   // zero rule: 1.0
+    const float s = __half2float(s16);
     const float r = __frcp_rn(s);
-    const uint32_t box = tile + h * kQBoxBytes;
-    // this half-row's 32 bytes of codes: row `prow` of storage tile (tn, g),
-    // words 8 h .. 8 h + 7
-    uint32_t* const dst = packed + ((static_cast<int64_t>(tn) * G + g) * kQRows + prow) * 16 + 8 * h;
-    const bool normal = (sb & 0x7C00u) != 0;
-    if (normal && (sb & 7u) != 0) {
+
+    // pass 2: the codes.  The quotient is corrected to fl32(w / s) for every
+    // normal scale (no divergence between rows); a subnormal scale takes the
+    // IEEE division and the clamp.
+    uint32_t* const dst = packed + ((static_cast<int64_t>(tn) * G + g) * kQRows + row) * 16 + 8 * h;
+    if ((__half_as_ushort(s16) & 0x7C00u) != 0) {
       uint32_t words[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         float f[8];
-        unpack8(ptx::lds128(chunk_addr(box, prow, (j + 4 * h) & 7)), f);
-        uint32_t y[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) y[e] = __float_as_uint(fmaf(f[e], r, kRoundMagic));
-        words[j] = pack8(y);   // chunk (j + 4 h) mod 8
+        unpack8(ptx::lds128(chunk_addr(box, row, (j + 4 * h) & 7)), f);
+        words[j] = codes_corrected(f, s, r);   // chunk (j + 4 h) mod 8
       }
       const uint4 w0 = make_uint4(words[0], words[1], words[2], words[3]);
       const uint4 w1 = make_uint4(words[4], words[5], words[6], words[7]);
       reinterpret_cast<uint4*>(dst)[0] = h ? w1 : w0;
       reinterpret_cast<uint4*>(dst)[1] = h ? w0 : w1;
-    } else if (normal) {
-#pragma unroll 1
-      for (int c = 0; c < 8; ++c) {
-        float f[8];
-        unpack8(ptx::lds128(chunk_addr(box, prow, c)), f);
-        dst[c] = codes_corrected(f, s, r);
-      }
     } else {
 #pragma unroll 1
       for (int c = 0; c < 8; ++c) {
         float f[8];
-        unpack8(ptx::lds128(chunk_addr(box, prow, c)), f);
+        unpack8(ptx::lds128(chunk_addr(box, row, c)), f);
         dst[c] = codes_exact(f, s);
       }
     }
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(&sh->empty[stage]);
-    const int n = tn * kQRows + prow;
-    if (h == 0 && n < N) scales[static_cast<int64_t>(g) * N + n] = __ushort_as_half(static_cast<unsigned short>(sb));
+    const int n = tn * kQRows + row;
+    if (h == 0 && n < N) scales[static_cast<int64_t>(g) * N + n] = s16;
   }
 }
 
