@@ -192,7 +192,8 @@ def run_gpu(args, rank, world):
     per_copy = sum(2 * c.N * c.K + c.N * c.K // 2 + 2 * c.N * c.K // 128 + 2 * c.M * c.K +
                    2 * c.M * c.N for c in cases)
     copies = max(1, min(64, -(-3 * L2_BYTES // per_copy)))
-    host_sets = [synthetic.draw(c) for c in cases]
+    host_sets = [synthetic.draw(c, act=args.act) for c in cases]
+    act_dtype = torch.float16 if args.act == "f16" else torch.bfloat16
     sets = []
     for r in range(copies):
         s = []
@@ -203,7 +204,7 @@ def run_gpu(args, rank, world):
                           packed=torch.empty(w4.w4a16_packed_bytes(c.N, c.K), dtype=torch.uint8,
                                              device=dev),
                           scales=torch.empty(c.K // 128, c.N, dtype=torch.float16, device=dev),
-                          Y=torch.empty(c.M, c.N, dtype=torch.bfloat16, device=dev)))
+                          Y=torch.empty(c.M, c.N, dtype=act_dtype, device=dev)))
         sets.append(s)
     ws_bytes = max(w4.w4a16_gemm_workspace_bytes_max(c.M, c.N, c.K) for c in cases)
     ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
@@ -320,7 +321,7 @@ def run_gpu(args, rank, world):
 
     # --- e2e: pinned host inputs -> device, the path, result -> host
     pinned = [(W.pin_memory(), A.pin_memory()) for (W, A, b) in host_sets]
-    yh = [torch.empty(c.M, c.N, dtype=torch.bfloat16).pin_memory() for c in cases]
+    yh = [torch.empty(c.M, c.N, dtype=act_dtype).pin_memory() for c in cases]
     h2d = sum(W.numel() * 2 + A.numel() * 2 for W, A in pinned)
     d2h = sum(c.M * c.N * 2 for c in cases)
     s0 = sets[0]
@@ -394,8 +395,8 @@ def run_gpu(args, rank, world):
 
     out = dict(metric=METRIC, value=round(value, 2), unit="GB/s", n_gpus=world, steps=args.steps,
                warmup=args.warmup, ms_per_step=round(ms_step, 5), higher_is_better=True,
-               scaling="weak", vs_baseline=None, dtype="bf16", data="synthetic",
-               config=dict(workload=args.workload,
+               scaling="weak", vs_baseline=None, dtype=args.act, data="synthetic",
+               config=dict(workload=args.workload, activations=args.act,
                            shapes=[[c.M, c.N, c.K] for c in cases],
                            step="rtn_quantize + w4a16_gemm per projection",
                            l2="inputs rotate over %d copies (%.0f MB > 3x L2)" % (copies, copies * per_copy / 2**20),
@@ -452,6 +453,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="expert_m50",
                     choices=["tiny", "expert_m50", "prefix_m816", "sweep", "large"])
+    ap.add_argument("--act", default="bf16", choices=["bf16", "f16"],
+                    help="activation type of the GEMMs (A, bias, Y)")
     ap.add_argument("--tune", action="store_true", help="tune the variant table first")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -129,6 +129,20 @@ int w4a16_gemm(const void* A_bf16, int64_t M, int64_t N, int64_t K, const void* 
                const void* scales, int group, const void* bias_bf16_or_null, void* Y_bf16,
                void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * W4A16 GEMM with FP16 activations ("Kernel dispatch and Humming quantization
+ * in PhyAI", section "Humming makes the separation useful": activations stay
+ * BF16 or FP16).  Same operation, packed codes, scales, shape limits,
+ * workspace and calling conventions as w4a16_gemm, with A [M, K], bias [N]
+ * and Y [M, N] in fp16: Y = fp16( A . dequant(packed, scales)^T + bias ),
+ * fp32 accumulation, bias added in fp32 before the one final rounding.  The
+ * weight operand enters the tensor cores as fp16 (exact integer codes with
+ * the group scale applied in fp32, or fp16_rn(q * s)).
+ */
+int w4a16_gemm_f16(const void* A_f16, int64_t M, int64_t N, int64_t K, const void* packed,
+                   const void* scales, int group, const void* bias_f16_or_null, void* Y_f16,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
 /* ---------------------------------------------------------------- variants
  * The GEMM catalogue holds several kernel configurations (activation-tile
  * width, scaling mode, schedule).  The table maps a shape to one of them; it
@@ -157,6 +171,12 @@ int w4a16_gemm_variant(int variant, const void* A_bf16, int64_t M, int64_t N, in
                        const void* packed, const void* scales, int group,
                        const void* bias_bf16_or_null, void* Y_bf16, void* workspace,
                        size_t workspace_bytes, void* stream);
+
+/* w4a16_gemm_f16 with an explicit variant.  Same contract. */
+int w4a16_gemm_variant_f16(int variant, const void* A_f16, int64_t M, int64_t N, int64_t K,
+                           const void* packed, const void* scales, int group,
+                           const void* bias_f16_or_null, void* Y_f16, void* workspace,
+                           size_t workspace_bytes, void* stream);
 
 /*
  * Time every eligible variant on synthetic device buffers of this shape

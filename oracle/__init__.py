@@ -7,8 +7,10 @@ from .w4a16_oracle import (  # noqa: F401
     TILE_ROWS,
     QMAX,
     QMIN,
+    act_bits_to_f32,
     bf16_bits_to_f32,
     dequantize,
+    f16_bits_to_f32,
     from_tile_layout,
     gemm,
     pack_codes,

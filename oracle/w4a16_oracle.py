@@ -43,7 +43,11 @@ reason in the design notes of the repository):
 6. Groups are contiguous runs of 128 along K, starting at k = 0, per row n.
 7. Dequantized weight = float(code) * float(scale), exact in fp32.
 8. GEMM: ``Y = A @ dequant(W)^T (+ bias)`` accumulated in FP32, bias added in
-   FP32; the oracle returns the FP32 result (the library rounds it to BF16).
+   FP32; the oracle returns the FP32 result (the library rounds it once to
+   the activation type).
+9. Activations, bias and output are BF16, or FP16 for the FP16-activation
+   GEMM (the same page allows BF16 or FP16 activations); either widens to
+   fp32 exactly.
 
 Every function here is pinned by ``tests/test_oracle_pins.py`` against values
 that do not come from this module: hand-worked examples, exact rational
@@ -64,6 +68,20 @@ def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
     half of an IEEE binary32."""
     b = np.ascontiguousarray(bits, dtype=np.uint16)
     return (b.astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def f16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    """Widen IEEE binary16 bit patterns (uint16) to float32 (exact)."""
+    return np.ascontiguousarray(bits, dtype=np.uint16).view(np.float16).astype(np.float32)
+
+
+def act_bits_to_f32(bits: np.ndarray, act: str = "bf16") -> np.ndarray:
+    """Activation bit patterns of type ``act`` ("bf16" or "f16") to float32."""
+    if act == "bf16":
+        return bf16_bits_to_f32(bits)
+    if act == "f16":
+        return f16_bits_to_f32(bits)
+    raise ValueError(f"unknown activation type {act!r}")
 
 
 def quantize_f32(x: np.ndarray, group: int = GROUP):
@@ -187,14 +205,15 @@ def dequantize(packed: np.ndarray, scale_bits: np.ndarray, group: int = GROUP) -
 
 def gemm(a_bits: np.ndarray, packed: np.ndarray, scale_bits: np.ndarray,
          bias_bits: np.ndarray | None = None, group: int = GROUP,
-         rows: np.ndarray | None = None) -> np.ndarray:
+         rows: np.ndarray | None = None, act: str = "bf16") -> np.ndarray:
     """``Y[M, N] = A[M, K] @ dequant(W)[N, K]^T (+ bias[N])`` in FP32.
 
-    ``a_bits`` and ``bias_bits`` are bf16 bit patterns.  ``rows`` (optional)
-    selects the rows of A to evaluate, for sampled checks of large cases.
-    Returns float32; the library's output is that value rounded to bf16.
+    ``a_bits`` and ``bias_bits`` are bit patterns of the activation type
+    ``act`` ("bf16" or "f16").  ``rows`` (optional) selects the rows of A to
+    evaluate, for sampled checks of large cases.  Returns float32; the
+    library's output is that value rounded once to the activation type.
     """
-    a = bf16_bits_to_f32(a_bits)
+    a = act_bits_to_f32(a_bits, act)
     if rows is not None:
         a = a[np.asarray(rows)]
     wd = dequantize(packed, scale_bits, group)
@@ -202,5 +221,5 @@ def gemm(a_bits: np.ndarray, packed: np.ndarray, scale_bits: np.ndarray,
         raise ValueError("A and W disagree on K")
     y = np.matmul(a, wd.T, dtype=np.float32)
     if bias_bits is not None:
-        y = y + bf16_bits_to_f32(bias_bits)[None, :]
+        y = y + act_bits_to_f32(bias_bits, act)[None, :]
     return y.astype(np.float32)

@@ -258,14 +258,16 @@ def exact_gemm(a: np.ndarray, wd: np.ndarray, bias=None) -> np.ndarray:
     return y
 
 
-def check_gemm_exact_bound(orc, a_bits, w_bits, bias_bits=None):
+def check_gemm_exact_bound(orc, a_bits, w_bits, bias_bits=None, act="bf16"):
     """|Y_oracle - Y_exact| <= gamma_{K+1} * (sum |a w| + |b|): the a-priori
-    bound of any FP32 summation order."""
+    bound of any FP32 summation order.  ``act``: type of the activation and
+    bias bit patterns ("bf16" or "f16")."""
     packed, sbits = orc.quantize(w_bits)
     wd = orc.dequantize(packed, sbits).astype(np.float64)
-    a = _bits_f64(a_bits)
-    b = None if bias_bits is None else _bits_f64(bias_bits)
-    y = orc.gemm(a_bits, packed, sbits, bias_bits).astype(np.float64)
+    a = _bits_f64(a_bits, act)
+    b = None if bias_bits is None else _bits_f64(bias_bits, act)
+    y = (orc.gemm(a_bits, packed, sbits, bias_bits) if act == "bf16" else
+         orc.gemm(a_bits, packed, sbits, bias_bits, act=act)).astype(np.float64)
     ye = exact_gemm(a, wd, b)
     K = a.shape[1]
     gamma = (K + 1) * U32 / (1 - (K + 1) * U32)
@@ -274,17 +276,17 @@ def check_gemm_exact_bound(orc, a_bits, w_bits, bias_bits=None):
     assert (np.abs(y - ye) <= gamma * mag + 1e-45).all(), np.max(np.abs(y - ye) - gamma * mag)
 
 
-def check_gemm_one_hot(orc, w_bits):
-    """A row of A equal to e_k (bf16 1.0 at k) returns column k of the
-    dequantized weight exactly: Y[m, n] = Wd[n, k_m]."""
+def check_gemm_one_hot(orc, w_bits, act="bf16"):
+    """A row of A equal to e_k (1.0 at k: bf16 0x3F80, fp16 0x3C00) returns
+    column k of the dequantized weight exactly: Y[m, n] = Wd[n, k_m]."""
     packed, sbits = orc.quantize(w_bits)
     wd = orc.dequantize(packed, sbits)
     N, K = wd.shape
     ks = [0, 1, 127, 128, K // 2 + 3, K - 1]
     a = np.zeros((len(ks), K), dtype=np.uint16)
     for m, k in enumerate(ks):
-        a[m, k] = 0x3F80
-    y = orc.gemm(a, packed, sbits)
+        a[m, k] = 0x3F80 if act == "bf16" else 0x3C00
+    y = orc.gemm(a, packed, sbits) if act == "bf16" else orc.gemm(a, packed, sbits, act=act)
     for m, k in enumerate(ks):
         assert (y[m] == wd[:, k]).all(), (m, k)
 
@@ -315,8 +317,32 @@ def check_gemm_integer_exact(orc, seed=7):
     assert (yb.astype(np.float64) == exact + bias[None, :].astype(np.float64)).all()
 
 
-def _bits_f64(bits):
+def _bits_f64(bits, act="bf16"):
+    if act == "f16":
+        return f16_values(bits)
     return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def f16_values(bits) -> np.ndarray:
+    """IEEE binary16 bit patterns -> float64 values from the format's
+    definition (sign, 5-bit biased exponent, 10-bit fraction; exponent 0 is
+    subnormal), not through any library conversion."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.int64)
+    sign = np.where((b >> 15) & 1, -1.0, 1.0)
+    e = (b >> 10) & 0x1F
+    f = (b & 0x3FF).astype(np.float64)
+    normal = sign * np.ldexp(1.0 + f / 1024.0, (e - 15).astype(np.int64))
+    sub = sign * np.ldexp(f / 1024.0, -14)
+    return np.where(e == 0, sub, normal)
+
+
+def check_f16_widening(orc):
+    """Every finite fp16 bit pattern widens to its defined value exactly."""
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    finite = ((bits.astype(np.int64) >> 10) & 0x1F) != 0x1F
+    got = orc.f16_bits_to_f32(bits[finite]).astype(np.float64)
+    want = f16_values(bits[finite])
+    assert np.array_equal(got, want)
 
 
 # --------------------------------------------------------------------------

@@ -62,9 +62,11 @@ def _quantize_variant(*, recip=False, fp32_scale_codes=False, zero_rule_before=F
     return q
 
 
-def _gemm_variant(*, transpose=False, drop_bias=False, neg=False, group_shift=False):
-    def g(a_bits, packed, scale_bits, bias_bits=None, group=128, rows=None):
-        a = base.bf16_bits_to_f32(a_bits)
+def _gemm_variant(*, transpose=False, drop_bias=False, neg=False, group_shift=False,
+                  f16_as_bf16=False):
+    def g(a_bits, packed, scale_bits, bias_bits=None, group=128, rows=None, act="bf16"):
+        widen = (lambda b: base.act_bits_to_f32(b, "bf16" if f16_as_bf16 else act))
+        a = widen(a_bits)
         if group_shift:
             codes = base.unpack_codes(packed).astype(np.float32)
             s = base.scales_f32(scale_bits)
@@ -75,7 +77,7 @@ def _gemm_variant(*, transpose=False, drop_bias=False, neg=False, group_shift=Fa
         if neg:
             y = -y
         if bias_bits is not None and not drop_bias:
-            y = y + base.bf16_bits_to_f32(bias_bits)[None, :]
+            y = y + widen(bias_bits)[None, :]
         return y.astype(np.float32)
     return g
 
@@ -99,6 +101,11 @@ def _all_gemm_pins(ns):
     pins.check_gemm_exact_bound(ns, pins.to_bits(a), pins.to_bits(x), pins.to_bits(b))
     pins.check_gemm_one_hot(ns, pins.to_bits(pins.random_weights(256, 256, 11, "t4")))
     pins.check_gemm_integer_exact(ns)
+    # fp16 activations
+    a16 = rng.standard_normal((3, 256)).astype(np.float16).view(np.uint16)
+    b16 = rng.standard_normal(10).astype(np.float16).view(np.uint16)
+    pins.check_gemm_exact_bound(ns, a16, pins.to_bits(x), b16, act="f16")
+    pins.check_gemm_one_hot(ns, pins.to_bits(pins.random_weights(256, 256, 12, "t4")), act="f16")
 
 
 def test_unmutated_copy_passes():
@@ -118,7 +125,7 @@ def test_quantize_mutant_is_caught(mutation):
         _all_quantize_pins(ns)
 
 
-@pytest.mark.parametrize("mutation", ["transpose", "drop_bias", "neg", "group_shift"])
+@pytest.mark.parametrize("mutation", ["transpose", "drop_bias", "neg", "group_shift", "f16_as_bf16"])
 def test_gemm_mutant_is_caught(mutation):
     ns = _namespace(gemm=_gemm_variant(**{mutation: True}))
     with pytest.raises((AssertionError, ValueError)):

@@ -62,6 +62,20 @@ def test_gemm_exact_bound():
     pins.check_gemm_exact_bound(oracle, pins.to_bits(a), pins.to_bits(x), pins.to_bits(b))
 
 
+def test_f16_widening_matches_format_definition():
+    pins.check_f16_widening(oracle)
+
+
+def test_gemm_f16_activations_exact_bound_and_one_hot():
+    x = pins.random_weights(10, 256, 9)
+    rng = np.random.default_rng(13)
+    a = rng.standard_normal((3, 256)).astype(np.float16).view(np.uint16)
+    b = rng.standard_normal(10).astype(np.float16).view(np.uint16)
+    pins.check_gemm_exact_bound(oracle, a, pins.to_bits(x), act="f16")
+    pins.check_gemm_exact_bound(oracle, a, pins.to_bits(x), b, act="f16")
+    pins.check_gemm_one_hot(oracle, pins.to_bits(pins.random_weights(256, 256, 11, "t4")), act="f16")
+
+
 def test_gemm_one_hot_square():
     # N == K so that a transposed operand would not raise a shape error
     pins.check_gemm_one_hot(oracle, pins.to_bits(pins.random_weights(256, 256, 11, "t4")))

@@ -41,12 +41,17 @@ SIGNATURES = [
     ("w4a16_workspace_init", ctypes.c_int, [_vp, _c_size, _vp]),
     ("w4a16_gemm", ctypes.c_int,
      [_vp, _c_int64, _c_int64, _c_int64, _vp, _vp, ctypes.c_int, _vp, _vp, _vp, _c_size, _vp]),
+    ("w4a16_gemm_f16", ctypes.c_int,
+     [_vp, _c_int64, _c_int64, _c_int64, _vp, _vp, ctypes.c_int, _vp, _vp, _vp, _c_size, _vp]),
     ("w4a16_variant_count", ctypes.c_int, []),
     ("w4a16_variant_name", ctypes.c_char_p, [ctypes.c_int]),
     ("w4a16_variant_eligible", ctypes.c_int, [ctypes.c_int, _c_int64, _c_int64, _c_int64]),
     ("w4a16_variant_workspace_bytes", _c_size, [ctypes.c_int, _c_int64, _c_int64, _c_int64]),
     ("w4a16_select_variant", ctypes.c_int, [_c_int64, _c_int64, _c_int64]),
     ("w4a16_gemm_variant", ctypes.c_int,
+     [ctypes.c_int, _vp, _c_int64, _c_int64, _c_int64, _vp, _vp, ctypes.c_int, _vp, _vp, _vp,
+      _c_size, _vp]),
+    ("w4a16_gemm_variant_f16", ctypes.c_int,
      [ctypes.c_int, _vp, _c_int64, _c_int64, _c_int64, _vp, _vp, ctypes.c_int, _vp, _vp, _vp,
       _c_size, _vp]),
     ("w4a16_tune", ctypes.c_int, [_c_int64, _c_int64, _c_int64, _vp, ctypes.POINTER(ctypes.c_int)]),
@@ -191,11 +196,16 @@ def w4a16_gemm(A: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor,
                bias: torch.Tensor | None = None, Y: torch.Tensor | None = None,
                workspace: torch.Tensor | None = None, group: int = GROUP, stream=None,
                variant: int | None = None) -> torch.Tensor:
-    """``Y[M, N] = bf16(A[M, K] @ dequant(packed, scales)^T + bias)`` on the GPU.
+    """``Y[M, N] = A[M, K] @ dequant(packed, scales)^T + bias`` on the GPU, in
+    the activation type of ``A`` (bf16: w4a16_gemm; fp16: w4a16_gemm_f16);
+    ``bias`` and ``Y`` take the same type.
 
     ``variant`` forces one entry of the kernel catalogue (tests, tuning);
     otherwise the library's per-shape table chooses."""
-    _require_cuda(A, "A", torch.bfloat16)
+    if not isinstance(A, torch.Tensor):
+        raise TypeError("A must be a torch.Tensor")
+    act = A.dtype if A.dtype in (torch.bfloat16, torch.float16) else torch.bfloat16
+    _require_cuda(A, "A", act)
     _require_cuda(packed, "packed", torch.uint8)
     _require_cuda(scales, "scales", torch.float16)
     if A.dim() != 2 or scales.dim() != 2:
@@ -207,12 +217,12 @@ def w4a16_gemm(A: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor,
     if packed.numel() != lib().w4a16_packed_bytes(N, K):
         raise ValueError("packed must hold w4a16_packed_bytes(N, K) bytes of tiled codes")
     if bias is not None:
-        _require_cuda(bias, "bias", torch.bfloat16)
+        _require_cuda(bias, "bias", act)
         if bias.numel() != N:
             raise ValueError("bias must have N elements")
     if Y is None:
-        Y = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
-    _require_cuda(Y, "Y", torch.bfloat16)
+        Y = torch.empty((M, N), dtype=act, device=A.device)
+    _require_cuda(Y, "Y", act)
     if Y.shape != (M, N):
         raise ValueError("Y must be [M, N]")
     sh = _stream_handle(A.device, stream)
@@ -224,14 +234,16 @@ def w4a16_gemm(A: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor,
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     bias_ptr = bias.data_ptr() if bias is not None else None
+    f16 = act == torch.float16
     if variant is None:
-        st = L.w4a16_gemm(A.data_ptr(), M, N, K, packed.data_ptr(), scales.data_ptr(), group,
-                          bias_ptr, Y.data_ptr(), ws_ptr, ws_bytes, sh)
+        fn = L.w4a16_gemm_f16 if f16 else L.w4a16_gemm
+        st = fn(A.data_ptr(), M, N, K, packed.data_ptr(), scales.data_ptr(), group,
+                bias_ptr, Y.data_ptr(), ws_ptr, ws_bytes, sh)
     else:
-        st = L.w4a16_gemm_variant(variant, A.data_ptr(), M, N, K, packed.data_ptr(),
-                                  scales.data_ptr(), group, bias_ptr, Y.data_ptr(), ws_ptr,
-                                  ws_bytes, sh)
-    _check(st, "w4a16_gemm")
+        fn = L.w4a16_gemm_variant_f16 if f16 else L.w4a16_gemm_variant
+        st = fn(variant, A.data_ptr(), M, N, K, packed.data_ptr(), scales.data_ptr(), group,
+                bias_ptr, Y.data_ptr(), ws_ptr, ws_bytes, sh)
+    _check(st, "w4a16_gemm_f16" if f16 else "w4a16_gemm")
     return Y
 
 

@@ -274,7 +274,7 @@ int check_gemm_args(const void* A, int64_t M, int64_t N, int64_t K, const void* 
 
 int run_gemm(int id, const void* A, int64_t M, int64_t N, int64_t K, const void* packed,
              const void* scales, const void* bias, void* Y, void* ws, size_t ws_bytes,
-             cudaStream_t stream) {
+             cudaStream_t stream, bool act_f16 = false) {
   DeviceInfo dev;
   if (!device_info(dev)) return W4A16_ERR_CUDA;
   const Variant& v = kVariants[id];
@@ -297,6 +297,7 @@ int run_gemm(int id, const void* A, int64_t M, int64_t N, int64_t K, const void*
   p.workspace_bytes = ws_bytes;
   p.error_word = dev.error_word;
   p.timeout_ns = g_timeout_ns.load();
+  p.act_f16 = act_f16;
   if (log_enabled())
     std::fprintf(stderr, "w4a16: gemm M=%lld N=%lld K=%lld variant=%s grid=%d dp_tiles=%d sk_units=%lld\n",
                  static_cast<long long>(M), static_cast<long long>(N), static_cast<long long>(K),
@@ -499,6 +500,29 @@ size_t w4a16_variant_workspace_bytes(int variant, int64_t M, int64_t N, int64_t 
 }
 
 int w4a16_select_variant(int64_t M, int64_t N, int64_t K) { return select_variant(M, N, K); }
+
+int w4a16_gemm_f16(const void* A_f16, int64_t M, int64_t N, int64_t K, const void* packed,
+                   const void* scales, int group, const void* bias_f16_or_null, void* Y_f16,
+                   void* workspace, size_t workspace_bytes, void* stream) {
+  const int st = check_gemm_args(A_f16, M, N, K, packed, scales, group, bias_f16_or_null, Y_f16);
+  if (st != W4A16_OK) return st;
+  const int id = select_variant(M, N, K);
+  if (id < 0) return W4A16_ERR_NO_VARIANT;
+  return run_gemm(id, A_f16, M, N, K, packed, scales, bias_f16_or_null, Y_f16, workspace,
+                  workspace_bytes, static_cast<cudaStream_t>(stream), /*act_f16=*/true);
+}
+
+int w4a16_gemm_variant_f16(int variant, const void* A_f16, int64_t M, int64_t N, int64_t K,
+                           const void* packed, const void* scales, int group,
+                           const void* bias_f16_or_null, void* Y_f16, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+  const int st = check_gemm_args(A_f16, M, N, K, packed, scales, group, bias_f16_or_null, Y_f16);
+  if (st != W4A16_OK) return st;
+  if (variant < 0 || variant >= kNumVariants) return W4A16_ERR_UNSUPPORTED;
+  if (!variant_eligible(variant, M, N, K)) return W4A16_ERR_NO_VARIANT;
+  return run_gemm(variant, A_f16, M, N, K, packed, scales, bias_f16_or_null, Y_f16, workspace,
+                  workspace_bytes, static_cast<cudaStream_t>(stream), /*act_f16=*/true);
+}
 
 int w4a16_gemm_variant(int variant, const void* A_bf16, int64_t M, int64_t N, int64_t K,
                        const void* packed, const void* scales, int group,

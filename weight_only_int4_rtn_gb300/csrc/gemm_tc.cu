@@ -1,973 +1,9 @@
-// W4A16 GEMM on the sm_103a tensor cores (tcgen05 + TMEM + TMA).
-//
-//   Y[M, N] = bf16( A[M, K] . dequant(W)[N, K]^T + bias[N] ),
-//   dequant(W)[n, k] = q[n, k] * s[k / 128, n]
-//
-// "Kernel dispatch and Humming quantization in PhyAI", section "Humming
-// makes the separation useful": INT4 group-128 weights execute through a
-// kernel that understands their packed layout, with BF16 activations.
-//
-// Orientation ("swap AB").  One tile is 128 weight rows x act_tile activation
-// rows.  The tcgen05 MMA computes D[128, act_tile] = Wt[128, 128k] .
-// At[act_tile, 128k]^T per K block, so the accumulator D holds a tile of
-// Y^T: TMEM lane i = weight row n0 + i, column j = activation row m0 + j.
-//   * The weight operand is produced by the dequant warps and written into
-//     TMEM with tcgen05.st (the MMA's A operand may live in TMEM): no shared
-//     memory round trip for the converted weights.
-//   * The activation operand is TMA-loaded into shared memory in the
-//     128-byte-swizzled K-major layout and described by a shared-memory
-//     descriptor (the MMA's B operand).
-//   * Each K block (128 values = one quantization group) is one pipeline
-//     unit: TMA brings the packed codes (one contiguous 8 KiB tile of the
-//     tiled storage: 128 rows x 64 B), the 128 scales of that group and the
-//     activation slice; the dequant warps convert; one thread issues 8 MMAs
-//     of K = 16.  (Row-major codes would make every unit 128 separate 64-byte
-//     pieces K/2 bytes apart, which TMA streams several times slower.)
-//
-// Two scaling modes:
-//   group_scale = true:  the weight operand holds the integer codes (exact in
-//     bf16); each unit's MMA result D_g is the integer-code partial sum of one
-//     group, which the readout warps accumulate as acc += s[g, n] * D_g in
-//     fp32 registers.  Cheapest conversion; used for small act_tile.
-//   group_scale = false: the weight operand is bf16_rn(q * s), computed
-//     exactly as fma(q, s_hi, q * s_lo) with s = s_hi + s_lo split into two
-//     bf16 values; D accumulates the whole K range in TMEM.
-//
-// Schedule.  Units are (tile, k-block) pairs, tiles ordered weight-row-tile
-// fastest.  Tiles 0 .. dp_tiles-1 run whole on CTA t % grid.  The units of
-// the remaining tiles are split into contiguous, balanced ranges over all
-// CTAs (stream-K).  A range that covers only part of a tile writes an fp32
-// partial tile to the workspace.  When every CTA is done, one grid-wide
-// barrier; then all CTAs together sum each split tile's partials in k order
-// (deterministic), add the bias and store Y.  The grid is at most one CTA
-// per SM and a CTA needs more than half an SM's shared memory, so all CTAs
-// are resident at once and the barrier cannot wait on an unscheduled CTA.
-//
-// Lanes.  One thread issuing tcgen05.mma with a small N (16..64) is limited
-// by its own issue rate (about 47 cycles per MMA), well below the tensor
-// pipe; two issuing threads reach the pipe's rate.  So the group-scale
-// variants run two lanes: even units and odd units each have their own
-// producer, dequant warpgroup and MMA issuer, their own shared-memory stages,
-// TMEM weight stages, accumulators and barrier rings; only the readout
-// visits all units, in order.
-//
-// Warp roles (16 warps):
-//   warps 0, 2  TMA producers (one lane each; even and odd units, because one
-//               thread can only complete a few mbarrier phases per
-//               microsecond, fewer than the weight stream needs)
-//   warp 1      TMEM allocator; MMA issuer of lane 0 (of all units with one lane)
-//   warp 15     MMA issuer of lane 1
-//   warps 3-6   readout: accumulator -> registers -> Y or partial tile
-//   warps 7-14  dequant, two warpgroups (even / odd units): packed codes
-//               (shared memory) -> weight operand (TMEM)
-// A warp may only touch TMEM lanes 32 * (warp % 4) .. + 31, so each readout
-// and dequant thread owns weight row 32 * (warp % 4) + lane.  The dequant
-// warps never wait on accumulators: they run up to the TMEM weight-stage
-// count ahead of the MMA, which runs up to the accumulator count ahead of the
-// readout.
-//
-// Every wait on an mbarrier is bounded by a time limit; on expiry the kernel
-// records an error word, lets every role leave its loop, waits (bounded) for
-// its own copies and MMAs in flight, frees TMEM and returns.
-#include <cuda_bf16.h>
-#include <cuda_fp16.h>
-#include <cuda_runtime.h>
-
-#include <cstdint>
-
-#include "kernels.h"
-#include "ptx.cuh"
-#include "waits.cuh"
+// W4A16 GEMM: bf16-activation instantiation of the tcgen05 kernel template,
+// the launch dispatcher, configuration queries and the wait self test.
+#include "gemm_tc.cuh"
 
 namespace w4a16 {
-
-#ifdef W4A16_TRACE
-// Timestamp probes for profiling builds only (never in the default build).
-__device__ unsigned long long* g_trace = nullptr;
-__device__ unsigned long long* g_trace_units = nullptr;
-#define W4A16_TRACE_POINT(id)                                                           \
-  do {                                                                                  \
-    if (trace_cta != nullptr) trace_cta[blockIdx.x * 16 + (id)] = ptx::globaltimer_ns(); \
-  } while (0)
-#define W4A16_TRACE_UNIT(role, i)                                                       \
-  do {                                                                                  \
-    if (trace_unit != nullptr && (i) < 64)                                              \
-      trace_unit[(role) * 64 + (i)] = static_cast<unsigned long long>(clock64());     \
-  } while (0)
-#else
-#define W4A16_TRACE_POINT(id) \
-  do {                        \
-  } while (0)
-#define W4A16_TRACE_UNIT(role, i) \
-  do {                            \
-  } while (0)
-#endif
-
 namespace {
-
-constexpr int kUnitK = 128;                    // K values per unit (one group)
-constexpr int kWBytes = kTileW * kUnitK / 2;   // packed codes per unit: 8 KiB
-constexpr int kSBytes = kTileW * 2;            // scales per unit: 256 B
-constexpr int kMaxAStages = 6;                 // weight-operand stages in TMEM (at most)
-constexpr int kAStageCols = kUnitK / 2;        // 64 TMEM columns per stage
-constexpr uint32_t kTmemCols = 512;
-constexpr int kWarps = 16;
-constexpr int kReadoutWarp0 = 3;
-constexpr int kDequantWarp0 = 7;
-constexpr int kMmaWarp2 = 15;                  // second MMA issuer (two lanes)
-constexpr int kScaleRing = 8;                  // group mode: units of scales in shared memory
-constexpr int kScaleAhead = 2;                 // ... copied this many unit pairs ahead
-constexpr int kPairRing = 8;                   // group mode: pair_done barriers
-
-struct Args {
-  int M, N, K, KB;
-  int n_tiles;
-  int dp_tiles;
-  int sk_units;
-  int act_3d;                  // activation map is 3-D: both 64-k halves in one copy
-  const __half* scales;        // [K/128, N]; the group-mode readout reads its scales here
-  const __nv_bfloat16* bias;
-  __nv_bfloat16* Y;
-  float* ws;
-  uint32_t* counters;
-  uint32_t* err;
-  uint64_t timeout_ns;
-};
-
-struct Unit {
-  int tile, kb;
-  bool seg_first, seg_last;   // first / last unit of this CTA's run on the tile
-  bool whole;                 // the run covers the whole tile
-  int slot;                   // partial slot (0: first stream-K tile of the CTA, 1: last)
-  int sk_tile;                // index among stream-K tiles, -1 for whole tiles
-};
-
-struct Sched {
-  int c, C, KB, dp_tiles, dp_iters;
-  int u0, u1;                 // this CTA's stream-K unit range [u0, u1)
-  int total;
-
-  __device__ void init(const Args& a) {
-    c = blockIdx.x;
-    C = gridDim.x;
-    KB = a.KB;
-    dp_tiles = a.dp_tiles;
-    dp_iters = (dp_tiles > c) ? (dp_tiles - c + C - 1) / C : 0;
-    u0 = static_cast<int>((static_cast<int64_t>(c) * a.sk_units) / C);
-    u1 = static_cast<int>((static_cast<int64_t>(c + 1) * a.sk_units) / C);
-    total = dp_iters * KB + (u1 - u0);
-  }
-};
-
-// Walks this CTA's units in order, one at a time, with no division per unit
-// (the issuing threads are on the critical path of the pipeline).
-struct UnitIter {
-  int C, KB, ndp, u0, u1, dp_tiles;
-  int i, tile, kb, u, tl, first_tl;
-
-  __device__ void init(const Sched& s) {
-    C = s.C;
-    KB = s.KB;
-    ndp = s.dp_iters * s.KB;
-    u0 = s.u0;
-    u1 = s.u1;
-    dp_tiles = s.dp_tiles;
-    i = 0;
-    tile = s.c;
-    kb = 0;
-    if (ndp == 0) start_sk();
-  }
-  __device__ void start_sk() {
-    u = u0;
-    tl = u0 / KB;
-    first_tl = tl;
-    kb = u0 - tl * KB;
-    tile = dp_tiles + tl;
-  }
-  __device__ Unit next() {
-    Unit r;
-    r.tile = tile;
-    r.kb = kb;
-    if (i < ndp) {
-      r.seg_first = (kb == 0);
-      r.seg_last = (kb == KB - 1);
-      r.whole = true;
-      r.slot = 0;
-      r.sk_tile = -1;
-      ++i;
-      if (++kb == KB) {
-        kb = 0;
-        tile += C;
-      }
-      if (i == ndp) start_sk();
-    } else {
-      r.seg_first = (kb == 0) || (u == u0);
-      r.seg_last = (kb == KB - 1) || (u == u1 - 1);
-      r.whole = (tl * KB >= u0) && ((tl + 1) * KB <= u1);
-      r.slot = (tl == first_tl) ? 0 : 1;
-      r.sk_tile = tl;
-      ++i;
-      ++u;
-      if (++kb == KB) {
-        kb = 0;
-        ++tl;
-        ++tile;
-      }
-    }
-    return r;
-  }
-};
-
-// Walks this CTA's runs ("segments": consecutive units on one tile) in
-// order.  For the readout, which needs tile-level facts only at the ends of
-// runs.
-struct SegCursor {
-  int C, KB, dp_left, tile, u, u1, first_sk;
-  __device__ void init(const Sched& s) {
-    C = s.C;
-    KB = s.KB;
-    dp_left = s.dp_iters;
-    tile = s.c;
-    u = s.u0;
-    u1 = s.u1;
-    first_sk = 1;
-  }
-  // Next run: its tile, first k-block, length, and whether it is the whole
-  // tile (else: the partial slot it writes).
-  __device__ void next(Unit& r, int& kb0, int& len, int dp_tiles) {
-    if (dp_left > 0) {
-      --dp_left;
-      r.tile = tile;
-      tile += C;
-      kb0 = 0;
-      len = KB;
-      r.whole = true;
-      r.slot = 0;
-      r.sk_tile = -1;
-    } else {
-      const int tl = u / KB;
-      kb0 = u - tl * KB;
-      const int end = min(u1, (tl + 1) * KB);
-      len = end - u;
-      r.tile = dp_tiles + tl;
-      r.whole = (kb0 == 0) && (len == KB);
-      r.slot = first_sk ? 0 : 1;
-      r.sk_tile = tl;
-      first_sk = 0;
-      u = end;
-    }
-    r.kb = kb0;
-    r.seg_first = true;
-    r.seg_last = true;
-  }
-};
-
-// CTA that owns stream-K unit u under the balanced split.
-__device__ __forceinline__ int sk_owner(int u, int C, int sk_units) {
-  return static_cast<int>(((static_cast<int64_t>(u) + 1) * C - 1) / sk_units);
-}
-
-struct Shared {
-  uint64_t full[16];          // a shared-memory stage's copies landed
-  uint64_t afull[kMaxAStages];   // a TMEM weight stage is written
-  uint64_t unit_done[32];     // per lane a ring: a unit's MMAs completed
-  uint64_t dfull[8];          // dequant mode: a run on a tile is accumulated
-  uint64_t dempty[8];         // the readout drained accumulator buffer(s)
-  uint64_t pair_done[8];       // group mode: both lanes' units of a pair completed
-  uint64_t mma_done[2];
-  uint32_t tmem_base;
-  int abort_flag;
-  int reduce_ok;
-};
-
-// ------------------------------------------------------- code -> bf16 pairs
-// Eight 4-bit codes (one 32-bit word, code k in nibble k) to four bf16x2
-// words holding the code pairs (k0,k1), (k2,k3), (k4,k5), (k6,k7) as exact
-// bf16 integers.  0x4300 | (nibble ^ 8) is the bf16 value 136 + q; one fused
-// multiply-add subtracts 136.
-__device__ __forceinline__ uint32_t bf16x2_fma(uint32_t a, uint32_t b, uint32_t c) {
-  uint32_t d;
-  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-  return d;
-}
-
-__device__ __forceinline__ void codes_to_bf16(uint32_t w, uint32_t* out) {
-  const uint32_t v = w >> 4;
-  const uint32_t one = 0x3F803F80u;       // (1.0, 1.0)
-  const uint32_t m136 = 0xC308C308u;      // (-136, -136)
-  out[0] = bf16x2_fma(ptx::and_xor(ptx::prmt(w, v, 0x0400), 0x000F000Fu, 0x43084308u), one, m136);
-  out[1] = bf16x2_fma(ptx::and_xor(ptx::prmt(w, v, 0x0501), 0x000F000Fu, 0x43084308u), one, m136);
-  out[2] = bf16x2_fma(ptx::and_xor(ptx::prmt(w, v, 0x0602), 0x000F000Fu, 0x43084308u), one, m136);
-  out[3] = bf16x2_fma(ptx::and_xor(ptx::prmt(w, v, 0x0703), 0x000F000Fu, 0x43084308u), one, m136);
-}
-
-// bf16_rn(q * s) for both halves: q * s_lo is exact (<= 7 significant bits),
-// so fma(q, s_hi, q * s_lo) rounds the exact product once.
-__device__ __forceinline__ uint32_t scale_pair(uint32_t q, uint32_t s_hi2, uint32_t s_lo2) {
-  const uint32_t lo = bf16x2_fma(q, s_lo2, 0x80008000u);   // q * s_lo + (-0)
-  return bf16x2_fma(q, s_hi2, lo);
-}
-
-template <int BA, int L, bool GRP, int STAGES>
-struct Cfg {
-  static constexpr int kActBox = BA * 128;                        // bytes per 64-k box
-  static constexpr int kStageRaw = 2 * kActBox + kWBytes + kSBytes;
-  static constexpr int kStage = (kStageRaw + 1023) / 1024 * 1024;
-  static constexpr int kThreads = 32 * kWarps;                    // 16 warps: <= 128 registers
-  static constexpr int kSL = STAGES / L;                          // shared-memory stages per lane
-  // TMEM: kAS weight stages of 64 columns, then the accumulators.  The
-  // narrowest group-mode tile needs few accumulator columns, so it takes
-  // three weight stages per lane (the dequant runs further ahead).
-  static constexpr int kAS = (GRP && BA == 16) ? 6 : 4;
-  static constexpr int kDCol = kAS * kAStageCols;
-  static constexpr int kDCols = 512 - kDCol;
-  static constexpr int kAL = kAS / L;                             // TMEM weight stages per lane
-  static constexpr int kDBfit = kDCols / BA;                      // accumulators that fit
-  static constexpr int kDB = kDBfit < (GRP ? 8 : 4) ? kDBfit : (GRP ? 8 : 4);
-  static constexpr int kDL = kDB / L;                             // accumulator buffers per lane
-  static constexpr int kRL = kSL > kAL ? kSL : kAL;               // unit_done ring per lane
-  static constexpr int kChunk = BA < (GRP ? 16 : 32) ? BA : (GRP ? 16 : 32);
-  static constexpr size_t kSmem = static_cast<size_t>(STAGES) * kStage + 1024 + sizeof(Shared) +
-                                  (GRP ? kScaleRing * kTileW * 2 : 0);
-  static constexpr uint32_t kTx = 2 * kActBox + kWBytes + kSBytes;
-  static_assert(BA % 16 == 0 && BA >= 16 && BA <= 256, "tcgen05 N for M=128");
-  static_assert(L == 1 || L == 2, "lanes");
-  static_assert(GRP || L == 1, "dequant mode accumulates a tile run in one lane");
-  static_assert(STAGES % L == 0 && STAGES <= 16, "stages split over the lanes");
-  static_assert(kDB % L == 0 && kDL >= 1, "accumulators split over the lanes");
-  // a unit_done phase may only be reused once every waiter saw the previous
-  // one: the readout is at most kDL units of a lane behind its MMAs
-  static_assert(kRL >= kDL, "unit_done ring covers the accumulator buffers");
-  static_assert(L * kRL <= 32, "barrier arrays");
-  static_assert(!GRP || BA <= 64, "group mode keeps BA fp32 accumulators per thread");
-  static_assert(!GRP || L == 2, "group mode runs two lanes (the readout takes units in pairs)");
-  // group mode: the pair ring replaces the unit ring for every waiter, so
-  // it must be as deep as the stage rings and the accumulator buffers
-  static_assert(!GRP || (kDL <= kPairRing && kSL <= kPairRing && kAL <= kPairRing),
-                "pair ring covers the stage rings and the accumulator buffers");
-};
-
-// Lane of unit i and its index within the lane.
-template <int L>
-__device__ __forceinline__ void lane_split(int i, int& p, int& j) {
-  if constexpr (L == 1) {
-    p = 0;
-    j = i;
-  } else {
-    p = i & 1;
-    j = i >> 1;
-  }
-}
-
-template <int N>
-__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t* r) {
-  if constexpr (N == 8) {
-    ptx::tmem_ld_x8_sync(taddr, r);
-  } else if constexpr (N == 16) {
-    ptx::tmem_ld_x16_sync(taddr, r);
-  } else {
-    static_assert(N == 32, "chunk");
-    ptx::tmem_ld_x32_sync(taddr, r);
-  }
-}
-
-template <int CNT>
-__device__ __forceinline__ void load_cols(uint32_t taddr, float (&v)[CNT]) {
-  uint32_t r[CNT];
-  tmem_ld_cols<CNT>(taddr, r);
-#pragma unroll
-  for (int j = 0; j < CNT; ++j) v[j] = __uint_as_float(r[j]);
-}
-
-// Write accumulator columns [col0, col0 + CNT) of this thread's weight row
-// either to Y (whole tile: bias added, one rounding to bf16) or to this CTA's
-// partial slot (fp32, no bias; column m of the slot holds 128 rows).
-template <int BA, int CNT>
-__device__ __forceinline__ void emit_cols(const Args& a, const Unit& u, int row, int col0,
-                                          const float (&v)[CNT], float bias_n) {
-  const int n0 = (u.tile % a.n_tiles) * kTileW;
-  const int m0 = (u.tile / a.n_tiles) * BA;
-  if (u.whole) {
-    const int n = n0 + row;
-    if (n < a.N) {
-#pragma unroll
-      for (int j = 0; j < CNT; ++j) {
-        const int m = m0 + col0 + j;
-        if (m < a.M) a.Y[static_cast<int64_t>(m) * a.N + n] = __float2bfloat16_rn(v[j] + bias_n);
-      }
-    }
-  } else {
-    float* slot = a.ws + (static_cast<int64_t>(blockIdx.x) * 2 + u.slot) * (BA * kTileW) + row;
-#pragma unroll
-    for (int j = 0; j < CNT; ++j) {
-      if (m0 + col0 + j < a.M) slot[(col0 + j) * kTileW] = v[j];
-    }
-  }
-}
-
-// Grid-wide barrier after every CTA wrote its partial tiles (one thread per
-// CTA).  The grid never exceeds one CTA per SM and each CTA needs more than
-// half an SM's shared memory, so all CTAs are resident together; the wait is
-// bounded all the same.  Self-resetting: the last arrival clears the count
-// and bumps the generation the others wait on.
-__device__ bool grid_barrier(const Args& a, const WaitCtx& wc) {
-  if (*reinterpret_cast<volatile int*>(wc.abort_flag)) return false;
-  uint32_t* count = a.counters;
-  uint32_t* gen = a.counters + 1;
-  const uint32_t g0 = ptx::ld_acquire_gpu(gen);
-  // acquire-release: the last arrival observes every other CTA's partials
-  const uint32_t old = ptx::atom_add_acq_rel_gpu(count, 1u);
-  if (old == gridDim.x - 1) {
-    atomicExch(count, 0u);
-    ptx::atom_add_release_gpu(gen, 1u);   // publishes all partials
-    return true;
-  }
-  const uint64_t t0 = ptx::globaltimer_ns();
-  for (uint32_t spin = 0; ptx::ld_acquire_gpu(gen) == g0; ++spin) {
-    if ((spin & 15) == 15) {
-      if (ptx::globaltimer_ns() - t0 > a.timeout_ns) {
-        wait_record_timeout(wc);
-        return false;
-      }
-      ptx::nanosleep(32);
-    }
-  }
-  return true;
-}
-
-// Second phase of stream-K: every element of every split tile is the sum of
-// its contributors' partials in k order (deterministic), plus the bias,
-// rounded once to bf16.  The elements are spread evenly over all CTAs and
-// all threads; consecutive threads take consecutive weight rows, so partial
-// reads and Y stores are coalesced.
-template <int BA>
-__device__ void stream_k_reduce(const Args& a) {
-  constexpr int kTileElems = BA * kTileW;
-  const int C = gridDim.x;
-  const int KB = a.KB;
-  const int S = a.sk_units;
-  const int64_t E = static_cast<int64_t>(S / KB) * kTileElems;
-  const int64_t e_lo = static_cast<int64_t>(blockIdx.x) * E / C;
-  const int64_t e_hi = static_cast<int64_t>(blockIdx.x + 1) * E / C;
-  int cached = -1, c_lo = 0, c_hi = 0, slot_lo = 0, m0 = 0, n0 = 0;
-  for (int64_t e = e_lo + threadIdx.x; e < e_hi; e += blockDim.x) {
-    const int tl = static_cast<int>(e / kTileElems);
-    const int rem = static_cast<int>(e - static_cast<int64_t>(tl) * kTileElems);
-    const int m = rem >> 7;
-    const int row = rem & (kTileW - 1);
-    if (tl != cached) {
-      cached = tl;
-      c_lo = sk_owner(tl * KB, C, S);
-      c_hi = sk_owner(tl * KB + KB - 1, C, S);
-      // the CTA holding the tile's first k-block keeps it in slot 0 only if
-      // its range starts exactly there; every later contributor's range
-      // starts inside the tile (slot 0)
-      const int u0_lo = static_cast<int>(static_cast<int64_t>(c_lo) * S / C);
-      slot_lo = (u0_lo == tl * KB) ? 0 : 1;
-      const int tile = a.dp_tiles + tl;
-      m0 = (tile / a.n_tiles) * BA;
-      n0 = (tile % a.n_tiles) * kTileW;
-    }
-    if (c_lo == c_hi) continue;   // one CTA ran the whole tile and stored Y
-    const int mm = m0 + m;
-    const int n = n0 + row;
-    if (mm >= a.M || n >= a.N) continue;
-    const float* col = a.ws + static_cast<int64_t>(m) * kTileW + row;
-    float sum = __ldcg(col + (static_cast<int64_t>(c_lo) * 2 + slot_lo) * kTileElems);
-#pragma unroll 4
-    for (int c = c_lo + 1; c <= c_hi; ++c) sum += __ldcg(col + static_cast<int64_t>(c) * 2 * kTileElems);
-    const float b = a.bias != nullptr ? __bfloat162float(a.bias[n]) : 0.0f;
-    a.Y[static_cast<int64_t>(mm) * a.N + n] = __float2bfloat16_rn(sum + b);
-  }
-}
-
-template <int BA, int L, bool GRP, int STAGES>
-__global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES>::kThreads, 1)
-    w4a16_gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_act,
-                         const __grid_constant__ CUtensorMap tm_w,
-                         const __grid_constant__ CUtensorMap tm_s, const Args a) {
-  using C = Cfg<BA, L, GRP, STAGES>;
-  constexpr int DB = C::kDB;
-  constexpr int SL = C::kSL;
-  constexpr int AL = C::kAL;
-  constexpr int DL = C::kDL;
-  constexpr int RL = C::kRL;
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
-  Shared* sh = reinterpret_cast<Shared*>(smem + STAGES * C::kStage);
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-
-  auto act_box = [&](int stage, int box) -> uint8_t* {
-    return smem + stage * C::kStage + box * C::kActBox;
-  };
-  auto w_tile = [&](int stage) -> uint8_t* { return smem + stage * C::kStage + 2 * C::kActBox; };
-  auto s_tile = [&](int stage) -> __half* {
-    return reinterpret_cast<__half*>(smem + stage * C::kStage + 2 * C::kActBox + kWBytes);
-  };
-  // Resources of unit i (lane p, index j in the lane): the lanes own
-  // interleaved shared-memory stages, TMEM weight stages and accumulators.
-  auto stage_of = [&](int i) -> int {
-    int p, j;
-    lane_split<L>(i, p, j);
-    return p + L * (j % SL);
-  };
-  auto astage_of = [&](int i) -> int {
-    int p, j;
-    lane_split<L>(i, p, j);
-    return p + L * (j % AL);
-  };
-  // Completion of unit i's MMAs.  Group mode: the pair ring (lane 0's and
-  // lane 1's j-th units complete together, one arrival each); one lane:
-  // the unit ring.
-  auto done_bar = [&](int i) -> uint64_t* {
-    int p, j;
-    lane_split<L>(i, p, j);
-    if constexpr (GRP) return &sh->pair_done[j % kPairRing];
-    return &sh->unit_done[p * RL + j % RL];
-  };
-  auto done_parity = [&](int i) -> uint32_t {
-    int p, j;
-    lane_split<L>(i, p, j);
-    if constexpr (GRP) return static_cast<uint32_t>((j / kPairRing) & 1);
-    return static_cast<uint32_t>((j / RL) & 1);
-  };
-
-  // ---------------------------------------------------------------- set-up
-#ifdef W4A16_TRACE
-  unsigned long long* const trace_cta = g_trace;
-  unsigned long long* const trace_unit = blockIdx.x == 0 ? g_trace_units : nullptr;
-#endif
-  if (threadIdx.x == 0) W4A16_TRACE_POINT(0);
-  if (threadIdx.x == 0) W4A16_TRACE_UNIT(9, 0);
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) ptx::mbar_init(&sh->full[s], 1);
-    for (int s = 0; s < L * RL; ++s) ptx::mbar_init(&sh->unit_done[s], 1);
-    for (int s = 0; s < C::kAS; ++s) ptx::mbar_init(&sh->afull[s], 4);
-    for (int s = 0; s < DB; ++s) {
-      ptx::mbar_init(&sh->dfull[s], 1);
-      ptx::mbar_init(&sh->dempty[s], 4);
-    }
-    for (int s = 0; s < kPairRing; ++s) ptx::mbar_init(&sh->pair_done[s], 2);
-    ptx::mbar_init(&sh->mma_done[0], 1);
-    ptx::mbar_init(&sh->mma_done[1], 1);
-    sh->abort_flag = 0;
-    sh->reduce_ok = 0;
-    ptx::fence_mbar_init();
-    ptx::prefetch_tmap(&tm_act);
-    ptx::prefetch_tmap(&tm_w);
-    ptx::prefetch_tmap(&tm_s);
-  }
-  if (warp == 1) {
-    ptx::tmem_alloc(&sh->tmem_base, kTmemCols);
-    ptx::tmem_relinquish();
-  }
-  ptx::tc_fence_before();
-  __syncthreads();
-  ptx::tc_fence_after();
-  const uint32_t tmem = sh->tmem_base;
-  const WaitCtx wc{a.err, a.timeout_ns, &sh->abort_flag};
-
-  if (threadIdx.x == 0) W4A16_TRACE_POINT(1);
-  if (threadIdx.x == 0) W4A16_TRACE_UNIT(9, 1);
-  // The schedule depends on the launch only, so it is worked out while the
-  // previous kernel on the stream may still run; the inputs may be that
-  // kernel's outputs, so nothing is read before the dependency wait.
-  Sched sched;
-  sched.init(a);
-  UnitIter it;
-  it.init(sched);
-  const int total = sched.total;
-  ptx::grid_dependency_wait();
-  ptx::grid_launch_dependents();
-  if (threadIdx.x == 0) W4A16_TRACE_POINT(2);
-  if (threadIdx.x == 0) W4A16_TRACE_UNIT(9, 2);
-
-  if (warp == 0 || warp == 2) {
-    // ----------------------------------------------------- TMA producers
-    // Even units from warp 0, odd units from warp 2 (with two lanes: one
-    // producer per lane).
-    if (lane == 0) {
-      const int mine = warp == 0 ? 0 : 1;
-      int issued = -1;
-      for (int i = 0; i < total; ++i) {
-        const Unit u = it.next();
-        if ((i & 1) != mine) continue;
-        const int stage = stage_of(i);
-        // the unit that last used this stage is i - STAGES (same lane)
-        if (i >= STAGES && !wait_one(done_bar(i - STAGES), done_parity(i - STAGES), wc)) break;
-        if (i == 0) W4A16_TRACE_UNIT(9, 3);
-        const int m0 = (u.tile / a.n_tiles) * BA;
-        ptx::mbar_arrive_expect_tx(&sh->full[stage], C::kTx);
-        if (i == 0) W4A16_TRACE_UNIT(9, 4);
-        if (a.act_3d) {
-          ptx::tma_load_3d(act_box(stage, 0), &tm_act, &sh->full[stage], 0, m0, u.kb * 2);
-        } else {
-          ptx::tma_load_2d(act_box(stage, 0), &tm_act, &sh->full[stage], u.kb * kUnitK, m0);
-          ptx::tma_load_2d(act_box(stage, 1), &tm_act, &sh->full[stage], u.kb * kUnitK + 64, m0);
-        }
-        if (i == 0) W4A16_TRACE_UNIT(9, 5);
-        // the unit's codes: one contiguous 8 KiB tile of the tiled storage
-        ptx::tma_load_2d(w_tile(stage), &tm_w, &sh->full[stage], 0,
-                         ((u.tile % a.n_tiles) * a.KB + u.kb) * kTileW);
-        if (i == 0) W4A16_TRACE_UNIT(9, 6);
-        ptx::tma_load_2d(s_tile(stage), &tm_s, &sh->full[stage], (u.tile % a.n_tiles) * kTileW,
-                         u.kb);
-        if (i == 0) W4A16_TRACE_UNIT(9, 7);
-        if (i <= 1) W4A16_TRACE_POINT(3);
-        W4A16_TRACE_UNIT(0, i);
-        issued = i;
-      }
-      if (*reinterpret_cast<volatile int*>(&sh->abort_flag)) {
-        // let this producer's copies still in flight land before the CTA exits
-        for (int i = issued; i >= 0 && i > issued - STAGES; i -= 2) {
-          int p, j;
-          lane_split<L>(i, p, j);
-          const uint64_t t0 = ptx::globaltimer_ns();
-          while (!ptx::mbar_try_wait(&sh->full[stage_of(i)], (j / SL) & 1)) {
-            if (ptx::globaltimer_ns() - t0 > a.timeout_ns) break;
-          }
-        }
-      }
-    }
-  } else if (warp == 1 || (L == 2 && warp == kMmaWarp2)) {
-    // ------------------------------------------------------- MMA issuers
-    // One thread per lane: one thread alone cannot issue small-N MMAs as
-    // fast as the tensor pipe runs them.
-    if (lane == 0) {
-      const int mine = warp == 1 ? 0 : 1;
-      constexpr uint32_t idesc = ptx::idesc_bf16_f32(kTileW, BA);
-      const uint32_t smem0 = ptx::smem_u32(smem);
-      if constexpr (GRP) {
-        // this lane's units j = 0, 1, ...: unit i = 2 j + mine; every unit
-        // starts a fresh accumulator (the readout applies the group scale)
-        const int nj = (total - mine + 1) >> 1;
-        for (int j = 0; j < nj; ++j) {
-          const int stage = mine + 2 * (j % SL);
-          const int as = mine + 2 * (j % AL);
-          const int dl = j % DL;
-          if (!wait_one(&sh->afull[as], (j / AL) & 1, wc)) break;
-          // the readout frees a lane's buffers in order: once it read the
-          // lane's unit j-1, buffers of units j .. j+DL-1 are free
-          if (dl == 0 && j >= DL && !wait_one(&sh->dempty[mine], ((j / DL) - 1) & 1, wc)) break;
-          ptx::tc_fence_after();
-          if (j == 0) W4A16_TRACE_POINT(4);
-          W4A16_TRACE_UNIT(4, 2 * j + mine);
-          const uint32_t d_tmem = tmem + C::kDCol + (mine + 2 * dl) * BA;
-          const uint32_t a_tmem = tmem + as * kAStageCols;
-          const uint32_t b0 = smem0 + stage * C::kStage;
-#pragma unroll
-          for (int kk = 0; kk < kUnitK / 16; ++kk) {
-            const uint32_t baddr = b0 + (kk >> 2) * C::kActBox + (kk & 3) * 32;
-            ptx::mma_bf16_tmem_a(d_tmem, a_tmem + kk * 8, ptx::smem_desc_sw128(baddr), idesc,
-                                 kk > 0 ? 1u : 0u);
-          }
-          // one arrival per lane on the pair's barrier; an unpaired last
-          // unit (lane 0) arrives for both
-          ptx::mma_commit(&sh->pair_done[j % kPairRing]);
-          if (mine == 0 && 2 * j == total - 1) ptx::mma_commit(&sh->pair_done[j % kPairRing]);
-          W4A16_TRACE_UNIT(5, 2 * j + mine);
-        }
-        if (nj > 0) W4A16_TRACE_POINT(5);
-      } else {
-        int seg = 0;
-        int db = 0;
-        for (int i = 0; i < total; ++i) {
-          const Unit u = it.next();
-          int p, j;
-          lane_split<L>(i, p, j);
-          const int stage = stage_of(i);
-          const int as = astage_of(i);
-          W4A16_TRACE_UNIT(8, i);
-          if (!wait_one(&sh->afull[as], (j / AL) & 1, wc)) break;
-          W4A16_TRACE_UNIT(10, i);
-          const bool fresh = u.seg_first;
-          if (u.seg_first) {
-            db = seg % DB;
-            if (seg >= DB && !wait_one(&sh->dempty[db], ((seg / DB) - 1) & 1, wc)) break;
-          }
-          ptx::tc_fence_after();
-          if (i == 0) W4A16_TRACE_POINT(4);
-          if (i == total - 1) W4A16_TRACE_POINT(5);
-          W4A16_TRACE_UNIT(4, i);
-          const uint32_t d_tmem = tmem + C::kDCol + db * BA;
-          const uint32_t a_tmem = tmem + as * kAStageCols;
-          const uint32_t b0 = smem0 + stage * C::kStage;
-  #pragma unroll
-          for (int kk = 0; kk < kUnitK / 16; ++kk) {
-            const uint32_t baddr = b0 + (kk >> 2) * C::kActBox + (kk & 3) * 32;
-            ptx::mma_bf16_tmem_a(d_tmem, a_tmem + kk * 8, ptx::smem_desc_sw128(baddr), idesc,
-                                 (kk > 0 || !fresh) ? 1u : 0u);
-          }
-          W4A16_TRACE_UNIT(11, i);
-          ptx::mma_commit(done_bar(i));
-          if (u.seg_last) {
-            ptx::mma_commit(&sh->dfull[db]);
-            ++seg;
-          }
-          W4A16_TRACE_UNIT(5, i);
-        }
-      }
-      // all MMAs of this thread complete before TMEM is freed
-      ptx::mma_commit(&sh->mma_done[mine]);
-      const uint64_t t0 = ptx::globaltimer_ns();
-      while (!ptx::mbar_try_wait(&sh->mma_done[mine], 0)) {
-        if (ptx::globaltimer_ns() - t0 > a.timeout_ns) {
-          wait_record_timeout(wc);
-          break;
-        }
-      }
-    }
-  } else if (warp >= kReadoutWarp0 && warp < kReadoutWarp0 + 4) {
-    // ------------------------------------------------------------ readout
-    const int quarter = warp & 3;
-    const int row = quarter * 32 + lane;
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    if constexpr (GRP) {
-      // Units come in pairs (lane 0's j-th unit, lane 1's j-th unit), behind
-      // one barrier that both lanes' MMA threads arrive on.  Per pair: one
-      // wait, both accumulators loaded, then acc += s * D for each unit in
-      // order.  Per unit only a countdown; tile, row and scale addresses are
-      // computed once per run ("segment") of the CTA.
-      float acc[BA];
-      // Scales: copied from global memory into a ring in shared memory
-      // kScaleAhead pairs before they are needed (per-thread asynchronous
-      // copies; each even lane copies its row's and the next row's scale).
-      uint16_t* const sring =
-          reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(sh) + sizeof(Shared));
-      SegCursor pf_cur;
-      pf_cur.init(sched);
-      int pf_left = 0;
-      const __half* pf_ptr = a.scales;
-      bool pf_ok = false;
-      auto prefetch_unit = [&](int jj) {
-        if (jj >= total) return;
-        if (pf_left == 0) {
-          Unit v;
-          int kb0;
-          pf_cur.next(v, kb0, pf_left, a.dp_tiles);
-          const int nn = (v.tile % a.n_tiles) * kTileW + row;
-          pf_ok = nn < a.N;   // N % 8 == 0: row nn + 1 exists too
-          pf_ptr = a.scales + static_cast<int64_t>(kb0) * a.N + nn;
-        } else {
-          pf_ptr += a.N;
-        }
-        --pf_left;
-        if ((lane & 1) == 0 && pf_ok)
-          ptx::cp_async_4(ptx::smem_u32(sring + (jj % kScaleRing) * kTileW + row), pf_ptr);
-      };
-#pragma unroll
-      for (int q = 0; q < kScaleAhead; ++q) {
-        prefetch_unit(2 * q);
-        prefetch_unit(2 * q + 1);
-        ptx::cp_async_commit();
-      }
-      // the current run
-      SegCursor cur;
-      cur.init(sched);
-      Unit seg;
-      int seg_left = 0;
-      bool first = true;
-      float bias_f = 0.0f;
-      auto open_run = [&]() {
-        int kb0;
-        cur.next(seg, kb0, seg_left, a.dp_tiles);
-        const int n = (seg.tile % a.n_tiles) * kTileW + row;
-        bias_f = (a.bias != nullptr && n < a.N) ? __bfloat162float(a.bias[n]) : 0.0f;
-        first = true;
-      };
-      if (total > 0) open_run();
-      // acc (+)= scale * D for one unit, 16 columns at a time; emits at the
-      // end of a run
-      auto accumulate = [&](float scale, const uint32_t* d, int c0) {
-#pragma unroll
-        for (int c = 0; c < 16; ++c)
-          acc[c0 + c] = first ? scale * __uint_as_float(d[c]) : fmaf(scale, __uint_as_float(d[c]), acc[c0 + c]);
-      };
-      auto finish_unit = [&](int i) {
-        first = false;
-        if (--seg_left == 0) {
-          emit_cols<BA, BA>(a, seg, row, 0, acc, bias_f);
-          if (i + 1 < total) open_run();
-        }
-      };
-      const int pairs = (total + 1) >> 1;
-      for (int q = 0; q < pairs; ++q) {
-        const int i0 = 2 * q;
-        const bool has1 = i0 + 1 < total;
-        const int dl = q % DL;
-        prefetch_unit(2 * (q + kScaleAhead));
-        prefetch_unit(2 * (q + kScaleAhead) + 1);
-        ptx::cp_async_commit();
-        ptx::cp_async_wait<kScaleAhead>();   // this pair's copies landed
-        __syncwarp();
-        const float s0 = __half2float(__ushort_as_half(sring[(i0 % kScaleRing) * kTileW + row]));
-        const float s1 = __half2float(__ushort_as_half(sring[((i0 + 1) % kScaleRing) * kTileW + row]));
-        if (threadIdx.x == 32 * kReadoutWarp0) W4A16_TRACE_UNIT(12, i0);
-        if (!wait_warp(&sh->pair_done[q % kPairRing], (q / kPairRing) & 1, wc)) break;
-        if (threadIdx.x == 32 * kReadoutWarp0 && q == 0) W4A16_TRACE_POINT(8);
-        if (threadIdx.x == 32 * kReadoutWarp0 && q == pairs - 1) W4A16_TRACE_POINT(9);
-        if (threadIdx.x == 32 * kReadoutWarp0) W4A16_TRACE_UNIT(6, i0);
-        ptx::tc_fence_after();
-        const uint32_t d0 = lane_base + C::kDCol + (0 + 2 * dl) * BA;
-        const uint32_t d1 = lane_base + C::kDCol + (1 + 2 * dl) * BA;
-        auto release = [&]() {
-          ptx::tc_fence_before();
-          __syncwarp();
-          if (lane == 0 && dl == DL - 1) {
-            ptx::mbar_arrive(&sh->dempty[0]);
-            if (has1) ptx::mbar_arrive(&sh->dempty[1]);
-          }
-          if (threadIdx.x == 32 * kReadoutWarp0) W4A16_TRACE_UNIT(7, i0);
-        };
-        if constexpr (BA == 16) {
-          // both accumulators with one TMEM wait
-          uint32_t r0[16], r1[16];
-          ptx::tmem_ld2_x16_sync(d0, d1, r0, r1);
-          release();
-          accumulate(s0, r0, 0);
-          finish_unit(i0);
-          if (has1) {
-            accumulate(s1, r1, 0);
-            finish_unit(i0 + 1);
-          }
-        } else {
-          // one unit at a time, 16 columns per TMEM load
-#pragma unroll 1
-          for (int h = 0; h <= (has1 ? 1 : 0); ++h) {
-#pragma unroll
-            for (int c0 = 0; c0 < BA; c0 += 16) {
-              uint32_t r[16];
-              ptx::tmem_ld_x16_sync((h ? d1 : d0) + c0, r);
-              accumulate(h ? s1 : s0, r, c0);
-            }
-            if (h == (has1 ? 1 : 0)) release();
-            finish_unit(i0 + h);
-          }
-        }
-      }
-      ptx::cp_async_wait<0>();   // no copy may land after exit
-    } else {
-      uint16_t bias_raw = 0;
-      int seg = 0;
-      for (int i = 0; i < total; ++i) {
-        const Unit u = it.next();
-        if (u.seg_first) {
-          const int n = (u.tile % a.n_tiles) * kTileW + row;
-          bias_raw = (a.bias != nullptr && n < a.N) ? __bfloat16_as_ushort(a.bias[n]) : 0;
-        }
-        if (!u.seg_last) continue;
-        const int db = seg % DB;
-        if (!wait_warp(&sh->dfull[db], (seg / DB) & 1, wc)) break;
-        ++seg;
-        ptx::tc_fence_after();
-#pragma unroll 1
-        for (int c0 = 0; c0 < BA; c0 += C::kChunk) {
-          float v[C::kChunk];
-          load_cols<C::kChunk>(lane_base + C::kDCol + db * BA + c0, v);
-          emit_cols<BA, C::kChunk>(a, u, row, c0, v, __bfloat162float(__ushort_as_bfloat16(bias_raw)));
-        }
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&sh->dempty[db]);
-      }
-    }
-  } else if (warp >= kDequantWarp0 && warp < kDequantWarp0 + 8) {
-    // ------------------------------------------------------------ dequant
-    // warpgroup wg converts units wg, wg + 2, ... (with two lanes: lane wg's
-    // units): every thread its whole row of 128 codes per unit
-    const int wg = (warp - kDequantWarp0) >> 2;
-    const int quarter = warp & 3;
-    const int row = quarter * 32 + lane;
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const uint32_t wrow0 = ptx::smem_u32(w_tile(0)) + row * 64;
-    const uint32_t swz = (row >> 1) & 3;
-    for (int i = wg; i < total; i += 2) {
-      int p, j;
-      lane_split<L>(i, p, j);
-      const int stage = stage_of(i);
-      const int as = astage_of(i);
-      if constexpr (L == 1 && (STAGES & 1) != 0) {
-        // With an odd stage count the uses of one stage alternate between
-        // the two warpgroups, so this warpgroup did not see the stage's
-        // previous phase (unit i - STAGES, the other warpgroup's), and a
-        // parity wait cannot tell that phase from this unit's.  The producer
-        // refills the stage only after the MMAs of unit i - STAGES completed,
-        // so waiting for those first proves the previous phase complete.
-        if (i >= STAGES && !wait_warp(done_bar(i - STAGES), done_parity(i - STAGES), wc)) break;
-      }
-      if (!wait_warp(&sh->full[stage], (j / SL) & 1, wc)) break;
-      if (i == 0 && threadIdx.x == 32 * kDequantWarp0) W4A16_TRACE_POINT(6);
-      if (threadIdx.x == 32 * kDequantWarp0) W4A16_TRACE_UNIT(1, i);
-
-      // the row's 64 B of packed codes, stored with the 64-byte swizzle:
-      // 16-byte chunk c of row r sits at chunk position c ^ ((r >> 1) & 3)
-      const uint32_t wrow = wrow0 + stage * C::kStage;
-      uint32_t words[16];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint4 v = ptx::lds128(wrow + ((q ^ swz) << 4));
-        words[4 * q + 0] = v.x;
-        words[4 * q + 1] = v.y;
-        words[4 * q + 2] = v.z;
-        words[4 * q + 3] = v.w;
-      }
-      float scale = 0.0f;
-      if constexpr (!GRP) scale = __half2float(s_tile(stage)[row]);
-
-      // the TMEM stage is free once the MMAs of the unit that used it
-      // (i - kAS, same lane) completed
-      if (i >= C::kAS && !wait_warp(done_bar(i - C::kAS), done_parity(i - C::kAS), wc)) break;
-      if (threadIdx.x == 32 * kDequantWarp0) W4A16_TRACE_UNIT(2, i);
-      ptx::tc_fence_after();
-      const uint32_t a_addr = lane_base + as * kAStageCols;
-      uint32_t s_hi2 = 0, s_lo2 = 0;
-      if constexpr (!GRP) {
-        const __nv_bfloat16 hi = __float2bfloat16_rn(scale);
-        const float lo_f = scale - __bfloat162float(hi);        // exact
-        const __nv_bfloat16 lo = __float2bfloat16_rn(lo_f);     // exact
-        const uint32_t hi_bits = static_cast<uint32_t>(__bfloat16_as_ushort(hi));
-        const uint32_t lo_bits = static_cast<uint32_t>(__bfloat16_as_ushort(lo));
-        s_hi2 = hi_bits | (hi_bits << 16);
-        s_lo2 = lo_bits | (lo_bits << 16);
-      }
-      // convert and store 16 columns (4 code words) at a time
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint32_t opnd[16];
-#pragma unroll
-        for (int w = 0; w < 4; ++w) codes_to_bf16(words[4 * q + w], &opnd[4 * w]);
-        if constexpr (!GRP) {
-#pragma unroll
-          for (int c = 0; c < 16; ++c) opnd[c] = scale_pair(opnd[c], s_hi2, s_lo2);
-        }
-        ptx::tmem_st_x16(a_addr + 16 * q, opnd);
-      }
-      ptx::tmem_st_wait();
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&sh->afull[as]);
-      if (threadIdx.x == 32 * kDequantWarp0) W4A16_TRACE_UNIT(3, i);
-      if (i >= total - 2 && threadIdx.x == 32 * kDequantWarp0) W4A16_TRACE_POINT(7);
-    }
-  }
-
-  // ------------------------------------------------------------- teardown
-  if (threadIdx.x == 32 * kReadoutWarp0) W4A16_TRACE_POINT(10);
-  ptx::tc_fence_before();
-  __syncthreads();
-  ptx::tc_fence_after();
-  if (warp == 1) ptx::tmem_dealloc(tmem, kTmemCols);
-  if (a.sk_units > 0) {
-    // split tiles: every CTA wrote its partials; after the grid barrier all
-    // CTAs reduce them together
-    if (threadIdx.x == 0) sh->reduce_ok = grid_barrier(a, wc) ? 1 : 0;
-    __syncthreads();
-    if (sh->reduce_ok) stream_k_reduce<BA>(a);
-  }
-  if (threadIdx.x == 32) W4A16_TRACE_POINT(11);
-}
 
 // One-thread kernel whose wait can never complete: exercises the bounded
 // wait and the error word without faulting or hanging the GPU.
@@ -982,84 +18,6 @@ __global__ void wait_timeout_selftest_kernel(uint32_t* err, uint64_t timeout_ns)
     (void)wait_one(&bar, 0, wc);   // nobody arrives: times out
   }
 }
-
-template <int BA, int L, bool GRP, int STAGES>
-cudaError_t launch_instance(const GemmSchedule& s, const GemmProblem& p, bool use_pdl,
-                            cudaStream_t stream) {
-  using C = Cfg<BA, L, GRP, STAGES>;
-  auto kernel = w4a16_gemm_tc_kernel<BA, L, GRP, STAGES>;
-
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  static bool attr_set[64] = {};
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!attr_set[dev]) {
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(C::kSmem));
-    if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
-  }
-
-  CUtensorMap tm_act, tm_w, tm_s;
-  // Activations as [K/64][M][64]: one box {64, BA, 2} brings both 64-wide K
-  // halves of a unit, in the same shared-memory order as two 2-D boxes.
-  int act_3d = 1;
-  if (encode_tmap_3d(&tm_act, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.A, 64, p.M, p.K / 64, p.K * 2, 128,
-                     64, BA, 2, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS) {
-    act_3d = 0;
-    if (encode_tmap_2d(&tm_act, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.A, p.K, p.M, p.K * 2, 64, BA,
-                       CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
-  // tiled code storage viewed as rows of 64 bytes: tile (tn, g) is rows
-  // (tn * K/128 + g) * 128 .. + 127
-  const uint64_t w_rows = static_cast<uint64_t>((p.N + kTileW - 1) / kTileW) * (p.K / kUnitK) * kTileW;
-  if (encode_tmap_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.packed, 64, w_rows, 64, 64, kTileW,
-                     CU_TENSOR_MAP_SWIZZLE_64B) != CUDA_SUCCESS)
-    return cudaErrorInvalidValue;
-  if (encode_tmap_2d(&tm_s, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.scales, p.N, p.K / kGroup, p.N * 2,
-                     kTileW, 1, CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
-    return cudaErrorInvalidValue;
-
-  Args a{};
-  a.M = static_cast<int>(p.M);
-  a.N = static_cast<int>(p.N);
-  a.K = static_cast<int>(p.K);
-  a.KB = static_cast<int>(p.K / kUnitK);
-  a.n_tiles = static_cast<int>((p.N + kTileW - 1) / kTileW);
-  a.dp_tiles = s.dp_tiles;
-  a.sk_units = static_cast<int>(s.sk_units);
-  a.act_3d = act_3d;
-  a.scales = static_cast<const __half*>(p.scales);
-  a.bias = static_cast<const __nv_bfloat16*>(p.bias);
-  a.Y = static_cast<__nv_bfloat16*>(p.Y);
-  a.counters = static_cast<uint32_t*>(p.workspace);
-  a.ws = reinterpret_cast<float*>(static_cast<uint8_t*>(p.workspace) + kCounterBytes);
-  a.err = p.error_word;
-  a.timeout_ns = p.timeout_ns;
-
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(s.grid));
-  cfg.blockDim = dim3(C::kThreads);
-  cfg.dynamicSmemBytes = C::kSmem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = use_pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kernel, tm_act, tm_w, tm_s, a);
-}
-
-// The compiled configurations: {act_tile, lanes, group_scale, stages}.
-#define W4A16_GEMM_INSTANCES(X) \
-  X(16, 2, true, 16)            \
-  X(32, 2, true, 12)            \
-  X(64, 2, true, 8)             \
-  X(64, 1, false, 8)            \
-  X(128, 1, false, 5)           \
-  X(256, 1, false, 3)
 
 }  // namespace
 
@@ -1085,12 +43,8 @@ size_t gemm_workspace_bytes(const GemmKernelConfig& c, const GemmSchedule& s, in
 
 cudaError_t launch_gemm_tc(const GemmKernelConfig& c, const GemmSchedule& s,
                            const GemmProblem& p, bool use_pdl, cudaStream_t stream) {
-#define W4A16_LAUNCH_CASE(BA, L, GRP, ST) \
-  if (c.act_tile == BA && c.lanes == L && c.group_scale == GRP && c.stages == ST) \
-    return launch_instance<BA, L, GRP, ST>(s, p, use_pdl, stream);
-  W4A16_GEMM_INSTANCES(W4A16_LAUNCH_CASE)
-#undef W4A16_LAUNCH_CASE
-  return cudaErrorInvalidConfiguration;
+  if (p.act_f16) return launch_gemm_tc_f16(c, s, p, use_pdl, stream);
+  return launch_gemm_tc_typed<false>(c, s, p, use_pdl, stream);
 }
 
 #ifdef W4A16_TRACE

@@ -46,6 +46,7 @@ struct GemmProblem {
   size_t workspace_bytes;
   uint32_t* error_word;
   uint64_t timeout_ns;
+  bool act_f16 = false;  // A, bias and Y are fp16 (else bf16)
 };
 
 // Number of tiles of a problem under a configuration.
@@ -72,6 +73,9 @@ bool gemm_config_available(const GemmKernelConfig& c);
 
 cudaError_t launch_gemm_tc(const GemmKernelConfig& c, const GemmSchedule& s,
                            const GemmProblem& p, bool use_pdl, cudaStream_t stream);
+// fp16-activation instantiation (gemm_tc_f16.cu), called by launch_gemm_tc.
+cudaError_t launch_gemm_tc_f16(const GemmKernelConfig& c, const GemmSchedule& s,
+                               const GemmProblem& p, bool use_pdl, cudaStream_t stream);
 
 // Failure-detection self test: one thread waits on an mbarrier nobody
 // arrives at, with a bounded wait; records a timeout in *error_word.

@@ -118,9 +118,10 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[tmem] * B[smem]^T, bf16 inputs, fp32 accumulate, one CTA.
-__device__ __forceinline__ void mma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                                uint32_t idesc, uint32_t accumulate) {
+// D[tmem] (+)= A[tmem] * B[smem]^T, 16-bit inputs (bf16 or fp16, as the
+// instruction descriptor says), fp32 accumulate, one CTA.
+__device__ __forceinline__ void mma_f16kind_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                   uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
@@ -148,6 +149,16 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
   d |= static_cast<uint64_t>(1) << 46;                    // descriptor version
   d |= static_cast<uint64_t>(2) << 61;                    // 128-byte swizzle
   return d;
+}
+
+// Instruction descriptor, kind::f16: A and B both of format `fmt` (0: fp16,
+// 1: bf16) -> fp32, both K-major.
+__host__ __device__ constexpr uint32_t idesc_f16kind_f32(int m, int n, uint32_t fmt) {
+  return (1u << 4)                                  // D format: f32
+         | (fmt << 7)                               // A format
+         | (fmt << 10)                              // B format
+         | (static_cast<uint32_t>(n >> 3) << 17)    // N / 8
+         | (static_cast<uint32_t>(m >> 4) << 24);   // M / 16
 }
 
 // Instruction descriptor, kind::f16: bf16 x bf16 -> fp32, both K-major.

@@ -43,6 +43,11 @@ def to_bf16(x: np.ndarray) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16)
 
 
+def to_f16(x: np.ndarray) -> torch.Tensor:
+    """float32 numpy -> fp16 CPU tensor (round to nearest even)."""
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.float16)
+
+
 def bits(t: torch.Tensor) -> np.ndarray:
     """Raw 16-bit patterns of a bf16/fp16 CPU tensor as a uint16 numpy array."""
     if t.dtype not in (torch.bfloat16, torch.float16):
@@ -60,14 +65,17 @@ def draw_weight(rng: np.random.Generator, N: int, K: int, wdist: str) -> np.ndar
     return w
 
 
-def draw(case: Case):
-    """Return ``(W bf16 [N,K], A bf16 [M,K], bias bf16 [N] or None)`` on CPU."""
+def draw(case: Case, act: str = "bf16"):
+    """Return ``(W bf16 [N,K], A [M,K], bias [N] or None)`` on CPU; A and the
+    bias in the activation type ``act`` ("bf16" or "f16"), from the same
+    float32 draws."""
     rng = np.random.default_rng(case.seed)
+    cast = to_bf16 if act == "bf16" else to_f16
     w = to_bf16(draw_weight(rng, case.N, case.K, case.wdist))
-    a = to_bf16(rng.standard_normal((case.M, case.K), dtype=np.float32))
+    a = cast(rng.standard_normal((case.M, case.K), dtype=np.float32))
     b = None
     if case.bias:
-        b = to_bf16(rng.standard_normal(case.N, dtype=np.float32) * np.float32(0.5))
+        b = cast(rng.standard_normal(case.N, dtype=np.float32) * np.float32(0.5))
     return w, a, b
 
 
