@@ -184,6 +184,8 @@ def run_gpu(args, rank, world):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
     torch.cuda.set_device(dev)
     cases = synthetic.WORKLOADS[args.workload]
+    if args.grouped and len(cases) > w4.MAX_GROUP:
+        raise SystemExit(f"--grouped takes at most {w4.MAX_GROUP} projections")
     if args.tune:
         for c in cases:
             w4.w4a16_tune(c.M, c.N, c.K)
@@ -207,23 +209,48 @@ def run_gpu(args, rank, world):
                           Y=torch.empty(c.M, c.N, dtype=act_dtype, device=dev)))
         sets.append(s)
     ws_bytes = max(w4.w4a16_gemm_workspace_bytes_max(c.M, c.N, c.K) for c in cases)
+    if args.grouped:
+        probs, _, _ = w4._gemm_problems([s["A"] for s in sets[0]], [s["packed"] for s in sets[0]],
+                                        [s["scales"] for s in sets[0]], None,
+                                        [s["Y"] for s in sets[0]])
+        ws_bytes = max(ws_bytes, w4.lib().w4a16_gemm_grouped_workspace_bytes(probs, len(cases), -1))
     ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    n_k = 2 * len(cases)
+    n_k = 2 if args.grouped else 2 * len(cases)
 
-    def step(r, evs=None):
+    def run_step(r, st, evs):
+        """One step on stream `st`: per projection quantize then GEMM, or
+        (--grouped) one grouped quantize then one grouped GEMM."""
+        if args.grouped:
+            sset = sets[r % copies]
+            if evs is not None:
+                evs[0][0].record(st)
+            w4.w4a16_quantize_grouped([s["W"] for s in sset],
+                                      outs=[(s["packed"], s["scales"]) for s in sset], stream=st)
+            if evs is not None:
+                evs[0][1].record(st)
+                evs[1][0].record(st)
+            w4.w4a16_gemm_grouped([s["A"] for s in sset], [s["packed"] for s in sset],
+                                  [s["scales"] for s in sset], Ys=[s["Y"] for s in sset],
+                                  workspace=ws, stream=st)
+            if evs is not None:
+                evs[1][1].record(st)
+            return
         for j, c in enumerate(cases):
             s = sets[r % copies][j]
             if evs is not None:
-                evs[2 * j][0].record(stream)
-            w4.w4a16_quantize(s["W"], packed=s["packed"], scales=s["scales"])
+                evs[2 * j][0].record(st)
+            w4.w4a16_quantize(s["W"], packed=s["packed"], scales=s["scales"], stream=st)
             if evs is not None:
-                evs[2 * j][1].record(stream)
-                evs[2 * j + 1][0].record(stream)
-            w4.w4a16_gemm(s["A"], s["packed"], s["scales"], Y=s["Y"], workspace=ws)
+                evs[2 * j][1].record(st)
+                evs[2 * j + 1][0].record(st)
+            w4.w4a16_gemm(s["A"], s["packed"], s["scales"], Y=s["Y"], workspace=ws, stream=st)
             if evs is not None:
-                evs[2 * j + 1][1].record(stream)
+                evs[2 * j + 1][1].record(st)
+
+    def step(r, evs=None):
+        run_step(r, stream, evs)
 
     # eager warm-up (also sets kernel attributes outside any capture)
     for r in range(min(args.warmup, copies)):
@@ -252,17 +279,7 @@ def run_gpu(args, rank, world):
         return g, evs, w4.w4a16_launch_count() - l0
 
     def step_on(r, st, evs):
-        for j, c in enumerate(cases):
-            s = sets[r % copies][j]
-            if evs is not None:
-                evs[2 * j][0].record(st)
-            w4.w4a16_quantize(s["W"], packed=s["packed"], scales=s["scales"], stream=st)
-            if evs is not None:
-                evs[2 * j][1].record(st)
-                evs[2 * j + 1][0].record(st)
-            w4.w4a16_gemm(s["A"], s["packed"], s["scales"], Y=s["Y"], workspace=ws, stream=st)
-            if evs is not None:
-                evs[2 * j + 1][1].record(st)
+        run_step(r, st, evs)
 
     g_warm, _, _ = capture(args.warmup, 0, False)
     g_timed, _, launches_per_replay = capture(args.steps, args.warmup, False)
@@ -304,10 +321,19 @@ def run_gpu(args, rank, world):
             j, is_gemm = divmod(k, 2)
             with torch.cuda.graph(gk):
                 for r in range(args.steps):
-                    s = sets[(args.warmup + r) % copies][j]
-                    if is_gemm:
+                    sset = sets[(args.warmup + r) % copies]
+                    if args.grouped and is_gemm:
+                        w4.w4a16_gemm_grouped([s["A"] for s in sset], [s["packed"] for s in sset],
+                                              [s["scales"] for s in sset], Ys=[s["Y"] for s in sset],
+                                              workspace=ws)
+                    elif args.grouped:
+                        w4.w4a16_quantize_grouped([s["W"] for s in sset],
+                                                  outs=[(s["packed"], s["scales"]) for s in sset])
+                    elif is_gemm:
+                        s = sset[j]
                         w4.w4a16_gemm(s["A"], s["packed"], s["scales"], Y=s["Y"], workspace=ws)
                     else:
+                        s = sset[j]
                         w4.w4a16_quantize(s["W"], packed=s["packed"], scales=s["scales"])
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             gk.replay()
@@ -325,24 +351,23 @@ def run_gpu(args, rank, world):
     h2d = sum(W.numel() * 2 + A.numel() * 2 for W, A in pinned)
     d2h = sum(c.M * c.N * 2 for c in cases)
     s0 = sets[0]
-    for _ in range(2):
+
+    def e2e_step():
         for j, c in enumerate(cases):
             s0[j]["W"].copy_(pinned[j][0], non_blocking=True)
             s0[j]["A"].copy_(pinned[j][1], non_blocking=True)
-            w4.w4a16_quantize(s0[j]["W"], packed=s0[j]["packed"], scales=s0[j]["scales"])
-            w4.w4a16_gemm(s0[j]["A"], s0[j]["packed"], s0[j]["scales"], Y=s0[j]["Y"], workspace=ws)
+        run_step(0, stream, None)
+        for j, c in enumerate(cases):
             yh[j].copy_(s0[j]["Y"], non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
     torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     e0.record(stream)
     for _ in range(args.steps):
-        for j, c in enumerate(cases):
-            s0[j]["W"].copy_(pinned[j][0], non_blocking=True)
-            s0[j]["A"].copy_(pinned[j][1], non_blocking=True)
-            w4.w4a16_quantize(s0[j]["W"], packed=s0[j]["packed"], scales=s0[j]["scales"])
-            w4.w4a16_gemm(s0[j]["A"], s0[j]["packed"], s0[j]["scales"], Y=s0[j]["Y"], workspace=ws)
-            yh[j].copy_(s0[j]["Y"], non_blocking=True)
+        e2e_step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
     barrier()
@@ -358,7 +383,16 @@ def run_gpu(args, rank, world):
 
     peaks = load_peaks()
     kernels = []
-    for j, c in enumerate(cases):
+    if args.grouped:
+        tq, tg = kern_ms[0], kern_ms[1]
+        qb = sum(quant_bytes(c.N, c.K) for c in cases)
+        gb = sum(gemm_bytes(c.M, c.N, c.K) for c in cases)
+        kernels.append(dict(kernel="rtn_quantize", grouped=len(cases), us=round(tq * 1e3, 3),
+                            gbs=round(qb / (tq * 1e-3) / 1e9, 1)))
+        kernels.append(dict(kernel="w4a16_gemm_tc", grouped=len(cases), us=round(tg * 1e3, 3),
+                            tflops=round(flops_step / (tg * 1e-3) / 1e12, 2),
+                            gbs=round(gb / (tg * 1e-3) / 1e9, 1)))
+    for j, c in enumerate([] if args.grouped else cases):
         tq, tg = kern_ms[2 * j], kern_ms[2 * j + 1]
         kernels.append(dict(kernel="rtn_quantize", shape=[c.N, c.K], us=round(tq * 1e3, 3),
                             gbs=round(quant_bytes(c.N, c.K) / (tq * 1e-3) / 1e9, 1)))
@@ -370,13 +404,14 @@ def run_gpu(args, rank, world):
     # dominant kernel: the kind with the larger share of kernel time
     t_q = sum(kern_ms[0::2])
     t_g = sum(kern_ms[1::2])
+    launches_kind = 1 if args.grouped else len(cases)
     if t_q >= t_g:
         dom, dom_bytes = "rtn_quantize", sum(quant_bytes(c.N, c.K) for c in cases)
-        dom_ms, launches_dom = t_q, len(cases)
+        dom_ms, launches_dom = t_q, launches_kind
         bound, achieved, peak, unit = "hbm", None, peaks["hbm_gbs"], "GB/s"
         achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
     else:
-        dom_ms, launches_dom = t_g, len(cases)
+        dom_ms, launches_dom = t_g, launches_kind
         big = max(cases, key=lambda c: gemm_flops(c.M, c.N, c.K) / max(gemm_bytes(c.M, c.N, c.K), 1))
         ai = gemm_flops(big.M, big.N, big.K) / gemm_bytes(big.M, big.N, big.K)
         tensor_bound = ai > peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
@@ -387,7 +422,7 @@ def run_gpu(args, rank, world):
         else:
             bound, peak, unit = "hbm", peaks["hbm_gbs"], "GB/s"
             achieved = sum(gemm_bytes(c.M, c.N, c.K) for c in cases) / (dom_ms * 1e-3) / 1e9
-    traffic = dram_traffic(dom, args.workload)
+    traffic = dram_traffic(dom, args.workload + ("_grouped" if args.grouped else ""))
     roofline = dict(bound=bound, achieved=round(achieved, 2), peak=peak, unit=unit,
                     frac=round(achieved / peak, 4),
                     traffic=None if traffic is None else traffic,
@@ -398,7 +433,9 @@ def run_gpu(args, rank, world):
                scaling="weak", vs_baseline=None, dtype=args.act, data="synthetic",
                config=dict(workload=args.workload, activations=args.act,
                            shapes=[[c.M, c.N, c.K] for c in cases],
-                           step="rtn_quantize + w4a16_gemm per projection",
+                           step=("one grouped rtn_quantize launch over all projections + one grouped "
+                                 "w4a16_gemm launch" if args.grouped else
+                                 "rtn_quantize + w4a16_gemm per projection"),
                            l2="inputs rotate over %d copies (%.0f MB > 3x L2)" % (copies, copies * per_copy / 2**20),
                            parallelism=f"replicas x{world}"),
                gemm=dict(tflops=round(job_rate(flops_step, args.steps, elapsed_ms, world) / 1e12, 3)),
@@ -455,6 +492,9 @@ def main():
                     choices=["tiny", "expert_m50", "prefix_m816", "sweep", "large"])
     ap.add_argument("--act", default="bf16", choices=["bf16", "f16"],
                     help="activation type of the GEMMs (A, bias, Y)")
+    ap.add_argument("--grouped", action="store_true",
+                    help="one grouped quantize and one grouped GEMM launch per step (the "
+                         "projections are independent problems)")
     ap.add_argument("--tune", action="store_true", help="tune the variant table first")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

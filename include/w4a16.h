@@ -196,6 +196,53 @@ void w4a16_table_clear(void);
 int w4a16_table_save(const char* path);
 int w4a16_table_load(const char* path);
 
+/* ----------------------------------------------------------------- groups
+ * Independent problems in one launch: "Kernel dispatch and Humming
+ * quantization in PhyAI", section "Humming makes the separation useful",
+ * quantizes the attention and MLP projections of a block (qkv, o, gate_up,
+ * down); with few tokens each of those GEMMs is too small to fill the GPU
+ * and pays a full launch, so the library can run a set of them together.
+ * Each problem runs on its own share of the CTAs (in proportion to its
+ * work); the problems must be independent: no output of one may be an input
+ * or output of another. */
+#define W4A16_MAX_GROUP 8
+
+typedef struct {
+  const void* A;             /* [M, K] activations (bf16; fp16 when act_f16) */
+  const void* packed;        /* tiled codes of the [N, K] weight            */
+  const void* scales;        /* [K/128, N] fp16                             */
+  const void* bias_or_null;  /* [N], activation type, or NULL               */
+  void* Y;                   /* [M, N], activation type                     */
+  int64_t M, N, K;
+} w4a16_gemm_problem;
+
+typedef struct {
+  const void* W_bf16;        /* [N, K] bf16 */
+  int64_t N, K;
+  void* packed_out;          /* w4a16_packed_bytes(N, K) bytes */
+  void* scales_out;          /* (K/128) * N fp16 */
+} w4a16_quantize_problem;
+
+/* w4a16_quantize for `count` (1 .. W4A16_MAX_GROUP) weights in one launch.
+ * Same per-problem contract as w4a16_quantize; argument errors of any
+ * problem are returned before anything is launched. */
+int w4a16_quantize_grouped(const w4a16_quantize_problem* problems, int count, int group,
+                           void* stream);
+
+/* Workspace the grouped GEMM needs for these problems (variant = -1: the one
+ * the library chooses; else that catalogue entry).  0 if none is needed or
+ * the arguments are invalid.  Same zero-once rule as w4a16_gemm. */
+size_t w4a16_gemm_grouped_workspace_bytes(const w4a16_gemm_problem* problems, int count,
+                                          int variant);
+
+/* `count` (1 .. W4A16_MAX_GROUP) independent W4A16 GEMMs in one launch:
+ * problem i computes Y_i = A_i . dequant(W_i)^T + bias_i as w4a16_gemm (or
+ * w4a16_gemm_f16 when act_f16 != 0).  One variant serves the whole group
+ * (variant = -1: chosen by the library).  Argument errors of any problem are
+ * returned before anything is launched. */
+int w4a16_gemm_grouped(const w4a16_gemm_problem* problems, int count, int group, int act_f16,
+                       int variant, void* workspace, size_t workspace_bytes, void* stream);
+
 /* ------------------------------------------------------------ diagnostics */
 
 /*

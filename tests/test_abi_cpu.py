@@ -122,3 +122,30 @@ def test_binding_rejects_cpu_tensors(built_lib):
     W = torch.zeros(256, 512, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         w4.w4a16_quantize(W)
+
+
+def test_group_structs_match_the_header():
+    # two pointer-sized fields per line of the C structs, no padding
+    assert ctypes.sizeof(w4.GemmProblem) == 5 * 8 + 3 * 8
+    assert ctypes.sizeof(w4.QuantizeProblem) == 8 + 2 * 8 + 2 * 8
+    text = open(HEADER).read()
+    assert "#define W4A16_MAX_GROUP 8" in text and w4.MAX_GROUP == 8
+
+
+def test_grouped_argument_errors_before_launch(built_lib):
+    L = w4.lib()
+    P = (w4.GemmProblem * 9)()
+    for i in range(9):
+        P[i] = w4.GemmProblem(16, 16, 16, None, 16, 4, 256, 512)
+    assert L.w4a16_gemm_grouped(P, 0, 128, 0, -1, None, 0, None) == w4.W4A16_ERR_INVALID_ARG
+    assert L.w4a16_gemm_grouped(P, 9, 128, 0, -1, None, 0, None) == w4.W4A16_ERR_UNSUPPORTED
+    assert L.w4a16_gemm_grouped(P, 2, 64, 0, -1, None, 0, None) == w4.W4A16_ERR_UNSUPPORTED
+    P[1] = w4.GemmProblem(16, 16, 16, None, 16, 4, 256, 500)      # K not a multiple of 128
+    assert L.w4a16_gemm_grouped(P, 2, 128, 0, -1, None, 0, None) == w4.W4A16_ERR_UNSUPPORTED
+    P[1] = w4.GemmProblem(24, 16, 16, None, 16, 4, 256, 512)      # A not 16-byte aligned
+    assert L.w4a16_gemm_grouped(P, 2, 128, 0, -1, None, 0, None) == w4.W4A16_ERR_ALIGNMENT
+    Q = (w4.QuantizeProblem * 2)()
+    Q[0] = w4.QuantizeProblem(16, 256, 512, 16, 16)
+    Q[1] = w4.QuantizeProblem(16, 250, 512, 16, 16)               # N not a multiple of 8
+    assert L.w4a16_quantize_grouped(Q, 2, 128, None) == w4.W4A16_ERR_UNSUPPORTED
+    assert L.w4a16_quantize_grouped(Q, 0, 128, None) == w4.W4A16_ERR_INVALID_ARG

@@ -31,6 +31,21 @@ W4A16_ERR_TIMEOUT = 7
 
 # (name, restype, argtypes) of every symbol the C header declares.
 _c_int64, _c_size, _vp = ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p
+class GemmProblem(ctypes.Structure):
+    """Mirror of w4a16_gemm_problem (include/w4a16.h)."""
+    _fields_ = [("A", ctypes.c_void_p), ("packed", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("bias_or_null", ctypes.c_void_p), ("Y", ctypes.c_void_p),
+                ("M", ctypes.c_int64), ("N", ctypes.c_int64), ("K", ctypes.c_int64)]
+
+
+class QuantizeProblem(ctypes.Structure):
+    """Mirror of w4a16_quantize_problem (include/w4a16.h)."""
+    _fields_ = [("W_bf16", ctypes.c_void_p), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("packed_out", ctypes.c_void_p), ("scales_out", ctypes.c_void_p)]
+
+
+MAX_GROUP = 8
+
 SIGNATURES = [
     ("w4a16_status_string", ctypes.c_char_p, [ctypes.c_int]),
     ("w4a16_packed_bytes", _c_size, [_c_int64, _c_int64]),
@@ -43,6 +58,13 @@ SIGNATURES = [
      [_vp, _c_int64, _c_int64, _c_int64, _vp, _vp, ctypes.c_int, _vp, _vp, _vp, _c_size, _vp]),
     ("w4a16_gemm_f16", ctypes.c_int,
      [_vp, _c_int64, _c_int64, _c_int64, _vp, _vp, ctypes.c_int, _vp, _vp, _vp, _c_size, _vp]),
+    ("w4a16_quantize_grouped", ctypes.c_int,
+     [ctypes.POINTER(QuantizeProblem), ctypes.c_int, ctypes.c_int, _vp]),
+    ("w4a16_gemm_grouped_workspace_bytes", _c_size,
+     [ctypes.POINTER(GemmProblem), ctypes.c_int, ctypes.c_int]),
+    ("w4a16_gemm_grouped", ctypes.c_int,
+     [ctypes.POINTER(GemmProblem), ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _vp,
+      _c_size, _vp]),
     ("w4a16_variant_count", ctypes.c_int, []),
     ("w4a16_variant_name", ctypes.c_char_p, [ctypes.c_int]),
     ("w4a16_variant_eligible", ctypes.c_int, [ctypes.c_int, _c_int64, _c_int64, _c_int64]),
@@ -245,6 +267,84 @@ def w4a16_gemm(A: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor,
                 bias_ptr, Y.data_ptr(), ws_ptr, ws_bytes, sh)
     _check(st, "w4a16_gemm_f16" if f16 else "w4a16_gemm")
     return Y
+
+
+# ----------------------------------------------------------------- groups
+def w4a16_quantize_grouped(weights, outs=None, stream=None):
+    """RTN-quantize several bf16 weights in one launch.  Returns a list of
+    ``(packed, scales)`` as ``w4a16_quantize`` would (``outs`` may supply
+    those buffers)."""
+    if not 1 <= len(weights) <= MAX_GROUP:
+        raise ValueError(f"1 .. {MAX_GROUP} weights")
+    given = outs
+    outs, probs = [], (QuantizeProblem * len(weights))()
+    for i, W in enumerate(weights):
+        _require_cuda(W, "W", torch.bfloat16)
+        N, K = W.shape
+        if given is not None:
+            packed, scales = given[i]
+            _require_cuda(packed, "packed", torch.uint8)
+            _require_cuda(scales, "scales", torch.float16)
+            if packed.numel() != lib().w4a16_packed_bytes(N, K) or scales.shape != (K // GROUP, N):
+                raise ValueError("packed / scales of the wrong size")
+        else:
+            packed = torch.empty(lib().w4a16_packed_bytes(N, K), dtype=torch.uint8, device=W.device)
+            scales = torch.empty((K // GROUP, N), dtype=torch.float16, device=W.device)
+        probs[i] = QuantizeProblem(W.data_ptr(), N, K, packed.data_ptr(), scales.data_ptr())
+        outs.append((packed, scales))
+    _check(lib().w4a16_quantize_grouped(probs, len(weights), GROUP,
+                                        _stream_handle(weights[0].device, stream)),
+           "w4a16_quantize_grouped")
+    return outs
+
+
+def _gemm_problems(As, packeds, scales_list, biases, Ys):
+    n = len(As)
+    if not 1 <= n <= MAX_GROUP or not (len(packeds) == len(scales_list) == n):
+        raise ValueError(f"1 .. {MAX_GROUP} problems with matching argument lists")
+    act = As[0].dtype if As[0].dtype in (torch.bfloat16, torch.float16) else torch.bfloat16
+    biases = biases if biases is not None else [None] * n
+    Ys = Ys if Ys is not None else [None] * n
+    probs, outs = (GemmProblem * n)(), []
+    for i in range(n):
+        A, packed, scales, bias, Y = As[i], packeds[i], scales_list[i], biases[i], Ys[i]
+        _require_cuda(A, "A", act)
+        _require_cuda(packed, "packed", torch.uint8)
+        _require_cuda(scales, "scales", torch.float16)
+        M, K = A.shape
+        N = scales.shape[1]
+        if scales.shape[0] * GROUP != K:
+            raise ValueError("scales must be [K/128, N]")
+        if packed.numel() != lib().w4a16_packed_bytes(N, K):
+            raise ValueError("packed must hold w4a16_packed_bytes(N, K) bytes of tiled codes")
+        if bias is not None:
+            _require_cuda(bias, "bias", act)
+        if Y is None:
+            Y = torch.empty((M, N), dtype=act, device=A.device)
+        _require_cuda(Y, "Y", act)
+        probs[i] = GemmProblem(A.data_ptr(), packed.data_ptr(), scales.data_ptr(),
+                               bias.data_ptr() if bias is not None else None, Y.data_ptr(), M, N, K)
+        outs.append(Y)
+    return probs, outs, act
+
+
+def w4a16_gemm_grouped(As, packeds, scales_list, biases=None, Ys=None, workspace=None,
+                       stream=None, variant=None):
+    """Independent W4A16 GEMMs ``Y_i = A_i @ dequant(W_i)^T + bias_i`` in one
+    launch (bf16 or fp16 activations, all of one type).  Returns the Y's."""
+    probs, outs, act = _gemm_problems(As, packeds, scales_list, biases, Ys)
+    n = len(outs)
+    L = lib()
+    v = -1 if variant is None else variant
+    need = L.w4a16_gemm_grouped_workspace_bytes(probs, n, v)
+    sh = _stream_handle(As[0].device, stream)
+    if workspace is None:
+        workspace = _default_ws.get(As[0].device, sh, need)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(L.w4a16_gemm_grouped(probs, n, GROUP, 1 if act == torch.float16 else 0, v, ws_ptr,
+                                ws_bytes, sh), "w4a16_gemm_grouped")
+    return outs
 
 
 # --------------------------------------------------------------- variants

@@ -12,6 +12,7 @@
 #include <cudaTypedefs.h>
 
 #include <atomic>
+#include <algorithm>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -308,6 +309,102 @@ int run_gemm(int id, const void* A, int64_t M, int64_t N, int64_t K, const void*
   return W4A16_OK;
 }
 
+// ------------------------------------------------------------ groups
+// A group of independent GEMMs runs in one launch, problem i on its own
+// sub-grid of CTAs.  Planning picks one variant for the group: CTAs are
+// shared out in proportion to each problem's units (at least one each, no
+// more than the SMs in total, so every sub-grid is resident at once), each
+// problem gets that variant's schedule on its share, and the variant whose
+// slowest problem has the smallest estimate wins.  Workspace: the fixed
+// counter region (problem i's grid-barrier words at 2 i, 2 i + 1), then each
+// split problem's partial slots.
+struct GroupPlan {
+  int variant = -1;
+  GemmSchedule s[kMaxGemmGroup];
+  size_t partial_off[kMaxGemmGroup];
+  size_t ws_bytes = 0;
+  double est_us = 0.0;
+};
+
+bool plan_for_variant(int id, const w4a16_gemm_problem* pr, int count, int sms, GroupPlan& plan) {
+  const Variant& v = kVariants[id];
+  int64_t units[kMaxGemmGroup];
+  int64_t total = 0;
+  for (int i = 0; i < count; ++i) {
+    if (!variant_eligible(id, pr[i].M, pr[i].N, pr[i].K)) return false;
+    units[i] = gemm_tiles(v.cfg, pr[i].M, pr[i].N) * (pr[i].K / kGroup);
+    total += units[i];
+  }
+  if (count > sms) return false;
+  int ctas[kMaxGemmGroup];
+  int used = 0;
+  for (int i = 0; i < count; ++i) {
+    int64_t c = (static_cast<int64_t>(sms) * units[i]) / total;
+    if (c < 1) c = 1;
+    ctas[i] = static_cast<int>(c);
+    used += ctas[i];
+  }
+  while (used > sms) {   // rounding up the small ones may overshoot
+    int big = 0;
+    for (int i = 1; i < count; ++i) big = ctas[i] > ctas[big] ? i : big;
+    --ctas[big];
+    --used;
+  }
+  while (used < sms) {   // spare SMs to the problems with most units per CTA
+    int best = 0;
+    for (int i = 1; i < count; ++i)
+      if (units[i] * ctas[best] > units[best] * ctas[i]) best = i;
+    ++ctas[best];
+    ++used;
+  }
+  plan.variant = id;
+  plan.est_us = 0.0;
+  size_t off = 0;
+  bool split = false;
+  for (int i = 0; i < count; ++i) {
+    plan.s[i] = make_schedule(v, pr[i].M, pr[i].N, pr[i].K, ctas[i]);
+    plan.est_us = std::max(plan.est_us, estimate_us(v, pr[i].M, pr[i].N, pr[i].K, ctas[i]));
+    plan.partial_off[i] = off;
+    if (plan.s[i].sk_units > 0) {
+      split = true;
+      off += (gemm_workspace_bytes(v.cfg, plan.s[i], pr[i].M, pr[i].N, pr[i].K) - kCounterBytes +
+              255) / 256 * 256;
+    }
+  }
+  plan.ws_bytes = split ? kCounterBytes + off : 0;
+  return true;
+}
+
+int plan_group(const w4a16_gemm_problem* pr, int count, int variant, GroupPlan& plan) {
+  DeviceInfo dev;
+  const int sms = std::min(device_info(dev) ? dev.num_sms : kDefaultSms, kMaxGrid);
+  if (variant >= 0) {
+    if (variant >= kNumVariants) return W4A16_ERR_UNSUPPORTED;
+    return plan_for_variant(variant, pr, count, sms, plan) ? W4A16_OK : W4A16_ERR_NO_VARIANT;
+  }
+  bool found = false;
+  for (int id = 0; id < kNumVariants; ++id) {
+    GroupPlan cand;
+    if (!plan_for_variant(id, pr, count, sms, cand)) continue;
+    if (!found || cand.est_us < plan.est_us) {
+      plan = cand;
+      found = true;
+    }
+  }
+  return found ? W4A16_OK : W4A16_ERR_NO_VARIANT;
+}
+
+int check_group_args(const w4a16_gemm_problem* pr, int count, int group) {
+  if (pr == nullptr || count < 1) return W4A16_ERR_INVALID_ARG;
+  if (count > kMaxGemmGroup) return W4A16_ERR_UNSUPPORTED;
+  for (int i = 0; i < count; ++i) {
+    const int st = check_gemm_args(pr[i].A, pr[i].M, pr[i].N, pr[i].K, pr[i].packed, pr[i].scales,
+                                   group, pr[i].bias_or_null, pr[i].Y);
+    if (st != W4A16_OK) return st;
+  }
+  return W4A16_OK;
+}
+
 size_t variant_ws(int id, int64_t M, int64_t N, int64_t K) {
   DeviceInfo dev;
   int sms = kDefaultSms;
@@ -500,6 +597,87 @@ size_t w4a16_variant_workspace_bytes(int variant, int64_t M, int64_t N, int64_t 
 }
 
 int w4a16_select_variant(int64_t M, int64_t N, int64_t K) { return select_variant(M, N, K); }
+
+size_t w4a16_gemm_grouped_workspace_bytes(const w4a16_gemm_problem* problems, int count,
+                                          int variant) {
+  if (check_group_args(problems, count, kGroup) != W4A16_OK) return 0;
+  GroupPlan plan;
+  if (plan_group(problems, count, variant, plan) != W4A16_OK) return 0;
+  return plan.ws_bytes;
+}
+
+int w4a16_gemm_grouped(const w4a16_gemm_problem* problems, int count, int group, int act_f16,
+                       int variant, void* workspace, size_t workspace_bytes, void* stream) {
+  int st = check_group_args(problems, count, group);
+  if (st != W4A16_OK) return st;
+  GroupPlan plan;
+  st = plan_group(problems, count, variant, plan);
+  if (st != W4A16_OK) return st;
+  if (plan.ws_bytes > 0) {
+    if (workspace == nullptr || workspace_bytes < plan.ws_bytes) return W4A16_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return W4A16_ERR_ALIGNMENT;
+  }
+  DeviceInfo dev;
+  if (!device_info(dev)) return W4A16_ERR_CUDA;
+  const Variant& v = kVariants[plan.variant];
+  GemmGroup grp;
+  grp.count = count;
+  for (int i = 0; i < count; ++i) {
+    GemmProblem& p = grp.p[i];
+    p.A = problems[i].A;
+    p.packed = problems[i].packed;
+    p.scales = problems[i].scales;
+    p.bias = problems[i].bias_or_null;
+    p.Y = problems[i].Y;
+    p.M = problems[i].M;
+    p.N = problems[i].N;
+    p.K = problems[i].K;
+    p.workspace = workspace;
+    p.workspace_bytes = workspace_bytes;
+    uint8_t* base = static_cast<uint8_t*>(workspace);
+    p.counters = base ? reinterpret_cast<uint32_t*>(base) + 2 * i : nullptr;
+    p.partials = base ? reinterpret_cast<float*>(base + kCounterBytes + plan.partial_off[i]) : nullptr;
+    p.error_word = dev.error_word;
+    p.timeout_ns = g_timeout_ns.load();
+    p.act_f16 = act_f16 != 0;
+    grp.s[i] = plan.s[i];
+  }
+  if (log_enabled())
+    std::fprintf(stderr, "w4a16: grouped gemm of %d, variant=%s, estimate %.1f us\n", count, v.name,
+                 plan.est_us);
+  const cudaError_t e = launch_gemm_tc_group(v.cfg, grp, /*use_pdl=*/true,
+                                             static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_failure(e, v.name);
+  g_launches.fetch_add(1);
+  return W4A16_OK;
+}
+
+int w4a16_quantize_grouped(const w4a16_quantize_problem* problems, int count, int group,
+                           void* stream) {
+  if (problems == nullptr || count < 1) return W4A16_ERR_INVALID_ARG;
+  if (count > kMaxQuantizeGroup) return W4A16_ERR_UNSUPPORTED;
+  if (group != kGroup) return W4A16_ERR_UNSUPPORTED;
+  QuantizeProblem qp[kMaxQuantizeGroup];
+  for (int i = 0; i < count; ++i) {
+    const w4a16_quantize_problem& p = problems[i];
+    if (p.W_bf16 == nullptr || p.packed_out == nullptr || p.scales_out == nullptr)
+      return W4A16_ERR_INVALID_ARG;
+    if (p.N < 1 || p.K < 1) return W4A16_ERR_INVALID_ARG;
+    if (p.K % kGroup != 0 || p.N % 8 != 0) return W4A16_ERR_UNSUPPORTED;
+    if (p.N >= (1ll << 31) || p.K >= (1ll << 31) || p.N * p.K >= (1ll << 40))
+      return W4A16_ERR_UNSUPPORTED;
+    if (!aligned16(p.W_bf16) || !aligned16(p.packed_out) || !aligned16(p.scales_out))
+      return W4A16_ERR_ALIGNMENT;
+    qp[i] = QuantizeProblem{p.W_bf16, p.N, p.K, p.packed_out, p.scales_out};
+  }
+  DeviceInfo dev;
+  if (!device_info(dev)) return W4A16_ERR_CUDA;
+  const cudaError_t e = launch_rtn_quantize_group(qp, count, dev.num_sms, dev.error_word,
+                                                  g_timeout_ns.load(), static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_failure(e, "rtn_quantize (grouped)");
+  g_launches.fetch_add(1);
+  return W4A16_OK;
+}
 
 int w4a16_gemm_f16(const void* A_f16, int64_t M, int64_t N, int64_t K, const void* packed,
                    const void* scales, int group, const void* bias_f16_or_null, void* Y_f16,

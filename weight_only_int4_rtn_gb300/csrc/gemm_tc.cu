@@ -1,5 +1,6 @@
-// W4A16 GEMM: bf16-activation instantiation of the tcgen05 kernel template,
-// the launch dispatcher, configuration queries and the wait self test.
+// W4A16 GEMM: the single-problem bf16-activation instantiation of the
+// tcgen05 kernel template, the launch dispatcher, configuration queries and
+// the wait self test.
 #include "gemm_tc.cuh"
 
 namespace w4a16 {
@@ -41,10 +42,25 @@ size_t gemm_workspace_bytes(const GemmKernelConfig& c, const GemmSchedule& s, in
   return kCounterBytes + static_cast<size_t>(s.grid) * 2 * c.act_tile * kTileW * sizeof(float);
 }
 
+cudaError_t launch_gemm_tc_group(const GemmKernelConfig& c, const GemmGroup& grp, bool use_pdl,
+                                 cudaStream_t stream) {
+  static_assert(kMaxGemmGroup == kMaxGroup, "group size of the kernel arguments");
+  if (grp.count < 1 || grp.count > kMaxGroup) return cudaErrorInvalidValue;
+  const bool f16 = grp.p[0].act_f16;
+  if (grp.count == 1)
+    return f16 ? launch_gemm_tc_f16(c, grp, use_pdl, stream)
+               : launch_gemm_tc_typed<false, 1>(c, grp, use_pdl, stream);
+  return f16 ? launch_gemm_tc_group_f16(c, grp, use_pdl, stream)
+             : launch_gemm_tc_group_bf16(c, grp, use_pdl, stream);
+}
+
 cudaError_t launch_gemm_tc(const GemmKernelConfig& c, const GemmSchedule& s,
                            const GemmProblem& p, bool use_pdl, cudaStream_t stream) {
-  if (p.act_f16) return launch_gemm_tc_f16(c, s, p, use_pdl, stream);
-  return launch_gemm_tc_typed<false>(c, s, p, use_pdl, stream);
+  GemmGroup grp;
+  grp.count = 1;
+  grp.p[0] = p;
+  grp.s[0] = s;
+  return launch_gemm_tc_group(c, grp, use_pdl, stream);
 }
 
 #ifdef W4A16_TRACE

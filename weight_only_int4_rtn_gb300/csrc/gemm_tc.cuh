@@ -138,6 +138,21 @@ struct Args {
   uint64_t timeout_ns;
 };
 
+// A launch runs up to kMaxGroup independent problems: problem p owns the
+// CTAs cta_start[p] .. cta_start[p+1]-1 (its "sub-grid") and runs the
+// single-problem schedule on them, with its own TMA descriptors, arguments
+// and workspace.  A single GEMM is a group of one.
+// The arguments are sized for G problems (kernel parameters are copied at
+// every launch, so a single GEMM uses G = 1).
+constexpr int kMaxGroup = 8;
+template <int G>
+struct GroupArgs {
+  CUtensorMap tm[G][3];   // per problem: activations, codes, scales
+  Args a[G];
+  int cta_start[G + 1];
+  int count;
+};
+
 struct Unit {
   int tile, kb;
   bool seg_first, seg_last;   // first / last unit of this CTA's run on the tile
@@ -151,9 +166,9 @@ struct Sched {
   int u0, u1;                 // this CTA's stream-K unit range [u0, u1)
   int total;
 
-  __device__ void init(const Args& a) {
-    c = blockIdx.x;
-    C = gridDim.x;
+  __device__ void init(const Args& a, int cta, int ctas) {
+    c = cta;
+    C = ctas;
     KB = a.KB;
     dp_tiles = a.dp_tiles;
     dp_iters = (dp_tiles > c) ? (dp_tiles - c + C - 1) / C : 0;
@@ -417,7 +432,7 @@ __device__ __forceinline__ void load_cols(uint32_t taddr, float (&v)[CNT]) {
 // partial slot (fp32, no bias; column m of the slot holds 128 rows).
 template <int BA, int CNT, bool F16>
 __device__ __forceinline__ void emit_cols(const Args& a, const Unit& u, int row, int col0,
-                                          const float (&v)[CNT], float bias_n) {
+                                          const float (&v)[CNT], float bias_n, int cta) {
   const int n0 = (u.tile % a.n_tiles) * kTileW;
   const int m0 = (u.tile / a.n_tiles) * BA;
   if (u.whole) {
@@ -430,7 +445,7 @@ __device__ __forceinline__ void emit_cols(const Args& a, const Unit& u, int row,
       }
     }
   } else {
-    float* slot = a.ws + (static_cast<int64_t>(blockIdx.x) * 2 + u.slot) * (BA * kTileW) + row;
+    float* slot = a.ws + (static_cast<int64_t>(cta) * 2 + u.slot) * (BA * kTileW) + row;
 #pragma unroll
     for (int j = 0; j < CNT; ++j) {
       if (m0 + col0 + j < a.M) slot[(col0 + j) * kTileW] = v[j];
@@ -443,14 +458,14 @@ __device__ __forceinline__ void emit_cols(const Args& a, const Unit& u, int row,
 // half an SM's shared memory, so all CTAs are resident together; the wait is
 // bounded all the same.  Self-resetting: the last arrival clears the count
 // and bumps the generation the others wait on.
-__device__ bool grid_barrier(const Args& a, const WaitCtx& wc) {
+__device__ bool grid_barrier(const Args& a, const WaitCtx& wc, int ctas) {
   if (*reinterpret_cast<volatile int*>(wc.abort_flag)) return false;
   uint32_t* count = a.counters;
   uint32_t* gen = a.counters + 1;
   const uint32_t g0 = ptx::ld_acquire_gpu(gen);
   // acquire-release: the last arrival observes every other CTA's partials
   const uint32_t old = ptx::atom_add_acq_rel_gpu(count, 1u);
-  if (old == gridDim.x - 1) {
+  if (old == static_cast<uint32_t>(ctas - 1)) {
     atomicExch(count, 0u);
     ptx::atom_add_release_gpu(gen, 1u);   // publishes all partials
     return true;
@@ -474,14 +489,14 @@ __device__ bool grid_barrier(const Args& a, const WaitCtx& wc) {
 // all threads; consecutive threads take consecutive weight rows, so partial
 // reads and Y stores are coalesced.
 template <int BA, bool F16>
-__device__ void stream_k_reduce(const Args& a) {
+__device__ void stream_k_reduce(const Args& a, int cta, int ctas) {
   constexpr int kTileElems = BA * kTileW;
-  const int C = gridDim.x;
+  const int C = ctas;
   const int KB = a.KB;
   const int S = a.sk_units;
   const int64_t E = static_cast<int64_t>(S / KB) * kTileElems;
-  const int64_t e_lo = static_cast<int64_t>(blockIdx.x) * E / C;
-  const int64_t e_hi = static_cast<int64_t>(blockIdx.x + 1) * E / C;
+  const int64_t e_lo = static_cast<int64_t>(cta) * E / C;
+  const int64_t e_hi = static_cast<int64_t>(cta + 1) * E / C;
   int cached = -1, c_lo = 0, c_hi = 0, slot_lo = 0, m0 = 0, n0 = 0;
   for (int64_t e = e_lo + threadIdx.x; e < e_hi; e += blockDim.x) {
     const int tl = static_cast<int>(e / kTileElems);
@@ -514,11 +529,20 @@ __device__ void stream_k_reduce(const Args& a) {
   }
 }
 
-template <int BA, int L, bool GRP, int STAGES, bool F16>
+template <int BA, int L, bool GRP, int STAGES, bool F16, int G>
 __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES>::kThreads, 1)
-    w4a16_gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_act,
-                         const __grid_constant__ CUtensorMap tm_w,
-                         const __grid_constant__ CUtensorMap tm_s, const Args a) {
+    w4a16_gemm_tc_kernel(const __grid_constant__ GroupArgs<G> g) {
+  // this CTA's problem and its index in the problem's sub-grid
+  int prob = 0;
+  if constexpr (G > 1) {
+    while (prob + 1 < g.count && static_cast<int>(blockIdx.x) >= g.cta_start[prob + 1]) ++prob;
+  }
+  const Args& a = g.a[prob];
+  const int cta = static_cast<int>(blockIdx.x) - g.cta_start[prob];
+  const int ctas = g.cta_start[prob + 1] - g.cta_start[prob];
+  const CUtensorMap* const tm_act = &g.tm[prob][0];
+  const CUtensorMap* const tm_w = &g.tm[prob][1];
+  const CUtensorMap* const tm_s = &g.tm[prob][2];
   using C = Cfg<BA, L, GRP, STAGES>;
   constexpr int DB = C::kDB;
   constexpr int SL = C::kSL;
@@ -588,9 +612,9 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES>::kThreads, 1)
     sh->abort_flag = 0;
     sh->reduce_ok = 0;
     ptx::fence_mbar_init();
-    ptx::prefetch_tmap(&tm_act);
-    ptx::prefetch_tmap(&tm_w);
-    ptx::prefetch_tmap(&tm_s);
+    ptx::prefetch_tmap(tm_act);
+    ptx::prefetch_tmap(tm_w);
+    ptx::prefetch_tmap(tm_s);
   }
   if (warp == 1) {
     ptx::tmem_alloc(&sh->tmem_base, kTmemCols);
@@ -608,7 +632,7 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES>::kThreads, 1)
   // previous kernel on the stream may still run; the inputs may be that
   // kernel's outputs, so nothing is read before the dependency wait.
   Sched sched;
-  sched.init(a);
+  sched.init(a, cta, ctas);
   UnitIter it;
   it.init(sched);
   const int total = sched.total;
@@ -635,17 +659,17 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES>::kThreads, 1)
         ptx::mbar_arrive_expect_tx(&sh->full[stage], C::kTx);
         if (i == 0) W4A16_TRACE_UNIT(9, 4);
         if (a.act_3d) {
-          ptx::tma_load_3d(act_box(stage, 0), &tm_act, &sh->full[stage], 0, m0, u.kb * 2);
+          ptx::tma_load_3d(act_box(stage, 0), tm_act, &sh->full[stage], 0, m0, u.kb * 2);
         } else {
-          ptx::tma_load_2d(act_box(stage, 0), &tm_act, &sh->full[stage], u.kb * kUnitK, m0);
-          ptx::tma_load_2d(act_box(stage, 1), &tm_act, &sh->full[stage], u.kb * kUnitK + 64, m0);
+          ptx::tma_load_2d(act_box(stage, 0), tm_act, &sh->full[stage], u.kb * kUnitK, m0);
+          ptx::tma_load_2d(act_box(stage, 1), tm_act, &sh->full[stage], u.kb * kUnitK + 64, m0);
         }
         if (i == 0) W4A16_TRACE_UNIT(9, 5);
         // the unit's codes: one contiguous 8 KiB tile of the tiled storage
-        ptx::tma_load_2d(w_tile(stage), &tm_w, &sh->full[stage], 0,
+        ptx::tma_load_2d(w_tile(stage), tm_w, &sh->full[stage], 0,
                          ((u.tile % a.n_tiles) * a.KB + u.kb) * kTileW);
         if (i == 0) W4A16_TRACE_UNIT(9, 6);
-        ptx::tma_load_2d(s_tile(stage), &tm_s, &sh->full[stage], (u.tile % a.n_tiles) * kTileW,
+        ptx::tma_load_2d(s_tile(stage), tm_s, &sh->full[stage], (u.tile % a.n_tiles) * kTileW,
                          u.kb);
         if (i == 0) W4A16_TRACE_UNIT(9, 7);
         if (i <= 1) W4A16_TRACE_POINT(3);
@@ -821,7 +845,7 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES>::kThreads, 1)
       auto finish_unit = [&](int i) {
         first = false;
         if (--seg_left == 0) {
-          emit_cols<BA, BA, F16>(a, seg, row, 0, acc, bias_f);
+          emit_cols<BA, BA, F16>(a, seg, row, 0, acc, bias_f, cta);
           if (i + 1 < total) open_run();
         }
       };
@@ -899,7 +923,7 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES>::kThreads, 1)
         for (int c0 = 0; c0 < BA; c0 += C::kChunk) {
           float v[C::kChunk];
           load_cols<C::kChunk>(lane_base + C::kDCol + db * BA + c0, v);
-          emit_cols<BA, C::kChunk, F16>(a, u, row, c0, v, act_to_float<F16>(bias_raw));
+          emit_cols<BA, C::kChunk, F16>(a, u, row, c0, v, act_to_float<F16>(bias_raw), cta);
         }
         ptx::tc_fence_before();
         __syncwarp();
@@ -1008,18 +1032,18 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES>::kThreads, 1)
   if (a.sk_units > 0) {
     // split tiles: every CTA wrote its partials; after the grid barrier all
     // CTAs reduce them together
-    if (threadIdx.x == 0) sh->reduce_ok = grid_barrier(a, wc) ? 1 : 0;
+    if (threadIdx.x == 0) sh->reduce_ok = grid_barrier(a, wc, ctas) ? 1 : 0;
     __syncthreads();
-    if (sh->reduce_ok) stream_k_reduce<BA, F16>(a);
+    if (sh->reduce_ok) stream_k_reduce<BA, F16>(a, cta, ctas);
   }
   if (threadIdx.x == 32) W4A16_TRACE_POINT(11);
 }
 
-template <int BA, int L, bool GRP, int STAGES, bool F16>
-cudaError_t launch_instance(const GemmSchedule& s, const GemmProblem& p, bool use_pdl,
-                            cudaStream_t stream) {
+template <int BA, int L, bool GRP, int STAGES, bool F16, int G>
+cudaError_t launch_instance(const GemmGroup& grp, bool use_pdl, cudaStream_t stream) {
   using C = Cfg<BA, L, GRP, STAGES>;
-  auto kernel = w4a16_gemm_tc_kernel<BA, L, GRP, STAGES, F16>;
+  auto kernel = w4a16_gemm_tc_kernel<BA, L, GRP, STAGES, F16, G>;
+  if (grp.count < 1 || grp.count > G) return cudaErrorInvalidValue;
 
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1033,48 +1057,60 @@ cudaError_t launch_instance(const GemmSchedule& s, const GemmProblem& p, bool us
     attr_set[dev] = true;
   }
 
-  CUtensorMap tm_act, tm_w, tm_s;
-  // Activations as [K/64][M][64]: one box {64, BA, 2} brings both 64-wide K
-  // halves of a unit, in the same shared-memory order as two 2-D boxes.
   constexpr CUtensorMapDataType kActType =
       F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  int act_3d = 1;
-  if (encode_tmap_3d(&tm_act, kActType, p.A, 64, p.M, p.K / 64, p.K * 2, 128,
-                     64, BA, 2, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS) {
-    act_3d = 0;
-    if (encode_tmap_2d(&tm_act, kActType, p.A, p.K, p.M, p.K * 2, 64, BA,
-                       CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+  GroupArgs<G> g{};
+  int start = 0;
+  for (int i = 0; i < grp.count; ++i) {
+    const GemmProblem& p = grp.p[i];
+    const GemmSchedule& s = grp.s[i];
+    // Activations as [K/64][M][64]: one box {64, BA, 2} brings both 64-wide
+    // K halves of a unit, in the same shared-memory order as two 2-D boxes.
+    int act_3d = 1;
+    if (encode_tmap_3d(&g.tm[i][0], kActType, p.A, 64, p.M, p.K / 64, p.K * 2, 128, 64, BA, 2,
+                       CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS) {
+      act_3d = 0;
+      if (encode_tmap_2d(&g.tm[i][0], kActType, p.A, p.K, p.M, p.K * 2, 64, BA,
+                         CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    }
+    // tiled code storage viewed as rows of 64 bytes: tile (tn, g) is rows
+    // (tn * K/128 + g) * 128 .. + 127
+    const uint64_t w_rows =
+        static_cast<uint64_t>((p.N + kTileW - 1) / kTileW) * (p.K / kUnitK) * kTileW;
+    if (encode_tmap_2d(&g.tm[i][1], CU_TENSOR_MAP_DATA_TYPE_UINT8, p.packed, 64, w_rows, 64, 64,
+                       kTileW, CU_TENSOR_MAP_SWIZZLE_64B) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
-  }
-  // tiled code storage viewed as rows of 64 bytes: tile (tn, g) is rows
-  // (tn * K/128 + g) * 128 .. + 127
-  const uint64_t w_rows = static_cast<uint64_t>((p.N + kTileW - 1) / kTileW) * (p.K / kUnitK) * kTileW;
-  if (encode_tmap_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.packed, 64, w_rows, 64, 64, kTileW,
-                     CU_TENSOR_MAP_SWIZZLE_64B) != CUDA_SUCCESS)
-    return cudaErrorInvalidValue;
-  if (encode_tmap_2d(&tm_s, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.scales, p.N, p.K / kGroup, p.N * 2,
-                     kTileW, 1, CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
-    return cudaErrorInvalidValue;
+    if (encode_tmap_2d(&g.tm[i][2], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.scales, p.N, p.K / kGroup,
+                       p.N * 2, kTileW, 1, CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
 
-  Args a{};
-  a.M = static_cast<int>(p.M);
-  a.N = static_cast<int>(p.N);
-  a.K = static_cast<int>(p.K);
-  a.KB = static_cast<int>(p.K / kUnitK);
-  a.n_tiles = static_cast<int>((p.N + kTileW - 1) / kTileW);
-  a.dp_tiles = s.dp_tiles;
-  a.sk_units = static_cast<int>(s.sk_units);
-  a.act_3d = act_3d;
-  a.scales = static_cast<const __half*>(p.scales);
-  a.bias = static_cast<const uint16_t*>(p.bias);
-  a.Y = static_cast<uint16_t*>(p.Y);
-  a.counters = static_cast<uint32_t*>(p.workspace);
-  a.ws = reinterpret_cast<float*>(static_cast<uint8_t*>(p.workspace) + kCounterBytes);
-  a.err = p.error_word;
-  a.timeout_ns = p.timeout_ns;
+    Args& a = g.a[i];
+    a.M = static_cast<int>(p.M);
+    a.N = static_cast<int>(p.N);
+    a.K = static_cast<int>(p.K);
+    a.KB = static_cast<int>(p.K / kUnitK);
+    a.n_tiles = static_cast<int>((p.N + kTileW - 1) / kTileW);
+    a.dp_tiles = s.dp_tiles;
+    a.sk_units = static_cast<int>(s.sk_units);
+    a.act_3d = act_3d;
+    a.scales = static_cast<const __half*>(p.scales);
+    a.bias = static_cast<const uint16_t*>(p.bias);
+    a.Y = static_cast<uint16_t*>(p.Y);
+    a.counters = p.counters != nullptr ? p.counters : static_cast<uint32_t*>(p.workspace);
+    a.ws = p.partials != nullptr
+               ? p.partials
+               : reinterpret_cast<float*>(static_cast<uint8_t*>(p.workspace) + kCounterBytes);
+    a.err = p.error_word;
+    a.timeout_ns = p.timeout_ns;
+    g.cta_start[i] = start;
+    start += s.grid;
+  }
+  g.cta_start[grp.count] = start;
+  g.count = grp.count;
 
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(s.grid));
+  cfg.gridDim = dim3(static_cast<unsigned>(start));
   cfg.blockDim = dim3(C::kThreads);
   cfg.dynamicSmemBytes = C::kSmem;
   cfg.stream = stream;
@@ -1083,7 +1119,7 @@ cudaError_t launch_instance(const GemmSchedule& s, const GemmProblem& p, bool us
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = use_pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kernel, tm_act, tm_w, tm_s, a);
+  return cudaLaunchKernelEx(&cfg, kernel, g);
 }
 
 // The compiled configurations: {act_tile, lanes, group_scale, stages}.
@@ -1095,13 +1131,13 @@ cudaError_t launch_instance(const GemmSchedule& s, const GemmProblem& p, bool us
   X(128, 1, false, 5)           \
   X(256, 1, false, 3)
 
-// All compiled configurations of one activation type.
-template <bool F16>
-cudaError_t launch_gemm_tc_typed(const GemmKernelConfig& c, const GemmSchedule& s,
-                                 const GemmProblem& p, bool use_pdl, cudaStream_t stream) {
+// All compiled configurations of one activation type and group size.
+template <bool F16, int G>
+cudaError_t launch_gemm_tc_typed(const GemmKernelConfig& c, const GemmGroup& grp, bool use_pdl,
+                                 cudaStream_t stream) {
 #define W4A16_LAUNCH_CASE(BA, L, GRP, ST)                                           \
   if (c.act_tile == BA && c.lanes == L && c.group_scale == GRP && c.stages == ST) \
-    return launch_instance<BA, L, GRP, ST, F16>(s, p, use_pdl, stream);
+    return launch_instance<BA, L, GRP, ST, F16, G>(grp, use_pdl, stream);
   W4A16_GEMM_INSTANCES(W4A16_LAUNCH_CASE)
 #undef W4A16_LAUNCH_CASE
   return cudaErrorInvalidConfiguration;

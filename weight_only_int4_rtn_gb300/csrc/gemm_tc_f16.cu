@@ -7,9 +7,9 @@
 
 namespace w4a16 {
 
-cudaError_t launch_gemm_tc_f16(const GemmKernelConfig& c, const GemmSchedule& s,
-                               const GemmProblem& p, bool use_pdl, cudaStream_t stream) {
-  return launch_gemm_tc_typed<true>(c, s, p, use_pdl, stream);
+cudaError_t launch_gemm_tc_f16(const GemmKernelConfig& c, const GemmGroup& grp, bool use_pdl,
+                               cudaStream_t stream) {
+  return launch_gemm_tc_typed<true, 1>(c, grp, use_pdl, stream);
 }
 
 }  // namespace w4a16

@@ -17,6 +17,18 @@ cudaError_t launch_rtn_quantize(const void* W, int64_t N, int64_t K, void* packe
                                 int num_sms, uint32_t* error_word, uint64_t timeout_ns,
                                 cudaStream_t stream);
 
+// Several weights quantized in one launch (independent problems).
+constexpr int kMaxQuantizeGroup = 8;
+struct QuantizeProblem {
+  const void* W;   // [N, K] bf16
+  int64_t N, K;
+  void* packed;    // tiled codes
+  void* scales;    // [K/128, N] fp16
+};
+cudaError_t launch_rtn_quantize_group(const QuantizeProblem* probs, int count, int num_sms,
+                                      uint32_t* error_word, uint64_t timeout_ns,
+                                      cudaStream_t stream);
+
 // One configuration of the tcgen05 GEMM kernel.
 struct GemmKernelConfig {
   int act_tile;      // activation rows per tile (tcgen05 N): 16..256
@@ -44,6 +56,9 @@ struct GemmProblem {
   int64_t M, N, K;
   void* workspace;
   size_t workspace_bytes;
+  uint32_t* counters = nullptr;   // grid-barrier words (2) of this problem, in the
+                                  // workspace's fixed counter region
+  float* partials = nullptr;      // this problem's partial-tile slots
   uint32_t* error_word;
   uint64_t timeout_ns;
   bool act_f16 = false;  // A, bias and Y are fp16 (else bf16)
@@ -71,11 +86,28 @@ size_t gemm_smem_bytes(const GemmKernelConfig& c);
 // True if the kernel for `c` is compiled in.
 bool gemm_config_available(const GemmKernelConfig& c);
 
+// Independent problems launched together (one kernel; problem i runs on its
+// own s[i].grid CTAs).  All problems use one configuration and one
+// activation type; workspaces must not overlap.
+constexpr int kMaxGemmGroup = 8;
+struct GemmGroup {
+  int count = 0;
+  GemmProblem p[kMaxGemmGroup];
+  GemmSchedule s[kMaxGemmGroup];
+};
+
 cudaError_t launch_gemm_tc(const GemmKernelConfig& c, const GemmSchedule& s,
                            const GemmProblem& p, bool use_pdl, cudaStream_t stream);
-// fp16-activation instantiation (gemm_tc_f16.cu), called by launch_gemm_tc.
-cudaError_t launch_gemm_tc_f16(const GemmKernelConfig& c, const GemmSchedule& s,
-                               const GemmProblem& p, bool use_pdl, cudaStream_t stream);
+cudaError_t launch_gemm_tc_group(const GemmKernelConfig& c, const GemmGroup& grp, bool use_pdl,
+                                 cudaStream_t stream);
+// Instantiations called by launch_gemm_tc_group: single-problem fp16
+// (gemm_tc_f16.cu) and the multi-problem ones (gemm_tc_group*.cu).
+cudaError_t launch_gemm_tc_f16(const GemmKernelConfig& c, const GemmGroup& grp, bool use_pdl,
+                               cudaStream_t stream);
+cudaError_t launch_gemm_tc_group_bf16(const GemmKernelConfig& c, const GemmGroup& grp,
+                                      bool use_pdl, cudaStream_t stream);
+cudaError_t launch_gemm_tc_group_f16(const GemmKernelConfig& c, const GemmGroup& grp,
+                                     bool use_pdl, cudaStream_t stream);
 
 // Failure-detection self test: one thread waits on an mbarrier nobody
 // arrives at, with a bounded wait; records a timeout in *error_word.

@@ -59,6 +59,20 @@ constexpr int kQTeamWarps = 8;                    // a team: 256 threads, two pe
 constexpr int kQConsumerWarps = 2 * kQTeamWarps;  // two teams, alternate tiles
 constexpr int kQThreads = 32 * (kQConsumerWarps + 1);
 
+// A launch quantizes up to kQMaxGroup independent weights: weight p owns the
+// CTAs cta_start[p] .. cta_start[p+1]-1.  A single weight is a group of one.
+constexpr int kQMaxGroup = 8;
+struct QGroupArgs {
+  CUtensorMap tm[kQMaxGroup];
+  uint32_t* packed[kQMaxGroup];
+  __half* scales[kQMaxGroup];
+  int N[kQMaxGroup];
+  int G[kQMaxGroup];
+  int tiles[kQMaxGroup];
+  int cta_start[kQMaxGroup + 1];
+  int count;
+};
+
 struct QShared {
   uint64_t full[kQStages];
   uint64_t empty[kQStages];
@@ -127,9 +141,18 @@ __device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t acc, uint32_t w) {
 }
 
 __global__ void __launch_bounds__(kQThreads, 1)
-    rtn_quantize_kernel(const __grid_constant__ CUtensorMap tm_w, int N, int G,
-                        uint32_t* __restrict__ packed, __half* __restrict__ scales, int tiles,
-                        uint32_t* err, uint64_t timeout_ns) {
+    rtn_quantize_kernel(const __grid_constant__ QGroupArgs q, uint32_t* err, uint64_t timeout_ns) {
+  // this CTA's weight and its index in that weight's sub-grid
+  int prob = 0;
+  while (prob + 1 < q.count && static_cast<int>(blockIdx.x) >= q.cta_start[prob + 1]) ++prob;
+  const CUtensorMap* const tm_w = &q.tm[prob];
+  const int N = q.N[prob];
+  const int G = q.G[prob];
+  const int tiles = q.tiles[prob];
+  uint32_t* const packed = q.packed[prob];
+  __half* const scales = q.scales[prob];
+  const int cta = static_cast<int>(blockIdx.x) - q.cta_start[prob];
+  const int ctas = q.cta_start[prob + 1] - q.cta_start[prob];
   extern __shared__ __align__(1024) uint8_t q_smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(q_smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -144,7 +167,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
     }
     sh->abort_flag = 0;
     ptx::fence_mbar_init();
-    ptx::prefetch_tmap(&tm_w);
+    ptx::prefetch_tmap(tm_w);
   }
   __syncthreads();
   const WaitCtx wc{err, timeout_ns, &sh->abort_flag};
@@ -154,8 +177,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
   ptx::grid_dependency_wait();
   ptx::grid_launch_dependents();
 
-  const int n_local = (tiles - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
-                      static_cast<int>(gridDim.x);
+  const int n_local = (tiles - cta + ctas - 1) / ctas;
 
   if (warp == kQConsumerWarps) {
     // ------------------------------------------------------------ producer
@@ -164,13 +186,13 @@ __global__ void __launch_bounds__(kQThreads, 1)
       for (int i = 0; i < n_local; ++i) {
         const int stage = i % kQStages;
         if (!wait_one(&sh->empty[stage], ((i / kQStages) & 1) ^ 1, wc)) break;
-        const int t = static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
+        const int t = cta + i * ctas;
         const int tn = t / G;
         const int g = t - tn * G;
         uint8_t* dst = smem + stage * kQTileBytes;
         ptx::mbar_arrive_expect_tx(&sh->full[stage], kQTileBytes);
-        ptx::tma_load_2d(dst, &tm_w, &sh->full[stage], g * kGroup, tn * kQRows);
-        ptx::tma_load_2d(dst + kQBoxBytes, &tm_w, &sh->full[stage], g * kGroup + 64, tn * kQRows);
+        ptx::tma_load_2d(dst, tm_w, &sh->full[stage], g * kGroup, tn * kQRows);
+        ptx::tma_load_2d(dst + kQBoxBytes, tm_w, &sh->full[stage], g * kGroup + 64, tn * kQRows);
         issued = i + 1;
       }
       if (*reinterpret_cast<volatile int*>(&sh->abort_flag)) {
@@ -198,7 +220,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
   for (int i = team; i < n_local; i += 2) {
     const int stage = i % kQStages;
     if (!wait_warp(&sh->full[stage], (i / kQStages) & 1, wc)) break;
-    const int t = static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
+    const int t = cta + i * ctas;
     const int tn = t / G;
     const int g = t - tn * G;
     const uint32_t box = ptx::smem_u32(smem + stage * kQTileBytes) + h * kQBoxBytes;
@@ -255,18 +277,57 @@ __global__ void __launch_bounds__(kQThreads, 1)
 
 }  // namespace
 
-cudaError_t launch_rtn_quantize(const void* W, int64_t N, int64_t K, void* packed, void* scales,
-                                int num_sms, uint32_t* error_word, uint64_t timeout_ns,
-                                cudaStream_t stream) {
-  // the weight as [N][K] bf16; boxes of 128 rows x 64 values, 128-byte
-  // swizzle; rows past N read as zeros
-  CUtensorMap tm_w;
-  if (encode_tmap_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, static_cast<uint64_t>(K),
-                     static_cast<uint64_t>(N), static_cast<uint64_t>(K) * 2, 64, kQRows,
-                     CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
-    return cudaErrorInvalidValue;
-  const int G = static_cast<int>(K / kGroup);
-  const int tiles = static_cast<int>((N + kQRows - 1) / kQRows) * G;
+cudaError_t launch_rtn_quantize_group(const QuantizeProblem* probs, int count, int num_sms,
+                                      uint32_t* error_word, uint64_t timeout_ns,
+                                      cudaStream_t stream) {
+  static_assert(kQMaxGroup == kMaxQuantizeGroup, "group size of the kernel arguments");
+  if (count < 1 || count > kQMaxGroup) return cudaErrorInvalidValue;
+  QGroupArgs q{};
+  int64_t total_tiles = 0;
+  for (int i = 0; i < count; ++i) {
+    const QuantizeProblem& p = probs[i];
+    // the weight as [N][K] bf16; boxes of 128 rows x 64 values, 128-byte
+    // swizzle; rows past N read as zeros
+    if (encode_tmap_2d(&q.tm[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.W, static_cast<uint64_t>(p.K),
+                       static_cast<uint64_t>(p.N), static_cast<uint64_t>(p.K) * 2, 64, kQRows,
+                       CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+    q.packed[i] = static_cast<uint32_t*>(p.packed);
+    q.scales[i] = static_cast<__half*>(p.scales);
+    q.N[i] = static_cast<int>(p.N);
+    q.G[i] = static_cast<int>(p.K / kGroup);
+    q.tiles[i] = static_cast<int>((p.N + kQRows - 1) / kQRows) * q.G[i];
+    total_tiles += q.tiles[i];
+  }
+  // CTAs in proportion to each weight's tiles, at least one each, at most
+  // one per tile, no more than the SMs in total
+  int ctas[kQMaxGroup];
+  int used = 0;
+  for (int i = 0; i < count; ++i) {
+    int64_t c = (static_cast<int64_t>(num_sms) * q.tiles[i]) / total_tiles;
+    if (c < 1) c = 1;
+    if (c > q.tiles[i]) c = q.tiles[i];
+    ctas[i] = static_cast<int>(c);
+    used += ctas[i];
+  }
+  while (used < num_sms) {   // hand spare SMs to the weights with most tiles per CTA
+    int best = -1;
+    for (int i = 0; i < count; ++i)
+      if (ctas[i] < q.tiles[i] &&
+          (best < 0 || static_cast<int64_t>(q.tiles[i]) * ctas[best] > static_cast<int64_t>(q.tiles[best]) * ctas[i]))
+        best = i;
+    if (best < 0) break;
+    ++ctas[best];
+    ++used;
+  }
+  int start = 0;
+  for (int i = 0; i < count; ++i) {
+    q.cta_start[i] = start;
+    start += ctas[i];
+  }
+  q.cta_start[count] = start;
+  q.count = count;
+
   constexpr size_t smem = static_cast<size_t>(kQStages) * kQTileBytes + sizeof(QShared) + 1024;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -279,10 +340,8 @@ cudaError_t launch_rtn_quantize(const void* W, int64_t N, int64_t K, void* packe
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  int grid = num_sms;
-  if (grid > tiles) grid = tiles;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.gridDim = dim3(static_cast<unsigned>(start));
   cfg.blockDim = dim3(kQThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
@@ -292,9 +351,14 @@ cudaError_t launch_rtn_quantize(const void* W, int64_t N, int64_t K, void* packe
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, rtn_quantize_kernel, tm_w, static_cast<int>(N), G,
-                            static_cast<uint32_t*>(packed), static_cast<__half*>(scales), tiles,
-                            error_word, timeout_ns);
+  return cudaLaunchKernelEx(&cfg, rtn_quantize_kernel, q, error_word, timeout_ns);
+}
+
+cudaError_t launch_rtn_quantize(const void* W, int64_t N, int64_t K, void* packed, void* scales,
+                                int num_sms, uint32_t* error_word, uint64_t timeout_ns,
+                                cudaStream_t stream) {
+  QuantizeProblem p{W, N, K, packed, scales};
+  return launch_rtn_quantize_group(&p, 1, num_sms, error_word, timeout_ns, stream);
 }
 
 }  // namespace w4a16
