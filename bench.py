@@ -184,9 +184,15 @@ def run_gpu(args, rank, world):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
     torch.cuda.set_device(dev)
     cases = synthetic.WORKLOADS[args.workload]
+    if args.grouped is None:
+        # the projections are independent problems: one grouped launch of
+        # each kind per step when they fit one launch
+        args.grouped = len(cases) <= w4.MAX_GROUP
     if args.grouped and len(cases) > w4.MAX_GROUP:
         raise SystemExit(f"--grouped takes at most {w4.MAX_GROUP} projections")
     if args.tune:
+        # kernel choice by measurement, once per shape, outside the timed
+        # region (later calls of the shape use the memoized choice)
         for c in cases:
             w4.w4a16_tune(c.M, c.N, c.K)
 
@@ -437,6 +443,8 @@ def run_gpu(args, rank, world):
                                  "w4a16_gemm launch" if args.grouped else
                                  "rtn_quantize + w4a16_gemm per projection"),
                            l2="inputs rotate over %d copies (%.0f MB > 3x L2)" % (copies, copies * per_copy / 2**20),
+                           selection=("per-shape table tuned by measurement before timing" if args.tune
+                                      else "cost-model rule"),
                            parallelism=f"replicas x{world}"),
                gemm=dict(tflops=round(job_rate(flops_step, args.steps, elapsed_ms, world) / 1e12, 3)),
                kernels=kernels, roofline=roofline, clocks=clk.summary(),
@@ -492,10 +500,15 @@ def main():
                     choices=["tiny", "expert_m50", "prefix_m816", "sweep", "large"])
     ap.add_argument("--act", default="bf16", choices=["bf16", "f16"],
                     help="activation type of the GEMMs (A, bias, Y)")
-    ap.add_argument("--grouped", action="store_true",
+    ap.add_argument("--grouped", dest="grouped", action="store_true", default=None,
                     help="one grouped quantize and one grouped GEMM launch per step (the "
-                         "projections are independent problems)")
-    ap.add_argument("--tune", action="store_true", help="tune the variant table first")
+                         "projections are independent problems; the default when the "
+                         "workload has at most 8 projections)")
+    ap.add_argument("--per-projection", dest="grouped", action="store_false",
+                    help="one quantize and one GEMM launch per projection")
+    ap.add_argument("--no-tune", dest="tune", action="store_false", default=True,
+                    help="select kernels by the cost-model rule instead of tuning each "
+                         "shape by measurement first")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -96,21 +96,28 @@ struct Variant {
 };
 
 const Variant kVariants[] = {
-    {"tc_a16_grp_sk", {16, 2, true, 16}, true, 1, 0.44},
+    {"tc_a16_grp_sk", {16, 2, true, 16}, true, 1, 0.43},
     {"tc_a32_grp_sk", {32, 2, true, 12}, true, 1, 0.57},
-    {"tc_a64_grp_sk", {64, 2, true, 8}, true, 1, 1.30},
-    {"tc_a64_deq_sk", {64, 1, false, 8}, true, 1, 0.71},
-    {"tc_a128_deq_sk", {128, 1, false, 5}, true, 1, 0.80},
-    {"tc_a256_deq_sk", {256, 1, false, 3}, true, 1, 1.08},
-    {"tc_a16_grp_dp", {16, 2, true, 16}, false, 1, 0.44},
-    {"tc_a64_grp_dp", {64, 2, true, 8}, false, 1, 1.30},
-    {"tc_a128_deq_dp", {128, 1, false, 5}, false, 1, 0.80},
-    {"tc_a256_deq_dp", {256, 1, false, 3}, false, 1, 1.08},
-    {"tc_a16_grp_sk4", {16, 2, true, 16}, true, 4, 0.44},
-    {"tc_a16_grp_sk8", {16, 2, true, 16}, true, 8, 0.44},
-    {"tc_a32_grp_sk4", {32, 2, true, 12}, true, 4, 0.57},
-    {"tc_a64_grp_sk4", {64, 2, true, 8}, true, 4, 1.30},
-    {"tc_a64_grp_sk8", {64, 2, true, 8}, true, 8, 1.30},
+    {"tc_a64_grp_sk", {64, 2, true, 8}, true, 1, 1.33},
+    {"tc_a64_deq_sk", {64, 1, false, 8}, true, 1, 0.59},
+    {"tc_a128_deq_sk", {128, 1, false, 5}, true, 1, 0.58},
+    {"tc_a256_deq_sk", {256, 1, false, 3}, true, 1, 0.67},
+    {"tc_a16_grp_dp", {16, 2, true, 16}, false, 1, 0.37},
+    {"tc_a64_grp_dp", {64, 2, true, 8}, false, 1, 1.13},
+    {"tc_a128_deq_dp", {128, 1, false, 5}, false, 1, 0.67},
+    {"tc_a256_deq_dp", {256, 1, false, 3}, false, 1, 0.96},
+    {"tc_a16_grp_sk4", {16, 2, true, 16}, true, 4, 0.42},
+    {"tc_a16_grp_sk8", {16, 2, true, 16}, true, 8, 0.38},
+    {"tc_a32_grp_sk4", {32, 2, true, 12}, true, 4, 0.55},
+    {"tc_a64_grp_sk4", {64, 2, true, 8}, true, 4, 1.29},
+    {"tc_a64_grp_sk8", {64, 2, true, 8}, true, 8, 1.07},
+    {"tc_a16_deq2_sk", {16, 2, false, 16}, true, 1, 0.46},
+    {"tc_a32_deq2_sk", {32, 2, false, 12}, true, 1, 0.48},
+    {"tc_a64_deq2_sk", {64, 2, false, 8}, true, 1, 0.51},
+    {"tc_a128_deq2_sk", {128, 2, false, 4}, true, 1, 0.66},
+    {"tc_a16_deq2_dp", {16, 2, false, 16}, false, 1, 0.44},
+    {"tc_a64_deq2_dp", {64, 2, false, 8}, false, 1, 0.47},
+    {"tc_a128_deq2_dp", {128, 2, false, 4}, false, 1, 0.70},
 };
 constexpr int kNumVariants = static_cast<int>(sizeof(kVariants) / sizeof(kVariants[0]));
 
@@ -154,6 +161,12 @@ GemmSchedule make_schedule(const Variant& v, int64_t M, int64_t N, int64_t K, in
     s.dp_tiles = 0;
     s.sk_units = units;
   }
+  // one arrival counter per split tile
+  if (s.sk_units / KB > kCountersPerProblem) {
+    s.grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
+    s.dp_tiles = static_cast<int>(tiles);
+    s.sk_units = 0;
+  }
   return s;
 }
 
@@ -170,12 +183,12 @@ bool variant_eligible(int id, int64_t M, int64_t N, int64_t K) {
 // Rule for shapes without a table entry: a cost model fitted to GB300
 // measurements.  A launch pays a fixed head (launch, set-up, pipeline fill);
 // each CTA then runs its units at the variant's per-unit time; a schedule
-// that splits tiles over CTAs adds the grid-wide barrier and the reduction
-// of the partial tiles (more for wider activation tiles).  The variant with
-// the smallest estimate wins.
-constexpr double kHeadUs = 3.0;
-constexpr double kSplitUs = 4.0;
-constexpr double kSplitUsPerCol = 0.02;
+// that splits tiles over CTAs adds the split-tile fixup (arrival count and
+// the last contributor's sum of the partials; more for wider activation
+// tiles).  The variant with the smallest estimate wins.
+constexpr double kHeadUs = 3.69;
+constexpr double kSplitUs = 2.49;
+constexpr double kSplitUsPerCol = 0.048;
 
 double estimate_us(const Variant& v, int64_t M, int64_t N, int64_t K, int num_sms) {
   const GemmSchedule s = make_schedule(v, M, N, K, num_sms);
@@ -635,7 +648,7 @@ int w4a16_gemm_grouped(const w4a16_gemm_problem* problems, int count, int group,
     p.workspace = workspace;
     p.workspace_bytes = workspace_bytes;
     uint8_t* base = static_cast<uint8_t*>(workspace);
-    p.counters = base ? reinterpret_cast<uint32_t*>(base) + 2 * i : nullptr;
+    p.counters = base ? reinterpret_cast<uint32_t*>(base) + kCountersPerProblem * i : nullptr;
     p.partials = base ? reinterpret_cast<float*>(base + kCounterBytes + plan.partial_off[i]) : nullptr;
     p.error_word = dev.error_word;
     p.timeout_ns = g_timeout_ns.load();

@@ -294,9 +294,10 @@ struct Shared {
   uint64_t dempty[8];         // the readout drained accumulator buffer(s)
   uint64_t pair_done[8];       // group mode: both lanes' units of a pair completed
   uint64_t mma_done[2];
+  uint64_t rsync;             // readout warps' barrier (split-tile fixup)
   uint32_t tmem_base;
   int abort_flag;
-  int reduce_ok;
+  int fixup_last;             // this CTA completed a split tile's count
 };
 
 // ------------------------------------------------ activation-type helpers
@@ -370,9 +371,13 @@ struct Cfg {
   static constexpr int kDCol = kAS * kAStageCols;
   static constexpr int kDCols = 512 - kDCol;
   static constexpr int kAL = kAS / L;                             // TMEM weight stages per lane
-  static constexpr int kDBfit = kDCols / BA;                      // accumulators that fit
+  // Group mode: kDB accumulators of BA columns, split over the lanes (kDL
+  // per lane).  Dequant mode: kDB run buffers of L * BA columns (one BA-wide
+  // half per lane; the readout adds the halves).
+  static constexpr int kBufCols = GRP ? BA : L * BA;
+  static constexpr int kDBfit = kDCols / kBufCols;                // buffers that fit
   static constexpr int kDB = kDBfit < (GRP ? 8 : 4) ? kDBfit : (GRP ? 8 : 4);
-  static constexpr int kDL = kDB / L;                             // accumulator buffers per lane
+  static constexpr int kDL = GRP ? kDB / L : kDB;                 // buffers a lane cycles through
   static constexpr int kRL = kSL > kAL ? kSL : kAL;               // unit_done ring per lane
   static constexpr int kChunk = BA < (GRP ? 16 : 32) ? BA : (GRP ? 16 : 32);
   static constexpr size_t kSmem = static_cast<size_t>(STAGES) * kStage + 1024 + sizeof(Shared) +
@@ -380,12 +385,9 @@ struct Cfg {
   static constexpr uint32_t kTx = 2 * kActBox + kWBytes + kSBytes;
   static_assert(BA % 16 == 0 && BA >= 16 && BA <= 256, "tcgen05 N for M=128");
   static_assert(L == 1 || L == 2, "lanes");
-  static_assert(GRP || L == 1, "dequant mode accumulates a tile run in one lane");
   static_assert(STAGES % L == 0 && STAGES <= 16, "stages split over the lanes");
-  static_assert(kDB % L == 0 && kDL >= 1, "accumulators split over the lanes");
-  // a unit_done phase may only be reused once every waiter saw the previous
-  // one: the readout is at most kDL units of a lane behind its MMAs
-  static_assert(kRL >= kDL, "unit_done ring covers the accumulator buffers");
+  static_assert(kDB >= 1 && kDL >= 1 && (!GRP || kDB % L == 0), "accumulators split over the lanes");
+  static_assert(kDB <= 8, "barrier arrays");
   static_assert(L * kRL <= 32, "barrier arrays");
   static_assert(!GRP || BA <= 64, "group mode keeps BA fp32 accumulators per thread");
   static_assert(!GRP || L == 2, "group mode runs two lanes (the readout takes units in pairs)");
@@ -453,80 +455,84 @@ __device__ __forceinline__ void emit_cols(const Args& a, const Unit& u, int row,
   }
 }
 
-// Grid-wide barrier after every CTA wrote its partial tiles (one thread per
-// CTA).  The grid never exceeds one CTA per SM and each CTA needs more than
-// half an SM's shared memory, so all CTAs are resident together; the wait is
-// bounded all the same.  Self-resetting: the last arrival clears the count
-// and bumps the generation the others wait on.
-__device__ bool grid_barrier(const Args& a, const WaitCtx& wc, int ctas) {
-  if (*reinterpret_cast<volatile int*>(wc.abort_flag)) return false;
-  uint32_t* count = a.counters;
-  uint32_t* gen = a.counters + 1;
-  const uint32_t g0 = ptx::ld_acquire_gpu(gen);
-  // acquire-release: the last arrival observes every other CTA's partials
-  const uint32_t old = ptx::atom_add_acq_rel_gpu(count, 1u);
-  if (old == static_cast<uint32_t>(ctas - 1)) {
-    atomicExch(count, 0u);
-    ptx::atom_add_release_gpu(gen, 1u);   // publishes all partials
-    return true;
+// A split tile's contributors: CTAs c_lo .. c_hi (in k order) of the
+// balanced stream-K split; CTA c_lo keeps the tile in slot 0 only if its
+// range starts exactly at the tile's first k-block, every later contributor's
+// range starts inside the tile (slot 0).
+struct SplitInfo {
+  int c_lo, c_hi, slot_lo;
+};
+
+__device__ __forceinline__ SplitInfo split_info(const Args& a, int tl, int ctas) {
+  SplitInfo r;
+  const int S = a.sk_units;
+  const int KB = a.KB;
+  r.c_lo = sk_owner(tl * KB, ctas, S);
+  r.c_hi = sk_owner(tl * KB + KB - 1, ctas, S);
+  const int u0_lo = static_cast<int>((static_cast<int64_t>(r.c_lo) * S) / ctas);
+  r.slot_lo = (u0_lo == tl * KB) ? 0 : 1;
+  return r;
+}
+
+// Barrier of the four readout warps on an mbarrier, so that a warp that gave
+// up after a timeout cannot leave the others blocked for good.
+__device__ __forceinline__ bool readout_sync(Shared* sh, uint32_t& nsync, const WaitCtx& wc) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(&sh->rsync);
+  const bool ok = wait_warp(&sh->rsync, nsync & 1, wc);
+  ++nsync;
+  return ok;
+}
+
+// After this CTA wrote its partial of a split tile (every readout thread its
+// weight row): count the arrival on the tile's counter.  The contributor
+// that completes the count sums all partials of the tile in k order (so the
+// result does not depend on who arrives last), adds the bias, rounds once to
+// the output type and stores Y; it also resets the counter for the next
+// launch.  Nobody waits for anybody: the last arrival finds every partial
+// written.
+template <int BA, bool F16>
+__device__ bool split_fixup(const Args& a, const Unit& u, const SplitInfo& si, Shared* sh, int row,
+                            float bias_n, uint32_t& nsync, const WaitCtx& wc) {
+  __threadfence();   // this thread's partial row is visible to the whole GPU
+  if (!readout_sync(sh, nsync, wc)) return false;
+  if (threadIdx.x == 32 * kReadoutWarp0) {
+    uint32_t* cnt = a.counters + u.sk_tile;
+    // acquire-release: the last arrival observes every contributor's partial
+    const uint32_t old = ptx::atom_add_acq_rel_gpu(cnt, 1u);
+    const bool last = old == static_cast<uint32_t>(si.c_hi - si.c_lo);
+    if (last) atomicExch(cnt, 0u);
+    sh->fixup_last = last ? 1 : 0;
   }
-  const uint64_t t0 = ptx::globaltimer_ns();
-  for (uint32_t spin = 0; ptx::ld_acquire_gpu(gen) == g0; ++spin) {
-    if ((spin & 15) == 15) {
-      if (ptx::globaltimer_ns() - t0 > a.timeout_ns) {
-        wait_record_timeout(wc);
-        return false;
+  if (!readout_sync(sh, nsync, wc)) return false;
+  if (!sh->fixup_last) return true;
+  __threadfence();
+  const int n0 = (u.tile % a.n_tiles) * kTileW;
+  const int m0 = (u.tile / a.n_tiles) * BA;
+  const int n = n0 + row;
+  const int mcols = min(BA, a.M - m0);
+  constexpr int64_t kSlot = static_cast<int64_t>(BA) * kTileW;
+  const float* lo = a.ws + (static_cast<int64_t>(si.c_lo) * 2 + si.slot_lo) * kSlot + row;
+#pragma unroll 1
+  for (int c0 = 0; c0 < mcols; c0 += 16) {
+    float acc[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) acc[j] = __ldcg(lo + (c0 + j) * kTileW);
+#pragma unroll 2
+    for (int c = si.c_lo + 1; c <= si.c_hi; ++c) {
+      const float* src = a.ws + static_cast<int64_t>(c) * 2 * kSlot + row;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) acc[j] += __ldcg(src + (c0 + j) * kTileW);
+    }
+    if (n < a.N) {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        if (c0 + j < mcols)
+          a.Y[static_cast<int64_t>(m0 + c0 + j) * a.N + n] = act_from_float<F16>(acc[j] + bias_n);
       }
-      ptx::nanosleep(32);
     }
   }
   return true;
-}
-
-// Second phase of stream-K: every element of every split tile is the sum of
-// its contributors' partials in k order (deterministic), plus the bias,
-// rounded once to the output type.  The elements are spread evenly over all CTAs and
-// all threads; consecutive threads take consecutive weight rows, so partial
-// reads and Y stores are coalesced.
-template <int BA, bool F16>
-__device__ void stream_k_reduce(const Args& a, int cta, int ctas) {
-  constexpr int kTileElems = BA * kTileW;
-  const int C = ctas;
-  const int KB = a.KB;
-  const int S = a.sk_units;
-  const int64_t E = static_cast<int64_t>(S / KB) * kTileElems;
-  const int64_t e_lo = static_cast<int64_t>(cta) * E / C;
-  const int64_t e_hi = static_cast<int64_t>(cta + 1) * E / C;
-  int cached = -1, c_lo = 0, c_hi = 0, slot_lo = 0, m0 = 0, n0 = 0;
-  for (int64_t e = e_lo + threadIdx.x; e < e_hi; e += blockDim.x) {
-    const int tl = static_cast<int>(e / kTileElems);
-    const int rem = static_cast<int>(e - static_cast<int64_t>(tl) * kTileElems);
-    const int m = rem >> 7;
-    const int row = rem & (kTileW - 1);
-    if (tl != cached) {
-      cached = tl;
-      c_lo = sk_owner(tl * KB, C, S);
-      c_hi = sk_owner(tl * KB + KB - 1, C, S);
-      // the CTA holding the tile's first k-block keeps it in slot 0 only if
-      // its range starts exactly there; every later contributor's range
-      // starts inside the tile (slot 0)
-      const int u0_lo = static_cast<int>(static_cast<int64_t>(c_lo) * S / C);
-      slot_lo = (u0_lo == tl * KB) ? 0 : 1;
-      const int tile = a.dp_tiles + tl;
-      m0 = (tile / a.n_tiles) * BA;
-      n0 = (tile % a.n_tiles) * kTileW;
-    }
-    if (c_lo == c_hi) continue;   // one CTA ran the whole tile and stored Y
-    const int mm = m0 + m;
-    const int n = n0 + row;
-    if (mm >= a.M || n >= a.N) continue;
-    const float* col = a.ws + static_cast<int64_t>(m) * kTileW + row;
-    float sum = __ldcg(col + (static_cast<int64_t>(c_lo) * 2 + slot_lo) * kTileElems);
-#pragma unroll 4
-    for (int c = c_lo + 1; c <= c_hi; ++c) sum += __ldcg(col + static_cast<int64_t>(c) * 2 * kTileElems);
-    const float b = a.bias != nullptr ? act_to_float<F16>(a.bias[n]) : 0.0f;
-    a.Y[static_cast<int64_t>(mm) * a.N + n] = act_from_float<F16>(sum + b);
-  }
 }
 
 template <int BA, int L, bool GRP, int STAGES, bool F16, int G>
@@ -603,14 +609,16 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES>::kThreads, 1)
     for (int s = 0; s < L * RL; ++s) ptx::mbar_init(&sh->unit_done[s], 1);
     for (int s = 0; s < C::kAS; ++s) ptx::mbar_init(&sh->afull[s], 4);
     for (int s = 0; s < DB; ++s) {
-      ptx::mbar_init(&sh->dfull[s], 1);
+      // dequant mode: both lanes' MMA threads arrive (L = 2)
+      ptx::mbar_init(&sh->dfull[s], GRP ? 1 : L);
       ptx::mbar_init(&sh->dempty[s], 4);
     }
     for (int s = 0; s < kPairRing; ++s) ptx::mbar_init(&sh->pair_done[s], 2);
     ptx::mbar_init(&sh->mma_done[0], 1);
     ptx::mbar_init(&sh->mma_done[1], 1);
+    ptx::mbar_init(&sh->rsync, 4);
     sh->abort_flag = 0;
-    sh->reduce_ok = 0;
+    sh->fixup_last = 0;
     ptx::fence_mbar_init();
     ptx::prefetch_tmap(tm_act);
     ptx::prefetch_tmap(tm_w);
@@ -655,6 +663,7 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES>::kThreads, 1)
         // the unit that last used this stage is i - STAGES (same lane)
         if (i >= STAGES && !wait_one(done_bar(i - STAGES), done_parity(i - STAGES), wc)) break;
         if (i == 0) W4A16_TRACE_UNIT(9, 3);
+        W4A16_TRACE_UNIT(13, i);
         const int m0 = (u.tile / a.n_tiles) * BA;
         ptx::mbar_arrive_expect_tx(&sh->full[stage], C::kTx);
         if (i == 0) W4A16_TRACE_UNIT(9, 4);
@@ -665,10 +674,12 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES>::kThreads, 1)
           ptx::tma_load_2d(act_box(stage, 1), tm_act, &sh->full[stage], u.kb * kUnitK + 64, m0);
         }
         if (i == 0) W4A16_TRACE_UNIT(9, 5);
+        W4A16_TRACE_UNIT(14, i);
         // the unit's codes: one contiguous 8 KiB tile of the tiled storage
         ptx::tma_load_2d(w_tile(stage), tm_w, &sh->full[stage], 0,
                          ((u.tile % a.n_tiles) * a.KB + u.kb) * kTileW);
         if (i == 0) W4A16_TRACE_UNIT(9, 6);
+        W4A16_TRACE_UNIT(15, i);
         ptx::tma_load_2d(s_tile(stage), tm_s, &sh->full[stage], (u.tile % a.n_tiles) * kTileW,
                          u.kb);
         if (i == 0) W4A16_TRACE_UNIT(9, 7);
@@ -728,42 +739,57 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES>::kThreads, 1)
         }
         if (nj > 0) W4A16_TRACE_POINT(5);
       } else {
+        // Dequant mode: a run accumulates in TMEM across its units.  Each
+        // lane accumulates its own units of the run in its own half of the
+        // run's buffer; the readout adds the halves.
         int seg = 0;
         int db = 0;
+        bool have = false;   // this lane issued into the current run's buffer
         for (int i = 0; i < total; ++i) {
           const Unit u = it.next();
-          int p, j;
-          lane_split<L>(i, p, j);
-          const int stage = stage_of(i);
-          const int as = astage_of(i);
-          W4A16_TRACE_UNIT(8, i);
-          if (!wait_one(&sh->afull[as], (j / AL) & 1, wc)) break;
-          W4A16_TRACE_UNIT(10, i);
-          const bool fresh = u.seg_first;
           if (u.seg_first) {
             db = seg % DB;
-            if (seg >= DB && !wait_one(&sh->dempty[db], ((seg / DB) - 1) & 1, wc)) break;
+            have = false;
           }
-          ptx::tc_fence_after();
-          if (i == 0) W4A16_TRACE_POINT(4);
-          if (i == total - 1) W4A16_TRACE_POINT(5);
-          W4A16_TRACE_UNIT(4, i);
-          const uint32_t d_tmem = tmem + C::kDCol + db * BA;
-          const uint32_t a_tmem = tmem + as * kAStageCols;
-          const uint32_t b0 = smem0 + stage * C::kStage;
-  #pragma unroll
-          for (int kk = 0; kk < kUnitK / 16; ++kk) {
-            const uint32_t baddr = b0 + (kk >> 2) * C::kActBox + (kk & 3) * 32;
-            ptx::mma_f16kind_tmem_a(d_tmem, a_tmem + kk * 8, ptx::smem_desc_sw128(baddr), idesc,
-                                 (kk > 0 || !fresh) ? 1u : 0u);
+          int p, j;
+          lane_split<L>(i, p, j);
+          if (p == mine) {
+            const int stage = stage_of(i);
+            const int as = astage_of(i);
+            W4A16_TRACE_UNIT(8, i);
+            if (!wait_one(&sh->afull[as], (j / AL) & 1, wc)) break;
+            W4A16_TRACE_UNIT(10, i);
+            // the buffer's previous run (seg - DB) was drained by the readout
+            if (!have && seg >= DB && !wait_one(&sh->dempty[db], ((seg / DB) - 1) & 1, wc)) break;
+            ptx::tc_fence_after();
+            if (i == 0) W4A16_TRACE_POINT(4);
+            if (i == total - 1) W4A16_TRACE_POINT(5);
+            W4A16_TRACE_UNIT(4, i);
+            const uint32_t d_tmem = tmem + C::kDCol + (db * L + mine) * BA;
+            const uint32_t a_tmem = tmem + as * kAStageCols;
+            const uint32_t b0 = smem0 + stage * C::kStage;
+#pragma unroll
+            for (int kk = 0; kk < kUnitK / 16; ++kk) {
+              const uint32_t baddr = b0 + (kk >> 2) * C::kActBox + (kk & 3) * 32;
+              ptx::mma_f16kind_tmem_a(d_tmem, a_tmem + kk * 8, ptx::smem_desc_sw128(baddr), idesc,
+                                      (kk > 0 || have) ? 1u : 0u);
+            }
+            W4A16_TRACE_UNIT(11, i);
+            ptx::mma_commit(done_bar(i));
+            have = true;
           }
-          W4A16_TRACE_UNIT(11, i);
-          ptx::mma_commit(done_bar(i));
           if (u.seg_last) {
-            ptx::mma_commit(&sh->dfull[db]);
+            if (have) {
+              ptx::mma_commit(&sh->dfull[db]);
+            } else {
+              // no unit of this lane in the run: arrive without MMAs, once
+              // the buffer's previous run was drained
+              if (seg >= DB && !wait_one(&sh->dempty[db], ((seg / DB) - 1) & 1, wc)) break;
+              ptx::mbar_arrive(&sh->dfull[db]);
+            }
             ++seg;
+            W4A16_TRACE_UNIT(5, i);
           }
-          W4A16_TRACE_UNIT(5, i);
         }
       }
       // all MMAs of this thread complete before TMEM is freed
@@ -824,14 +850,18 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES>::kThreads, 1)
       SegCursor cur;
       cur.init(sched);
       Unit seg;
+      SplitInfo si{0, 0, 0};
       int seg_left = 0;
       bool first = true;
       float bias_f = 0.0f;
+      uint32_t nsync = 0;
+      bool ok = true;
       auto open_run = [&]() {
         int kb0;
         cur.next(seg, kb0, seg_left, a.dp_tiles);
         const int n = (seg.tile % a.n_tiles) * kTileW + row;
         bias_f = (a.bias != nullptr && n < a.N) ? act_to_float<F16>(a.bias[n]) : 0.0f;
+        if (!seg.whole) si = split_info(a, seg.sk_tile, ctas);
         first = true;
       };
       if (total > 0) open_run();
@@ -846,6 +876,7 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES>::kThreads, 1)
         first = false;
         if (--seg_left == 0) {
           emit_cols<BA, BA, F16>(a, seg, row, 0, acc, bias_f, cta);
+          if (!seg.whole) ok = split_fixup<BA, F16>(a, seg, si, sh, row, bias_f, nsync, wc);
           if (i + 1 < total) open_run();
         }
       };
@@ -903,31 +934,49 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES>::kThreads, 1)
             finish_unit(i0 + h);
           }
         }
+        if (!ok) break;
       }
       ptx::cp_async_wait<0>();   // no copy may land after exit
     } else {
       uint16_t bias_raw = 0;
       int seg = 0;
+      int i_first = 0;
+      uint32_t nsync = 0;
       for (int i = 0; i < total; ++i) {
         const Unit u = it.next();
         if (u.seg_first) {
           const int n = (u.tile % a.n_tiles) * kTileW + row;
           bias_raw = (a.bias != nullptr && n < a.N) ? a.bias[n] : static_cast<uint16_t>(0);
+          i_first = i;
         }
         if (!u.seg_last) continue;
         const int db = seg % DB;
         if (!wait_warp(&sh->dfull[db], (seg / DB) & 1, wc)) break;
         ++seg;
         ptx::tc_fence_after();
+        const float bias_f = act_to_float<F16>(bias_raw);
+        // the lanes that hold units of this run (a run of one unit has one)
+        const bool has0 = L == 1 || i > i_first || (i_first & 1) == 0;
+        const bool has1 = L == 2 && (i > i_first || (i_first & 1) == 1);
+        const uint32_t buf = lane_base + C::kDCol + db * L * BA;
 #pragma unroll 1
         for (int c0 = 0; c0 < BA; c0 += C::kChunk) {
           float v[C::kChunk];
-          load_cols<C::kChunk>(lane_base + C::kDCol + db * BA + c0, v);
-          emit_cols<BA, C::kChunk, F16>(a, u, row, c0, v, act_to_float<F16>(bias_raw), cta);
+          load_cols<C::kChunk>(buf + (has0 ? 0 : BA) + c0, v);
+          if (has0 && has1) {
+            float w[C::kChunk];
+            load_cols<C::kChunk>(buf + BA + c0, w);
+#pragma unroll
+            for (int c = 0; c < C::kChunk; ++c) v[c] += w[c];
+          }
+          emit_cols<BA, C::kChunk, F16>(a, u, row, c0, v, bias_f, cta);
         }
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&sh->dempty[db]);
+        if (!u.whole &&
+            !split_fixup<BA, F16>(a, u, split_info(a, u.sk_tile, ctas), sh, row, bias_f, nsync, wc))
+          break;
       }
     }
   } else if (warp >= kDequantWarp0 && warp < kDequantWarp0 + 8) {
@@ -1029,13 +1078,6 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES>::kThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   if (warp == 1) ptx::tmem_dealloc(tmem, kTmemCols);
-  if (a.sk_units > 0) {
-    // split tiles: every CTA wrote its partials; after the grid barrier all
-    // CTAs reduce them together
-    if (threadIdx.x == 0) sh->reduce_ok = grid_barrier(a, wc, ctas) ? 1 : 0;
-    __syncthreads();
-    if (sh->reduce_ok) stream_k_reduce<BA, F16>(a, cta, ctas);
-  }
   if (threadIdx.x == 32) W4A16_TRACE_POINT(11);
 }
 
@@ -1127,6 +1169,10 @@ cudaError_t launch_instance(const GemmGroup& grp, bool use_pdl, cudaStream_t str
   X(16, 2, true, 16)            \
   X(32, 2, true, 12)            \
   X(64, 2, true, 8)             \
+  X(16, 2, false, 16)           \
+  X(32, 2, false, 12)           \
+  X(64, 2, false, 8)            \
+  X(128, 2, false, 4)           \
   X(64, 1, false, 8)            \
   X(128, 1, false, 5)           \
   X(256, 1, false, 3)

@@ -56,8 +56,9 @@ struct GemmProblem {
   int64_t M, N, K;
   void* workspace;
   size_t workspace_bytes;
-  uint32_t* counters = nullptr;   // grid-barrier words (2) of this problem, in the
-                                  // workspace's fixed counter region
+  uint32_t* counters = nullptr;   // arrival counters of this problem's split tiles
+                                  // (kCountersPerProblem words of the workspace's
+                                  // fixed counter region)
   float* partials = nullptr;      // this problem's partial-tile slots
   uint32_t* error_word;
   uint64_t timeout_ns;
@@ -69,14 +70,18 @@ inline int64_t gemm_tiles(const GemmKernelConfig& c, int64_t M, int64_t N) {
   return ((N + kTileW - 1) / kTileW) * ((M + c.act_tile - 1) / c.act_tile);
 }
 
-// Workspace layout: kCounterBytes of uint32 counters (words 0 and 1: the
-// grid barrier's arrival count and generation; the region has a fixed size so
-// every variant finds them at the same place), then [grid][2][act_tile][128]
-// fp32 partial slots (slot 0: the first stream-K tile of a CTA's range,
-// slot 1: its last; inside a slot, column m of the tile is 128 contiguous
-// weight rows).
-constexpr size_t kCounterBytes = 4096;
-constexpr int kMaxGrid = static_cast<int>(kCounterBytes / 4);
+// Workspace layout: kCounterBytes of uint32 counters (problem i of a launch
+// owns words i * kCountersPerProblem .. + kCountersPerProblem - 1: one
+// arrival counter per split tile; the region has a fixed size so every
+// variant finds them at the same place), then [grid][2][act_tile][128] fp32
+// partial slots (slot 0: the first stream-K tile of a CTA's range, slot 1:
+// its last; inside a slot, column m of the tile is 128 contiguous weight
+// rows).
+constexpr int kCountersPerProblem = 256;
+constexpr int kMaxGemmGroupCounters = 8;
+constexpr size_t kCounterBytes =
+    static_cast<size_t>(kMaxGemmGroupCounters) * kCountersPerProblem * sizeof(uint32_t);
+constexpr int kMaxGrid = 1024;
 size_t gemm_workspace_bytes(const GemmKernelConfig& c, const GemmSchedule& s, int64_t M,
                             int64_t N, int64_t K);
 
@@ -90,6 +95,7 @@ bool gemm_config_available(const GemmKernelConfig& c);
 // own s[i].grid CTAs).  All problems use one configuration and one
 // activation type; workspaces must not overlap.
 constexpr int kMaxGemmGroup = 8;
+static_assert(kMaxGemmGroup <= kMaxGemmGroupCounters, "a counter block per problem");
 struct GemmGroup {
   int count = 0;
   GemmProblem p[kMaxGemmGroup];
