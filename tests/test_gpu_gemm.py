@@ -35,6 +35,7 @@ SHAPES = [
     synthetic.Case("m129", 129, 256, 256, 13),
     synthetic.Case("m300_multi_tile", 300, 384, 1024, 14, bias=True),
     synthetic.Case("m17_long_k", 17, 136, 4096, 15),
+    synthetic.Case("m3_ragged_n_even_groups", 3, 200, 768, 18, bias=True),
 ]
 
 
@@ -127,6 +128,12 @@ def test_hand_worked_example(w4):
     packed, scales = w4.w4a16_quantize(W)
     A = torch.ones(1, 128, dtype=torch.bfloat16, device="cuda")
     for v in variant_ids(w4):
+        if not w4.w4a16_variant_eligible(v, 1, 8, 128):
+            # units of two groups need an even number of groups along K
+            with pytest.raises(w4.W4A16Error) as ei:
+                w4.w4a16_gemm(A, packed, scales, variant=v)
+            assert ei.value.status == w4.W4A16_ERR_NO_VARIANT
+            continue
         Y = w4.w4a16_gemm(A, packed, scales, variant=v)
         torch.cuda.synchronize()
         got = Y.float().cpu().numpy()[0]
@@ -153,6 +160,8 @@ def test_integer_exact(w4):
     assert np.all(exact == np.round(exact * 8) / 8) and np.abs(exact).max() < 4096
     expected = bits(synthetic.to_bf16(exact.astype(np.float32)))
     for v in variant_ids(w4):
+        if not w4.w4a16_variant_eligible(v, M, N, K):
+            continue
         Y = w4.w4a16_gemm(A.cuda(), packed, scales, variant=v)
         torch.cuda.synchronize()
         assert np.array_equal(bits(Y), expected), w4.w4a16_variant_name(v)

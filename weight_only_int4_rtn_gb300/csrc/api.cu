@@ -91,33 +91,42 @@ struct Variant {
   bool stream_k;   // false: whole tiles only (data parallel)
   int min_units;   // stream-K: at least this many units per CTA (fewer CTAs and
                    // fewer split tiles on small problems)
-  double unit_us;  // measured time of one unit (128 weight rows x one group)
+  double unit_us;  // measured time of one unit (128 weight rows x unit_groups groups)
                    // in steady state on GB300, for the selection rule
 };
 
 const Variant kVariants[] = {
-    {"tc_a16_grp_sk", {16, 2, true, 16}, true, 1, 0.43},
+    {"tc_a16_grp_sk", {16, 2, true, 16}, true, 1, 0.44},
     {"tc_a32_grp_sk", {32, 2, true, 12}, true, 1, 0.57},
-    {"tc_a64_grp_sk", {64, 2, true, 8}, true, 1, 1.33},
-    {"tc_a64_deq_sk", {64, 1, false, 8}, true, 1, 0.59},
-    {"tc_a128_deq_sk", {128, 1, false, 5}, true, 1, 0.58},
-    {"tc_a256_deq_sk", {256, 1, false, 3}, true, 1, 0.67},
-    {"tc_a16_grp_dp", {16, 2, true, 16}, false, 1, 0.37},
-    {"tc_a64_grp_dp", {64, 2, true, 8}, false, 1, 1.13},
-    {"tc_a128_deq_dp", {128, 1, false, 5}, false, 1, 0.67},
-    {"tc_a256_deq_dp", {256, 1, false, 3}, false, 1, 0.96},
-    {"tc_a16_grp_sk4", {16, 2, true, 16}, true, 4, 0.42},
-    {"tc_a16_grp_sk8", {16, 2, true, 16}, true, 8, 0.38},
+    {"tc_a64_grp_sk", {64, 2, true, 8}, true, 1, 1.30},
+    {"tc_a64_deq_sk", {64, 1, false, 8}, true, 1, 0.60},
+    {"tc_a128_deq_sk", {128, 1, false, 5}, true, 1, 0.57},
+    {"tc_a256_deq_sk", {256, 1, false, 3}, true, 1, 0.63},
+    {"tc_a16_grp_dp", {16, 2, true, 16}, false, 1, 0.38},
+    {"tc_a64_grp_dp", {64, 2, true, 8}, false, 1, 1.10},
+    {"tc_a128_deq_dp", {128, 1, false, 5}, false, 1, 0.68},
+    {"tc_a256_deq_dp", {256, 1, false, 3}, false, 1, 0.95},
+    {"tc_a16_grp_sk4", {16, 2, true, 16}, true, 4, 0.43},
+    {"tc_a16_grp_sk8", {16, 2, true, 16}, true, 8, 0.39},
     {"tc_a32_grp_sk4", {32, 2, true, 12}, true, 4, 0.55},
-    {"tc_a64_grp_sk4", {64, 2, true, 8}, true, 4, 1.29},
-    {"tc_a64_grp_sk8", {64, 2, true, 8}, true, 8, 1.07},
-    {"tc_a16_deq2_sk", {16, 2, false, 16}, true, 1, 0.46},
+    {"tc_a64_grp_sk4", {64, 2, true, 8}, true, 4, 1.27},
+    {"tc_a64_grp_sk8", {64, 2, true, 8}, true, 8, 1.06},
+    {"tc_a16_deq2_sk", {16, 2, false, 16}, true, 1, 0.48},
     {"tc_a32_deq2_sk", {32, 2, false, 12}, true, 1, 0.48},
-    {"tc_a64_deq2_sk", {64, 2, false, 8}, true, 1, 0.51},
-    {"tc_a128_deq2_sk", {128, 2, false, 4}, true, 1, 0.66},
-    {"tc_a16_deq2_dp", {16, 2, false, 16}, false, 1, 0.44},
+    {"tc_a64_deq2_sk", {64, 2, false, 8}, true, 1, 0.50},
+    {"tc_a128_deq2_sk", {128, 2, false, 4}, true, 1, 0.65},
+    {"tc_a16_deq2_dp", {16, 2, false, 16}, false, 1, 0.45},
     {"tc_a64_deq2_dp", {64, 2, false, 8}, false, 1, 0.47},
     {"tc_a128_deq2_dp", {128, 2, false, 4}, false, 1, 0.70},
+    // units of two groups (one 16 KiB copy of codes per unit)
+    {"tc_a16_grp_sk_u2", {16, 2, true, 8, 2}, true, 1, 0.76},
+    {"tc_a16_grp_sk8_u2", {16, 2, true, 8, 2}, true, 8, 0.61},
+    {"tc_a16_grp_dp_u2", {16, 2, true, 8, 2}, false, 1, 0.66},
+    {"tc_a16_deq2_sk_u2", {16, 2, false, 8, 2}, true, 1, 0.92},
+    {"tc_a16_deq2_dp_u2", {16, 2, false, 8, 2}, false, 1, 0.86},
+    {"tc_a32_deq2_sk_u2", {32, 2, false, 6, 2}, true, 1, 1.01},
+    {"tc_a64_deq2_sk_u2", {64, 2, false, 4, 2}, true, 1, 1.08},
+    {"tc_a64_deq2_dp_u2", {64, 2, false, 4, 2}, false, 1, 0.98},
 };
 constexpr int kNumVariants = static_cast<int>(sizeof(kVariants) / sizeof(kVariants[0]));
 
@@ -137,7 +146,7 @@ GemmSchedule make_schedule(const Variant& v, int64_t M, int64_t N, int64_t K, in
   GemmSchedule s{};
   if (num_sms > kMaxGrid) num_sms = kMaxGrid;
   const int64_t tiles = gemm_tiles(v.cfg, M, N);
-  const int64_t KB = K / kGroup;
+  const int64_t KB = K / kGroup / v.cfg.unit_groups;   // units per tile
   const int64_t units = tiles * KB;
   if (!v.stream_k) {
     s.grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
@@ -177,6 +186,7 @@ bool variant_eligible(int id, int64_t M, int64_t N, int64_t K) {
   if (!gemm_config_available(v.cfg)) return false;
   const int64_t tiles = gemm_tiles(v.cfg, M, N);
   if (tiles * (K / kGroup) >= (1ll << 31)) return false;
+  if ((K / kGroup) % v.cfg.unit_groups != 0) return false;
   return true;
 }
 
@@ -186,13 +196,13 @@ bool variant_eligible(int id, int64_t M, int64_t N, int64_t K) {
 // that splits tiles over CTAs adds the split-tile fixup (arrival count and
 // the last contributor's sum of the partials; more for wider activation
 // tiles).  The variant with the smallest estimate wins.
-constexpr double kHeadUs = 3.69;
-constexpr double kSplitUs = 2.49;
-constexpr double kSplitUsPerCol = 0.048;
+constexpr double kHeadUs = 3.71;
+constexpr double kSplitUs = 2.44;
+constexpr double kSplitUsPerCol = 0.051;
 
 double estimate_us(const Variant& v, int64_t M, int64_t N, int64_t K, int num_sms) {
   const GemmSchedule s = make_schedule(v, M, N, K, num_sms);
-  const int64_t KB = K / kGroup;
+  const int64_t KB = K / kGroup / v.cfg.unit_groups;
   const int64_t dp_per_cta = (s.dp_tiles + s.grid - 1) / s.grid;
   const int64_t sk_per_cta = (s.sk_units + s.grid - 1) / s.grid;
   double t = kHeadUs + static_cast<double>(dp_per_cta * KB + sk_per_cta) * v.unit_us;
@@ -345,7 +355,7 @@ bool plan_for_variant(int id, const w4a16_gemm_problem* pr, int count, int sms, 
   int64_t total = 0;
   for (int i = 0; i < count; ++i) {
     if (!variant_eligible(id, pr[i].M, pr[i].N, pr[i].K)) return false;
-    units[i] = gemm_tiles(v.cfg, pr[i].M, pr[i].N) * (pr[i].K / kGroup);
+    units[i] = gemm_tiles(v.cfg, pr[i].M, pr[i].N) * (pr[i].K / kGroup / v.cfg.unit_groups);
     total += units[i];
   }
   if (count > sms) return false;

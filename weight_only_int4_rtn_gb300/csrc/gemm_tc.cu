@@ -23,9 +23,10 @@ __global__ void wait_timeout_selftest_kernel(uint32_t* err, uint64_t timeout_ns)
 }  // namespace
 
 size_t gemm_smem_bytes(const GemmKernelConfig& c) {
-#define W4A16_SMEM_CASE(BA, L, GRP, ST) \
-  if (c.act_tile == BA && c.lanes == L && c.group_scale == GRP && c.stages == ST) \
-    return Cfg<BA, L, GRP, ST>::kSmem;
+#define W4A16_SMEM_CASE(BA, L, GRP, ST, UG)                                          \
+  if (c.act_tile == BA && c.lanes == L && c.group_scale == GRP && c.stages == ST && \
+      c.unit_groups == UG)                                                          \
+    return Cfg<BA, L, GRP, ST, UG>::kSmem;
   W4A16_GEMM_INSTANCES(W4A16_SMEM_CASE)
 #undef W4A16_SMEM_CASE
   return 0;

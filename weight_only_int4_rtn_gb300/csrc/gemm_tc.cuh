@@ -95,7 +95,7 @@ static __device__ unsigned long long* g_trace_units = nullptr;
   } while (0)
 #define W4A16_TRACE_UNIT(role, i)                                                       \
   do {                                                                                  \
-    if (trace_unit != nullptr && (i) < 64)                                              \
+    if (trace_unit != nullptr && (i) < 64 && (role) < 32)                               \
       trace_unit[(role) * 64 + (i)] = static_cast<unsigned long long>(clock64());     \
   } while (0)
 #else
@@ -289,6 +289,7 @@ __device__ __forceinline__ int sk_owner(int u, int C, int sk_units) {
 struct Shared {
   uint64_t full[16];          // a shared-memory stage's copies landed
   uint64_t afull[kMaxAStages];   // a TMEM weight stage is written
+  uint64_t aempty[kMaxAStages];  // a TMEM weight stage's MMAs completed
   uint64_t unit_done[32];     // per lane a ring: a unit's MMAs completed
   uint64_t dfull[8];          // dequant mode: a run on a tile is accumulated
   uint64_t dempty[8];         // the readout drained accumulator buffer(s)
@@ -357,34 +358,40 @@ __device__ __forceinline__ uint32_t scale_pair_bf16(uint32_t q, uint32_t s_hi2, 
   return x2_fma<false>(q, s_hi2, lo);
 }
 
-template <int BA, int L, bool GRP, int STAGES>
+template <int BA, int L, bool GRP, int STAGES, int UG>
 struct Cfg {
+  // A shared-memory stage holds one unit of UG groups: 2 * UG activation
+  // boxes (64 k each), then UG code tiles (8 KiB each), then UG scale rows.
   static constexpr int kActBox = BA * 128;                        // bytes per 64-k box
-  static constexpr int kStageRaw = 2 * kActBox + kWBytes + kSBytes;
+  static constexpr int kWOff = 2 * UG * kActBox;
+  static constexpr int kSOff = kWOff + UG * kWBytes;
+  static constexpr int kStageRaw = UG * (2 * kActBox + kWBytes + kSBytes);
   static constexpr int kStage = (kStageRaw + 1023) / 1024 * 1024;
   static constexpr int kThreads = 32 * kWarps;                    // 16 warps: <= 128 registers
   static constexpr int kSL = STAGES / L;                          // shared-memory stages per lane
   // TMEM: kAS weight stages of 64 columns, then the accumulators.  The
   // narrowest group-mode tile needs few accumulator columns, so it takes
   // three weight stages per lane (the dequant runs further ahead).
-  static constexpr int kAS = (GRP && BA == 16) ? 6 : 4;
+  static constexpr int kAS = (BA == 16 && (GRP || UG == 2)) ? 6 : 4;
   static constexpr int kDCol = kAS * kAStageCols;
   static constexpr int kDCols = 512 - kDCol;
   static constexpr int kAL = kAS / L;                             // TMEM weight stages per lane
   // Group mode: kDB accumulators of BA columns, split over the lanes (kDL
   // per lane).  Dequant mode: kDB run buffers of L * BA columns (one BA-wide
   // half per lane; the readout adds the halves).
-  static constexpr int kBufCols = GRP ? BA : L * BA;
+  static constexpr int kBufCols = GRP ? UG * BA : L * BA;
   static constexpr int kDBfit = kDCols / kBufCols;                // buffers that fit
   static constexpr int kDB = kDBfit < (GRP ? 8 : 4) ? kDBfit : (GRP ? 8 : 4);
   static constexpr int kDL = GRP ? kDB / L : kDB;                 // buffers a lane cycles through
   static constexpr int kRL = kSL > kAL ? kSL : kAL;               // unit_done ring per lane
   static constexpr int kChunk = BA < (GRP ? 16 : 32) ? BA : (GRP ? 16 : 32);
   static constexpr size_t kSmem = static_cast<size_t>(STAGES) * kStage + 1024 + sizeof(Shared) +
-                                  (GRP ? kScaleRing * kTileW * 2 : 0);
-  static constexpr uint32_t kTx = 2 * kActBox + kWBytes + kSBytes;
+                                  (GRP ? kScaleRing * UG * kTileW * 2 : 0);
+  static constexpr uint32_t kTx = kStageRaw;
   static_assert(BA % 16 == 0 && BA >= 16 && BA <= 256, "tcgen05 N for M=128");
   static_assert(L == 1 || L == 2, "lanes");
+  static_assert(UG == 1 || UG == 2, "groups per unit (TMA boxes of up to 256 rows)");
+  static_assert(kAS % L == 0 && kAS <= kMaxAStages, "TMEM weight stages split over the lanes");
   static_assert(STAGES % L == 0 && STAGES <= 16, "stages split over the lanes");
   static_assert(kDB >= 1 && kDL >= 1 && (!GRP || kDB % L == 0), "accumulators split over the lanes");
   static_assert(kDB <= 8, "barrier arrays");
@@ -535,8 +542,8 @@ __device__ bool split_fixup(const Args& a, const Unit& u, const SplitInfo& si, S
   return true;
 }
 
-template <int BA, int L, bool GRP, int STAGES, bool F16, int G>
-__global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES>::kThreads, 1)
+template <int BA, int L, bool GRP, int STAGES, int UG, bool F16, int G>
+__global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG>::kThreads, 1)
     w4a16_gemm_tc_kernel(const __grid_constant__ GroupArgs<G> g) {
   // this CTA's problem and its index in the problem's sub-grid
   int prob = 0;
@@ -549,7 +556,7 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES>::kThreads, 1)
   const CUtensorMap* const tm_act = &g.tm[prob][0];
   const CUtensorMap* const tm_w = &g.tm[prob][1];
   const CUtensorMap* const tm_s = &g.tm[prob][2];
-  using C = Cfg<BA, L, GRP, STAGES>;
+  using C = Cfg<BA, L, GRP, STAGES, UG>;
   constexpr int DB = C::kDB;
   constexpr int SL = C::kSL;
   constexpr int AL = C::kAL;
@@ -565,9 +572,9 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES>::kThreads, 1)
   auto act_box = [&](int stage, int box) -> uint8_t* {
     return smem + stage * C::kStage + box * C::kActBox;
   };
-  auto w_tile = [&](int stage) -> uint8_t* { return smem + stage * C::kStage + 2 * C::kActBox; };
-  auto s_tile = [&](int stage) -> __half* {
-    return reinterpret_cast<__half*>(smem + stage * C::kStage + 2 * C::kActBox + kWBytes);
+  auto w_tile = [&](int stage) -> uint8_t* { return smem + stage * C::kStage + C::kWOff; };
+  auto s_tile = [&](int stage, int gi) -> __half* {
+    return reinterpret_cast<__half*>(smem + stage * C::kStage + C::kSOff + gi * kSBytes);
   };
   // Resources of unit i (lane p, index j in the lane): the lanes own
   // interleaved shared-memory stages, TMEM weight stages and accumulators.
@@ -576,11 +583,9 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES>::kThreads, 1)
     lane_split<L>(i, p, j);
     return p + L * (j % SL);
   };
-  auto astage_of = [&](int i) -> int {
-    int p, j;
-    lane_split<L>(i, p, j);
-    return p + L * (j % AL);
-  };
+  // TMEM weight stages go round per group: group jg of lane p's groups
+  // (jg = UG * j + gi for group gi of the lane's unit j).
+  auto gstage_of = [&](int p, int jg) -> int { return p + L * (jg % AL); };
   // Completion of unit i's MMAs.  Group mode: the pair ring (lane 0's and
   // lane 1's j-th units complete together, one arrival each); one lane:
   // the unit ring.
@@ -607,7 +612,10 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES>::kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) ptx::mbar_init(&sh->full[s], 1);
     for (int s = 0; s < L * RL; ++s) ptx::mbar_init(&sh->unit_done[s], 1);
-    for (int s = 0; s < C::kAS; ++s) ptx::mbar_init(&sh->afull[s], 4);
+    for (int s = 0; s < C::kAS; ++s) {
+      ptx::mbar_init(&sh->afull[s], 4);
+      ptx::mbar_init(&sh->aempty[s], 1);
+    }
     for (int s = 0; s < DB; ++s) {
       // dequant mode: both lanes' MMA threads arrive (L = 2)
       ptx::mbar_init(&sh->dfull[s], GRP ? 1 : L);
@@ -667,21 +675,24 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES>::kThreads, 1)
         const int m0 = (u.tile / a.n_tiles) * BA;
         ptx::mbar_arrive_expect_tx(&sh->full[stage], C::kTx);
         if (i == 0) W4A16_TRACE_UNIT(9, 4);
+        const int g0 = u.kb * UG;   // the unit's first group
         if (a.act_3d) {
-          ptx::tma_load_3d(act_box(stage, 0), tm_act, &sh->full[stage], 0, m0, u.kb * 2);
+          ptx::tma_load_3d(act_box(stage, 0), tm_act, &sh->full[stage], 0, m0, g0 * 2);
         } else {
-          ptx::tma_load_2d(act_box(stage, 0), tm_act, &sh->full[stage], u.kb * kUnitK, m0);
-          ptx::tma_load_2d(act_box(stage, 1), tm_act, &sh->full[stage], u.kb * kUnitK + 64, m0);
+#pragma unroll
+          for (int b = 0; b < 2 * UG; ++b)
+            ptx::tma_load_2d(act_box(stage, b), tm_act, &sh->full[stage], g0 * kUnitK + 64 * b, m0);
         }
         if (i == 0) W4A16_TRACE_UNIT(9, 5);
         W4A16_TRACE_UNIT(14, i);
-        // the unit's codes: one contiguous 8 KiB tile of the tiled storage
+        // the unit's codes: UG consecutive 8 KiB tiles of the tiled storage
+        // (one contiguous block)
         ptx::tma_load_2d(w_tile(stage), tm_w, &sh->full[stage], 0,
-                         ((u.tile % a.n_tiles) * a.KB + u.kb) * kTileW);
+                         ((u.tile % a.n_tiles) * a.KB * UG + g0) * kTileW);
         if (i == 0) W4A16_TRACE_UNIT(9, 6);
         W4A16_TRACE_UNIT(15, i);
-        ptx::tma_load_2d(s_tile(stage), tm_s, &sh->full[stage], (u.tile % a.n_tiles) * kTileW,
-                         u.kb);
+        ptx::tma_load_2d(s_tile(stage, 0), tm_s, &sh->full[stage], (u.tile % a.n_tiles) * kTileW,
+                         g0);
         if (i == 0) W4A16_TRACE_UNIT(9, 7);
         if (i <= 1) W4A16_TRACE_POINT(3);
         W4A16_TRACE_UNIT(0, i);
@@ -711,26 +722,44 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES>::kThreads, 1)
         // this lane's units j = 0, 1, ...: unit i = 2 j + mine; every unit
         // starts a fresh accumulator (the readout applies the group scale)
         const int nj = (total - mine + 1) >> 1;
-        for (int j = 0; j < nj; ++j) {
+        bool ok = true;
+        for (int j = 0; j < nj && ok; ++j) {
           const int stage = mine + 2 * (j % SL);
-          const int as = mine + 2 * (j % AL);
           const int dl = j % DL;
-          if (!wait_one(&sh->afull[as], (j / AL) & 1, wc)) break;
-          // the readout frees a lane's buffers in order: once it read the
-          // lane's unit j-1, buffers of units j .. j+DL-1 are free
-          if (dl == 0 && j >= DL && !wait_one(&sh->dempty[mine], ((j / DL) - 1) & 1, wc)) break;
-          ptx::tc_fence_after();
-          if (j == 0) W4A16_TRACE_POINT(4);
-          W4A16_TRACE_UNIT(4, 2 * j + mine);
-          const uint32_t d_tmem = tmem + C::kDCol + (mine + 2 * dl) * BA;
-          const uint32_t a_tmem = tmem + as * kAStageCols;
           const uint32_t b0 = smem0 + stage * C::kStage;
 #pragma unroll
-          for (int kk = 0; kk < kUnitK / 16; ++kk) {
-            const uint32_t baddr = b0 + (kk >> 2) * C::kActBox + (kk & 3) * 32;
-            ptx::mma_f16kind_tmem_a(d_tmem, a_tmem + kk * 8, ptx::smem_desc_sw128(baddr), idesc,
-                                 kk > 0 ? 1u : 0u);
+          for (int gi = 0; gi < UG; ++gi) {
+            const int jg = UG * j + gi;
+            const int as = gstage_of(mine, jg);
+            if (!wait_one(&sh->afull[as], (jg / AL) & 1, wc)) {
+              ok = false;
+              break;
+            }
+            // the readout frees a lane's buffers in order: once it read the
+            // lane's unit j-1, buffers of units j .. j+DL-1 are free
+            if (gi == 0 && dl == 0 && j >= DL &&
+                !wait_one(&sh->dempty[mine], ((j / DL) - 1) & 1, wc)) {
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+            if (j == 0 && gi == 0) W4A16_TRACE_POINT(4);
+            W4A16_TRACE_UNIT(gi == 0 ? 4 : 20, 2 * j + mine);
+            // group gi of the unit: its own accumulator
+            const uint32_t d_tmem = tmem + C::kDCol + ((mine + 2 * dl) * UG + gi) * BA;
+            const uint32_t a_tmem = tmem + as * kAStageCols;
+            const uint64_t bdesc = ptx::smem_desc_sw128(b0 + 2 * gi * C::kActBox);
+#pragma unroll
+            for (int kk = 0; kk < kUnitK / 16; ++kk) {
+              // K step kk: 64-k half kk / 4, 32 bytes per 16 k inside it
+              const uint32_t boff = ((kk >> 2) * C::kActBox + (kk & 3) * 32) >> 4;
+              ptx::mma_f16kind_tmem_a(d_tmem, a_tmem + kk * 8, bdesc + boff, idesc,
+                                      kk > 0 ? 1u : 0u);
+            }
+            ptx::mma_commit(&sh->aempty[as]);   // the TMEM stage is free once these complete
+            W4A16_TRACE_UNIT(gi == 0 ? 21 : 22, 2 * j + mine);
           }
+          if (!ok) break;
           // one arrival per lane on the pair's barrier; an unpaired last
           // unit (lane 0) arrives for both
           ptx::mma_commit(&sh->pair_done[j % kPairRing]);
@@ -755,28 +784,43 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES>::kThreads, 1)
           lane_split<L>(i, p, j);
           if (p == mine) {
             const int stage = stage_of(i);
-            const int as = astage_of(i);
-            W4A16_TRACE_UNIT(8, i);
-            if (!wait_one(&sh->afull[as], (j / AL) & 1, wc)) break;
-            W4A16_TRACE_UNIT(10, i);
-            // the buffer's previous run (seg - DB) was drained by the readout
-            if (!have && seg >= DB && !wait_one(&sh->dempty[db], ((seg / DB) - 1) & 1, wc)) break;
-            ptx::tc_fence_after();
-            if (i == 0) W4A16_TRACE_POINT(4);
-            if (i == total - 1) W4A16_TRACE_POINT(5);
-            W4A16_TRACE_UNIT(4, i);
-            const uint32_t d_tmem = tmem + C::kDCol + (db * L + mine) * BA;
-            const uint32_t a_tmem = tmem + as * kAStageCols;
             const uint32_t b0 = smem0 + stage * C::kStage;
+            const uint32_t d_tmem = tmem + C::kDCol + (db * L + mine) * BA;
+            W4A16_TRACE_UNIT(8, i);
+            bool ok = true;
 #pragma unroll
-            for (int kk = 0; kk < kUnitK / 16; ++kk) {
-              const uint32_t baddr = b0 + (kk >> 2) * C::kActBox + (kk & 3) * 32;
-              ptx::mma_f16kind_tmem_a(d_tmem, a_tmem + kk * 8, ptx::smem_desc_sw128(baddr), idesc,
-                                      (kk > 0 || have) ? 1u : 0u);
+            for (int gi = 0; gi < UG; ++gi) {
+              const int jg = UG * j + gi;
+              const int as = gstage_of(mine, jg);
+              if (!wait_one(&sh->afull[as], (jg / AL) & 1, wc)) {
+                ok = false;
+                break;
+              }
+              if (gi == 0) W4A16_TRACE_UNIT(10, i);
+              // the buffer's previous run (seg - DB) was drained by the readout
+              if (!have && seg >= DB &&
+                  !wait_one(&sh->dempty[db], ((seg / DB) - 1) & 1, wc)) {
+                ok = false;
+                break;
+              }
+              ptx::tc_fence_after();
+              if (i == 0 && gi == 0) W4A16_TRACE_POINT(4);
+              if (i == total - 1 && gi == 0) W4A16_TRACE_POINT(5);
+              if (gi == 0) W4A16_TRACE_UNIT(4, i);
+              const uint32_t a_tmem = tmem + as * kAStageCols;
+              const uint64_t bdesc = ptx::smem_desc_sw128(b0 + 2 * gi * C::kActBox);
+#pragma unroll
+              for (int kk = 0; kk < kUnitK / 16; ++kk) {
+                const uint32_t boff = ((kk >> 2) * C::kActBox + (kk & 3) * 32) >> 4;
+                ptx::mma_f16kind_tmem_a(d_tmem, a_tmem + kk * 8, bdesc + boff, idesc,
+                                        (kk > 0 || have) ? 1u : 0u);
+              }
+              ptx::mma_commit(&sh->aempty[as]);   // the TMEM stage is free once these complete
+              have = true;
             }
+            if (!ok) break;
             W4A16_TRACE_UNIT(11, i);
             ptx::mma_commit(done_bar(i));
-            have = true;
           }
           if (u.seg_last) {
             if (have) {
@@ -832,13 +876,17 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES>::kThreads, 1)
           pf_cur.next(v, kb0, pf_left, a.dp_tiles);
           const int nn = (v.tile % a.n_tiles) * kTileW + row;
           pf_ok = nn < a.N;   // N % 8 == 0: row nn + 1 exists too
-          pf_ptr = a.scales + static_cast<int64_t>(kb0) * a.N + nn;
+          pf_ptr = a.scales + static_cast<int64_t>(kb0) * UG * a.N + nn;
         } else {
-          pf_ptr += a.N;
+          pf_ptr += static_cast<int64_t>(UG) * a.N;
         }
         --pf_left;
-        if ((lane & 1) == 0 && pf_ok)
-          ptx::cp_async_4(ptx::smem_u32(sring + (jj % kScaleRing) * kTileW + row), pf_ptr);
+        if ((lane & 1) == 0 && pf_ok) {
+#pragma unroll
+          for (int gi = 0; gi < UG; ++gi)
+            ptx::cp_async_4(ptx::smem_u32(sring + ((jj % kScaleRing) * UG + gi) * kTileW + row),
+                            pf_ptr + static_cast<int64_t>(gi) * a.N);
+        }
       };
 #pragma unroll
       for (int q = 0; q < kScaleAhead; ++q) {
@@ -865,12 +913,16 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES>::kThreads, 1)
         first = true;
       };
       if (total > 0) open_run();
-      // acc (+)= scale * D for one unit, 16 columns at a time; emits at the
-      // end of a run
+      // acc (+)= scale * D for one group, 16 columns at a time (`first`:
+      // the run's first group sets acc); emits at the end of a run
       auto accumulate = [&](float scale, const uint32_t* d, int c0) {
 #pragma unroll
         for (int c = 0; c < 16; ++c)
           acc[c0 + c] = first ? scale * __uint_as_float(d[c]) : fmaf(scale, __uint_as_float(d[c]), acc[c0 + c]);
+      };
+      auto scale_at = [&](int i, int gi) -> float {
+        return __half2float(
+            __ushort_as_half(sring[((i % kScaleRing) * UG + gi) * kTileW + row]));
       };
       auto finish_unit = [&](int i) {
         first = false;
@@ -890,16 +942,21 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES>::kThreads, 1)
         ptx::cp_async_commit();
         ptx::cp_async_wait<kScaleAhead>();   // this pair's copies landed
         __syncwarp();
-        const float s0 = __half2float(__ushort_as_half(sring[(i0 % kScaleRing) * kTileW + row]));
-        const float s1 = __half2float(__ushort_as_half(sring[((i0 + 1) % kScaleRing) * kTileW + row]));
+        float s0[UG], s1[UG];
+#pragma unroll
+        for (int gi = 0; gi < UG; ++gi) {
+          s0[gi] = scale_at(i0, gi);
+          s1[gi] = scale_at(i0 + 1, gi);
+        }
         if (threadIdx.x == 32 * kReadoutWarp0) W4A16_TRACE_UNIT(12, i0);
         if (!wait_warp(&sh->pair_done[q % kPairRing], (q / kPairRing) & 1, wc)) break;
         if (threadIdx.x == 32 * kReadoutWarp0 && q == 0) W4A16_TRACE_POINT(8);
         if (threadIdx.x == 32 * kReadoutWarp0 && q == pairs - 1) W4A16_TRACE_POINT(9);
         if (threadIdx.x == 32 * kReadoutWarp0) W4A16_TRACE_UNIT(6, i0);
         ptx::tc_fence_after();
-        const uint32_t d0 = lane_base + C::kDCol + (0 + 2 * dl) * BA;
-        const uint32_t d1 = lane_base + C::kDCol + (1 + 2 * dl) * BA;
+        // unit accumulators: UG groups of BA columns each
+        const uint32_t d0 = lane_base + C::kDCol + (0 + 2 * dl) * UG * BA;
+        const uint32_t d1 = lane_base + C::kDCol + (1 + 2 * dl) * UG * BA;
         auto release = [&]() {
           ptx::tc_fence_before();
           __syncwarp();
@@ -910,25 +967,41 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES>::kThreads, 1)
           if (threadIdx.x == 32 * kReadoutWarp0) W4A16_TRACE_UNIT(7, i0);
         };
         if constexpr (BA == 16) {
-          // both accumulators with one TMEM wait
-          uint32_t r0[16], r1[16];
-          ptx::tmem_ld2_x16_sync(d0, d1, r0, r1);
+          // both units' accumulators (all their groups) with one TMEM wait
+          uint32_t r0[16 * UG], r1[16 * UG];
+          if constexpr (UG == 1) {
+            ptx::tmem_ld2_x16_sync(d0, d1, r0, r1);
+          } else {
+            ptx::tmem_ld2_x32_sync(d0, d1, r0, r1);
+          }
           release();
-          accumulate(s0, r0, 0);
+#pragma unroll
+          for (int gi = 0; gi < UG; ++gi) {
+            accumulate(s0[gi], r0 + 16 * gi, 0);
+            first = false;
+          }
           finish_unit(i0);
           if (has1) {
-            accumulate(s1, r1, 0);
+#pragma unroll
+            for (int gi = 0; gi < UG; ++gi) {
+              accumulate(s1[gi], r1 + 16 * gi, 0);
+              first = false;
+            }
             finish_unit(i0 + 1);
           }
         } else {
-          // one unit at a time, 16 columns per TMEM load
+          // one unit at a time, one group at a time, 16 columns per TMEM load
 #pragma unroll 1
           for (int h = 0; h <= (has1 ? 1 : 0); ++h) {
 #pragma unroll
-            for (int c0 = 0; c0 < BA; c0 += 16) {
-              uint32_t r[16];
-              ptx::tmem_ld_x16_sync((h ? d1 : d0) + c0, r);
-              accumulate(h ? s1 : s0, r, c0);
+            for (int gi = 0; gi < UG; ++gi) {
+#pragma unroll
+              for (int c0 = 0; c0 < BA; c0 += 16) {
+                uint32_t r[16];
+                ptx::tmem_ld_x16_sync((h ? d1 : d0) + gi * BA + c0, r);
+                accumulate(h ? s1[gi] : s0[gi], r, c0);
+              }
+              first = false;
             }
             if (h == (has1 ? 1 : 0)) release();
             finish_unit(i0 + h);
@@ -993,7 +1066,6 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES>::kThreads, 1)
       int p, j;
       lane_split<L>(i, p, j);
       const int stage = stage_of(i);
-      const int as = astage_of(i);
       if constexpr (L == 1 && (STAGES & 1) != 0) {
         // With an odd stage count the uses of one stage alternate between
         // the two warpgroups, so this warpgroup did not see the stage's
@@ -1006,67 +1078,87 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES>::kThreads, 1)
       if (!wait_warp(&sh->full[stage], (j / SL) & 1, wc)) break;
       if (i == 0 && threadIdx.x == 32 * kDequantWarp0) W4A16_TRACE_POINT(6);
       if (threadIdx.x == 32 * kDequantWarp0) W4A16_TRACE_UNIT(1, i);
-
-      // the row's 64 B of packed codes, stored with the 64-byte swizzle:
-      // 16-byte chunk c of row r sits at chunk position c ^ ((r >> 1) & 3)
-      const uint32_t wrow = wrow0 + stage * C::kStage;
-      uint32_t words[16];
+      bool ok = true;
+      // the row's 64 B of packed codes of every group of the unit, stored
+      // with the 64-byte swizzle: 16-byte chunk c of row r sits at chunk
+      // position c ^ ((r >> 1) & 3)
+      uint32_t words[UG][16];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint4 v = ptx::lds128(wrow + ((q ^ swz) << 4));
-        words[4 * q + 0] = v.x;
-        words[4 * q + 1] = v.y;
-        words[4 * q + 2] = v.z;
-        words[4 * q + 3] = v.w;
-      }
-      float scale = 0.0f;
-      if constexpr (!GRP) scale = __half2float(s_tile(stage)[row]);
-
-      // the TMEM stage is free once the MMAs of the unit that used it
-      // (i - kAS, same lane) completed
-      if (i >= C::kAS && !wait_warp(done_bar(i - C::kAS), done_parity(i - C::kAS), wc)) break;
-      if (threadIdx.x == 32 * kDequantWarp0) W4A16_TRACE_UNIT(2, i);
-      ptx::tc_fence_after();
-      const uint32_t a_addr = lane_base + as * kAStageCols;
-      uint32_t s_hi2 = 0, s_lo2 = 0;
-      if constexpr (!GRP) {
-        if constexpr (F16) {
-          // fp16 operand: fp16_rn(q * s) is one fused multiply-add (q and
-          // s are both fp16)
-          const uint32_t sb = static_cast<uint32_t>(__half_as_ushort(s_tile(stage)[row]));
-          s_hi2 = sb | (sb << 16);
-        } else {
-          const __nv_bfloat16 hi = __float2bfloat16_rn(scale);
-          const float lo_f = scale - __bfloat162float(hi);        // exact
-          const __nv_bfloat16 lo = __float2bfloat16_rn(lo_f);     // exact
-          const uint32_t hi_bits = static_cast<uint32_t>(__bfloat16_as_ushort(hi));
-          const uint32_t lo_bits = static_cast<uint32_t>(__bfloat16_as_ushort(lo));
-          s_hi2 = hi_bits | (hi_bits << 16);
-          s_lo2 = lo_bits | (lo_bits << 16);
+      for (int gi = 0; gi < UG; ++gi) {
+        const uint32_t wrow = wrow0 + stage * C::kStage + gi * kWBytes;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint4 v = ptx::lds128(wrow + ((q ^ swz) << 4));
+          words[gi][4 * q + 0] = v.x;
+          words[gi][4 * q + 1] = v.y;
+          words[gi][4 * q + 2] = v.z;
+          words[gi][4 * q + 3] = v.w;
         }
       }
-      // convert and store 16 columns (4 code words) at a time
+      if (threadIdx.x == 32 * kDequantWarp0) W4A16_TRACE_UNIT(16, i);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint32_t opnd[16];
-#pragma unroll
-        for (int w = 0; w < 4; ++w) codes_to_operand<F16>(words[4 * q + w], &opnd[4 * w]);
+      for (int gi = 0; gi < UG; ++gi) {
+        // the TMEM stage is free once the MMAs of its previous group (jg - AL
+        // of this lane) completed
+        const int jg = UG * j + gi;
+        const int as = gstage_of(p, jg);
+        if (jg >= AL && !wait_warp(&sh->aempty[as], ((jg / AL) - 1) & 1, wc)) {
+          ok = false;
+          break;
+        }
+        if (threadIdx.x == 32 * kDequantWarp0) W4A16_TRACE_UNIT(gi == 0 ? 2 : 17, i);
+        ptx::tc_fence_after();
+        const uint32_t a_addr = lane_base + as * kAStageCols;
+        uint32_t s_hi2 = 0, s_lo2 = 0;
         if constexpr (!GRP) {
-#pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            if constexpr (F16) {
-              opnd[c] = x2_fma<true>(opnd[c], s_hi2, 0x80008000u);   // q * s + (-0)
-            } else {
-              opnd[c] = scale_pair_bf16(opnd[c], s_hi2, s_lo2);
-            }
+          if constexpr (F16) {
+            // fp16 operand: fp16_rn(q * s) is one fused multiply-add (q and
+            // s are both fp16)
+            const uint32_t sb = static_cast<uint32_t>(__half_as_ushort(s_tile(stage, gi)[row]));
+            s_hi2 = sb | (sb << 16);
+          } else {
+            const float scale = __half2float(s_tile(stage, gi)[row]);
+            const __nv_bfloat16 hi = __float2bfloat16_rn(scale);
+            const float lo_f = scale - __bfloat162float(hi);        // exact
+            const __nv_bfloat16 lo = __float2bfloat16_rn(lo_f);     // exact
+            const uint32_t hi_bits = static_cast<uint32_t>(__bfloat16_as_ushort(hi));
+            const uint32_t lo_bits = static_cast<uint32_t>(__bfloat16_as_ushort(lo));
+            s_hi2 = hi_bits | (hi_bits << 16);
+            s_lo2 = lo_bits | (lo_bits << 16);
           }
         }
-        ptx::tmem_st_x16(a_addr + 16 * q, opnd);
+        // convert and store 16 columns (4 code words) at a time
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t opnd[16];
+#pragma unroll
+          for (int w = 0; w < 4; ++w) codes_to_operand<F16>(words[gi][4 * q + w], &opnd[4 * w]);
+          if constexpr (!GRP) {
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              if constexpr (F16) {
+                opnd[c] = x2_fma<true>(opnd[c], s_hi2, 0x80008000u);   // q * s + (-0)
+              } else {
+                opnd[c] = scale_pair_bf16(opnd[c], s_hi2, s_lo2);
+              }
+            }
+          }
+          ptx::tmem_st_x16(a_addr + 16 * q, opnd);
+        }
       }
+      if (!ok) break;
+      // one wait for all groups' TMEM stores (the stores of one group
+      // complete while the next one converts), then one arrival per group
+      if (threadIdx.x == 32 * kDequantWarp0) W4A16_TRACE_UNIT(18, i);
       ptx::tmem_st_wait();
+      if (threadIdx.x == 32 * kDequantWarp0) W4A16_TRACE_UNIT(19, i);
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&sh->afull[as]);
+      if (lane == 0) {
+#pragma unroll
+        for (int gi = 0; gi < UG; ++gi) ptx::mbar_arrive(&sh->afull[gstage_of(p, UG * j + gi)]);
+      }
+      if (!ok) break;
       if (threadIdx.x == 32 * kDequantWarp0) W4A16_TRACE_UNIT(3, i);
       if (i >= total - 2 && threadIdx.x == 32 * kDequantWarp0) W4A16_TRACE_POINT(7);
     }
@@ -1081,10 +1173,10 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES>::kThreads, 1)
   if (threadIdx.x == 32) W4A16_TRACE_POINT(11);
 }
 
-template <int BA, int L, bool GRP, int STAGES, bool F16, int G>
+template <int BA, int L, bool GRP, int STAGES, int UG, bool F16, int G>
 cudaError_t launch_instance(const GemmGroup& grp, bool use_pdl, cudaStream_t stream) {
-  using C = Cfg<BA, L, GRP, STAGES>;
-  auto kernel = w4a16_gemm_tc_kernel<BA, L, GRP, STAGES, F16, G>;
+  using C = Cfg<BA, L, GRP, STAGES, UG>;
+  auto kernel = w4a16_gemm_tc_kernel<BA, L, GRP, STAGES, UG, F16, G>;
   if (grp.count < 1 || grp.count > G) return cudaErrorInvalidValue;
 
   int dev = 0;
@@ -1106,32 +1198,34 @@ cudaError_t launch_instance(const GemmGroup& grp, bool use_pdl, cudaStream_t str
   for (int i = 0; i < grp.count; ++i) {
     const GemmProblem& p = grp.p[i];
     const GemmSchedule& s = grp.s[i];
-    // Activations as [K/64][M][64]: one box {64, BA, 2} brings both 64-wide
-    // K halves of a unit, in the same shared-memory order as two 2-D boxes.
+    if ((p.K / kUnitK) % UG != 0) return cudaErrorInvalidValue;
+    // Activations as [K/64][M][64]: one box {64, BA, 2 * UG} brings all
+    // 64-wide K pieces of a unit, in the same shared-memory order as 2 * UG
+    // 2-D boxes.
     int act_3d = 1;
-    if (encode_tmap_3d(&g.tm[i][0], kActType, p.A, 64, p.M, p.K / 64, p.K * 2, 128, 64, BA, 2,
-                       CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS) {
+    if (encode_tmap_3d(&g.tm[i][0], kActType, p.A, 64, p.M, p.K / 64, p.K * 2, 128, 64, BA,
+                       2 * UG, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS) {
       act_3d = 0;
       if (encode_tmap_2d(&g.tm[i][0], kActType, p.A, p.K, p.M, p.K * 2, 64, BA,
                          CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     }
     // tiled code storage viewed as rows of 64 bytes: tile (tn, g) is rows
-    // (tn * K/128 + g) * 128 .. + 127
+    // (tn * K/128 + g) * 128 .. + 127; a unit's UG tiles are one box
     const uint64_t w_rows =
         static_cast<uint64_t>((p.N + kTileW - 1) / kTileW) * (p.K / kUnitK) * kTileW;
     if (encode_tmap_2d(&g.tm[i][1], CU_TENSOR_MAP_DATA_TYPE_UINT8, p.packed, 64, w_rows, 64, 64,
-                       kTileW, CU_TENSOR_MAP_SWIZZLE_64B) != CUDA_SUCCESS)
+                       kTileW * UG, CU_TENSOR_MAP_SWIZZLE_64B) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
     if (encode_tmap_2d(&g.tm[i][2], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.scales, p.N, p.K / kGroup,
-                       p.N * 2, kTileW, 1, CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
+                       p.N * 2, kTileW, UG, CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
 
     Args& a = g.a[i];
     a.M = static_cast<int>(p.M);
     a.N = static_cast<int>(p.N);
     a.K = static_cast<int>(p.K);
-    a.KB = static_cast<int>(p.K / kUnitK);
+    a.KB = static_cast<int>(p.K / kUnitK / UG);   // units per tile
     a.n_tiles = static_cast<int>((p.N + kTileW - 1) / kTileW);
     a.dp_tiles = s.dp_tiles;
     a.sk_units = static_cast<int>(s.sk_units);
@@ -1164,26 +1258,32 @@ cudaError_t launch_instance(const GemmGroup& grp, bool use_pdl, cudaStream_t str
   return cudaLaunchKernelEx(&cfg, kernel, g);
 }
 
-// The compiled configurations: {act_tile, lanes, group_scale, stages}.
+// The compiled configurations: {act_tile, lanes, group_scale, stages,
+// unit_groups}.
 #define W4A16_GEMM_INSTANCES(X) \
-  X(16, 2, true, 16)            \
-  X(32, 2, true, 12)            \
-  X(64, 2, true, 8)             \
-  X(16, 2, false, 16)           \
-  X(32, 2, false, 12)           \
-  X(64, 2, false, 8)            \
-  X(128, 2, false, 4)           \
-  X(64, 1, false, 8)            \
-  X(128, 1, false, 5)           \
-  X(256, 1, false, 3)
+  X(16, 2, true, 16, 1)         \
+  X(32, 2, true, 12, 1)         \
+  X(64, 2, true, 8, 1)          \
+  X(16, 2, false, 16, 1)        \
+  X(32, 2, false, 12, 1)        \
+  X(64, 2, false, 8, 1)         \
+  X(128, 2, false, 4, 1)        \
+  X(64, 1, false, 8, 1)         \
+  X(128, 1, false, 5, 1)        \
+  X(256, 1, false, 3, 1)        \
+  X(16, 2, true, 8, 2)          \
+  X(16, 2, false, 8, 2)         \
+  X(32, 2, false, 6, 2)         \
+  X(64, 2, false, 4, 2)
 
 // All compiled configurations of one activation type and group size.
 template <bool F16, int G>
 cudaError_t launch_gemm_tc_typed(const GemmKernelConfig& c, const GemmGroup& grp, bool use_pdl,
                                  cudaStream_t stream) {
-#define W4A16_LAUNCH_CASE(BA, L, GRP, ST)                                           \
-  if (c.act_tile == BA && c.lanes == L && c.group_scale == GRP && c.stages == ST) \
-    return launch_instance<BA, L, GRP, ST, F16, G>(grp, use_pdl, stream);
+#define W4A16_LAUNCH_CASE(BA, L, GRP, ST, UG)                                    \
+  if (c.act_tile == BA && c.lanes == L && c.group_scale == GRP && c.stages == ST && \
+      c.unit_groups == UG)                                                          \
+    return launch_instance<BA, L, GRP, ST, UG, F16, G>(grp, use_pdl, stream);
   W4A16_GEMM_INSTANCES(W4A16_LAUNCH_CASE)
 #undef W4A16_LAUNCH_CASE
   return cudaErrorInvalidConfiguration;

@@ -37,6 +37,8 @@ struct GemmKernelConfig {
   bool group_scale;  // true: per-group fp32 scaling of integer-code partial sums
                      // false: weights dequantized to bf16(q*s) before the MMA
   int stages;        // shared-memory pipeline depth (all lanes together)
+  int unit_groups = 1;  // k-groups per pipeline unit (1 or 2): one copy of the
+                        // codes, scales and activations per unit
 };
 
 // The schedule of one launch.
