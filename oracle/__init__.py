@@ -1,5 +1,7 @@
-"""CPU oracle for W4A16 RTN quantization and GEMM.  Test infrastructure only:
-see ``w4a16_oracle`` for what it computes and which passages it follows."""
+"""CPU oracle for W4A16 RTN quantization and GEMM, and for the seeded
+stochastic-rounding quantize mode.  Test infrastructure only: see
+``w4a16_oracle`` and ``stochastic`` for what they compute and which passages
+they follow."""
 
 from .w4a16_oracle import (  # noqa: F401
     GROUP,
@@ -20,4 +22,12 @@ from .w4a16_oracle import (  # noqa: F401
     tiled_bytes,
     to_tile_layout,
     unpack_codes,
+)
+from .stochastic import (  # noqa: F401
+    philox4x32_10,
+    quantize_sr,
+    quantize_sr_f32,
+    stochastic_code,
+    uniform_at,
+    uniform_block,
 )
