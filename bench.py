@@ -186,10 +186,14 @@ def run_gpu(args, rank, world):
     cases = synthetic.WORKLOADS[args.workload]
     if args.grouped is None:
         # the projections are independent problems: one grouped launch of
-        # each kind per step when they fit one launch
-        args.grouped = len(cases) <= w4.MAX_GROUP
+        # each kind per step when they fit one launch (the grouped quantize
+        # rounds to nearest)
+        args.grouped = len(cases) <= w4.MAX_GROUP and args.sr_seed is None
     if args.grouped and len(cases) > w4.MAX_GROUP:
         raise SystemExit(f"--grouped takes at most {w4.MAX_GROUP} projections")
+    if args.grouped and args.sr_seed is not None:
+        raise SystemExit("--sr-seed quantizes per projection (no --grouped)")
+    qname = "rtn_quantize" if args.sr_seed is None else "sr_quantize"
     if args.tune:
         # kernel choice by measurement, once per shape, outside the timed
         # region (later calls of the shape use the memoized choice)
@@ -247,7 +251,8 @@ def run_gpu(args, rank, world):
             s = sets[r % copies][j]
             if evs is not None:
                 evs[2 * j][0].record(st)
-            w4.w4a16_quantize(s["W"], packed=s["packed"], scales=s["scales"], stream=st)
+            w4.w4a16_quantize(s["W"], packed=s["packed"], scales=s["scales"], stream=st,
+                              seed=args.sr_seed)
             if evs is not None:
                 evs[2 * j][1].record(st)
                 evs[2 * j + 1][0].record(st)
@@ -340,7 +345,8 @@ def run_gpu(args, rank, world):
                         w4.w4a16_gemm(s["A"], s["packed"], s["scales"], Y=s["Y"], workspace=ws)
                     else:
                         s = sset[j]
-                        w4.w4a16_quantize(s["W"], packed=s["packed"], scales=s["scales"])
+                        w4.w4a16_quantize(s["W"], packed=s["packed"], scales=s["scales"],
+                                          seed=args.sr_seed)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             gk.replay()
             e0.record(stream)
@@ -400,7 +406,7 @@ def run_gpu(args, rank, world):
                             gbs=round(gb / (tg * 1e-3) / 1e9, 1)))
     for j, c in enumerate([] if args.grouped else cases):
         tq, tg = kern_ms[2 * j], kern_ms[2 * j + 1]
-        kernels.append(dict(kernel="rtn_quantize", shape=[c.N, c.K], us=round(tq * 1e3, 3),
+        kernels.append(dict(kernel=qname, shape=[c.N, c.K], us=round(tq * 1e3, 3),
                             gbs=round(quant_bytes(c.N, c.K) / (tq * 1e-3) / 1e9, 1)))
         kernels.append(dict(kernel="w4a16_gemm_tc", shape=[c.M, c.N, c.K], us=round(tg * 1e3, 3),
                             variant=w4.w4a16_variant_name(w4.w4a16_select_variant(c.M, c.N, c.K)),
@@ -412,7 +418,7 @@ def run_gpu(args, rank, world):
     t_g = sum(kern_ms[1::2])
     launches_kind = 1 if args.grouped else len(cases)
     if t_q >= t_g:
-        dom, dom_bytes = "rtn_quantize", sum(quant_bytes(c.N, c.K) for c in cases)
+        dom, dom_bytes = qname, sum(quant_bytes(c.N, c.K) for c in cases)
         dom_ms, launches_dom = t_q, launches_kind
         bound, achieved, peak, unit = "hbm", None, peaks["hbm_gbs"], "GB/s"
         achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
@@ -428,7 +434,8 @@ def run_gpu(args, rank, world):
         else:
             bound, peak, unit = "hbm", peaks["hbm_gbs"], "GB/s"
             achieved = sum(gemm_bytes(c.M, c.N, c.K) for c in cases) / (dom_ms * 1e-3) / 1e9
-    traffic = dram_traffic(dom, args.workload + ("_grouped" if args.grouped else ""))
+    traffic = dram_traffic(dom, args.workload + ("_grouped" if args.grouped else "") +
+                           ("_sr" if args.sr_seed is not None else ""))
     roofline = dict(bound=bound, achieved=round(achieved, 2), peak=peak, unit=unit,
                     frac=round(achieved / peak, 4),
                     traffic=None if traffic is None else traffic,
@@ -441,7 +448,9 @@ def run_gpu(args, rank, world):
                            shapes=[[c.M, c.N, c.K] for c in cases],
                            step=("one grouped rtn_quantize launch over all projections + one grouped "
                                  "w4a16_gemm launch" if args.grouped else
-                                 "rtn_quantize + w4a16_gemm per projection"),
+                                 "rtn_quantize + w4a16_gemm per projection" if args.sr_seed is None
+                                 else "stochastic-rounding quantize (seed %d) + w4a16_gemm per "
+                                 "projection" % args.sr_seed),
                            l2="inputs rotate over %d copies (%.0f MB > 3x L2)" % (copies, copies * per_copy / 2**20),
                            selection=("per-shape table tuned by measurement before timing" if args.tune
                                       else "cost-model rule"),
@@ -455,9 +464,10 @@ def run_gpu(args, rank, world):
 
 
 # ------------------------------------------------------------- CPU oracle
-def time_oracle(workload: str, budget_s: float):
+def time_oracle(workload: str, budget_s: float, sr_seed=None):
     """The oracle as it stands, on the host cores, over whole passes of the
-    workload (quantize + GEMM per projection) until `budget_s` is used."""
+    workload (quantize + GEMM per projection; the stochastic-rounding quantize
+    when `sr_seed` is given) until `budget_s` is used."""
     import numpy as np
 
     import oracle
@@ -475,7 +485,7 @@ def time_oracle(workload: str, budget_s: float):
     t0 = time.perf_counter()
     while True:
         for c, (wb, ab), mr in zip(cases, inputs, sample_rows):
-            p, s = oracle.quantize(wb)
+            p, s = oracle.quantize(wb) if sr_seed is None else oracle.quantize_sr(wb, sr_seed)
             oracle.gemm(ab[:mr], p, s)
             done_bytes += quant_bytes(c.N, c.K) + gemm_bytes(mr, c.N, c.K)
         passes += 1
@@ -483,7 +493,9 @@ def time_oracle(workload: str, budget_s: float):
             break
     dt = time.perf_counter() - t0
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    sample = (f"{passes} pass(es) of {workload}: oracle quantize + FP32 GEMM per projection"
+    sample = (f"{passes} pass(es) of {workload}: oracle "
+              + ("" if sr_seed is None else "stochastic-rounding ")
+              + "quantize + FP32 GEMM per projection"
               + ("" if all(mr == c.M for mr, c in zip(sample_rows, cases)) else
                  ", GEMM on the first 64 rows of A"))
     return dict(value=round(done_bytes / dt / 1e9, 4), unit="GB/s", cores=cores, kind="oracle",
@@ -506,6 +518,9 @@ def main():
                          "workload has at most 8 projections)")
     ap.add_argument("--per-projection", dest="grouped", action="store_false",
                     help="one quantize and one GEMM launch per projection")
+    ap.add_argument("--sr-seed", type=int, default=None,
+                    help="quantize with seeded stochastic rounding (w4a16_quantize_sr) instead "
+                         "of round to nearest")
     ap.add_argument("--no-tune", dest="tune", action="store_false", default=True,
                     help="select kernels by the cost-model rule instead of tuning each "
                          "shape by measurement first")
@@ -522,7 +537,7 @@ def main():
         if rank != 0:
             return 0
         t_budget = max(5.0, min(60.0, args.cpu_budget * (args.steps + args.warmup) / 10))
-        cb = time_oracle(args.workload, t_budget)
+        cb = time_oracle(args.workload, t_budget, args.sr_seed)
         line = dict(metric=METRIC, value=cb["value"], unit="GB/s", n_gpus=world, steps=args.steps,
                     warmup=args.warmup, ms_per_step=None, higher_is_better=True, scaling="weak",
                     vs_baseline=None, dtype="f32", data="synthetic", impl="reference",
@@ -542,7 +557,7 @@ def main():
     build()
     out = run_gpu(args, rank, world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = time_oracle(args.workload, args.cpu_budget)
+        out["cpu_baseline"] = time_oracle(args.workload, args.cpu_budget, args.sr_seed)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

@@ -102,6 +102,24 @@ int w4a16_quantize(const void* W_bf16, int64_t N, int64_t K, int group, void* pa
                    void* scales_out, void* stream);
 
 /*
+ * Stochastic-rounding quantize/pack ("Piper Kernels", section "Stochastic
+ * quantization": one of the two adjacent codes, chosen with probability
+ * proportional to the distance, so the expected code is the unrounded
+ * ratio; section "ConvRot INT8": the deterministic scales are kept).  Same
+ * arguments, scales, storage, alignment and errors as w4a16_quantize, plus
+ * an unsigned 64-bit seed.  With r = W[n, k] / s (IEEE fp32 division):
+ *   if -8 <= r <= 7:  q = floor(r) + (u < r - floor(r) ? 1 : 0)
+ *   else:             q = clamp(rint_even(r), -8, 7)  (never perturbed)
+ * u = (word >> 8) * 2^-24 from Philox4x32-10 (Salmon et al., "Parallel
+ * random numbers: as easy as 1, 2, 3"): key (seed mod 2^32, seed div 2^32),
+ * counter (e div 4 as two 32-bit words, 0, 0), word e mod 4, with e = n * K
+ * + k the logical element offset.  The same seed gives the same codes on
+ * every launch and launch geometry.  One kernel launch on `stream`.
+ */
+int w4a16_quantize_sr(const void* W_bf16, int64_t N, int64_t K, int group, uint64_t seed,
+                      void* packed_out, void* scales_out, void* stream);
+
+/*
  * Workspace the GEMM needs for this shape with the variant the library's
  * table selects (split-K partial sums and per-tile arrival counters).  May
  * be 0.  The workspace must be zero-filled before its first use

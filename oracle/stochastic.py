@@ -129,8 +129,10 @@ def stochastic_code(ratio: np.ndarray, u: np.ndarray) -> np.ndarray:
     return np.where(interior, sr, det).astype(np.int8)
 
 
-def quantize_sr_f32(x: np.ndarray, seed: int, group: int = GROUP):
-    """Stochastic-rounding quantize of a float32 weight ``x[N, K]``.
+def quantize_sr_f32(x: np.ndarray, seed: int, group: int = GROUP, row0: int = 0):
+    """Stochastic-rounding quantize of a float32 weight ``x[N, K]``
+    (``row0``: ``x`` holds rows row0 .. row0 + N - 1 of a larger logical
+    weight; the draws follow the logical offsets).
 
     Returns ``(packed uint8 [N, K/2], scale_bits uint16 [K/group, N])``.
     Steps, per row n and group g:
@@ -155,11 +157,11 @@ def quantize_sr_f32(x: np.ndarray, seed: int, group: int = GROUP):
     s16 = (amax / np.float32(7.0)).astype(np.float16)
     s16 = np.where(s16 == np.float16(0.0), np.float16(1.0), s16)
     ratio = (xg / s16.astype(np.float32)[:, :, None]).reshape(n_rows, k_cols)   # step 2
-    u = uniform_block(seed, k_cols, slice(0, n_rows), slice(0, k_cols))        # step 3
+    u = uniform_block(seed, k_cols, slice(row0, row0 + n_rows), slice(0, k_cols))  # step 3
     codes = stochastic_code(ratio, u)                                           # step 4
     return pack_codes(codes), np.ascontiguousarray(s16.T).view(np.uint16)       # step 5
 
 
-def quantize_sr(w_bits: np.ndarray, seed: int, group: int = GROUP):
+def quantize_sr(w_bits: np.ndarray, seed: int, group: int = GROUP, row0: int = 0):
     """Stochastic-rounding quantize of a bf16 weight (uint16 bit patterns)."""
-    return quantize_sr_f32(bf16_bits_to_f32(w_bits), seed, group)
+    return quantize_sr_f32(bf16_bits_to_f32(w_bits), seed, group, row0)

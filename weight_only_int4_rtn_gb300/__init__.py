@@ -51,6 +51,8 @@ SIGNATURES = [
     ("w4a16_packed_bytes", _c_size, [_c_int64, _c_int64]),
     ("w4a16_scales_bytes", _c_size, [_c_int64, _c_int64, ctypes.c_int]),
     ("w4a16_quantize", ctypes.c_int, [_vp, _c_int64, _c_int64, ctypes.c_int, _vp, _vp, _vp]),
+    ("w4a16_quantize_sr", ctypes.c_int,
+     [_vp, _c_int64, _c_int64, ctypes.c_int, ctypes.c_uint64, _vp, _vp, _vp]),
     ("w4a16_gemm_workspace_bytes", _c_size, [_c_int64, _c_int64, _c_int64]),
     ("w4a16_gemm_workspace_bytes_max", _c_size, [_c_int64, _c_int64, _c_int64]),
     ("w4a16_workspace_init", ctypes.c_int, [_vp, _c_size, _vp]),
@@ -168,11 +170,15 @@ def w4a16_gemm_workspace_bytes_max(M: int, N: int, K: int) -> int:
 
 # --------------------------------------------------------------- quantize
 def w4a16_quantize(W: torch.Tensor, group: int = GROUP, packed: torch.Tensor | None = None,
-                   scales: torch.Tensor | None = None, stream=None):
-    """RTN-quantize ``W[N, K]`` (bf16, CUDA).  Returns ``(packed, scales)``:
+                   scales: torch.Tensor | None = None, stream=None, seed: int | None = None):
+    """Quantize ``W[N, K]`` (bf16, CUDA).  Returns ``(packed, scales)``:
     ``packed`` is the 1-D uint8 tiled code storage of w4a16_packed_bytes(N, K)
     bytes, ``scales`` fp16 ``[K/128, N]``; outputs are allocated when not
-    given."""
+    given.  Round to nearest (w4a16_quantize), or, with an unsigned 64-bit
+    ``seed``, seeded stochastic rounding with the same scales
+    (w4a16_quantize_sr)."""
+    if seed is not None and not 0 <= int(seed) < (1 << 64):
+        raise ValueError("seed must be an unsigned 64-bit integer")
     _require_cuda(W, "W", torch.bfloat16)
     if W.dim() != 2:
         raise ValueError("W must be [N, K]")
@@ -186,9 +192,14 @@ def w4a16_quantize(W: torch.Tensor, group: int = GROUP, packed: torch.Tensor | N
     _require_cuda(scales, "scales", torch.float16)
     if packed.numel() != nbytes or scales.numel() * group != N * K:
         raise ValueError("output buffers have the wrong size")
-    st = lib().w4a16_quantize(W.data_ptr(), N, K, group, packed.data_ptr(), scales.data_ptr(),
-                              _stream_handle(W.device, stream))
-    _check(st, "w4a16_quantize")
+    if seed is None:
+        st = lib().w4a16_quantize(W.data_ptr(), N, K, group, packed.data_ptr(), scales.data_ptr(),
+                                  _stream_handle(W.device, stream))
+        _check(st, "w4a16_quantize")
+    else:
+        st = lib().w4a16_quantize_sr(W.data_ptr(), N, K, group, int(seed), packed.data_ptr(),
+                                     scales.data_ptr(), _stream_handle(W.device, stream))
+        _check(st, "w4a16_quantize_sr")
     return packed, scales
 
 

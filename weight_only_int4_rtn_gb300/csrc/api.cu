@@ -548,8 +548,9 @@ size_t w4a16_scales_bytes(int64_t N, int64_t K, int group) {
   return static_cast<size_t>(K / group) * static_cast<size_t>(N) * 2;
 }
 
-int w4a16_quantize(const void* W_bf16, int64_t N, int64_t K, int group, void* packed_out,
-                   void* scales_out, void* stream) {
+namespace {
+int quantize_impl(const void* W_bf16, int64_t N, int64_t K, int group, const uint64_t* sr_seed,
+                  void* packed_out, void* scales_out, void* stream) {
   if (W_bf16 == nullptr || packed_out == nullptr || scales_out == nullptr)
     return W4A16_ERR_INVALID_ARG;
   if (N < 1 || K < 1) return W4A16_ERR_INVALID_ARG;
@@ -562,10 +563,21 @@ int w4a16_quantize(const void* W_bf16, int64_t N, int64_t K, int group, void* pa
   if (!device_info(dev)) return W4A16_ERR_CUDA;
   const cudaError_t e =
       launch_rtn_quantize(W_bf16, N, K, packed_out, scales_out, dev.num_sms, dev.error_word,
-                          g_timeout_ns.load(), static_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return cuda_failure(e, "rtn_quantize");
+                          g_timeout_ns.load(), static_cast<cudaStream_t>(stream), sr_seed);
+  if (e != cudaSuccess) return cuda_failure(e, sr_seed ? "rtn_quantize (stochastic)" : "rtn_quantize");
   g_launches.fetch_add(1);
   return W4A16_OK;
+}
+}  // namespace
+
+int w4a16_quantize(const void* W_bf16, int64_t N, int64_t K, int group, void* packed_out,
+                   void* scales_out, void* stream) {
+  return quantize_impl(W_bf16, N, K, group, nullptr, packed_out, scales_out, stream);
+}
+
+int w4a16_quantize_sr(const void* W_bf16, int64_t N, int64_t K, int group, uint64_t seed,
+                      void* packed_out, void* scales_out, void* stream) {
+  return quantize_impl(W_bf16, N, K, group, &seed, packed_out, scales_out, stream);
 }
 
 size_t w4a16_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {

@@ -12,10 +12,11 @@ namespace w4a16 {
 constexpr int kGroup = 128;     // quantization group along K
 constexpr int kTileW = 128;     // weight rows per GEMM tile (tcgen05 M)
 
-// RTN quantize/pack; one launch.
+// RTN quantize/pack; one launch.  sr_seed non-null: stochastic rounding with
+// that seed (same scales and storage).
 cudaError_t launch_rtn_quantize(const void* W, int64_t N, int64_t K, void* packed, void* scales,
                                 int num_sms, uint32_t* error_word, uint64_t timeout_ns,
-                                cudaStream_t stream);
+                                cudaStream_t stream, const uint64_t* sr_seed = nullptr);
 
 // Several weights quantized in one launch (independent problems).
 constexpr int kMaxQuantizeGroup = 8;
@@ -27,7 +28,7 @@ struct QuantizeProblem {
 };
 cudaError_t launch_rtn_quantize_group(const QuantizeProblem* probs, int count, int num_sms,
                                       uint32_t* error_word, uint64_t timeout_ns,
-                                      cudaStream_t stream);
+                                      cudaStream_t stream, const uint64_t* sr_seed = nullptr);
 
 // One configuration of the tcgen05 GEMM kernel.
 struct GemmKernelConfig {

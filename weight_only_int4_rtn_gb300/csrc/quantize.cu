@@ -35,6 +35,18 @@
 // two's-complement nibble.  For a normal scale |w / s| <= 7 (1 + 2^-11) < 7.5,
 // so no clamp can be active.  A subnormal scale (rare) takes the IEEE
 // division __fdiv_rn and the clamp value by value.
+//
+// Stochastic-rounding mode ("Piper Kernels", section "Stochastic
+// quantization"; the scales stay the round-to-nearest ones, section "ConvRot
+// INT8").  The same kernel with the last step replaced: with r = fl32(w / s)
+// (the same correctly rounded quotient), a value interior to the code range
+// (-8 <= r <= 7) takes floor(r) + 1 when u < r - floor(r), else floor(r);
+// others take the round-to-nearest code.  u is drawn from Philox4x32-10
+// (Salmon et al., "Parallel random numbers: as easy as 1, 2, 3") by logical
+// element offset e = n * K + k: key (seed mod 2^32, seed div 2^32), counter
+// (e div 4 as two 32-bit words, 0, 0), word e mod 4, u = (word >> 8) * 2^-24.
+// Exact hits (r integral) and values outside the range are never perturbed,
+// and the draws do not depend on the launch geometry.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -71,6 +83,7 @@ struct QGroupArgs {
   int tiles[kQMaxGroup];
   int cta_start[kQMaxGroup + 1];
   int count;
+  uint64_t seed;   // stochastic-rounding mode: the generator's key
 };
 
 struct QShared {
@@ -124,6 +137,57 @@ __device__ __forceinline__ uint32_t codes_exact(const float (&f)[8], float s) {
   return pack8(y);
 }
 
+// ------------------------------------------------- stochastic-rounding mode
+constexpr uint32_t kPhiloxM0 = 0xD2511F53u;
+constexpr uint32_t kPhiloxM1 = 0xCD9E8D57u;
+constexpr uint32_t kPhiloxW0 = 0x9E3779B9u;
+constexpr uint32_t kPhiloxW1 = 0xBB67AE85u;
+
+// Philox4x32-10: ten rounds; one round maps (c0, c1, c2, c3) under (k0, k1)
+// to (hi(M1 c2) ^ c1 ^ k0, lo(M1 c2), hi(M0 c0) ^ c3 ^ k1, lo(M0 c0)), the
+// key advancing by the Weyl constants before every round but the first.
+__device__ __forceinline__ void philox4x32_10(uint32_t (&c)[4], uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint32_t hi0 = __umulhi(kPhiloxM0, c[0]);
+    const uint32_t lo0 = kPhiloxM0 * c[0];
+    const uint32_t hi1 = __umulhi(kPhiloxM1, c[2]);
+    const uint32_t lo1 = kPhiloxM1 * c[2];
+    const uint32_t n0 = hi1 ^ c[1] ^ (k0 + static_cast<uint32_t>(r) * kPhiloxW0);
+    const uint32_t n2 = hi0 ^ c[3] ^ (k1 + static_cast<uint32_t>(r) * kPhiloxW1);
+    c[0] = n0;
+    c[1] = lo1;
+    c[2] = n2;
+    c[3] = lo0;
+  }
+}
+
+// Codes of 8 values at logical offsets e0 .. e0 + 7 (e0 a multiple of 4)
+// from their correctly rounded quotients x[i] = fl32(w / s): stochastic
+// between the adjacent integers where -8 <= x <= 7, nearest (clamped)
+// elsewhere.
+__device__ __forceinline__ uint32_t codes_stochastic(const float (&x)[8], uint64_t e0, uint32_t k0,
+                                                     uint32_t k1) {
+  uint32_t y[8];
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    const uint64_t ctr = (e0 >> 2) + static_cast<uint64_t>(half);
+    uint32_t c[4] = {static_cast<uint32_t>(ctr), static_cast<uint32_t>(ctr >> 32), 0u, 0u};
+    philox4x32_10(c, k0, k1);
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const float r = x[4 * half + w];
+      const float u = __uint2float_rn(c[w] >> 8) * 5.9604644775390625e-08f;   // * 2^-24, exact
+      const float lo = floorf(r);
+      const float up = (u < r - lo) ? 1.0f : 0.0f;                          // r - lo exact
+      const bool interior = (r >= -8.0f) && (r <= 7.0f);
+      const float code = interior ? lo + up : fminf(fmaxf(r, -8.0f), 7.0f);
+      y[4 * half + w] = __float_as_uint(__fadd_rn(code, kRoundMagic));     // rint for the clamp
+    }
+  }
+  return pack8(y);
+}
+
 __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -140,6 +204,7 @@ __device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t acc, uint32_t w) {
   return *reinterpret_cast<const uint32_t*>(&m);
 }
 
+template <bool SR>
 __global__ void __launch_bounds__(kQThreads, 1)
     rtn_quantize_kernel(const __grid_constant__ QGroupArgs q, uint32_t* err, uint64_t timeout_ns) {
   // this CTA's weight and its index in that weight's sub-grid
@@ -248,7 +313,29 @@ __global__ void __launch_bounds__(kQThreads, 1)
     // normal scale (no divergence between rows); a subnormal scale takes the
     // IEEE division and the clamp.
     uint32_t* const dst = packed + ((static_cast<int64_t>(tn) * G + g) * kQRows + row) * 16 + 8 * h;
-    if ((__half_as_ushort(s16) & 0x7C00u) != 0) {
+    if constexpr (SR) {
+      // logical offset of this thread's first value: row n, k = 128 g + 64 h
+      const uint64_t e_row = static_cast<uint64_t>(tn * kQRows + row) * static_cast<uint64_t>(G) *
+                                 kGroup + static_cast<uint64_t>(g * kGroup + 64 * h);
+      const uint32_t k0 = static_cast<uint32_t>(q.seed);
+      const uint32_t k1 = static_cast<uint32_t>(q.seed >> 32);
+      const bool normal = (__half_as_ushort(s16) & 0x7C00u) != 0;
+#pragma unroll 1
+      for (int c = 0; c < 8; ++c) {
+        float f[8];
+        unpack8(ptx::lds128(chunk_addr(box, row, c)), f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (normal) {
+            const float q1 = __fmul_rn(f[i], r);
+            f[i] = fmaf(fmaf(-q1, s, f[i]), r, q1);   // fl32(w / s), as in the RTN mode
+          } else {
+            f[i] = __fdiv_rn(f[i], s);
+          }
+        }
+        dst[c] = codes_stochastic(f, e_row + 8 * c, k0, k1);
+      }
+    } else if ((__half_as_ushort(s16) & 0x7C00u) != 0) {
       uint32_t words[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
@@ -279,7 +366,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
 
 cudaError_t launch_rtn_quantize_group(const QuantizeProblem* probs, int count, int num_sms,
                                       uint32_t* error_word, uint64_t timeout_ns,
-                                      cudaStream_t stream) {
+                                      cudaStream_t stream, const uint64_t* sr_seed) {
   static_assert(kQMaxGroup == kMaxQuantizeGroup, "group size of the kernel arguments");
   if (count < 1 || count > kQMaxGroup) return cudaErrorInvalidValue;
   QGroupArgs q{};
@@ -327,18 +414,21 @@ cudaError_t launch_rtn_quantize_group(const QuantizeProblem* probs, int count, i
   }
   q.cta_start[count] = start;
   q.count = count;
+  q.seed = sr_seed != nullptr ? *sr_seed : 0;
+  auto kernel = sr_seed != nullptr ? rtn_quantize_kernel<true> : rtn_quantize_kernel<false>;
 
   constexpr size_t smem = static_cast<size_t>(kQStages) * kQTileBytes + sizeof(QShared) + 1024;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  static bool attr_set[64] = {};
+  static bool attr_set[2][64] = {};
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!attr_set[dev]) {
-    e = cudaFuncSetAttribute(rtn_quantize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const int mode = sr_seed != nullptr ? 1 : 0;
+  if (!attr_set[mode][dev]) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+    attr_set[mode][dev] = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(start));
@@ -351,14 +441,14 @@ cudaError_t launch_rtn_quantize_group(const QuantizeProblem* probs, int count, i
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, rtn_quantize_kernel, q, error_word, timeout_ns);
+  return cudaLaunchKernelEx(&cfg, kernel, q, error_word, timeout_ns);
 }
 
 cudaError_t launch_rtn_quantize(const void* W, int64_t N, int64_t K, void* packed, void* scales,
                                 int num_sms, uint32_t* error_word, uint64_t timeout_ns,
-                                cudaStream_t stream) {
+                                cudaStream_t stream, const uint64_t* sr_seed) {
   QuantizeProblem p{W, N, K, packed, scales};
-  return launch_rtn_quantize_group(&p, 1, num_sms, error_word, timeout_ns, stream);
+  return launch_rtn_quantize_group(&p, 1, num_sms, error_word, timeout_ns, stream, sr_seed);
 }
 
 }  // namespace w4a16
