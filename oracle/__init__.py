@@ -1,7 +1,7 @@
-"""CPU oracle for W4A16 RTN quantization and GEMM, and for the seeded
-stochastic-rounding quantize mode.  Test infrastructure only: see
-``w4a16_oracle`` and ``stochastic`` for what they compute and which passages
-they follow."""
+"""CPU oracle for W4A16 RTN quantization and GEMM, the seeded
+stochastic-rounding quantize mode and the INT8 weight-only (W8A16) scheme.
+Test infrastructure only: see ``w4a16_oracle``, ``stochastic`` and
+``w8a16_oracle`` for what they compute and which passages they follow."""
 
 from .w4a16_oracle import (  # noqa: F401
     GROUP,
@@ -30,4 +30,15 @@ from .stochastic import (  # noqa: F401
     stochastic_code,
     uniform_at,
     uniform_block,
+)
+from .w8a16_oracle import (  # noqa: F401
+    Q8MAX,
+    Q8MIN,
+    dequantize8,
+    from_tile_layout8,
+    gemm8,
+    quantize8,
+    quantize8_f32,
+    tiled8_bytes,
+    to_tile_layout8,
 )

@@ -149,16 +149,15 @@ constexpr uint32_t kPhiloxW1 = 0xBB67AE85u;
 __device__ __forceinline__ void philox4x32_10(uint32_t (&c)[4], uint32_t k0, uint32_t k1) {
 #pragma unroll
   for (int r = 0; r < 10; ++r) {
-    const uint32_t hi0 = __umulhi(kPhiloxM0, c[0]);
-    const uint32_t lo0 = kPhiloxM0 * c[0];
-    const uint32_t hi1 = __umulhi(kPhiloxM1, c[2]);
-    const uint32_t lo1 = kPhiloxM1 * c[2];
-    const uint32_t n0 = hi1 ^ c[1] ^ (k0 + static_cast<uint32_t>(r) * kPhiloxW0);
-    const uint32_t n2 = hi0 ^ c[3] ^ (k1 + static_cast<uint32_t>(r) * kPhiloxW1);
+    // one 32 x 32 -> 64-bit product gives both halves
+    const uint64_t p0 = static_cast<uint64_t>(kPhiloxM0) * c[0];
+    const uint64_t p1 = static_cast<uint64_t>(kPhiloxM1) * c[2];
+    const uint32_t n0 = static_cast<uint32_t>(p1 >> 32) ^ c[1] ^ (k0 + static_cast<uint32_t>(r) * kPhiloxW0);
+    const uint32_t n2 = static_cast<uint32_t>(p0 >> 32) ^ c[3] ^ (k1 + static_cast<uint32_t>(r) * kPhiloxW1);
     c[0] = n0;
-    c[1] = lo1;
+    c[1] = static_cast<uint32_t>(p1);
     c[2] = n2;
-    c[3] = lo0;
+    c[3] = static_cast<uint32_t>(p0);
   }
 }
 
