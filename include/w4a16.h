@@ -316,6 +316,56 @@ int w4a16_gemm_noalloc(const void* A_bf16, int64_t M, int64_t N, int64_t K, cons
                        const void* scales, int group, const void* bias_bf16_or_null, void* Y_bf16,
                        void* stream);
 
+/* ------------------------------------------------------------------------
+ * INT8 weight-only scheme (W8A16).  "Kernel dispatch and Humming
+ * quantization in PhyAI", section "Choose precision by layer and hardware":
+ * INT8 is one of the Humming weight schemes, with BF16 activations.  The
+ * method is the INT4 one with 8-bit codes; scales, groups, alignment,
+ * workspace rules and error codes are those of the INT4 calls.
+ * ---------------------------------------------------------------------- */
+
+/* Bytes of the tiled INT8 code storage: (N rounded up to 128) * K. */
+size_t w8a16_packed_bytes(int64_t N, int64_t K);
+
+/*
+ * RTN INT8 quantize/pack.  For each row n and group g of 128 along K:
+ *   amax = max |W[n, k]| (fp32);  s = fp16_rn(amax / 127.0f);  s = 1 if s == 0;
+ *   q = clamp(rint_even(W[n, k] / s), -128, 127)   (IEEE fp32 division)
+ * Codes as two's-complement bytes in tiles of 128 rows x 128 K values
+ * (16 KiB, row-major inside), tile (n/128, g) at ((n/128) * K/128 + g) *
+ * 16384, padding rows zero; s to scales_out[g * N + n].  W: [N, K] bf16
+ * (read); packed_out: w8a16_packed_bytes(N, K) bytes; scales_out: (K/128)*N
+ * fp16 (both written).  One kernel launch on `stream`.
+ */
+int w8a16_quantize(const void* W_bf16, int64_t N, int64_t K, int group, void* packed_out,
+                   void* scales_out, void* stream);
+
+/* Workspace the W8A16 GEMM needs for this shape (0: none). */
+size_t w8a16_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+/*
+ * Y[M, N] = bf16( A[M, K] . dequant8(W)[N, K]^T + bias[N] ), dequant8(W)[n, k]
+ * = q[n, k] * s[k/128, n], accumulated in fp32, bias added in fp32; packed and
+ * scales as written by w8a16_quantize; otherwise as w4a16_gemm.  The variant
+ * is chosen by the library's cost model over the INT8 catalogue.
+ */
+int w8a16_gemm(const void* A_bf16, int64_t M, int64_t N, int64_t K, const void* packed,
+               const void* scales, int group, const void* bias_bf16_or_null, void* Y_bf16,
+               void* workspace, size_t workspace_bytes, void* stream);
+
+/* The INT8 catalogue: count, names, eligibility, workspace, the rule's
+ * choice (-1: none) and a forced-variant GEMM (W4A16_ERR_NO_VARIANT when the
+ * variant cannot run the shape). */
+int w8a16_variant_count(void);
+const char* w8a16_variant_name(int variant);
+int w8a16_variant_eligible(int variant, int64_t M, int64_t N, int64_t K);
+size_t w8a16_variant_workspace_bytes(int variant, int64_t M, int64_t N, int64_t K);
+int w8a16_select_variant(int64_t M, int64_t N, int64_t K);
+int w8a16_gemm_variant(int variant, const void* A_bf16, int64_t M, int64_t N, int64_t K,
+                       const void* packed, const void* scales, int group,
+                       const void* bias_bf16_or_null, void* Y_bf16, void* workspace,
+                       size_t workspace_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

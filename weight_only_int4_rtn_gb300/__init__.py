@@ -53,6 +53,19 @@ SIGNATURES = [
     ("w4a16_quantize", ctypes.c_int, [_vp, _c_int64, _c_int64, ctypes.c_int, _vp, _vp, _vp]),
     ("w4a16_quantize_sr", ctypes.c_int,
      [_vp, _c_int64, _c_int64, ctypes.c_int, ctypes.c_uint64, _vp, _vp, _vp]),
+    ("w8a16_packed_bytes", _c_size, [_c_int64, _c_int64]),
+    ("w8a16_quantize", ctypes.c_int, [_vp, _c_int64, _c_int64, ctypes.c_int, _vp, _vp, _vp]),
+    ("w8a16_gemm_workspace_bytes", _c_size, [_c_int64, _c_int64, _c_int64]),
+    ("w8a16_gemm", ctypes.c_int,
+     [_vp, _c_int64, _c_int64, _c_int64, _vp, _vp, ctypes.c_int, _vp, _vp, _vp, _c_size, _vp]),
+    ("w8a16_variant_count", ctypes.c_int, []),
+    ("w8a16_variant_name", ctypes.c_char_p, [ctypes.c_int]),
+    ("w8a16_variant_eligible", ctypes.c_int, [ctypes.c_int, _c_int64, _c_int64, _c_int64]),
+    ("w8a16_variant_workspace_bytes", _c_size, [ctypes.c_int, _c_int64, _c_int64, _c_int64]),
+    ("w8a16_select_variant", ctypes.c_int, [_c_int64, _c_int64, _c_int64]),
+    ("w8a16_gemm_variant", ctypes.c_int,
+     [ctypes.c_int, _vp, _c_int64, _c_int64, _c_int64, _vp, _vp, ctypes.c_int, _vp, _vp, _vp,
+      _c_size, _vp]),
     ("w4a16_gemm_workspace_bytes", _c_size, [_c_int64, _c_int64, _c_int64]),
     ("w4a16_gemm_workspace_bytes_max", _c_size, [_c_int64, _c_int64, _c_int64]),
     ("w4a16_workspace_init", ctypes.c_int, [_vp, _c_size, _vp]),
@@ -277,6 +290,76 @@ def w4a16_gemm(A: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor,
         st = fn(variant, A.data_ptr(), M, N, K, packed.data_ptr(), scales.data_ptr(), group,
                 bias_ptr, Y.data_ptr(), ws_ptr, ws_bytes, sh)
     _check(st, "w4a16_gemm_f16" if f16 else "w4a16_gemm")
+    return Y
+
+
+# ------------------------------------------------------------ INT8 (W8A16)
+def w8a16_quantize(W: torch.Tensor, group: int = GROUP, packed: torch.Tensor | None = None,
+                   scales: torch.Tensor | None = None, stream=None):
+    """RTN INT8 quantize ``W[N, K]`` (bf16, CUDA).  Returns ``(packed,
+    scales)``: 1-D uint8 tiled codes of w8a16_packed_bytes(N, K) bytes and fp16
+    scales ``[K/128, N]``."""
+    _require_cuda(W, "W", torch.bfloat16)
+    if W.dim() != 2:
+        raise ValueError("W must be [N, K]")
+    N, K = W.shape
+    nbytes = lib().w8a16_packed_bytes(N, K)
+    if packed is None:
+        packed = torch.empty(nbytes, dtype=torch.uint8, device=W.device)
+    if scales is None:
+        scales = torch.empty((max(K // group, 0), N), dtype=torch.float16, device=W.device)
+    _require_cuda(packed, "packed", torch.uint8)
+    _require_cuda(scales, "scales", torch.float16)
+    if packed.numel() != nbytes or scales.numel() * group != N * K:
+        raise ValueError("output buffers have the wrong size")
+    _check(lib().w8a16_quantize(W.data_ptr(), N, K, group, packed.data_ptr(), scales.data_ptr(),
+                                _stream_handle(W.device, stream)), "w8a16_quantize")
+    return packed, scales
+
+
+def w8a16_gemm(A: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor,
+               bias: torch.Tensor | None = None, Y: torch.Tensor | None = None,
+               workspace: torch.Tensor | None = None, group: int = GROUP, stream=None,
+               variant: int | None = None) -> torch.Tensor:
+    """``Y[M, N] = A[M, K] @ dequant8(packed, scales)^T + bias`` (bf16) on
+    the GPU; ``variant`` forces one entry of the INT8 catalogue."""
+    _require_cuda(A, "A", torch.bfloat16)
+    _require_cuda(packed, "packed", torch.uint8)
+    _require_cuda(scales, "scales", torch.float16)
+    if A.dim() != 2 or scales.dim() != 2:
+        raise ValueError("A and scales must be 2-D")
+    M, K = A.shape
+    N = scales.shape[1]
+    if scales.shape[0] * group != K:
+        raise ValueError("scales must be [K/128, N]")
+    if packed.numel() != lib().w8a16_packed_bytes(N, K):
+        raise ValueError("packed must hold w8a16_packed_bytes(N, K) bytes of tiled codes")
+    if bias is not None:
+        _require_cuda(bias, "bias", torch.bfloat16)
+        if bias.numel() != N:
+            raise ValueError("bias must have N elements")
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    _require_cuda(Y, "Y", torch.bfloat16)
+    if Y.shape != (M, N):
+        raise ValueError("Y must be [M, N]")
+    sh = _stream_handle(A.device, stream)
+    L = lib()
+    need = (L.w8a16_gemm_workspace_bytes(M, N, K) if variant is None
+            else L.w8a16_variant_workspace_bytes(variant, M, N, K))
+    if workspace is None:
+        workspace = _default_ws.get(A.device, sh, need)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    bias_ptr = bias.data_ptr() if bias is not None else None
+    if variant is None:
+        st = L.w8a16_gemm(A.data_ptr(), M, N, K, packed.data_ptr(), scales.data_ptr(), group,
+                          bias_ptr, Y.data_ptr(), ws_ptr, ws_bytes, sh)
+    else:
+        st = L.w8a16_gemm_variant(variant, A.data_ptr(), M, N, K, packed.data_ptr(),
+                                  scales.data_ptr(), group, bias_ptr, Y.data_ptr(), ws_ptr,
+                                  ws_bytes, sh)
+    _check(st, "w8a16_gemm")
     return Y
 
 

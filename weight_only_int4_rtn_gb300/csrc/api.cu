@@ -130,6 +130,21 @@ const Variant kVariants[] = {
 };
 constexpr int kNumVariants = static_cast<int>(sizeof(kVariants) / sizeof(kVariants[0]));
 
+// INT8 weights (W8A16), bf16 activations.
+const Variant kVariants8[] = {
+    {"w8_tc_a16_grp_sk", {16, 2, true, 10, 1, 8}, true, 1, 0.60},
+    {"w8_tc_a16_grp_sk8", {16, 2, true, 10, 1, 8}, true, 8, 0.55},
+    {"w8_tc_a16_grp_dp", {16, 2, true, 10, 1, 8}, false, 1, 0.55},
+    {"w8_tc_a32_grp_sk", {32, 2, true, 8, 1, 8}, true, 1, 0.70},
+    {"w8_tc_a64_deq2_sk", {64, 2, false, 6, 1, 8}, true, 1, 0.70},
+    {"w8_tc_a64_deq2_dp", {64, 2, false, 6, 1, 8}, false, 1, 0.70},
+    {"w8_tc_a128_deq_sk", {128, 1, false, 4, 1, 8}, true, 1, 0.80},
+    {"w8_tc_a128_deq_dp", {128, 1, false, 4, 1, 8}, false, 1, 0.80},
+    {"w8_tc_a256_deq_sk", {256, 1, false, 2, 1, 8}, true, 1, 1.00},
+    {"w8_tc_a256_deq_dp", {256, 1, false, 2, 1, 8}, false, 1, 1.00},
+};
+constexpr int kNumVariants8 = static_cast<int>(sizeof(kVariants8) / sizeof(kVariants8[0]));
+
 int variant_by_name(const std::string& n) {
   for (int i = 0; i < kNumVariants; ++i)
     if (n == kVariants[i].name) return i;
@@ -179,15 +194,21 @@ GemmSchedule make_schedule(const Variant& v, int64_t M, int64_t N, int64_t K, in
   return s;
 }
 
-bool variant_eligible(int id, int64_t M, int64_t N, int64_t K) {
-  if (id < 0 || id >= kNumVariants) return false;
+bool variant_ok(const Variant& v, int64_t M, int64_t N, int64_t K) {
   if (!shape_ok(M, N, K)) return false;
-  const Variant& v = kVariants[id];
   if (!gemm_config_available(v.cfg)) return false;
   const int64_t tiles = gemm_tiles(v.cfg, M, N);
   if (tiles * (K / kGroup) >= (1ll << 31)) return false;
   if ((K / kGroup) % v.cfg.unit_groups != 0) return false;
   return true;
+}
+
+bool variant_eligible(int id, int64_t M, int64_t N, int64_t K) {
+  return id >= 0 && id < kNumVariants && variant_ok(kVariants[id], M, N, K);
+}
+
+bool variant8_eligible(int id, int64_t M, int64_t N, int64_t K) {
+  return id >= 0 && id < kNumVariants8 && variant_ok(kVariants8[id], M, N, K);
 }
 
 // Rule for shapes without a table entry: a cost model fitted to GB300
@@ -296,12 +317,11 @@ int check_gemm_args(const void* A, int64_t M, int64_t N, int64_t K, const void* 
   return W4A16_OK;
 }
 
-int run_gemm(int id, const void* A, int64_t M, int64_t N, int64_t K, const void* packed,
-             const void* scales, const void* bias, void* Y, void* ws, size_t ws_bytes,
-             cudaStream_t stream, bool act_f16 = false) {
+int run_gemm_v(const Variant& v, const void* A, int64_t M, int64_t N, int64_t K,
+               const void* packed, const void* scales, const void* bias, void* Y, void* ws,
+               size_t ws_bytes, cudaStream_t stream, bool act_f16) {
   DeviceInfo dev;
   if (!device_info(dev)) return W4A16_ERR_CUDA;
-  const Variant& v = kVariants[id];
   const GemmSchedule s = make_schedule(v, M, N, K, dev.num_sms);
   const size_t need = gemm_workspace_bytes(v.cfg, s, M, N, K);
   if (need > 0) {
@@ -330,6 +350,38 @@ int run_gemm(int id, const void* A, int64_t M, int64_t N, int64_t K, const void*
   if (e != cudaSuccess) return cuda_failure(e, v.name);
   g_launches.fetch_add(1);
   return W4A16_OK;
+}
+
+int run_gemm(int id, const void* A, int64_t M, int64_t N, int64_t K, const void* packed,
+             const void* scales, const void* bias, void* Y, void* ws, size_t ws_bytes,
+             cudaStream_t stream, bool act_f16 = false) {
+  return run_gemm_v(kVariants[id], A, M, N, K, packed, scales, bias, Y, ws, ws_bytes, stream,
+                    act_f16);
+}
+
+// INT8: the rule over the INT8 catalogue (no measured table).
+int select_variant8(int64_t M, int64_t N, int64_t K) {
+  DeviceInfo dev;
+  const int sms = device_info(dev) ? dev.num_sms : kDefaultSms;
+  int best = -1;
+  double best_t = 0.0;
+  for (int id = 0; id < kNumVariants8; ++id) {
+    if (!variant8_eligible(id, M, N, K)) continue;
+    const double t = estimate_us(kVariants8[id], M, N, K, sms);
+    if (best < 0 || t < best_t) {
+      best = id;
+      best_t = t;
+    }
+  }
+  return best;
+}
+
+size_t variant8_ws(int id, int64_t M, int64_t N, int64_t K) {
+  DeviceInfo dev;
+  int sms = kDefaultSms;
+  if (device_info(dev)) sms = dev.num_sms;
+  const Variant& v = kVariants8[id];
+  return gemm_workspace_bytes(v.cfg, make_schedule(v, M, N, K, sms), M, N, K);
 }
 
 // ------------------------------------------------------------ groups
@@ -550,7 +602,7 @@ size_t w4a16_scales_bytes(int64_t N, int64_t K, int group) {
 
 namespace {
 int quantize_impl(const void* W_bf16, int64_t N, int64_t K, int group, const uint64_t* sr_seed,
-                  void* packed_out, void* scales_out, void* stream) {
+                  void* packed_out, void* scales_out, void* stream, bool int8 = false) {
   if (W_bf16 == nullptr || packed_out == nullptr || scales_out == nullptr)
     return W4A16_ERR_INVALID_ARG;
   if (N < 1 || K < 1) return W4A16_ERR_INVALID_ARG;
@@ -563,8 +615,10 @@ int quantize_impl(const void* W_bf16, int64_t N, int64_t K, int group, const uin
   if (!device_info(dev)) return W4A16_ERR_CUDA;
   const cudaError_t e =
       launch_rtn_quantize(W_bf16, N, K, packed_out, scales_out, dev.num_sms, dev.error_word,
-                          g_timeout_ns.load(), static_cast<cudaStream_t>(stream), sr_seed);
-  if (e != cudaSuccess) return cuda_failure(e, sr_seed ? "rtn_quantize (stochastic)" : "rtn_quantize");
+                          g_timeout_ns.load(), static_cast<cudaStream_t>(stream), sr_seed, int8);
+  if (e != cudaSuccess)
+    return cuda_failure(e, int8 ? "rtn_quantize (int8)"
+                                : sr_seed ? "rtn_quantize (stochastic)" : "rtn_quantize");
   g_launches.fetch_add(1);
   return W4A16_OK;
 }
@@ -578,6 +632,63 @@ int w4a16_quantize(const void* W_bf16, int64_t N, int64_t K, int group, void* pa
 int w4a16_quantize_sr(const void* W_bf16, int64_t N, int64_t K, int group, uint64_t seed,
                       void* packed_out, void* scales_out, void* stream) {
   return quantize_impl(W_bf16, N, K, group, &seed, packed_out, scales_out, stream);
+}
+
+// ------------------------------------------------------- INT8 (W8A16)
+size_t w8a16_packed_bytes(int64_t N, int64_t K) {
+  if (N < 1 || K < 1) return 0;
+  return static_cast<size_t>((N + kTileW - 1) / kTileW) * kTileW * static_cast<size_t>(K);
+}
+
+int w8a16_quantize(const void* W_bf16, int64_t N, int64_t K, int group, void* packed_out,
+                   void* scales_out, void* stream) {
+  return quantize_impl(W_bf16, N, K, group, nullptr, packed_out, scales_out, stream, true);
+}
+
+size_t w8a16_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  const int id = select_variant8(M, N, K);
+  return id < 0 ? 0 : variant8_ws(id, M, N, K);
+}
+
+int w8a16_gemm(const void* A_bf16, int64_t M, int64_t N, int64_t K, const void* packed,
+               const void* scales, int group, const void* bias_bf16_or_null, void* Y_bf16,
+               void* workspace, size_t workspace_bytes, void* stream) {
+  const int st = check_gemm_args(A_bf16, M, N, K, packed, scales, group, bias_bf16_or_null, Y_bf16);
+  if (st != W4A16_OK) return st;
+  const int id = select_variant8(M, N, K);
+  if (id < 0) return W4A16_ERR_NO_VARIANT;
+  return run_gemm_v(kVariants8[id], A_bf16, M, N, K, packed, scales, bias_bf16_or_null, Y_bf16,
+                    workspace, workspace_bytes, static_cast<cudaStream_t>(stream), false);
+}
+
+int w8a16_variant_count(void) { return kNumVariants8; }
+
+const char* w8a16_variant_name(int variant) {
+  if (variant < 0 || variant >= kNumVariants8) return nullptr;
+  return kVariants8[variant].name;
+}
+
+int w8a16_variant_eligible(int variant, int64_t M, int64_t N, int64_t K) {
+  return variant8_eligible(variant, M, N, K) ? 1 : 0;
+}
+
+size_t w8a16_variant_workspace_bytes(int variant, int64_t M, int64_t N, int64_t K) {
+  if (!variant8_eligible(variant, M, N, K)) return 0;
+  return variant8_ws(variant, M, N, K);
+}
+
+int w8a16_select_variant(int64_t M, int64_t N, int64_t K) { return select_variant8(M, N, K); }
+
+int w8a16_gemm_variant(int variant, const void* A_bf16, int64_t M, int64_t N, int64_t K,
+                       const void* packed, const void* scales, int group,
+                       const void* bias_bf16_or_null, void* Y_bf16, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  const int st = check_gemm_args(A_bf16, M, N, K, packed, scales, group, bias_bf16_or_null, Y_bf16);
+  if (st != W4A16_OK) return st;
+  if (variant < 0 || variant >= kNumVariants8) return W4A16_ERR_UNSUPPORTED;
+  if (!variant8_eligible(variant, M, N, K)) return W4A16_ERR_NO_VARIANT;
+  return run_gemm_v(kVariants8[variant], A_bf16, M, N, K, packed, scales, bias_bf16_or_null,
+                    Y_bf16, workspace, workspace_bytes, static_cast<cudaStream_t>(stream), false);
 }
 
 size_t w4a16_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {

@@ -110,7 +110,9 @@ static __device__ unsigned long long* g_trace_units = nullptr;
 namespace {
 
 constexpr int kUnitK = 128;                    // K values per unit (one group)
-constexpr int kWBytes = kTileW * kUnitK / 2;   // packed codes per unit: 8 KiB
+// code bytes of one group of a tile: 8 KiB (INT4) or 16 KiB (INT8)
+template <int WB>
+constexpr int w_group_bytes() { return kTileW * kUnitK * WB / 8; }
 constexpr int kSBytes = kTileW * 2;            // scales per unit: 256 B
 constexpr int kMaxAStages = 6;                 // weight-operand stages in TMEM (at most)
 constexpr int kAStageCols = kUnitK / 2;        // 64 TMEM columns per stage
@@ -351,6 +353,34 @@ __device__ __forceinline__ void codes_to_operand(uint32_t w, uint32_t* out) {
   out[3] = x2_fma<F16>(ptx::and_xor(ptx::prmt(w, v, 0x0703), 0x000F000Fu, magic), one, off);
 }
 
+// Four 8-bit codes (one word, code k in byte k, two's complement) to two
+// words of bf16 pairs (k0, k1), (k2, k3), exact: with q = 16 hi + lo (hi the
+// signed high nibble, lo the unsigned low nibble), one byte permute puts each
+// nibble under the exponent byte 0x43 (bf16 128 + nibble; the high nibble in
+// offset binary: 136 + hi), then t = 16 X_hi - 2304 = 16 hi - 128 and q =
+// X_lo + t, both exact (every value is a small integer).
+__device__ __forceinline__ void bytes_to_operand_bf16(uint32_t w, uint32_t* out) {
+  const uint32_t lo = w & 0x0F0F0F0Fu;
+  const uint32_t hi = ((w >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;
+  constexpr uint32_t kExp = 0x43434343u;
+  constexpr uint32_t k16 = 0x41804180u;        // (16, 16)
+  constexpr uint32_t kOff = 0xC510C510u;       // (-2304, -2304)
+  constexpr uint32_t kOne = 0x3F803F80u;       // (1, 1)
+  const uint32_t xl0 = ptx::prmt(lo, kExp, 0x4140), xl1 = ptx::prmt(lo, kExp, 0x4342);
+  const uint32_t xh0 = ptx::prmt(hi, kExp, 0x4140), xh1 = ptx::prmt(hi, kExp, 0x4342);
+  out[0] = x2_fma<false>(xl0, kOne, x2_fma<false>(xh0, k16, kOff));
+  out[1] = x2_fma<false>(xl1, kOne, x2_fma<false>(xh1, k16, kOff));
+}
+
+// bf16_rn(q * s) for an exact pair of codes (INT8): q * s is exact in fp32
+// (8- and 11-bit significands), then one rounding to bf16.
+__device__ __forceinline__ uint32_t scale_pair_bf16_f32(uint32_t q2, float s) {
+  const float a = __uint_as_float(q2 << 16) * s;
+  const float b = __uint_as_float(q2 & 0xFFFF0000u) * s;
+  const __nv_bfloat162 r = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
 // bf16_rn(q * s) for both halves: q * s_lo is exact (<= 7 significant bits),
 // so fma(q, s_hi, q * s_lo) rounds the exact product once.
 __device__ __forceinline__ uint32_t scale_pair_bf16(uint32_t q, uint32_t s_hi2, uint32_t s_lo2) {
@@ -358,14 +388,15 @@ __device__ __forceinline__ uint32_t scale_pair_bf16(uint32_t q, uint32_t s_hi2, 
   return x2_fma<false>(q, s_hi2, lo);
 }
 
-template <int BA, int L, bool GRP, int STAGES, int UG>
+template <int BA, int L, bool GRP, int STAGES, int UG, int WB = 4>
 struct Cfg {
+  static constexpr int kWB = w_group_bytes<WB>();               // code bytes per group
   // A shared-memory stage holds one unit of UG groups: 2 * UG activation
   // boxes (64 k each), then UG code tiles (8 KiB each), then UG scale rows.
   static constexpr int kActBox = BA * 128;                        // bytes per 64-k box
   static constexpr int kWOff = 2 * UG * kActBox;
-  static constexpr int kSOff = kWOff + UG * kWBytes;
-  static constexpr int kStageRaw = UG * (2 * kActBox + kWBytes + kSBytes);
+  static constexpr int kSOff = kWOff + UG * kWB;
+  static constexpr int kStageRaw = UG * (2 * kActBox + kWB + kSBytes);
   static constexpr int kStage = (kStageRaw + 1023) / 1024 * 1024;
   static constexpr int kThreads = 32 * kWarps;                    // 16 warps: <= 128 registers
   static constexpr int kSL = STAGES / L;                          // shared-memory stages per lane
@@ -391,6 +422,7 @@ struct Cfg {
   static_assert(BA % 16 == 0 && BA >= 16 && BA <= 256, "tcgen05 N for M=128");
   static_assert(L == 1 || L == 2, "lanes");
   static_assert(UG == 1 || UG == 2, "groups per unit (TMA boxes of up to 256 rows)");
+  static_assert(WB == 4 || WB == 8, "INT4 or INT8 codes");
   static_assert(kAS % L == 0 && kAS <= kMaxAStages, "TMEM weight stages split over the lanes");
   static_assert(STAGES % L == 0 && STAGES <= 16, "stages split over the lanes");
   static_assert(kDB >= 1 && kDL >= 1 && (!GRP || kDB % L == 0), "accumulators split over the lanes");
@@ -542,9 +574,10 @@ __device__ bool split_fixup(const Args& a, const Unit& u, const SplitInfo& si, S
   return true;
 }
 
-template <int BA, int L, bool GRP, int STAGES, int UG, bool F16, int G>
-__global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG>::kThreads, 1)
+template <int BA, int L, bool GRP, int STAGES, int UG, int WB, bool F16, int G>
+__global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG, WB>::kThreads, 1)
     w4a16_gemm_tc_kernel(const __grid_constant__ GroupArgs<G> g) {
+  static_assert(WB == 4 || !F16, "INT8 weights with bf16 activations");
   // this CTA's problem and its index in the problem's sub-grid
   int prob = 0;
   if constexpr (G > 1) {
@@ -556,7 +589,7 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG>::kThreads, 1)
   const CUtensorMap* const tm_act = &g.tm[prob][0];
   const CUtensorMap* const tm_w = &g.tm[prob][1];
   const CUtensorMap* const tm_s = &g.tm[prob][2];
-  using C = Cfg<BA, L, GRP, STAGES, UG>;
+  using C = Cfg<BA, L, GRP, STAGES, UG, WB>;
   constexpr int DB = C::kDB;
   constexpr int SL = C::kSL;
   constexpr int AL = C::kAL;
@@ -1060,8 +1093,13 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG>::kThreads, 1)
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const uint32_t wrow0 = ptx::smem_u32(w_tile(0)) + row * 64;
-    const uint32_t swz = (row >> 1) & 3;
+    // a row of a group's codes: 64 B (INT4, 64-byte swizzle: 16-byte chunk c
+    // of row r at c ^ ((r >> 1) & 3)) or 128 B (INT8, 128-byte swizzle:
+    // chunk c at c ^ (r & 7))
+    constexpr int kRowBytes = WB * 16;
+    constexpr int kChunks = kRowBytes / 16;
+    const uint32_t wrow0 = ptx::smem_u32(w_tile(0)) + row * kRowBytes;
+    const uint32_t swz = WB == 4 ? ((row >> 1) & 3) : (row & 7);
     for (int i = wg; i < total; i += 2) {
       int p, j;
       lane_split<L>(i, p, j);
@@ -1079,15 +1117,13 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG>::kThreads, 1)
       if (i == 0 && threadIdx.x == 32 * kDequantWarp0) W4A16_TRACE_POINT(6);
       if (threadIdx.x == 32 * kDequantWarp0) W4A16_TRACE_UNIT(1, i);
       bool ok = true;
-      // the row's 64 B of packed codes of every group of the unit, stored
-      // with the 64-byte swizzle: 16-byte chunk c of row r sits at chunk
-      // position c ^ ((r >> 1) & 3)
-      uint32_t words[UG][16];
+      // the row's codes of every group of the unit
+      uint32_t words[UG][4 * kChunks];
 #pragma unroll
       for (int gi = 0; gi < UG; ++gi) {
-        const uint32_t wrow = wrow0 + stage * C::kStage + gi * kWBytes;
+        const uint32_t wrow = wrow0 + stage * C::kStage + gi * C::kWB;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < kChunks; ++q) {
           const uint4 v = ptx::lds128(wrow + ((q ^ swz) << 4));
           words[gi][4 * q + 0] = v.x;
           words[gi][4 * q + 1] = v.y;
@@ -1110,7 +1146,10 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG>::kThreads, 1)
         ptx::tc_fence_after();
         const uint32_t a_addr = lane_base + as * kAStageCols;
         uint32_t s_hi2 = 0, s_lo2 = 0;
-        if constexpr (!GRP) {
+        float s_w8 = 0.0f;
+        if constexpr (!GRP && WB == 8) {
+          s_w8 = __half2float(s_tile(stage, gi)[row]);
+        } else if constexpr (!GRP) {
           if constexpr (F16) {
             // fp16 operand: fp16_rn(q * s) is one fused multiply-add (q and
             // s are both fp16)
@@ -1131,9 +1170,17 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG>::kThreads, 1)
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           uint32_t opnd[16];
+          if constexpr (WB == 4) {
 #pragma unroll
-          for (int w = 0; w < 4; ++w) codes_to_operand<F16>(words[gi][4 * q + w], &opnd[4 * w]);
-          if constexpr (!GRP) {
+            for (int w = 0; w < 4; ++w) codes_to_operand<F16>(words[gi][4 * q + w], &opnd[4 * w]);
+          } else {
+#pragma unroll
+            for (int w = 0; w < 8; ++w) bytes_to_operand_bf16(words[gi][8 * q + w], &opnd[2 * w]);
+          }
+          if constexpr (!GRP && WB == 8) {
+#pragma unroll
+            for (int c = 0; c < 16; ++c) opnd[c] = scale_pair_bf16_f32(opnd[c], s_w8);
+          } else if constexpr (!GRP) {
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
               if constexpr (F16) {
@@ -1173,10 +1220,10 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG>::kThreads, 1)
   if (threadIdx.x == 32) W4A16_TRACE_POINT(11);
 }
 
-template <int BA, int L, bool GRP, int STAGES, int UG, bool F16, int G>
+template <int BA, int L, bool GRP, int STAGES, int UG, int WB, bool F16, int G>
 cudaError_t launch_instance(const GemmGroup& grp, bool use_pdl, cudaStream_t stream) {
-  using C = Cfg<BA, L, GRP, STAGES, UG>;
-  auto kernel = w4a16_gemm_tc_kernel<BA, L, GRP, STAGES, UG, F16, G>;
+  using C = Cfg<BA, L, GRP, STAGES, UG, WB>;
+  auto kernel = w4a16_gemm_tc_kernel<BA, L, GRP, STAGES, UG, WB, F16, G>;
   if (grp.count < 1 || grp.count > G) return cudaErrorInvalidValue;
 
   int dev = 0;
@@ -1210,12 +1257,16 @@ cudaError_t launch_instance(const GemmGroup& grp, bool use_pdl, cudaStream_t str
                          CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     }
-    // tiled code storage viewed as rows of 64 bytes: tile (tn, g) is rows
-    // (tn * K/128 + g) * 128 .. + 127; a unit's UG tiles are one box
+    // tiled code storage viewed as rows of 64 bytes (INT4) or 128 bytes
+    // (INT8): tile (tn, g) is rows (tn * K/128 + g) * 128 .. + 127; a unit's
+    // UG tiles are one box
     const uint64_t w_rows =
         static_cast<uint64_t>((p.N + kTileW - 1) / kTileW) * (p.K / kUnitK) * kTileW;
-    if (encode_tmap_2d(&g.tm[i][1], CU_TENSOR_MAP_DATA_TYPE_UINT8, p.packed, 64, w_rows, 64, 64,
-                       kTileW * UG, CU_TENSOR_MAP_SWIZZLE_64B) != CUDA_SUCCESS)
+    constexpr uint32_t kRowBytes = WB * 16;
+    if (encode_tmap_2d(&g.tm[i][1], CU_TENSOR_MAP_DATA_TYPE_UINT8, p.packed, kRowBytes, w_rows,
+                       kRowBytes, kRowBytes, kTileW * UG,
+                       WB == 4 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B) !=
+        CUDA_SUCCESS)
       return cudaErrorInvalidValue;
     if (encode_tmap_2d(&g.tm[i][2], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.scales, p.N, p.K / kGroup,
                        p.N * 2, kTileW, UG, CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
@@ -1276,14 +1327,34 @@ cudaError_t launch_instance(const GemmGroup& grp, bool use_pdl, cudaStream_t str
   X(32, 2, false, 6, 2)         \
   X(64, 2, false, 4, 2)
 
+// INT8 weights (bf16 activations, single problems): {act_tile, lanes,
+// group_scale, stages, unit_groups}.
+#define W8A16_GEMM_INSTANCES(X) \
+  X(16, 2, true, 10, 1)         \
+  X(32, 2, true, 8, 1)          \
+  X(64, 2, false, 6, 1)         \
+  X(128, 1, false, 4, 1)        \
+  X(256, 1, false, 2, 1)
+
+inline cudaError_t launch_gemm_tc_w8_typed(const GemmKernelConfig& c, const GemmGroup& grp,
+                                           bool use_pdl, cudaStream_t stream) {
+#define W8A16_LAUNCH_CASE(BA, L, GRP, ST, UG)                                    \
+  if (c.act_tile == BA && c.lanes == L && c.group_scale == GRP && c.stages == ST && \
+      c.unit_groups == UG && c.weight_bits == 8)                                    \
+    return launch_instance<BA, L, GRP, ST, UG, 8, false, 1>(grp, use_pdl, stream);
+  W8A16_GEMM_INSTANCES(W8A16_LAUNCH_CASE)
+#undef W8A16_LAUNCH_CASE
+  return cudaErrorInvalidConfiguration;
+}
+
 // All compiled configurations of one activation type and group size.
 template <bool F16, int G>
 cudaError_t launch_gemm_tc_typed(const GemmKernelConfig& c, const GemmGroup& grp, bool use_pdl,
                                  cudaStream_t stream) {
 #define W4A16_LAUNCH_CASE(BA, L, GRP, ST, UG)                                    \
   if (c.act_tile == BA && c.lanes == L && c.group_scale == GRP && c.stages == ST && \
-      c.unit_groups == UG)                                                          \
-    return launch_instance<BA, L, GRP, ST, UG, F16, G>(grp, use_pdl, stream);
+      c.unit_groups == UG && c.weight_bits == 4)                                    \
+    return launch_instance<BA, L, GRP, ST, UG, 4, F16, G>(grp, use_pdl, stream);
   W4A16_GEMM_INSTANCES(W4A16_LAUNCH_CASE)
 #undef W4A16_LAUNCH_CASE
   return cudaErrorInvalidConfiguration;

@@ -12,11 +12,13 @@ namespace w4a16 {
 constexpr int kGroup = 128;     // quantization group along K
 constexpr int kTileW = 128;     // weight rows per GEMM tile (tcgen05 M)
 
-// RTN quantize/pack; one launch.  sr_seed non-null: stochastic rounding with
-// that seed (same scales and storage).
+// RTN quantize/pack; one launch.  sr_seed non-null: INT4 stochastic rounding
+// with that seed (same scales and storage).  int8: the INT8 scheme (8-bit
+// codes, 16 KiB tiles).
 cudaError_t launch_rtn_quantize(const void* W, int64_t N, int64_t K, void* packed, void* scales,
                                 int num_sms, uint32_t* error_word, uint64_t timeout_ns,
-                                cudaStream_t stream, const uint64_t* sr_seed = nullptr);
+                                cudaStream_t stream, const uint64_t* sr_seed = nullptr,
+                                bool int8 = false);
 
 // Several weights quantized in one launch (independent problems).
 constexpr int kMaxQuantizeGroup = 8;
@@ -28,7 +30,8 @@ struct QuantizeProblem {
 };
 cudaError_t launch_rtn_quantize_group(const QuantizeProblem* probs, int count, int num_sms,
                                       uint32_t* error_word, uint64_t timeout_ns,
-                                      cudaStream_t stream, const uint64_t* sr_seed = nullptr);
+                                      cudaStream_t stream, const uint64_t* sr_seed = nullptr,
+                                      bool int8 = false);
 
 // One configuration of the tcgen05 GEMM kernel.
 struct GemmKernelConfig {
@@ -40,6 +43,7 @@ struct GemmKernelConfig {
   int stages;        // shared-memory pipeline depth (all lanes together)
   int unit_groups = 1;  // k-groups per pipeline unit (1 or 2): one copy of the
                         // codes, scales and activations per unit
+  int weight_bits = 4;  // 4: INT4 codes (W4A16); 8: INT8 codes (W8A16)
 };
 
 // The schedule of one launch.
@@ -117,6 +121,9 @@ cudaError_t launch_gemm_tc_group_bf16(const GemmKernelConfig& c, const GemmGroup
                                       bool use_pdl, cudaStream_t stream);
 cudaError_t launch_gemm_tc_group_f16(const GemmKernelConfig& c, const GemmGroup& grp,
                                      bool use_pdl, cudaStream_t stream);
+// INT8 weights (gemm_tc_w8.cu): one problem, bf16 activations.
+cudaError_t launch_gemm_tc_w8(const GemmKernelConfig& c, const GemmGroup& grp, bool use_pdl,
+                              cudaStream_t stream);
 
 // Failure-detection self test: one thread waits on an mbarrier nobody
 // arrives at, with a bounded wait; records a timeout in *error_word.

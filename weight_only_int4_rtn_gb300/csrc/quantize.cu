@@ -47,6 +47,14 @@
 // (e div 4 as two 32-bit words, 0, 0), word e mod 4, u = (word >> 8) * 2^-24.
 // Exact hits (r integral) and values outside the range are never perturbed,
 // and the draws do not depend on the launch geometry.
+//
+// INT8 mode (the W8A16 scheme: "Kernel dispatch and Humming quantization in
+// PhyAI", section "Choose precision by layer and hardware").  The same
+// kernel with 8-bit codes: s = fp16_rn(amax / 127.0f) (1 if that is 0), q =
+// clamp(rint_even(fl32(w / s)), -128, 127), one two's-complement byte per
+// code, tiles of 128 rows x 128 K values (16 KiB, 128 B per row).  For a
+// normal scale |w / s| <= 127 (1 + 2^-11) < 127.5, so again no clamp is
+// active and the low byte of the rounded float is the code.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -187,6 +195,41 @@ __device__ __forceinline__ uint32_t codes_stochastic(const float (&x)[8], uint64
   return pack8(y);
 }
 
+// Low bytes of 4 rounded values (float bit patterns) into one word, code i
+// in byte i.
+__device__ __forceinline__ uint32_t pack4_bytes(uint32_t y0, uint32_t y1, uint32_t y2, uint32_t y3) {
+  return ptx::prmt(ptx::prmt(y0, y1, 0x0040), ptx::prmt(y2, y3, 0x0040), 0x5410);
+}
+
+// INT8 codes of 8 values (two words), normal scale: the corrected quotient
+// rounded half to even (|w / s| < 127.5: no clamp is active).
+__device__ __forceinline__ void codes8_corrected(const float (&f)[8], float s, float r,
+                                                 uint32_t& w0, uint32_t& w1) {
+  uint32_t y[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float q1 = __fmul_rn(f[i], r);
+    const float e = fmaf(-q1, s, f[i]);
+    const float q2 = fmaf(e, r, q1);
+    y[i] = __float_as_uint(__fadd_rn(q2, kRoundMagic));
+  }
+  w0 = pack4_bytes(y[0], y[1], y[2], y[3]);
+  w1 = pack4_bytes(y[4], y[5], y[6], y[7]);
+}
+
+// INT8 codes of 8 values, subnormal scale: IEEE quotient, clamp, round.
+__device__ __forceinline__ void codes8_exact(const float (&f)[8], float s, uint32_t& w0,
+                                             uint32_t& w1) {
+  uint32_t y[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float tc = fminf(fmaxf(__fdiv_rn(f[i], s), -128.0f), 127.0f);
+    y[i] = __float_as_uint(__fadd_rn(tc, kRoundMagic));
+  }
+  w0 = pack4_bytes(y[0], y[1], y[2], y[3]);
+  w1 = pack4_bytes(y[4], y[5], y[6], y[7]);
+}
+
 __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -203,9 +246,17 @@ __device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t acc, uint32_t w) {
   return *reinterpret_cast<const uint32_t*>(&m);
 }
 
-template <bool SR>
+// MODE: kModeRtn4 (INT4, round to nearest), kModeSr4 (INT4, stochastic
+// rounding), kModeRtn8 (INT8, round to nearest).
+constexpr int kModeRtn4 = 0;
+constexpr int kModeSr4 = 1;
+constexpr int kModeRtn8 = 2;
+
+template <int MODE>
 __global__ void __launch_bounds__(kQThreads, 1)
     rtn_quantize_kernel(const __grid_constant__ QGroupArgs q, uint32_t* err, uint64_t timeout_ns) {
+  constexpr bool SR = MODE == kModeSr4;
+  constexpr bool W8 = MODE == kModeRtn8;
   // this CTA's weight and its index in that weight's sub-grid
   int prob = 0;
   while (prob + 1 < q.count && static_cast<int>(blockIdx.x) >= q.cta_start[prob + 1]) ++prob;
@@ -303,7 +354,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
     ma = bf16x2_absmax(ma, mb);
     float amax = fmaxf(__uint_as_float(ma << 16), __uint_as_float(ma & 0xFFFF0000u));
     amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-    __half s16 = __float2half_rn(__fdiv_rn(amax, 7.0f));
+    __half s16 = __float2half_rn(__fdiv_rn(amax, W8 ? 127.0f : 7.0f));
     if (__half_as_ushort(s16) == 0) s16 = __ushort_as_half(0x3C00);   // zero rule: 1.0
     const float s = __half2float(s16);
     const float r = __frcp_rn(s);
@@ -311,8 +362,35 @@ __global__ void __launch_bounds__(kQThreads, 1)
     // pass 2: the codes.  The quotient is corrected to fl32(w / s) for every
     // normal scale (no divergence between rows); a subnormal scale takes the
     // IEEE division and the clamp.
-    uint32_t* const dst = packed + ((static_cast<int64_t>(tn) * G + g) * kQRows + row) * 16 + 8 * h;
-    if constexpr (SR) {
+    // this thread's half row of codes: 8 words (INT4) or 16 words (INT8)
+    constexpr int kRowWords = W8 ? 32 : 16;
+    uint32_t* const dst =
+        packed + ((static_cast<int64_t>(tn) * G + g) * kQRows + row) * kRowWords + (kRowWords / 2) * h;
+    if constexpr (W8) {
+      if ((__half_as_ushort(s16) & 0x7C00u) != 0) {
+        // chunks in the rotated order (j + 4 h) mod 8, as in the INT4 path;
+        // chunk c's two words are words 2c, 2c + 1 of the half row, so the
+        // j-th pair of chunks goes to 16-byte store (j + 2 h) mod 4
+        uint32_t words[16];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          float f[8];
+          unpack8(ptx::lds128(chunk_addr(box, row, (j + 4 * h) & 7)), f);
+          codes8_corrected(f, s, r, words[2 * j], words[2 * j + 1]);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          reinterpret_cast<uint4*>(dst)[(i + 2 * h) & 3] =
+              make_uint4(words[4 * i], words[4 * i + 1], words[4 * i + 2], words[4 * i + 3]);
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          float f[8];
+          unpack8(ptx::lds128(chunk_addr(box, row, c)), f);
+          codes8_exact(f, s, dst[2 * c], dst[2 * c + 1]);
+        }
+      }
+    } else if constexpr (SR) {
       // logical offset of this thread's first value: row n, k = 128 g + 64 h
       const uint64_t e_row = static_cast<uint64_t>(tn * kQRows + row) * static_cast<uint64_t>(G) *
                                  kGroup + static_cast<uint64_t>(g * kGroup + 64 * h);
@@ -365,7 +443,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
 
 cudaError_t launch_rtn_quantize_group(const QuantizeProblem* probs, int count, int num_sms,
                                       uint32_t* error_word, uint64_t timeout_ns,
-                                      cudaStream_t stream, const uint64_t* sr_seed) {
+                                      cudaStream_t stream, const uint64_t* sr_seed, bool int8) {
+  if (int8 && sr_seed != nullptr) return cudaErrorInvalidValue;
   static_assert(kQMaxGroup == kMaxQuantizeGroup, "group size of the kernel arguments");
   if (count < 1 || count > kQMaxGroup) return cudaErrorInvalidValue;
   QGroupArgs q{};
@@ -414,15 +493,17 @@ cudaError_t launch_rtn_quantize_group(const QuantizeProblem* probs, int count, i
   q.cta_start[count] = start;
   q.count = count;
   q.seed = sr_seed != nullptr ? *sr_seed : 0;
-  auto kernel = sr_seed != nullptr ? rtn_quantize_kernel<true> : rtn_quantize_kernel<false>;
+  const int mode = int8 ? kModeRtn8 : sr_seed != nullptr ? kModeSr4 : kModeRtn4;
+  auto kernel = mode == kModeRtn8 ? rtn_quantize_kernel<kModeRtn8>
+                : mode == kModeSr4 ? rtn_quantize_kernel<kModeSr4>
+                                   : rtn_quantize_kernel<kModeRtn4>;
 
   constexpr size_t smem = static_cast<size_t>(kQStages) * kQTileBytes + sizeof(QShared) + 1024;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  static bool attr_set[2][64] = {};
+  static bool attr_set[3][64] = {};
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  const int mode = sr_seed != nullptr ? 1 : 0;
   if (!attr_set[mode][dev]) {
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem));
@@ -445,9 +526,9 @@ cudaError_t launch_rtn_quantize_group(const QuantizeProblem* probs, int count, i
 
 cudaError_t launch_rtn_quantize(const void* W, int64_t N, int64_t K, void* packed, void* scales,
                                 int num_sms, uint32_t* error_word, uint64_t timeout_ns,
-                                cudaStream_t stream, const uint64_t* sr_seed) {
+                                cudaStream_t stream, const uint64_t* sr_seed, bool int8) {
   QuantizeProblem p{W, N, K, packed, scales};
-  return launch_rtn_quantize_group(&p, 1, num_sms, error_word, timeout_ns, stream, sr_seed);
+  return launch_rtn_quantize_group(&p, 1, num_sms, error_word, timeout_ns, stream, sr_seed, int8);
 }
 
 }  // namespace w4a16
