@@ -52,12 +52,18 @@ METRIC = "W4A16 GEMM TFLOPS & weight-stream GB/s vs roofline (M=1..8192), 1×GB3
 
 
 # ----------------------------------------------------------------- helpers
-def quant_bytes(N, K):
-    return 2.515625 * N * K
+def quant_bytes(N, K, bits=4):
+    """Algorithmic bytes of a quantize: bf16 weight in, codes and fp16 scales out."""
+    return (2.0 + bits / 8 + 2.0 / 128) * N * K
 
 
-def gemm_bytes(M, N, K):
-    return 0.515625 * N * K + 2.0 * M * K
+def weight_bytes(N, K, bits=4):
+    """Codes plus fp16 scales of an [N, K] weight."""
+    return (bits / 8 + 2.0 / 128) * N * K
+
+
+def gemm_bytes(M, N, K, bits=4):
+    return weight_bytes(N, K, bits) + 2.0 * M * K
 
 
 def gemm_flops(M, N, K):
@@ -188,12 +194,39 @@ def run_gpu(args, rank, world):
         # the projections are independent problems: one grouped launch of
         # each kind per step when they fit one launch (the grouped quantize
         # rounds to nearest)
-        args.grouped = len(cases) <= w4.MAX_GROUP and args.sr_seed is None
+        args.grouped = len(cases) <= w4.MAX_GROUP and args.sr_seed is None and args.weights == "int4"
     if args.grouped and len(cases) > w4.MAX_GROUP:
         raise SystemExit(f"--grouped takes at most {w4.MAX_GROUP} projections")
     if args.grouped and args.sr_seed is not None:
         raise SystemExit("--sr-seed quantizes per projection (no --grouped)")
-    qname = "rtn_quantize" if args.sr_seed is None else "sr_quantize"
+    int8 = args.weights == "int8"
+    if int8 and (args.grouped or args.sr_seed is not None or args.act != "bf16"):
+        raise SystemExit("--weights int8: bf16 activations, per projection, round to nearest")
+    bits = 8 if int8 else 4
+    qname = "rtn_quantize_int8" if int8 else "rtn_quantize" if args.sr_seed is None else "sr_quantize"
+    gname = "w8a16_gemm_tc" if int8 else "w4a16_gemm_tc"
+    packed_bytes = w4.lib().w8a16_packed_bytes if int8 else w4.w4a16_packed_bytes
+
+    def quantize_one(s, st):
+        if int8:
+            w4.w8a16_quantize(s["W"], packed=s["packed"], scales=s["scales"], stream=st)
+        else:
+            w4.w4a16_quantize(s["W"], packed=s["packed"], scales=s["scales"], stream=st,
+                              seed=args.sr_seed)
+
+    def gemm_one(A, packed, scales, Y, st, workspace):
+        if int8:
+            w4.w8a16_gemm(A, packed, scales, Y=Y, workspace=workspace, stream=st)
+        else:
+            w4.w4a16_gemm(A, packed, scales, Y=Y, workspace=workspace, stream=st)
+
+    def variant_of(c):
+        if int8:
+            return w4.lib().w8a16_variant_name(w4.lib().w8a16_select_variant(c.M, c.N, c.K)).decode()
+        return w4.w4a16_variant_name(w4.w4a16_select_variant(c.M, c.N, c.K))
+
+    if args.tune and int8:
+        args.tune = False   # the INT8 catalogue is chosen by the cost model
     if args.tune:
         # kernel choice by measurement, once per shape, outside the timed
         # region (later calls of the shape use the memoized choice)
@@ -213,12 +246,13 @@ def run_gpu(args, rank, world):
             Wd = W.to(dev) if r == 0 else sets[0][len(s)]["W"].clone()
             Ad = A.to(dev) if r == 0 else sets[0][len(s)]["A"].clone()
             s.append(dict(W=Wd, A=Ad,
-                          packed=torch.empty(w4.w4a16_packed_bytes(c.N, c.K), dtype=torch.uint8,
+                          packed=torch.empty(packed_bytes(c.N, c.K), dtype=torch.uint8,
                                              device=dev),
                           scales=torch.empty(c.K // 128, c.N, dtype=torch.float16, device=dev),
                           Y=torch.empty(c.M, c.N, dtype=act_dtype, device=dev)))
         sets.append(s)
-    ws_bytes = max(w4.w4a16_gemm_workspace_bytes_max(c.M, c.N, c.K) for c in cases)
+    ws_bytes = max((w4.lib().w8a16_gemm_workspace_bytes(c.M, c.N, c.K) if int8 else
+                    w4.w4a16_gemm_workspace_bytes_max(c.M, c.N, c.K)) for c in cases)
     if args.grouped:
         probs, _, _ = w4._gemm_problems([s["A"] for s in sets[0]], [s["packed"] for s in sets[0]],
                                         [s["scales"] for s in sets[0]], None,
@@ -251,12 +285,11 @@ def run_gpu(args, rank, world):
             s = sets[r % copies][j]
             if evs is not None:
                 evs[2 * j][0].record(st)
-            w4.w4a16_quantize(s["W"], packed=s["packed"], scales=s["scales"], stream=st,
-                              seed=args.sr_seed)
+            quantize_one(s, st)
             if evs is not None:
                 evs[2 * j][1].record(st)
                 evs[2 * j + 1][0].record(st)
-            w4.w4a16_gemm(s["A"], s["packed"], s["scales"], Y=s["Y"], workspace=ws, stream=st)
+            gemm_one(s["A"], s["packed"], s["scales"], s["Y"], st, ws)
             if evs is not None:
                 evs[2 * j + 1][1].record(st)
 
@@ -342,11 +375,9 @@ def run_gpu(args, rank, world):
                                                   outs=[(s["packed"], s["scales"]) for s in sset])
                     elif is_gemm:
                         s = sset[j]
-                        w4.w4a16_gemm(s["A"], s["packed"], s["scales"], Y=s["Y"], workspace=ws)
+                        gemm_one(s["A"], s["packed"], s["scales"], s["Y"], None, ws)
                     else:
-                        s = sset[j]
-                        w4.w4a16_quantize(s["W"], packed=s["packed"], scales=s["scales"],
-                                          seed=args.sr_seed)
+                        quantize_one(sset[j], None)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             gk.replay()
             e0.record(stream)
@@ -387,7 +418,7 @@ def run_gpu(args, rank, world):
 
     elapsed_ms, e2e_ms = max_over_ranks([elapsed_ms, e2e_ms], world, dev)
 
-    bytes_step = sum(quant_bytes(c.N, c.K) + gemm_bytes(c.M, c.N, c.K) for c in cases)
+    bytes_step = sum(quant_bytes(c.N, c.K, bits) + gemm_bytes(c.M, c.N, c.K, bits) for c in cases)
     flops_step = sum(gemm_flops(c.M, c.N, c.K) for c in cases)
     ms_step = elapsed_ms / args.steps
     value = job_rate(bytes_step, args.steps, elapsed_ms, world) / 1e9
@@ -397,8 +428,8 @@ def run_gpu(args, rank, world):
     kernels = []
     if args.grouped:
         tq, tg = kern_ms[0], kern_ms[1]
-        qb = sum(quant_bytes(c.N, c.K) for c in cases)
-        gb = sum(gemm_bytes(c.M, c.N, c.K) for c in cases)
+        qb = sum(quant_bytes(c.N, c.K, bits) for c in cases)
+        gb = sum(gemm_bytes(c.M, c.N, c.K, bits) for c in cases)
         kernels.append(dict(kernel="rtn_quantize", grouped=len(cases), us=round(tq * 1e3, 3),
                             gbs=round(qb / (tq * 1e-3) / 1e9, 1)))
         kernels.append(dict(kernel="w4a16_gemm_tc", grouped=len(cases), us=round(tg * 1e3, 3),
@@ -407,35 +438,72 @@ def run_gpu(args, rank, world):
     for j, c in enumerate([] if args.grouped else cases):
         tq, tg = kern_ms[2 * j], kern_ms[2 * j + 1]
         kernels.append(dict(kernel=qname, shape=[c.N, c.K], us=round(tq * 1e3, 3),
-                            gbs=round(quant_bytes(c.N, c.K) / (tq * 1e-3) / 1e9, 1)))
-        kernels.append(dict(kernel="w4a16_gemm_tc", shape=[c.M, c.N, c.K], us=round(tg * 1e3, 3),
-                            variant=w4.w4a16_variant_name(w4.w4a16_select_variant(c.M, c.N, c.K)),
+                            gbs=round(quant_bytes(c.N, c.K, bits) / (tq * 1e-3) / 1e9, 1)))
+        kernels.append(dict(kernel=gname, shape=[c.M, c.N, c.K], us=round(tg * 1e3, 3),
+                            variant=variant_of(c),
                             tflops=round(gemm_flops(c.M, c.N, c.K) / (tg * 1e-3) / 1e12, 2),
-                            weight_gbs=round(0.515625 * c.N * c.K / (tg * 1e-3) / 1e9, 1),
-                            gbs=round(gemm_bytes(c.M, c.N, c.K) / (tg * 1e-3) / 1e9, 1)))
+                            weight_gbs=round(weight_bytes(c.N, c.K, bits) / (tg * 1e-3) / 1e9, 1),
+                            gbs=round(gemm_bytes(c.M, c.N, c.K, bits) / (tg * 1e-3) / 1e9, 1)))
     # dominant kernel: the kind with the larger share of kernel time
     t_q = sum(kern_ms[0::2])
     t_g = sum(kern_ms[1::2])
     launches_kind = 1 if args.grouped else len(cases)
     if t_q >= t_g:
-        dom, dom_bytes = qname, sum(quant_bytes(c.N, c.K) for c in cases)
+        dom, dom_bytes = qname, sum(quant_bytes(c.N, c.K, bits) for c in cases)
         dom_ms, launches_dom = t_q, launches_kind
         bound, achieved, peak, unit = "hbm", None, peaks["hbm_gbs"], "GB/s"
         achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
     else:
         dom_ms, launches_dom = t_g, launches_kind
-        big = max(cases, key=lambda c: gemm_flops(c.M, c.N, c.K) / max(gemm_bytes(c.M, c.N, c.K), 1))
-        ai = gemm_flops(big.M, big.N, big.K) / gemm_bytes(big.M, big.N, big.K)
+        big = max(cases, key=lambda c: gemm_flops(c.M, c.N, c.K) / max(gemm_bytes(c.M, c.N, c.K, bits), 1))
+        ai = gemm_flops(big.M, big.N, big.K) / gemm_bytes(big.M, big.N, big.K, bits)
         tensor_bound = ai > peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
-        dom = "w4a16_gemm_tc"
+        dom = gname
         if tensor_bound:
             bound, peak, unit = "tensor", peaks["bf16_tflops"], "TFLOP/s"
             achieved = sum(gemm_flops(c.M, c.N, c.K) for c in cases) / (dom_ms * 1e-3) / 1e12
         else:
             bound, peak, unit = "hbm", peaks["hbm_gbs"], "GB/s"
-            achieved = sum(gemm_bytes(c.M, c.N, c.K) for c in cases) / (dom_ms * 1e-3) / 1e9
+            achieved = sum(gemm_bytes(c.M, c.N, c.K, bits) for c in cases) / (dom_ms * 1e-3) / 1e9
     traffic = dram_traffic(dom, args.workload + ("_grouped" if args.grouped else "") +
                            ("_sr" if args.sr_seed is not None else ""))
+
+    # --- each GEMM shape alone: a CUDA graph of back-to-back launches on
+    # weight copies rotating through more than 3x L2 (launch overhead
+    # amortised, no quantize in between), against the roofline of the shape
+    b2b = []
+    for c in {(c.M, c.N, c.K): c for c in cases}.values():
+        s0 = sets[0][cases.index(c)]
+        nb = packed_bytes(c.N, c.K) + 2 * c.N * c.K // 128
+        ncp = max(1, min(16, -(-3 * L2_BYTES // nb)))
+        cps = [(s0["packed"], s0["scales"])] + [(s0["packed"].clone(), s0["scales"].clone())
+                                                for _ in range(ncp - 1)]
+        reps = max(8, 2 * ncp)
+        gb = torch.cuda.CUDAGraph()
+        cs = torch.cuda.Stream(dev)
+        cs.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(cs):
+            with torch.cuda.graph(gb, stream=cs):
+                for r in range(reps):
+                    gemm_one(s0["A"], cps[r % ncp][0], cps[r % ncp][1], s0["Y"], cs, ws)
+        torch.cuda.current_stream(dev).wait_stream(cs)
+        gb.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        gb.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        us = e0.elapsed_time(e1) / reps * 1e3
+        t_hbm = gemm_bytes(c.M, c.N, c.K, bits) / (peaks["hbm_gbs"] * 1e9) * 1e6
+        t_tc = gemm_flops(c.M, c.N, c.K) / (peaks["bf16_tflops"] * 1e12) * 1e6
+        b2b.append(dict(shape=[c.M, c.N, c.K], variant=variant_of(c), us=round(us, 3),
+                        weight_gbs=round(weight_bytes(c.N, c.K, bits) / (us * 1e-6) / 1e9, 1),
+                        tflops=round(gemm_flops(c.M, c.N, c.K) / (us * 1e-6) / 1e12, 2),
+                        bound="hbm" if t_hbm >= t_tc else "tensor",
+                        roofline_frac=round(max(t_hbm, t_tc) / us, 4), weight_copies=ncp))
+        del cps, gb
+    if w4.w4a16_get_device_error() != w4.W4A16_OK:
+        raise RuntimeError("device error during the back-to-back GEMM timing")
     roofline = dict(bound=bound, achieved=round(achieved, 2), peak=peak, unit=unit,
                     frac=round(achieved / peak, 4),
                     traffic=None if traffic is None else traffic,
@@ -444,10 +512,11 @@ def run_gpu(args, rank, world):
     out = dict(metric=METRIC, value=round(value, 2), unit="GB/s", n_gpus=world, steps=args.steps,
                warmup=args.warmup, ms_per_step=round(ms_step, 5), higher_is_better=True,
                scaling="weak", vs_baseline=None, dtype=args.act, data="synthetic",
-               config=dict(workload=args.workload, activations=args.act,
+               config=dict(workload=args.workload, activations=args.act, weights=args.weights,
                            shapes=[[c.M, c.N, c.K] for c in cases],
                            step=("one grouped rtn_quantize launch over all projections + one grouped "
                                  "w4a16_gemm launch" if args.grouped else
+                                 "INT8 rtn_quantize + w8a16_gemm per projection" if int8 else
                                  "rtn_quantize + w4a16_gemm per projection" if args.sr_seed is None
                                  else "stochastic-rounding quantize (seed %d) + w4a16_gemm per "
                                  "projection" % args.sr_seed),
@@ -457,6 +526,7 @@ def run_gpu(args, rank, world):
                            parallelism=f"replicas x{world}"),
                gemm=dict(tflops=round(job_rate(flops_step, args.steps, elapsed_ms, world) / 1e12, 3)),
                kernels=kernels, roofline=roofline, clocks=clk.summary(),
+               gemm_back_to_back=b2b,
                gpu_launches=int(launches),
                e2e=dict(value=round(e2e_value, 2), unit="GB/s", h2d_bytes_per_step=int(h2d),
                         d2h_bytes_per_step=int(d2h)))
@@ -464,7 +534,7 @@ def run_gpu(args, rank, world):
 
 
 # ------------------------------------------------------------- CPU oracle
-def time_oracle(workload: str, budget_s: float, sr_seed=None):
+def time_oracle(workload: str, budget_s: float, sr_seed=None, weights="int4"):
     """The oracle as it stands, on the host cores, over whole passes of the
     workload (quantize + GEMM per projection; the stochastic-rounding quantize
     when `sr_seed` is given) until `budget_s` is used."""
@@ -485,16 +555,21 @@ def time_oracle(workload: str, budget_s: float, sr_seed=None):
     t0 = time.perf_counter()
     while True:
         for c, (wb, ab), mr in zip(cases, inputs, sample_rows):
-            p, s = oracle.quantize(wb) if sr_seed is None else oracle.quantize_sr(wb, sr_seed)
-            oracle.gemm(ab[:mr], p, s)
-            done_bytes += quant_bytes(c.N, c.K) + gemm_bytes(mr, c.N, c.K)
+            if weights == "int8":
+                p, s = oracle.quantize8(wb)
+                oracle.gemm8(ab[:mr], p, s)
+                done_bytes += quant_bytes(c.N, c.K, 8) + gemm_bytes(mr, c.N, c.K, 8)
+            else:
+                p, s = oracle.quantize(wb) if sr_seed is None else oracle.quantize_sr(wb, sr_seed)
+                oracle.gemm(ab[:mr], p, s)
+                done_bytes += quant_bytes(c.N, c.K) + gemm_bytes(mr, c.N, c.K)
         passes += 1
         if time.perf_counter() - t0 >= budget_s:
             break
     dt = time.perf_counter() - t0
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
     sample = (f"{passes} pass(es) of {workload}: oracle "
-              + ("" if sr_seed is None else "stochastic-rounding ")
+              + ("INT8 " if weights == "int8" else "" if sr_seed is None else "stochastic-rounding ")
               + "quantize + FP32 GEMM per projection"
               + ("" if all(mr == c.M for mr, c in zip(sample_rows, cases)) else
                  ", GEMM on the first 64 rows of A"))
@@ -518,6 +593,8 @@ def main():
                          "workload has at most 8 projections)")
     ap.add_argument("--per-projection", dest="grouped", action="store_false",
                     help="one quantize and one GEMM launch per projection")
+    ap.add_argument("--weights", default="int4", choices=["int4", "int8"],
+                    help="weight scheme: INT4 (W4A16) or INT8 (W8A16)")
     ap.add_argument("--sr-seed", type=int, default=None,
                     help="quantize with seeded stochastic rounding (w4a16_quantize_sr) instead "
                          "of round to nearest")
@@ -537,7 +614,7 @@ def main():
         if rank != 0:
             return 0
         t_budget = max(5.0, min(60.0, args.cpu_budget * (args.steps + args.warmup) / 10))
-        cb = time_oracle(args.workload, t_budget, args.sr_seed)
+        cb = time_oracle(args.workload, t_budget, args.sr_seed, args.weights)
         line = dict(metric=METRIC, value=cb["value"], unit="GB/s", n_gpus=world, steps=args.steps,
                     warmup=args.warmup, ms_per_step=None, higher_is_better=True, scaling="weak",
                     vs_baseline=None, dtype="f32", data="synthetic", impl="reference",
@@ -557,7 +634,7 @@ def main():
     build()
     out = run_gpu(args, rank, world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = time_oracle(args.workload, args.cpu_budget, args.sr_seed)
+        out["cpu_baseline"] = time_oracle(args.workload, args.cpu_budget, args.sr_seed, args.weights)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
