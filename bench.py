@@ -228,10 +228,15 @@ def run_gpu(args, rank, world):
     if args.tune and int8:
         args.tune = False   # the INT8 catalogue is chosen by the cost model
     if args.tune:
-        # kernel choice by measurement, once per shape, outside the timed
-        # region (later calls of the shape use the memoized choice)
-        for c in cases:
-            w4.w4a16_tune(c.M, c.N, c.K)
+        # kernel choice by measurement, once per shape (or per set of shapes
+        # of a grouped launch), outside the timed region; later calls use the
+        # memoized choice
+        if args.grouped:
+            w4.w4a16_tune_grouped([(c.M, c.N, c.K) for c in cases],
+                                  act=torch.float16 if args.act == "f16" else torch.bfloat16)
+        else:
+            for c in cases:
+                w4.w4a16_tune(c.M, c.N, c.K)
 
     # one set of inputs per copy; the copies rotate step by step
     per_copy = sum(2 * c.N * c.K + c.N * c.K // 2 + 2 * c.N * c.K // 128 + 2 * c.M * c.K +

@@ -247,6 +247,19 @@ typedef struct {
 int w4a16_quantize_grouped(const w4a16_quantize_problem* problems, int count, int group,
                            void* stream);
 
+/*
+ * Times every candidate plan of a grouped GEMM of these shapes (each variant
+ * with its per-problem schedules) as CUDA graphs of back-to-back launches on
+ * synthetic operands of the same shapes, and memoizes the fastest: later
+ * grouped launches of these shapes with variant -1 use it ("Kernel dispatch
+ * and Humming quantization in PhyAI", section "Keep selection work out of
+ * repeated inference").  Only the shapes of `problems` are read; the
+ * library allocates its own operands (not capture-safe; synchronizes
+ * `stream`).  *out_variant (may be NULL) receives the chosen variant.
+ */
+int w4a16_tune_grouped(const w4a16_gemm_problem* problems, int count, int act_f16, void* stream,
+                       int* out_variant);
+
 /* Workspace the grouped GEMM needs for these problems (variant = -1: the one
  * the library chooses; else that catalogue entry).  0 if none is needed or
  * the arguments are invalid.  Same zero-once rule as w4a16_gemm. */

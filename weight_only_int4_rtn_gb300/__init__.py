@@ -53,6 +53,8 @@ SIGNATURES = [
     ("w4a16_quantize", ctypes.c_int, [_vp, _c_int64, _c_int64, ctypes.c_int, _vp, _vp, _vp]),
     ("w4a16_quantize_sr", ctypes.c_int,
      [_vp, _c_int64, _c_int64, ctypes.c_int, ctypes.c_uint64, _vp, _vp, _vp]),
+    ("w4a16_tune_grouped", ctypes.c_int,
+     [ctypes.POINTER(GemmProblem), ctypes.c_int, ctypes.c_int, _vp, ctypes.POINTER(ctypes.c_int)]),
     ("w8a16_packed_bytes", _c_size, [_c_int64, _c_int64]),
     ("w8a16_quantize", ctypes.c_int, [_vp, _c_int64, _c_int64, ctypes.c_int, _vp, _vp, _vp]),
     ("w8a16_gemm_workspace_bytes", _c_size, [_c_int64, _c_int64, _c_int64]),
@@ -420,6 +422,28 @@ def _gemm_problems(As, packeds, scales_list, biases, Ys):
                                bias.data_ptr() if bias is not None else None, Y.data_ptr(), M, N, K)
         outs.append(Y)
     return probs, outs, act
+
+
+def w4a16_tune_grouped(shapes, act=torch.bfloat16, stream=None, device=None) -> int:
+    """Choose the grouped-GEMM plan for these ``(M, N, K)`` shapes by
+    measurement and memoize it (later ``w4a16_gemm_grouped`` calls of the
+    same shapes use it).  Returns the chosen variant id."""
+    n = len(shapes)
+    if not 1 <= n <= MAX_GROUP:
+        raise ValueError(f"1 .. {MAX_GROUP} shapes")
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    probs = (GemmProblem * n)()
+    # only the shapes are read; the pointers must still be 16-byte aligned
+    # and non-null for the argument checks
+    dummy = torch.empty(256, dtype=torch.uint8, device=dev)
+    for i, (M, N, K) in enumerate(shapes):
+        probs[i] = GemmProblem(dummy.data_ptr(), dummy.data_ptr(), dummy.data_ptr(), None,
+                               dummy.data_ptr(), M, N, K)
+    out = ctypes.c_int(-1)
+    _check(lib().w4a16_tune_grouped(probs, n, 1 if act == torch.float16 else 0,
+                                    _stream_handle(dev, stream), ctypes.byref(out)),
+           "w4a16_tune_grouped")
+    return out.value
 
 
 def w4a16_gemm_grouped(As, packeds, scales_list, biases=None, Ys=None, workspace=None,

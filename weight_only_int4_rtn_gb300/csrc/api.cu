@@ -221,14 +221,17 @@ constexpr double kHeadUs = 3.71;
 constexpr double kSplitUs = 2.44;
 constexpr double kSplitUsPerCol = 0.051;
 
-double estimate_us(const Variant& v, int64_t M, int64_t N, int64_t K, int num_sms) {
-  const GemmSchedule s = make_schedule(v, M, N, K, num_sms);
+double estimate_sched(const Variant& v, const GemmSchedule& s, int64_t K) {
   const int64_t KB = K / kGroup / v.cfg.unit_groups;
   const int64_t dp_per_cta = (s.dp_tiles + s.grid - 1) / s.grid;
   const int64_t sk_per_cta = (s.sk_units + s.grid - 1) / s.grid;
   double t = kHeadUs + static_cast<double>(dp_per_cta * KB + sk_per_cta) * v.unit_us;
   if (s.sk_units > 0) t += kSplitUs + kSplitUsPerCol * v.cfg.act_tile;
   return t;
+}
+
+double estimate_us(const Variant& v, int64_t M, int64_t N, int64_t K, int num_sms) {
+  return estimate_sched(v, make_schedule(v, M, N, K, num_sms), K);
 }
 
 int rule_variant(int64_t M, int64_t N, int64_t K, int num_sms) {
@@ -401,44 +404,77 @@ struct GroupPlan {
   double est_us = 0.0;
 };
 
-bool plan_for_variant(int id, const w4a16_gemm_problem* pr, int count, int sms, GroupPlan& plan) {
-  const Variant& v = kVariants[id];
-  int64_t units[kMaxGemmGroup];
-  int64_t total = 0;
-  for (int i = 0; i < count; ++i) {
-    if (!variant_eligible(id, pr[i].M, pr[i].N, pr[i].K)) return false;
-    units[i] = gemm_tiles(v.cfg, pr[i].M, pr[i].N) * (pr[i].K / kGroup / v.cfg.unit_groups);
-    total += units[i];
+// The schedule of one problem of a grouped launch on `ctas` CTAs: the
+// variant's own, or (when the variant is not forced) for a stream-K variant
+// whole tiles only when that is estimated faster (every split tile pays the
+// fixup).
+GemmSchedule group_schedule(const Variant& v, const w4a16_gemm_problem& p, int ctas, double& est,
+                            bool own_only) {
+  GemmSchedule s = make_schedule(v, p.M, p.N, p.K, ctas);
+  est = estimate_sched(v, s, p.K);
+  if (!own_only && v.stream_k && s.sk_units > 0) {
+    const int64_t tiles = gemm_tiles(v.cfg, p.M, p.N);
+    GemmSchedule d{};
+    d.grid = static_cast<int>(tiles < ctas ? tiles : ctas);
+    d.dp_tiles = static_cast<int>(tiles);
+    d.sk_units = 0;
+    const double ed = estimate_sched(v, d, p.K);
+    if (ed < est) {
+      s = d;
+      est = ed;
+    }
   }
+  return s;
+}
+
+// CTAs of a grouped launch: a single problem gets every SM (exactly the
+// single-call schedule when the variant is forced); several start with one
+// CTA each and take the rest one at a time, to the problem with the largest
+// estimate while that estimate improves.
+bool plan_for_variant(int id, const w4a16_gemm_problem* pr, int count, int sms, GroupPlan& plan,
+                      bool forced) {
+  const Variant& v = kVariants[id];
+  for (int i = 0; i < count; ++i)
+    if (!variant_eligible(id, pr[i].M, pr[i].N, pr[i].K)) return false;
   if (count > sms) return false;
   int ctas[kMaxGemmGroup];
-  int used = 0;
+  double est[kMaxGemmGroup];
   for (int i = 0; i < count; ++i) {
-    int64_t c = (static_cast<int64_t>(sms) * units[i]) / total;
-    if (c < 1) c = 1;
-    ctas[i] = static_cast<int>(c);
-    used += ctas[i];
+    ctas[i] = count == 1 ? sms : 1;
+    (void)group_schedule(v, pr[i], ctas[i], est[i], forced);
   }
-  while (used > sms) {   // rounding up the small ones may overshoot
-    int big = 0;
-    for (int i = 1; i < count; ++i) big = ctas[i] > ctas[big] ? i : big;
-    --ctas[big];
-    --used;
-  }
-  while (used < sms) {   // spare SMs to the problems with most units per CTA
-    int best = 0;
-    for (int i = 1; i < count; ++i)
-      if (units[i] * ctas[best] > units[best] * ctas[i]) best = i;
-    ++ctas[best];
-    ++used;
+  // units per CTA fall in steps, so a problem may need several more CTAs
+  // before its estimate improves: look ahead to the next improving count
+  int used = count;
+  while (count > 1 && used < sms) {
+    int pick = -1, pick_k = 0;
+    double pick_est = 0.0;
+    for (int i = 0; i < count; ++i) {
+      if (pick >= 0 && est[i] <= est[pick]) continue;
+      for (int k = 1; used + k <= sms; ++k) {
+        double e1;
+        (void)group_schedule(v, pr[i], ctas[i] + k, e1, forced);
+        if (e1 < est[i]) {
+          pick = i;
+          pick_k = k;
+          pick_est = e1;
+          break;
+        }
+      }
+    }
+    if (pick < 0) break;
+    ctas[pick] += pick_k;
+    used += pick_k;
+    est[pick] = pick_est;
   }
   plan.variant = id;
   plan.est_us = 0.0;
   size_t off = 0;
   bool split = false;
   for (int i = 0; i < count; ++i) {
-    plan.s[i] = make_schedule(v, pr[i].M, pr[i].N, pr[i].K, ctas[i]);
-    plan.est_us = std::max(plan.est_us, estimate_us(v, pr[i].M, pr[i].N, pr[i].K, ctas[i]));
+    double e;
+    plan.s[i] = group_schedule(v, pr[i], ctas[i], e, forced);
+    plan.est_us = std::max(plan.est_us, e);
     plan.partial_off[i] = off;
     if (plan.s[i].sk_units > 0) {
       split = true;
@@ -450,23 +486,62 @@ bool plan_for_variant(int id, const w4a16_gemm_problem* pr, int count, int sms, 
   return true;
 }
 
+// Plans are memoized per (variant, problem shapes): the selection work runs
+// once per set of shapes, not on every call.
+struct GroupKey {
+  int variant, count, sms;
+  int64_t mnk[kMaxGemmGroup][3];
+  bool operator<(const GroupKey& o) const {
+    if (sms != o.sms) return sms < o.sms;
+    if (variant != o.variant) return variant < o.variant;
+    if (count != o.count) return count < o.count;
+    for (int i = 0; i < count; ++i)
+      for (int j = 0; j < 3; ++j)
+        if (mnk[i][j] != o.mnk[i][j]) return mnk[i][j] < o.mnk[i][j];
+    return false;
+  }
+};
+std::map<GroupKey, GroupPlan> g_group_plans;
+std::mutex g_group_mutex;
+
 int plan_group(const w4a16_gemm_problem* pr, int count, int variant, GroupPlan& plan) {
   DeviceInfo dev;
   const int sms = std::min(device_info(dev) ? dev.num_sms : kDefaultSms, kMaxGrid);
-  if (variant >= 0) {
-    if (variant >= kNumVariants) return W4A16_ERR_UNSUPPORTED;
-    return plan_for_variant(variant, pr, count, sms, plan) ? W4A16_OK : W4A16_ERR_NO_VARIANT;
+  if (variant >= kNumVariants) return W4A16_ERR_UNSUPPORTED;
+  GroupKey key{};
+  key.variant = variant < 0 ? -1 : variant;
+  key.count = count;
+  key.sms = sms;
+  for (int i = 0; i < count; ++i) {
+    key.mnk[i][0] = pr[i].M;
+    key.mnk[i][1] = pr[i].N;
+    key.mnk[i][2] = pr[i].K;
   }
-  bool found = false;
-  for (int id = 0; id < kNumVariants; ++id) {
-    GroupPlan cand;
-    if (!plan_for_variant(id, pr, count, sms, cand)) continue;
-    if (!found || cand.est_us < plan.est_us) {
-      plan = cand;
-      found = true;
+  {
+    std::lock_guard<std::mutex> lock(g_group_mutex);
+    auto it = g_group_plans.find(key);
+    if (it != g_group_plans.end()) {
+      plan = it->second;
+      return W4A16_OK;
     }
   }
-  return found ? W4A16_OK : W4A16_ERR_NO_VARIANT;
+  bool found = false;
+  if (variant >= 0) {
+    found = plan_for_variant(variant, pr, count, sms, plan, true);
+  } else {
+    for (int id = 0; id < kNumVariants; ++id) {
+      GroupPlan cand;
+      if (!plan_for_variant(id, pr, count, sms, cand, false)) continue;
+      if (!found || cand.est_us < plan.est_us) {
+        plan = cand;
+        found = true;
+      }
+    }
+  }
+  if (!found) return W4A16_ERR_NO_VARIANT;
+  std::lock_guard<std::mutex> lock(g_group_mutex);
+  g_group_plans[key] = plan;
+  return W4A16_OK;
 }
 
 int check_group_args(const w4a16_gemm_problem* pr, int count, int group) {
@@ -744,25 +819,13 @@ size_t w4a16_variant_workspace_bytes(int variant, int64_t M, int64_t N, int64_t 
 
 int w4a16_select_variant(int64_t M, int64_t N, int64_t K) { return select_variant(M, N, K); }
 
-size_t w4a16_gemm_grouped_workspace_bytes(const w4a16_gemm_problem* problems, int count,
-                                          int variant) {
-  if (check_group_args(problems, count, kGroup) != W4A16_OK) return 0;
-  GroupPlan plan;
-  if (plan_group(problems, count, variant, plan) != W4A16_OK) return 0;
-  return plan.ws_bytes;
-}
+}  // extern "C"
 
-int w4a16_gemm_grouped(const w4a16_gemm_problem* problems, int count, int group, int act_f16,
-                       int variant, void* workspace, size_t workspace_bytes, void* stream) {
-  int st = check_group_args(problems, count, group);
-  if (st != W4A16_OK) return st;
-  GroupPlan plan;
-  st = plan_group(problems, count, variant, plan);
-  if (st != W4A16_OK) return st;
-  if (plan.ws_bytes > 0) {
-    if (workspace == nullptr || workspace_bytes < plan.ws_bytes) return W4A16_ERR_WORKSPACE;
-    if (!aligned16(workspace)) return W4A16_ERR_ALIGNMENT;
-  }
+namespace {
+// One launch of a planned group (the caller checked the arguments and the
+// workspace size).
+int launch_group_plan(const GroupPlan& plan, const w4a16_gemm_problem* problems, int count,
+                      int act_f16, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   DeviceInfo dev;
   if (!device_info(dev)) return W4A16_ERR_CUDA;
   const Variant& v = kVariants[plan.variant];
@@ -791,10 +854,190 @@ int w4a16_gemm_grouped(const w4a16_gemm_problem* problems, int count, int group,
   if (log_enabled())
     std::fprintf(stderr, "w4a16: grouped gemm of %d, variant=%s, estimate %.1f us\n", count, v.name,
                  plan.est_us);
-  const cudaError_t e = launch_gemm_tc_group(v.cfg, grp, /*use_pdl=*/true,
-                                             static_cast<cudaStream_t>(stream));
+  const cudaError_t e = launch_gemm_tc_group(v.cfg, grp, /*use_pdl=*/true, stream);
   if (e != cudaSuccess) return cuda_failure(e, v.name);
   g_launches.fetch_add(1);
+  return W4A16_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t w4a16_gemm_grouped_workspace_bytes(const w4a16_gemm_problem* problems, int count,
+                                          int variant) {
+  if (check_group_args(problems, count, kGroup) != W4A16_OK) return 0;
+  GroupPlan plan;
+  if (plan_group(problems, count, variant, plan) != W4A16_OK) return 0;
+  return plan.ws_bytes;
+}
+
+int w4a16_gemm_grouped(const w4a16_gemm_problem* problems, int count, int group, int act_f16,
+                       int variant, void* workspace, size_t workspace_bytes, void* stream) {
+  int st = check_group_args(problems, count, group);
+  if (st != W4A16_OK) return st;
+  GroupPlan plan;
+  st = plan_group(problems, count, variant, plan);
+  if (st != W4A16_OK) return st;
+  if (plan.ws_bytes > 0) {
+    if (workspace == nullptr || workspace_bytes < plan.ws_bytes) return W4A16_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return W4A16_ERR_ALIGNMENT;
+  }
+  return launch_group_plan(plan, problems, count, act_f16, workspace, workspace_bytes,
+                           static_cast<cudaStream_t>(stream));
+}
+
+int w4a16_tune_grouped(const w4a16_gemm_problem* problems, int count, int act_f16, void* stream_v,
+                       int* out_variant) {
+  int st = check_group_args(problems, count, kGroup);
+  if (st != W4A16_OK) return st;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone)
+    return W4A16_ERR_INVALID_ARG;
+  DeviceInfo dev;
+  if (!device_info(dev)) return W4A16_ERR_CUDA;
+  const int sms = std::min(dev.num_sms, kMaxGrid);
+
+  // Synthetic operands of the problems' shapes; enough weight copies that
+  // the timed launches stream them from HBM rather than L2.
+  std::vector<void*> bufs;
+  auto alloc = [&](size_t b) -> void* {
+    void* p = nullptr;
+    if (cudaMalloc(&p, b < 256 ? 256 : b) != cudaSuccess) return nullptr;
+    bufs.push_back(p);
+    return p;
+  };
+  auto release = [&]() {
+    for (void* p : bufs) cudaFree(p);
+    bufs.clear();
+  };
+  size_t per_copy = 0;
+  for (int i = 0; i < count; ++i)
+    per_copy += w4a16_packed_bytes(problems[i].N, problems[i].K) +
+                w4a16_scales_bytes(problems[i].N, problems[i].K, kGroup);
+  int copies = static_cast<int>((512ull << 20) / (per_copy + 1)) + 1;
+  if (copies > 16) copies = 16;
+  std::vector<std::vector<w4a16_gemm_problem>> sets(copies);
+  bool ok = true;
+  for (int c = 0; ok && c < copies; ++c) {
+    sets[c].assign(problems, problems + count);
+    for (int i = 0; ok && i < count; ++i) {
+      w4a16_gemm_problem& q = sets[c][i];
+      const size_t wb = w4a16_packed_bytes(q.N, q.K), sb = w4a16_scales_bytes(q.N, q.K, kGroup);
+      void* w = alloc(wb);
+      void* sc = alloc(sb);
+      void* a = c == 0 ? alloc(static_cast<size_t>(q.M) * q.K * 2) : const_cast<void*>(sets[0][i].A);
+      void* y = c == 0 ? alloc(static_cast<size_t>(q.M) * q.N * 2) : sets[0][i].Y;
+      ok = w && sc && a && y;
+      if (!ok) break;
+      cudaMemsetAsync(w, 0x5A, wb, stream);
+      cudaMemsetAsync(sc, 0x1C, sb, stream);
+      if (c == 0) cudaMemsetAsync(a, 0x3C, static_cast<size_t>(q.M) * q.K * 2, stream);
+      q.packed = w;
+      q.scales = sc;
+      q.A = a;
+      q.Y = y;
+      q.bias_or_null = nullptr;
+    }
+  }
+  // every candidate plan: each variant with its per-problem schedules
+  std::vector<GroupPlan> cands;
+  size_t ws_max = 0;
+  for (int id = 0; ok && id < kNumVariants; ++id) {
+    GroupPlan cand;
+    if (!plan_for_variant(id, problems, count, sms, cand, false)) continue;
+    cands.push_back(cand);
+    ws_max = std::max(ws_max, cand.ws_bytes);
+  }
+  void* ws = ok && ws_max ? alloc(ws_max) : nullptr;
+  if (ok && ws_max) {
+    ok = ws != nullptr;
+    if (ok) cudaMemsetAsync(ws, 0, ws_max, stream);
+  }
+  if (!ok || cands.empty()) {
+    release();
+    return ok ? W4A16_ERR_NO_VARIANT : W4A16_ERR_CUDA;
+  }
+
+  cudaEvent_t e0, e1;
+  cudaEventCreate(&e0);
+  cudaEventCreate(&e1);
+  cudaStream_t cs = nullptr;
+  if (cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess) ok = false;
+  if (ok && cudaStreamSynchronize(stream) != cudaSuccess) ok = false;
+  constexpr int kIters = 20;
+  int best = -1;
+  float best_ms = 0.0f;
+  for (size_t k = 0; ok && k < cands.size(); ++k) {
+    const GroupPlan& pl = cands[k];
+    bool fine = true;
+    for (int it = 0; it < 2 && fine; ++it)
+      fine = launch_group_plan(pl, sets[it % copies].data(), count, act_f16, ws, ws_max, cs) ==
+             W4A16_OK;
+    if (!fine) continue;
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t exec = nullptr;
+    if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+      ok = false;
+      break;
+    }
+    for (int it = 0; it < kIters; ++it)
+      launch_group_plan(pl, sets[it % copies].data(), count, act_f16, ws, ws_max, cs);
+    if (cudaStreamEndCapture(cs, &graph) != cudaSuccess ||
+        cudaGraphInstantiate(&exec, graph, 0) != cudaSuccess) {
+      if (graph) cudaGraphDestroy(graph);
+      ok = false;
+      break;
+    }
+    cudaGraphLaunch(exec, cs);   // warm
+    cudaEventRecord(e0, cs);
+    cudaGraphLaunch(exec, cs);
+    cudaEventRecord(e1, cs);
+    const bool synced = cudaEventSynchronize(e1) == cudaSuccess;
+    cudaGraphExecDestroy(exec);
+    cudaGraphDestroy(graph);
+    if (!synced) {
+      ok = false;
+      break;
+    }
+    float ms = 0.0f;
+    cudaEventElapsedTime(&ms, e0, e1);
+    if (log_enabled())
+      std::fprintf(stderr, "w4a16: tune group of %d %s %.3f us (estimate %.1f)\n", count,
+                   kVariants[pl.variant].name, 1000.0 * ms / kIters, pl.est_us);
+    if (best < 0 || ms < best_ms) {
+      best_ms = ms;
+      best = static_cast<int>(k);
+    }
+  }
+  if (cs) {
+    cudaStreamSynchronize(cs);
+    cudaStreamDestroy(cs);
+  }
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  cudaGetLastError();
+  const int dev_err = w4a16_get_device_error(stream);
+  release();
+  if (!ok) return cuda_failure(cudaErrorUnknown, "w4a16_tune_grouped: graph timing failed");
+  if (dev_err != W4A16_OK) return dev_err;
+  if (best < 0) return W4A16_ERR_NO_VARIANT;
+  // memoize: later automatic grouped launches of these shapes use it
+  GroupKey key{};
+  key.variant = -1;
+  key.count = count;
+  key.sms = sms;
+  for (int i = 0; i < count; ++i) {
+    key.mnk[i][0] = problems[i].M;
+    key.mnk[i][1] = problems[i].N;
+    key.mnk[i][2] = problems[i].K;
+  }
+  {
+    std::lock_guard<std::mutex> lock(g_group_mutex);
+    g_group_plans[key] = cands[best];
+  }
+  if (out_variant) *out_variant = cands[best].variant;
   return W4A16_OK;
 }
 
