@@ -260,6 +260,12 @@ int w4a16_quantize_grouped(const w4a16_quantize_problem* problems, int count, in
 int w4a16_tune_grouped(const w4a16_gemm_problem* problems, int count, int act_f16, void* stream,
                        int* out_variant);
 
+/* Sets the memoized plan of grouped launches of these shapes (variant -1) to
+ * `variant` with its per-problem schedules, as w4a16_tune_grouped would when
+ * it chose that variant (for replaying a tuned choice without timing).  Only
+ * the shapes of `problems` are read. */
+int w4a16_set_grouped_variant(const w4a16_gemm_problem* problems, int count, int variant);
+
 /* Workspace the grouped GEMM needs for these problems (variant = -1: the one
  * the library chooses; else that catalogue entry).  0 if none is needed or
  * the arguments are invalid.  Same zero-once rule as w4a16_gemm. */

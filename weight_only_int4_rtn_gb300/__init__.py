@@ -55,6 +55,7 @@ SIGNATURES = [
      [_vp, _c_int64, _c_int64, ctypes.c_int, ctypes.c_uint64, _vp, _vp, _vp]),
     ("w4a16_tune_grouped", ctypes.c_int,
      [ctypes.POINTER(GemmProblem), ctypes.c_int, ctypes.c_int, _vp, ctypes.POINTER(ctypes.c_int)]),
+    ("w4a16_set_grouped_variant", ctypes.c_int, [ctypes.POINTER(GemmProblem), ctypes.c_int, ctypes.c_int]),
     ("w8a16_packed_bytes", _c_size, [_c_int64, _c_int64]),
     ("w8a16_quantize", ctypes.c_int, [_vp, _c_int64, _c_int64, ctypes.c_int, _vp, _vp, _vp]),
     ("w8a16_gemm_workspace_bytes", _c_size, [_c_int64, _c_int64, _c_int64]),
@@ -444,6 +445,26 @@ def w4a16_tune_grouped(shapes, act=torch.bfloat16, stream=None, device=None) -> 
                                     _stream_handle(dev, stream), ctypes.byref(out)),
            "w4a16_tune_grouped")
     return out.value
+
+
+def _shape_problems(shapes, device):
+    n = len(shapes)
+    if not 1 <= n <= MAX_GROUP:
+        raise ValueError(f"1 .. {MAX_GROUP} shapes")
+    probs = (GemmProblem * n)()
+    dummy = torch.empty(256, dtype=torch.uint8, device=device)
+    for i, (M, N, K) in enumerate(shapes):
+        probs[i] = GemmProblem(dummy.data_ptr(), dummy.data_ptr(), dummy.data_ptr(), None,
+                               dummy.data_ptr(), M, N, K)
+    return probs, dummy
+
+
+def w4a16_set_grouped_variant(shapes, variant: int, device=None) -> None:
+    """Memoize ``variant`` (with its per-problem schedules) as the plan of
+    grouped launches of these ``(M, N, K)`` shapes, as a tuned choice."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    probs, _keep = _shape_problems(shapes, dev)
+    _check(lib().w4a16_set_grouped_variant(probs, len(shapes), variant), "w4a16_set_grouped_variant")
 
 
 def w4a16_gemm_grouped(As, packeds, scales_list, biases=None, Ys=None, workspace=None,

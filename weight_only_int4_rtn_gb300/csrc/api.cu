@@ -1041,6 +1041,28 @@ int w4a16_tune_grouped(const w4a16_gemm_problem* problems, int count, int act_f1
   return W4A16_OK;
 }
 
+int w4a16_set_grouped_variant(const w4a16_gemm_problem* problems, int count, int variant) {
+  int st = check_group_args(problems, count, kGroup);
+  if (st != W4A16_OK) return st;
+  if (variant < 0 || variant >= kNumVariants) return W4A16_ERR_UNSUPPORTED;
+  DeviceInfo dev;
+  const int sms = std::min(device_info(dev) ? dev.num_sms : kDefaultSms, kMaxGrid);
+  GroupPlan plan;
+  if (!plan_for_variant(variant, problems, count, sms, plan, false)) return W4A16_ERR_NO_VARIANT;
+  GroupKey key{};
+  key.variant = -1;
+  key.count = count;
+  key.sms = sms;
+  for (int i = 0; i < count; ++i) {
+    key.mnk[i][0] = problems[i].M;
+    key.mnk[i][1] = problems[i].N;
+    key.mnk[i][2] = problems[i].K;
+  }
+  std::lock_guard<std::mutex> lock(g_group_mutex);
+  g_group_plans[key] = plan;
+  return W4A16_OK;
+}
+
 int w4a16_quantize_grouped(const w4a16_quantize_problem* problems, int count, int group,
                            void* stream) {
   if (problems == nullptr || count < 1) return W4A16_ERR_INVALID_ARG;
