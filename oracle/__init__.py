@@ -1,7 +1,8 @@
 """CPU oracle for W4A16 RTN quantization and GEMM, the seeded
-stochastic-rounding quantize mode and the INT8 weight-only (W8A16) scheme.
-Test infrastructure only: see ``w4a16_oracle``, ``stochastic`` and
-``w8a16_oracle`` for what they compute and which passages they follow."""
+stochastic-rounding quantize mode, the INT8 weight-only (W8A16) scheme and
+the FP4 weight-only schemes (MXFP4, NVFP4).  Test infrastructure only: see
+``w4a16_oracle``, ``stochastic``, ``w8a16_oracle`` and ``fp4_oracle`` for what
+they compute and which passages they follow."""
 
 from .w4a16_oracle import (  # noqa: F401
     GROUP,
@@ -41,4 +42,18 @@ from .w8a16_oracle import (  # noqa: F401
     quantize8_f32,
     tiled8_bytes,
     to_tile_layout8,
+)
+from .fp4_oracle import (  # noqa: F401
+    dequantize_mxfp4,
+    dequantize_nvfp4,
+    e2m1_decode,
+    e2m1_encode,
+    e4m3_decode,
+    e4m3_encode,
+    gemm_fp4,
+    mx_exponent,
+    pack_codes_fp4,
+    quantize_mxfp4_f32,
+    quantize_nvfp4_f32,
+    unpack_codes_fp4,
 )
