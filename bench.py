@@ -52,18 +52,27 @@ METRIC = "W4A16 GEMM TFLOPS & weight-stream GB/s vs roofline (M=1..8192), 1×GB3
 
 
 # ----------------------------------------------------------------- helpers
-def quant_bytes(N, K, bits=4):
-    """Algorithmic bytes of a quantize: bf16 weight in, codes and fp16 scales out."""
-    return (2.0 + bits / 8 + 2.0 / 128) * N * K
+# bytes per weight of the codes and of the scales, per weight format: fp16
+# scales per 128 values (INT4, INT8), one E8M0 byte per 32 (MXFP4), one E4M3
+# byte per 16 (NVFP4)
+FMT_BYTES = {"int4": (0.5, 2.0 / 128), "int8": (1.0, 2.0 / 128),
+             "mxfp4": (0.5, 1.0 / 32), "nvfp4": (0.5, 1.0 / 16)}
 
 
-def weight_bytes(N, K, bits=4):
-    """Codes plus fp16 scales of an [N, K] weight."""
-    return (bits / 8 + 2.0 / 128) * N * K
+def quant_bytes(N, K, fmt="int4"):
+    """Algorithmic bytes of a quantize: bf16 weight in (NVFP4 reads it twice:
+    the tensor absmax pass, then the packing pass), codes and scales out."""
+    reads = 4.0 if fmt == "nvfp4" else 2.0
+    return (reads + sum(FMT_BYTES[fmt])) * N * K
 
 
-def gemm_bytes(M, N, K, bits=4):
-    return weight_bytes(N, K, bits) + 2.0 * M * K
+def weight_bytes(N, K, fmt="int4"):
+    """Codes plus scales of an [N, K] weight."""
+    return sum(FMT_BYTES[fmt]) * N * K
+
+
+def gemm_bytes(M, N, K, fmt="int4"):
+    return weight_bytes(N, K, fmt) + 2.0 * M * K
 
 
 def gemm_flops(M, N, K):
@@ -199,34 +208,51 @@ def run_gpu(args, rank, world):
         raise SystemExit(f"--grouped takes at most {w4.MAX_GROUP} projections")
     if args.grouped and args.sr_seed is not None:
         raise SystemExit("--sr-seed quantizes per projection (no --grouped)")
-    int8 = args.weights == "int8"
-    if int8 and (args.grouped or args.sr_seed is not None or args.act != "bf16"):
-        raise SystemExit("--weights int8: bf16 activations, per projection, round to nearest")
-    bits = 8 if int8 else 4
-    qname = "rtn_quantize_int8" if int8 else "rtn_quantize" if args.sr_seed is None else "sr_quantize"
-    gname = "w8a16_gemm_tc" if int8 else "w4a16_gemm_tc"
+    fmt = args.weights
+    int8 = fmt == "int8"
+    fp4 = fmt in ("mxfp4", "nvfp4")
+    if fmt != "int4" and (args.grouped or args.sr_seed is not None or args.act != "bf16"):
+        raise SystemExit(f"--weights {fmt}: bf16 activations, per projection, round to nearest")
+    qname = {"int4": "rtn_quantize" if args.sr_seed is None else "sr_quantize",
+             "int8": "rtn_quantize_int8", "mxfp4": "quantize_mxfp4", "nvfp4": "quantize_nvfp4"}[fmt]
+    gname = {"int4": "w4a16_gemm_tc", "int8": "w8a16_gemm_tc", "mxfp4": "mxfp4_gemm_tc",
+             "nvfp4": "nvfp4_gemm_tc"}[fmt]
     packed_bytes = w4.lib().w8a16_packed_bytes if int8 else w4.w4a16_packed_bytes
+
+    def scales_like(c):
+        if fp4:
+            return torch.empty(c.K // (32 if fmt == "mxfp4" else 16), c.N, dtype=torch.uint8,
+                               device=dev)
+        return torch.empty(c.K // 128, c.N, dtype=torch.float16, device=dev)
 
     def quantize_one(s, st):
         if int8:
             w4.w8a16_quantize(s["W"], packed=s["packed"], scales=s["scales"], stream=st)
+        elif fp4:
+            w4.fp4a16_quantize(s["W"], fmt, packed=s["packed"], scales=s["scales"],
+                               tensor_scale=s["ts"], stream=st)
         else:
             w4.w4a16_quantize(s["W"], packed=s["packed"], scales=s["scales"], stream=st,
                               seed=args.sr_seed)
 
-    def gemm_one(A, packed, scales, Y, st, workspace):
+    def gemm_one(A, packed, scales, Y, st, workspace, ts=None):
         if int8:
             w4.w8a16_gemm(A, packed, scales, Y=Y, workspace=workspace, stream=st)
+        elif fp4:
+            w4.fp4a16_gemm(A, packed, scales, fmt, tensor_scale=ts, Y=Y, workspace=workspace,
+                           stream=st)
         else:
             w4.w4a16_gemm(A, packed, scales, Y=Y, workspace=workspace, stream=st)
 
     def variant_of(c):
         if int8:
             return w4.lib().w8a16_variant_name(w4.lib().w8a16_select_variant(c.M, c.N, c.K)).decode()
+        if fp4:
+            return w4.fp4a16_variant_name(w4.fp4a16_select_variant(c.M, c.N, c.K))
         return w4.w4a16_variant_name(w4.w4a16_select_variant(c.M, c.N, c.K))
 
-    if args.tune and int8:
-        args.tune = False   # the INT8 catalogue is chosen by the cost model
+    if args.tune and fmt != "int4":
+        args.tune = False   # the INT8 and FP4 catalogues are chosen by the cost model
     shapes = [(c.M, c.N, c.K) for c in cases]
     if args.tune and args.tune_file and os.path.exists(args.tune_file):
         # replay choices an earlier run made by measurement (for profiling:
@@ -267,11 +293,13 @@ def run_gpu(args, rank, world):
             s.append(dict(W=Wd, A=Ad,
                           packed=torch.empty(packed_bytes(c.N, c.K), dtype=torch.uint8,
                                              device=dev),
-                          scales=torch.empty(c.K // 128, c.N, dtype=torch.float16, device=dev),
+                          scales=scales_like(c),
+                          ts=torch.zeros(2, dtype=torch.float32, device=dev),
                           Y=torch.empty(c.M, c.N, dtype=act_dtype, device=dev)))
         sets.append(s)
     ws_bytes = max((w4.lib().w8a16_gemm_workspace_bytes(c.M, c.N, c.K) if int8 else
-                    w4.w4a16_gemm_workspace_bytes_max(c.M, c.N, c.K)) for c in cases)
+                    w4.lib().fp4a16_gemm_workspace_bytes(w4.FP4_FORMATS[fmt], c.M, c.N, c.K) if fp4
+                    else w4.w4a16_gemm_workspace_bytes_max(c.M, c.N, c.K)) for c in cases)
     if args.grouped:
         probs, _, _ = w4._gemm_problems([s["A"] for s in sets[0]], [s["packed"] for s in sets[0]],
                                         [s["scales"] for s in sets[0]], None,
@@ -308,7 +336,7 @@ def run_gpu(args, rank, world):
             if evs is not None:
                 evs[2 * j][1].record(st)
                 evs[2 * j + 1][0].record(st)
-            gemm_one(s["A"], s["packed"], s["scales"], s["Y"], st, ws)
+            gemm_one(s["A"], s["packed"], s["scales"], s["Y"], st, ws, s["ts"])
             if evs is not None:
                 evs[2 * j + 1][1].record(st)
 
@@ -398,7 +426,7 @@ def run_gpu(args, rank, world):
                                                   outs=[(s["packed"], s["scales"]) for s in sset])
                     elif is_gemm:
                         s = sset[j]
-                        gemm_one(s["A"], s["packed"], s["scales"], s["Y"], None, ws)
+                        gemm_one(s["A"], s["packed"], s["scales"], s["Y"], None, ws, s["ts"])
                     else:
                         quantize_one(sset[j], None)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -441,7 +469,7 @@ def run_gpu(args, rank, world):
 
     elapsed_ms, e2e_ms = max_over_ranks([elapsed_ms, e2e_ms], world, dev)
 
-    bytes_step = sum(quant_bytes(c.N, c.K, bits) + gemm_bytes(c.M, c.N, c.K, bits) for c in cases)
+    bytes_step = sum(quant_bytes(c.N, c.K, fmt) + gemm_bytes(c.M, c.N, c.K, fmt) for c in cases)
     flops_step = sum(gemm_flops(c.M, c.N, c.K) for c in cases)
     ms_step = elapsed_ms / args.steps
     value = job_rate(bytes_step, args.steps, elapsed_ms, world) / 1e9
@@ -451,8 +479,8 @@ def run_gpu(args, rank, world):
     kernels = []
     if args.grouped:
         tq, tg = kern_ms[0], kern_ms[1]
-        qb = sum(quant_bytes(c.N, c.K, bits) for c in cases)
-        gb = sum(gemm_bytes(c.M, c.N, c.K, bits) for c in cases)
+        qb = sum(quant_bytes(c.N, c.K, fmt) for c in cases)
+        gb = sum(gemm_bytes(c.M, c.N, c.K, fmt) for c in cases)
         kernels.append(dict(kernel="rtn_quantize", grouped=len(cases), us=round(tq * 1e3, 3),
                             gbs=round(qb / (tq * 1e-3) / 1e9, 1)))
         kernels.append(dict(kernel="w4a16_gemm_tc", grouped=len(cases), us=round(tg * 1e3, 3),
@@ -461,25 +489,25 @@ def run_gpu(args, rank, world):
     for j, c in enumerate([] if args.grouped else cases):
         tq, tg = kern_ms[2 * j], kern_ms[2 * j + 1]
         kernels.append(dict(kernel=qname, shape=[c.N, c.K], us=round(tq * 1e3, 3),
-                            gbs=round(quant_bytes(c.N, c.K, bits) / (tq * 1e-3) / 1e9, 1)))
+                            gbs=round(quant_bytes(c.N, c.K, fmt) / (tq * 1e-3) / 1e9, 1)))
         kernels.append(dict(kernel=gname, shape=[c.M, c.N, c.K], us=round(tg * 1e3, 3),
                             variant=variant_of(c),
                             tflops=round(gemm_flops(c.M, c.N, c.K) / (tg * 1e-3) / 1e12, 2),
-                            weight_gbs=round(weight_bytes(c.N, c.K, bits) / (tg * 1e-3) / 1e9, 1),
-                            gbs=round(gemm_bytes(c.M, c.N, c.K, bits) / (tg * 1e-3) / 1e9, 1)))
+                            weight_gbs=round(weight_bytes(c.N, c.K, fmt) / (tg * 1e-3) / 1e9, 1),
+                            gbs=round(gemm_bytes(c.M, c.N, c.K, fmt) / (tg * 1e-3) / 1e9, 1)))
     # dominant kernel: the kind with the larger share of kernel time
     t_q = sum(kern_ms[0::2])
     t_g = sum(kern_ms[1::2])
     launches_kind = 1 if args.grouped else len(cases)
     if t_q >= t_g:
-        dom, dom_bytes = qname, sum(quant_bytes(c.N, c.K, bits) for c in cases)
+        dom, dom_bytes = qname, sum(quant_bytes(c.N, c.K, fmt) for c in cases)
         dom_ms, launches_dom = t_q, launches_kind
         bound, achieved, peak, unit = "hbm", None, peaks["hbm_gbs"], "GB/s"
         achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
     else:
         dom_ms, launches_dom = t_g, launches_kind
-        big = max(cases, key=lambda c: gemm_flops(c.M, c.N, c.K) / max(gemm_bytes(c.M, c.N, c.K, bits), 1))
-        ai = gemm_flops(big.M, big.N, big.K) / gemm_bytes(big.M, big.N, big.K, bits)
+        big = max(cases, key=lambda c: gemm_flops(c.M, c.N, c.K) / max(gemm_bytes(c.M, c.N, c.K, fmt), 1))
+        ai = gemm_flops(big.M, big.N, big.K) / gemm_bytes(big.M, big.N, big.K, fmt)
         tensor_bound = ai > peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
         dom = gname
         if tensor_bound:
@@ -487,7 +515,7 @@ def run_gpu(args, rank, world):
             achieved = sum(gemm_flops(c.M, c.N, c.K) for c in cases) / (dom_ms * 1e-3) / 1e12
         else:
             bound, peak, unit = "hbm", peaks["hbm_gbs"], "GB/s"
-            achieved = sum(gemm_bytes(c.M, c.N, c.K, bits) for c in cases) / (dom_ms * 1e-3) / 1e9
+            achieved = sum(gemm_bytes(c.M, c.N, c.K, fmt) for c in cases) / (dom_ms * 1e-3) / 1e9
     traffic = dram_traffic(dom, args.workload + ("_grouped" if args.grouped else "") +
                            ("_sr" if args.sr_seed is not None else ""))
 
@@ -497,7 +525,7 @@ def run_gpu(args, rank, world):
     b2b = []
     for c in {(c.M, c.N, c.K): c for c in cases}.values():
         s0 = sets[0][cases.index(c)]
-        nb = packed_bytes(c.N, c.K) + 2 * c.N * c.K // 128
+        nb = packed_bytes(c.N, c.K) + s0["scales"].numel() * s0["scales"].element_size()
         ncp = max(1, min(16, -(-3 * L2_BYTES // nb)))
         cps = [(s0["packed"], s0["scales"])] + [(s0["packed"].clone(), s0["scales"].clone())
                                                 for _ in range(ncp - 1)]
@@ -508,7 +536,7 @@ def run_gpu(args, rank, world):
         with torch.cuda.stream(cs):
             with torch.cuda.graph(gb, stream=cs):
                 for r in range(reps):
-                    gemm_one(s0["A"], cps[r % ncp][0], cps[r % ncp][1], s0["Y"], cs, ws)
+                    gemm_one(s0["A"], cps[r % ncp][0], cps[r % ncp][1], s0["Y"], cs, ws, s0["ts"])
         torch.cuda.current_stream(dev).wait_stream(cs)
         gb.replay()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -517,10 +545,10 @@ def run_gpu(args, rank, world):
         e1.record(stream)
         torch.cuda.synchronize(dev)
         us = e0.elapsed_time(e1) / reps * 1e3
-        t_hbm = gemm_bytes(c.M, c.N, c.K, bits) / (peaks["hbm_gbs"] * 1e9) * 1e6
+        t_hbm = gemm_bytes(c.M, c.N, c.K, fmt) / (peaks["hbm_gbs"] * 1e9) * 1e6
         t_tc = gemm_flops(c.M, c.N, c.K) / (peaks["bf16_tflops"] * 1e12) * 1e6
         b2b.append(dict(shape=[c.M, c.N, c.K], variant=variant_of(c), us=round(us, 3),
-                        weight_gbs=round(weight_bytes(c.N, c.K, bits) / (us * 1e-6) / 1e9, 1),
+                        weight_gbs=round(weight_bytes(c.N, c.K, fmt) / (us * 1e-6) / 1e9, 1),
                         tflops=round(gemm_flops(c.M, c.N, c.K) / (us * 1e-6) / 1e12, 2),
                         bound="hbm" if t_hbm >= t_tc else "tensor",
                         roofline_frac=round(max(t_hbm, t_tc) / us, 4), weight_copies=ncp))
@@ -540,6 +568,7 @@ def run_gpu(args, rank, world):
                            step=("one grouped rtn_quantize launch over all projections + one grouped "
                                  "w4a16_gemm launch" if args.grouped else
                                  "INT8 rtn_quantize + w8a16_gemm per projection" if int8 else
+                                 f"{fmt.upper()} quantize + fp4a16_gemm per projection" if fp4 else
                                  "rtn_quantize + w4a16_gemm per projection" if args.sr_seed is None
                                  else "stochastic-rounding quantize (seed %d) + w4a16_gemm per "
                                  "projection" % args.sr_seed),
@@ -581,18 +610,24 @@ def time_oracle(workload: str, budget_s: float, sr_seed=None, weights="int4"):
             if weights == "int8":
                 p, s = oracle.quantize8(wb)
                 oracle.gemm8(ab[:mr], p, s)
-                done_bytes += quant_bytes(c.N, c.K, 8) + gemm_bytes(mr, c.N, c.K, 8)
+            elif weights == "mxfp4":
+                p, s = oracle.quantize_mxfp4_f32(oracle.bf16_bits_to_f32(wb))
+                oracle.gemm_fp4(ab[:mr], oracle.dequantize_mxfp4(p, s))
+            elif weights == "nvfp4":
+                p, s, g = oracle.quantize_nvfp4_f32(oracle.bf16_bits_to_f32(wb))
+                oracle.gemm_fp4(ab[:mr], oracle.dequantize_nvfp4(p, s, g))
             else:
                 p, s = oracle.quantize(wb) if sr_seed is None else oracle.quantize_sr(wb, sr_seed)
                 oracle.gemm(ab[:mr], p, s)
-                done_bytes += quant_bytes(c.N, c.K) + gemm_bytes(mr, c.N, c.K)
+            done_bytes += quant_bytes(c.N, c.K, weights) + gemm_bytes(mr, c.N, c.K, weights)
         passes += 1
         if time.perf_counter() - t0 >= budget_s:
             break
     dt = time.perf_counter() - t0
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
     sample = (f"{passes} pass(es) of {workload}: oracle "
-              + ("INT8 " if weights == "int8" else "" if sr_seed is None else "stochastic-rounding ")
+              + ({"int8": "INT8 ", "mxfp4": "MXFP4 ", "nvfp4": "NVFP4 "}.get(weights, "")
+                 if weights != "int4" else "" if sr_seed is None else "stochastic-rounding ")
               + "quantize + FP32 GEMM per projection"
               + ("" if all(mr == c.M for mr, c in zip(sample_rows, cases)) else
                  ", GEMM on the first 64 rows of A"))
@@ -616,8 +651,8 @@ def main():
                          "workload has at most 8 projections)")
     ap.add_argument("--per-projection", dest="grouped", action="store_false",
                     help="one quantize and one GEMM launch per projection")
-    ap.add_argument("--weights", default="int4", choices=["int4", "int8"],
-                    help="weight scheme: INT4 (W4A16) or INT8 (W8A16)")
+    ap.add_argument("--weights", default="int4", choices=["int4", "int8", "mxfp4", "nvfp4"],
+                    help="weight scheme: INT4 (W4A16), INT8 (W8A16), MXFP4 or NVFP4 weights")
     ap.add_argument("--sr-seed", type=int, default=None,
                     help="quantize with seeded stochastic rounding (w4a16_quantize_sr) instead "
                          "of round to nearest")

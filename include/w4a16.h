@@ -385,6 +385,80 @@ int w8a16_gemm_variant(int variant, const void* A_bf16, int64_t M, int64_t N, in
                        const void* bias_bf16_or_null, void* Y_bf16, void* workspace,
                        size_t workspace_bytes, void* stream);
 
+/* ------------------------------------------------------------------------
+ * FP4 weight-only schemes (MXFP4, NVFP4) with BF16 activations.  "Kernel
+ * dispatch and Humming quantization in PhyAI", section "Choose precision by
+ * layer and hardware": MXFP4 and NVFP4 are Humming weight schemes.  "Piper
+ * Kernels", section "NVFP4 construction": NVFP4 weights use blocks of 16
+ * values and a global per-tensor scale, applied with the bias in FP32 before
+ * the final output conversion.
+ *
+ * Elements are FP4 E2M1 (sign, 2 exponent bits with bias 1, 1 mantissa bit:
+ * magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6), rounded to nearest with ties to
+ * the even mantissa and saturated at +-6; a value that rounds to 0 is +0.
+ *   MXFP4 (OCP MX v1.0): per row and block of 32 values along K, the E8M0
+ *     scale code E = floor(log2 amax) - 2 + 127 (clamped to [0, 254]; 127
+ *     for an all-zero block); codes e2m1(W / 2^(E - 127)).
+ *   NVFP4: g = fl32(amax(W) / 2688) (1 for an all-zero tensor); per row and
+ *     block of 16, the E4M3 scale code sb = e4m3_rn_sat(fl32(fl32(amax_b /
+ *     6) / g)); codes e2m1(fl32(W / fl32(sb * g))) (0 where that step is 0).
+ * Codes are nibbles in the INT4 tiled layout (w4a16_quantize: byte j of a
+ * row holds k = 2j low, 2j + 1 high; 128 x 128 tiles of 8 KiB); the scale
+ * codes are bytes, scales_out[b * N + n] for block b of row n.  N must be a
+ * multiple of 16 and K of 128.
+ * ---------------------------------------------------------------------- */
+#define FP4A16_MXFP4 1
+#define FP4A16_NVFP4 2
+
+/* Bytes of the packed codes (as w4a16_packed_bytes) and of the scale codes:
+ * (K/32) * N (MXFP4) or (K/16) * N (NVFP4); 0 for an unknown format. */
+size_t fp4a16_packed_bytes(int64_t N, int64_t K);
+size_t fp4a16_scales_bytes(int format, int64_t N, int64_t K);
+
+/*
+ * FP4 quantize/pack of W: [N, K] bf16 (read).  packed_out:
+ * fp4a16_packed_bytes(N, K) bytes; scales_out: fp4a16_scales_bytes bytes
+ * (both written).  NVFP4 also writes tensor_scale_out[0] = g and
+ * tensor_scale_out[1] = amax(W) (device fp32[2], 8-byte aligned; ignored for
+ * MXFP4, may be null there).  Work on `stream`: MXFP4 one kernel; NVFP4 a
+ * memset of tensor_scale_out, an absmax kernel and the quantize kernel.
+ * Errors: W4A16_ERR_UNSUPPORTED (format, K % 128, N % 16),
+ * W4A16_ERR_INVALID_ARG (null pointers), W4A16_ERR_ALIGNMENT.
+ */
+int fp4a16_quantize(int format, const void* W_bf16, int64_t N, int64_t K, void* packed_out,
+                    void* scales_out, float* tensor_scale_out, void* stream);
+
+/* Workspace the FP4 GEMM needs for this shape (0: none). */
+size_t fp4a16_gemm_workspace_bytes(int format, int64_t M, int64_t N, int64_t K);
+
+/*
+ * Y[M, N] = bf16( g * (A[M, K] . D[N, K]^T) + bias[N] ), D[n, k] =
+ * e2m1(code) * block scale (MXFP4: 2^(E - 127); NVFP4: the E4M3 value), the
+ * products rounded to bf16 (exact for MXFP4 block exponents E in [2, 248]
+ * and every NVFP4 scale), accumulated in fp32; g = tensor_scale[0] (NVFP4,
+ * device fp32) or 1 (MXFP4: tensor_scale is ignored); the bias is added in
+ * fp32.  packed, scales, tensor_scale as written by fp4a16_quantize; A, Y,
+ * bias, workspace and errors as w4a16_gemm.  The variant is chosen by the
+ * library's cost model over the FP4 catalogue.
+ */
+int fp4a16_gemm(int format, const void* A_bf16, int64_t M, int64_t N, int64_t K,
+                const void* packed, const void* scales, const float* tensor_scale,
+                const void* bias_bf16_or_null, void* Y_bf16, void* workspace,
+                size_t workspace_bytes, void* stream);
+
+/* The FP4 catalogue (one for both formats): count, names, eligibility,
+ * workspace, the rule's choice (-1: none) and a forced-variant GEMM
+ * (W4A16_ERR_NO_VARIANT when the variant cannot run the shape). */
+int fp4a16_variant_count(void);
+const char* fp4a16_variant_name(int variant);
+int fp4a16_variant_eligible(int variant, int64_t M, int64_t N, int64_t K);
+size_t fp4a16_variant_workspace_bytes(int variant, int64_t M, int64_t N, int64_t K);
+int fp4a16_select_variant(int64_t M, int64_t N, int64_t K);
+int fp4a16_gemm_variant(int variant, int format, const void* A_bf16, int64_t M, int64_t N,
+                        int64_t K, const void* packed, const void* scales,
+                        const float* tensor_scale, const void* bias_bf16_or_null, void* Y_bf16,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

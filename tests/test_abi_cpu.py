@@ -15,7 +15,7 @@ HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(w[48]a16_[a-z0-9_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b((?:w[48]|fp4)a16_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_declares_the_boundary():
@@ -42,6 +42,10 @@ def test_sizes(built_lib):
     assert w4.w4a16_packed_bytes(264, 512) == 384 * 256     # rows padded to whole 128-row tiles
     assert w4.w4a16_scales_bytes(256, 512) == 4 * 256 * 2
     assert w4.w4a16_scales_bytes(256, 512, 64) == 0
+    assert w4.lib().fp4a16_packed_bytes(256, 512) == 256 * 256
+    assert w4.lib().fp4a16_scales_bytes(1, 256, 512) == 16 * 256      # MXFP4: K/32 bytes per row
+    assert w4.lib().fp4a16_scales_bytes(2, 256, 512) == 32 * 256      # NVFP4: K/16 bytes per row
+    assert w4.lib().fp4a16_scales_bytes(3, 256, 512) == 0
 
 
 def test_status_strings(built_lib):

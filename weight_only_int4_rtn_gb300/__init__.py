@@ -69,6 +69,20 @@ SIGNATURES = [
     ("w8a16_gemm_variant", ctypes.c_int,
      [ctypes.c_int, _vp, _c_int64, _c_int64, _c_int64, _vp, _vp, ctypes.c_int, _vp, _vp, _vp,
       _c_size, _vp]),
+    ("fp4a16_packed_bytes", _c_size, [_c_int64, _c_int64]),
+    ("fp4a16_scales_bytes", _c_size, [ctypes.c_int, _c_int64, _c_int64]),
+    ("fp4a16_quantize", ctypes.c_int, [ctypes.c_int, _vp, _c_int64, _c_int64, _vp, _vp, _vp, _vp]),
+    ("fp4a16_gemm_workspace_bytes", _c_size, [ctypes.c_int, _c_int64, _c_int64, _c_int64]),
+    ("fp4a16_gemm", ctypes.c_int,
+     [ctypes.c_int, _vp, _c_int64, _c_int64, _c_int64, _vp, _vp, _vp, _vp, _vp, _vp, _c_size, _vp]),
+    ("fp4a16_variant_count", ctypes.c_int, []),
+    ("fp4a16_variant_name", ctypes.c_char_p, [ctypes.c_int]),
+    ("fp4a16_variant_eligible", ctypes.c_int, [ctypes.c_int, _c_int64, _c_int64, _c_int64]),
+    ("fp4a16_variant_workspace_bytes", _c_size, [ctypes.c_int, _c_int64, _c_int64, _c_int64]),
+    ("fp4a16_select_variant", ctypes.c_int, [_c_int64, _c_int64, _c_int64]),
+    ("fp4a16_gemm_variant", ctypes.c_int,
+     [ctypes.c_int, ctypes.c_int, _vp, _c_int64, _c_int64, _c_int64, _vp, _vp, _vp, _vp, _vp, _vp,
+      _c_size, _vp]),
     ("w4a16_gemm_workspace_bytes", _c_size, [_c_int64, _c_int64, _c_int64]),
     ("w4a16_gemm_workspace_bytes_max", _c_size, [_c_int64, _c_int64, _c_int64]),
     ("w4a16_workspace_init", ctypes.c_int, [_vp, _c_size, _vp]),
@@ -367,6 +381,127 @@ def w8a16_gemm(A: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor,
 
 
 # ----------------------------------------------------------------- groups
+# ------------------------------------------------- FP4 (MXFP4, NVFP4)
+FP4_FORMATS = {"mxfp4": 1, "nvfp4": 2}
+
+
+def _fp4_format(fmt) -> int:
+    if isinstance(fmt, str):
+        if fmt not in FP4_FORMATS:
+            raise ValueError(f"unknown FP4 format {fmt!r}: one of {sorted(FP4_FORMATS)}")
+        return FP4_FORMATS[fmt]
+    if fmt not in FP4_FORMATS.values():
+        raise ValueError(f"unknown FP4 format {fmt!r}")
+    return int(fmt)
+
+
+def fp4a16_quantize(W: torch.Tensor, fmt="mxfp4", packed: torch.Tensor | None = None,
+                    scales: torch.Tensor | None = None, tensor_scale: torch.Tensor | None = None,
+                    stream=None):
+    """FP4 quantize ``W[N, K]`` (bf16, CUDA) as ``fmt`` ("mxfp4" or
+    "nvfp4").  Returns ``(packed, scales, tensor_scale)``: 1-D uint8 tiled
+    E2M1 codes (fp4a16_packed_bytes), uint8 scale codes ``[K/32, N]`` (E8M0)
+    or ``[K/16, N]`` (E4M3), and for NVFP4 a float32 pair ``(g, amax)`` on the
+    device (None for MXFP4)."""
+    f = _fp4_format(fmt)
+    _require_cuda(W, "W", torch.bfloat16)
+    if W.dim() != 2:
+        raise ValueError("W must be [N, K]")
+    N, K = W.shape
+    L = lib()
+    nbytes = L.fp4a16_packed_bytes(N, K)
+    blk = 32 if f == 1 else 16
+    if packed is None:
+        packed = torch.empty(nbytes, dtype=torch.uint8, device=W.device)
+    if scales is None:
+        scales = torch.empty((max(K // blk, 0), N), dtype=torch.uint8, device=W.device)
+    if f == 2 and tensor_scale is None:
+        tensor_scale = torch.empty(2, dtype=torch.float32, device=W.device)
+    _require_cuda(packed, "packed", torch.uint8)
+    _require_cuda(scales, "scales", torch.uint8)
+    if f == 2:
+        _require_cuda(tensor_scale, "tensor_scale", torch.float32)
+        if tensor_scale.numel() != 2:
+            raise ValueError("tensor_scale must hold 2 floats")
+    if packed.numel() != nbytes or scales.numel() != L.fp4a16_scales_bytes(f, N, K):
+        raise ValueError("output buffers have the wrong size")
+    ts_ptr = tensor_scale.data_ptr() if f == 2 else None
+    _check(L.fp4a16_quantize(f, W.data_ptr(), N, K, packed.data_ptr(), scales.data_ptr(), ts_ptr,
+                             _stream_handle(W.device, stream)), "fp4a16_quantize")
+    return packed, scales, (tensor_scale if f == 2 else None)
+
+
+def fp4a16_gemm(A: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor, fmt="mxfp4",
+                tensor_scale: torch.Tensor | None = None, bias: torch.Tensor | None = None,
+                Y: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                stream=None, variant: int | None = None) -> torch.Tensor:
+    """``Y[M, N] = g * (A[M, K] @ D^T) + bias`` (bf16) on the GPU, D the
+    dequantized FP4 weight (E2M1 code times its block scale), g NVFP4's tensor
+    scale (``tensor_scale[0]``); ``variant`` forces one entry of the FP4
+    catalogue."""
+    f = _fp4_format(fmt)
+    _require_cuda(A, "A", torch.bfloat16)
+    _require_cuda(packed, "packed", torch.uint8)
+    _require_cuda(scales, "scales", torch.uint8)
+    if A.dim() != 2 or scales.dim() != 2:
+        raise ValueError("A and scales must be 2-D")
+    M, K = A.shape
+    N = scales.shape[1]
+    if scales.shape[0] * (32 if f == 1 else 16) != K:
+        raise ValueError("scales must be [K/32, N] (mxfp4) or [K/16, N] (nvfp4)")
+    L = lib()
+    if packed.numel() != L.fp4a16_packed_bytes(N, K):
+        raise ValueError("packed must hold fp4a16_packed_bytes(N, K) bytes of tiled codes")
+    if f == 2:
+        if tensor_scale is None:
+            raise ValueError("nvfp4 needs the tensor scale written by fp4a16_quantize")
+        _require_cuda(tensor_scale, "tensor_scale", torch.float32)
+    if bias is not None:
+        _require_cuda(bias, "bias", torch.bfloat16)
+        if bias.numel() != N:
+            raise ValueError("bias must have N elements")
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    _require_cuda(Y, "Y", torch.bfloat16)
+    if Y.shape != (M, N):
+        raise ValueError("Y must be [M, N]")
+    sh = _stream_handle(A.device, stream)
+    need = (L.fp4a16_gemm_workspace_bytes(f, M, N, K) if variant is None
+            else L.fp4a16_variant_workspace_bytes(variant, M, N, K))
+    if workspace is None:
+        workspace = _default_ws.get(A.device, sh, need)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    bias_ptr = bias.data_ptr() if bias is not None else None
+    ts_ptr = tensor_scale.data_ptr() if f == 2 else None
+    if variant is None:
+        st = L.fp4a16_gemm(f, A.data_ptr(), M, N, K, packed.data_ptr(), scales.data_ptr(), ts_ptr,
+                           bias_ptr, Y.data_ptr(), ws_ptr, ws_bytes, sh)
+    else:
+        st = L.fp4a16_gemm_variant(variant, f, A.data_ptr(), M, N, K, packed.data_ptr(),
+                                   scales.data_ptr(), ts_ptr, bias_ptr, Y.data_ptr(), ws_ptr,
+                                   ws_bytes, sh)
+    _check(st, "fp4a16_gemm")
+    return Y
+
+
+def fp4a16_variant_count() -> int:
+    return lib().fp4a16_variant_count()
+
+
+def fp4a16_variant_name(variant: int) -> str | None:
+    n = lib().fp4a16_variant_name(variant)
+    return n.decode() if n is not None else None
+
+
+def fp4a16_variant_eligible(variant: int, M: int, N: int, K: int) -> bool:
+    return bool(lib().fp4a16_variant_eligible(variant, M, N, K))
+
+
+def fp4a16_select_variant(M: int, N: int, K: int) -> int:
+    return lib().fp4a16_select_variant(M, N, K)
+
+
 def w4a16_quantize_grouped(weights, outs=None, stream=None):
     """RTN-quantize several bf16 weights in one launch.  Returns a list of
     ``(packed, scales)`` as ``w4a16_quantize`` would (``outs`` may supply

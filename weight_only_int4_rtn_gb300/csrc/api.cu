@@ -145,6 +145,35 @@ const Variant kVariants8[] = {
 };
 constexpr int kNumVariants8 = static_cast<int>(sizeof(kVariants8) / sizeof(kVariants8[0]));
 
+// FP4 weights (MXFP4 or NVFP4: the format is set per call), bf16
+// activations, dequant mode.
+const Variant kVariantsF4[] = {
+    {"fp4_tc_a16_deq2_sk", {16, 2, false, 16, 1, kFmtMxfp4}, true, 1, 0.48},
+    {"fp4_tc_a16_deq2_dp", {16, 2, false, 16, 1, kFmtMxfp4}, false, 1, 0.45},
+    {"fp4_tc_a32_deq2_sk", {32, 2, false, 12, 1, kFmtMxfp4}, true, 1, 0.48},
+    {"fp4_tc_a64_deq2_sk", {64, 2, false, 8, 1, kFmtMxfp4}, true, 1, 0.50},
+    {"fp4_tc_a64_deq2_dp", {64, 2, false, 8, 1, kFmtMxfp4}, false, 1, 0.47},
+    {"fp4_tc_a128_deq_sk", {128, 1, false, 5, 1, kFmtMxfp4}, true, 1, 0.57},
+    {"fp4_tc_a128_deq_dp", {128, 1, false, 5, 1, kFmtMxfp4}, false, 1, 0.68},
+    {"fp4_tc_a256_deq_sk", {256, 1, false, 3, 1, kFmtMxfp4}, true, 1, 0.63},
+    {"fp4_tc_a256_deq_dp", {256, 1, false, 3, 1, kFmtMxfp4}, false, 1, 0.95},
+    {"fp4_tc_a16_deq2_sk_u2", {16, 2, false, 8, 2, kFmtMxfp4}, true, 1, 0.92},
+    {"fp4_tc_a16_deq2_dp_u2", {16, 2, false, 8, 2, kFmtMxfp4}, false, 1, 0.86},
+};
+constexpr int kNumVariantsF4 = static_cast<int>(sizeof(kVariantsF4) / sizeof(kVariantsF4[0]));
+
+// Public format codes (FP4A16_MXFP4, FP4A16_NVFP4) to the kernels' ones; 0
+// for anything else.
+int fp4_format(int public_format) {
+  return public_format == FP4A16_MXFP4 ? kFmtMxfp4 : public_format == FP4A16_NVFP4 ? kFmtNvfp4 : 0;
+}
+
+Variant variant_f4(int id, int fmt) {
+  Variant v = kVariantsF4[id];
+  v.cfg.weight_format = fmt;
+  return v;
+}
+
 int variant_by_name(const std::string& n) {
   for (int i = 0; i < kNumVariants; ++i)
     if (n == kVariants[i].name) return i;
@@ -209,6 +238,12 @@ bool variant_eligible(int id, int64_t M, int64_t N, int64_t K) {
 
 bool variant8_eligible(int id, int64_t M, int64_t N, int64_t K) {
   return id >= 0 && id < kNumVariants8 && variant_ok(kVariants8[id], M, N, K);
+}
+
+// FP4: the scale rows are N bytes, a TMA stride, so N % 16 == 0.
+bool variantf4_eligible(int id, int64_t M, int64_t N, int64_t K) {
+  return id >= 0 && id < kNumVariantsF4 && N % 16 == 0 &&
+         variant_ok(variant_f4(id, kFmtMxfp4), M, N, K);
 }
 
 // Rule for shapes without a table entry: a cost model fitted to GB300
@@ -322,7 +357,8 @@ int check_gemm_args(const void* A, int64_t M, int64_t N, int64_t K, const void* 
 
 int run_gemm_v(const Variant& v, const void* A, int64_t M, int64_t N, int64_t K,
                const void* packed, const void* scales, const void* bias, void* Y, void* ws,
-               size_t ws_bytes, cudaStream_t stream, bool act_f16) {
+               size_t ws_bytes, cudaStream_t stream, bool act_f16,
+               const float* tensor_scale = nullptr) {
   DeviceInfo dev;
   if (!device_info(dev)) return W4A16_ERR_CUDA;
   const GemmSchedule s = make_schedule(v, M, N, K, dev.num_sms);
@@ -345,6 +381,7 @@ int run_gemm_v(const Variant& v, const void* A, int64_t M, int64_t N, int64_t K,
   p.error_word = dev.error_word;
   p.timeout_ns = g_timeout_ns.load();
   p.act_f16 = act_f16;
+  p.tensor_scale = tensor_scale;
   if (log_enabled())
     std::fprintf(stderr, "w4a16: gemm M=%lld N=%lld K=%lld variant=%s grid=%d dp_tiles=%d sk_units=%lld\n",
                  static_cast<long long>(M), static_cast<long long>(N), static_cast<long long>(K),
@@ -377,6 +414,31 @@ int select_variant8(int64_t M, int64_t N, int64_t K) {
     }
   }
   return best;
+}
+
+// FP4: the rule over the FP4 catalogue.
+int select_variantf4(int64_t M, int64_t N, int64_t K) {
+  DeviceInfo dev;
+  const int sms = device_info(dev) ? dev.num_sms : kDefaultSms;
+  int best = -1;
+  double best_t = 0.0;
+  for (int id = 0; id < kNumVariantsF4; ++id) {
+    if (!variantf4_eligible(id, M, N, K)) continue;
+    const double t = estimate_us(kVariantsF4[id], M, N, K, sms);
+    if (best < 0 || t < best_t) {
+      best = id;
+      best_t = t;
+    }
+  }
+  return best;
+}
+
+size_t variantf4_ws(int id, int64_t M, int64_t N, int64_t K) {
+  DeviceInfo dev;
+  int sms = kDefaultSms;
+  if (device_info(dev)) sms = dev.num_sms;
+  const Variant& v = kVariantsF4[id];
+  return gemm_workspace_bytes(v.cfg, make_schedule(v, M, N, K, sms), M, N, K);
 }
 
 size_t variant8_ws(int id, int64_t M, int64_t N, int64_t K) {
@@ -764,6 +826,107 @@ int w8a16_gemm_variant(int variant, const void* A_bf16, int64_t M, int64_t N, in
   if (!variant8_eligible(variant, M, N, K)) return W4A16_ERR_NO_VARIANT;
   return run_gemm_v(kVariants8[variant], A_bf16, M, N, K, packed, scales, bias_bf16_or_null,
                     Y_bf16, workspace, workspace_bytes, static_cast<cudaStream_t>(stream), false);
+}
+
+// ------------------------------------------- FP4 weights (MXFP4, NVFP4)
+size_t fp4a16_packed_bytes(int64_t N, int64_t K) { return w4a16_packed_bytes(N, K); }
+
+size_t fp4a16_scales_bytes(int format, int64_t N, int64_t K) {
+  const int f = fp4_format(format);
+  if (f == 0 || N < 0 || K < 0 || K % kGroup != 0) return 0;
+  return static_cast<size_t>(K / (f == kFmtMxfp4 ? 32 : 16)) * static_cast<size_t>(N);
+}
+
+int fp4a16_quantize(int format, const void* W_bf16, int64_t N, int64_t K, void* packed_out,
+                    void* scales_out, float* tensor_scale_out, void* stream) {
+  const int f = fp4_format(format);
+  if (f == 0) return W4A16_ERR_UNSUPPORTED;
+  if (W_bf16 == nullptr || packed_out == nullptr || scales_out == nullptr ||
+      (f == kFmtNvfp4 && tensor_scale_out == nullptr))
+    return W4A16_ERR_INVALID_ARG;
+  if (N < 1 || K < 1) return W4A16_ERR_INVALID_ARG;
+  if (K % kGroup != 0 || N % 16 != 0) return W4A16_ERR_UNSUPPORTED;
+  if (N >= (1ll << 31) || K >= (1ll << 31) || N * K >= (1ll << 40)) return W4A16_ERR_UNSUPPORTED;
+  if (!aligned16(W_bf16) || !aligned16(packed_out) || !aligned16(scales_out) ||
+      (tensor_scale_out != nullptr && (reinterpret_cast<uintptr_t>(tensor_scale_out) & 7u) != 0))
+    return W4A16_ERR_ALIGNMENT;
+  DeviceInfo dev;
+  if (!device_info(dev)) return W4A16_ERR_CUDA;
+  const cudaError_t e =
+      launch_fp4_quantize(W_bf16, N, K, packed_out, scales_out, tensor_scale_out, f, dev.num_sms,
+                          dev.error_word, g_timeout_ns.load(), static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_failure(e, f == kFmtMxfp4 ? "quantize (mxfp4)" : "quantize (nvfp4)");
+  g_launches.fetch_add(f == kFmtMxfp4 ? 1 : 2);
+  return W4A16_OK;
+}
+
+namespace {
+int check_fp4_gemm_args(int f, const void* A, int64_t M, int64_t N, int64_t K, const void* packed,
+                        const void* scales, const float* tensor_scale, const void* bias,
+                        void* Y) {
+  if (f == 0) return W4A16_ERR_UNSUPPORTED;
+  if (f == kFmtNvfp4 && tensor_scale == nullptr) return W4A16_ERR_INVALID_ARG;
+  const int st = check_gemm_args(A, M, N, K, packed, scales, kGroup, bias, Y);
+  if (st != W4A16_OK) return st;
+  if (N % 16 != 0) return W4A16_ERR_UNSUPPORTED;
+  if (tensor_scale != nullptr && (reinterpret_cast<uintptr_t>(tensor_scale) & 3u) != 0)
+    return W4A16_ERR_ALIGNMENT;
+  return W4A16_OK;
+}
+}  // namespace
+
+size_t fp4a16_gemm_workspace_bytes(int format, int64_t M, int64_t N, int64_t K) {
+  if (fp4_format(format) == 0) return 0;
+  const int id = select_variantf4(M, N, K);
+  return id < 0 ? 0 : variantf4_ws(id, M, N, K);
+}
+
+int fp4a16_gemm(int format, const void* A_bf16, int64_t M, int64_t N, int64_t K,
+                const void* packed, const void* scales, const float* tensor_scale,
+                const void* bias_bf16_or_null, void* Y_bf16, void* workspace,
+                size_t workspace_bytes, void* stream) {
+  const int f = fp4_format(format);
+  const int st = check_fp4_gemm_args(f, A_bf16, M, N, K, packed, scales, tensor_scale,
+                                     bias_bf16_or_null, Y_bf16);
+  if (st != W4A16_OK) return st;
+  const int id = select_variantf4(M, N, K);
+  if (id < 0) return W4A16_ERR_NO_VARIANT;
+  return run_gemm_v(variant_f4(id, f), A_bf16, M, N, K, packed, scales, bias_bf16_or_null,
+                    Y_bf16, workspace, workspace_bytes, static_cast<cudaStream_t>(stream), false,
+                    f == kFmtNvfp4 ? tensor_scale : nullptr);
+}
+
+int fp4a16_variant_count(void) { return kNumVariantsF4; }
+
+const char* fp4a16_variant_name(int variant) {
+  if (variant < 0 || variant >= kNumVariantsF4) return nullptr;
+  return kVariantsF4[variant].name;
+}
+
+int fp4a16_variant_eligible(int variant, int64_t M, int64_t N, int64_t K) {
+  return variantf4_eligible(variant, M, N, K) ? 1 : 0;
+}
+
+size_t fp4a16_variant_workspace_bytes(int variant, int64_t M, int64_t N, int64_t K) {
+  if (!variantf4_eligible(variant, M, N, K)) return 0;
+  return variantf4_ws(variant, M, N, K);
+}
+
+int fp4a16_select_variant(int64_t M, int64_t N, int64_t K) { return select_variantf4(M, N, K); }
+
+int fp4a16_gemm_variant(int variant, int format, const void* A_bf16, int64_t M, int64_t N,
+                        int64_t K, const void* packed, const void* scales,
+                        const float* tensor_scale, const void* bias_bf16_or_null, void* Y_bf16,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+  const int f = fp4_format(format);
+  const int st = check_fp4_gemm_args(f, A_bf16, M, N, K, packed, scales, tensor_scale,
+                                     bias_bf16_or_null, Y_bf16);
+  if (st != W4A16_OK) return st;
+  if (variant < 0 || variant >= kNumVariantsF4) return W4A16_ERR_UNSUPPORTED;
+  if (!variantf4_eligible(variant, M, N, K)) return W4A16_ERR_NO_VARIANT;
+  return run_gemm_v(variant_f4(variant, f), A_bf16, M, N, K, packed, scales, bias_bf16_or_null,
+                    Y_bf16, workspace, workspace_bytes, static_cast<cudaStream_t>(stream), false,
+                    f == kFmtNvfp4 ? tensor_scale : nullptr);
 }
 
 size_t w4a16_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {

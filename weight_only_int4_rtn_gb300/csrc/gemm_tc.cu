@@ -25,16 +25,25 @@ __global__ void wait_timeout_selftest_kernel(uint32_t* err, uint64_t timeout_ns)
 size_t gemm_smem_bytes(const GemmKernelConfig& c) {
 #define W4A16_SMEM_CASE(BA, L, GRP, ST, UG)                                          \
   if (c.act_tile == BA && c.lanes == L && c.group_scale == GRP && c.stages == ST && \
-      c.unit_groups == UG && c.weight_bits == 4)                                    \
-    return Cfg<BA, L, GRP, ST, UG, 4>::kSmem;
+      c.unit_groups == UG && c.weight_format == kFmtInt4)                                    \
+    return Cfg<BA, L, GRP, ST, UG, kFmtInt4>::kSmem;
   W4A16_GEMM_INSTANCES(W4A16_SMEM_CASE)
 #undef W4A16_SMEM_CASE
 #define W8A16_SMEM_CASE(BA, L, GRP, ST, UG)                                          \
   if (c.act_tile == BA && c.lanes == L && c.group_scale == GRP && c.stages == ST && \
-      c.unit_groups == UG && c.weight_bits == 8)                                    \
-    return Cfg<BA, L, GRP, ST, UG, 8>::kSmem;
+      c.unit_groups == UG && c.weight_format == kFmtInt8)                                    \
+    return Cfg<BA, L, GRP, ST, UG, kFmtInt8>::kSmem;
   W8A16_GEMM_INSTANCES(W8A16_SMEM_CASE)
 #undef W8A16_SMEM_CASE
+#define FP4A16_SMEM_CASE(BA, L, GRP, ST, UG)                                         \
+  if (c.act_tile == BA && c.lanes == L && c.group_scale == GRP && c.stages == ST && \
+      c.unit_groups == UG && c.weight_format == kFmtMxfp4)                          \
+    return Cfg<BA, L, GRP, ST, UG, kFmtMxfp4>::kSmem;                                \
+  if (c.act_tile == BA && c.lanes == L && c.group_scale == GRP && c.stages == ST && \
+      c.unit_groups == UG && c.weight_format == kFmtNvfp4)                          \
+    return Cfg<BA, L, GRP, ST, UG, kFmtNvfp4>::kSmem;
+  FP4A16_GEMM_INSTANCES(FP4A16_SMEM_CASE)
+#undef FP4A16_SMEM_CASE
   return 0;
 }
 
@@ -53,7 +62,9 @@ cudaError_t launch_gemm_tc_group(const GemmKernelConfig& c, const GemmGroup& grp
                                  cudaStream_t stream) {
   static_assert(kMaxGemmGroup == kMaxGroup, "group size of the kernel arguments");
   if (grp.count < 1 || grp.count > kMaxGroup) return cudaErrorInvalidValue;
-  if (c.weight_bits == 8) return launch_gemm_tc_w8(c, grp, use_pdl, stream);
+  if (c.weight_format == kFmtInt8) return launch_gemm_tc_w8(c, grp, use_pdl, stream);
+  if (c.weight_format == kFmtMxfp4) return launch_gemm_tc_mxfp4(c, grp, use_pdl, stream);
+  if (c.weight_format == kFmtNvfp4) return launch_gemm_tc_nvfp4(c, grp, use_pdl, stream);
   const bool f16 = grp.p[0].act_f16;
   if (grp.count == 1)
     return f16 ? launch_gemm_tc_f16(c, grp, use_pdl, stream)

@@ -110,10 +110,16 @@ static __device__ unsigned long long* g_trace_units = nullptr;
 namespace {
 
 constexpr int kUnitK = 128;                    // K values per unit (one group)
-// code bytes of one group of a tile: 8 KiB (INT4) or 16 KiB (INT8)
-template <int WB>
-constexpr int w_group_bytes() { return kTileW * kUnitK * WB / 8; }
-constexpr int kSBytes = kTileW * 2;            // scales per unit: 256 B
+// Weight formats (kernels.h): INT4 or INT8 codes with one fp16 scale per
+// row and group; E2M1 codes (INT4 layout) with one E8M0 byte per 32 values
+// (MXFP4) or one E4M3 byte per 16 values (NVFP4).
+constexpr int wf_bits(int wf) { return wf == kFmtInt8 ? 8 : 4; }
+constexpr bool wf_fp4(int wf) { return wf == kFmtMxfp4 || wf == kFmtNvfp4; }
+constexpr int wf_blocks(int wf) { return wf == kFmtMxfp4 ? 4 : wf == kFmtNvfp4 ? 8 : 1; }
+// code bytes of one group of a tile: 8 KiB (4-bit codes) or 16 KiB (INT8)
+constexpr int w_group_bytes(int wf) { return kTileW * kUnitK * wf_bits(wf) / 8; }
+// scale bytes of one group of a tile: 256 B of fp16, or the block-scale bytes
+constexpr int w_scale_bytes(int wf) { return wf_fp4(wf) ? kTileW * wf_blocks(wf) : kTileW * 2; }
 constexpr int kMaxAStages = 6;                 // weight-operand stages in TMEM (at most)
 constexpr int kAStageCols = kUnitK / 2;        // 64 TMEM columns per stage
 constexpr uint32_t kTmemCols = 512;
@@ -132,6 +138,7 @@ struct Args {
   int sk_units;
   int act_3d;                  // activation map is 3-D: both 64-k halves in one copy
   const __half* scales;        // [K/128, N]; the group-mode readout reads its scales here
+  const float* out_scale;      // NVFP4: the tensor scale g, applied to the fp32 sums
   const uint16_t* bias;        // [N] activation type (bf16 or fp16 bits)
   uint16_t* Y;                 // [M, N] activation type
   float* ws;
@@ -388,15 +395,66 @@ __device__ __forceinline__ uint32_t scale_pair_bf16(uint32_t q, uint32_t s_hi2, 
   return x2_fma<false>(q, s_hi2, lo);
 }
 
-template <int BA, int L, bool GRP, int STAGES, int UG, int WB = 4>
+// FP4 (E2M1) codes to bf16 operand pairs, scaled: eight codes (one word,
+// code k in nibble k; sign bit 3, magnitude index bits 0..2) to four words
+// (k0,k1) .. (k6,k7) of bf16 e2m1(c) * s.  One byte permute looks up
+// m = 2 |e2m1| (0, 1, 2, 3, 4, 6, 8, 12) for four magnitude indices; with the
+// exponent byte 0x43 above it a bf16 holds 128 + m, and one fused
+// multiply-add with h = s / 2 and off = -128 h leaves m h = |e2m1| s,
+// rounded once (exact whenever the product fits bf16).  The sign bits are
+// replicated into place by a sign-extending byte permute: nibble 2 i's sign
+// is the top bit of byte i of w << 4, nibble 2 i + 1's of byte i of w.
+__device__ __forceinline__ void e2m1_to_operand(uint32_t w, uint32_t h2, uint32_t off2,
+                                                uint32_t* out) {
+  constexpr uint32_t kLo = 0x03020100u;     // m for indices 0..3
+  constexpr uint32_t kHi = 0x0C080604u;     // m for indices 4..7
+  constexpr uint32_t kExp = 0x43434343u;
+  const uint32_t sel = w & 0x77777777u;
+  const uint32_t m0 = ptx::prmt(kLo, kHi, sel);          // m of codes 0..3
+  const uint32_t m1 = ptx::prmt(kLo, kHi, sel >> 16);    // m of codes 4..7
+  const uint32_t w4 = w << 4;
+  out[0] = x2_fma<false>(ptx::prmt(m0, kExp, 0x4140), h2, off2) |
+           (ptx::prmt(w4, w, 0xC080) & 0x80008000u);
+  out[1] = x2_fma<false>(ptx::prmt(m0, kExp, 0x4342), h2, off2) |
+           (ptx::prmt(w4, w, 0xD090) & 0x80008000u);
+  out[2] = x2_fma<false>(ptx::prmt(m1, kExp, 0x4140), h2, off2) |
+           (ptx::prmt(w4, w, 0xE0A0) & 0x80008000u);
+  out[3] = x2_fma<false>(ptx::prmt(m1, kExp, 0x4342), h2, off2) |
+           (ptx::prmt(w4, w, 0xF0B0) & 0x80008000u);
+}
+
+// MXFP4 block scale (E8M0 code E: 2^(E - 127)) as the pair h = 2^(E - 128),
+// off = -128 h = -2^(E - 121) in bf16 (both halves).  h is subnormal for
+// E <= 1; off overflows for E > 248 (blocks with |w| >= 2^123, outside the
+// GEMM's range).
+__device__ __forceinline__ void mx_half_scale(uint32_t e, uint32_t& h2, uint32_t& off2) {
+  const uint32_t h = e >= 2u ? (e - 1u) << 7 : 0x40u >> (1u - e);
+  const uint32_t off = 0x8000u | ((e + 6u) << 7);
+  h2 = h | (h << 16);
+  off2 = off | (off << 16);
+}
+
+// NVFP4 block scale (E4M3 code: bias 7, three mantissa bits) as h = s / 2,
+// off = -64 s in bf16; both exact (s has 4 significant bits, 2^-9 <= s <=
+// 448 or s = 0).
+__device__ __forceinline__ void nv_half_scale(uint32_t code, uint32_t& h2, uint32_t& off2) {
+  const float s = __uint_as_float((code & 0x7Fu) << 20) * 0x1p120f;   // exact E4M3 value
+  const __nv_bfloat162 hv = __float2bfloat162_rn(s * 0.5f);
+  const __nv_bfloat162 ov = __float2bfloat162_rn(s * -64.0f);
+  h2 = *reinterpret_cast<const uint32_t*>(&hv);
+  off2 = *reinterpret_cast<const uint32_t*>(&ov);
+}
+
+template <int BA, int L, bool GRP, int STAGES, int UG, int WF = kFmtInt4>
 struct Cfg {
-  static constexpr int kWB = w_group_bytes<WB>();               // code bytes per group
+  static constexpr int kWB = w_group_bytes(WF);                 // code bytes per group
+  static constexpr int kSB = w_scale_bytes(WF);                 // scale bytes per group
   // A shared-memory stage holds one unit of UG groups: 2 * UG activation
   // boxes (64 k each), then UG code tiles (8 KiB each), then UG scale rows.
   static constexpr int kActBox = BA * 128;                        // bytes per 64-k box
   static constexpr int kWOff = 2 * UG * kActBox;
   static constexpr int kSOff = kWOff + UG * kWB;
-  static constexpr int kStageRaw = UG * (2 * kActBox + kWB + kSBytes);
+  static constexpr int kStageRaw = UG * (2 * kActBox + kWB + kSB);
   static constexpr int kStage = (kStageRaw + 1023) / 1024 * 1024;
   static constexpr int kThreads = 32 * kWarps;                    // 16 warps: <= 128 registers
   static constexpr int kSL = STAGES / L;                          // shared-memory stages per lane
@@ -422,7 +480,8 @@ struct Cfg {
   static_assert(BA % 16 == 0 && BA >= 16 && BA <= 256, "tcgen05 N for M=128");
   static_assert(L == 1 || L == 2, "lanes");
   static_assert(UG == 1 || UG == 2, "groups per unit (TMA boxes of up to 256 rows)");
-  static_assert(WB == 4 || WB == 8, "INT4 or INT8 codes");
+  static_assert(WF == kFmtInt4 || WF == kFmtInt8 || wf_fp4(WF), "weight format");
+  static_assert(!wf_fp4(WF) || !GRP, "FP4 weights run in dequant mode (block scales inside a group)");
   static_assert(kAS % L == 0 && kAS <= kMaxAStages, "TMEM weight stages split over the lanes");
   static_assert(STAGES % L == 0 && STAGES <= 16, "stages split over the lanes");
   static_assert(kDB >= 1 && kDL >= 1 && (!GRP || kDB % L == 0), "accumulators split over the lanes");
@@ -574,10 +633,10 @@ __device__ bool split_fixup(const Args& a, const Unit& u, const SplitInfo& si, S
   return true;
 }
 
-template <int BA, int L, bool GRP, int STAGES, int UG, int WB, bool F16, int G>
-__global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG, WB>::kThreads, 1)
+template <int BA, int L, bool GRP, int STAGES, int UG, int WF, bool F16, int G>
+__global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG, WF>::kThreads, 1)
     w4a16_gemm_tc_kernel(const __grid_constant__ GroupArgs<G> g) {
-  static_assert(WB == 4 || !F16, "INT8 weights with bf16 activations");
+  static_assert(WF == kFmtInt4 || !F16, "INT8 and FP4 weights with bf16 activations");
   // this CTA's problem and its index in the problem's sub-grid
   int prob = 0;
   if constexpr (G > 1) {
@@ -589,7 +648,7 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG, WB>::kThreads, 1)
   const CUtensorMap* const tm_act = &g.tm[prob][0];
   const CUtensorMap* const tm_w = &g.tm[prob][1];
   const CUtensorMap* const tm_s = &g.tm[prob][2];
-  using C = Cfg<BA, L, GRP, STAGES, UG, WB>;
+  using C = Cfg<BA, L, GRP, STAGES, UG, WF>;
   constexpr int DB = C::kDB;
   constexpr int SL = C::kSL;
   constexpr int AL = C::kAL;
@@ -607,7 +666,11 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG, WB>::kThreads, 1)
   };
   auto w_tile = [&](int stage) -> uint8_t* { return smem + stage * C::kStage + C::kWOff; };
   auto s_tile = [&](int stage, int gi) -> __half* {
-    return reinterpret_cast<__half*>(smem + stage * C::kStage + C::kSOff + gi * kSBytes);
+    return reinterpret_cast<__half*>(smem + stage * C::kStage + C::kSOff + gi * C::kSB);
+  };
+  // FP4: block-scale bytes of group gi of a stage, [block][128 rows]
+  auto s_bytes = [&](int stage, int gi) -> const uint8_t* {
+    return smem + stage * C::kStage + C::kSOff + gi * C::kSB;
   };
   // Resources of unit i (lane p, index j in the lane): the lanes own
   // interleaved shared-memory stages, TMEM weight stages and accumulators.
@@ -725,7 +788,7 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG, WB>::kThreads, 1)
         if (i == 0) W4A16_TRACE_UNIT(9, 6);
         W4A16_TRACE_UNIT(15, i);
         ptx::tma_load_2d(s_tile(stage, 0), tm_s, &sh->full[stage], (u.tile % a.n_tiles) * kTileW,
-                         g0);
+                         g0 * wf_blocks(WF));
         if (i == 0) W4A16_TRACE_UNIT(9, 7);
         if (i <= 1) W4A16_TRACE_POINT(3);
         W4A16_TRACE_UNIT(0, i);
@@ -1048,6 +1111,10 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG, WB>::kThreads, 1)
       int seg = 0;
       int i_first = 0;
       uint32_t nsync = 0;
+      // NVFP4: g multiplies every fp32 sum (partials too: the fixup adds
+      // scaled partials) before the bias
+      float g_t = 1.0f;
+      if constexpr (WF == kFmtNvfp4) g_t = __ldg(a.out_scale);
       for (int i = 0; i < total; ++i) {
         const Unit u = it.next();
         if (u.seg_first) {
@@ -1075,6 +1142,10 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG, WB>::kThreads, 1)
 #pragma unroll
             for (int c = 0; c < C::kChunk; ++c) v[c] += w[c];
           }
+          if constexpr (WF == kFmtNvfp4) {
+#pragma unroll
+            for (int c = 0; c < C::kChunk; ++c) v[c] *= g_t;
+          }
           emit_cols<BA, C::kChunk, F16>(a, u, row, c0, v, bias_f, cta);
         }
         ptx::tc_fence_before();
@@ -1096,10 +1167,10 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG, WB>::kThreads, 1)
     // a row of a group's codes: 64 B (INT4, 64-byte swizzle: 16-byte chunk c
     // of row r at c ^ ((r >> 1) & 3)) or 128 B (INT8, 128-byte swizzle:
     // chunk c at c ^ (r & 7))
-    constexpr int kRowBytes = WB * 16;
+    constexpr int kRowBytes = wf_bits(WF) * 16;
     constexpr int kChunks = kRowBytes / 16;
     const uint32_t wrow0 = ptx::smem_u32(w_tile(0)) + row * kRowBytes;
-    const uint32_t swz = WB == 4 ? ((row >> 1) & 3) : (row & 7);
+    const uint32_t swz = wf_bits(WF) == 4 ? ((row >> 1) & 3) : (row & 7);
     for (int i = wg; i < total; i += 2) {
       int p, j;
       lane_split<L>(i, p, j);
@@ -1147,7 +1218,9 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG, WB>::kThreads, 1)
         const uint32_t a_addr = lane_base + as * kAStageCols;
         uint32_t s_hi2 = 0, s_lo2 = 0;
         float s_w8 = 0.0f;
-        if constexpr (!GRP && WB == 8) {
+        if constexpr (wf_fp4(WF)) {
+          // the block scales are read per block below
+        } else if constexpr (!GRP && WF == kFmtInt8) {
           s_w8 = __half2float(s_tile(stage, gi)[row]);
         } else if constexpr (!GRP) {
           if constexpr (F16) {
@@ -1170,14 +1243,32 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG, WB>::kThreads, 1)
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           uint32_t opnd[16];
-          if constexpr (WB == 4) {
+          if constexpr (wf_fp4(WF)) {
+            // 32 K values: one MXFP4 block, or two NVFP4 blocks (words 4 q,
+            // 4 q + 1 and 4 q + 2, 4 q + 3)
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              constexpr int kWordsPerBlock = WF == kFmtMxfp4 ? 4 : 2;
+              const int blk = (4 * q + w) / kWordsPerBlock;
+              const uint32_t sc = s_bytes(stage, gi)[blk * kTileW + row];
+              uint32_t h2, off2;
+              if constexpr (WF == kFmtMxfp4) {
+                mx_half_scale(sc, h2, off2);
+              } else {
+                nv_half_scale(sc, h2, off2);
+              }
+              e2m1_to_operand(words[gi][4 * q + w], h2, off2, &opnd[4 * w]);
+            }
+          } else if constexpr (WF == kFmtInt4) {
 #pragma unroll
             for (int w = 0; w < 4; ++w) codes_to_operand<F16>(words[gi][4 * q + w], &opnd[4 * w]);
           } else {
 #pragma unroll
             for (int w = 0; w < 8; ++w) bytes_to_operand_bf16(words[gi][8 * q + w], &opnd[2 * w]);
           }
-          if constexpr (!GRP && WB == 8) {
+          if constexpr (wf_fp4(WF)) {
+            // scaled during the conversion
+          } else if constexpr (!GRP && WF == kFmtInt8) {
 #pragma unroll
             for (int c = 0; c < 16; ++c) opnd[c] = scale_pair_bf16_f32(opnd[c], s_w8);
           } else if constexpr (!GRP) {
@@ -1220,10 +1311,10 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG, WB>::kThreads, 1)
   if (threadIdx.x == 32) W4A16_TRACE_POINT(11);
 }
 
-template <int BA, int L, bool GRP, int STAGES, int UG, int WB, bool F16, int G>
+template <int BA, int L, bool GRP, int STAGES, int UG, int WF, bool F16, int G>
 cudaError_t launch_instance(const GemmGroup& grp, bool use_pdl, cudaStream_t stream) {
-  using C = Cfg<BA, L, GRP, STAGES, UG, WB>;
-  auto kernel = w4a16_gemm_tc_kernel<BA, L, GRP, STAGES, UG, WB, F16, G>;
+  using C = Cfg<BA, L, GRP, STAGES, UG, WF>;
+  auto kernel = w4a16_gemm_tc_kernel<BA, L, GRP, STAGES, UG, WF, F16, G>;
   if (grp.count < 1 || grp.count > G) return cudaErrorInvalidValue;
 
   int dev = 0;
@@ -1262,15 +1353,26 @@ cudaError_t launch_instance(const GemmGroup& grp, bool use_pdl, cudaStream_t str
     // UG tiles are one box
     const uint64_t w_rows =
         static_cast<uint64_t>((p.N + kTileW - 1) / kTileW) * (p.K / kUnitK) * kTileW;
-    constexpr uint32_t kRowBytes = WB * 16;
+    constexpr uint32_t kRowBytes = wf_bits(WF) * 16;
     if (encode_tmap_2d(&g.tm[i][1], CU_TENSOR_MAP_DATA_TYPE_UINT8, p.packed, kRowBytes, w_rows,
                        kRowBytes, kRowBytes, kTileW * UG,
-                       WB == 4 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B) !=
+                       wf_bits(WF) == 4 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B) !=
         CUDA_SUCCESS)
       return cudaErrorInvalidValue;
-    if (encode_tmap_2d(&g.tm[i][2], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.scales, p.N, p.K / kGroup,
-                       p.N * 2, kTileW, UG, CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
+    if constexpr (wf_fp4(WF)) {
+      // block-scale bytes [K/32 or K/16][N]: a unit's blocks for 128 rows
+      // are one box {128, UG * blocks per group}
+      if (p.tensor_scale == nullptr && WF == kFmtNvfp4) return cudaErrorInvalidValue;
+      if (encode_tmap_2d(&g.tm[i][2], CU_TENSOR_MAP_DATA_TYPE_UINT8, p.scales, p.N,
+                         p.K / kUnitK * wf_blocks(WF), p.N, kTileW, UG * wf_blocks(WF),
+                         CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    } else {
+      if (encode_tmap_2d(&g.tm[i][2], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.scales, p.N,
+                         p.K / kGroup, p.N * 2, kTileW, UG, CU_TENSOR_MAP_SWIZZLE_NONE) !=
+          CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    }
 
     Args& a = g.a[i];
     a.M = static_cast<int>(p.M);
@@ -1282,6 +1384,7 @@ cudaError_t launch_instance(const GemmGroup& grp, bool use_pdl, cudaStream_t str
     a.sk_units = static_cast<int>(s.sk_units);
     a.act_3d = act_3d;
     a.scales = static_cast<const __half*>(p.scales);
+    a.out_scale = p.tensor_scale;
     a.bias = static_cast<const uint16_t*>(p.bias);
     a.Y = static_cast<uint16_t*>(p.Y);
     a.counters = p.counters != nullptr ? p.counters : static_cast<uint32_t*>(p.workspace);
@@ -1336,12 +1439,37 @@ cudaError_t launch_instance(const GemmGroup& grp, bool use_pdl, cudaStream_t str
   X(128, 1, false, 4, 1)        \
   X(256, 1, false, 2, 1)
 
-inline cudaError_t launch_gemm_tc_w8_typed(const GemmKernelConfig& c, const GemmGroup& grp,
-                                           bool use_pdl, cudaStream_t stream) {
+// FP4 weights (MXFP4 or NVFP4, bf16 activations, single problems; dequant
+// mode only): {act_tile, lanes, group_scale, stages, unit_groups}.
+#define FP4A16_GEMM_INSTANCES(X) \
+  X(16, 2, false, 16, 1)         \
+  X(32, 2, false, 12, 1)         \
+  X(64, 2, false, 8, 1)          \
+  X(128, 1, false, 5, 1)         \
+  X(256, 1, false, 3, 1)         \
+  X(16, 2, false, 8, 2)
+
+template <int WF>
+cudaError_t launch_gemm_tc_fp4_typed(const GemmKernelConfig& c, const GemmGroup& grp,
+                                     bool use_pdl, cudaStream_t stream) {
+#define FP4A16_LAUNCH_CASE(BA, L, GRP, ST, UG)                                   \
+  if (c.act_tile == BA && c.lanes == L && c.group_scale == GRP && c.stages == ST && \
+      c.unit_groups == UG && c.weight_format == WF)                                 \
+    return launch_instance<BA, L, GRP, ST, UG, WF, false, 1>(grp, use_pdl, stream);
+  FP4A16_GEMM_INSTANCES(FP4A16_LAUNCH_CASE)
+#undef FP4A16_LAUNCH_CASE
+  return cudaErrorInvalidConfiguration;
+}
+
+// (a template, so that only the unit that calls it compiles these kernels)
+template <int WF>
+cudaError_t launch_gemm_tc_w8_typed(const GemmKernelConfig& c, const GemmGroup& grp, bool use_pdl,
+                                    cudaStream_t stream) {
+  static_assert(WF == kFmtInt8, "INT8 weights");
 #define W8A16_LAUNCH_CASE(BA, L, GRP, ST, UG)                                    \
   if (c.act_tile == BA && c.lanes == L && c.group_scale == GRP && c.stages == ST && \
-      c.unit_groups == UG && c.weight_bits == 8)                                    \
-    return launch_instance<BA, L, GRP, ST, UG, 8, false, 1>(grp, use_pdl, stream);
+      c.unit_groups == UG && c.weight_format == kFmtInt8)                                    \
+    return launch_instance<BA, L, GRP, ST, UG, kFmtInt8, false, 1>(grp, use_pdl, stream);
   W8A16_GEMM_INSTANCES(W8A16_LAUNCH_CASE)
 #undef W8A16_LAUNCH_CASE
   return cudaErrorInvalidConfiguration;
@@ -1353,8 +1481,8 @@ cudaError_t launch_gemm_tc_typed(const GemmKernelConfig& c, const GemmGroup& grp
                                  cudaStream_t stream) {
 #define W4A16_LAUNCH_CASE(BA, L, GRP, ST, UG)                                    \
   if (c.act_tile == BA && c.lanes == L && c.group_scale == GRP && c.stages == ST && \
-      c.unit_groups == UG && c.weight_bits == 4)                                    \
-    return launch_instance<BA, L, GRP, ST, UG, 4, F16, G>(grp, use_pdl, stream);
+      c.unit_groups == UG && c.weight_format == kFmtInt4)                                    \
+    return launch_instance<BA, L, GRP, ST, UG, kFmtInt4, F16, G>(grp, use_pdl, stream);
   W4A16_GEMM_INSTANCES(W4A16_LAUNCH_CASE)
 #undef W4A16_LAUNCH_CASE
   return cudaErrorInvalidConfiguration;

@@ -11,7 +11,7 @@ namespace w4a16 {
 cudaError_t launch_gemm_tc_w8(const GemmKernelConfig& c, const GemmGroup& grp, bool use_pdl,
                               cudaStream_t stream) {
   if (grp.count != 1 || grp.p[0].act_f16) return cudaErrorInvalidValue;
-  return launch_gemm_tc_w8_typed(c, grp, use_pdl, stream);
+  return launch_gemm_tc_w8_typed<kFmtInt8>(c, grp, use_pdl, stream);
 }
 
 }  // namespace w4a16

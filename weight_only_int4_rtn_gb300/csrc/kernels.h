@@ -12,6 +12,14 @@ namespace w4a16 {
 constexpr int kGroup = 128;     // quantization group along K
 constexpr int kTileW = 128;     // weight rows per GEMM tile (tcgen05 M)
 
+// Weight formats: INT4 and INT8 codes with fp16 group scales; E2M1 codes (in
+// the INT4 tile layout) with E8M0 scales per 32 values (MXFP4) or E4M3 scales
+// per 16 values and an fp32 tensor scale (NVFP4).
+constexpr int kFmtInt4 = 4;
+constexpr int kFmtInt8 = 8;
+constexpr int kFmtMxfp4 = 41;
+constexpr int kFmtNvfp4 = 42;
+
 // RTN quantize/pack; one launch.  sr_seed non-null: INT4 stochastic rounding
 // with that seed (same scales and storage).  int8: the INT8 scheme (8-bit
 // codes, 16 KiB tiles).
@@ -19,6 +27,14 @@ cudaError_t launch_rtn_quantize(const void* W, int64_t N, int64_t K, void* packe
                                 int num_sms, uint32_t* error_word, uint64_t timeout_ns,
                                 cudaStream_t stream, const uint64_t* sr_seed = nullptr,
                                 bool int8 = false);
+
+// FP4 quantize (format kFmtMxfp4 or kFmtNvfp4): codes in the INT4 tile
+// layout, scale bytes [K/32, N] or [K/16, N].  NVFP4 also writes
+// tensor_scale[0] = g and tensor_scale[1] = the tensor absmax (a memset, an
+// absmax kernel, then the quantize kernel).
+cudaError_t launch_fp4_quantize(const void* W, int64_t N, int64_t K, void* packed, void* scales,
+                                float* tensor_scale, int format, int num_sms,
+                                uint32_t* error_word, uint64_t timeout_ns, cudaStream_t stream);
 
 // Several weights quantized in one launch (independent problems).
 constexpr int kMaxQuantizeGroup = 8;
@@ -43,7 +59,8 @@ struct GemmKernelConfig {
   int stages;        // shared-memory pipeline depth (all lanes together)
   int unit_groups = 1;  // k-groups per pipeline unit (1 or 2): one copy of the
                         // codes, scales and activations per unit
-  int weight_bits = 4;  // 4: INT4 codes (W4A16); 8: INT8 codes (W8A16)
+  int weight_format = kFmtInt4;  // kFmtInt4 (W4A16), kFmtInt8 (W8A16), kFmtMxfp4,
+                                 // kFmtNvfp4 (FP4 weights, dequant mode)
 };
 
 // The schedule of one launch.
@@ -57,7 +74,7 @@ struct GemmSchedule {
 struct GemmProblem {
   const void* A;       // [M, K] bf16
   const void* packed;  // [N, K/2] u8
-  const void* scales;  // [K/128, N] fp16
+  const void* scales;  // [K/128, N] fp16, or FP4 block-scale bytes [K/32 | K/16, N]
   const void* bias;    // [N] bf16 or null
   void* Y;             // [M, N] bf16
   int64_t M, N, K;
@@ -70,6 +87,7 @@ struct GemmProblem {
   uint32_t* error_word;
   uint64_t timeout_ns;
   bool act_f16 = false;  // A, bias and Y are fp16 (else bf16)
+  const float* tensor_scale = nullptr;   // NVFP4: the fp32 tensor scale g (device)
 };
 
 // Number of tiles of a problem under a configuration.
@@ -124,6 +142,12 @@ cudaError_t launch_gemm_tc_group_f16(const GemmKernelConfig& c, const GemmGroup&
 // INT8 weights (gemm_tc_w8.cu): one problem, bf16 activations.
 cudaError_t launch_gemm_tc_w8(const GemmKernelConfig& c, const GemmGroup& grp, bool use_pdl,
                               cudaStream_t stream);
+// FP4 weights (gemm_tc_mxfp4.cu, gemm_tc_nvfp4.cu): one problem, bf16
+// activations.
+cudaError_t launch_gemm_tc_mxfp4(const GemmKernelConfig& c, const GemmGroup& grp, bool use_pdl,
+                                 cudaStream_t stream);
+cudaError_t launch_gemm_tc_nvfp4(const GemmKernelConfig& c, const GemmGroup& grp, bool use_pdl,
+                                 cudaStream_t stream);
 
 // Failure-detection self test: one thread waits on an mbarrier nobody
 // arrives at, with a bounded wait; records a timeout in *error_word.

@@ -55,6 +55,24 @@
 // code, tiles of 128 rows x 128 K values (16 KiB, 128 B per row).  For a
 // normal scale |w / s| <= 127 (1 + 2^-11) < 127.5, so again no clamp is
 // active and the low byte of the rounded float is the code.
+//
+// FP4 modes (MXFP4 and NVFP4 weights: "Kernel dispatch and Humming
+// quantization in PhyAI", section "Choose precision by layer and hardware";
+// NVFP4's blocks of 16 and per-tensor scale: "Piper Kernels", section "NVFP4
+// construction").  E2M1 codes (sign in the nibble's top bit) in the INT4 tile
+// layout; the rounding is the conversion instruction cvt.rn.satfinite.e2m1x2
+// (nearest, ties to the even mantissa, saturating at 6), with the sign of a
+// code whose magnitude rounds to 0 cleared afterwards.
+//   MXFP4 (OCP MX v1.0): blocks of 32 values; E = floor(log2 amax) - 2 + 127
+//   read off amax's exponent field (127 for an all-zero block), one scale
+//   byte per block; the elements are w * 2^(127 - E), an exact product.
+//   NVFP4: a first kernel takes the tensor's absmax (atomic max of the bit
+//   patterns, non-negative floats order like integers) into the second word
+//   of the caller's tensor-scale pair; here g = fl32(amax / 2688) (1 for a
+//   zero tensor) is written to the first word; per block of 16, the scale
+//   code is E4M3_rn_sat(fl32(fl32(amax_b / 6) / g)) (cvt.rn.satfinite.e4m3x2)
+//   and the elements are fl32(w / fl32(s_b g)), the quotient corrected to the
+//   correctly rounded one as in the INT4 mode.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -85,13 +103,14 @@ constexpr int kQMaxGroup = 8;
 struct QGroupArgs {
   CUtensorMap tm[kQMaxGroup];
   uint32_t* packed[kQMaxGroup];
-  __half* scales[kQMaxGroup];
+  void* scales[kQMaxGroup];   // fp16 (INT4, INT8) or bytes (FP4 block scales)
   int N[kQMaxGroup];
   int G[kQMaxGroup];
   int tiles[kQMaxGroup];
   int cta_start[kQMaxGroup + 1];
   int count;
   uint64_t seed;   // stochastic-rounding mode: the generator's key
+  float* tscale;   // NVFP4 mode: {g (written here), tensor absmax (read)}
 };
 
 struct QShared {
@@ -230,6 +249,41 @@ __device__ __forceinline__ void codes8_exact(const float (&f)[8], float s, uint3
   w1 = pack4_bytes(y[4], y[5], y[6], y[7]);
 }
 
+// ------------------------------------------------------------- FP4 modes
+// E2M1 codes of two values in one byte: b in the low nibble, a in the high
+// nibble (round to nearest even, saturating at +-6).
+__device__ __forceinline__ uint32_t e2m1x2(float a, float b) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
+      : "=r"(r)
+      : "f"(a), "f"(b));
+  return r;
+}
+
+// Eight E2M1 codes (x[i] in nibble i) with the sign of zero magnitudes
+// cleared: a nibble keeps its sign bit only if its low three bits are not 0.
+__device__ __forceinline__ uint32_t e2m1_word(const float (&x)[8]) {
+  const uint32_t w = ptx::prmt(ptx::prmt(e2m1x2(x[1], x[0]), e2m1x2(x[3], x[2]), 0x0040),
+                               ptx::prmt(e2m1x2(x[5], x[4]), e2m1x2(x[7], x[6]), 0x0040), 0x5410);
+  const uint32_t mag = w & 0x77777777u;
+  return mag | (w & ((mag + 0x77777777u) & 0x88888888u));
+}
+
+// E4M3 code (round to nearest even, saturating at 448) of a non-negative
+// float.
+__device__ __forceinline__ uint32_t e4m3_code(float v) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(v));
+  return static_cast<uint32_t>(r) & 0xFFu;
+}
+
+// Value of an E4M3 code (bias 7): its 7 bits placed under the fp32 exponent
+// field's low bits give the value * 2^-120 (normal or subnormal alike), and
+// one exact product restores the scale.
+__device__ __forceinline__ float e4m3_value(uint32_t code) {
+  return __uint_as_float((code & 0x7Fu) << 20) * 0x1p120f;
+}
+
 __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -246,17 +300,51 @@ __device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t acc, uint32_t w) {
   return *reinterpret_cast<const uint32_t*>(&m);
 }
 
+// |bf16| maximum of 16 values (two 16-byte chunks) as a float.
+__device__ __forceinline__ float absmax16(const uint4& a, const uint4& b) {
+  uint32_t m = bf16x2_absmax(bf16x2_absmax(bf16x2_absmax(0u, a.x), a.y),
+                             bf16x2_absmax(bf16x2_absmax(0u, a.z), a.w));
+  m = bf16x2_absmax(m, bf16x2_absmax(bf16x2_absmax(bf16x2_absmax(0u, b.x), b.y),
+                                     bf16x2_absmax(bf16x2_absmax(0u, b.z), b.w)));
+  return fmaxf(__uint_as_float(m << 16), __uint_as_float(m & 0xFFFF0000u));
+}
+
+// Tensor absmax of an NVFP4 weight: every thread takes 16-byte pieces of
+// the [N, K] bf16 weight (N K a multiple of 128), reduces them, a warp
+// reduces its lanes and lane 0 takes an atomic max into *amax_bits (zeroed
+// before the launch).
+__global__ void __launch_bounds__(256) tensor_absmax_kernel(const uint4* __restrict__ w,
+                                                            int64_t n16, uint32_t* amax_bits) {
+  uint32_t m = 0;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16;
+       i += stride) {
+    const uint4 v = __ldg(w + i);
+    m = bf16x2_absmax(m, v.x);
+    m = bf16x2_absmax(m, v.y);
+    m = bf16x2_absmax(m, v.z);
+    m = bf16x2_absmax(m, v.w);
+  }
+  uint32_t a = __float_as_uint(fmaxf(__uint_as_float(m << 16), __uint_as_float(m & 0xFFFF0000u)));
+  a = __reduce_max_sync(0xFFFFFFFFu, a);
+  if ((threadIdx.x & 31) == 0 && a != 0) atomicMax(amax_bits, a);
+}
+
 // MODE: kModeRtn4 (INT4, round to nearest), kModeSr4 (INT4, stochastic
 // rounding), kModeRtn8 (INT8, round to nearest).
 constexpr int kModeRtn4 = 0;
 constexpr int kModeSr4 = 1;
 constexpr int kModeRtn8 = 2;
+constexpr int kModeMx4 = 3;   // MXFP4
+constexpr int kModeNv4 = 4;   // NVFP4
+constexpr int kModes = 5;
 
 template <int MODE>
 __global__ void __launch_bounds__(kQThreads, 1)
     rtn_quantize_kernel(const __grid_constant__ QGroupArgs q, uint32_t* err, uint64_t timeout_ns) {
   constexpr bool SR = MODE == kModeSr4;
   constexpr bool W8 = MODE == kModeRtn8;
+  constexpr bool FP4 = MODE == kModeMx4 || MODE == kModeNv4;
   // this CTA's weight and its index in that weight's sub-grid
   int prob = 0;
   while (prob + 1 < q.count && static_cast<int>(blockIdx.x) >= q.cta_start[prob + 1]) ++prob;
@@ -265,7 +353,6 @@ __global__ void __launch_bounds__(kQThreads, 1)
   const int G = q.G[prob];
   const int tiles = q.tiles[prob];
   uint32_t* const packed = q.packed[prob];
-  __half* const scales = q.scales[prob];
   const int cta = static_cast<int>(blockIdx.x) - q.cta_start[prob];
   const int ctas = q.cta_start[prob + 1] - q.cta_start[prob];
   extern __shared__ __align__(1024) uint8_t q_smem_raw[];
@@ -291,6 +378,14 @@ __global__ void __launch_bounds__(kQThreads, 1)
   // before it reads anything this kernel writes).
   ptx::grid_dependency_wait();
   ptx::grid_launch_dependents();
+
+  // NVFP4: the tensor scale from the absmax the previous kernel reduced
+  float g_t = 1.0f;
+  if constexpr (MODE == kModeNv4) {
+    const float amax_t = __ldcg(q.tscale + 1);
+    g_t = amax_t == 0.0f ? 1.0f : __fdiv_rn(amax_t, 2688.0f);
+    if (blockIdx.x == 0 && threadIdx.x == 0) q.tscale[0] = g_t;
+  }
 
   const int n_local = (tiles - cta + ctas - 1) / ctas;
 
@@ -339,6 +434,75 @@ __global__ void __launch_bounds__(kQThreads, 1)
     const int tn = t / G;
     const int g = t - tn * G;
     const uint32_t box = ptx::smem_u32(smem + stage * kQTileBytes) + h * kQBoxBytes;
+    const int n = tn * kQRows + row;
+
+    if constexpr (FP4) {
+      // this thread's half row: values 64 h .. 64 h + 63 of the group, 32
+      // code bytes at word 8 h of the row's 16 words.  Blocks are taken in
+      // the rotated order (the two threads of a pair read chunks four apart,
+      // so one instruction never hits one bank twice).
+      uint32_t* const dst = packed + ((static_cast<int64_t>(tn) * G + g) * kQRows + row) * 16 + 8 * h;
+      uint8_t* const sc = static_cast<uint8_t*>(q.scales[prob]);
+      if constexpr (MODE == kModeMx4) {
+#pragma unroll
+        for (int bb = 0; bb < 2; ++bb) {
+          const int b = bb ^ h;   // block of 32 values: chunks 4 b .. 4 b + 3
+          uint4 v[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) v[j] = ptx::lds128(chunk_addr(box, row, 4 * b + j));
+          const float amax = fmaxf(absmax16(v[0], v[1]), absmax16(v[2], v[3]));
+          const uint32_t ef = __float_as_uint(amax) >> 23;   // amax >= 0: the exponent field
+          const uint32_t E = amax == 0.0f ? 127u : (ef > 2u ? ef - 2u : 0u);
+          // 2^(127 - E): E <= 252 for bf16 input, so the factor is normal
+          const float inv = __uint_as_float((254u - E) << 23);
+          uint32_t words[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            float f[8];
+            unpack8(v[j], f);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) f[i] = __fmul_rn(f[i], inv);
+            words[j] = e2m1_word(f);
+          }
+          reinterpret_cast<uint4*>(dst)[b] = make_uint4(words[0], words[1], words[2], words[3]);
+          if (n < N) sc[static_cast<int64_t>(4 * g + 2 * h + b) * N + n] = static_cast<uint8_t>(E);
+        }
+      } else {
+#pragma unroll
+        for (int bb = 0; bb < 4; ++bb) {
+          const int b = (bb + 2 * h) & 3;   // block of 16 values: chunks 2 b, 2 b + 1
+          const uint4 v0 = ptx::lds128(chunk_addr(box, row, 2 * b));
+          const uint4 v1 = ptx::lds128(chunk_addr(box, row, 2 * b + 1));
+          const float amax = absmax16(v0, v1);
+          const uint32_t code = e4m3_code(__fdiv_rn(__fdiv_rn(amax, 6.0f), g_t));
+          const float step = __fmul_rn(e4m3_value(code), g_t);
+          float f[16];
+          unpack8(v0, *reinterpret_cast<float(*)[8]>(&f[0]));
+          unpack8(v1, *reinterpret_cast<float(*)[8]>(&f[8]));
+          if (step == 0.0f) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) f[i] = 0.0f;
+          } else if ((__float_as_uint(step) & 0x7F800000u) != 0) {
+            const float r = __frcp_rn(step);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float q1 = __fmul_rn(f[i], r);
+              f[i] = fmaf(fmaf(-q1, step, f[i]), r, q1);   // fl32(w / step)
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) f[i] = __fdiv_rn(f[i], step);
+          }
+          const uint32_t w0 = e2m1_word(*reinterpret_cast<const float(*)[8]>(&f[0]));
+          const uint32_t w1 = e2m1_word(*reinterpret_cast<const float(*)[8]>(&f[8]));
+          reinterpret_cast<uint2*>(dst)[b] = make_uint2(w0, w1);
+          if (n < N) sc[static_cast<int64_t>(8 * g + 4 * h + b) * N + n] = static_cast<uint8_t>(code);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&sh->empty[stage]);
+      continue;
+    }
 
     // pass 1: absmax of the row's 128 values (two independent chains per
     // thread, then across the pair), and the scale
@@ -434,17 +598,17 @@ __global__ void __launch_bounds__(kQThreads, 1)
     }
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(&sh->empty[stage]);
-    const int n = tn * kQRows + row;
-    if (h == 0 && n < N) scales[static_cast<int64_t>(g) * N + n] = s16;
+    if (h == 0 && n < N) static_cast<__half*>(q.scales[prob])[static_cast<int64_t>(g) * N + n] = s16;
   }
 }
 
 }  // namespace
 
-cudaError_t launch_rtn_quantize_group(const QuantizeProblem* probs, int count, int num_sms,
-                                      uint32_t* error_word, uint64_t timeout_ns,
-                                      cudaStream_t stream, const uint64_t* sr_seed, bool int8) {
-  if (int8 && sr_seed != nullptr) return cudaErrorInvalidValue;
+namespace {
+
+cudaError_t launch_quantize_mode(const QuantizeProblem* probs, int count, int num_sms,
+                                 uint32_t* error_word, uint64_t timeout_ns, cudaStream_t stream,
+                                 int mode, uint64_t seed, float* tscale) {
   static_assert(kQMaxGroup == kMaxQuantizeGroup, "group size of the kernel arguments");
   if (count < 1 || count > kQMaxGroup) return cudaErrorInvalidValue;
   QGroupArgs q{};
@@ -458,7 +622,7 @@ cudaError_t launch_rtn_quantize_group(const QuantizeProblem* probs, int count, i
                        CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
     q.packed[i] = static_cast<uint32_t*>(p.packed);
-    q.scales[i] = static_cast<__half*>(p.scales);
+    q.scales[i] = p.scales;
     q.N[i] = static_cast<int>(p.N);
     q.G[i] = static_cast<int>(p.K / kGroup);
     q.tiles[i] = static_cast<int>((p.N + kQRows - 1) / kQRows) * q.G[i];
@@ -492,17 +656,19 @@ cudaError_t launch_rtn_quantize_group(const QuantizeProblem* probs, int count, i
   }
   q.cta_start[count] = start;
   q.count = count;
-  q.seed = sr_seed != nullptr ? *sr_seed : 0;
-  const int mode = int8 ? kModeRtn8 : sr_seed != nullptr ? kModeSr4 : kModeRtn4;
+  q.seed = seed;
+  q.tscale = tscale;
   auto kernel = mode == kModeRtn8 ? rtn_quantize_kernel<kModeRtn8>
                 : mode == kModeSr4 ? rtn_quantize_kernel<kModeSr4>
+                : mode == kModeMx4 ? rtn_quantize_kernel<kModeMx4>
+                : mode == kModeNv4 ? rtn_quantize_kernel<kModeNv4>
                                    : rtn_quantize_kernel<kModeRtn4>;
 
   constexpr size_t smem = static_cast<size_t>(kQStages) * kQTileBytes + sizeof(QShared) + 1024;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  static bool attr_set[3][64] = {};
+  static bool attr_set[kModes][64] = {};
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_set[mode][dev]) {
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -524,11 +690,44 @@ cudaError_t launch_rtn_quantize_group(const QuantizeProblem* probs, int count, i
   return cudaLaunchKernelEx(&cfg, kernel, q, error_word, timeout_ns);
 }
 
+}  // namespace
+
+cudaError_t launch_rtn_quantize_group(const QuantizeProblem* probs, int count, int num_sms,
+                                      uint32_t* error_word, uint64_t timeout_ns,
+                                      cudaStream_t stream, const uint64_t* sr_seed, bool int8) {
+  if (int8 && sr_seed != nullptr) return cudaErrorInvalidValue;
+  const int mode = int8 ? kModeRtn8 : sr_seed != nullptr ? kModeSr4 : kModeRtn4;
+  return launch_quantize_mode(probs, count, num_sms, error_word, timeout_ns, stream, mode,
+                              sr_seed != nullptr ? *sr_seed : 0, nullptr);
+}
+
 cudaError_t launch_rtn_quantize(const void* W, int64_t N, int64_t K, void* packed, void* scales,
                                 int num_sms, uint32_t* error_word, uint64_t timeout_ns,
                                 cudaStream_t stream, const uint64_t* sr_seed, bool int8) {
   QuantizeProblem p{W, N, K, packed, scales};
   return launch_rtn_quantize_group(&p, 1, num_sms, error_word, timeout_ns, stream, sr_seed, int8);
+}
+
+cudaError_t launch_fp4_quantize(const void* W, int64_t N, int64_t K, void* packed, void* scales,
+                                float* tensor_scale, int format, int num_sms,
+                                uint32_t* error_word, uint64_t timeout_ns, cudaStream_t stream) {
+  QuantizeProblem p{W, N, K, packed, scales};
+  if (format == kFmtMxfp4)
+    return launch_quantize_mode(&p, 1, num_sms, error_word, timeout_ns, stream, kModeMx4, 0,
+                                nullptr);
+  if (format != kFmtNvfp4 || tensor_scale == nullptr) return cudaErrorInvalidValue;
+  // the tensor absmax into tensor_scale[1] (zeroed first), then the codes
+  cudaError_t e = cudaMemsetAsync(tensor_scale, 0, 2 * sizeof(float), stream);
+  if (e != cudaSuccess) return e;
+  const int64_t n16 = N * K / 8;
+  int blocks = 4 * num_sms;
+  if (static_cast<int64_t>(blocks) * 256 > n16) blocks = static_cast<int>((n16 + 255) / 256);
+  tensor_absmax_kernel<<<blocks, 256, 0, stream>>>(static_cast<const uint4*>(W), n16,
+                                                     reinterpret_cast<uint32_t*>(tensor_scale + 1));
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_quantize_mode(&p, 1, num_sms, error_word, timeout_ns, stream, kModeNv4, 0,
+                              tensor_scale);
 }
 
 }  // namespace w4a16
