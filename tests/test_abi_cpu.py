@@ -94,8 +94,11 @@ def test_variant_catalogue_is_host_only(built_lib):
     assert len(set(names)) == n and all(names)
     assert w4.w4a16_variant_name(n) is None
     for i in range(n):
-        assert w4.w4a16_variant_eligible(i, 16, 256, 512)
-        assert not w4.w4a16_variant_eligible(i, 16, 256, 500)
+        # the CUDA-core streaming variants take M up to their own tile
+        m = int(names[i].split("_")[1][1:]) if names[i].startswith("simt_") else 16
+        assert w4.w4a16_variant_eligible(i, m, 256, 512)
+        assert not w4.w4a16_variant_eligible(i, m, 256, 500)
+        assert not names[i].startswith("simt_") or not w4.w4a16_variant_eligible(i, m + 1, 256, 512)
     for M in (1, 4, 16, 50, 64, 816, 8192):
         v = w4.w4a16_select_variant(M, 8192, 8192)
         assert 0 <= v < n

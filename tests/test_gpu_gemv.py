@@ -1,0 +1,128 @@
+"""The CUDA-core streaming GEMM variants for tiny M (simt_m{1,2,4,8}_sk)
+against the oracle's FP32 GEMM on identical packed operands: every M from 1
+to 8 on ragged, multi-tile and long-K shapes within |y - y_ref| <= 1e-2
+|y_ref| + 1e-2 rms(y_ref); bit-exact on integer-exact inputs; split tiles
+bit-identical across runs with NaN-filled partial slots."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_helpers import bits, check_gemm_close, guarded
+from weight_only_int4_rtn_gb300 import synthetic
+
+pytestmark = pytest.mark.gpu
+
+NAN_BF16 = 0x7FC1
+
+
+def simt_variants(w4):
+    return [v for v in range(w4.w4a16_variant_count()) if w4.w4a16_variant_name(v).startswith("simt_")]
+
+
+def reference(A, packed, scales, b, rows=None):
+    s = scales.cpu().view(torch.int16).numpy().view(np.uint16)
+    K, N = s.shape[0] * 128, s.shape[1]
+    p = oracle.from_tile_layout(packed.cpu().numpy(), N, K)
+    return oracle.gemm(bits(A), p, s, None if b is None else bits(b), rows=rows)
+
+
+SHAPES = [synthetic.Case(f"m{m}_{n}x{k}", m, n, k, 40 + m + k // 128, "t4" if m % 2 else "normal",
+                         bias=(m % 3 != 0))
+          for m in (1, 2, 3, 4, 5, 7, 8)
+          for (n, k) in ((264, 384), (2048, 4096), (136, 16384))]
+
+
+@pytest.mark.parametrize("case", SHAPES, ids=[c.name for c in SHAPES])
+def test_simt_variants(w4, case):
+    W, A, b = synthetic.draw(case)
+    packed, scales = w4.w4a16_quantize(W.cuda())
+    y_ref = reference(A, packed, scales, b)
+    Ad = A.cuda()
+    bd = None if b is None else b.cuda()
+    ran = 0
+    for v in simt_variants(w4):
+        if not w4.w4a16_variant_eligible(v, case.M, case.N, case.K):
+            continue
+        Y, ok = guarded((case.M, case.N), torch.bfloat16, Ad.device, NAN_BF16)
+        w4.w4a16_gemm(Ad, packed, scales, bias=bd, Y=Y, variant=v)
+        torch.cuda.synchronize()
+        assert ok(), f"{w4.w4a16_variant_name(v)} wrote outside Y"
+        check_gemm_close(Y, y_ref, what=w4.w4a16_variant_name(v))
+        ran += 1
+    assert ran >= 1
+    assert w4.w4a16_get_device_error() == w4.W4A16_OK
+
+
+def test_simt_ineligible_above_its_m(w4):
+    for v in simt_variants(w4):
+        mt = int(w4.w4a16_variant_name(v).split("_")[1][1:])
+        assert w4.w4a16_variant_eligible(v, mt, 256, 512)
+        assert not w4.w4a16_variant_eligible(v, mt + 1, 256, 512)
+
+
+def test_simt_integer_exact(w4):
+    # power-of-two scales, activations in {-1, 0, 1}: every product, the
+    # offset corrections and every partial sum are exact in fp32, so Y is the
+    # exact sum rounded once to bf16
+    rng = np.random.default_rng(35)
+    M, N, K = 8, 384, 2048
+    codes = rng.integers(-7, 8, size=(N, K))
+    codes[:, ::128] = 7
+    e = rng.integers(-3, 0, size=(N, K // 128))
+    x = (codes * np.repeat(2.0 ** e, 128, axis=1)).astype(np.float32)
+    a = rng.integers(-1, 2, size=(M, K)).astype(np.float32)
+    W = synthetic.to_bf16(x).cuda()
+    packed, scales = w4.w4a16_quantize(W)
+    for m in range(1, M + 1):
+        A = synthetic.to_bf16(a[:m])
+        exact = a[:m].astype(np.float64) @ x.astype(np.float64).T
+        expected = bits(synthetic.to_bf16(exact.astype(np.float32)))
+        for v in simt_variants(w4):
+            if not w4.w4a16_variant_eligible(v, m, N, K):
+                continue
+            Y = w4.w4a16_gemm(A.cuda(), packed, scales, variant=v)
+            torch.cuda.synchronize()
+            assert np.array_equal(bits(Y), expected), (m, w4.w4a16_variant_name(v))
+
+
+def test_simt_split_tiles_deterministic(w4):
+    """Every tile split over several CTAs; fresh workspaces whose partial
+    slots hold NaN; the k-ordered sums give bit-identical repeats."""
+    case = synthetic.Case("m4_k16384", 4, 1024, 16384, 47, bias=True)
+    W, A, b = synthetic.draw(case)
+    packed, scales = w4.w4a16_quantize(W.cuda())
+    y_ref = reference(A, packed, scales, b)
+    Ad, bd = A.cuda(), b.cuda()
+    for v in simt_variants(w4):
+        if not w4.w4a16_variant_eligible(v, case.M, case.N, case.K):
+            continue
+        need = w4.w4a16_variant_workspace_bytes(v, case.M, case.N, case.K)
+        assert need > 8192
+        ys = []
+        for _ in range(2):
+            ws = torch.zeros(need, dtype=torch.uint8, device=Ad.device)
+            ws[8192:].fill_(0xFF)
+            ys.append(w4.w4a16_gemm(Ad, packed, scales, bias=bd, workspace=ws, variant=v))
+        torch.cuda.synchronize()
+        assert w4.w4a16_get_device_error() == w4.W4A16_OK
+        check_gemm_close(ys[0], y_ref, what=w4.w4a16_variant_name(v))
+        assert torch.equal(ys[0].view(torch.int16), ys[1].view(torch.int16)), w4.w4a16_variant_name(v)
+
+
+@pytest.mark.parametrize("case", [c for c in synthetic.WORKLOADS["sweep"] if c.M <= 8],
+                         ids=lambda c: c.name)
+def test_simt_sweep_shapes(w4, case):
+    # the sweep's M <= 8 shapes through every eligible streaming variant,
+    # all rows against the oracle
+    W, A, b = synthetic.draw(case)
+    packed, scales = w4.w4a16_quantize(W.cuda())
+    y_ref = reference(A, packed, scales, b)
+    Ad = A.cuda()
+    for v in simt_variants(w4):
+        if not w4.w4a16_variant_eligible(v, case.M, case.N, case.K):
+            continue
+        Y = w4.w4a16_gemm(Ad, packed, scales, variant=v)
+        torch.cuda.synchronize()
+        check_gemm_close(Y, y_ref, what=f"{case.name} {w4.w4a16_variant_name(v)}")

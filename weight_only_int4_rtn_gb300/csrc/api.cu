@@ -93,6 +93,8 @@ struct Variant {
                    // fewer split tiles on small problems)
   double unit_us;  // measured time of one unit (128 weight rows x unit_groups groups)
                    // in steady state on GB300, for the selection rule
+  double head_us = -1.0;   // launch-to-steady-state cost if not the common one
+  double split_us = -1.0;  // split-tile fixup cost if not the common model's
 };
 
 const Variant kVariants[] = {
@@ -127,6 +129,11 @@ const Variant kVariants[] = {
     {"tc_a32_deq2_sk_u2", {32, 2, false, 6, 2}, true, 1, 1.01},
     {"tc_a64_deq2_sk_u2", {64, 2, false, 4, 2}, true, 1, 1.08},
     {"tc_a64_deq2_dp_u2", {64, 2, false, 4, 2}, false, 1, 0.98},
+    // CUDA-core streaming kernel for M <= 1, 2, 4, 8
+    {"simt_m1_sk", {1, 1, true, 8, 1, kFmtInt4, true}, true, 1, 1.50, 2.0, 0.8},
+    {"simt_m2_sk", {2, 1, true, 8, 1, kFmtInt4, true}, true, 1, 2.00, 2.0, 0.8},
+    {"simt_m4_sk", {4, 1, true, 6, 1, kFmtInt4, true}, true, 1, 2.90, 2.0, 0.8},
+    {"simt_m8_sk", {8, 1, true, 6, 1, kFmtInt4, true}, true, 1, 2.60, 2.0, 0.8},
 };
 constexpr int kNumVariants = static_cast<int>(sizeof(kVariants) / sizeof(kVariants[0]));
 
@@ -188,6 +195,7 @@ bool shape_ok(int64_t M, int64_t N, int64_t K) {
 
 GemmSchedule make_schedule(const Variant& v, int64_t M, int64_t N, int64_t K, int num_sms) {
   GemmSchedule s{};
+  if (v.cfg.simt) num_sms *= gemv_ctas_per_sm(v.cfg.act_tile);
   if (num_sms > kMaxGrid) num_sms = kMaxGrid;
   const int64_t tiles = gemm_tiles(v.cfg, M, N);
   const int64_t KB = K / kGroup / v.cfg.unit_groups;   // units per tile
@@ -225,6 +233,7 @@ GemmSchedule make_schedule(const Variant& v, int64_t M, int64_t N, int64_t K, in
 
 bool variant_ok(const Variant& v, int64_t M, int64_t N, int64_t K) {
   if (!shape_ok(M, N, K)) return false;
+  if (v.cfg.simt && M > v.cfg.act_tile) return false;
   if (!gemm_config_available(v.cfg)) return false;
   const int64_t tiles = gemm_tiles(v.cfg, M, N);
   if (tiles * (K / kGroup) >= (1ll << 31)) return false;
@@ -260,8 +269,9 @@ double estimate_sched(const Variant& v, const GemmSchedule& s, int64_t K) {
   const int64_t KB = K / kGroup / v.cfg.unit_groups;
   const int64_t dp_per_cta = (s.dp_tiles + s.grid - 1) / s.grid;
   const int64_t sk_per_cta = (s.sk_units + s.grid - 1) / s.grid;
-  double t = kHeadUs + static_cast<double>(dp_per_cta * KB + sk_per_cta) * v.unit_us;
-  if (s.sk_units > 0) t += kSplitUs + kSplitUsPerCol * v.cfg.act_tile;
+  double t = (v.head_us >= 0.0 ? v.head_us : kHeadUs) +
+             static_cast<double>(dp_per_cta * KB + sk_per_cta) * v.unit_us;
+  if (s.sk_units > 0) t += v.split_us >= 0.0 ? v.split_us : kSplitUs + kSplitUsPerCol * v.cfg.act_tile;
   return t;
 }
 
@@ -496,6 +506,7 @@ GemmSchedule group_schedule(const Variant& v, const w4a16_gemm_problem& p, int c
 bool plan_for_variant(int id, const w4a16_gemm_problem* pr, int count, int sms, GroupPlan& plan,
                       bool forced) {
   const Variant& v = kVariants[id];
+  if (v.cfg.simt && count > 1) return false;   // single problems only
   for (int i = 0; i < count; ++i)
     if (!variant_eligible(id, pr[i].M, pr[i].N, pr[i].K)) return false;
   if (count > sms) return false;

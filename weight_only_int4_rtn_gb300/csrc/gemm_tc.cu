@@ -23,6 +23,7 @@ __global__ void wait_timeout_selftest_kernel(uint32_t* err, uint64_t timeout_ns)
 }  // namespace
 
 size_t gemm_smem_bytes(const GemmKernelConfig& c) {
+  if (c.simt) return gemv_smem_bytes(c);
 #define W4A16_SMEM_CASE(BA, L, GRP, ST, UG)                                          \
   if (c.act_tile == BA && c.lanes == L && c.group_scale == GRP && c.stages == ST && \
       c.unit_groups == UG && c.weight_format == kFmtInt4)                                    \
@@ -62,6 +63,7 @@ cudaError_t launch_gemm_tc_group(const GemmKernelConfig& c, const GemmGroup& grp
                                  cudaStream_t stream) {
   static_assert(kMaxGemmGroup == kMaxGroup, "group size of the kernel arguments");
   if (grp.count < 1 || grp.count > kMaxGroup) return cudaErrorInvalidValue;
+  if (c.simt) return launch_gemv(c, grp, use_pdl, stream);
   if (c.weight_format == kFmtInt8) return launch_gemm_tc_w8(c, grp, use_pdl, stream);
   if (c.weight_format == kFmtMxfp4) return launch_gemm_tc_mxfp4(c, grp, use_pdl, stream);
   if (c.weight_format == kFmtNvfp4) return launch_gemm_tc_nvfp4(c, grp, use_pdl, stream);

@@ -61,7 +61,14 @@ struct GemmKernelConfig {
                         // codes, scales and activations per unit
   int weight_format = kFmtInt4;  // kFmtInt4 (W4A16), kFmtInt8 (W8A16), kFmtMxfp4,
                                  // kFmtNvfp4 (FP4 weights, dequant mode)
+  bool simt = false;  // the CUDA-core streaming kernel (gemv.cu) for M <= act_tile
+                      // (1, 2, 4 or 8), INT4 weights
 };
+
+// CTAs of the CUDA-core streaming kernel resident per SM (its schedules use
+// this many CTAs per SM): two up to M = 4 (<= 96 registers a thread), one for
+// M = 8 (its operands need more registers).
+constexpr int gemv_ctas_per_sm(int act_tile) { return act_tile <= 4 ? 2 : 1; }
 
 // The schedule of one launch.
 struct GemmSchedule {
@@ -148,6 +155,13 @@ cudaError_t launch_gemm_tc_mxfp4(const GemmKernelConfig& c, const GemmGroup& grp
                                  cudaStream_t stream);
 cudaError_t launch_gemm_tc_nvfp4(const GemmKernelConfig& c, const GemmGroup& grp, bool use_pdl,
                                  cudaStream_t stream);
+
+// The CUDA-core streaming kernel for tiny M (gemv.cu): one problem, INT4
+// weights, bf16 or fp16 activations; shared memory of a configuration (0:
+// none).
+cudaError_t launch_gemv(const GemmKernelConfig& c, const GemmGroup& grp, bool use_pdl,
+                        cudaStream_t stream);
+size_t gemv_smem_bytes(const GemmKernelConfig& c);
 
 // Failure-detection self test: one thread waits on an mbarrier nobody
 // arrives at, with a bounded wait; records a timeout in *error_word.
