@@ -129,11 +129,12 @@ const Variant kVariants[] = {
     {"tc_a32_deq2_sk_u2", {32, 2, false, 6, 2}, true, 1, 1.01},
     {"tc_a64_deq2_sk_u2", {64, 2, false, 4, 2}, true, 1, 1.08},
     {"tc_a64_deq2_dp_u2", {64, 2, false, 4, 2}, false, 1, 0.98},
-    // CUDA-core streaming kernel for M <= 1, 2, 4, 8
-    {"simt_m1_sk", {1, 1, true, 8, 1, kFmtInt4, true}, true, 1, 1.50, 2.0, 0.8},
-    {"simt_m2_sk", {2, 1, true, 8, 1, kFmtInt4, true}, true, 1, 2.00, 2.0, 0.8},
-    {"simt_m4_sk", {4, 1, true, 6, 1, kFmtInt4, true}, true, 1, 2.90, 2.0, 0.8},
-    {"simt_m8_sk", {8, 1, true, 6, 1, kFmtInt4, true}, true, 1, 2.60, 2.0, 0.8},
+    // CUDA-core streaming kernel for M <= 1, 2, 4, 8: unit_us is the time of
+    // one unit on one worker (a warp; many warps share an SM)
+    {"simt_m1_sk", {1, 1, true, 2, 1, kFmtInt4, true}, true, 1, 6.0, 2.0, 0.8},
+    {"simt_m2_sk", {2, 1, true, 2, 1, kFmtInt4, true}, true, 1, 5.2, 2.0, 0.8},
+    {"simt_m4_sk", {4, 1, true, 2, 1, kFmtInt4, true}, true, 1, 7.0, 2.0, 0.8},
+    {"simt_m8_sk", {8, 1, true, 2, 1, kFmtInt4, true}, true, 1, 10.2, 2.0, 0.8},
 };
 constexpr int kNumVariants = static_cast<int>(sizeof(kVariants) / sizeof(kVariants[0]));
 
@@ -195,7 +196,26 @@ bool shape_ok(int64_t M, int64_t N, int64_t K) {
 
 GemmSchedule make_schedule(const Variant& v, int64_t M, int64_t N, int64_t K, int num_sms) {
   GemmSchedule s{};
-  if (v.cfg.simt) num_sms *= gemv_ctas_per_sm(v.cfg.act_tile);
+  if (v.cfg.simt) {
+    // workers (warps) of the CUDA-core streaming kernel: the fewest that
+    // give every worker the same whole number of units, within the resident
+    // capacity; whole tiles only when there are more split tiles than
+    // counters
+    const int64_t tiles = gemm_tiles(v.cfg, M, N);
+    const int64_t units = tiles * (K / kGroup);
+    const int64_t cap = static_cast<int64_t>(num_sms) * gemv_workers_per_sm(v.cfg.act_tile);
+    if (tiles > kCountersPerProblem) {
+      s.grid = static_cast<int>(tiles < cap ? tiles : cap);
+      s.dp_tiles = static_cast<int>(tiles);
+      s.sk_units = 0;
+      return s;
+    }
+    const int64_t per = (units + cap - 1) / cap;
+    s.grid = static_cast<int>((units + per - 1) / per);
+    s.dp_tiles = 0;
+    s.sk_units = units;
+    return s;
+  }
   if (num_sms > kMaxGrid) num_sms = kMaxGrid;
   const int64_t tiles = gemm_tiles(v.cfg, M, N);
   const int64_t KB = K / kGroup / v.cfg.unit_groups;   // units per tile

@@ -65,10 +65,14 @@ struct GemmKernelConfig {
                       // (1, 2, 4 or 8), INT4 weights
 };
 
-// CTAs of the CUDA-core streaming kernel resident per SM (its schedules use
-// this many CTAs per SM): two up to M = 4 (<= 96 registers a thread), one for
-// M = 8 (its operands need more registers).
-constexpr int gemv_ctas_per_sm(int act_tile) { return act_tile <= 4 ? 2 : 1; }
+// The CUDA-core streaming kernel: every warp is a stream-K worker with two
+// shared-memory stages of its own (9.1, 9.9, 11.5 or 14.8 KiB for M <= 1, 2,
+// 4, 8); warps per CTA and the workers resident per SM that its schedules
+// count on.
+constexpr int gemv_warps_per_cta(int act_tile) { return act_tile <= 4 ? 4 : 2; }
+constexpr int gemv_workers_per_sm(int act_tile) {
+  return act_tile <= 1 ? 12 : act_tile <= 4 ? 8 : 6;
+}
 
 // The schedule of one launch.
 struct GemmSchedule {
