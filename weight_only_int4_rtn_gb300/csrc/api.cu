@@ -197,10 +197,10 @@ bool shape_ok(int64_t M, int64_t N, int64_t K) {
 GemmSchedule make_schedule(const Variant& v, int64_t M, int64_t N, int64_t K, int num_sms) {
   GemmSchedule s{};
   if (v.cfg.simt) {
-    // workers (warps) of the CUDA-core streaming kernel: the fewest that
-    // give every worker the same whole number of units, within the resident
-    // capacity; whole tiles only when there are more split tiles than
-    // counters
+    // workers (warps) of the CUDA-core streaming kernel: every resident slot
+    // (the warps of an SM share its issue slots, so units balance per SM,
+    // and a warp left with fewer units frees slots for its neighbours);
+    // whole tiles only when there are more split tiles than counters
     const int64_t tiles = gemm_tiles(v.cfg, M, N);
     const int64_t units = tiles * (K / kGroup);
     const int64_t cap = static_cast<int64_t>(num_sms) * gemv_workers_per_sm(v.cfg.act_tile);
@@ -210,8 +210,7 @@ GemmSchedule make_schedule(const Variant& v, int64_t M, int64_t N, int64_t K, in
       s.sk_units = 0;
       return s;
     }
-    const int64_t per = (units + cap - 1) / cap;
-    s.grid = static_cast<int>((units + per - 1) / per);
+    s.grid = static_cast<int>(units < cap ? units : cap);
     s.dp_tiles = 0;
     s.sk_units = units;
     return s;
