@@ -87,6 +87,26 @@ def test_quantize_argument_errors_before_any_launch(built_lib):
     assert L.w4a16_quantize(16, 256, 512, 128, 16, 24, None) == w4.W4A16_ERR_ALIGNMENT
 
 
+def test_fp4_argument_errors_before_any_launch(built_lib):
+    L = w4.lib()
+    # quantize: format, nulls (NVFP4 needs the tensor-scale pair), sizes, alignment
+    assert L.fp4a16_quantize(3, 16, 256, 512, 16, 16, 16, None) == w4.W4A16_ERR_UNSUPPORTED
+    assert L.fp4a16_quantize(1, None, 256, 512, 16, 16, None, None) == w4.W4A16_ERR_INVALID_ARG
+    assert L.fp4a16_quantize(2, 16, 256, 512, 16, 16, None, None) == w4.W4A16_ERR_INVALID_ARG
+    assert L.fp4a16_quantize(1, 16, 264, 512, 16, 16, None, None) == w4.W4A16_ERR_UNSUPPORTED
+    assert L.fp4a16_quantize(1, 16, 256, 500, 16, 16, None, None) == w4.W4A16_ERR_UNSUPPORTED
+    assert L.fp4a16_quantize(1, 24, 256, 512, 16, 16, None, None) == w4.W4A16_ERR_ALIGNMENT
+    assert L.fp4a16_quantize(2, 16, 256, 512, 16, 16, 20, None) == w4.W4A16_ERR_ALIGNMENT
+    # GEMM: format, NVFP4 without its tensor scale, N % 16, alignment
+    g = lambda f, N=256, ts=16, A=16: L.fp4a16_gemm(f, A, 4, N, 512, 16, 16, ts, None, 16, None, 0, None)
+    assert g(0) == w4.W4A16_ERR_UNSUPPORTED
+    assert g(2, ts=None) == w4.W4A16_ERR_INVALID_ARG
+    assert g(1, N=264) == w4.W4A16_ERR_UNSUPPORTED
+    assert g(1, A=18) == w4.W4A16_ERR_ALIGNMENT
+    assert g(2, ts=18) == w4.W4A16_ERR_ALIGNMENT
+    assert L.fp4a16_gemm_workspace_bytes(5, 1, 256, 512) == 0
+
+
 def test_variant_catalogue_is_host_only(built_lib):
     n = w4.w4a16_variant_count()
     assert n >= 4

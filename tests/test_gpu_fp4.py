@@ -265,3 +265,41 @@ def test_fp4_argument_errors(w4):
                          Y.data_ptr(), None, 0, sh) == w4.W4A16_ERR_INVALID_ARG
     assert L.fp4a16_gemm(1, A.data_ptr(), 2, 24, 256, p.data_ptr(), s.data_ptr(), None, None,
                          Y.data_ptr(), None, 0, sh) == w4.W4A16_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("fmt", FORMATS)
+def test_fp4_graph_capture(w4, fmt):
+    # the whole FP4 path (NVFP4: the memset of the tensor-scale pair, the
+    # absmax kernel, the quantize kernel; then the GEMM) captured in a CUDA
+    # graph and replayed: the same codes, scales and Y as eager calls
+    case = synthetic.Case("fp4_graph", 50, 1024, 1024, 9, bias=True)
+    W, A, b = synthetic.draw(case)
+    Wd, Ad, bd = W.cuda(), A.cuda(), b.cuda()
+    p_e, s_e, t_e = w4.fp4a16_quantize(Wd, fmt)
+    y_e = w4.fp4a16_gemm(Ad, p_e, s_e, fmt, tensor_scale=t_e, bias=bd)
+    torch.cuda.synchronize()
+    packed, scales = torch.zeros_like(p_e), torch.zeros_like(s_e)
+    ts = torch.zeros(2, dtype=torch.float32, device="cuda")
+    Y = torch.empty_like(y_e)
+    ws = torch.zeros(max(w4.lib().fp4a16_gemm_workspace_bytes(w4.FP4_FORMATS[fmt], 50, 1024, 1024), 16),
+                     dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):          # warm-up outside capture
+        w4.fp4a16_quantize(Wd, fmt, packed=packed, scales=scales, tensor_scale=ts)
+        w4.fp4a16_gemm(Ad, packed, scales, fmt, tensor_scale=ts, bias=bd, Y=Y, workspace=ws)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    packed.zero_(), scales.zero_(), ts.fill_(-1.0), Y.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        w4.fp4a16_quantize(Wd, fmt, packed=packed, scales=scales, tensor_scale=ts)
+        w4.fp4a16_gemm(Ad, packed, scales, fmt, tensor_scale=ts, bias=bd, Y=Y, workspace=ws)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(packed, p_e) and torch.equal(scales, s_e)
+    if fmt == "nvfp4":
+        assert torch.equal(ts, t_e)
+    assert torch.equal(Y.view(torch.int16), y_e.view(torch.int16))
+    assert w4.w4a16_get_device_error() == w4.W4A16_OK

@@ -126,3 +126,33 @@ def test_simt_sweep_shapes(w4, case):
         Y = w4.w4a16_gemm(Ad, packed, scales, variant=v)
         torch.cuda.synchronize()
         check_gemm_close(Y, y_ref, what=f"{case.name} {w4.w4a16_variant_name(v)}")
+
+
+def test_simt_graph_capture(w4):
+    # a streaming variant captured in a CUDA graph and replayed: Y identical
+    # to the eager call (k-ordered split-tile sums are deterministic)
+    case = synthetic.Case("simt_graph", 1, 2048, 4096, 51, bias=True)
+    W, A, b = synthetic.draw(case)
+    packed, scales = w4.w4a16_quantize(W.cuda())
+    Ad, bd = A.cuda(), b.cuda()
+    v = w4.variant_id("simt_m1_sk")
+    y_e = w4.w4a16_gemm(Ad, packed, scales, bias=bd, variant=v)
+    torch.cuda.synchronize()
+    Y = torch.zeros_like(y_e)
+    ws = torch.zeros(max(w4.w4a16_variant_workspace_bytes(v, 1, 2048, 4096), 16), dtype=torch.uint8,
+                     device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        w4.w4a16_gemm(Ad, packed, scales, bias=bd, Y=Y, workspace=ws, variant=v)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    Y.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        w4.w4a16_gemm(Ad, packed, scales, bias=bd, Y=Y, workspace=ws, variant=v)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(Y.view(torch.int16), y_e.view(torch.int16))
+    assert w4.w4a16_get_device_error() == w4.W4A16_OK
