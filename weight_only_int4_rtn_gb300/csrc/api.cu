@@ -156,17 +156,17 @@ constexpr int kNumVariants8 = static_cast<int>(sizeof(kVariants8) / sizeof(kVari
 // FP4 weights (MXFP4 or NVFP4: the format is set per call), bf16
 // activations, dequant mode.
 const Variant kVariantsF4[] = {
-    {"fp4_tc_a16_deq2_sk", {16, 2, false, 16, 1, kFmtMxfp4}, true, 1, 0.48},
-    {"fp4_tc_a16_deq2_dp", {16, 2, false, 16, 1, kFmtMxfp4}, false, 1, 0.45},
-    {"fp4_tc_a32_deq2_sk", {32, 2, false, 12, 1, kFmtMxfp4}, true, 1, 0.48},
-    {"fp4_tc_a64_deq2_sk", {64, 2, false, 8, 1, kFmtMxfp4}, true, 1, 0.50},
-    {"fp4_tc_a64_deq2_dp", {64, 2, false, 8, 1, kFmtMxfp4}, false, 1, 0.47},
-    {"fp4_tc_a128_deq_sk", {128, 1, false, 5, 1, kFmtMxfp4}, true, 1, 0.57},
-    {"fp4_tc_a128_deq_dp", {128, 1, false, 5, 1, kFmtMxfp4}, false, 1, 0.68},
-    {"fp4_tc_a256_deq_sk", {256, 1, false, 3, 1, kFmtMxfp4}, true, 1, 0.63},
-    {"fp4_tc_a256_deq_dp", {256, 1, false, 3, 1, kFmtMxfp4}, false, 1, 0.95},
-    {"fp4_tc_a16_deq2_sk_u2", {16, 2, false, 8, 2, kFmtMxfp4}, true, 1, 0.92},
-    {"fp4_tc_a16_deq2_dp_u2", {16, 2, false, 8, 2, kFmtMxfp4}, false, 1, 0.86},
+    {"fp4_tc_a16_deq2_sk", {16, 2, false, 16, 1, kFmtMxfp4}, true, 1, 0.47},
+    {"fp4_tc_a16_deq2_dp", {16, 2, false, 16, 1, kFmtMxfp4}, false, 1, 0.47},
+    {"fp4_tc_a32_deq2_sk", {32, 2, false, 12, 1, kFmtMxfp4}, true, 1, 0.47},
+    {"fp4_tc_a64_deq2_sk", {64, 2, false, 8, 1, kFmtMxfp4}, true, 1, 0.48},
+    {"fp4_tc_a64_deq2_dp", {64, 2, false, 8, 1, kFmtMxfp4}, false, 1, 0.48},
+    {"fp4_tc_a128_deq_sk", {128, 1, false, 5, 1, kFmtMxfp4}, true, 1, 0.65},
+    {"fp4_tc_a128_deq_dp", {128, 1, false, 5, 1, kFmtMxfp4}, false, 1, 0.65},
+    {"fp4_tc_a256_deq_sk", {256, 1, false, 3, 1, kFmtMxfp4}, true, 1, 0.84},
+    {"fp4_tc_a256_deq_dp", {256, 1, false, 3, 1, kFmtMxfp4}, false, 1, 0.92},
+    {"fp4_tc_a16_deq2_sk_u2", {16, 2, false, 8, 2, kFmtMxfp4}, true, 1, 0.89},
+    {"fp4_tc_a16_deq2_dp_u2", {16, 2, false, 8, 2, kFmtMxfp4}, false, 1, 0.88},
 };
 constexpr int kNumVariantsF4 = static_cast<int>(sizeof(kVariantsF4) / sizeof(kVariantsF4[0]));
 
