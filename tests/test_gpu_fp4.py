@@ -85,6 +85,25 @@ def test_quantize_special_and_ragged(w4, fmt):
 
 
 @pytest.mark.parametrize("fmt", FORMATS)
+def test_gemm_on_special_groups(w4, fmt):
+    # zero blocks, spikes, ties, blocks of tiny values (MXFP4 exponent codes
+    # 0 and 1: subnormal bf16 operands), large values: every variant within
+    # tolerance of the oracle on the same codes and scales
+    x = pins.special_groups(64).reshape(16, 512)
+    W = synthetic.to_bf16(x)
+    A = synthetic.to_bf16(np.random.default_rng(61).standard_normal((9, 512)).astype(np.float32))
+    packed, scales, ts = w4.fp4a16_quantize(W.cuda(), fmt)
+    y_ref = reference(fmt, A, packed, scales, ts, None, 16, 512)
+    for v in variants(w4):
+        if not w4.fp4a16_variant_eligible(v, 9, 16, 512):
+            continue
+        Y = w4.fp4a16_gemm(A.cuda(), packed, scales, fmt, tensor_scale=ts, variant=v)
+        torch.cuda.synchronize()
+        check_gemm_close(Y, y_ref, what=f"{fmt} {vname(w4, v)}")
+    assert w4.w4a16_get_device_error() == w4.W4A16_OK
+
+
+@pytest.mark.parametrize("fmt", FORMATS)
 def test_quantize_ties_and_saturation(w4, fmt):
     # block scales that are powers of two (MXFP4: amax 6 * 2^e; NVFP4: g = 1
     # from one value 2688 and block amax 6 * 2^j, so s_b = 2^j), elements on
