@@ -322,3 +322,17 @@ def test_fp4_graph_capture(w4, fmt):
         assert torch.equal(ts, t_e)
     assert torch.equal(Y.view(torch.int16), y_e.view(torch.int16))
     assert w4.w4a16_get_device_error() == w4.W4A16_OK
+
+
+@pytest.mark.parametrize("fmt", FORMATS)
+def test_quantize_extreme_magnitudes(w4, fmt):
+    # the special groups scaled to amax 1e-35 (NVFP4: a subnormal tensor scale,
+    # so both zero and subnormal steps s_b g, the quantizer's IEEE-division
+    # branches; MXFP4: exponent codes near 0) and to amax 4e37 (MXFP4 exponent
+    # codes up to 249): codes, scale codes and the tensor scale bit-exact
+    base = pins.special_groups(64).reshape(16, 512).astype(np.float64)
+    for factor in (2.5e-41, 1e32):
+        W = synthetic.to_bf16((base * factor).astype(np.float32))
+        packed, scales, ts = w4.fp4a16_quantize(W.cuda(), fmt)
+        torch.cuda.synchronize()
+        check_fp4_exact(W, fmt, packed, scales, ts)
