@@ -167,6 +167,47 @@ def test_integer_exact(w4):
         assert np.array_equal(bits(Y), expected), w4.w4a16_variant_name(v)
 
 
+@pytest.mark.parametrize("N", [128, 256, 512, 1024, 2048])
+def test_split_fixup_modes_integer_exact(w4, N):
+    """Split tiles with few and with very many contributors, summed by the
+    readout warps in the middle of a run or by the whole CTA at its exit: with
+    M = 50, K = 8192 the tiles of the different activation widths are spread
+    over roughly 5 to 80 CTAs.  Integer-valued inputs make every partial and
+    every order of summing them exact, so a partial summed twice or missed
+    changes the result: every split variant must return the exact sum rounded
+    once to bf16, twice, each launch on a workspace whose partial slots hold
+    NaN."""
+    rng = np.random.default_rng(33 + N)
+    M, K = 50, 8192
+    codes = rng.integers(-3, 4, size=(N, K))
+    codes[:, ::128] = 7
+    e = rng.integers(-3, 0, size=(N, K // 128))
+    x = (codes * np.repeat(2.0 ** e, 128, axis=1)).astype(np.float32)
+    a = rng.integers(-1, 2, size=(M, K)).astype(np.float32)
+    W = synthetic.to_bf16(x).cuda()
+    Ad = synthetic.to_bf16(a).cuda()
+    packed, scales = w4.w4a16_quantize(W)
+    exact = a.astype(np.float64) @ x.astype(np.float64).T
+    assert np.all(exact == np.round(exact * 8) / 8) and np.abs(exact).max() < 2 ** 20
+    expected = bits(synthetic.to_bf16(exact.astype(np.float32)))
+    checked = 0
+    for v in variant_ids(w4):
+        if not w4.w4a16_variant_eligible(v, M, N, K):
+            continue
+        need = w4.w4a16_variant_workspace_bytes(v, M, N, K)
+        if need == 0:
+            continue   # whole tiles only
+        for _ in range(2):
+            ws = torch.zeros(need, dtype=torch.uint8, device=Ad.device)
+            ws[8192:].fill_(0xFF)   # partial slots (after the 8 KiB counter region)
+            Y = w4.w4a16_gemm(Ad, packed, scales, workspace=ws, variant=v)
+            torch.cuda.synchronize()
+            assert np.array_equal(bits(Y), expected), (w4.w4a16_variant_name(v), N)
+        checked += 1
+    assert checked > 0
+    assert w4.w4a16_get_device_error() == w4.W4A16_OK
+
+
 def test_workspace_too_small_is_an_error(w4):
     M, N, K = 16, 2048, 2048
     v = w4.variant_id("tc_a16_grp_sk")

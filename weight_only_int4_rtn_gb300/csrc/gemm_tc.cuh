@@ -308,6 +308,8 @@ struct Shared {
   uint32_t tmem_base;
   int abort_flag;
   int fixup_last;             // this CTA completed a split tile's count
+  int fixup_defer;            // ... on its last run: the whole CTA sums it at exit
+  int fix_tile, fix_clo, fix_chi, fix_slot;   // that tile and its contributors
 };
 
 // ------------------------------------------------ activation-type helpers
@@ -588,10 +590,15 @@ __device__ __forceinline__ bool readout_sync(Shared* sh, uint32_t& nsync, const 
 // result does not depend on who arrives last), adds the bias, rounds once to
 // the output type and stores Y; it also resets the counter for the next
 // launch.  Nobody waits for anybody: the last arrival finds every partial
-// written.
+// written.  On the CTA's last run (`defer`) the sum is left to wide_fixup,
+// which all the CTA's warps run once their roles are done: the last arrival
+// is most often a contributor finishing its last run, and the sum's time is
+// the latency of loads that four warps alone keep too few of in flight.  (A
+// sum in the middle of a run stays with the readout warps, where it overlaps
+// the CTA's remaining units.)
 template <int BA, bool F16>
 __device__ bool split_fixup(const Args& a, const Unit& u, const SplitInfo& si, Shared* sh, int row,
-                            float bias_n, uint32_t& nsync, const WaitCtx& wc) {
+                            float bias_n, uint32_t& nsync, const WaitCtx& wc, bool defer) {
   __threadfence();   // this thread's partial row is visible to the whole GPU
   if (!readout_sync(sh, nsync, wc)) return false;
   if (threadIdx.x == 32 * kReadoutWarp0) {
@@ -600,7 +607,14 @@ __device__ bool split_fixup(const Args& a, const Unit& u, const SplitInfo& si, S
     const uint32_t old = ptx::atom_add_acq_rel_gpu(cnt, 1u);
     const bool last = old == static_cast<uint32_t>(si.c_hi - si.c_lo);
     if (last) atomicExch(cnt, 0u);
-    sh->fixup_last = last ? 1 : 0;
+    sh->fixup_last = last && !defer ? 1 : 0;
+    if (last && defer) {
+      sh->fix_tile = u.tile;
+      sh->fix_clo = si.c_lo;
+      sh->fix_chi = si.c_hi;
+      sh->fix_slot = si.slot_lo;
+      sh->fixup_defer = 1;
+    }
   }
   if (!readout_sync(sh, nsync, wc)) return false;
   if (!sh->fixup_last) return true;
@@ -631,6 +645,57 @@ __device__ bool split_fixup(const Args& a, const Unit& u, const SplitInfo& si, S
     }
   }
   return true;
+}
+
+// The deferred sum of split_fixup, by every thread of the CTA after the
+// teardown barrier: thread t takes weight row t % 128 and the columns
+// t / 128 + P j (P = threads / 128) that hold activation rows, adding the
+// contributors' partials in the same k order as split_fixup (so the result is
+// the same bit for bit).  Up to 64 loads per thread are in flight.
+template <int BA, bool F16>
+__device__ void wide_fixup(const Args& a, const Shared* sh) {
+  constexpr int P = kWarps * 32 / kTileW;
+  constexpr int kCols = BA / P;                   // columns per thread
+  constexpr int kCh = kCols < 16 ? kCols : 16;     // columns per pass
+  constexpr int kUnroll = 64 / kCh;                // contributors per round
+  static_assert(BA % P == 0, "columns split evenly over the parts");
+  __threadfence();
+  const int row = static_cast<int>(threadIdx.x) % kTileW;
+  const int part = static_cast<int>(threadIdx.x) / kTileW;
+  const int tile = sh->fix_tile;
+  const int c_lo = sh->fix_clo, c_hi = sh->fix_chi;
+  const int n = (tile % a.n_tiles) * kTileW + row;
+  const int m0 = (tile / a.n_tiles) * BA;
+  const int mcols = min(BA, a.M - m0);
+  const float bias_n = (a.bias != nullptr && n < a.N) ? act_to_float<F16>(a.bias[n]) : 0.0f;
+  constexpr int64_t kSlot = static_cast<int64_t>(BA) * kTileW;
+  const float* lo = a.ws + (static_cast<int64_t>(c_lo) * 2 + sh->fix_slot) * kSlot + row;
+#pragma unroll 1
+  for (int j0 = 0; j0 < kCols; j0 += kCh) {
+    if (part + P * j0 >= mcols) break;
+    float acc[kCh];
+#pragma unroll
+    for (int j = 0; j < kCh; ++j) {
+      const int col = part + P * (j0 + j);
+      acc[j] = col < mcols ? __ldcg(lo + col * kTileW) : 0.0f;
+    }
+#pragma unroll kUnroll
+    for (int c = c_lo + 1; c <= c_hi; ++c) {
+      const float* src = a.ws + static_cast<int64_t>(c) * 2 * kSlot + row;
+#pragma unroll
+      for (int j = 0; j < kCh; ++j) {
+        const int col = part + P * (j0 + j);
+        if (col < mcols) acc[j] += __ldcg(src + col * kTileW);
+      }
+    }
+    if (n < a.N) {
+#pragma unroll
+      for (int j = 0; j < kCh; ++j) {
+        const int col = part + P * (j0 + j);
+        if (col < mcols) a.Y[static_cast<int64_t>(m0 + col) * a.N + n] = act_from_float<F16>(acc[j] + bias_n);
+      }
+    }
+  }
 }
 
 template <int BA, int L, bool GRP, int STAGES, int UG, int WF, bool F16, int G>
@@ -723,6 +788,7 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG, WF>::kThreads, 1)
     ptx::mbar_init(&sh->rsync, 4);
     sh->abort_flag = 0;
     sh->fixup_last = 0;
+    sh->fixup_defer = 0;
     ptx::fence_mbar_init();
     ptx::prefetch_tmap(tm_act);
     ptx::prefetch_tmap(tm_w);
@@ -1024,7 +1090,8 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG, WF>::kThreads, 1)
         first = false;
         if (--seg_left == 0) {
           emit_cols<BA, BA, F16>(a, seg, row, 0, acc, bias_f, cta);
-          if (!seg.whole) ok = split_fixup<BA, F16>(a, seg, si, sh, row, bias_f, nsync, wc);
+          if (!seg.whole)
+            ok = split_fixup<BA, F16>(a, seg, si, sh, row, bias_f, nsync, wc, i + 1 == total);
           if (i + 1 < total) open_run();
         }
       };
@@ -1152,7 +1219,8 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG, WF>::kThreads, 1)
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&sh->dempty[db]);
         if (!u.whole &&
-            !split_fixup<BA, F16>(a, u, split_info(a, u.sk_tile, ctas), sh, row, bias_f, nsync, wc))
+            !split_fixup<BA, F16>(a, u, split_info(a, u.sk_tile, ctas), sh, row, bias_f, nsync, wc,
+                                  i + 1 == total))
           break;
       }
     }
@@ -1308,6 +1376,7 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG, WF>::kThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   if (warp == 1) ptx::tmem_dealloc(tmem, kTmemCols);
+  if (sh->fixup_defer) wide_fixup<BA, F16>(a, sh);
   if (threadIdx.x == 32) W4A16_TRACE_POINT(11);
 }
 
