@@ -16,10 +16,12 @@ from .w4a16_oracle import (  # noqa: F401
     f16_bits_to_f32,
     from_tile_layout,
     gemm,
+    gemm_swiglu,
     pack_codes,
     quantize,
     quantize_f32,
     scales_f32,
+    swiglu,
     tiled_bytes,
     to_tile_layout,
     unpack_codes,

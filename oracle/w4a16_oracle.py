@@ -20,7 +20,8 @@ What it computes, and where that is defined:
   rather than reproducing extra FP16/BF16 rounding; section "NVFP4
   construction": bias is applied in FP32 before the final output conversion,
   and projection tests compare against the independent reference on identical
-  packed operands.
+  packed operands; section "ConvRot INT8": an MLP's SwiGLU of a raw
+  [up | gate] tensor (``swiglu``, ``gemm_swiglu``).
 
 Readings taken where the text leaves a step open (each one is listed with its
 reason in the design notes of the repository):
@@ -223,3 +224,30 @@ def gemm(a_bits: np.ndarray, packed: np.ndarray, scale_bits: np.ndarray,
     if bias_bits is not None:
         y = y + act_bits_to_f32(bias_bits, act)[None, :]
     return y.astype(np.float32)
+
+
+def swiglu(y: np.ndarray) -> np.ndarray:
+    """SwiGLU of a pre-activation ``y[M, N]`` whose columns interleave up
+    (even columns) and gate (odd columns): ``h[m, f] = silu(y[m, 2f + 1]) *
+    y[m, 2f]`` with ``silu(g) = g / (1 + e^-g)``, in float64.
+
+    "Piper Kernels", section "ConvRot INT8": the MLP's SwiGLU takes a raw
+    [up | gate] tensor.  Interleaving the two halves column by column (up f,
+    then gate f) is the reading that keeps each pair in one output tile, so
+    the GEMM that produces them can apply SwiGLU before its one rounding.
+    """
+    y = np.asarray(y, dtype=np.float64)
+    if y.shape[1] % 2 != 0:
+        raise ValueError("N must be even (interleaved up and gate columns)")
+    up, gate = y[:, 0::2], y[:, 1::2]
+    with np.errstate(over="ignore"):
+        return gate / (1.0 + np.exp(-gate)) * up
+
+
+def gemm_swiglu(a_bits: np.ndarray, packed: np.ndarray, scale_bits: np.ndarray,
+                bias_bits: np.ndarray | None = None, group: int = GROUP,
+                rows: np.ndarray | None = None) -> np.ndarray:
+    """``swiglu(gemm(...))``: the FP32 W4A16 GEMM with bf16 activations and
+    bias, then SwiGLU of its interleaved up/gate columns (float64).  The
+    library's output is that value rounded once to bf16."""
+    return swiglu(gemm(a_bits, packed, scale_bits, bias_bits, group, rows))
