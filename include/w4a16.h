@@ -161,6 +161,40 @@ int w4a16_gemm_f16(const void* A_f16, int64_t M, int64_t N, int64_t K, const voi
                    const void* scales, int group, const void* bias_f16_or_null, void* Y_f16,
                    void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * W4A16 GEMM with a SwiGLU epilogue, for the gate/up projection of an MLP.
+ * The pages fuse SwiGLU into the input preparation of the next linear, from a
+ * raw [up | gate] tensor ("Piper Kernels", section "ConvRot INT8"); here it is
+ * fused into the GEMM that produces that tensor, which then writes half the
+ * bytes.  The weight's N rows (N even) interleave the two halves in the same
+ * order: row 2f is up row f, row 2f + 1 is gate row f (a weight stored as
+ * halves is interleaved once before w4a16_quantize; quantization is per row,
+ * so the packed codes and scales are the interleaved ones).  bias (optional)
+ * is [N] in the same interleaved order.  With y = A . dequant(packed,
+ * scales)^T + bias in fp32 (as w4a16_gemm, before its rounding):
+ *   Y[m, f] = bf16( silu(y[m, 2f + 1]) * y[m, 2f] ),  silu(g) = g / (1 + e^-g),
+ * computed in fp32 (expf), one rounding.  Y is [M, N/2] bf16.  Shape limits,
+ * packed layout, alignment and workspace rules are w4a16_gemm's; workspace
+ * bytes from w4a16_gemm_swiglu_workspace_bytes.  The variant is the one
+ * w4a16_select_variant gives unless that is a CUDA-core streaming variant
+ * (simt_*), whose epilogue has no SwiGLU form: then the rule's best tcgen05
+ * variant.  1 launch on `stream`.
+ */
+int w4a16_gemm_swiglu(const void* A_bf16, int64_t M, int64_t N, int64_t K, const void* packed,
+                      const void* scales, int group, const void* bias_bf16_or_null, void* Y_bf16,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace bytes w4a16_gemm_swiglu needs for this shape (may be 0). */
+size_t w4a16_gemm_swiglu_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+/* w4a16_gemm_swiglu with an explicit variant; W4A16_ERR_UNSUPPORTED for a
+ * CUDA-core streaming variant or a bad id, W4A16_ERR_NO_VARIANT if the
+ * variant cannot run the shape.  Otherwise the same contract. */
+int w4a16_gemm_swiglu_variant(int variant, const void* A_bf16, int64_t M, int64_t N, int64_t K,
+                              const void* packed, const void* scales, int group,
+                              const void* bias_bf16_or_null, void* Y_bf16, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
 /* ---------------------------------------------------------------- variants
  * The GEMM catalogue holds several kernel configurations (activation-tile
  * width, scaling mode, schedule).  The table maps a shape to one of them; it

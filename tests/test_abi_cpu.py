@@ -107,6 +107,23 @@ def test_fp4_argument_errors_before_any_launch(built_lib):
     assert L.fp4a16_gemm_workspace_bytes(5, 1, 256, 512) == 0
 
 
+def test_swiglu_argument_errors_before_any_launch(built_lib):
+    L = w4.lib()
+    names = [w4.w4a16_variant_name(i) for i in range(w4.w4a16_variant_count())]
+    args = (16, 4, 256, 512, 16, 16, 128, None, 16, None, 0, None)
+    simt = [i for i, n in enumerate(names) if n.startswith("simt_")]
+    assert simt
+    for v in simt:   # the streaming variants have no SwiGLU epilogue
+        assert L.w4a16_gemm_swiglu_variant(v, *args) == w4.W4A16_ERR_UNSUPPORTED
+    assert L.w4a16_gemm_swiglu_variant(len(names), *args) == w4.W4A16_ERR_UNSUPPORTED
+    assert L.w4a16_gemm_swiglu(16, 4, 250, 512, 16, 16, 128, None, 16, None, 0, None) == \
+        w4.W4A16_ERR_UNSUPPORTED
+    assert L.w4a16_gemm_swiglu(18, 4, 256, 512, 16, 16, 128, None, 16, None, 0, None) == \
+        w4.W4A16_ERR_ALIGNMENT
+    assert L.w4a16_gemm_swiglu(None, 4, 256, 512, 16, 16, 128, None, 16, None, 0, None) == \
+        w4.W4A16_ERR_INVALID_ARG
+
+
 def test_variant_catalogue_is_host_only(built_lib):
     n = w4.w4a16_variant_count()
     assert n >= 4

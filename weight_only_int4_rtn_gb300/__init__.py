@@ -105,6 +105,12 @@ SIGNATURES = [
     ("w4a16_gemm_variant", ctypes.c_int,
      [ctypes.c_int, _vp, _c_int64, _c_int64, _c_int64, _vp, _vp, ctypes.c_int, _vp, _vp, _vp,
       _c_size, _vp]),
+    ("w4a16_gemm_swiglu", ctypes.c_int,
+     [_vp, _c_int64, _c_int64, _c_int64, _vp, _vp, ctypes.c_int, _vp, _vp, _vp, _c_size, _vp]),
+    ("w4a16_gemm_swiglu_workspace_bytes", _c_size, [_c_int64, _c_int64, _c_int64]),
+    ("w4a16_gemm_swiglu_variant", ctypes.c_int,
+     [ctypes.c_int, _vp, _c_int64, _c_int64, _c_int64, _vp, _vp, ctypes.c_int, _vp, _vp, _vp,
+      _c_size, _vp]),
     ("w4a16_gemm_variant_f16", ctypes.c_int,
      [ctypes.c_int, _vp, _c_int64, _c_int64, _c_int64, _vp, _vp, ctypes.c_int, _vp, _vp, _vp,
       _c_size, _vp]),
@@ -307,6 +313,56 @@ def w4a16_gemm(A: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor,
         st = fn(variant, A.data_ptr(), M, N, K, packed.data_ptr(), scales.data_ptr(), group,
                 bias_ptr, Y.data_ptr(), ws_ptr, ws_bytes, sh)
     _check(st, "w4a16_gemm_f16" if f16 else "w4a16_gemm")
+    return Y
+
+
+def w4a16_gemm_swiglu(A: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor,
+                      bias: torch.Tensor | None = None, Y: torch.Tensor | None = None,
+                      workspace: torch.Tensor | None = None, group: int = GROUP, stream=None,
+                      variant: int | None = None) -> torch.Tensor:
+    """``Y[M, N/2] = silu(y[:, 1::2]) * y[:, 0::2]`` with ``y = A @
+    dequant(packed, scales)^T + bias`` in fp32 (bf16 A, bias and Y): the
+    weight's rows interleave up (even rows) and gate (odd rows).  ``variant``
+    forces one tcgen05 entry of the catalogue."""
+    _require_cuda(A, "A", torch.bfloat16)
+    _require_cuda(packed, "packed", torch.uint8)
+    _require_cuda(scales, "scales", torch.float16)
+    if A.dim() != 2 or scales.dim() != 2:
+        raise ValueError("A and scales must be 2-D")
+    M, K = A.shape
+    N = scales.shape[1]
+    if scales.shape[0] * group != K:
+        raise ValueError("scales must be [K/128, N]")
+    if N % 2 != 0:
+        raise ValueError("N must be even (interleaved up and gate rows)")
+    if packed.numel() != lib().w4a16_packed_bytes(N, K):
+        raise ValueError("packed must hold w4a16_packed_bytes(N, K) bytes of tiled codes")
+    if bias is not None:
+        _require_cuda(bias, "bias", torch.bfloat16)
+        if bias.numel() != N:
+            raise ValueError("bias must have N elements")
+    if Y is None:
+        Y = torch.empty((M, N // 2), dtype=torch.bfloat16, device=A.device)
+    _require_cuda(Y, "Y", torch.bfloat16)
+    if Y.shape != (M, N // 2):
+        raise ValueError("Y must be [M, N/2]")
+    sh = _stream_handle(A.device, stream)
+    L = lib()
+    need = (L.w4a16_gemm_swiglu_workspace_bytes(M, N, K) if variant is None
+            else L.w4a16_variant_workspace_bytes(variant, M, N, K))
+    if workspace is None:
+        workspace = _default_ws.get(A.device, sh, need)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    bias_ptr = bias.data_ptr() if bias is not None else None
+    if variant is None:
+        st = L.w4a16_gemm_swiglu(A.data_ptr(), M, N, K, packed.data_ptr(), scales.data_ptr(),
+                                 group, bias_ptr, Y.data_ptr(), ws_ptr, ws_bytes, sh)
+    else:
+        st = L.w4a16_gemm_swiglu_variant(variant, A.data_ptr(), M, N, K, packed.data_ptr(),
+                                         scales.data_ptr(), group, bias_ptr, Y.data_ptr(), ws_ptr,
+                                         ws_bytes, sh)
+    _check(st, "w4a16_gemm_swiglu")
     return Y
 
 

@@ -369,6 +369,29 @@ int select_variant(int64_t M, int64_t N, int64_t K) {
   return id;
 }
 
+// SwiGLU epilogue: the variant select_variant gives for the shape, unless it
+// is a CUDA-core streaming variant (whose epilogue does not pair rows); then
+// the rule over the tcgen05 variants.
+bool swiglu_ok(int id) { return id >= 0 && id < kNumVariants && !kVariants[id].cfg.simt; }
+
+int select_variant_swiglu(int64_t M, int64_t N, int64_t K) {
+  const int id = select_variant(M, N, K);
+  if (id < 0 || swiglu_ok(id)) return id;
+  DeviceInfo dev;
+  const int sms = device_info(dev) ? dev.num_sms : kDefaultSms;
+  int best = -1;
+  double best_t = 0.0;
+  for (int v = 0; v < kNumVariants; ++v) {
+    if (!swiglu_ok(v) || !variant_eligible(v, M, N, K)) continue;
+    const double t = estimate_us(kVariants[v], M, N, K, sms);
+    if (best < 0 || t < best_t) {
+      best = v;
+      best_t = t;
+    }
+  }
+  return best;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int check_gemm_args(const void* A, int64_t M, int64_t N, int64_t K, const void* packed,
@@ -387,7 +410,7 @@ int check_gemm_args(const void* A, int64_t M, int64_t N, int64_t K, const void* 
 int run_gemm_v(const Variant& v, const void* A, int64_t M, int64_t N, int64_t K,
                const void* packed, const void* scales, const void* bias, void* Y, void* ws,
                size_t ws_bytes, cudaStream_t stream, bool act_f16,
-               const float* tensor_scale = nullptr) {
+               const float* tensor_scale = nullptr, bool swiglu = false) {
   DeviceInfo dev;
   if (!device_info(dev)) return W4A16_ERR_CUDA;
   const GemmSchedule s = make_schedule(v, M, N, K, dev.num_sms);
@@ -411,6 +434,7 @@ int run_gemm_v(const Variant& v, const void* A, int64_t M, int64_t N, int64_t K,
   p.timeout_ns = g_timeout_ns.load();
   p.act_f16 = act_f16;
   p.tensor_scale = tensor_scale;
+  p.swiglu = swiglu;
   if (log_enabled())
     std::fprintf(stderr, "w4a16: gemm M=%lld N=%lld K=%lld variant=%s grid=%d dp_tiles=%d sk_units=%lld\n",
                  static_cast<long long>(M), static_cast<long long>(N), static_cast<long long>(K),
@@ -992,6 +1016,36 @@ int w4a16_gemm(const void* A_bf16, int64_t M, int64_t N, int64_t K, const void* 
   if (id < 0) return W4A16_ERR_NO_VARIANT;
   return run_gemm(id, A_bf16, M, N, K, packed, scales, bias_bf16_or_null, Y_bf16, workspace,
                   workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+size_t w4a16_gemm_swiglu_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  const int id = select_variant_swiglu(M, N, K);
+  if (id < 0) return 0;
+  return variant_ws(id, M, N, K);
+}
+
+int w4a16_gemm_swiglu_variant(int variant, const void* A_bf16, int64_t M, int64_t N, int64_t K,
+                              const void* packed, const void* scales, int group,
+                              const void* bias_bf16_or_null, void* Y_bf16, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  const int st = check_gemm_args(A_bf16, M, N, K, packed, scales, group, bias_bf16_or_null, Y_bf16);
+  if (st != W4A16_OK) return st;
+  if (!swiglu_ok(variant)) return W4A16_ERR_UNSUPPORTED;
+  if (!variant_eligible(variant, M, N, K)) return W4A16_ERR_NO_VARIANT;
+  return run_gemm_v(kVariants[variant], A_bf16, M, N, K, packed, scales, bias_bf16_or_null, Y_bf16,
+                    workspace, workspace_bytes, static_cast<cudaStream_t>(stream),
+                    /*act_f16=*/false, /*tensor_scale=*/nullptr, /*swiglu=*/true);
+}
+
+int w4a16_gemm_swiglu(const void* A_bf16, int64_t M, int64_t N, int64_t K, const void* packed,
+                      const void* scales, int group, const void* bias_bf16_or_null, void* Y_bf16,
+                      void* workspace, size_t workspace_bytes, void* stream) {
+  const int st = check_gemm_args(A_bf16, M, N, K, packed, scales, group, bias_bf16_or_null, Y_bf16);
+  if (st != W4A16_OK) return st;
+  const int id = select_variant_swiglu(M, N, K);
+  if (id < 0) return W4A16_ERR_NO_VARIANT;
+  return w4a16_gemm_swiglu_variant(id, A_bf16, M, N, K, packed, scales, group, bias_bf16_or_null,
+                                   Y_bf16, workspace, workspace_bytes, stream);
 }
 
 int w4a16_variant_count(void) { return kNumVariants; }

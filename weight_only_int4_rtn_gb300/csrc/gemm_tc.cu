@@ -64,6 +64,7 @@ cudaError_t launch_gemm_tc_group(const GemmKernelConfig& c, const GemmGroup& grp
   static_assert(kMaxGemmGroup == kMaxGroup, "group size of the kernel arguments");
   if (grp.count < 1 || grp.count > kMaxGroup) return cudaErrorInvalidValue;
   if (c.simt) return launch_gemv(c, grp, use_pdl, stream);
+  if (grp.p[0].swiglu) return launch_gemm_tc_swiglu(c, grp, use_pdl, stream);
   if (c.weight_format == kFmtInt8) return launch_gemm_tc_w8(c, grp, use_pdl, stream);
   if (c.weight_format == kFmtMxfp4) return launch_gemm_tc_mxfp4(c, grp, use_pdl, stream);
   if (c.weight_format == kFmtNvfp4) return launch_gemm_tc_nvfp4(c, grp, use_pdl, stream);

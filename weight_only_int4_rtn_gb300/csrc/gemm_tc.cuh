@@ -529,17 +529,55 @@ __device__ __forceinline__ void load_cols(uint32_t taddr, float (&v)[CNT]) {
   for (int j = 0; j < CNT; ++j) v[j] = __uint_as_float(r[j]);
 }
 
+// SwiGLU epilogue.  Weight rows 2f (up) and 2f + 1 (gate) are held by
+// adjacent lanes (a thread's weight row is its lane plus a multiple of 32).
+// swiglu_vals turns K final fp32 values y (bias added) of this lane's row into
+// silu(gate) * up = gate / (1 + e^-gate) * up with the neighbouring lane's
+// values as gate (meaningful on the lanes of even rows, which store them at
+// Y[m, f] of the [M, N/2] output), in fp32: the exponential and quotient by
+// the fast intrinsics, whose relative error, near 2^-21, is far below the
+// output's rounding.  All shuffles of a batch come before its arithmetic and
+// its stores, so the K chains overlap.  Every lane of the warp calls it.  The
+// epilogue is a template parameter (SW) of the kernel: the plain instances
+// compile none of it, so their code (and its instruction-cache footprint) is
+// unchanged.
+template <int K>
+__device__ __forceinline__ void swiglu_vals(float (&h)[K]) {
+  float g[K];
+#pragma unroll
+  for (int i = 0; i < K; ++i) g[i] = __shfl_xor_sync(0xFFFFFFFFu, h[i], 1);
+#pragma unroll
+  for (int i = 0; i < K; ++i) h[i] = __fdividef(g[i], 1.0f + __expf(-g[i])) * h[i];
+}
+
 // Write accumulator columns [col0, col0 + CNT) of this thread's weight row
-// either to Y (whole tile: bias added, one rounding to the output type) or to this CTA's
-// partial slot (fp32, no bias; column m of the slot holds 128 rows).
-template <int BA, int CNT, bool F16>
+// either to Y (whole tile: bias added, one rounding to the output type; or
+// the SwiGLU epilogue, swiglu_vals) or to this CTA's partial slot (fp32, no
+// bias; column m of the slot holds 128 rows).  Called by whole warps.
+template <int BA, int CNT, bool F16, bool SW>
 __device__ __forceinline__ void emit_cols(const Args& a, const Unit& u, int row, int col0,
                                           const float (&v)[CNT], float bias_n, int cta) {
   const int n0 = (u.tile % a.n_tiles) * kTileW;
   const int m0 = (u.tile / a.n_tiles) * BA;
   if (u.whole) {
     const int n = n0 + row;
-    if (n < a.N) {
+    if constexpr (SW) {
+      constexpr int kB = CNT < 8 ? CNT : 8;
+#pragma unroll
+      for (int j0 = 0; j0 < CNT; j0 += kB) {
+        float h[kB];
+#pragma unroll
+        for (int i = 0; i < kB; ++i) h[i] = v[j0 + i] + bias_n;
+        swiglu_vals(h);
+        if (n < a.N && (n & 1) == 0) {
+#pragma unroll
+          for (int i = 0; i < kB; ++i) {
+            const int m = m0 + col0 + j0 + i;
+            if (m < a.M) a.Y[static_cast<int64_t>(m) * (a.N >> 1) + (n >> 1)] = act_from_float<F16>(h[i]);
+          }
+        }
+      }
+    } else if (n < a.N) {
 #pragma unroll
       for (int j = 0; j < CNT; ++j) {
         const int m = m0 + col0 + j;
@@ -596,7 +634,7 @@ __device__ __forceinline__ bool readout_sync(Shared* sh, uint32_t& nsync, const 
 // the latency of loads that four warps alone keep too few of in flight.  (A
 // sum in the middle of a run stays with the readout warps, where it overlaps
 // the CTA's remaining units.)
-template <int BA, bool F16>
+template <int BA, bool F16, bool SW>
 __device__ bool split_fixup(const Args& a, const Unit& u, const SplitInfo& si, Shared* sh, int row,
                             float bias_n, uint32_t& nsync, const WaitCtx& wc, bool defer) {
   __threadfence();   // this thread's partial row is visible to the whole GPU
@@ -636,7 +674,23 @@ __device__ bool split_fixup(const Args& a, const Unit& u, const SplitInfo& si, S
 #pragma unroll
       for (int j = 0; j < 16; ++j) acc[j] += __ldcg(src + (c0 + j) * kTileW);
     }
-    if (n < a.N) {
+    if constexpr (SW) {
+#pragma unroll
+      for (int j0 = 0; j0 < 16; j0 += 8) {
+        float h[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) h[i] = acc[j0 + i] + bias_n;
+        swiglu_vals(h);
+        if (n < a.N && (n & 1) == 0) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            if (c0 + j0 + i < mcols)
+              a.Y[static_cast<int64_t>(m0 + c0 + j0 + i) * (a.N >> 1) + (n >> 1)] =
+                  act_from_float<F16>(h[i]);
+          }
+        }
+      }
+    } else if (n < a.N) {
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         if (c0 + j < mcols)
@@ -652,7 +706,7 @@ __device__ bool split_fixup(const Args& a, const Unit& u, const SplitInfo& si, S
 // t / 128 + P j (P = threads / 128) that hold activation rows, adding the
 // contributors' partials in the same k order as split_fixup (so the result is
 // the same bit for bit).  Up to 64 loads per thread are in flight.
-template <int BA, bool F16>
+template <int BA, bool F16, bool SW>
 __device__ void wide_fixup(const Args& a, const Shared* sh) {
   constexpr int P = kWarps * 32 / kTileW;
   constexpr int kCols = BA / P;                   // columns per thread
@@ -688,7 +742,19 @@ __device__ void wide_fixup(const Args& a, const Shared* sh) {
         if (col < mcols) acc[j] += __ldcg(src + col * kTileW);
       }
     }
-    if (n < a.N) {
+    if constexpr (SW) {
+      float h[kCh];
+#pragma unroll
+      for (int j = 0; j < kCh; ++j) h[j] = acc[j] + bias_n;
+      swiglu_vals(h);
+      if (n < a.N && (n & 1) == 0) {
+#pragma unroll
+        for (int j = 0; j < kCh; ++j) {
+          const int col = part + P * (j0 + j);
+          if (col < mcols) a.Y[static_cast<int64_t>(m0 + col) * (a.N >> 1) + (n >> 1)] = act_from_float<F16>(h[j]);
+        }
+      }
+    } else if (n < a.N) {
 #pragma unroll
       for (int j = 0; j < kCh; ++j) {
         const int col = part + P * (j0 + j);
@@ -698,7 +764,7 @@ __device__ void wide_fixup(const Args& a, const Shared* sh) {
   }
 }
 
-template <int BA, int L, bool GRP, int STAGES, int UG, int WF, bool F16, int G>
+template <int BA, int L, bool GRP, int STAGES, int UG, int WF, bool F16, int G, bool SW>
 __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG, WF>::kThreads, 1)
     w4a16_gemm_tc_kernel(const __grid_constant__ GroupArgs<G> g) {
   static_assert(WF == kFmtInt4 || !F16, "INT8 and FP4 weights with bf16 activations");
@@ -1089,9 +1155,9 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG, WF>::kThreads, 1)
       auto finish_unit = [&](int i) {
         first = false;
         if (--seg_left == 0) {
-          emit_cols<BA, BA, F16>(a, seg, row, 0, acc, bias_f, cta);
+          emit_cols<BA, BA, F16, SW>(a, seg, row, 0, acc, bias_f, cta);
           if (!seg.whole)
-            ok = split_fixup<BA, F16>(a, seg, si, sh, row, bias_f, nsync, wc, i + 1 == total);
+            ok = split_fixup<BA, F16, SW>(a, seg, si, sh, row, bias_f, nsync, wc, i + 1 == total);
           if (i + 1 < total) open_run();
         }
       };
@@ -1213,13 +1279,13 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG, WF>::kThreads, 1)
 #pragma unroll
             for (int c = 0; c < C::kChunk; ++c) v[c] *= g_t;
           }
-          emit_cols<BA, C::kChunk, F16>(a, u, row, c0, v, bias_f, cta);
+          emit_cols<BA, C::kChunk, F16, SW>(a, u, row, c0, v, bias_f, cta);
         }
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&sh->dempty[db]);
         if (!u.whole &&
-            !split_fixup<BA, F16>(a, u, split_info(a, u.sk_tile, ctas), sh, row, bias_f, nsync, wc,
+            !split_fixup<BA, F16, SW>(a, u, split_info(a, u.sk_tile, ctas), sh, row, bias_f, nsync, wc,
                                   i + 1 == total))
           break;
       }
@@ -1376,14 +1442,14 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG, WF>::kThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   if (warp == 1) ptx::tmem_dealloc(tmem, kTmemCols);
-  if (sh->fixup_defer) wide_fixup<BA, F16>(a, sh);
+  if (sh->fixup_defer) wide_fixup<BA, F16, SW>(a, sh);
   if (threadIdx.x == 32) W4A16_TRACE_POINT(11);
 }
 
-template <int BA, int L, bool GRP, int STAGES, int UG, int WF, bool F16, int G>
+template <int BA, int L, bool GRP, int STAGES, int UG, int WF, bool F16, int G, bool SW = false>
 cudaError_t launch_instance(const GemmGroup& grp, bool use_pdl, cudaStream_t stream) {
   using C = Cfg<BA, L, GRP, STAGES, UG, WF>;
-  auto kernel = w4a16_gemm_tc_kernel<BA, L, GRP, STAGES, UG, WF, F16, G>;
+  auto kernel = w4a16_gemm_tc_kernel<BA, L, GRP, STAGES, UG, WF, F16, G, SW>;
   if (grp.count < 1 || grp.count > G) return cudaErrorInvalidValue;
 
   int dev = 0;
@@ -1544,14 +1610,15 @@ cudaError_t launch_gemm_tc_w8_typed(const GemmKernelConfig& c, const GemmGroup& 
   return cudaErrorInvalidConfiguration;
 }
 
-// All compiled configurations of one activation type and group size.
-template <bool F16, int G>
+// All compiled configurations of one activation type and group size (SW:
+// the SwiGLU epilogue).
+template <bool F16, int G, bool SW = false>
 cudaError_t launch_gemm_tc_typed(const GemmKernelConfig& c, const GemmGroup& grp, bool use_pdl,
                                  cudaStream_t stream) {
 #define W4A16_LAUNCH_CASE(BA, L, GRP, ST, UG)                                    \
   if (c.act_tile == BA && c.lanes == L && c.group_scale == GRP && c.stages == ST && \
       c.unit_groups == UG && c.weight_format == kFmtInt4)                                    \
-    return launch_instance<BA, L, GRP, ST, UG, kFmtInt4, F16, G>(grp, use_pdl, stream);
+    return launch_instance<BA, L, GRP, ST, UG, kFmtInt4, F16, G, SW>(grp, use_pdl, stream);
   W4A16_GEMM_INSTANCES(W4A16_LAUNCH_CASE)
 #undef W4A16_LAUNCH_CASE
   return cudaErrorInvalidConfiguration;

@@ -363,6 +363,7 @@ cudaError_t launch_gemv_typed(const GemmProblem& p, const GemmSchedule& s, bool 
     attr_set[dev] = true;
   }
   if (p.M > MT || p.K % kUnitK != 0 || s.grid < 1) return cudaErrorInvalidValue;
+  if (p.swiglu) return cudaErrorInvalidValue;   // the fused epilogue is the tcgen05 path's
   GvArgs g{};
   Args& a = g.a;
   a.M = static_cast<int>(p.M);

@@ -99,6 +99,8 @@ struct GemmProblem {
   uint64_t timeout_ns;
   bool act_f16 = false;  // A, bias and Y are fp16 (else bf16)
   const float* tensor_scale = nullptr;   // NVFP4: the fp32 tensor scale g (device)
+  bool swiglu = false;   // SwiGLU epilogue: rows 2f (up) and 2f + 1 (gate) give
+                         // Y[M, N/2][f] = silu(gate) * up
 };
 
 // Number of tiles of a problem under a configuration.
@@ -150,6 +152,10 @@ cudaError_t launch_gemm_tc_group_bf16(const GemmKernelConfig& c, const GemmGroup
                                       bool use_pdl, cudaStream_t stream);
 cudaError_t launch_gemm_tc_group_f16(const GemmKernelConfig& c, const GemmGroup& grp,
                                      bool use_pdl, cudaStream_t stream);
+// The SwiGLU epilogue (gemm_tc_swiglu.cu): one problem, INT4 weights, bf16
+// activations.
+cudaError_t launch_gemm_tc_swiglu(const GemmKernelConfig& c, const GemmGroup& grp, bool use_pdl,
+                                  cudaStream_t stream);
 // INT8 weights (gemm_tc_w8.cu): one problem, bf16 activations.
 cudaError_t launch_gemm_tc_w8(const GemmKernelConfig& c, const GemmGroup& grp, bool use_pdl,
                               cudaStream_t stream);
