@@ -88,3 +88,37 @@ def _halves(y):
 def test_planted_mistakes_fail_a_pin(mutant):
     gemm_mutant = lambda a_bits, packed, scales: mutant(base.gemm(a_bits, packed, scales))
     assert not (_rational_points(mutant) and _hand_gemm(gemm_mutant))
+
+
+def _bias_only(gemm_swiglu):
+    # A = 0, so the pre-activation is the bias: (up0, gate0, up1, gate1) =
+    # (2, ln 3, 5, 0) gives h = (2 ln 3 * 3/4, 0)
+    w = np.zeros((4, 128), np.float32)
+    w[:, 0] = 7.0
+    packed, scales = oracle.quantize_f32(w)
+    a_bits = np.zeros((1, 128), np.uint16)
+    bias = np.array([2.0, LN3, 5.0, 0.0], np.float32)
+    bias_bits = (bias.view(np.uint32) >> 16).astype(np.uint16)     # bf16 (truncation)
+    b = (bias_bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    h = gemm_swiglu(a_bits, packed, scales, bias_bits)
+    want = np.array([[b[0] * b[1] / (1.0 + math.exp(-b[1])), 0.0]])
+    return h.shape == want.shape and np.allclose(h, want, rtol=1e-6, atol=1e-12)
+
+
+def test_bias_enters_before_swiglu():
+    assert _bias_only(oracle.gemm_swiglu)
+    # sigmoid(bf16(ln 3)) is within 1e-2 of 3/4: the bias pair is (up, gate)
+    b1 = float(((np.array([LN3], np.float32).view(np.uint32) >> 16) << 16).view(np.float32)[0])
+    assert abs(1.0 / (1.0 + math.exp(-b1)) - 0.75) < 1e-2
+
+
+@pytest.mark.parametrize("where", ["after", "halves"])
+def test_bias_mistakes_fail_the_pin(where):
+    def mutant(a_bits, packed, scales, bias_bits=None):
+        y = base.gemm(a_bits, packed, scales)
+        b = base.act_bits_to_f32(bias_bits, "bf16").astype(np.float64)
+        if where == "after":       # bias added to h instead of to y
+            return oracle.swiglu(y) + b[0::2][None, :]
+        F = b.size // 2            # bias read as [up | gate] halves
+        return oracle.swiglu(y + np.stack([b[:F], b[F:]], axis=1).reshape(-1)[None, :])
+    assert not _bias_only(mutant)
