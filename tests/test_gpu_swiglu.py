@@ -139,3 +139,36 @@ def test_workload_gate_up_shapes(w4, case):
     got = Y if rows is None else Y[torch.as_tensor(rows, device=Y.device)]
     check_swiglu_close(got, y_pre, what=case.name)
     assert w4.w4a16_get_device_error() == w4.W4A16_OK
+
+
+def test_graph_capture(w4):
+    """The SwiGLU call is capture-safe: a captured quantize + SwiGLU GEMM,
+    replayed, gives the eager result bit for bit."""
+    case = synthetic.Case("m50_capture", 50, 2048, 1024, 49, bias=True)
+    W, A, b = synthetic.draw(case)
+    Wd, Ad, bd = W.cuda(), A.cuda(), b.cuda()
+    p_e, s_e = w4.w4a16_quantize(Wd)
+    y_e = w4.w4a16_gemm_swiglu(Ad, p_e, s_e, bias=bd).clone()
+    torch.cuda.synchronize()
+    packed, scales = torch.zeros_like(p_e), torch.zeros_like(s_e)
+    Y = torch.empty_like(y_e)
+    ws = torch.zeros(max(w4.lib().w4a16_gemm_swiglu_workspace_bytes(case.M, case.N, case.K), 16),
+                     dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):          # warm-up outside capture
+        w4.w4a16_quantize(Wd, packed=packed, scales=scales)
+        w4.w4a16_gemm_swiglu(Ad, packed, scales, bias=bd, Y=Y, workspace=ws)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    packed.zero_(), scales.zero_(), Y.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        w4.w4a16_quantize(Wd, packed=packed, scales=scales)
+        w4.w4a16_gemm_swiglu(Ad, packed, scales, bias=bd, Y=Y, workspace=ws)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(packed, p_e) and torch.equal(scales, s_e)
+    assert torch.equal(Y.view(torch.int16), y_e.view(torch.int16))
+    assert w4.w4a16_get_device_error() == w4.W4A16_OK
