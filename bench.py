@@ -1,32 +1,33 @@
 #!/usr/bin/env python3
-"""Benchmark of the W4A16 hot path on GB300.
+"""Benchmark of the W4A16 GEMM on GB300.
 
-One step = one pass of the whole path over one batch of synthetic inputs:
-for every projection of the workload, RTN quantize/pack of its bf16 weight
-(w4a16_quantize) followed by the W4A16 GEMM (w4a16_gemm).  Default workload:
-the action-expert projections at M = 50 tokens, (N, K) = (2048, 1024),
-(1024, 1024), (8192, 1024), (1024, 4096), seeds 1..4.
+Metric: W4A16 GEMM TFLOP/s and weight-stream GB/s against the roofline over
+M = 1 .. 8192.  One step = one pass of the GEMM over one batch of synthetic
+inputs: the W4A16 GEMM of every projection of the workload, on INT4 weights
+that were RTN-quantized at load and stay resident in HBM (one grouped launch
+when the workload has 2 .. 8 projections).  The quantize/pack is load-time
+work: it is timed apart and reported under `kernels`, outside the step.
+
+Default workload: `large` (M = N = K = 8192), the compute-bound end of the
+metric's M range; `value` is its GEMM TFLOP/s.  The same line carries
+`sweep`: the bandwidth-bound end (M in {1, 4, 16, 64} x (N, K) in {(16384,
+2048), (2048, 16384), (8192, 8192)}), every shape's GEMM alone, back to back,
+with its weight GB/s and roofline fraction.
 
 Timing: the steps are captured into CUDA graphs (the library's calls are
 capture-safe), so no host launch overhead sits between kernels.  W untimed
 warm-up steps replay first, then exactly K timed steps replay between CUDA
-events on the launching stream, with a device synchronize (and, for N > 1,
-a barrier) on both sides; the max over ranks is reported.  Every step reads
-a different copy of all inputs and the copies together exceed 3x the L2
-size, so each step streams its inputs from HBM.  Kernel durations for the
-roofline come from a second replay of the same K steps with CUDA events
-recorded around each launch on the same stream.  The e2e figure is the
-eager public API (no graph) with pinned host inputs copied in and results
-copied out every step.
-
-`value` is whole-job algorithmic HBM bytes per second (GB/s): for each
-quantize 2.515625 * N * K bytes (bf16 read, codes and scales written), for
-each GEMM 0.515625 * N * K + 2 * M * K bytes (packed weight, scales and
-activations read).  GEMM TFLOP/s and weight-stream GB/s are reported per
-kernel alongside.
+events on the launching stream, with a device synchronize (and, for N > 1, a
+barrier) on both sides; the max over ranks is reported.  Every step reads a
+different copy of the weights and activations, and the copies together
+exceed 3x the L2 size, so each step streams its inputs from HBM.  SM clocks
+and throttle reasons are sampled during the timed region (NVML, read only).
+The e2e figure is the same steps through the public API with the
+activations copied in from pinned host memory and the outputs copied back,
+every step.
 
 --impl reference times the CPU oracle (test infrastructure, never the
-product path) on a bounded sample of the same workload.
+product path) on a bounded sample of the same workload, in the same unit.
 Multi-GPU: the path is replicated (each rank runs the whole workload on its
 own GPU); there is no collective on the data path.
 """
@@ -138,34 +139,91 @@ def dram_traffic(kernel: str, workload: str):
 
 
 class ClockSampler:
-    """Samples nvidia-smi SM clocks and throttle reasons every 200 ms."""
+    """SM clocks and throttle reasons of one GPU, sampled every 2 ms while
+    the context is open: NVML through ctypes (read-only queries; the device
+    found by its PCI bus id), else nvidia-smi every 200 ms."""
 
+    NVML_CLOCK_SM = 1
+    REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown",
+               0x4: "sw_power_cap", 0x80: "hw_power_brake_slowdown"}
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int):
-        self.index = index
-        self.samples = []
+    def __init__(self, device):
+        self.device = device
+        self.samples = []          # (host time, sm_mhz, max_mhz, {reason names})
+        self.window = None         # host-time window of the timed region
+        self.source = None
         self._stop = threading.Event()
         self._t = None
+        self._nvml = None
+        self._handle = None
+
+    def _open_nvml(self):
+        import ctypes
+        import torch
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return False
+            p = torch.cuda.get_device_properties(self.device)
+            bus = "%08X:%02X:%02X.0" % (getattr(p, "pci_domain_id", 0), p.pci_bus_id,
+                                        p.pci_device_id)
+            h = ctypes.c_void_p()
+            if nv.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)) != 0:
+                return False
+            self._nvml, self._handle = nv, h
+            return True
+        except Exception:
+            return False
+
+    def _sample_nvml(self):
+        import ctypes
+        nv, h = self._nvml, self._handle
+        clk, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        if nv.nvmlDeviceGetClockInfo(h, self.NVML_CLOCK_SM, ctypes.byref(clk)) != 0:
+            return
+        nv.nvmlDeviceGetMaxClockInfo(h, self.NVML_CLOCK_SM, ctypes.byref(mx))
+        fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        fn(h, ctypes.byref(rs))
+        names = {n for bit, n in self.REASONS.items() if rs.value & bit}
+        self.samples.append((time.perf_counter(), float(clk.value), float(mx.value), names))
+
+    def _sample_smi(self):
+        out = subprocess.run(
+            ["nvidia-smi", "-i", str(self.device.index), f"--query-gpu={self.FIELDS}",
+             "--format=csv,noheader,nounits"], capture_output=True, text=True, timeout=5)
+        if out.returncode == 0 and out.stdout.strip():
+            s = [x.strip() for x in out.stdout.strip().split(",")]
+            if s[0].replace(".", "").isdigit() and s[1].replace(".", "").isdigit():
+                names = {n for n, v in zip(["hw_slowdown", "hw_thermal_slowdown",
+                                            "sw_thermal_slowdown", "sw_power_cap"], s[4:8])
+                         if v.strip().lower() == "active"}
+                self.samples.append((time.perf_counter(), float(s[0]), float(s[1]), names))
 
     def _run(self):
+        use_nvml = self._open_nvml()
+        self.source = "nvml" if use_nvml else "nvidia-smi"
         while not self._stop.is_set():
             try:
-                out = subprocess.run(
-                    ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                     "--format=csv,noheader,nounits"], capture_output=True, text=True, timeout=5)
-                if out.returncode == 0 and out.stdout.strip():
-                    self.samples.append([x.strip() for x in out.stdout.strip().split(",")])
+                self._sample_nvml() if use_nvml else self._sample_smi()
             except Exception:
                 pass
-            self._stop.wait(0.2)
+            self._stop.wait(0.002 if use_nvml else 0.2)
 
     def __enter__(self):
         self._t = threading.Thread(target=self._run, daemon=True)
         self._t.start()
+        time.sleep(0.05)   # sampling runs before the timed region starts
         return self
+
+    def mark(self, t0, t1):
+        """The timed region's host-time window; summary() keeps the samples
+        inside it (and the one just before it, so a very short region still
+        has one)."""
+        self.window = (t0, t1)
 
     def __exit__(self, *exc):
         self._stop.set()
@@ -173,24 +231,163 @@ class ClockSampler:
             self._t.join(timeout=10)
 
     def summary(self):
-        if not self.samples:
+        samples = self.samples
+        if self.window is not None:
+            t0, t1 = self.window
+            before = [s for s in samples if s[0] < t0][-1:]
+            samples = before + [s for s in samples if t0 <= s[0] <= t1]
+        if not samples:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        sm = [float(s[0]) for s in self.samples if s[0].replace(".", "").isdigit()]
-        mx = [float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()]
         reasons = set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for s in self.samples:
-            for name, v in zip(names, s[4:8]):
-                if v.strip().lower() == "active":
-                    reasons.add(name)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(self.samples)}
+        for s in samples:
+            reasons |= s[3]
+        return {"sm_mhz": statistics.median(s[1] for s in samples),
+                "sm_max_mhz": max(s[2] for s in samples),
+                "reasons": sorted(reasons), "samples": len(samples), "source": self.source}
 
 
 # ------------------------------------------------------------- GPU arm
+class Formats:
+    """The calls of one weight scheme (INT4, INT8, MXFP4, NVFP4) through the
+    binding: quantize (load time), GEMM (the step), variant names."""
+
+    def __init__(self, w4, fmt, act, sr_seed, dev):
+        import torch
+        self.w4, self.fmt, self.act, self.sr_seed, self.dev = w4, fmt, act, sr_seed, dev
+        self.int8 = fmt == "int8"
+        self.fp4 = fmt in ("mxfp4", "nvfp4")
+        self.act_dtype = torch.float16 if act == "f16" else torch.bfloat16
+        self.qname = {"int4": "rtn_quantize" if sr_seed is None else "sr_quantize",
+                      "int8": "rtn_quantize_int8", "mxfp4": "quantize_mxfp4",
+                      "nvfp4": "quantize_nvfp4"}[fmt]
+        self.gname = {"int4": "w4a16_gemm_tc", "int8": "w8a16_gemm_tc", "mxfp4": "mxfp4_gemm_tc",
+                      "nvfp4": "nvfp4_gemm_tc"}[fmt]
+
+    def packed_bytes(self, N, K):
+        L = self.w4.lib()
+        return L.w8a16_packed_bytes(N, K) if self.int8 else self.w4.w4a16_packed_bytes(N, K)
+
+    def new_weight(self, N, K):
+        """Empty (packed, scales, tensor scale) buffers of an [N, K] weight."""
+        import torch
+        packed = torch.empty(self.packed_bytes(N, K), dtype=torch.uint8, device=self.dev)
+        if self.fp4:
+            scales = torch.empty(K // (32 if self.fmt == "mxfp4" else 16), N, dtype=torch.uint8,
+                                 device=self.dev)
+        else:
+            scales = torch.empty(K // 128, N, dtype=torch.float16, device=self.dev)
+        ts = torch.zeros(2, dtype=torch.float32, device=self.dev)
+        return dict(packed=packed, scales=scales, ts=ts)
+
+    def quantize(self, W, wt, st=None):
+        w4 = self.w4
+        if self.int8:
+            w4.w8a16_quantize(W, packed=wt["packed"], scales=wt["scales"], stream=st)
+        elif self.fp4:
+            w4.fp4a16_quantize(W, self.fmt, packed=wt["packed"], scales=wt["scales"],
+                               tensor_scale=wt["ts"], stream=st)
+        else:
+            w4.w4a16_quantize(W, packed=wt["packed"], scales=wt["scales"], stream=st,
+                              seed=self.sr_seed)
+
+    def gemm(self, A, wt, Y, ws, st=None):
+        w4 = self.w4
+        if self.int8:
+            w4.w8a16_gemm(A, wt["packed"], wt["scales"], Y=Y, workspace=ws, stream=st)
+        elif self.fp4:
+            w4.fp4a16_gemm(A, wt["packed"], wt["scales"], self.fmt, tensor_scale=wt["ts"], Y=Y,
+                           workspace=ws, stream=st)
+        else:
+            w4.w4a16_gemm(A, wt["packed"], wt["scales"], Y=Y, workspace=ws, stream=st)
+
+    def workspace_bytes(self, M, N, K):
+        L = self.w4.lib()
+        if self.int8:
+            return L.w8a16_gemm_workspace_bytes(M, N, K)
+        if self.fp4:
+            return L.fp4a16_gemm_workspace_bytes(self.w4.FP4_FORMATS[self.fmt], M, N, K)
+        return self.w4.w4a16_gemm_workspace_bytes_max(M, N, K)
+
+    def variant(self, M, N, K):
+        w4 = self.w4
+        if self.int8:
+            L = w4.lib()
+            return L.w8a16_variant_name(L.w8a16_select_variant(M, N, K)).decode()
+        if self.fp4:
+            return w4.fp4a16_variant_name(w4.fp4a16_select_variant(M, N, K))
+        return w4.w4a16_variant_name(w4.w4a16_select_variant(M, N, K))
+
+
+def graph_of(dev, fn, n):
+    """A CUDA graph of n calls fn(i, stream), captured on a side stream."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    cs = torch.cuda.Stream(dev)
+    cs.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(cs):
+        with torch.cuda.graph(g, stream=cs):
+            for i in range(n):
+                fn(i, cs)
+    torch.cuda.current_stream(dev).wait_stream(cs)
+    return g
+
+
+def time_graph_us(dev, g, reps):
+    """Device time per call of a replayed graph of `reps` calls (CUDA events
+    on the current stream, after one untimed replay)."""
+    import torch
+    stream = torch.cuda.current_stream(dev)
+    g.replay()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    return e0.elapsed_time(e1) / reps * 1e3
+
+
+def back_to_back(fx, c, peaks, wcache, tune, dev):
+    """One GEMM shape alone: a CUDA graph of back-to-back launches on weight
+    copies that rotate through more than 3x L2 (SURVEY's timing method), no
+    other kernel in between, against the roofline of the shape."""
+    import torch
+
+    from weight_only_int4_rtn_gb300 import synthetic
+    w4 = fx.w4
+    if tune and fx.fmt == "int4":
+        w4.w4a16_tune(c.M, c.N, c.K)
+    key = (c.N, c.K, c.seed, c.wdist)
+    if key not in wcache:
+        wcache.clear()
+        W = synthetic.draw_weight_only(c.seed, c.N, c.K, c.wdist).to(dev)
+        wt = fx.new_weight(c.N, c.K)
+        fx.quantize(W, wt)
+        del W
+        wcache[key] = wt
+    wt = wcache[key]
+    _, A, _ = synthetic.draw(c, act=fx.act)
+    A = A.to(dev)
+    Y = torch.empty(c.M, c.N, dtype=fx.act_dtype, device=dev)
+    nb = sum(t.numel() * t.element_size() for t in (wt["packed"], wt["scales"]))
+    ncp = max(1, min(16, -(-3 * L2_BYTES // nb)))
+    cps = [wt] + [{k: v.clone() for k, v in wt.items()} for _ in range(ncp - 1)]
+    ws = torch.zeros(max(fx.workspace_bytes(c.M, c.N, c.K), 256), dtype=torch.uint8, device=dev)
+    reps = max(8, 2 * ncp)
+    for i in range(2):   # kernel attributes are set outside the capture
+        fx.gemm(A, cps[i % ncp], Y, ws)
+    g = graph_of(dev, lambda i, st: fx.gemm(A, cps[i % ncp], Y, ws, st), reps)
+    us = time_graph_us(dev, g, reps)
+    t_hbm = gemm_bytes(c.M, c.N, c.K, fx.fmt) / (peaks["hbm_gbs"] * 1e9) * 1e6
+    t_tc = gemm_flops(c.M, c.N, c.K) / (peaks["bf16_tflops"] * 1e12) * 1e6
+    del g, cps, ws
+    return dict(shape=[c.M, c.N, c.K], variant=fx.variant(c.M, c.N, c.K), us=round(us, 3),
+                weight_gbs=round(weight_bytes(c.N, c.K, fx.fmt) / (us * 1e-6) / 1e9, 1),
+                tflops=round(gemm_flops(c.M, c.N, c.K) / (us * 1e-6) / 1e12, 2),
+                bound="hbm" if t_hbm >= t_tc else "tensor",
+                roofline_frac=round(max(t_hbm, t_tc) / us, 4), weight_copies=ncp)
+
+
 def run_gpu(args, rank, world):
-    import numpy as np
     import torch
 
     import weight_only_int4_rtn_gb300 as w4
@@ -199,185 +396,97 @@ def run_gpu(args, rank, world):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
     torch.cuda.set_device(dev)
     cases = synthetic.WORKLOADS[args.workload]
+    fmt = args.weights
+    fx = Formats(w4, fmt, args.act, args.sr_seed, dev)
+    if fmt != "int4" and (args.grouped or args.act != "bf16"):
+        raise SystemExit(f"--weights {fmt}: bf16 activations, one launch per projection")
     if args.grouped is None:
-        # the projections are independent problems: one grouped launch of
-        # each kind per step when they fit one launch (the grouped quantize
-        # rounds to nearest)
-        args.grouped = len(cases) <= w4.MAX_GROUP and args.sr_seed is None and args.weights == "int4"
+        # the projections are independent problems: one grouped GEMM launch
+        # per step when they fit one launch (INT4 weights)
+        args.grouped = len(cases) > 1 and len(cases) <= w4.MAX_GROUP and fmt == "int4"
     if args.grouped and len(cases) > w4.MAX_GROUP:
         raise SystemExit(f"--grouped takes at most {w4.MAX_GROUP} projections")
-    if args.grouped and args.sr_seed is not None:
-        raise SystemExit("--sr-seed quantizes per projection (no --grouped)")
-    fmt = args.weights
-    int8 = fmt == "int8"
-    fp4 = fmt in ("mxfp4", "nvfp4")
-    if fmt != "int4" and (args.grouped or args.sr_seed is not None or args.act != "bf16"):
-        raise SystemExit(f"--weights {fmt}: bf16 activations, per projection, round to nearest")
-    qname = {"int4": "rtn_quantize" if args.sr_seed is None else "sr_quantize",
-             "int8": "rtn_quantize_int8", "mxfp4": "quantize_mxfp4", "nvfp4": "quantize_nvfp4"}[fmt]
-    gname = {"int4": "w4a16_gemm_tc", "int8": "w8a16_gemm_tc", "mxfp4": "mxfp4_gemm_tc",
-             "nvfp4": "nvfp4_gemm_tc"}[fmt]
-    packed_bytes = w4.lib().w8a16_packed_bytes if int8 else w4.w4a16_packed_bytes
+    peaks = load_peaks()
 
-    def scales_like(c):
-        if fp4:
-            return torch.empty(c.K // (32 if fmt == "mxfp4" else 16), c.N, dtype=torch.uint8,
-                               device=dev)
-        return torch.empty(c.K // 128, c.N, dtype=torch.float16, device=dev)
-
-    def quantize_one(s, st):
-        if int8:
-            w4.w8a16_quantize(s["W"], packed=s["packed"], scales=s["scales"], stream=st)
-        elif fp4:
-            w4.fp4a16_quantize(s["W"], fmt, packed=s["packed"], scales=s["scales"],
-                               tensor_scale=s["ts"], stream=st)
-        else:
-            w4.w4a16_quantize(s["W"], packed=s["packed"], scales=s["scales"], stream=st,
-                              seed=args.sr_seed)
-
-    def gemm_one(A, packed, scales, Y, st, workspace, ts=None):
-        if int8:
-            w4.w8a16_gemm(A, packed, scales, Y=Y, workspace=workspace, stream=st)
-        elif fp4:
-            w4.fp4a16_gemm(A, packed, scales, fmt, tensor_scale=ts, Y=Y, workspace=workspace,
-                           stream=st)
-        else:
-            w4.w4a16_gemm(A, packed, scales, Y=Y, workspace=workspace, stream=st)
-
-    def variant_of(c):
-        if int8:
-            return w4.lib().w8a16_variant_name(w4.lib().w8a16_select_variant(c.M, c.N, c.K)).decode()
-        if fp4:
-            return w4.fp4a16_variant_name(w4.fp4a16_select_variant(c.M, c.N, c.K))
-        return w4.w4a16_variant_name(w4.w4a16_select_variant(c.M, c.N, c.K))
-
-    if args.tune and fmt != "int4":
+    # --- kernel choice by measurement, once per shape (or per set of shapes
+    # of a grouped launch), outside the timed region
+    if fmt != "int4":
         args.tune = False   # the INT8 and FP4 catalogues are chosen by the cost model
     shapes = [(c.M, c.N, c.K) for c in cases]
-    if args.tune and args.tune_file and os.path.exists(args.tune_file):
-        # replay choices an earlier run made by measurement (for profiling:
-        # a profiler distorts the tuners' own timings)
-        with open(args.tune_file) as f:
-            saved = json.load(f)
-        for (M, N, K), v in saved.get("table", []):
-            w4.w4a16_table_set(M, N, K, v)
-        if args.grouped and saved.get("group") is not None:
-            w4.w4a16_set_grouped_variant(shapes, saved["group"])
-    elif args.tune:
-        # kernel choice by measurement, once per shape (or per set of shapes
-        # of a grouped launch), outside the timed region; later calls use the
-        # memoized choice
-        saved = {"table": [], "group": None}
+    if args.tune:
         if args.grouped:
-            saved["group"] = w4.w4a16_tune_grouped(
-                shapes, act=torch.float16 if args.act == "f16" else torch.bfloat16)
+            w4.w4a16_tune_grouped(shapes, act=fx.act_dtype)
         else:
             for c in cases:
-                saved["table"].append([[c.M, c.N, c.K], w4.w4a16_tune(c.M, c.N, c.K)])
-        if args.tune_file:
-            with open(args.tune_file, "w") as f:
-                json.dump(saved, f)
+                w4.w4a16_tune(c.M, c.N, c.K)
 
-    # one set of inputs per copy; the copies rotate step by step
-    per_copy = sum(2 * c.N * c.K + c.N * c.K // 2 + 2 * c.N * c.K // 128 + 2 * c.M * c.K +
-                   2 * c.M * c.N for c in cases)
-    copies = max(1, min(64, -(-3 * L2_BYTES // per_copy)))
-    host_sets = [synthetic.draw(c, act=args.act) for c in cases]
-    act_dtype = torch.float16 if args.act == "f16" else torch.bfloat16
+    # --- resident inputs: the weights are quantized at load (once per copy);
+    # the copies rotate step by step so that every step reads its weights and
+    # activations from HBM (more than 3x L2 in total)
+    host = [synthetic.draw(c, act=args.act) for c in cases]
+    in_bytes = sum(gemm_bytes(c.M, c.N, c.K, fmt) for c in cases)
+    copies = max(2, min(64, -(-3 * L2_BYTES // int(in_bytes))))
+    W_dev = [W.to(dev) for (W, _, _) in host]
     sets = []
     for r in range(copies):
         s = []
-        for c, (W, A, b) in zip(cases, host_sets):
-            Wd = W.to(dev) if r == 0 else sets[0][len(s)]["W"].clone()
-            Ad = A.to(dev) if r == 0 else sets[0][len(s)]["A"].clone()
-            s.append(dict(W=Wd, A=Ad,
-                          packed=torch.empty(packed_bytes(c.N, c.K), dtype=torch.uint8,
-                                             device=dev),
-                          scales=scales_like(c),
-                          ts=torch.zeros(2, dtype=torch.float32, device=dev),
-                          Y=torch.empty(c.M, c.N, dtype=act_dtype, device=dev)))
+        for j, c in enumerate(cases):
+            wt = fx.new_weight(c.N, c.K)
+            fx.quantize(W_dev[j], wt)
+            s.append(dict(wt=wt, A=host[j][1].to(dev),
+                          Y=torch.empty(c.M, c.N, dtype=fx.act_dtype, device=dev)))
         sets.append(s)
-    ws_bytes = max((w4.lib().w8a16_gemm_workspace_bytes(c.M, c.N, c.K) if int8 else
-                    w4.lib().fp4a16_gemm_workspace_bytes(w4.FP4_FORMATS[fmt], c.M, c.N, c.K) if fp4
-                    else w4.w4a16_gemm_workspace_bytes_max(c.M, c.N, c.K)) for c in cases)
+    torch.cuda.synchronize(dev)
+    ws_bytes = max(fx.workspace_bytes(c.M, c.N, c.K) for c in cases)
     if args.grouped:
-        probs, _, _ = w4._gemm_problems([s["A"] for s in sets[0]], [s["packed"] for s in sets[0]],
-                                        [s["scales"] for s in sets[0]], None,
+        probs, _, _ = w4._gemm_problems([s["A"] for s in sets[0]],
+                                        [s["wt"]["packed"] for s in sets[0]],
+                                        [s["wt"]["scales"] for s in sets[0]], None,
                                         [s["Y"] for s in sets[0]])
         ws_bytes = max(ws_bytes, w4.lib().w4a16_gemm_grouped_workspace_bytes(probs, len(cases), -1))
     ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    n_k = 2 if args.grouped else 2 * len(cases)
-
-    def run_step(r, st, evs):
-        """One step on stream `st`: per projection quantize then GEMM, or
-        (--grouped) one grouped quantize then one grouped GEMM."""
+    def step(r, st, evs=None):
+        """One step: the GEMM of every projection on copy r % copies (one
+        grouped launch, or one launch per projection)."""
+        sset = sets[r % copies]
         if args.grouped:
-            sset = sets[r % copies]
             if evs is not None:
                 evs[0][0].record(st)
-            w4.w4a16_quantize_grouped([s["W"] for s in sset],
-                                      outs=[(s["packed"], s["scales"]) for s in sset], stream=st)
-            if evs is not None:
-                evs[0][1].record(st)
-                evs[1][0].record(st)
-            w4.w4a16_gemm_grouped([s["A"] for s in sset], [s["packed"] for s in sset],
-                                  [s["scales"] for s in sset], Ys=[s["Y"] for s in sset],
+            w4.w4a16_gemm_grouped([s["A"] for s in sset], [s["wt"]["packed"] for s in sset],
+                                  [s["wt"]["scales"] for s in sset], Ys=[s["Y"] for s in sset],
                                   workspace=ws, stream=st)
             if evs is not None:
-                evs[1][1].record(st)
+                evs[0][1].record(st)
             return
-        for j, c in enumerate(cases):
-            s = sets[r % copies][j]
+        for j, s in enumerate(sset):
             if evs is not None:
-                evs[2 * j][0].record(st)
-            quantize_one(s, st)
+                evs[j][0].record(st)
+            fx.gemm(s["A"], s["wt"], s["Y"], ws, st)
             if evs is not None:
-                evs[2 * j][1].record(st)
-                evs[2 * j + 1][0].record(st)
-            gemm_one(s["A"], s["packed"], s["scales"], s["Y"], st, ws, s["ts"])
-            if evs is not None:
-                evs[2 * j + 1][1].record(st)
+                evs[j][1].record(st)
 
-    def step(r, evs=None):
-        run_step(r, stream, evs)
-
+    n_launch = 1 if args.grouped else len(cases)
     # eager warm-up (also sets kernel attributes outside any capture)
     for r in range(min(args.warmup, copies)):
-        step(r)
+        step(r, stream)
     torch.cuda.synchronize(dev)
     if w4.w4a16_get_device_error() != w4.W4A16_OK:
         raise RuntimeError("device error during warm-up")
 
-    # The timed steps run as one CUDA graph (no host launch overhead between
-    # kernels): graph A holds warm-up + timed steps back to back; graph B is
-    # the same steps with timing events around every kernel.
-    def capture(n_steps, first, with_events):
-        evs = None
-        if with_events:
-            evs = [[[torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
-                    for _ in range(n_k)] for _ in range(n_steps)]
-        g = torch.cuda.CUDAGraph()
-        cap_stream = torch.cuda.Stream(dev)
-        cap_stream.wait_stream(torch.cuda.current_stream(dev))
-        l0 = w4.w4a16_launch_count()
-        with torch.cuda.stream(cap_stream):
-            with torch.cuda.graph(g, stream=cap_stream):
-                for r in range(n_steps):
-                    step_on(first + r, cap_stream, None if evs is None else evs[r])
-        torch.cuda.current_stream(dev).wait_stream(cap_stream)
-        return g, evs, w4.w4a16_launch_count() - l0
-
-    def step_on(r, st, evs):
-        run_step(r, st, evs)
-
-    g_warm, _, _ = capture(args.warmup, 0, False)
-    g_timed, _, launches_per_replay = capture(args.steps, args.warmup, False)
+    # graph A: warm-up steps; graph B: the timed steps back to back; graph C:
+    # the same steps with events around every launch (per-launch durations)
+    g_warm = graph_of(dev, lambda i, st: step(i, st), args.warmup)
+    l0 = w4.w4a16_launch_count()
+    g_timed = graph_of(dev, lambda i, st: step(args.warmup + i, st), args.steps)
+    launches = w4.w4a16_launch_count() - l0
+    kev = [[[torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
+            for _ in range(n_launch)] for _ in range(args.steps)]
     try:
-        g_ev, kev, _ = capture(args.steps, args.warmup, True)
-    except TypeError:
-        g_ev, kev = None, None
+        g_ev = graph_of(dev, lambda i, st: step(args.warmup + i, st, kev[i]), args.steps)
+    except (TypeError, RuntimeError):
+        g_ev = None
 
     def barrier():
         if world > 1:
@@ -389,70 +498,64 @@ def run_gpu(args, rank, world):
     g_warm.replay()
     barrier()
     torch.cuda.synchronize(dev)
-    with ClockSampler(dev.index) as clk:
-        # the NVTX range marks the timed steps for profilers (ncu --nvtx
-        # --nvtx-include "bench_timed/" captures only these kernels)
+    with ClockSampler(dev) as clk:
+        # the NVTX range marks the timed steps for profilers
         torch.cuda.nvtx.range_push("bench_timed")
+        t0 = time.perf_counter()
         start.record(stream)
         g_timed.replay()
         end.record(stream)
         torch.cuda.synchronize(dev)
+        clk.mark(t0, time.perf_counter())
         torch.cuda.nvtx.range_pop()
     barrier()
-    launches = launches_per_replay
     elapsed_ms = start.elapsed_time(end)
 
-    # --- per-kernel durations: the same steps with events around each kernel
-    if g_ev is not None:
+    # --- per-launch durations (one launch per step: the timed region itself)
+    if n_launch == 1:
+        launch_ms = [elapsed_ms / args.steps]
+    elif g_ev is not None:
         g_warm.replay()
         g_ev.replay()
         torch.cuda.synchronize(dev)
-        kern_ms = [statistics.mean(kev[r][k][0].elapsed_time(kev[r][k][1]) for r in range(args.steps))
-                   for k in range(n_k)]
+        launch_ms = [statistics.mean(kev[r][j][0].elapsed_time(kev[r][j][1])
+                                     for r in range(args.steps)) for j in range(n_launch)]
     else:
-        kern_ms = []
-        for k in range(n_k):
-            gk = torch.cuda.CUDAGraph()
-            j, is_gemm = divmod(k, 2)
-            with torch.cuda.graph(gk):
-                for r in range(args.steps):
-                    sset = sets[(args.warmup + r) % copies]
-                    if args.grouped and is_gemm:
-                        w4.w4a16_gemm_grouped([s["A"] for s in sset], [s["packed"] for s in sset],
-                                              [s["scales"] for s in sset], Ys=[s["Y"] for s in sset],
-                                              workspace=ws)
-                    elif args.grouped:
-                        w4.w4a16_quantize_grouped([s["W"] for s in sset],
-                                                  outs=[(s["packed"], s["scales"]) for s in sset])
-                    elif is_gemm:
-                        s = sset[j]
-                        gemm_one(s["A"], s["packed"], s["scales"], s["Y"], None, ws, s["ts"])
-                    else:
-                        quantize_one(sset[j], None)
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            gk.replay()
-            e0.record(stream)
-            gk.replay()
-            e1.record(stream)
-            torch.cuda.synchronize(dev)
-            kern_ms.append(e0.elapsed_time(e1) / args.steps)
+        launch_ms = [elapsed_ms / args.steps / n_launch] * n_launch
     if w4.w4a16_get_device_error() != w4.W4A16_OK:
         raise RuntimeError("device error during timing")
 
-    # --- e2e: pinned host inputs -> device, the path, result -> host
-    pinned = [(W.pin_memory(), A.pin_memory()) for (W, A, b) in host_sets]
-    yh = [torch.empty(c.M, c.N, dtype=act_dtype).pin_memory() for c in cases]
-    h2d = sum(W.numel() * 2 + A.numel() * 2 for W, A in pinned)
-    d2h = sum(c.M * c.N * 2 for c in cases)
+    # --- the load-time quantize, timed apart: a graph of back-to-back
+    # launches (grouped over the projections when the step is grouped) on
+    # the resident bf16 weights
+    qreps = max(4, min(args.steps, 20))
+    if args.grouped:
+        qouts = [(s["wt"]["packed"], s["wt"]["scales"]) for s in sets[0]]
+        w4.w4a16_quantize_grouped(W_dev, outs=qouts)
+        gq = graph_of(dev, lambda i, st: w4.w4a16_quantize_grouped(W_dev, outs=qouts, stream=st),
+                      qreps)
+        q_us = [time_graph_us(dev, gq, qreps)]
+    else:
+        q_us = []
+        for j, c in enumerate(cases):
+            gq = graph_of(dev, lambda i, st: fx.quantize(W_dev[j], sets[0][j]["wt"], st), qreps)
+            q_us.append(time_graph_us(dev, gq, qreps))
+    del gq
+
+    # --- e2e: the public API on host buffers: pinned activations copied in,
+    # the step's GEMMs on the resident weights, the outputs copied back
+    a_host = [A.pin_memory() for (_, A, _) in host]
+    y_host = [torch.empty(c.M, c.N, dtype=fx.act_dtype).pin_memory() for c in cases]
+    h2d = sum(a.numel() * a.element_size() for a in a_host)
+    d2h = sum(y.numel() * y.element_size() for y in y_host)
     s0 = sets[0]
 
     def e2e_step():
-        for j, c in enumerate(cases):
-            s0[j]["W"].copy_(pinned[j][0], non_blocking=True)
-            s0[j]["A"].copy_(pinned[j][1], non_blocking=True)
-        run_step(0, stream, None)
-        for j, c in enumerate(cases):
-            yh[j].copy_(s0[j]["Y"], non_blocking=True)
+        for j in range(len(cases)):
+            s0[j]["A"].copy_(a_host[j], non_blocking=True)
+        step(0, stream)
+        for j in range(len(cases)):
+            y_host[j].copy_(s0[j]["Y"], non_blocking=True)
 
     for _ in range(2):
         e2e_step()
@@ -468,241 +571,185 @@ def run_gpu(args, rank, world):
     e2e_ms = e0.elapsed_time(e1)
 
     elapsed_ms, e2e_ms = max_over_ranks([elapsed_ms, e2e_ms], world, dev)
-
-    bytes_step = sum(quant_bytes(c.N, c.K, fmt) + gemm_bytes(c.M, c.N, c.K, fmt) for c in cases)
     flops_step = sum(gemm_flops(c.M, c.N, c.K) for c in cases)
-    ms_step = elapsed_ms / args.steps
-    value = job_rate(bytes_step, args.steps, elapsed_ms, world) / 1e9
-    e2e_value = job_rate(bytes_step, args.steps, e2e_ms, world) / 1e9
+    bytes_step = sum(gemm_bytes(c.M, c.N, c.K, fmt) for c in cases)
+    wbytes_step = sum(weight_bytes(c.N, c.K, fmt) for c in cases)
+    value = job_rate(flops_step, args.steps, elapsed_ms, world) / 1e12
+    e2e_value = job_rate(flops_step, args.steps, e2e_ms, world) / 1e12
 
-    peaks = load_peaks()
+    # --- kernels: the step's GEMM launches, then the load-time quantize
     kernels = []
     if args.grouped:
-        tq, tg = kern_ms[0], kern_ms[1]
+        kernels.append(dict(kernel=fx.gname, grouped=len(cases), us=round(launch_ms[0] * 1e3, 3),
+                            tflops=round(flops_step / (launch_ms[0] * 1e-3) / 1e12, 2),
+                            weight_gbs=round(wbytes_step / (launch_ms[0] * 1e-3) / 1e9, 1),
+                            gbs=round(bytes_step / (launch_ms[0] * 1e-3) / 1e9, 1)))
         qb = sum(quant_bytes(c.N, c.K, fmt) for c in cases)
-        gb = sum(gemm_bytes(c.M, c.N, c.K, fmt) for c in cases)
-        kernels.append(dict(kernel="rtn_quantize", grouped=len(cases), us=round(tq * 1e3, 3),
-                            gbs=round(qb / (tq * 1e-3) / 1e9, 1)))
-        kernels.append(dict(kernel="w4a16_gemm_tc", grouped=len(cases), us=round(tg * 1e3, 3),
-                            tflops=round(flops_step / (tg * 1e-3) / 1e12, 2),
-                            gbs=round(gb / (tg * 1e-3) / 1e9, 1)))
-    for j, c in enumerate([] if args.grouped else cases):
-        tq, tg = kern_ms[2 * j], kern_ms[2 * j + 1]
-        kernels.append(dict(kernel=qname, shape=[c.N, c.K], us=round(tq * 1e3, 3),
-                            gbs=round(quant_bytes(c.N, c.K, fmt) / (tq * 1e-3) / 1e9, 1)))
-        kernels.append(dict(kernel=gname, shape=[c.M, c.N, c.K], us=round(tg * 1e3, 3),
-                            variant=variant_of(c),
-                            tflops=round(gemm_flops(c.M, c.N, c.K) / (tg * 1e-3) / 1e12, 2),
-                            weight_gbs=round(weight_bytes(c.N, c.K, fmt) / (tg * 1e-3) / 1e9, 1),
-                            gbs=round(gemm_bytes(c.M, c.N, c.K, fmt) / (tg * 1e-3) / 1e9, 1)))
-    # dominant kernel: the kind with the larger share of kernel time
-    t_q = sum(kern_ms[0::2])
-    t_g = sum(kern_ms[1::2])
-    launches_kind = 1 if args.grouped else len(cases)
-    if t_q >= t_g:
-        dom, dom_bytes = qname, sum(quant_bytes(c.N, c.K, fmt) for c in cases)
-        dom_ms, launches_dom = t_q, launches_kind
-        bound, achieved, peak, unit = "hbm", None, peaks["hbm_gbs"], "GB/s"
-        achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+        kernels.append(dict(kernel=fx.qname, grouped=len(cases), us=round(q_us[0], 3),
+                            gbs=round(qb / (q_us[0] * 1e-6) / 1e9, 1),
+                            when="load time, outside the step"))
     else:
-        dom_ms, launches_dom = t_g, launches_kind
-        big = max(cases, key=lambda c: gemm_flops(c.M, c.N, c.K) / max(gemm_bytes(c.M, c.N, c.K, fmt), 1))
-        ai = gemm_flops(big.M, big.N, big.K) / gemm_bytes(big.M, big.N, big.K, fmt)
-        tensor_bound = ai > peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
-        dom = gname
-        if tensor_bound:
-            bound, peak, unit = "tensor", peaks["bf16_tflops"], "TFLOP/s"
-            achieved = sum(gemm_flops(c.M, c.N, c.K) for c in cases) / (dom_ms * 1e-3) / 1e12
-        else:
-            bound, peak, unit = "hbm", peaks["hbm_gbs"], "GB/s"
-            achieved = sum(gemm_bytes(c.M, c.N, c.K, fmt) for c in cases) / (dom_ms * 1e-3) / 1e9
-    traffic = dram_traffic(dom, args.workload + ("_grouped" if args.grouped else "") +
-                           ("_sr" if args.sr_seed is not None else ""))
+        for j, c in enumerate(cases):
+            t = launch_ms[j]
+            kernels.append(dict(kernel=fx.gname, shape=[c.M, c.N, c.K], us=round(t * 1e3, 3),
+                                variant=fx.variant(c.M, c.N, c.K),
+                                tflops=round(gemm_flops(c.M, c.N, c.K) / (t * 1e-3) / 1e12, 2),
+                                weight_gbs=round(weight_bytes(c.N, c.K, fmt) / (t * 1e-3) / 1e9, 1),
+                                gbs=round(gemm_bytes(c.M, c.N, c.K, fmt) / (t * 1e-3) / 1e9, 1)))
+        for j, c in enumerate(cases):
+            kernels.append(dict(kernel=fx.qname, shape=[c.N, c.K], us=round(q_us[j], 3),
+                                gbs=round(quant_bytes(c.N, c.K, fmt) / (q_us[j] * 1e-6) / 1e9, 1),
+                                when="load time, outside the step"))
 
-    # --- each GEMM shape alone: a CUDA graph of back-to-back launches on
-    # weight copies rotating through more than 3x L2 (launch overhead
-    # amortised, no quantize in between), against the roofline of the shape
-    b2b = []
-    for c in {(c.M, c.N, c.K): c for c in cases}.values():
-        s0 = sets[0][cases.index(c)]
-        nb = packed_bytes(c.N, c.K) + s0["scales"].numel() * s0["scales"].element_size()
-        ncp = max(1, min(16, -(-3 * L2_BYTES // nb)))
-        cps = [(s0["packed"], s0["scales"])] + [(s0["packed"].clone(), s0["scales"].clone())
-                                                for _ in range(ncp - 1)]
-        reps = max(8, 2 * ncp)
-        gb = torch.cuda.CUDAGraph()
-        cs = torch.cuda.Stream(dev)
-        cs.wait_stream(torch.cuda.current_stream(dev))
-        with torch.cuda.stream(cs):
-            with torch.cuda.graph(gb, stream=cs):
-                for r in range(reps):
-                    gemm_one(s0["A"], cps[r % ncp][0], cps[r % ncp][1], s0["Y"], cs, ws, s0["ts"])
-        torch.cuda.current_stream(dev).wait_stream(cs)
-        gb.replay()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        gb.replay()
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        us = e0.elapsed_time(e1) / reps * 1e3
-        t_hbm = gemm_bytes(c.M, c.N, c.K, fmt) / (peaks["hbm_gbs"] * 1e9) * 1e6
-        t_tc = gemm_flops(c.M, c.N, c.K) / (peaks["bf16_tflops"] * 1e12) * 1e6
-        b2b.append(dict(shape=[c.M, c.N, c.K], variant=variant_of(c), us=round(us, 3),
-                        weight_gbs=round(weight_bytes(c.N, c.K, fmt) / (us * 1e-6) / 1e9, 1),
-                        tflops=round(gemm_flops(c.M, c.N, c.K) / (us * 1e-6) / 1e12, 2),
-                        bound="hbm" if t_hbm >= t_tc else "tensor",
-                        roofline_frac=round(max(t_hbm, t_tc) / us, 4), weight_copies=ncp))
-        if args.swiglu and "gate_up" in c.name and not (int8 or fp4) and args.act == "bf16":
-            # the same weight copies through the SwiGLU epilogue (rows read as
-            # interleaved up/gate pairs; Y is [M, N/2]), each eligible tcgen05
-            # variant timed the same way, the fastest reported (the epilogue's
-            # own choice by measurement, passed as w4a16_gemm_swiglu's variant)
-            Yh = torch.empty(c.M, c.N // 2, dtype=torch.bfloat16, device=dev)
-            best = None
-            for vid in range(w4.w4a16_variant_count()):
-                vname = w4.w4a16_variant_name(vid)
-                if vname.startswith("simt_") or not w4.w4a16_variant_eligible(vid, c.M, c.N, c.K):
-                    continue
-                wsh = torch.zeros(max(w4.w4a16_variant_workspace_bytes(vid, c.M, c.N, c.K), 256),
-                                  dtype=torch.uint8, device=dev)
-                gh = torch.cuda.CUDAGraph()
-                with torch.cuda.stream(cs):
-                    for r in range(2):   # outside the capture: kernel attributes
-                        w4.w4a16_gemm_swiglu(s0["A"], cps[r % ncp][0], cps[r % ncp][1], Y=Yh,
-                                             workspace=wsh, stream=cs, variant=vid)
-                    with torch.cuda.graph(gh, stream=cs):
-                        for r in range(reps):
-                            w4.w4a16_gemm_swiglu(s0["A"], cps[r % ncp][0], cps[r % ncp][1], Y=Yh,
-                                                 workspace=wsh, stream=cs, variant=vid)
-                torch.cuda.current_stream(dev).wait_stream(cs)
-                gh.replay()
-                e0.record(stream)
-                gh.replay()
-                e1.record(stream)
-                torch.cuda.synchronize(dev)
-                us = e0.elapsed_time(e1) / reps * 1e3
-                if best is None or us < best[0]:
-                    best = (us, vname)
-                del gh, wsh
-            us, vname = best
-            b2b.append(dict(shape=[c.M, c.N, c.K], epilogue="swiglu", variant=vname,
-                            us=round(us, 3),
-                            weight_gbs=round(weight_bytes(c.N, c.K, fmt) / (us * 1e-6) / 1e9, 1),
-                            tflops=round(gemm_flops(c.M, c.N, c.K) / (us * 1e-6) / 1e12, 2),
-                            bound="hbm" if t_hbm >= t_tc else "tensor",
-                            roofline_frac=round(max(t_hbm, t_tc) / us, 4), weight_copies=ncp))
-            del Yh
-        del cps, gb
-    if w4.w4a16_get_device_error() != w4.W4A16_OK:
-        raise RuntimeError("device error during the back-to-back GEMM timing")
+    # --- roofline of the step's kernel family (the GEMM): algorithmic work
+    # per launch over the launches' measured durations
+    dom_ms = sum(launch_ms)
+    t_hbm = bytes_step / (peaks["hbm_gbs"] * 1e9)
+    t_tc = flops_step / (peaks["bf16_tflops"] * 1e12)
+    if t_tc >= t_hbm:
+        bound, peak, unit = "tensor", peaks["bf16_tflops"], "TFLOP/s"
+        achieved = flops_step / (dom_ms * 1e-3) / 1e12
+    else:
+        bound, peak, unit = "hbm", peaks["hbm_gbs"], "GB/s"
+        achieved = bytes_step / (dom_ms * 1e-3) / 1e9
+    tkey = args.workload + ("_grouped" if args.grouped else "") + \
+        ("" if fmt == "int4" else "_" + fmt) + ("_f16" if args.act == "f16" else "")
+    traffic = dram_traffic(fx.gname, tkey)
     roofline = dict(bound=bound, achieved=round(achieved, 2), peak=peak, unit=unit,
                     frac=round(achieved / peak, 4),
-                    traffic=None if traffic is None else traffic,
-                    kernel=dom, launches_per_step=launches_dom, peak_source=peaks["source"])
+                    traffic=None if traffic is None else traffic / n_launch,
+                    traffic_source=(None if traffic is None else
+                                    "profiles/dram_traffic.txt: ncu dram__bytes_read.sum + "
+                                    "dram__bytes_write.sum per launch, taken on kernel sources "
+                                    "hash %s (the current ones)" % kernel_source_hash()),
+                    kernel=fx.gname, launches_per_step=n_launch, peak_source=peaks["source"],
+                    algorithmic=("%.0f flops per step" % flops_step if bound == "tensor" else
+                                 "%.0f bytes per step (codes + scales + activations)" % bytes_step))
 
-    out = dict(metric=METRIC, value=round(value, 2), unit="GB/s", n_gpus=world, steps=args.steps,
-               warmup=args.warmup, ms_per_step=round(ms_step, 5), higher_is_better=True,
-               scaling="weak", vs_baseline=None, dtype=args.act, data="synthetic",
-               config=dict(workload=args.workload, activations=args.act, weights=args.weights,
+    # --- each distinct GEMM shape of the workload alone, back to back; and
+    # (default run) the metric's bandwidth-bound end: the M in {1, 4, 16, 64}
+    # sweep, every shape back to back with its roofline fraction
+    del g_timed, g_warm, g_ev
+    wcache = {}
+    b2b = [back_to_back(fx, c, peaks, wcache, args.tune, dev) for c in
+           {(c.M, c.N, c.K): c for c in cases}.values()] if len(cases) > 1 else []
+    sweep = None
+    if args.workload == "large" and not args.no_sweep:
+        del sets, W_dev
+        torch.cuda.empty_cache()
+        sweep = [back_to_back(fx, c, peaks, wcache, args.tune, dev) for c in synthetic.SWEEP]
+    if w4.w4a16_get_device_error() != w4.W4A16_OK:
+        raise RuntimeError("device error during the back-to-back GEMM timing")
+
+    out = dict(metric=METRIC, value=round(value, 3), unit="TFLOP/s", n_gpus=world, steps=args.steps,
+               warmup=args.warmup, ms_per_step=round(elapsed_ms / args.steps, 5),
+               higher_is_better=True, scaling="weak", vs_baseline=None, dtype=args.act,
+               data="synthetic",
+               config=dict(workload=args.workload, activations=args.act, weights=fmt,
                            shapes=[[c.M, c.N, c.K] for c in cases],
-                           step=("one grouped rtn_quantize launch over all projections + one grouped "
-                                 "w4a16_gemm launch" if args.grouped else
-                                 "INT8 rtn_quantize + w8a16_gemm per projection" if int8 else
-                                 f"{fmt.upper()} quantize + fp4a16_gemm per projection" if fp4 else
-                                 "rtn_quantize + w4a16_gemm per projection" if args.sr_seed is None
-                                 else "stochastic-rounding quantize (seed %d) + w4a16_gemm per "
-                                 "projection" % args.sr_seed),
-                           l2="inputs rotate over %d copies (%.0f MB > 3x L2)" % (copies, copies * per_copy / 2**20),
-                           selection=("per-shape table tuned by measurement before timing" if args.tune
+                           step=("one grouped W4A16 GEMM launch over all projections"
+                                 if args.grouped else "one GEMM launch per projection") +
+                                " on weights quantized at load (the quantize is timed apart, "
+                                "under kernels)",
+                           l2="inputs rotate over %d copies (%.0f MB of weights and activations "
+                              "> 3x L2)" % (copies, copies * in_bytes / 2**20),
+                           selection=("tuned by measurement before timing" if args.tune
                                       else "cost-model rule"),
                            parallelism=f"replicas x{world}"),
-               gemm=dict(tflops=round(job_rate(flops_step, args.steps, elapsed_ms, world) / 1e12, 3)),
+               gemm=dict(tflops=round(value, 3),
+                         weight_gbs=round(job_rate(wbytes_step, args.steps, elapsed_ms, world) / 1e9, 1),
+                         gbs=round(job_rate(bytes_step, args.steps, elapsed_ms, world) / 1e9, 1)),
                kernels=kernels, roofline=roofline, clocks=clk.summary(),
-               gemm_back_to_back=b2b,
                gpu_launches=int(launches),
-               e2e=dict(value=round(e2e_value, 2), unit="GB/s", h2d_bytes_per_step=int(h2d),
+               e2e=dict(value=round(e2e_value, 3), unit="TFLOP/s", h2d_bytes_per_step=int(h2d),
                         d2h_bytes_per_step=int(d2h)))
+    if b2b:
+        out["gemm_back_to_back"] = b2b
+    if sweep is not None:
+        out["sweep"] = sweep
+        out["sweep_roofline_frac"] = dict(
+            min=min(e["roofline_frac"] for e in sweep), max=max(e["roofline_frac"] for e in sweep),
+            bound="hbm", peak=peaks["hbm_gbs"], unit="GB/s",
+            note="each sweep shape alone, back to back, weight copies > 3x L2; roofline = max of "
+                 "(codes + scales + activations) / HBM peak and flops / bf16 peak")
     return out
 
 
 # ------------------------------------------------------------- CPU oracle
-def time_oracle(workload: str, budget_s: float, sr_seed=None, weights="int4"):
-    """The oracle as it stands, on the host cores, over whole passes of the
-    workload (quantize + GEMM per projection; the stochastic-rounding quantize
-    when `sr_seed` is given) until `budget_s` is used."""
-    import numpy as np
+def time_oracle(workload: str, budget_s: float, weights="int4", rows=1024):
+    """The oracle as it stands, on the host cores: each projection's weight
+    quantized once by the oracle (load time, untimed), then the oracle's GEMM
+    (dequantize + FP32 matmul) on the first `rows` rows of the activations,
+    projection after projection, until `budget_s` is used.  Returns the rate
+    in the metric's unit (TFLOP/s of the GEMM flops done)."""
+    import numpy as np  # noqa: F401
 
     import oracle
     from weight_only_int4_rtn_gb300 import synthetic
 
     cases = synthetic.WORKLOADS[workload]
-    inputs = []
+    prepared = []
     for c in cases:
-        W, A, b = synthetic.draw(c)
-        inputs.append((synthetic.bits(W), synthetic.bits(A)))
-    # bounded sample: for very large workloads only the first rows of A
-    sample_rows = [min(c.M, 64) for c in cases]
-    done_bytes = 0.0
+        W, A, _ = synthetic.draw(c)
+        wb, ab = synthetic.bits(W), synthetic.bits(A)
+        mr = min(c.M, rows)
+        if weights == "int8":
+            p, s = oracle.quantize8(wb)
+            fn = (lambda a, p=p, s=s: oracle.gemm8(a, p, s))
+        elif weights == "mxfp4":
+            p, s = oracle.quantize_mxfp4_f32(oracle.bf16_bits_to_f32(wb))
+            fn = (lambda a, p=p, s=s: oracle.gemm_fp4(a, oracle.dequantize_mxfp4(p, s)))
+        elif weights == "nvfp4":
+            p, s, g = oracle.quantize_nvfp4_f32(oracle.bf16_bits_to_f32(wb))
+            fn = (lambda a, p=p, s=s, g=g: oracle.gemm_fp4(a, oracle.dequantize_nvfp4(p, s, g)))
+        else:
+            p, s = oracle.quantize(wb)
+            fn = (lambda a, p=p, s=s: oracle.gemm(a, p, s))
+        prepared.append((c, ab[:mr], mr, fn))
+    flops = 0.0
     passes = 0
     t0 = time.perf_counter()
     while True:
-        for c, (wb, ab), mr in zip(cases, inputs, sample_rows):
-            if weights == "int8":
-                p, s = oracle.quantize8(wb)
-                oracle.gemm8(ab[:mr], p, s)
-            elif weights == "mxfp4":
-                p, s = oracle.quantize_mxfp4_f32(oracle.bf16_bits_to_f32(wb))
-                oracle.gemm_fp4(ab[:mr], oracle.dequantize_mxfp4(p, s))
-            elif weights == "nvfp4":
-                p, s, g = oracle.quantize_nvfp4_f32(oracle.bf16_bits_to_f32(wb))
-                oracle.gemm_fp4(ab[:mr], oracle.dequantize_nvfp4(p, s, g))
-            else:
-                p, s = oracle.quantize(wb) if sr_seed is None else oracle.quantize_sr(wb, sr_seed)
-                oracle.gemm(ab[:mr], p, s)
-            done_bytes += quant_bytes(c.N, c.K, weights) + gemm_bytes(mr, c.N, c.K, weights)
+        for c, a, mr, fn in prepared:
+            fn(a)
+            flops += gemm_flops(mr, c.N, c.K)
         passes += 1
         if time.perf_counter() - t0 >= budget_s:
             break
     dt = time.perf_counter() - t0
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    sample = (f"{passes} pass(es) of {workload}: oracle "
-              + ({"int8": "INT8 ", "mxfp4": "MXFP4 ", "nvfp4": "NVFP4 "}.get(weights, "")
-                 if weights != "int4" else "" if sr_seed is None else "stochastic-rounding ")
-              + "quantize + FP32 GEMM per projection"
-              + ("" if all(mr == c.M for mr, c in zip(sample_rows, cases)) else
-                 ", GEMM on the first 64 rows of A"))
-    return dict(value=round(done_bytes / dt / 1e9, 4), unit="GB/s", cores=cores, kind="oracle",
+    sampled = any(mr < c.M for c, _, mr, _ in prepared)
+    sample = (f"{passes} pass(es) of {workload}: the oracle's "
+              + ({"int8": "INT8 ", "mxfp4": "MXFP4 ", "nvfp4": "NVFP4 "}.get(weights, ""))
+              + "GEMM (dequantize + FP32 matmul) per projection"
+              + (f" on the first {rows} rows of A" if sampled else "")
+              + "; weights quantized once by the oracle beforehand (load time, untimed)")
+    return dict(value=round(flops / dt / 1e12, 6), unit="TFLOP/s", cores=cores, kind="oracle",
                 sample=sample, seconds=round(dt, 2))
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="expert_m50",
+    ap.add_argument("--workload", default="large",
                     choices=["tiny", "expert_m50", "prefix_m816", "sweep", "large"])
     ap.add_argument("--act", default="bf16", choices=["bf16", "f16"],
                     help="activation type of the GEMMs (A, bias, Y)")
     ap.add_argument("--grouped", dest="grouped", action="store_true", default=None,
-                    help="one grouped quantize and one grouped GEMM launch per step (the "
-                         "projections are independent problems; the default when the "
-                         "workload has at most 8 projections)")
+                    help="one grouped GEMM launch per step (the projections are independent "
+                         "problems; the default when the workload has 2 to 8 projections)")
     ap.add_argument("--per-projection", dest="grouped", action="store_false",
-                    help="one quantize and one GEMM launch per projection")
+                    help="one GEMM launch per projection")
     ap.add_argument("--weights", default="int4", choices=["int4", "int8", "mxfp4", "nvfp4"],
                     help="weight scheme: INT4 (W4A16), INT8 (W8A16), MXFP4 or NVFP4 weights")
     ap.add_argument("--sr-seed", type=int, default=None,
-                    help="quantize with seeded stochastic rounding (w4a16_quantize_sr) instead "
-                         "of round to nearest")
-    ap.add_argument("--swiglu", action="store_true",
-                    help="also time each gate/up projection's GEMM with the SwiGLU epilogue "
-                         "(w4a16_gemm_swiglu) back to back, with the variant that measures "
-                         "fastest (INT4 weights, bf16 activations)")
-    ap.add_argument("--tune-file", default=None,
-                    help="write the tuned choices to this JSON file, or replay them from it "
-                         "when it exists (no timing under a profiler)")
+                    help="quantize at load with seeded stochastic rounding (w4a16_quantize_sr) "
+                         "instead of round to nearest")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="leave out the M in {1, 4, 16, 64} sweep of the default line")
     ap.add_argument("--no-tune", dest="tune", action="store_false", default=True,
                     help="select kernels by the cost-model rule instead of tuning each "
                          "shape by measurement first")
@@ -718,13 +765,15 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return 0
-        t_budget = max(5.0, min(60.0, args.cpu_budget * (args.steps + args.warmup) / 10))
-        cb = time_oracle(args.workload, t_budget, args.sr_seed, args.weights)
-        line = dict(metric=METRIC, value=cb["value"], unit="GB/s", n_gpus=world, steps=args.steps,
-                    warmup=args.warmup, ms_per_step=None, higher_is_better=True, scaling="weak",
-                    vs_baseline=None, dtype="f32", data="synthetic", impl="reference",
-                    config=dict(workload=args.workload), cpu_baseline=cb,
-                    e2e=dict(value=cb["value"], unit="GB/s", h2d_bytes_per_step=0,
+        # each step a bounded sample of the workload: about 1.2 s of oracle work
+        t_budget = max(5.0, min(90.0, 1.2 * (args.steps + args.warmup)))
+        cb = time_oracle(args.workload, t_budget, args.weights)
+        line = dict(metric=METRIC, value=cb["value"], unit="TFLOP/s", n_gpus=world,
+                    steps=args.steps, warmup=args.warmup, ms_per_step=None, higher_is_better=True,
+                    scaling="weak", vs_baseline=None, dtype="f32", data="synthetic",
+                    impl="reference", config=dict(workload=args.workload, weights=args.weights),
+                    cpu_baseline=cb,
+                    e2e=dict(value=cb["value"], unit="TFLOP/s", h2d_bytes_per_step=0,
                              d2h_bytes_per_step=0))
         print(json.dumps(line), flush=True)
         return 0
@@ -739,7 +788,7 @@ def main():
     build()
     out = run_gpu(args, rank, world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = time_oracle(args.workload, args.cpu_budget, args.sr_seed, args.weights)
+        out["cpu_baseline"] = time_oracle(args.workload, args.cpu_budget, args.weights)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

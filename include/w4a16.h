@@ -87,6 +87,31 @@ size_t w4a16_packed_bytes(int64_t N, int64_t K);
 /* Bytes of the scale array: (K / group) * N * 2.  0 if group != 128. */
 size_t w4a16_scales_bytes(int64_t N, int64_t K, int group);
 
+/* Bytes of the row-major packed codes of an [N, K] weight: N * K / 2 (byte
+ * j of row n holds the codes of k = 2j, low nibble, and k = 2j + 1, high
+ * nibble, two's complement). */
+size_t w4a16_packed_rowmajor_bytes(int64_t N, int64_t K);
+
+/*
+ * Row-major packed codes -> the tiled storage the GEMM reads ("Kernel
+ * dispatch and Humming quantization in PhyAI", section "Humming makes the
+ * separation useful": a packed INT4 layout runs only through the kernel that
+ * understands it; this is the conversion from the plain interchange form,
+ * e.g. codes read from a checkpoint, to this library's layout).
+ * packed_rowmajor: [N, K/2] bytes as above, w4a16_packed_rowmajor_bytes(N,
+ * K) (read).  packed_out: w4a16_packed_bytes(N, K) bytes (written; rows past
+ * N zero).  Byte (n, j) lands at the offset given in the layout table at the
+ * top of this file; nothing is decoded, so the same call serves the FP4
+ * formats' nibbles.  Shape limits: K % 128 == 0, N % 8 == 0, N, K >= 1 and
+ * the limits of w4a16_quantize; both pointers 16-byte aligned and not
+ * overlapping.  Errors: W4A16_ERR_INVALID_ARG (null pointer, N or K < 1),
+ * W4A16_ERR_UNSUPPORTED (K % 128, N % 8, size limits), W4A16_ERR_ALIGNMENT,
+ * W4A16_ERR_CUDA (launch).  Allocates nothing, one kernel launch on
+ * `stream`, capture-safe.
+ */
+int w4a16_repack_rowmajor(const void* packed_rowmajor, int64_t N, int64_t K, void* packed_out,
+                          void* stream);
+
 /*
  * RTN quantize/pack ("Kernel dispatch and Humming quantization in PhyAI",
  * section "Humming makes the separation useful": round-to-nearest at load,
@@ -321,6 +346,12 @@ int w4a16_gemm_grouped(const w4a16_gemm_problem* problems, int count, int group,
  * current device: W4A16_OK, or W4A16_ERR_TIMEOUT if a kernel's bounded wait
  * expired since the last call (that kernel's output is then undefined and a
  * workspace it used must be re-initialised).
+ *
+ * The library looks up device addresses of its own static device storage
+ * (this error word, the scratch of w4a16_gemm_noalloc) once per device and
+ * keeps them for the life of the process.  cudaDeviceReset destroys the
+ * device's primary context and with it those addresses: after a reset, do
+ * not call this library on that device again in the same process.
  */
 int w4a16_get_device_error(void* stream);
 
@@ -335,6 +366,24 @@ void w4a16_set_wait_timeout_ns(uint64_t ns);
  * Nothing faults or hangs.  Read the result with w4a16_get_device_error.
  */
 int w4a16_selftest_wait_timeout(uint64_t timeout_ns, void* stream);
+
+/*
+ * Self test of the quantizer's division.  The quantize kernels compute
+ * fl32(w / s) as a reciprocal product plus one remainder correction
+ * (Markstein's theorem gives the correctly rounded quotient when 1 / s is
+ * correctly rounded); this launch checks that code against the IEEE division
+ * on the device, value by value:
+ *   mode 0: every normal finite fp16 scale s and every finite bf16 w with
+ *           |w| <= 7.5 s (the INT4 modes' whole domain);
+ *   mode 1: the same scales, |w| <= 127.5 s (INT8);
+ *   mode 2: NVFP4 steps fl32(e4m3 * g) for the 126 nonzero E4M3 codes and
+ *           512 fixed tensor scales g in [2^-40, 2^41), |w| <= 8 step.
+ * counts: device uint64[2], 8-byte aligned, caller-owned; the call zeroes it
+ * on `stream`, then counts[0] = pairs checked, counts[1] = quotients that
+ * differ (+0 and -0 count as equal).  Errors: W4A16_ERR_INVALID_ARG (null),
+ * W4A16_ERR_UNSUPPORTED (mode), W4A16_ERR_ALIGNMENT, W4A16_ERR_CUDA.
+ */
+int w4a16_selftest_quotient(int mode, unsigned long long* counts, void* stream);
 
 /* Number of kernel launches this library has made in this process. */
 uint64_t w4a16_launch_count(void);

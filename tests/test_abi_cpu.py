@@ -193,3 +193,29 @@ def test_grouped_argument_errors_before_launch(built_lib):
     Q[1] = w4.QuantizeProblem(16, 250, 512, 16, 16)               # N not a multiple of 8
     assert L.w4a16_quantize_grouped(Q, 2, 128, None) == w4.W4A16_ERR_UNSUPPORTED
     assert L.w4a16_quantize_grouped(Q, 0, 128, None) == w4.W4A16_ERR_INVALID_ARG
+
+
+def test_rowmajor_sizes(built_lib):
+    L = w4.lib()
+    assert L.w4a16_packed_rowmajor_bytes(256, 512) == 256 * 256
+    assert L.w4a16_packed_rowmajor_bytes(264, 512) == 264 * 256   # no padding rows
+    assert L.w4a16_packed_rowmajor_bytes(-1, 512) == 0
+
+
+def test_repack_argument_errors_before_any_launch(built_lib):
+    L = w4.lib()
+    assert L.w4a16_repack_rowmajor(None, 256, 512, 16, None) == w4.W4A16_ERR_INVALID_ARG
+    assert L.w4a16_repack_rowmajor(16, 256, 512, None, None) == w4.W4A16_ERR_INVALID_ARG
+    assert L.w4a16_repack_rowmajor(16, 0, 512, 16, None) == w4.W4A16_ERR_INVALID_ARG
+    assert L.w4a16_repack_rowmajor(16, 256, 500, 16, None) == w4.W4A16_ERR_UNSUPPORTED
+    assert L.w4a16_repack_rowmajor(16, 250, 512, 16, None) == w4.W4A16_ERR_UNSUPPORTED
+    assert L.w4a16_repack_rowmajor(8, 256, 512, 16, None) == w4.W4A16_ERR_ALIGNMENT
+    assert L.w4a16_repack_rowmajor(16, 256, 512, 24, None) == w4.W4A16_ERR_ALIGNMENT
+
+
+def test_quotient_selftest_argument_errors(built_lib):
+    L = w4.lib()
+    assert L.w4a16_selftest_quotient(0, None, None) == w4.W4A16_ERR_INVALID_ARG
+    assert L.w4a16_selftest_quotient(3, 16, None) == w4.W4A16_ERR_UNSUPPORTED
+    assert L.w4a16_selftest_quotient(-1, 16, None) == w4.W4A16_ERR_UNSUPPORTED
+    assert L.w4a16_selftest_quotient(0, 12, None) == w4.W4A16_ERR_ALIGNMENT

@@ -72,3 +72,21 @@ def test_workload_weights_full_size(w4, case):
     W = synthetic.draw_weight_only(case.seed, case.N, case.K, case.wdist)
     packed, scales = run_quantize(w4, W)
     check_quantize_exact(W, packed, scales)
+
+
+def test_scale_overflow_matches_oracle(w4):
+    # amax / 7 above fp16's range (outside the preconditions): the kernel
+    # takes the IEEE division for an infinite scale, as the oracle does
+    # (scale 0x7C00, codes 0); the other groups are unaffected
+    rng = np.random.default_rng(11)
+    x = (rng.standard_normal((16, 512)) * 0.02).astype(np.float32)
+    x[3, 5] = 524288.0          # group 0 of row 3
+    x[7, 300] = -1048576.0      # group 2 of row 7
+    x[9, 128:256] = 0.0
+    x[9, 130] = 600000.0        # group 1 of row 9
+    W = synthetic.to_bf16(x)
+    packed, scales = run_quantize(w4, W)
+    s = scales.cpu().view(torch.int16).numpy().view(np.uint16)
+    assert s[0, 3] == 0x7C00 and s[2, 7] == 0x7C00 and s[1, 9] == 0x7C00
+    with np.errstate(over="ignore"):
+        check_quantize_exact(W, packed, scales)

@@ -122,3 +122,19 @@ def test_tile_layout_closed_form():
             pad[base:base + 64] = False
     assert not t[pad].any()
     assert (oracle.from_tile_layout(t, N, K) == p).all()
+
+
+def test_scale_overflow_follows_ieee():
+    # Outside the method's preconditions (|w| small enough that amax / 7 fits
+    # fp16), the oracle's steps still have one IEEE reading, worked by hand:
+    # amax = 2^19 = 524288 (bf16-exact); fl32(524288 / 7) = 74898.28...,
+    # above fp16's largest finite value 65504 and above the rounding boundary
+    # 65520, so fp16 round-to-nearest gives +inf (0x7C00), which is not 0, so
+    # the zero rule does not apply; every x / inf is +-0 and rounds to code 0.
+    x = np.zeros((1, 128), dtype=np.float32)
+    x[0, :3] = [524288.0, 3.0, -3.0]
+    with np.errstate(over="ignore"):
+        packed, sbits = oracle.quantize_f32(x)
+    assert int(sbits[0, 0]) == 0x7C00
+    assert not oracle.unpack_codes(packed).any()
+    assert not packed.any()

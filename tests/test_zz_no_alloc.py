@@ -49,11 +49,14 @@ def test_noalloc_matches_regular_entry_point_twice(w4):
 
 def test_noalloc_rejects_shapes_beyond_its_scratch(w4):
     L = w4.lib()
-    # a stream-K variant whose partial tiles need far more than 16 MiB
-    M, N, K = 816, 2048, 16384
-    v = w4.w4a16_select_variant(M, N, K)
-    if w4.w4a16_variant_workspace_bytes(v, M, N, K) <= (16 << 20):
-        pytest.skip("the selected variant fits the static scratch")
+    # a shape whose selected variant needs more than the 16 MiB static
+    # scratch: searched, so that the rejection path is always exercised
+    limit = 16 << 20
+    over = [(M, N, K) for M in (816, 2048, 4096, 8192) for (N, K) in
+            ((2048, 16384), (1024, 65536), (2048, 65536), (4096, 32768))
+            if w4.w4a16_gemm_workspace_bytes(M, N, K) > limit]
+    assert over, "no searched shape needs more scratch than the static array holds"
+    M, N, K = over[0]
     # real (zero) buffers, although the call must return before any launch
     A = torch.zeros(M, K, dtype=torch.bfloat16, device="cuda")
     packed = torch.zeros(w4.w4a16_packed_bytes(N, K), dtype=torch.uint8, device="cuda")

@@ -124,6 +124,9 @@ SIGNATURES = [
     ("w4a16_selftest_wait_timeout", ctypes.c_int, [ctypes.c_uint64, _vp]),
     ("w4a16_launch_count", ctypes.c_uint64, []),
     ("w4a16_last_error_detail", ctypes.c_char_p, []),
+    ("w4a16_packed_rowmajor_bytes", _c_size, [_c_int64, _c_int64]),
+    ("w4a16_repack_rowmajor", ctypes.c_int, [_vp, _c_int64, _c_int64, _vp, _vp]),
+    ("w4a16_selftest_quotient", ctypes.c_int, [ctypes.c_int, _vp, _vp]),
     ("w4a16_gemm_noalloc", ctypes.c_int,
      [_vp, _c_int64, _c_int64, _c_int64, _vp, _vp, ctypes.c_int, _vp, _vp, _vp]),
 ]
@@ -237,6 +240,39 @@ def w4a16_quantize(W: torch.Tensor, group: int = GROUP, packed: torch.Tensor | N
                                      scales.data_ptr(), _stream_handle(W.device, stream))
         _check(st, "w4a16_quantize_sr")
     return packed, scales
+
+
+def w4a16_repack_rowmajor(packed_rowmajor: torch.Tensor, N: int, K: int,
+                          packed: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Row-major packed codes (uint8 ``[N, K/2]`` or 1-D with N*K/2 bytes;
+    byte j of row n: code 2j low nibble, 2j+1 high nibble) to the tiled
+    storage the GEMM reads (w4a16_repack_rowmajor).  Returns ``packed`` (1-D
+    uint8, w4a16_packed_bytes(N, K) bytes), allocated when not given."""
+    _require_cuda(packed_rowmajor, "packed_rowmajor", torch.uint8)
+    if packed_rowmajor.numel() != lib().w4a16_packed_rowmajor_bytes(N, K):
+        raise ValueError("packed_rowmajor must hold N * K / 2 bytes")
+    nbytes = lib().w4a16_packed_bytes(N, K)
+    if packed is None:
+        packed = torch.empty(nbytes, dtype=torch.uint8, device=packed_rowmajor.device)
+    _require_cuda(packed, "packed", torch.uint8)
+    if packed.numel() != nbytes:
+        raise ValueError("packed must hold w4a16_packed_bytes(N, K) bytes")
+    _check(lib().w4a16_repack_rowmajor(packed_rowmajor.data_ptr(), N, K, packed.data_ptr(),
+                                       _stream_handle(packed.device, stream)),
+           "w4a16_repack_rowmajor")
+    return packed
+
+
+def selftest_quotient(mode: int, device=None) -> tuple[int, int]:
+    """Run w4a16_selftest_quotient (0: INT4 scales, 1: INT8 scales, 2: NVFP4
+    steps) on ``device`` and return ``(pairs checked, mismatches)``
+    (synchronises)."""
+    dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
+    counts = torch.zeros(2, dtype=torch.int64, device=dev)
+    _check(lib().w4a16_selftest_quotient(int(mode), counts.data_ptr(), _stream_handle(dev)),
+           "w4a16_selftest_quotient")
+    c = counts.cpu().tolist()
+    return int(c[0]), int(c[1])
 
 
 # ------------------------------------------------------------------- GEMM

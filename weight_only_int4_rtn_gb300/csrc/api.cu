@@ -1564,6 +1564,37 @@ int w4a16_selftest_wait_timeout(uint64_t timeout_ns, void* stream) {
   return W4A16_OK;
 }
 
+size_t w4a16_packed_rowmajor_bytes(int64_t N, int64_t K) {
+  if (N < 0 || K < 0) return 0;
+  return static_cast<size_t>(N) * static_cast<size_t>(K) / 2;
+}
+
+int w4a16_repack_rowmajor(const void* packed_rowmajor, int64_t N, int64_t K, void* packed_out,
+                          void* stream) {
+  if (packed_rowmajor == nullptr || packed_out == nullptr) return W4A16_ERR_INVALID_ARG;
+  if (N < 1 || K < 1) return W4A16_ERR_INVALID_ARG;
+  if (K % kGroup != 0 || N % 8 != 0) return W4A16_ERR_UNSUPPORTED;
+  if (N >= (1ll << 31) || K >= (1ll << 31) || N * K >= (1ll << 40)) return W4A16_ERR_UNSUPPORTED;
+  if (!aligned16(packed_rowmajor) || !aligned16(packed_out)) return W4A16_ERR_ALIGNMENT;
+  DeviceInfo dev;
+  if (!device_info(dev)) return W4A16_ERR_CUDA;
+  const cudaError_t e = launch_repack_rowmajor(packed_rowmajor, N, K, packed_out, dev.num_sms,
+                                               static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_failure(e, "repack_rowmajor");
+  g_launches.fetch_add(1);
+  return W4A16_OK;
+}
+
+int w4a16_selftest_quotient(int mode, unsigned long long* counts, void* stream) {
+  if (counts == nullptr) return W4A16_ERR_INVALID_ARG;
+  if (mode < 0 || mode > 2) return W4A16_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(counts) & 7u) != 0) return W4A16_ERR_ALIGNMENT;
+  const cudaError_t e = launch_quotient_selftest(mode, counts, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_failure(e, "quotient_selftest");
+  g_launches.fetch_add(1);
+  return W4A16_OK;
+}
+
 uint64_t w4a16_launch_count(void) { return g_launches.load(); }
 
 const char* w4a16_last_error_detail(void) { return g_error_detail; }

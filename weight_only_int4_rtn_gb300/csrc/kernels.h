@@ -173,6 +173,16 @@ cudaError_t launch_gemv(const GemmKernelConfig& c, const GemmGroup& grp, bool us
                         cudaStream_t stream);
 size_t gemv_smem_bytes(const GemmKernelConfig& c);
 
+// Row-major packed codes [N, K/2] (16-byte aligned, K % 128 == 0) to the
+// tiled storage (layout.cu); one launch.
+cudaError_t launch_repack_rowmajor(const void* rowmajor, int64_t N, int64_t K, void* tiled,
+                                   int num_sms, cudaStream_t stream);
+
+// Self test of the quantizer's corrected quotient against the IEEE division
+// (quantize.cu): mode 0 INT4 scales, 1 INT8 scales, 2 NVFP4 steps; zeroes
+// counts[0..1] on `stream`, then adds the pairs checked and the mismatches.
+cudaError_t launch_quotient_selftest(int mode, unsigned long long* counts, cudaStream_t stream);
+
 // Failure-detection self test: one thread waits on an mbarrier nobody
 // arrives at, with a bounded wait; records a timeout in *error_word.
 cudaError_t launch_wait_timeout_selftest(uint32_t* error_word, uint64_t timeout_ns,

@@ -33,7 +33,7 @@
 // q2 = fl32(w / s) (Markstein's theorem), which a fused add of 1.5 * 2^23
 // rounds half to even; the low four bits of that float are the code's
 // two's-complement nibble.  For a normal scale |w / s| <= 7 (1 + 2^-11) < 7.5,
-// so no clamp can be active.  A subnormal scale (rare) takes the IEEE
+// so no clamp can be active.  A subnormal or infinite scale (rare) takes the IEEE
 // division __fdiv_rn and the clamp value by value.
 //
 // Stochastic-rounding mode ("Piper Kernels", section "Stochastic
@@ -135,20 +135,36 @@ __device__ __forceinline__ uint32_t pack8(const uint32_t (&y)[8]) {
   return ptx::prmt(lo, hi, 0x5410);
 }
 
-// Codes of 8 values for a normal scale: the quotient corrected to the
-// correctly rounded fl32(w / s) by one remainder step (Markstein: with r the
-// correctly rounded reciprocal, the remainder w - q1 s is exact and
-// q1 + (w - q1 s) r rounds to fl32(w / s)), then rounded half to even.
-// |w / s| < 7.5, so no clamp is active.
+// The quotient fl32(w / s) from r = fl32(1 / s): q1 = fl32(w r), the
+// remainder e = w - q1 s (exact: one fused multiply-add) and one correction
+// q2 = fl32(q1 + e r).  With r the correctly rounded reciprocal this gives
+// the correctly rounded quotient (Markstein's theorem) for a normal, finite
+// s.  Every quantize mode that divides by a normal scale uses this function,
+// and w4a16_selftest_quotient checks it against the IEEE division over
+// every scale and weight value the INT4 and INT8 modes can meet.
+__device__ __forceinline__ float quotient_corrected(float w, float s, float r) {
+  const float q1 = __fmul_rn(w, r);
+  const float e = fmaf(-q1, s, w);
+  return fmaf(e, r, q1);
+}
+
+// True for an fp16 scale that takes the corrected quotient: normal and
+// finite.  A subnormal scale, and an infinite one (amax / 7 above fp16's
+// range: outside the method's preconditions, but then the IEEE division
+// gives the oracle's code 0 where the remainder step would give NaN), take
+// the IEEE division value by value.
+__device__ __forceinline__ bool scale_fast(__half s16) {
+  const uint32_t e = __half_as_ushort(s16) & 0x7C00u;
+  return e != 0u && e != 0x7C00u;
+}
+
+// Codes of 8 values for a normal scale: the corrected quotient, rounded half
+// to even.  |w / s| < 7.5, so no clamp is active.
 __device__ __forceinline__ uint32_t codes_corrected(const float (&f)[8], float s, float r) {
   uint32_t y[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float q1 = __fmul_rn(f[i], r);
-    const float e = fmaf(-q1, s, f[i]);
-    const float q2 = fmaf(e, r, q1);
-    y[i] = __float_as_uint(__fadd_rn(q2, kRoundMagic));
-  }
+  for (int i = 0; i < 8; ++i)
+    y[i] = __float_as_uint(__fadd_rn(quotient_corrected(f[i], s, r), kRoundMagic));
   return pack8(y);
 }
 
@@ -226,12 +242,8 @@ __device__ __forceinline__ void codes8_corrected(const float (&f)[8], float s, f
                                                  uint32_t& w0, uint32_t& w1) {
   uint32_t y[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float q1 = __fmul_rn(f[i], r);
-    const float e = fmaf(-q1, s, f[i]);
-    const float q2 = fmaf(e, r, q1);
-    y[i] = __float_as_uint(__fadd_rn(q2, kRoundMagic));
-  }
+  for (int i = 0; i < 8; ++i)
+    y[i] = __float_as_uint(__fadd_rn(quotient_corrected(f[i], s, r), kRoundMagic));
   w0 = pack4_bytes(y[0], y[1], y[2], y[3]);
   w1 = pack4_bytes(y[4], y[5], y[6], y[7]);
 }
@@ -485,10 +497,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
           } else if ((__float_as_uint(step) & 0x7F800000u) != 0) {
             const float r = __frcp_rn(step);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float q1 = __fmul_rn(f[i], r);
-              f[i] = fmaf(fmaf(-q1, step, f[i]), r, q1);   // fl32(w / step)
-            }
+            for (int i = 0; i < 16; ++i) f[i] = quotient_corrected(f[i], step, r);   // fl32(w / step)
           } else {
 #pragma unroll
             for (int i = 0; i < 16; ++i) f[i] = __fdiv_rn(f[i], step);
@@ -531,7 +540,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
     uint32_t* const dst =
         packed + ((static_cast<int64_t>(tn) * G + g) * kQRows + row) * kRowWords + (kRowWords / 2) * h;
     if constexpr (W8) {
-      if ((__half_as_ushort(s16) & 0x7C00u) != 0) {
+      if (scale_fast(s16)) {
         // chunks in the rotated order (j + 4 h) mod 8, as in the INT4 path;
         // chunk c's two words are words 2c, 2c + 1 of the half row, so the
         // j-th pair of chunks goes to 16-byte store (j + 2 h) mod 4
@@ -560,7 +569,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
                                  kGroup + static_cast<uint64_t>(g * kGroup + 64 * h);
       const uint32_t k0 = static_cast<uint32_t>(q.seed);
       const uint32_t k1 = static_cast<uint32_t>(q.seed >> 32);
-      const bool normal = (__half_as_ushort(s16) & 0x7C00u) != 0;
+      const bool normal = scale_fast(s16);
 #pragma unroll 1
       for (int c = 0; c < 8; ++c) {
         float f[8];
@@ -568,15 +577,14 @@ __global__ void __launch_bounds__(kQThreads, 1)
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           if (normal) {
-            const float q1 = __fmul_rn(f[i], r);
-            f[i] = fmaf(fmaf(-q1, s, f[i]), r, q1);   // fl32(w / s), as in the RTN mode
+            f[i] = quotient_corrected(f[i], s, r);   // fl32(w / s), as in the RTN mode
           } else {
             f[i] = __fdiv_rn(f[i], s);
           }
         }
         dst[c] = codes_stochastic(f, e_row + 8 * c, k0, k1);
       }
-    } else if ((__half_as_ushort(s16) & 0x7C00u) != 0) {
+    } else if (scale_fast(s16)) {
       uint32_t words[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
@@ -690,6 +698,64 @@ cudaError_t launch_quantize_mode(const QuantizeProblem* probs, int count, int nu
   return cudaLaunchKernelEx(&cfg, kernel, q, error_word, timeout_ns);
 }
 
+// Self test of quotient_corrected against the IEEE division __fdiv_rn.
+// Block b takes one divisor d and every finite bf16 value w (both signs)
+// with |w| <= bound * d; a thread counts the w whose corrected quotient
+// differs from fl32(w / d) (compared as floats, so +0 and -0 are equal: both
+// round to code 0), and one atomic per warp adds the counts to
+// counts[0] (pairs checked) and counts[1] (mismatches).
+//   mode 0 (INT4): d = every normal finite fp16 scale, bound 7.5 (a normal
+//     scale s = fp16(amax / 7) keeps |w| <= amax <= 7.0035 s);
+//   mode 1 (INT8): the same scales, bound 127.5;
+//   mode 2 (NVFP4 steps): d = fl32(e4m3(c) * g) for the E4M3 codes c = 1 ..
+//     126 and 512 tensor scales g = 2^e (1 + f), e in [-40, 40] and f from a
+//     fixed integer hash; bound 8 (codes saturate at 6), normal d only (the
+//     kernel divides by a subnormal step with __fdiv_rn).
+__global__ void __launch_bounds__(256) quotient_selftest_kernel(int mode,
+                                                                unsigned long long* counts) {
+  float d, bound;
+  if (mode == 2) {
+    const uint32_t c = 1u + blockIdx.x % 126u;
+    uint32_t h = blockIdx.x / 126u;
+    h = (h ^ 61u) ^ (h >> 16);
+    h *= 9u;
+    h ^= h >> 4;
+    h *= 0x27D4EB2Du;
+    h ^= h >> 15;
+    const int ex = static_cast<int>(h % 81u) - 40;
+    const float g = __uint_as_float(static_cast<uint32_t>(127 + ex) << 23 | (h >> 9));
+    d = __fmul_rn(e4m3_value(c), g);
+    bound = 8.0f;
+    if ((__float_as_uint(d) & 0x7F800000u) == 0u || (__float_as_uint(d) & 0x7F800000u) == 0x7F800000u)
+      return;
+  } else {
+    d = __half2float(__ushort_as_half(static_cast<unsigned short>(0x0400u + blockIdx.x)));
+    bound = mode == 0 ? 7.5f : 127.5f;
+  }
+  const float r = __frcp_rn(d);
+  const float lim = bound * d;
+  unsigned long long checked = 0, bad = 0;
+  for (uint32_t b = threadIdx.x; b < 0x7F80u; b += blockDim.x) {
+    const float w = __uint_as_float(b << 16);
+    if (w > lim) continue;
+#pragma unroll
+    for (int sgn = 0; sgn < 2; ++sgn) {
+      const float x = sgn ? -w : w;
+      checked += 1;
+      bad += quotient_corrected(x, d, r) != __fdiv_rn(x, d) ? 1 : 0;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    checked += __shfl_xor_sync(0xFFFFFFFFu, checked, o);
+    bad += __shfl_xor_sync(0xFFFFFFFFu, bad, o);
+  }
+  if ((threadIdx.x & 31) == 0) {
+    atomicAdd(counts, checked);
+    if (bad != 0) atomicAdd(counts + 1, bad);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_rtn_quantize_group(const QuantizeProblem* probs, int count, int num_sms,
@@ -728,6 +794,16 @@ cudaError_t launch_fp4_quantize(const void* W, int64_t N, int64_t K, void* packe
   if (e != cudaSuccess) return e;
   return launch_quantize_mode(&p, 1, num_sms, error_word, timeout_ns, stream, kModeNv4, 0,
                               tensor_scale);
+}
+
+cudaError_t launch_quotient_selftest(int mode, unsigned long long* counts, cudaStream_t stream) {
+  if (mode < 0 || mode > 2 || counts == nullptr) return cudaErrorInvalidValue;
+  cudaError_t e = cudaMemsetAsync(counts, 0, 2 * sizeof(unsigned long long), stream);
+  if (e != cudaSuccess) return e;
+  // mode 0, 1: the fp16 scales 0x0400 .. 0x7BFF; mode 2: 126 codes x 512 g
+  const unsigned blocks = mode == 2 ? 126u * 512u : 0x7C00u - 0x0400u;
+  quotient_selftest_kernel<<<blocks, 256, 0, stream>>>(mode, counts);
+  return cudaGetLastError();
 }
 
 }  // namespace w4a16
