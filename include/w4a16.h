@@ -376,12 +376,22 @@ int w4a16_selftest_wait_timeout(uint64_t timeout_ns, void* stream);
  *   mode 0: every normal finite fp16 scale s and every finite bf16 w with
  *           |w| <= 7.5 s (the INT4 modes' whole domain);
  *   mode 1: the same scales, |w| <= 127.5 s (INT8);
- *   mode 2: NVFP4 steps fl32(e4m3 * g) for the 126 nonzero E4M3 codes and
- *           512 fixed tensor scales g in [2^-40, 2^41), |w| <= 8 step.
- * counts: device uint64[2], 8-byte aligned, caller-owned; the call zeroes it
- * on `stream`, then counts[0] = pairs checked, counts[1] = quotients that
- * differ (+0 and -0 count as equal).  Errors: W4A16_ERR_INVALID_ARG (null),
- * W4A16_ERR_UNSUPPORTED (mode), W4A16_ERR_ALIGNMENT, W4A16_ERR_CUDA.
+ *   mode 2: fp32 divisors of the NVFP4 form fl32(e4m3 * g) for the 126
+ *           nonzero E4M3 codes and 512 fixed tensor scales g in [2^-40,
+ *           2^41), |w| <= 8 d, E2M1 codes.  No kernel uses the corrected
+ *           quotient for such divisors (the NVFP4 quantize divides with
+ *           IEEE division): this mode shows why, it finds codes that differ.
+ * counts: device uint64[4], 8-byte aligned, caller-owned; the call zeroes it
+ * on `stream`, then counts[0] = pairs checked, counts[1] = pairs whose
+ * stored code differs (rint of the quotient, ties to even, for INT4 and
+ * INT8; the E2M1 code in mode 2): the bit-exactness claim, counts[2] =
+ * quotients that differ where |w| >= 2^-100 (the remainder is then a normal
+ * float, computed exactly), counts[3] = quotients that differ anywhere (for
+ * smaller |w| the remainder can underflow; with a normal fp16 scale those
+ * quotients are below 2^-86 and round to code 0 either way).  +0 and -0
+ * count as equal.
+ * Errors: W4A16_ERR_INVALID_ARG (null), W4A16_ERR_UNSUPPORTED (mode),
+ * W4A16_ERR_ALIGNMENT, W4A16_ERR_CUDA.
  */
 int w4a16_selftest_quotient(int mode, unsigned long long* counts, void* stream);
 

@@ -263,16 +263,18 @@ def w4a16_repack_rowmajor(packed_rowmajor: torch.Tensor, N: int, K: int,
     return packed
 
 
-def selftest_quotient(mode: int, device=None) -> tuple[int, int]:
+def selftest_quotient(mode: int, device=None) -> dict:
     """Run w4a16_selftest_quotient (0: INT4 scales, 1: INT8 scales, 2: NVFP4
-    steps) on ``device`` and return ``(pairs checked, mismatches)``
+    steps) on ``device`` and return its counts: pairs checked, codes that
+    differ, quotients that differ in the normal range and anywhere
     (synchronises)."""
     dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
-    counts = torch.zeros(2, dtype=torch.int64, device=dev)
+    counts = torch.zeros(4, dtype=torch.int64, device=dev)
     _check(lib().w4a16_selftest_quotient(int(mode), counts.data_ptr(), _stream_handle(dev)),
            "w4a16_selftest_quotient")
-    c = counts.cpu().tolist()
-    return int(c[0]), int(c[1])
+    c = [int(v) for v in counts.cpu().tolist()]
+    return dict(checked=c[0], code_mismatches=c[1], quotient_mismatches_normal=c[2],
+                quotient_mismatches=c[3])
 
 
 # ------------------------------------------------------------------- GEMM

@@ -180,7 +180,8 @@ cudaError_t launch_repack_rowmajor(const void* rowmajor, int64_t N, int64_t K, v
 
 // Self test of the quantizer's corrected quotient against the IEEE division
 // (quantize.cu): mode 0 INT4 scales, 1 INT8 scales, 2 NVFP4 steps; zeroes
-// counts[0..1] on `stream`, then adds the pairs checked and the mismatches.
+// counts[0..3] on `stream`, then adds the pairs checked, the codes that
+// differ, the quotients that differ in the normal range and anywhere.
 cudaError_t launch_quotient_selftest(int mode, unsigned long long* counts, cudaStream_t stream);
 
 // Failure-detection self test: one thread waits on an mbarrier nobody

@@ -71,8 +71,9 @@
 //   of the caller's tensor-scale pair; here g = fl32(amax / 2688) (1 for a
 //   zero tensor) is written to the first word; per block of 16, the scale
 //   code is E4M3_rn_sat(fl32(fl32(amax_b / 6) / g)) (cvt.rn.satfinite.e4m3x2)
-//   and the elements are fl32(w / fl32(s_b g)), the quotient corrected to the
-//   correctly rounded one as in the INT4 mode.
+//   and the elements are fl32(w / fl32(s_b g)) by IEEE division (the step
+//   is a full fp32 value, for which the one-step correction of the other
+//   modes is not always correctly rounded).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -136,12 +137,14 @@ __device__ __forceinline__ uint32_t pack8(const uint32_t (&y)[8]) {
 }
 
 // The quotient fl32(w / s) from r = fl32(1 / s): q1 = fl32(w r), the
-// remainder e = w - q1 s (exact: one fused multiply-add) and one correction
-// q2 = fl32(q1 + e r).  With r the correctly rounded reciprocal this gives
-// the correctly rounded quotient (Markstein's theorem) for a normal, finite
-// s.  Every quantize mode that divides by a normal scale uses this function,
-// and w4a16_selftest_quotient checks it against the IEEE division over
-// every scale and weight value the INT4 and INT8 modes can meet.
+// remainder e = w - q1 s (exact: one fused multiply-add, while it is a
+// normal float) and one correction q2 = fl32(q1 + e r) (Markstein's
+// refinement).  The INT4 and INT8 modes use it for normal, finite fp16
+// scales (11 significant bits), and w4a16_selftest_quotient checks it
+// against the IEEE division over every such scale and every bf16 weight
+// those modes can meet: no code differs, and no quotient differs where
+// |w| >= 2^-100.  For general fp32 divisors (the NVFP4 steps) the same
+// check finds codes that differ, so that mode divides with __fdiv_rn.
 __device__ __forceinline__ float quotient_corrected(float w, float s, float r) {
   const float q1 = __fmul_rn(w, r);
   const float e = fmaf(-q1, s, w);
@@ -491,13 +494,13 @@ __global__ void __launch_bounds__(kQThreads, 1)
           float f[16];
           unpack8(v0, *reinterpret_cast<float(*)[8]>(&f[0]));
           unpack8(v1, *reinterpret_cast<float(*)[8]>(&f[8]));
+          // IEEE division: the step is a full fp32 value (fl32(e4m3 * g)),
+          // for which the one-step reciprocal correction is not always the
+          // correctly rounded quotient (w4a16_selftest_quotient finds E2M1
+          // codes that differ), unlike the fp16 scales of the other modes
           if (step == 0.0f) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) f[i] = 0.0f;
-          } else if ((__float_as_uint(step) & 0x7F800000u) != 0) {
-            const float r = __frcp_rn(step);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) f[i] = quotient_corrected(f[i], step, r);   // fl32(w / step)
           } else {
 #pragma unroll
             for (int i = 0; i < 16; ++i) f[i] = __fdiv_rn(f[i], step);
@@ -700,17 +703,25 @@ cudaError_t launch_quantize_mode(const QuantizeProblem* probs, int count, int nu
 
 // Self test of quotient_corrected against the IEEE division __fdiv_rn.
 // Block b takes one divisor d and every finite bf16 value w (both signs)
-// with |w| <= bound * d; a thread counts the w whose corrected quotient
-// differs from fl32(w / d) (compared as floats, so +0 and -0 are equal: both
-// round to code 0), and one atomic per warp adds the counts to
-// counts[0] (pairs checked) and counts[1] (mismatches).
+// with |w| <= bound * d.  For each pair it compares what the quantizer
+// stores, the code (rint, ties to even, of the quotient for INT4 and INT8;
+// the E2M1 conversion for NVFP4), and the quotient itself; one atomic per
+// warp adds the counts to counts[0] (pairs checked), counts[1] (codes that
+// differ), counts[2] (quotients that differ where |w| >= 2^-100: then the
+// remainder w - q1 d, about 2^-24 |w|, is a normal float and the fused
+// multiply-add gives it exactly) and counts[3] (quotients that differ
+// anywhere; for |w| < 2^-100 and a normal fp16 scale the quotient is below
+// 2^-86, so its code is 0 either way).  Floats compare as values, so +0 and
+// -0 are equal.
 //   mode 0 (INT4): d = every normal finite fp16 scale, bound 7.5 (a normal
 //     scale s = fp16(amax / 7) keeps |w| <= amax <= 7.0035 s);
 //   mode 1 (INT8): the same scales, bound 127.5;
-//   mode 2 (NVFP4 steps): d = fl32(e4m3(c) * g) for the E4M3 codes c = 1 ..
-//     126 and 512 tensor scales g = 2^e (1 + f), e in [-40, 40] and f from a
-//     fixed integer hash; bound 8 (codes saturate at 6), normal d only (the
-//     kernel divides by a subnormal step with __fdiv_rn).
+//   mode 2 (fp32 divisors of the NVFP4 form): d = fl32(e4m3(c) * g) for the
+//     E4M3 codes c = 1 .. 126 and 512 tensor scales g = 2^e (1 + f), e in
+//     [-40, 40] and f from a fixed integer hash; bound 8 (E2M1 codes
+//     saturate at 6); normal d only.  No kernel uses the corrected quotient
+//     for such divisors: this mode is the check that shows why (it finds
+//     codes that differ), so the NVFP4 quantize divides with __fdiv_rn.
 __global__ void __launch_bounds__(256) quotient_selftest_kernel(int mode,
                                                                 unsigned long long* counts) {
   float d, bound;
@@ -734,25 +745,36 @@ __global__ void __launch_bounds__(256) quotient_selftest_kernel(int mode,
   }
   const float r = __frcp_rn(d);
   const float lim = bound * d;
-  unsigned long long checked = 0, bad = 0;
+  unsigned long long cnt[4] = {0, 0, 0, 0};
   for (uint32_t b = threadIdx.x; b < 0x7F80u; b += blockDim.x) {
     const float w = __uint_as_float(b << 16);
     if (w > lim) continue;
 #pragma unroll
     for (int sgn = 0; sgn < 2; ++sgn) {
       const float x = sgn ? -w : w;
-      checked += 1;
-      bad += quotient_corrected(x, d, r) != __fdiv_rn(x, d) ? 1 : 0;
+      const float q = quotient_corrected(x, d, r);
+      const float ref = __fdiv_rn(x, d);
+      bool code_differs;
+      if (mode == 2) {
+        code_differs = e2m1x2(q, q) != e2m1x2(ref, ref);
+      } else {
+        code_differs = __fadd_rn(q, kRoundMagic) != __fadd_rn(ref, kRoundMagic);
+      }
+      cnt[0] += 1;
+      cnt[1] += code_differs ? 1 : 0;
+      cnt[2] += (q != ref && w >= 0x1p-100f) ? 1 : 0;
+      cnt[3] += q != ref ? 1 : 0;
     }
   }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    checked += __shfl_xor_sync(0xFFFFFFFFu, checked, o);
-    bad += __shfl_xor_sync(0xFFFFFFFFu, bad, o);
+  for (int i = 0; i < 4; ++i) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) cnt[i] += __shfl_xor_sync(0xFFFFFFFFu, cnt[i], o);
   }
   if ((threadIdx.x & 31) == 0) {
-    atomicAdd(counts, checked);
-    if (bad != 0) atomicAdd(counts + 1, bad);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (cnt[i] != 0) atomicAdd(counts + i, cnt[i]);
   }
 }
 
@@ -798,7 +820,7 @@ cudaError_t launch_fp4_quantize(const void* W, int64_t N, int64_t K, void* packe
 
 cudaError_t launch_quotient_selftest(int mode, unsigned long long* counts, cudaStream_t stream) {
   if (mode < 0 || mode > 2 || counts == nullptr) return cudaErrorInvalidValue;
-  cudaError_t e = cudaMemsetAsync(counts, 0, 2 * sizeof(unsigned long long), stream);
+  cudaError_t e = cudaMemsetAsync(counts, 0, 4 * sizeof(unsigned long long), stream);
   if (e != cudaSuccess) return e;
   // mode 0, 1: the fp16 scales 0x0400 .. 0x7BFF; mode 2: 126 codes x 512 g
   const unsigned blocks = mode == 2 ? 126u * 512u : 0x7C00u - 0x0400u;
