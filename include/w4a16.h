@@ -360,6 +360,27 @@ int w4a16_get_device_error(void* stream);
 void w4a16_set_wait_timeout_ns(uint64_t ns);
 
 /*
+ * Declare the GEMM weights static (enable != 0) or not (0, the default), for
+ * GEMM launches from now on (every w4a16_gemm* and w8a16/fp4a16 GEMM call of
+ * the process, and the tuners' timings).  Static means: no kernel that can
+ * run just before a GEMM launch on the same stream writes that GEMM's packed
+ * codes or scales; that holds for weights quantized at load ("Kernel
+ * dispatch and Humming quantization in PhyAI", section "Humming makes the
+ * separation useful": post-training quantization at load), and fails for a
+ * quantize launched on the stream right before the GEMM that reads its
+ * output.  With static weights a GEMM launched behind another kernel
+ * (programmatic dependent launch) starts copying the codes and scales of its
+ * first pipeline stages before that kernel has finished; activations, bias,
+ * workspace and output are still touched only after it finished.  With the
+ * declaration broken the GEMM may read stale weights.  Not synchronised with
+ * launches in flight: change it only between launches.
+ */
+void w4a16_set_weights_static(int enable);
+
+/* The current declaration of w4a16_set_weights_static (0 or 1). */
+int w4a16_weights_static(void);
+
+/*
  * Failure-detection self test: launch one small kernel whose thread waits on
  * an mbarrier that nothing ever arrives at, with a limit of `timeout_ns`;
  * the wait runs out, the kernel records W4A16_ERR_TIMEOUT and returns.

@@ -239,3 +239,53 @@ def test_workloads_full_size_sampled(w4, case):
                                                        np.random.default_rng(0).integers(0, M, 11)])
     y_ref = reference(A, packed, scales, b, rows=rows)
     check_gemm_close(Y[torch.as_tensor(rows, device=Y.device)], y_ref, what=case.name)
+
+
+def test_static_weights_prefetch_back_to_back(w4):
+    """With the weights declared static (w4a16_set_weights_static), each GEMM
+    copies its first codes and scales before the previous kernel on the
+    stream finishes.  Back-to-back launches in one CUDA graph, every launch on
+    other weights and activations and each writing its own output, must still
+    give each launch's own result (every variant, a stream-K and a
+    data-parallel shape); a launch that used another launch's operands would
+    miss the tolerance."""
+    cases = [synthetic.Case("static_m16_n1024_k2048", 16, 1024, 2048, 31, bias=True),
+             synthetic.Case("static_m64_n256_k4096", 64, 256, 4096, 32)]
+    try:
+        w4.w4a16_set_weights_static(True)
+        assert w4.w4a16_weights_static()
+        for case in cases:
+            ops = []
+            for r in range(3):
+                c = synthetic.Case(case.name, case.M, case.N, case.K, case.seed + 10 * r, bias=case.bias)
+                W, A, b, packed, scales = make_operands(w4, c)
+                ops.append((A.cuda(), None if b is None else b.cuda(), packed, scales,
+                            reference(A, packed, scales, b)))
+            torch.cuda.synchronize()   # the quantizes are done before any GEMM reads early
+            for v in variant_ids(w4):
+                if not w4.w4a16_variant_eligible(v, case.M, case.N, case.K):
+                    continue
+                need = w4.w4a16_variant_workspace_bytes(v, case.M, case.N, case.K)
+                ws = torch.zeros(max(need, 256), dtype=torch.uint8, device="cuda")
+                Ys = [torch.full((case.M, case.N), float("nan"), dtype=torch.bfloat16, device="cuda")
+                      for _ in ops]
+                for (A, b, p, s, _), Y in zip(ops, Ys):   # outside the capture: attributes
+                    w4.w4a16_gemm(A, p, s, bias=b, Y=Y, workspace=ws, variant=v)
+                g = torch.cuda.CUDAGraph()
+                cs = torch.cuda.Stream()
+                cs.wait_stream(torch.cuda.current_stream())
+                with torch.cuda.stream(cs):
+                    with torch.cuda.graph(g, stream=cs):
+                        for _ in range(2):
+                            for (A, b, p, s, _), Y in zip(ops, Ys):
+                                w4.w4a16_gemm(A, p, s, bias=b, Y=Y, workspace=ws, variant=v, stream=cs)
+                torch.cuda.current_stream().wait_stream(cs)
+                for Y in Ys:
+                    Y.fill_(float("nan"))
+                g.replay()
+                torch.cuda.synchronize()
+                for (_, _, _, _, y_ref), Y in zip(ops, Ys):
+                    check_gemm_close(Y, y_ref, what=f"static {w4.w4a16_variant_name(v)}")
+    finally:
+        w4.w4a16_set_weights_static(False)
+    assert w4.w4a16_get_device_error() == w4.W4A16_OK

@@ -121,6 +121,8 @@ SIGNATURES = [
     ("w4a16_table_load", ctypes.c_int, [ctypes.c_char_p]),
     ("w4a16_get_device_error", ctypes.c_int, [_vp]),
     ("w4a16_set_wait_timeout_ns", None, [ctypes.c_uint64]),
+    ("w4a16_set_weights_static", None, [ctypes.c_int]),
+    ("w4a16_weights_static", ctypes.c_int, []),
     ("w4a16_selftest_wait_timeout", ctypes.c_int, [ctypes.c_uint64, _vp]),
     ("w4a16_launch_count", ctypes.c_uint64, []),
     ("w4a16_last_error_detail", ctypes.c_char_p, []),
@@ -781,6 +783,17 @@ def w4a16_selftest_wait_timeout(timeout_ns: int, stream=None, device=None) -> No
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
     _check(lib().w4a16_selftest_wait_timeout(timeout_ns, _stream_handle(dev, stream)),
            "w4a16_selftest_wait_timeout")
+
+
+def w4a16_set_weights_static(enable: bool) -> None:
+    """Declare the GEMM weights static (w4a16_set_weights_static): no kernel
+    that can run just before a GEMM on its stream writes that GEMM's packed
+    codes or scales, so the GEMM may start copying them early."""
+    lib().w4a16_set_weights_static(1 if enable else 0)
+
+
+def w4a16_weights_static() -> bool:
+    return bool(lib().w4a16_weights_static())
 
 
 def w4a16_launch_count() -> int:

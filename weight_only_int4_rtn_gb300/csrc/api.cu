@@ -36,6 +36,9 @@ __device__ uint32_t g_error_word;
 namespace {
 
 std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+// w4a16_set_weights_static: GEMM launches may read their weights before the
+// dependency wait of programmatic dependent launch
+std::atomic<int> g_weights_static{0};
 thread_local char g_error_detail[256] = "";
 
 // Record a failed CUDA call for w4a16_last_error_detail and clear the
@@ -435,6 +438,7 @@ int run_gemm_v(const Variant& v, const void* A, int64_t M, int64_t N, int64_t K,
   p.act_f16 = act_f16;
   p.tensor_scale = tensor_scale;
   p.swiglu = swiglu;
+  p.weights_static = g_weights_static.load() != 0;
   if (log_enabled())
     std::fprintf(stderr, "w4a16: gemm M=%lld N=%lld K=%lld variant=%s grid=%d dp_tiles=%d sk_units=%lld\n",
                  static_cast<long long>(M), static_cast<long long>(N), static_cast<long long>(K),
@@ -1096,6 +1100,7 @@ int launch_group_plan(const GroupPlan& plan, const w4a16_gemm_problem* problems,
     p.error_word = dev.error_word;
     p.timeout_ns = g_timeout_ns.load();
     p.act_f16 = act_f16 != 0;
+    p.weights_static = g_weights_static.load() != 0;
     grp.s[i] = plan.s[i];
   }
   if (log_enabled())
@@ -1553,6 +1558,10 @@ int w4a16_get_device_error(void* stream) {
 }
 
 void w4a16_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns == 0 ? 1 : ns); }
+
+void w4a16_set_weights_static(int enable) { g_weights_static.store(enable != 0 ? 1 : 0); }
+
+int w4a16_weights_static(void) { return g_weights_static.load(); }
 
 int w4a16_selftest_wait_timeout(uint64_t timeout_ns, void* stream) {
   DeviceInfo dev;

@@ -137,6 +137,9 @@ struct Args {
   int dp_tiles;
   int sk_units;
   int act_3d;                  // activation map is 3-D: both 64-k halves in one copy
+  int prefetch_w;              // weights are not written by the previous kernel on
+                               // the stream: the codes and scales of this many
+                               // first units go out before the dependency wait
   const __half* scales;        // [K/128, N]; the group-mode readout reads its scales here
   const float* out_scale;      // NVFP4: the tensor scale g, applied to the fp32 sums
   const uint16_t* bias;        // [N] activation type (bf16 or fp16 bits)
@@ -297,11 +300,12 @@ __device__ __forceinline__ int sk_owner(int u, int C, int sk_units) {
 
 struct Shared {
   uint64_t full[16];          // a shared-memory stage's copies landed
-  uint64_t afull[kMaxAStages];   // a TMEM weight stage is written
-  uint64_t aempty[kMaxAStages];  // a TMEM weight stage's MMAs completed
+  uint64_t afull[kMaxAStages];   // a TMEM weight stage is written (it is free
+                                 // again when its unit's MMAs completed)
   uint64_t unit_done[32];     // per lane a ring: a unit's MMAs completed
   uint64_t dfull[8];          // dequant mode: a run on a tile is accumulated
-  uint64_t dempty[8];         // the readout drained accumulator buffer(s)
+  uint64_t dempty[8];         // the readout drained an accumulator buffer
+                              // (group mode: buffer dl of lane p at p * DL + dl)
   uint64_t pair_done[8];       // group mode: both lanes' units of a pair completed
   uint64_t mma_done[2];
   uint64_t rsync;             // readout warps' barrier (split-tile fixup)
@@ -836,29 +840,39 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG, WF>::kThreads, 1)
 #endif
   if (threadIdx.x == 0) W4A16_TRACE_POINT(0);
   if (threadIdx.x == 0) W4A16_TRACE_UNIT(9, 0);
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) ptx::mbar_init(&sh->full[s], 1);
-    for (int s = 0; s < L * RL; ++s) ptx::mbar_init(&sh->unit_done[s], 1);
-    for (int s = 0; s < C::kAS; ++s) {
-      ptx::mbar_init(&sh->afull[s], 4);
-      ptx::mbar_init(&sh->aempty[s], 1);
-    }
-    for (int s = 0; s < DB; ++s) {
+  {
+    // barriers initialised in parallel, one per thread (one thread doing all
+    // of them in turn costs several hundred cycles of the launch's head)
+    const int t = static_cast<int>(threadIdx.x);
+    bool init = true;
+    if (t < STAGES) {
+      ptx::mbar_init(&sh->full[t], 1);
+    } else if (t >= 32 && t < 32 + L * RL) {
+      ptx::mbar_init(&sh->unit_done[t - 32], 1);
+    } else if (t >= 64 && t < 64 + C::kAS) {
+      ptx::mbar_init(&sh->afull[t - 64], 4);
+    } else if (t >= 96 && t < 96 + DB) {
       // dequant mode: both lanes' MMA threads arrive (L = 2)
-      ptx::mbar_init(&sh->dfull[s], GRP ? 1 : L);
-      ptx::mbar_init(&sh->dempty[s], 4);
+      ptx::mbar_init(&sh->dfull[t - 96], GRP ? 1 : L);
+      ptx::mbar_init(&sh->dempty[t - 96], 4);
+    } else if (t >= 128 && t < 128 + kPairRing) {
+      ptx::mbar_init(&sh->pair_done[t - 128], 2);
+    } else if (t == 160) {
+      ptx::mbar_init(&sh->mma_done[0], 1);
+      ptx::mbar_init(&sh->mma_done[1], 1);
+      ptx::mbar_init(&sh->rsync, 4);
+      sh->abort_flag = 0;
+      sh->fixup_last = 0;
+      sh->fixup_defer = 0;
+    } else {
+      init = false;
     }
-    for (int s = 0; s < kPairRing; ++s) ptx::mbar_init(&sh->pair_done[s], 2);
-    ptx::mbar_init(&sh->mma_done[0], 1);
-    ptx::mbar_init(&sh->mma_done[1], 1);
-    ptx::mbar_init(&sh->rsync, 4);
-    sh->abort_flag = 0;
-    sh->fixup_last = 0;
-    sh->fixup_defer = 0;
-    ptx::fence_mbar_init();
-    ptx::prefetch_tmap(tm_act);
-    ptx::prefetch_tmap(tm_w);
-    ptx::prefetch_tmap(tm_s);
+    if (init) ptx::fence_mbar_init();
+    if (t == 192) {
+      ptx::prefetch_tmap(tm_act);
+      ptx::prefetch_tmap(tm_w);
+      ptx::prefetch_tmap(tm_s);
+    }
   }
   if (warp == 1) {
     ptx::tmem_alloc(&sh->tmem_base, kTmemCols);
@@ -877,33 +891,61 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG, WF>::kThreads, 1)
   // kernel's outputs, so nothing is read before the dependency wait.
   Sched sched;
   sched.init(a, cta, ctas);
-  UnitIter it;
-  it.init(sched);
   const int total = sched.total;
-  ptx::grid_dependency_wait();
-  ptx::grid_launch_dependents();
-  if (threadIdx.x == 0) W4A16_TRACE_POINT(2);
-  if (threadIdx.x == 0) W4A16_TRACE_UNIT(9, 2);
+  // Every role but the producers waits for the previous kernel on the stream
+  // here (its outputs may be this kernel's inputs); the producers wait in
+  // their own branch, after any early weight copies.
+  const bool producer = warp == 0 || warp == 2;
+  if (!producer) {
+    ptx::grid_dependency_wait();
+    ptx::grid_launch_dependents();
+  }
+  if (threadIdx.x == 32) W4A16_TRACE_POINT(2);
+  if (threadIdx.x == 32) W4A16_TRACE_UNIT(9, 2);
 
-  if (warp == 0 || warp == 2) {
+  if (producer) {
     // ----------------------------------------------------- TMA producers
     // Even units from warp 0, odd units from warp 2 (with two lanes: one
-    // producer per lane).
-    if (lane == 0) {
+    // producer per lane).  A producer walks the CTA's runs (consecutive
+    // units on one tile): a run's coordinates are worked out once, a unit's
+    // by additions, so that the one issuing thread spends its time on the
+    // copies.  With prefetch_w, the codes and scales of the first stages go
+    // out before the dependency wait (the weights are not the previous
+    // kernel's outputs) and the activations of those stages after it.
+    if (lane != 0) {
+      ptx::grid_dependency_wait();
+    } else {
       const int mine = warp == 0 ? 0 : 1;
       int issued = -1;
-      for (int i = 0; i < total; ++i) {
-        const Unit u = it.next();
-        if ((i & 1) != mine) continue;
-        const int stage = stage_of(i);
-        // the unit that last used this stage is i - STAGES (same lane)
-        if (i >= STAGES && !wait_one(done_bar(i - STAGES), done_parity(i - STAGES), wc)) break;
-        if (i == 0) W4A16_TRACE_UNIT(9, 3);
-        W4A16_TRACE_UNIT(13, i);
-        const int m0 = (u.tile / a.n_tiles) * BA;
+      auto walk = [&](int limit, auto&& fn) -> bool {
+        SegCursor cur;
+        cur.init(sched);
+        int i0 = 0;
+        while (i0 < total && i0 < limit) {
+          Unit r;
+          int kb0, len;
+          cur.next(r, kb0, len, a.dp_tiles);
+          const int mt = r.tile / a.n_tiles;
+          const int tn = r.tile - mt * a.n_tiles;
+          const int m0 = mt * BA;
+          const int wrow0 = tn * a.KB * UG * kTileW;
+          const int sx = tn * kTileW;
+          for (int i = i0 + ((i0 & 1) != mine ? 1 : 0); i < i0 + len && i < limit; i += 2) {
+            const int g0 = (kb0 + i - i0) * UG;   // the unit's first group
+            if (!fn(i, m0, wrow0 + g0 * kTileW, sx, g0)) return false;
+          }
+          i0 += len;
+        }
+        return true;
+      };
+      // the unit's codes (UG consecutive 8 KiB tiles of the tiled storage:
+      // one contiguous block) and its scales
+      auto issue_w = [&](int stage, int wrow, int sx, int g0) {
         ptx::mbar_arrive_expect_tx(&sh->full[stage], C::kTx);
-        if (i == 0) W4A16_TRACE_UNIT(9, 4);
-        const int g0 = u.kb * UG;   // the unit's first group
+        ptx::tma_load_2d(w_tile(stage), tm_w, &sh->full[stage], 0, wrow);
+        ptx::tma_load_2d(s_tile(stage, 0), tm_s, &sh->full[stage], sx, g0 * wf_blocks(WF));
+      };
+      auto issue_a = [&](int stage, int m0, int g0) {
         if (a.act_3d) {
           ptx::tma_load_3d(act_box(stage, 0), tm_act, &sh->full[stage], 0, m0, g0 * 2);
         } else {
@@ -911,21 +953,35 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG, WF>::kThreads, 1)
           for (int b = 0; b < 2 * UG; ++b)
             ptx::tma_load_2d(act_box(stage, b), tm_act, &sh->full[stage], g0 * kUnitK + 64 * b, m0);
         }
-        if (i == 0) W4A16_TRACE_UNIT(9, 5);
-        W4A16_TRACE_UNIT(14, i);
-        // the unit's codes: UG consecutive 8 KiB tiles of the tiled storage
-        // (one contiguous block)
-        ptx::tma_load_2d(w_tile(stage), tm_w, &sh->full[stage], 0,
-                         ((u.tile % a.n_tiles) * a.KB * UG + g0) * kTileW);
-        if (i == 0) W4A16_TRACE_UNIT(9, 6);
-        W4A16_TRACE_UNIT(15, i);
-        ptx::tma_load_2d(s_tile(stage, 0), tm_s, &sh->full[stage], (u.tile % a.n_tiles) * kTileW,
-                         g0 * wf_blocks(WF));
-        if (i == 0) W4A16_TRACE_UNIT(9, 7);
+      };
+      // a shallow prefetch: the copies of one TMA unit run in order, so every
+      // early weight copy sits ahead of the first activation copy
+      const int npre = a.prefetch_w < STAGES ? a.prefetch_w : STAGES;
+      if (npre > 0) {
+        walk(npre, [&](int i, int, int wrow, int sx, int g0) {
+          issue_w(stage_of(i), wrow, sx, g0);
+          return true;
+        });
+      }
+      ptx::grid_dependency_wait();
+      ptx::grid_launch_dependents();
+      walk(total, [&](int i, int m0, int wrow, int sx, int g0) {
+        const int stage = stage_of(i);
+        if (i < npre) {
+          issue_a(stage, m0, g0);
+        } else {
+          // the unit that last used this stage is i - STAGES (same producer)
+          if (i >= STAGES && !wait_one(done_bar(i - STAGES), done_parity(i - STAGES), wc))
+            return false;
+          W4A16_TRACE_UNIT(13, i);
+          issue_w(stage, wrow, sx, g0);
+          issue_a(stage, m0, g0);
+        }
         if (i <= 1) W4A16_TRACE_POINT(3);
         W4A16_TRACE_UNIT(0, i);
         issued = i;
-      }
+        return true;
+      });
       if (*reinterpret_cast<volatile int*>(&sh->abort_flag)) {
         // let this producer's copies still in flight land before the CTA exits
         for (int i = issued; i >= 0 && i > issued - STAGES; i -= 2) {
@@ -959,14 +1015,17 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG, WF>::kThreads, 1)
           for (int gi = 0; gi < UG; ++gi) {
             const int jg = UG * j + gi;
             const int as = gstage_of(mine, jg);
+            if (gi == 0) W4A16_TRACE_UNIT(23, 2 * j + mine);
             if (!wait_one(&sh->afull[as], (jg / AL) & 1, wc)) {
               ok = false;
               break;
             }
-            // the readout frees a lane's buffers in order: once it read the
-            // lane's unit j-1, buffers of units j .. j+DL-1 are free
-            if (gi == 0 && dl == 0 && j >= DL &&
-                !wait_one(&sh->dempty[mine], ((j / DL) - 1) & 1, wc)) {
+            if (gi == 0) W4A16_TRACE_UNIT(24, 2 * j + mine);
+            // accumulator buffer dl of this lane is free once the readout
+            // loaded the lane's unit j - DL (one barrier per buffer, so the
+            // MMAs run up to DL units ahead of the readout)
+            if (gi == 0 && j >= DL &&
+                !wait_one(&sh->dempty[mine * DL + dl], ((j / DL) - 1) & 1, wc)) {
               ok = false;
               break;
             }
@@ -984,7 +1043,6 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG, WF>::kThreads, 1)
               ptx::mma_f16kind_tmem_a(d_tmem, a_tmem + kk * 8, bdesc + boff, idesc,
                                       kk > 0 ? 1u : 0u);
             }
-            ptx::mma_commit(&sh->aempty[as]);   // the TMEM stage is free once these complete
             W4A16_TRACE_UNIT(gi == 0 ? 21 : 22, 2 * j + mine);
           }
           if (!ok) break;
@@ -1002,6 +1060,8 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG, WF>::kThreads, 1)
         int seg = 0;
         int db = 0;
         bool have = false;   // this lane issued into the current run's buffer
+        UnitIter it;
+        it.init(sched);
         for (int i = 0; i < total; ++i) {
           const Unit u = it.next();
           if (u.seg_first) {
@@ -1043,7 +1103,6 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG, WF>::kThreads, 1)
                 ptx::mma_f16kind_tmem_a(d_tmem, a_tmem + kk * 8, bdesc + boff, idesc,
                                         (kk > 0 || have) ? 1u : 0u);
               }
-              ptx::mma_commit(&sh->aempty[as]);   // the TMEM stage is free once these complete
               have = true;
             }
             if (!ok) break;
@@ -1189,9 +1248,9 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG, WF>::kThreads, 1)
         auto release = [&]() {
           ptx::tc_fence_before();
           __syncwarp();
-          if (lane == 0 && dl == DL - 1) {
-            ptx::mbar_arrive(&sh->dempty[0]);
-            if (has1) ptx::mbar_arrive(&sh->dempty[1]);
+          if (lane == 0) {
+            ptx::mbar_arrive(&sh->dempty[dl]);
+            if (has1) ptx::mbar_arrive(&sh->dempty[DL + dl]);
           }
           if (threadIdx.x == 32 * kReadoutWarp0) W4A16_TRACE_UNIT(7, i0);
         };
@@ -1248,6 +1307,8 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG, WF>::kThreads, 1)
       // scaled partials) before the bias
       float g_t = 1.0f;
       if constexpr (WF == kFmtNvfp4) g_t = __ldg(a.out_scale);
+      UnitIter it;
+      it.init(sched);
       for (int i = 0; i < total; ++i) {
         const Unit u = it.next();
         if (u.seg_first) {
@@ -1318,6 +1379,7 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG, WF>::kThreads, 1)
         // so waiting for those first proves the previous phase complete.
         if (i >= STAGES && !wait_warp(done_bar(i - STAGES), done_parity(i - STAGES), wc)) break;
       }
+      if (threadIdx.x == 32 * kDequantWarp0) W4A16_TRACE_UNIT(25, i);
       if (!wait_warp(&sh->full[stage], (j / SL) & 1, wc)) break;
       if (i == 0 && threadIdx.x == 32 * kDequantWarp0) W4A16_TRACE_POINT(6);
       if (threadIdx.x == 32 * kDequantWarp0) W4A16_TRACE_UNIT(1, i);
@@ -1340,12 +1402,18 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG, WF>::kThreads, 1)
 #pragma unroll
       for (int gi = 0; gi < UG; ++gi) {
         // the TMEM stage is free once the MMAs of its previous group (jg - AL
-        // of this lane) completed
+        // of this lane) completed: the completion of the unit that group
+        // belongs to (one commit per unit and issuer serves the stage, the
+        // shared-memory stage and the readout; a commit costs an issuing
+        // thread about as much as two MMAs)
         const int jg = UG * j + gi;
         const int as = gstage_of(p, jg);
-        if (jg >= AL && !wait_warp(&sh->aempty[as], ((jg / AL) - 1) & 1, wc)) {
-          ok = false;
-          break;
+        if (jg >= AL) {
+          const int iprev = L * ((jg - AL) / UG) + p;
+          if (!wait_warp(done_bar(iprev), done_parity(iprev), wc)) {
+            ok = false;
+            break;
+          }
         }
         if (threadIdx.x == 32 * kDequantWarp0) W4A16_TRACE_UNIT(gi == 0 ? 2 : 17, i);
         ptx::tc_fence_after();
@@ -1518,6 +1586,9 @@ cudaError_t launch_instance(const GemmGroup& grp, bool use_pdl, cudaStream_t str
     a.dp_tiles = s.dp_tiles;
     a.sk_units = static_cast<int>(s.sk_units);
     a.act_3d = act_3d;
+    // two units per producer: deeper early copies sit ahead of the first
+    // activation copy in the TMA queue and delay the start (measured)
+    a.prefetch_w = p.weights_static ? 4 : 0;
     a.scales = static_cast<const __half*>(p.scales);
     a.out_scale = p.tensor_scale;
     a.bias = static_cast<const uint16_t*>(p.bias);

@@ -101,6 +101,9 @@ struct GemmProblem {
   const float* tensor_scale = nullptr;   // NVFP4: the fp32 tensor scale g (device)
   bool swiglu = false;   // SwiGLU epilogue: rows 2f (up) and 2f + 1 (gate) give
                          // Y[M, N/2][f] = silu(gate) * up
+  bool weights_static = false;   // no kernel that may run just before this launch
+                                 // on its stream writes packed or scales: the GEMM
+                                 // may read them before the dependency wait
 };
 
 // Number of tiles of a problem under a configuration.
