@@ -266,10 +266,36 @@ int w4a16_tune(int64_t M, int64_t N, int64_t K, void* stream, int* out_variant);
 /* Put an entry in the table by hand (variant must be eligible). */
 int w4a16_table_set(int64_t M, int64_t N, int64_t K, int variant);
 
-/* Forget every table entry. */
+/*
+ * The other catalogues are chosen by measurement the same way, each with its
+ * own entries in the table ("Kernel dispatch and Humming quantization in
+ * PhyAI", section "Keep selection work out of repeated inference": every
+ * prepared kernel choice is tuned and memoized, not redone per call):
+ *   w4a16_tune_swiglu: the INT4 variants with the SwiGLU epilogue (its best
+ *     variant can differ from the plain GEMM's); w4a16_gemm_swiglu uses it;
+ *   w8a16_tune: the INT8 catalogue, used by w8a16_gemm;
+ *   fp4a16_tune: the FP4 catalogue, timed with `format`'s scales; one entry
+ *     per shape serves both FP4 formats in fp4a16_gemm.
+ * Same contract as w4a16_tune: allocates, synchronises and launches many
+ * kernels (never inside graph capture); the fastest id goes to *out_variant
+ * (may be NULL).  W4A16_ERR_UNSUPPORTED for shapes the catalogue cannot run
+ * (SwiGLU: odd N; FP4: N % 16, unknown format).  The *_table_set calls put
+ * an entry by hand (W4A16_ERR_NO_VARIANT if the variant is not eligible).
+ */
+int w4a16_tune_swiglu(int64_t M, int64_t N, int64_t K, void* stream, int* out_variant);
+int w8a16_tune(int64_t M, int64_t N, int64_t K, void* stream, int* out_variant);
+int fp4a16_tune(int format, int64_t M, int64_t N, int64_t K, void* stream, int* out_variant);
+int w4a16_swiglu_table_set(int64_t M, int64_t N, int64_t K, int variant);
+int w8a16_table_set(int64_t M, int64_t N, int64_t K, int variant);
+int fp4a16_table_set(int64_t M, int64_t N, int64_t K, int variant);
+
+/* Forget every table entry (all catalogues). */
 void w4a16_table_clear(void);
 
-/* Write / read the table as text lines "M N K variant_name". */
+/* Write / read the table (all catalogues) as text: lines "M N K variant"
+ * for the INT4 GEMM and "swiglu|int8|fp4 M N K variant" for the others; '#'
+ * starts a comment line.  W4A16_VARIANT_TABLE names a file loaded at the
+ * first selection. */
 int w4a16_table_save(const char* path);
 int w4a16_table_load(const char* path);
 
@@ -284,13 +310,22 @@ int w4a16_table_load(const char* path);
  * or output of another. */
 #define W4A16_MAX_GROUP 8
 
+/* Epilogue of one problem of a grouped GEMM. */
+#define W4A16_EPILOGUE_NONE 0    /* Y = A . dequant(W)^T + bias                 */
+#define W4A16_EPILOGUE_SWIGLU 1  /* w4a16_gemm_swiglu's: the weight's rows
+                                  * interleave up and gate (row 2f up f, row 2f+1
+                                  * gate f); Y is [M, N/2] = silu(gate) * up in
+                                  * fp32, one rounding to bf16; N even, bf16
+                                  * activations only                           */
+
 typedef struct {
   const void* A;             /* [M, K] activations (bf16; fp16 when act_f16) */
   const void* packed;        /* tiled codes of the [N, K] weight            */
   const void* scales;        /* [K/128, N] fp16                             */
   const void* bias_or_null;  /* [N], activation type, or NULL               */
-  void* Y;                   /* [M, N], activation type                     */
+  void* Y;                   /* [M, N] (or [M, N/2] for SwiGLU), act. type  */
   int64_t M, N, K;
+  int epilogue;              /* W4A16_EPILOGUE_NONE (0) or _SWIGLU          */
 } w4a16_gemm_problem;
 
 typedef struct {
@@ -333,9 +368,13 @@ size_t w4a16_gemm_grouped_workspace_bytes(const w4a16_gemm_problem* problems, in
 
 /* `count` (1 .. W4A16_MAX_GROUP) independent W4A16 GEMMs in one launch:
  * problem i computes Y_i = A_i . dequant(W_i)^T + bias_i as w4a16_gemm (or
- * w4a16_gemm_f16 when act_f16 != 0).  One variant serves the whole group
- * (variant = -1: chosen by the library).  Argument errors of any problem are
- * returned before anything is launched. */
+ * w4a16_gemm_f16 when act_f16 != 0), or, with epilogue
+ * W4A16_EPILOGUE_SWIGLU, Y_i = silu(gate) * up as w4a16_gemm_swiglu (bf16
+ * only: W4A16_ERR_UNSUPPORTED with act_f16, an odd N or another epilogue
+ * value), so an MLP block's gate/up projection runs in the same launch as
+ * its other projections.  One variant serves the whole group (variant = -1:
+ * chosen by the library).  Argument errors of any problem are returned
+ * before anything is launched. */
 int w4a16_gemm_grouped(const w4a16_gemm_problem* problems, int count, int group, int act_f16,
                        int variant, void* workspace, size_t workspace_bytes, void* stream);
 

@@ -169,8 +169,9 @@ def test_binding_rejects_cpu_tensors(built_lib):
 
 
 def test_group_structs_match_the_header():
-    # two pointer-sized fields per line of the C structs, no padding
-    assert ctypes.sizeof(w4.GemmProblem) == 5 * 8 + 3 * 8
+    # five pointers, three int64 and the int epilogue (padded to 8 bytes)
+    assert ctypes.sizeof(w4.GemmProblem) == 5 * 8 + 3 * 8 + 8
+    assert w4.GemmProblem.epilogue.offset == 64
     assert ctypes.sizeof(w4.QuantizeProblem) == 8 + 2 * 8 + 2 * 8
     text = open(HEADER).read()
     assert "#define W4A16_MAX_GROUP 8" in text and w4.MAX_GROUP == 8
@@ -219,3 +220,76 @@ def test_quotient_selftest_argument_errors(built_lib):
     assert L.w4a16_selftest_quotient(3, 16, None) == w4.W4A16_ERR_UNSUPPORTED
     assert L.w4a16_selftest_quotient(-1, 16, None) == w4.W4A16_ERR_UNSUPPORTED
     assert L.w4a16_selftest_quotient(0, 12, None) == w4.W4A16_ERR_ALIGNMENT
+
+
+def test_table_roundtrip_every_catalogue(built_lib, tmp_path):
+    """Entries of the INT4, SwiGLU, INT8 and FP4 catalogues are kept apart,
+    selected, saved and loaded back (no GPU: selection is host logic)."""
+    L = w4.lib()
+    w4.w4a16_table_clear()
+    M, N, K = 16, 2048, 2048
+    rule4, rule_sw = w4.w4a16_select_variant(M, N, K), None
+    rule8 = L.w8a16_select_variant(M, N, K)
+    rulef4 = L.fp4a16_select_variant(M, N, K)
+    v4 = w4.variant_id("tc_a32_grp_sk")
+    vsw = w4.variant_id("tc_a64_deq2_sk")
+    v8 = next(i for i in range(L.w8a16_variant_count())
+              if L.w8a16_variant_eligible(i, M, N, K) and i != rule8)
+    vf4 = next(i for i in range(L.fp4a16_variant_count())
+               if L.fp4a16_variant_eligible(i, M, N, K) and i != rulef4)
+    w4.w4a16_table_set(M, N, K, v4)
+    w4.w4a16_swiglu_table_set(M, N, K, vsw)
+    w4.w8a16_table_set(M, N, K, v8)
+    w4.fp4a16_table_set(M, N, K, vf4)
+    assert w4.w4a16_select_variant(M, N, K) == v4
+    assert L.w8a16_select_variant(M, N, K) == v8
+    assert L.fp4a16_select_variant(M, N, K) == vf4
+    p = str(tmp_path / "table_all.txt")
+    w4.w4a16_table_save(p)
+    text = open(p).read()
+    assert "swiglu 16 2048 2048 tc_a64_deq2_sk" in text
+    assert f"int8 16 2048 2048 {L.w8a16_variant_name(v8).decode()}" in text
+    assert f"fp4 16 2048 2048 {L.fp4a16_variant_name(vf4).decode()}" in text
+    w4.w4a16_table_clear()
+    assert w4.w4a16_select_variant(M, N, K) == rule4
+    assert L.w8a16_select_variant(M, N, K) == rule8
+    assert L.fp4a16_select_variant(M, N, K) == rulef4
+    w4.w4a16_table_load(p)
+    assert w4.w4a16_select_variant(M, N, K) == v4
+    assert L.w8a16_select_variant(M, N, K) == v8
+    assert L.fp4a16_select_variant(M, N, K) == vf4
+    # a variant of another catalogue is refused
+    with pytest.raises(w4.W4A16Error):
+        w4.w8a16_table_set(M, N, K, 10 ** 6)
+    with open(p, "a") as f:
+        f.write("int8 16 256 512 tc_a16_grp_sk\n")   # an INT4 name in the INT8 catalogue
+    with pytest.raises(w4.W4A16Error):
+        w4.w4a16_table_load(p)
+    with open(p, "w") as f:
+        f.write("nosuchtag 16 256 512 tc_a16_grp_sk\n")
+    with pytest.raises(w4.W4A16Error):
+        w4.w4a16_table_load(p)
+    w4.w4a16_table_clear()
+    del rule_sw
+
+
+def test_tuners_refuse_bad_shapes(built_lib):
+    L = w4.lib()
+    out = ctypes.c_int(-1)
+    assert L.w4a16_tune_swiglu(16, 250, 512, None, ctypes.byref(out)) == w4.W4A16_ERR_UNSUPPORTED
+    assert L.w8a16_tune(16, 256, 500, None, ctypes.byref(out)) == w4.W4A16_ERR_UNSUPPORTED
+    assert L.fp4a16_tune(1, 16, 264, 512, None, ctypes.byref(out)) == w4.W4A16_ERR_UNSUPPORTED
+    assert L.fp4a16_tune(7, 16, 256, 512, None, ctypes.byref(out)) == w4.W4A16_ERR_UNSUPPORTED
+
+
+def test_grouped_epilogue_argument_errors(built_lib):
+    L = w4.lib()
+    P = (w4.GemmProblem * 2)()
+    P[0] = w4.GemmProblem(16, 16, 16, None, 16, 4, 256, 512, 0)
+    P[1] = w4.GemmProblem(16, 16, 16, None, 16, 4, 256, 512, 2)        # no such epilogue
+    assert L.w4a16_gemm_grouped(P, 2, 128, 0, -1, None, 0, None) == w4.W4A16_ERR_UNSUPPORTED
+    P[1] = w4.GemmProblem(16, 16, 16, None, 16, 4, 264, 512, 1)        # SwiGLU needs N even...
+    P[1].N = 260
+    assert L.w4a16_gemm_grouped(P, 2, 128, 0, -1, None, 0, None) == w4.W4A16_ERR_UNSUPPORTED
+    P[1] = w4.GemmProblem(16, 16, 16, None, 16, 4, 256, 512, 1)
+    assert L.w4a16_gemm_grouped(P, 2, 128, 1, -1, None, 0, None) == w4.W4A16_ERR_UNSUPPORTED  # fp16

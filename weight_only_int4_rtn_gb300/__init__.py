@@ -35,7 +35,12 @@ class GemmProblem(ctypes.Structure):
     """Mirror of w4a16_gemm_problem (include/w4a16.h)."""
     _fields_ = [("A", ctypes.c_void_p), ("packed", ctypes.c_void_p), ("scales", ctypes.c_void_p),
                 ("bias_or_null", ctypes.c_void_p), ("Y", ctypes.c_void_p),
-                ("M", ctypes.c_int64), ("N", ctypes.c_int64), ("K", ctypes.c_int64)]
+                ("M", ctypes.c_int64), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("epilogue", ctypes.c_int)]
+
+
+EPILOGUE_NONE = 0
+EPILOGUE_SWIGLU = 1
 
 
 class QuantizeProblem(ctypes.Structure):
@@ -116,6 +121,13 @@ SIGNATURES = [
       _c_size, _vp]),
     ("w4a16_tune", ctypes.c_int, [_c_int64, _c_int64, _c_int64, _vp, ctypes.POINTER(ctypes.c_int)]),
     ("w4a16_table_set", ctypes.c_int, [_c_int64, _c_int64, _c_int64, ctypes.c_int]),
+    ("w4a16_tune_swiglu", ctypes.c_int, [_c_int64, _c_int64, _c_int64, _vp, ctypes.POINTER(ctypes.c_int)]),
+    ("w8a16_tune", ctypes.c_int, [_c_int64, _c_int64, _c_int64, _vp, ctypes.POINTER(ctypes.c_int)]),
+    ("fp4a16_tune", ctypes.c_int,
+     [ctypes.c_int, _c_int64, _c_int64, _c_int64, _vp, ctypes.POINTER(ctypes.c_int)]),
+    ("w4a16_swiglu_table_set", ctypes.c_int, [_c_int64, _c_int64, _c_int64, ctypes.c_int]),
+    ("w8a16_table_set", ctypes.c_int, [_c_int64, _c_int64, _c_int64, ctypes.c_int]),
+    ("fp4a16_table_set", ctypes.c_int, [_c_int64, _c_int64, _c_int64, ctypes.c_int]),
     ("w4a16_table_clear", None, []),
     ("w4a16_table_save", ctypes.c_int, [ctypes.c_char_p]),
     ("w4a16_table_load", ctypes.c_int, [ctypes.c_char_p]),
@@ -626,16 +638,18 @@ def w4a16_quantize_grouped(weights, outs=None, stream=None):
     return outs
 
 
-def _gemm_problems(As, packeds, scales_list, biases, Ys):
+def _gemm_problems(As, packeds, scales_list, biases, Ys, epilogues=None):
     n = len(As)
     if not 1 <= n <= MAX_GROUP or not (len(packeds) == len(scales_list) == n):
         raise ValueError(f"1 .. {MAX_GROUP} problems with matching argument lists")
     act = As[0].dtype if As[0].dtype in (torch.bfloat16, torch.float16) else torch.bfloat16
     biases = biases if biases is not None else [None] * n
     Ys = Ys if Ys is not None else [None] * n
+    epilogues = epilogues if epilogues is not None else [EPILOGUE_NONE] * n
     probs, outs = (GemmProblem * n)(), []
     for i in range(n):
         A, packed, scales, bias, Y = As[i], packeds[i], scales_list[i], biases[i], Ys[i]
+        epi = int(epilogues[i])
         _require_cuda(A, "A", act)
         _require_cuda(packed, "packed", torch.uint8)
         _require_cuda(scales, "scales", torch.float16)
@@ -647,30 +661,29 @@ def _gemm_problems(As, packeds, scales_list, biases, Ys):
             raise ValueError("packed must hold w4a16_packed_bytes(N, K) bytes of tiled codes")
         if bias is not None:
             _require_cuda(bias, "bias", act)
+        ncols = N // 2 if epi == EPILOGUE_SWIGLU else N
         if Y is None:
-            Y = torch.empty((M, N), dtype=act, device=A.device)
+            Y = torch.empty((M, ncols), dtype=act, device=A.device)
         _require_cuda(Y, "Y", act)
+        if Y.shape != (M, ncols):
+            raise ValueError(f"Y of problem {i} must be [{M}, {ncols}]")
         probs[i] = GemmProblem(A.data_ptr(), packed.data_ptr(), scales.data_ptr(),
-                               bias.data_ptr() if bias is not None else None, Y.data_ptr(), M, N, K)
+                               bias.data_ptr() if bias is not None else None, Y.data_ptr(), M, N, K,
+                               epi)
         outs.append(Y)
     return probs, outs, act
 
 
 def w4a16_tune_grouped(shapes, act=torch.bfloat16, stream=None, device=None) -> int:
-    """Choose the grouped-GEMM plan for these ``(M, N, K)`` shapes by
-    measurement and memoize it (later ``w4a16_gemm_grouped`` calls of the
-    same shapes use it).  Returns the chosen variant id."""
-    n = len(shapes)
-    if not 1 <= n <= MAX_GROUP:
-        raise ValueError(f"1 .. {MAX_GROUP} shapes")
+    """Choose the grouped-GEMM plan for these ``(M, N, K)`` (or ``(M, N, K,
+    epilogue)``) shapes by measurement and memoize it (later
+    ``w4a16_gemm_grouped`` calls of the same shapes use it).  Returns the
+    chosen variant id."""
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
-    probs = (GemmProblem * n)()
     # only the shapes are read; the pointers must still be 16-byte aligned
     # and non-null for the argument checks
-    dummy = torch.empty(256, dtype=torch.uint8, device=dev)
-    for i, (M, N, K) in enumerate(shapes):
-        probs[i] = GemmProblem(dummy.data_ptr(), dummy.data_ptr(), dummy.data_ptr(), None,
-                               dummy.data_ptr(), M, N, K)
+    probs, dummy = _shape_problems(shapes, dev)
+    n = len(shapes)
     out = ctypes.c_int(-1)
     _check(lib().w4a16_tune_grouped(probs, n, 1 if act == torch.float16 else 0,
                                     _stream_handle(dev, stream), ctypes.byref(out)),
@@ -684,9 +697,11 @@ def _shape_problems(shapes, device):
         raise ValueError(f"1 .. {MAX_GROUP} shapes")
     probs = (GemmProblem * n)()
     dummy = torch.empty(256, dtype=torch.uint8, device=device)
-    for i, (M, N, K) in enumerate(shapes):
+    for i, shp in enumerate(shapes):
+        M, N, K = shp[:3]
+        epi = shp[3] if len(shp) > 3 else EPILOGUE_NONE
         probs[i] = GemmProblem(dummy.data_ptr(), dummy.data_ptr(), dummy.data_ptr(), None,
-                               dummy.data_ptr(), M, N, K)
+                               dummy.data_ptr(), M, N, K, epi)
     return probs, dummy
 
 
@@ -699,10 +714,12 @@ def w4a16_set_grouped_variant(shapes, variant: int, device=None) -> None:
 
 
 def w4a16_gemm_grouped(As, packeds, scales_list, biases=None, Ys=None, workspace=None,
-                       stream=None, variant=None):
+                       stream=None, variant=None, epilogues=None):
     """Independent W4A16 GEMMs ``Y_i = A_i @ dequant(W_i)^T + bias_i`` in one
-    launch (bf16 or fp16 activations, all of one type).  Returns the Y's."""
-    probs, outs, act = _gemm_problems(As, packeds, scales_list, biases, Ys)
+    launch (bf16 or fp16 activations, all of one type).  ``epilogues[i] ==
+    EPILOGUE_SWIGLU`` gives problem i the SwiGLU epilogue (interleaved
+    up/gate rows, ``Y_i`` of ``[M, N/2]``, bf16).  Returns the Y's."""
+    probs, outs, act = _gemm_problems(As, packeds, scales_list, biases, Ys, epilogues)
     n = len(outs)
     L = lib()
     v = -1 if variant is None else variant
@@ -753,8 +770,48 @@ def w4a16_tune(M: int, N: int, K: int, stream=None, device=None) -> int:
     return out.value
 
 
+def w4a16_tune_swiglu(M: int, N: int, K: int, stream=None, device=None) -> int:
+    """Choose the SwiGLU-epilogue GEMM's variant for this shape by measurement
+    (w4a16_tune_swiglu); returns the id."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    out = ctypes.c_int(-1)
+    _check(lib().w4a16_tune_swiglu(M, N, K, _stream_handle(dev, stream), ctypes.byref(out)),
+           "w4a16_tune_swiglu")
+    return out.value
+
+
+def w8a16_tune(M: int, N: int, K: int, stream=None, device=None) -> int:
+    """Choose the INT8 GEMM's variant for this shape by measurement."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    out = ctypes.c_int(-1)
+    _check(lib().w8a16_tune(M, N, K, _stream_handle(dev, stream), ctypes.byref(out)), "w8a16_tune")
+    return out.value
+
+
+def fp4a16_tune(M: int, N: int, K: int, fmt="mxfp4", stream=None, device=None) -> int:
+    """Choose the FP4 GEMM's variant for this shape by measurement (timed with
+    ``fmt``'s scales; the entry serves both formats)."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    out = ctypes.c_int(-1)
+    _check(lib().fp4a16_tune(_fp4_format(fmt), M, N, K, _stream_handle(dev, stream),
+                             ctypes.byref(out)), "fp4a16_tune")
+    return out.value
+
+
 def w4a16_table_set(M: int, N: int, K: int, variant: int) -> None:
     _check(lib().w4a16_table_set(M, N, K, variant), "w4a16_table_set")
+
+
+def w4a16_swiglu_table_set(M: int, N: int, K: int, variant: int) -> None:
+    _check(lib().w4a16_swiglu_table_set(M, N, K, variant), "w4a16_swiglu_table_set")
+
+
+def w8a16_table_set(M: int, N: int, K: int, variant: int) -> None:
+    _check(lib().w8a16_table_set(M, N, K, variant), "w8a16_table_set")
+
+
+def fp4a16_table_set(M: int, N: int, K: int, variant: int) -> None:
+    _check(lib().fp4a16_table_set(M, N, K, variant), "fp4a16_table_set")
 
 
 def w4a16_table_clear() -> None:

@@ -12,6 +12,7 @@
 #include <cudaTypedefs.h>
 
 #include <atomic>
+#include <cctype>
 #include <algorithm>
 #include <cstdio>
 #include <cstdlib>
@@ -316,10 +317,46 @@ int rule_variant(int64_t M, int64_t N, int64_t K, int num_sms) {
 }
 
 // ---------------------------------------------------------------- table
+// Catalogues with a measured table: the INT4 GEMM, the INT4 GEMM with the
+// SwiGLU epilogue (same variants, chosen separately: its best variant can
+// differ), the INT8 GEMM and the FP4 GEMM (one catalogue for both formats).
+enum Catalogue { kCatInt4 = 0, kCatSwiglu = 1, kCatInt8 = 2, kCatFp4 = 3, kNumCats = 4 };
+const char* const kCatTag[kNumCats] = {"", "swiglu", "int8", "fp4"};
+
 std::mutex g_table_mutex;
-std::map<std::tuple<int64_t, int64_t, int64_t>, int> g_table;
+std::map<std::tuple<int, int64_t, int64_t, int64_t>, int> g_table;   // (catalogue, M, N, K)
 bool g_table_env_loaded = false;
 
+bool swiglu_ok(int id);
+
+int cat_count(int cat) {
+  return cat == kCatInt8 ? kNumVariants8 : cat == kCatFp4 ? kNumVariantsF4 : kNumVariants;
+}
+
+const char* cat_name(int cat, int id) {
+  if (id < 0 || id >= cat_count(cat)) return nullptr;
+  return cat == kCatInt8 ? kVariants8[id].name : cat == kCatFp4 ? kVariantsF4[id].name
+                                                               : kVariants[id].name;
+}
+
+int cat_by_name(int cat, const std::string& n) {
+  for (int i = 0; i < cat_count(cat); ++i)
+    if (n == cat_name(cat, i)) return i;
+  return -1;
+}
+
+bool cat_eligible(int cat, int id, int64_t M, int64_t N, int64_t K) {
+  switch (cat) {
+    case kCatInt4: return variant_eligible(id, M, N, K);
+    case kCatSwiglu: return swiglu_ok(id) && N % 2 == 0 && variant_eligible(id, M, N, K);
+    case kCatInt8: return variant8_eligible(id, M, N, K);
+    case kCatFp4: return variantf4_eligible(id, M, N, K);
+    default: return false;
+  }
+}
+
+// Text lines "M N K variant" (INT4) or "tag M N K variant" (tag swiglu, int8
+// or fp4).
 int load_table_locked(const char* path) {
   std::ifstream f(path);
   if (!f) return W4A16_ERR_INVALID_ARG;
@@ -327,15 +364,27 @@ int load_table_locked(const char* path) {
   while (std::getline(f, line)) {
     if (line.empty() || line[0] == '#') continue;
     std::istringstream ss(line);
+    int cat = kCatInt4;
+    if (!std::isdigit(static_cast<unsigned char>(line[0]))) {
+      std::string tag;
+      ss >> tag;
+      cat = -1;
+      for (int c = 1; c < kNumCats; ++c)
+        if (tag == kCatTag[c]) cat = c;
+      if (cat < 0) return W4A16_ERR_INVALID_ARG;
+    }
     int64_t M, N, K;
     std::string name;
     if (!(ss >> M >> N >> K >> name)) return W4A16_ERR_INVALID_ARG;
-    const int id = variant_by_name(name);
-    if (id < 0 || !variant_eligible(id, M, N, K)) return W4A16_ERR_NO_VARIANT;
-    g_table[{M, N, K}] = id;
+    const int id = cat_by_name(cat, name);
+    if (id < 0 || !cat_eligible(cat, id, M, N, K)) return W4A16_ERR_NO_VARIANT;
+    g_table[{cat, M, N, K}] = id;
   }
   return W4A16_OK;
 }
+
+// The table's entry for a shape of a catalogue, or -1.
+int table_get(int cat, int64_t M, int64_t N, int64_t K);
 
 void maybe_load_env_table_locked() {
   if (g_table_env_loaded) return;
@@ -355,14 +404,23 @@ bool log_enabled() {
   return on;
 }
 
+int table_get(int cat, int64_t M, int64_t N, int64_t K) {
+  std::lock_guard<std::mutex> lock(g_table_mutex);
+  maybe_load_env_table_locked();
+  auto it = g_table.find({cat, M, N, K});
+  return it != g_table.end() ? it->second : -1;
+}
+
+int table_put(int cat, int64_t M, int64_t N, int64_t K, int id) {
+  if (!cat_eligible(cat, id, M, N, K)) return W4A16_ERR_NO_VARIANT;
+  std::lock_guard<std::mutex> lock(g_table_mutex);
+  maybe_load_env_table_locked();
+  g_table[{cat, M, N, K}] = id;
+  return W4A16_OK;
+}
+
 int select_variant(int64_t M, int64_t N, int64_t K) {
-  int id = -1;
-  {
-    std::lock_guard<std::mutex> lock(g_table_mutex);
-    maybe_load_env_table_locked();
-    auto it = g_table.find({M, N, K});
-    if (it != g_table.end()) id = it->second;
-  }
+  int id = table_get(kCatInt4, M, N, K);
   if (id < 0) {
     DeviceInfo dev;
     const int sms = device_info(dev) ? dev.num_sms : kDefaultSms;
@@ -378,6 +436,8 @@ int select_variant(int64_t M, int64_t N, int64_t K) {
 bool swiglu_ok(int id) { return id >= 0 && id < kNumVariants && !kVariants[id].cfg.simt; }
 
 int select_variant_swiglu(int64_t M, int64_t N, int64_t K) {
+  const int tuned = table_get(kCatSwiglu, M, N, K);
+  if (tuned >= 0 && cat_eligible(kCatSwiglu, tuned, M, N, K)) return tuned;
   const int id = select_variant(M, N, K);
   if (id < 0 || swiglu_ok(id)) return id;
   DeviceInfo dev;
@@ -458,6 +518,8 @@ int run_gemm(int id, const void* A, int64_t M, int64_t N, int64_t K, const void*
 
 // INT8: the rule over the INT8 catalogue (no measured table).
 int select_variant8(int64_t M, int64_t N, int64_t K) {
+  const int tuned = table_get(kCatInt8, M, N, K);
+  if (tuned >= 0 && variant8_eligible(tuned, M, N, K)) return tuned;
   DeviceInfo dev;
   const int sms = device_info(dev) ? dev.num_sms : kDefaultSms;
   int best = -1;
@@ -475,6 +537,8 @@ int select_variant8(int64_t M, int64_t N, int64_t K) {
 
 // FP4: the rule over the FP4 catalogue.
 int select_variantf4(int64_t M, int64_t N, int64_t K) {
+  const int tuned = table_get(kCatFp4, M, N, K);
+  if (tuned >= 0 && variantf4_eligible(tuned, M, N, K)) return tuned;
   DeviceInfo dev;
   const int sms = device_info(dev) ? dev.num_sms : kDefaultSms;
   int best = -1;
@@ -554,8 +618,10 @@ bool plan_for_variant(int id, const w4a16_gemm_problem* pr, int count, int sms, 
                       bool forced) {
   const Variant& v = kVariants[id];
   if (v.cfg.simt && count > 1) return false;   // single problems only
-  for (int i = 0; i < count; ++i)
+  for (int i = 0; i < count; ++i) {
     if (!variant_eligible(id, pr[i].M, pr[i].N, pr[i].K)) return false;
+    if (pr[i].epilogue == W4A16_EPILOGUE_SWIGLU && !swiglu_ok(id)) return false;
+  }
   if (count > sms) return false;
   int ctas[kMaxGemmGroup];
   double est[kMaxGemmGroup];
@@ -610,13 +676,13 @@ bool plan_for_variant(int id, const w4a16_gemm_problem* pr, int count, int sms, 
 // once per set of shapes, not on every call.
 struct GroupKey {
   int variant, count, sms;
-  int64_t mnk[kMaxGemmGroup][3];
+  int64_t mnk[kMaxGemmGroup][4];   // M, N, K, epilogue
   bool operator<(const GroupKey& o) const {
     if (sms != o.sms) return sms < o.sms;
     if (variant != o.variant) return variant < o.variant;
     if (count != o.count) return count < o.count;
     for (int i = 0; i < count; ++i)
-      for (int j = 0; j < 3; ++j)
+      for (int j = 0; j < 4; ++j)
         if (mnk[i][j] != o.mnk[i][j]) return mnk[i][j] < o.mnk[i][j];
     return false;
   }
@@ -624,10 +690,7 @@ struct GroupKey {
 std::map<GroupKey, GroupPlan> g_group_plans;
 std::mutex g_group_mutex;
 
-int plan_group(const w4a16_gemm_problem* pr, int count, int variant, GroupPlan& plan) {
-  DeviceInfo dev;
-  const int sms = std::min(device_info(dev) ? dev.num_sms : kDefaultSms, kMaxGrid);
-  if (variant >= kNumVariants) return W4A16_ERR_UNSUPPORTED;
+GroupKey group_key(int variant, const w4a16_gemm_problem* pr, int count, int sms) {
   GroupKey key{};
   key.variant = variant < 0 ? -1 : variant;
   key.count = count;
@@ -636,7 +699,16 @@ int plan_group(const w4a16_gemm_problem* pr, int count, int variant, GroupPlan& 
     key.mnk[i][0] = pr[i].M;
     key.mnk[i][1] = pr[i].N;
     key.mnk[i][2] = pr[i].K;
+    key.mnk[i][3] = pr[i].epilogue;
   }
+  return key;
+}
+
+int plan_group(const w4a16_gemm_problem* pr, int count, int variant, GroupPlan& plan) {
+  DeviceInfo dev;
+  const int sms = std::min(device_info(dev) ? dev.num_sms : kDefaultSms, kMaxGrid);
+  if (variant >= kNumVariants) return W4A16_ERR_UNSUPPORTED;
+  const GroupKey key = group_key(variant, pr, count, sms);
   {
     std::lock_guard<std::mutex> lock(g_group_mutex);
     auto it = g_group_plans.find(key);
@@ -671,8 +743,17 @@ int check_group_args(const w4a16_gemm_problem* pr, int count, int group) {
     const int st = check_gemm_args(pr[i].A, pr[i].M, pr[i].N, pr[i].K, pr[i].packed, pr[i].scales,
                                    group, pr[i].bias_or_null, pr[i].Y);
     if (st != W4A16_OK) return st;
+    if (pr[i].epilogue != W4A16_EPILOGUE_NONE && pr[i].epilogue != W4A16_EPILOGUE_SWIGLU)
+      return W4A16_ERR_UNSUPPORTED;
+    if (pr[i].epilogue == W4A16_EPILOGUE_SWIGLU && pr[i].N % 2 != 0) return W4A16_ERR_UNSUPPORTED;
   }
   return W4A16_OK;
+}
+
+bool group_has_swiglu(const w4a16_gemm_problem* pr, int count) {
+  for (int i = 0; i < count; ++i)
+    if (pr[i].epilogue == W4A16_EPILOGUE_SWIGLU) return true;
+  return false;
 }
 
 size_t variant_ws(int id, int64_t M, int64_t N, int64_t K) {
@@ -1100,6 +1181,7 @@ int launch_group_plan(const GroupPlan& plan, const w4a16_gemm_problem* problems,
     p.error_word = dev.error_word;
     p.timeout_ns = g_timeout_ns.load();
     p.act_f16 = act_f16 != 0;
+    p.swiglu = problems[i].epilogue == W4A16_EPILOGUE_SWIGLU;
     p.weights_static = g_weights_static.load() != 0;
     grp.s[i] = plan.s[i];
   }
@@ -1128,6 +1210,7 @@ int w4a16_gemm_grouped(const w4a16_gemm_problem* problems, int count, int group,
                        int variant, void* workspace, size_t workspace_bytes, void* stream) {
   int st = check_group_args(problems, count, group);
   if (st != W4A16_OK) return st;
+  if (act_f16 && group_has_swiglu(problems, count)) return W4A16_ERR_UNSUPPORTED;
   GroupPlan plan;
   st = plan_group(problems, count, variant, plan);
   if (st != W4A16_OK) return st;
@@ -1143,6 +1226,7 @@ int w4a16_tune_grouped(const w4a16_gemm_problem* problems, int count, int act_f1
                        int* out_variant) {
   int st = check_group_args(problems, count, kGroup);
   if (st != W4A16_OK) return st;
+  if (act_f16 && group_has_swiglu(problems, count)) return W4A16_ERR_UNSUPPORTED;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
   cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
   if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone)
@@ -1276,15 +1360,7 @@ int w4a16_tune_grouped(const w4a16_gemm_problem* problems, int count, int act_f1
   if (dev_err != W4A16_OK) return dev_err;
   if (best < 0) return W4A16_ERR_NO_VARIANT;
   // memoize: later automatic grouped launches of these shapes use it
-  GroupKey key{};
-  key.variant = -1;
-  key.count = count;
-  key.sms = sms;
-  for (int i = 0; i < count; ++i) {
-    key.mnk[i][0] = problems[i].M;
-    key.mnk[i][1] = problems[i].N;
-    key.mnk[i][2] = problems[i].K;
-  }
+  const GroupKey key = group_key(-1, problems, count, sms);
   {
     std::lock_guard<std::mutex> lock(g_group_mutex);
     g_group_plans[key] = cands[best];
@@ -1301,15 +1377,7 @@ int w4a16_set_grouped_variant(const w4a16_gemm_problem* problems, int count, int
   const int sms = std::min(device_info(dev) ? dev.num_sms : kDefaultSms, kMaxGrid);
   GroupPlan plan;
   if (!plan_for_variant(variant, problems, count, sms, plan, false)) return W4A16_ERR_NO_VARIANT;
-  GroupKey key{};
-  key.variant = -1;
-  key.count = count;
-  key.sms = sms;
-  for (int i = 0; i < count; ++i) {
-    key.mnk[i][0] = problems[i].M;
-    key.mnk[i][1] = problems[i].N;
-    key.mnk[i][2] = problems[i].K;
-  }
+  const GroupKey key = group_key(-1, problems, count, sms);
   std::lock_guard<std::mutex> lock(g_group_mutex);
   g_group_plans[key] = plan;
   return W4A16_OK;
@@ -1378,11 +1446,19 @@ int w4a16_gemm_variant(int variant, const void* A_bf16, int64_t M, int64_t N, in
 }
 
 int w4a16_table_set(int64_t M, int64_t N, int64_t K, int variant) {
-  if (!variant_eligible(variant, M, N, K)) return W4A16_ERR_NO_VARIANT;
-  std::lock_guard<std::mutex> lock(g_table_mutex);
-  maybe_load_env_table_locked();
-  g_table[{M, N, K}] = variant;
-  return W4A16_OK;
+  return table_put(kCatInt4, M, N, K, variant);
+}
+
+int w4a16_swiglu_table_set(int64_t M, int64_t N, int64_t K, int variant) {
+  return table_put(kCatSwiglu, M, N, K, variant);
+}
+
+int w8a16_table_set(int64_t M, int64_t N, int64_t K, int variant) {
+  return table_put(kCatInt8, M, N, K, variant);
+}
+
+int fp4a16_table_set(int64_t M, int64_t N, int64_t K, int variant) {
+  return table_put(kCatFp4, M, N, K, variant);
 }
 
 void w4a16_table_clear(void) {
@@ -1396,10 +1472,13 @@ int w4a16_table_save(const char* path) {
   std::lock_guard<std::mutex> lock(g_table_mutex);
   std::ofstream f(path);
   if (!f) return W4A16_ERR_INVALID_ARG;
-  f << "# M N K variant\n";
-  for (const auto& kv : g_table)
-    f << std::get<0>(kv.first) << ' ' << std::get<1>(kv.first) << ' ' << std::get<2>(kv.first)
-      << ' ' << kVariants[kv.second].name << '\n';
+  f << "# [catalogue] M N K variant  (no catalogue: INT4 GEMM; swiglu, int8, fp4)\n";
+  for (const auto& kv : g_table) {
+    const int cat = std::get<0>(kv.first);
+    if (cat != kCatInt4) f << kCatTag[cat] << ' ';
+    f << std::get<1>(kv.first) << ' ' << std::get<2>(kv.first) << ' ' << std::get<3>(kv.first)
+      << ' ' << cat_name(cat, kv.second) << '\n';
+  }
   return f ? W4A16_OK : W4A16_ERR_INVALID_ARG;
 }
 
@@ -1410,8 +1489,15 @@ int w4a16_table_load(const char* path) {
   return load_table_locked(path);
 }
 
-int w4a16_tune(int64_t M, int64_t N, int64_t K, void* stream_v, int* out_variant) {
+// Times every eligible variant of a catalogue on synthetic device buffers of
+// the shape (each as one CUDA graph of back-to-back launches on weight copies
+// rotating through more than the L2 size) and stores the fastest in the
+// table.  fmt: the FP4 format (kFmtMxfp4 / kFmtNvfp4) for kCatFp4.
+static int tune_impl(int cat, int fmt, int64_t M, int64_t N, int64_t K, void* stream_v,
+                     int* out_variant) {
   if (!shape_ok(M, N, K)) return W4A16_ERR_UNSUPPORTED;
+  if (cat == kCatFp4 && N % 16 != 0) return W4A16_ERR_UNSUPPORTED;
+  if (cat == kCatSwiglu && N % 2 != 0) return W4A16_ERR_UNSUPPORTED;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
   cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
   if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone)
@@ -1419,11 +1505,20 @@ int w4a16_tune(int64_t M, int64_t N, int64_t K, void* stream_v, int* out_variant
 
   // Synthetic operands; enough weight copies that the timed launches stream
   // them from HBM rather than L2.
-  const size_t wbytes = w4a16_packed_bytes(N, K);
-  const size_t sbytes = w4a16_scales_bytes(N, K, kGroup);
+  const size_t wbytes = cat == kCatInt8 ? w8a16_packed_bytes(N, K) : w4a16_packed_bytes(N, K);
+  const size_t sbytes = cat == kCatFp4 ? fp4a16_scales_bytes(fmt == kFmtNvfp4 ? FP4A16_NVFP4
+                                                                                : FP4A16_MXFP4, N, K)
+                                       : w4a16_scales_bytes(N, K, kGroup);
   const size_t abytes = static_cast<size_t>(M) * K * 2;
-  const size_t ybytes = static_cast<size_t>(M) * N * 2;
-  const size_t wsbytes = w4a16_gemm_workspace_bytes_max(M, N, K);
+  const size_t ybytes = static_cast<size_t>(M) * (cat == kCatSwiglu ? N / 2 : N) * 2;
+  size_t wsbytes = 0;
+  for (int id = 0; id < cat_count(cat); ++id) {
+    if (!cat_eligible(cat, id, M, N, K)) continue;
+    const size_t w = cat == kCatInt8 ? variant8_ws(id, M, N, K)
+                     : cat == kCatFp4 ? variantf4_ws(id, M, N, K)
+                                      : variant_ws(id, M, N, K);
+    wsbytes = std::max(wsbytes, w);
+  }
   const size_t per_copy = wbytes + sbytes + 4096;
   int copies = static_cast<int>((512ull << 20) / per_copy) + 1;
   if (copies > 16) copies = 16;
@@ -1443,8 +1538,9 @@ int w4a16_tune(int64_t M, int64_t N, int64_t K, void* stream_v, int* out_variant
   void* A = alloc(abytes);
   void* Y = alloc(ybytes);
   void* ws = wsbytes ? alloc(wsbytes) : nullptr;
+  float* ts = cat == kCatFp4 ? static_cast<float*>(alloc(256)) : nullptr;
   std::vector<void*> Wp(copies), Sc(copies);
-  bool ok = A && Y && (wsbytes == 0 || ws);
+  bool ok = A && Y && (wsbytes == 0 || ws) && (cat != kCatFp4 || ts);
   for (int c = 0; ok && c < copies; ++c) {
     Wp[c] = alloc(wbytes);
     Sc[c] = alloc(sbytes);
@@ -1454,12 +1550,33 @@ int w4a16_tune(int64_t M, int64_t N, int64_t K, void* stream_v, int* out_variant
     release();
     return W4A16_ERR_CUDA;
   }
+  // finite operands: bf16 activations 0x3C3C, codes 0x5A, scales of a small
+  // normal value (fp16 0x1C1C; E8M0 0x7A, i.e. 2^-5; E4M3 0x30, i.e. 0.5),
+  // NVFP4 tensor scale 0x3C3C3C3C (about 0.0115)
   cudaMemsetAsync(A, 0x3C, abytes, stream);
+  const int sfill = cat == kCatFp4 ? (fmt == kFmtNvfp4 ? 0x30 : 0x7A) : 0x1C;
   for (int c = 0; c < copies; ++c) {
     cudaMemsetAsync(Wp[c], 0x5A, wbytes, stream);
-    cudaMemsetAsync(Sc[c], 0x1C, sbytes, stream);
+    cudaMemsetAsync(Sc[c], sfill, sbytes, stream);
   }
+  if (ts) cudaMemsetAsync(ts, 0x3C, 256, stream);
   if (ws) cudaMemsetAsync(ws, 0, wsbytes, stream);
+
+  auto launch = [&](int id, int c, cudaStream_t st) -> int {
+    switch (cat) {
+      case kCatSwiglu:
+        return run_gemm_v(kVariants[id], A, M, N, K, Wp[c], Sc[c], nullptr, Y, ws, wsbytes, st,
+                          false, nullptr, true);
+      case kCatInt8:
+        return run_gemm_v(kVariants8[id], A, M, N, K, Wp[c], Sc[c], nullptr, Y, ws, wsbytes, st,
+                          false);
+      case kCatFp4:
+        return run_gemm_v(variant_f4(id, fmt), A, M, N, K, Wp[c], Sc[c], nullptr, Y, ws, wsbytes,
+                          st, false, fmt == kFmtNvfp4 ? ts : nullptr);
+      default:
+        return run_gemm(id, A, M, N, K, Wp[c], Sc[c], nullptr, Y, ws, wsbytes, st);
+    }
+  };
 
   // Each variant is timed as one CUDA graph of kIters launches (so host
   // launch overhead does not hide short kernels), on a private stream.
@@ -1472,12 +1589,10 @@ int w4a16_tune(int64_t M, int64_t N, int64_t K, void* stream_v, int* out_variant
   float best_ms = 0.0f;
   int best = -1;
   constexpr int kIters = 20;
-  for (int id = 0; ok && id < kNumVariants; ++id) {
-    if (!variant_eligible(id, M, N, K)) continue;
+  for (int id = 0; ok && id < cat_count(cat); ++id) {
+    if (!cat_eligible(cat, id, M, N, K)) continue;
     bool fine = true;
-    for (int it = 0; it < 3 && fine; ++it)
-      fine = run_gemm(id, A, M, N, K, Wp[it % copies], Sc[it % copies], nullptr, Y, ws, wsbytes,
-                      cs) == W4A16_OK;
+    for (int it = 0; it < 3 && fine; ++it) fine = launch(id, it % copies, cs) == W4A16_OK;
     if (!fine) continue;
     cudaGraph_t graph = nullptr;
     cudaGraphExec_t exec = nullptr;
@@ -1485,8 +1600,7 @@ int w4a16_tune(int64_t M, int64_t N, int64_t K, void* stream_v, int* out_variant
       ok = false;
       break;
     }
-    for (int it = 0; it < kIters; ++it)
-      run_gemm(id, A, M, N, K, Wp[it % copies], Sc[it % copies], nullptr, Y, ws, wsbytes, cs);
+    for (int it = 0; it < kIters; ++it) launch(id, it % copies, cs);
     if (cudaStreamEndCapture(cs, &graph) != cudaSuccess ||
         cudaGraphInstantiate(&exec, graph, 0) != cudaSuccess) {
       if (graph) cudaGraphDestroy(graph);
@@ -1507,9 +1621,9 @@ int w4a16_tune(int64_t M, int64_t N, int64_t K, void* stream_v, int* out_variant
     float ms = 0.0f;
     cudaEventElapsedTime(&ms, e0, e1);
     if (log_enabled())
-      std::fprintf(stderr, "w4a16: tune M=%lld N=%lld K=%lld %s %.3f us\n",
+      std::fprintf(stderr, "w4a16: tune %s M=%lld N=%lld K=%lld %s %.3f us\n", kCatTag[cat],
                    static_cast<long long>(M), static_cast<long long>(N), static_cast<long long>(K),
-                   kVariants[id].name, 1000.0 * ms / kIters);
+                   cat_name(cat, id), 1000.0 * ms / kIters);
     if (best < 0 || ms < best_ms) {
       best_ms = ms;
       best = id;
@@ -1524,20 +1638,35 @@ int w4a16_tune(int64_t M, int64_t N, int64_t K, void* stream_v, int* out_variant
   cudaGetLastError();   // a failed capture leaves no sticky error behind
   const int dev_err = w4a16_get_device_error(stream);
   release();
-  if (!ok) return cuda_failure(cudaErrorUnknown, "w4a16_tune: graph timing failed");
+  if (!ok) return cuda_failure(cudaErrorUnknown, "tune: graph timing failed");
   if (dev_err != W4A16_OK) return dev_err;
   if (best < 0) return W4A16_ERR_NO_VARIANT;
-  {
-    std::lock_guard<std::mutex> lock(g_table_mutex);
-    maybe_load_env_table_locked();
-    g_table[{M, N, K}] = best;
-  }
+  const int st = table_put(cat, M, N, K, best);
+  if (st != W4A16_OK) return st;
   if (out_variant) *out_variant = best;
   if (log_enabled())
-    std::fprintf(stderr, "w4a16: tuned M=%lld N=%lld K=%lld -> %s (%.3f us)\n",
+    std::fprintf(stderr, "w4a16: tuned %s M=%lld N=%lld K=%lld -> %s (%.3f us)\n", kCatTag[cat],
                  static_cast<long long>(M), static_cast<long long>(N), static_cast<long long>(K),
-                 kVariants[best].name, 1000.0 * best_ms / kIters);
+                 cat_name(cat, best), 1000.0 * best_ms / kIters);
   return W4A16_OK;
+}
+
+int w4a16_tune(int64_t M, int64_t N, int64_t K, void* stream, int* out_variant) {
+  return tune_impl(kCatInt4, kFmtInt4, M, N, K, stream, out_variant);
+}
+
+int w4a16_tune_swiglu(int64_t M, int64_t N, int64_t K, void* stream, int* out_variant) {
+  return tune_impl(kCatSwiglu, kFmtInt4, M, N, K, stream, out_variant);
+}
+
+int w8a16_tune(int64_t M, int64_t N, int64_t K, void* stream, int* out_variant) {
+  return tune_impl(kCatInt8, kFmtInt8, M, N, K, stream, out_variant);
+}
+
+int fp4a16_tune(int format, int64_t M, int64_t N, int64_t K, void* stream, int* out_variant) {
+  const int f = fp4_format(format);
+  if (f == 0) return W4A16_ERR_UNSUPPORTED;
+  return tune_impl(kCatFp4, f, M, N, K, stream, out_variant);
 }
 
 int w4a16_get_device_error(void* stream) {

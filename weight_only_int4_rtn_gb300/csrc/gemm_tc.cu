@@ -64,7 +64,11 @@ cudaError_t launch_gemm_tc_group(const GemmKernelConfig& c, const GemmGroup& grp
   static_assert(kMaxGemmGroup == kMaxGroup, "group size of the kernel arguments");
   if (grp.count < 1 || grp.count > kMaxGroup) return cudaErrorInvalidValue;
   if (c.simt) return launch_gemv(c, grp, use_pdl, stream);
-  if (grp.p[0].swiglu) return launch_gemm_tc_swiglu(c, grp, use_pdl, stream);
+  bool any_sw = false;
+  for (int i = 0; i < grp.count; ++i) any_sw = any_sw || grp.p[i].swiglu;
+  if (any_sw)
+    return grp.count == 1 ? launch_gemm_tc_swiglu(c, grp, use_pdl, stream)
+                          : launch_gemm_tc_group_swiglu(c, grp, use_pdl, stream);
   if (c.weight_format == kFmtInt8) return launch_gemm_tc_w8(c, grp, use_pdl, stream);
   if (c.weight_format == kFmtMxfp4) return launch_gemm_tc_mxfp4(c, grp, use_pdl, stream);
   if (c.weight_format == kFmtNvfp4) return launch_gemm_tc_nvfp4(c, grp, use_pdl, stream);

@@ -137,6 +137,8 @@ struct Args {
   int dp_tiles;
   int sk_units;
   int act_3d;                  // activation map is 3-D: both 64-k halves in one copy
+  int sw;                      // this problem takes the SwiGLU epilogue (read by the
+                               // instances compiled with it only)
   int prefetch_w;              // weights are not written by the previous kernel on
                                // the stream: the codes and scales of this many
                                // first units go out before the dependency wait
@@ -565,7 +567,7 @@ __device__ __forceinline__ void emit_cols(const Args& a, const Unit& u, int row,
   const int m0 = (u.tile / a.n_tiles) * BA;
   if (u.whole) {
     const int n = n0 + row;
-    if constexpr (SW) {
+    if (SW && a.sw) {
       constexpr int kB = CNT < 8 ? CNT : 8;
 #pragma unroll
       for (int j0 = 0; j0 < CNT; j0 += kB) {
@@ -678,7 +680,7 @@ __device__ bool split_fixup(const Args& a, const Unit& u, const SplitInfo& si, S
 #pragma unroll
       for (int j = 0; j < 16; ++j) acc[j] += __ldcg(src + (c0 + j) * kTileW);
     }
-    if constexpr (SW) {
+    if (SW && a.sw) {
 #pragma unroll
       for (int j0 = 0; j0 < 16; j0 += 8) {
         float h[8];
@@ -746,7 +748,7 @@ __device__ void wide_fixup(const Args& a, const Shared* sh) {
         if (col < mcols) acc[j] += __ldcg(src + col * kTileW);
       }
     }
-    if constexpr (SW) {
+    if (SW && a.sw) {
       float h[kCh];
 #pragma unroll
       for (int j = 0; j < kCh; ++j) h[j] = acc[j] + bias_n;
@@ -1586,6 +1588,7 @@ cudaError_t launch_instance(const GemmGroup& grp, bool use_pdl, cudaStream_t str
     a.dp_tiles = s.dp_tiles;
     a.sk_units = static_cast<int>(s.sk_units);
     a.act_3d = act_3d;
+    a.sw = SW && p.swiglu ? 1 : 0;
     // two units per producer: deeper early copies sit ahead of the first
     // activation copy in the TMA queue and delay the start (measured)
     a.prefetch_w = p.weights_static ? 4 : 0;

@@ -159,6 +159,10 @@ cudaError_t launch_gemm_tc_group_f16(const GemmKernelConfig& c, const GemmGroup&
 // activations.
 cudaError_t launch_gemm_tc_swiglu(const GemmKernelConfig& c, const GemmGroup& grp, bool use_pdl,
                                   cudaStream_t stream);
+// Grouped launches in which some problems take the SwiGLU epilogue
+// (gemm_tc_group_swiglu.cu): INT4 weights, bf16 activations.
+cudaError_t launch_gemm_tc_group_swiglu(const GemmKernelConfig& c, const GemmGroup& grp,
+                                        bool use_pdl, cudaStream_t stream);
 // INT8 weights (gemm_tc_w8.cu): one problem, bf16 activations.
 cudaError_t launch_gemm_tc_w8(const GemmKernelConfig& c, const GemmGroup& grp, bool use_pdl,
                               cudaStream_t stream);
