@@ -308,6 +308,18 @@ class Formats:
             return L.fp4a16_gemm_workspace_bytes(self.w4.FP4_FORMATS[self.fmt], M, N, K)
         return self.w4.w4a16_gemm_workspace_bytes_max(M, N, K)
 
+    def tune(self, M, N, K, swiglu=False):
+        """Choose this catalogue's variant for the shape by measurement (the
+        library's tuners; memoized in its table)."""
+        w4 = self.w4
+        if swiglu:
+            return w4.w4a16_tune_swiglu(M, N, K)
+        if self.int8:
+            return w4.w8a16_tune(M, N, K)
+        if self.fp4:
+            return w4.fp4a16_tune(M, N, K, self.fmt)
+        return w4.w4a16_tune(M, N, K)
+
     def variant(self, M, N, K):
         w4 = self.w4
         if self.int8:
@@ -346,16 +358,18 @@ def time_graph_us(dev, g, reps):
     return e0.elapsed_time(e1) / reps * 1e3
 
 
-def back_to_back(fx, c, peaks, wcache, tune, dev):
+def back_to_back(fx, c, peaks, wcache, tune, dev, swiglu=False):
     """One GEMM shape alone: a CUDA graph of back-to-back launches on weight
     copies that rotate through more than 3x L2 (SURVEY's timing method), no
-    other kernel in between, against the roofline of the shape."""
+    other kernel in between, against the roofline of the shape.  swiglu: the
+    same weights through w4a16_gemm_swiglu (rows read as interleaved up/gate
+    pairs, Y of [M, N/2]), its variant chosen by its own tuner."""
     import torch
 
     from weight_only_int4_rtn_gb300 import synthetic
     w4 = fx.w4
-    if tune and fx.fmt == "int4":
-        w4.w4a16_tune(c.M, c.N, c.K)
+    if tune:
+        fx.tune(c.M, c.N, c.K, swiglu)
     key = (c.N, c.K, c.seed, c.wdist)
     if key not in wcache:
         wcache.clear()
@@ -367,24 +381,97 @@ def back_to_back(fx, c, peaks, wcache, tune, dev):
     wt = wcache[key]
     _, A, _ = synthetic.draw(c, act=fx.act)
     A = A.to(dev)
-    Y = torch.empty(c.M, c.N, dtype=fx.act_dtype, device=dev)
+    Y = torch.empty(c.M, c.N // 2 if swiglu else c.N, dtype=fx.act_dtype, device=dev)
     nb = sum(t.numel() * t.element_size() for t in (wt["packed"], wt["scales"]))
     ncp = max(1, min(16, -(-3 * L2_BYTES // nb)))
     cps = [wt] + [{k: v.clone() for k, v in wt.items()} for _ in range(ncp - 1)]
     ws = torch.zeros(max(fx.workspace_bytes(c.M, c.N, c.K), 256), dtype=torch.uint8, device=dev)
     reps = max(8, 2 * ncp)
+
+    def one(i, st=None):
+        if swiglu:
+            w4.w4a16_gemm_swiglu(A, cps[i % ncp]["packed"], cps[i % ncp]["scales"], Y=Y,
+                                 workspace=ws, stream=st)
+        else:
+            fx.gemm(A, cps[i % ncp], Y, ws, st)
+
     for i in range(2):   # kernel attributes are set outside the capture
-        fx.gemm(A, cps[i % ncp], Y, ws)
-    g = graph_of(dev, lambda i, st: fx.gemm(A, cps[i % ncp], Y, ws, st), reps)
+        one(i)
+    g = graph_of(dev, one, reps)
     us = time_graph_us(dev, g, reps)
     t_hbm = gemm_bytes(c.M, c.N, c.K, fx.fmt) / (peaks["hbm_gbs"] * 1e9) * 1e6
     t_tc = gemm_flops(c.M, c.N, c.K) / (peaks["bf16_tflops"] * 1e12) * 1e6
     del g, cps, ws
-    return dict(shape=[c.M, c.N, c.K], variant=fx.variant(c.M, c.N, c.K), us=round(us, 3),
-                weight_gbs=round(weight_bytes(c.N, c.K, fx.fmt) / (us * 1e-6) / 1e9, 1),
-                tflops=round(gemm_flops(c.M, c.N, c.K) / (us * 1e-6) / 1e12, 2),
+    out = dict(shape=[c.M, c.N, c.K],
+               variant=(w4.w4a16_variant_name(w4.lib().w4a16_select_variant(c.M, c.N, c.K))
+                        if not swiglu else None) or fx.variant(c.M, c.N, c.K),
+               us=round(us, 3),
+               weight_gbs=round(weight_bytes(c.N, c.K, fx.fmt) / (us * 1e-6) / 1e9, 1),
+               tflops=round(gemm_flops(c.M, c.N, c.K) / (us * 1e-6) / 1e12, 2),
+               bound="hbm" if t_hbm >= t_tc else "tensor",
+               roofline_frac=round(max(t_hbm, t_tc) / us, 4), weight_copies=ncp)
+    if swiglu:
+        out["epilogue"] = "swiglu"
+        out["variant"] = "tuned (w4a16_tune_swiglu)"
+    elif fx.fmt != "int4":
+        out["variant"] = fx.variant(c.M, c.N, c.K)
+    return out
+
+
+def grouped_back_to_back(w4, cases, epilogues, peaks, tune, dev):
+    """The projections of one block as one grouped launch (optionally with
+    the SwiGLU epilogue on some problems), back to back on weight copies
+    rotating through more than 3x L2, plan tuned by measurement."""
+    import torch
+
+    from weight_only_int4_rtn_gb300 import synthetic
+    shapes = [(c.M, c.N, c.K, e) for c, e in zip(cases, epilogues)]
+    if tune:
+        w4.w4a16_tune_grouped(shapes)
+    drawn = [synthetic.draw(c) for c in cases]
+    q = w4.w4a16_quantize_grouped([W.to(dev) for W, _, _ in drawn])
+    nb = sum(p.numel() + s.numel() * 2 for p, s in q)
+    ncp = max(1, min(16, -(-3 * L2_BYTES // nb)))
+    cps = [q] + [[(p.clone(), s.clone()) for p, s in q] for _ in range(ncp - 1)]
+    As = [A.to(dev) for _, A, _ in drawn]
+    Ys = [torch.empty(c.M, c.N // 2 if e else c.N, dtype=torch.bfloat16, device=dev)
+          for c, e in zip(cases, epilogues)]
+    probs, _, _ = w4._gemm_problems(As, [p for p, _ in q], [s for _, s in q], None, Ys, epilogues)
+    ws = torch.zeros(max(w4.lib().w4a16_gemm_grouped_workspace_bytes(probs, len(cases), -1), 256),
+                     dtype=torch.uint8, device=dev)
+    reps = max(8, 2 * ncp)
+
+    def one(i, st=None):
+        cp = cps[i % ncp]
+        w4.w4a16_gemm_grouped(As, [p for p, _ in cp], [s for _, s in cp], Ys=Ys, workspace=ws,
+                              stream=st, epilogues=epilogues)
+
+    for i in range(2):
+        one(i)
+    g = graph_of(dev, one, reps)
+    us = time_graph_us(dev, g, reps)
+    del g, cps, ws
+    byts = sum(gemm_bytes(c.M, c.N, c.K) for c in cases)
+    flops = sum(gemm_flops(c.M, c.N, c.K) for c in cases)
+    t_hbm = byts / (peaks["hbm_gbs"] * 1e9) * 1e6
+    t_tc = flops / (peaks["bf16_tflops"] * 1e12) * 1e6
+    return dict(shapes=[[c.M, c.N, c.K] for c in cases], epilogues=["swiglu" if e else "none"
+                                                                    for e in epilogues],
+                us=round(us, 3), gbs=round(byts / (us * 1e-6) / 1e9, 1),
+                tflops=round(flops / (us * 1e-6) / 1e12, 2),
                 bound="hbm" if t_hbm >= t_tc else "tensor",
                 roofline_frac=round(max(t_hbm, t_tc) / us, 4), weight_copies=ncp)
+
+
+def workload_cases(args):
+    """The workload's projections, or (--shape M,N,K) one projection of that
+    shape (N(0, 0.02) weights, seed 0), e.g. a smaller case of a kernel for a
+    profiler."""
+    from weight_only_int4_rtn_gb300 import synthetic
+    if args.shape:
+        M, N, K = (int(x) for x in args.shape.split(","))
+        return [synthetic.Case(f"shape_m{M}_n{N}_k{K}", M, N, K, 0)]
+    return synthetic.WORKLOADS[args.workload]
 
 
 def run_gpu(args, rank, world):
@@ -395,7 +482,7 @@ def run_gpu(args, rank, world):
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
     torch.cuda.set_device(dev)
-    cases = synthetic.WORKLOADS[args.workload]
+    cases = workload_cases(args)
     fmt = args.weights
     fx = Formats(w4, fmt, args.act, args.sr_seed, dev)
     if fmt != "int4" and (args.grouped or args.act != "bf16"):
@@ -410,15 +497,17 @@ def run_gpu(args, rank, world):
 
     # --- kernel choice by measurement, once per shape (or per set of shapes
     # of a grouped launch), outside the timed region
-    if fmt != "int4":
-        args.tune = False   # the INT8 and FP4 catalogues are chosen by the cost model
-    shapes = [(c.M, c.N, c.K) for c in cases]
+    # the block's gate/up projection with the SwiGLU epilogue (--swiglu)
+    epilogues = [1 if (args.swiglu and "gate_up" in c.name) else 0 for c in cases]
+    if any(epilogues) and (not args.grouped or fmt != "int4" or args.act != "bf16"):
+        raise SystemExit("--swiglu: INT4 weights, bf16 activations, grouped step")
+    shapes = [(c.M, c.N, c.K, e) for c, e in zip(cases, epilogues)]
     if args.tune:
         if args.grouped:
             w4.w4a16_tune_grouped(shapes, act=fx.act_dtype)
         else:
             for c in cases:
-                w4.w4a16_tune(c.M, c.N, c.K)
+                fx.tune(c.M, c.N, c.K)
 
     # --- resident inputs: the weights are quantized at load (once per copy);
     # the copies rotate step by step so that every step reads its weights and
@@ -434,7 +523,8 @@ def run_gpu(args, rank, world):
             wt = fx.new_weight(c.N, c.K)
             fx.quantize(W_dev[j], wt)
             s.append(dict(wt=wt, A=host[j][1].to(dev),
-                          Y=torch.empty(c.M, c.N, dtype=fx.act_dtype, device=dev)))
+                          Y=torch.empty(c.M, c.N // 2 if epilogues[j] else c.N,
+                                        dtype=fx.act_dtype, device=dev)))
         sets.append(s)
     torch.cuda.synchronize(dev)
     ws_bytes = max(fx.workspace_bytes(c.M, c.N, c.K) for c in cases)
@@ -442,7 +532,7 @@ def run_gpu(args, rank, world):
         probs, _, _ = w4._gemm_problems([s["A"] for s in sets[0]],
                                         [s["wt"]["packed"] for s in sets[0]],
                                         [s["wt"]["scales"] for s in sets[0]], None,
-                                        [s["Y"] for s in sets[0]])
+                                        [s["Y"] for s in sets[0]], epilogues)
         ws_bytes = max(ws_bytes, w4.lib().w4a16_gemm_grouped_workspace_bytes(probs, len(cases), -1))
     ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -456,7 +546,7 @@ def run_gpu(args, rank, world):
                 evs[0][0].record(st)
             w4.w4a16_gemm_grouped([s["A"] for s in sset], [s["wt"]["packed"] for s in sset],
                                   [s["wt"]["scales"] for s in sset], Ys=[s["Y"] for s in sset],
-                                  workspace=ws, stream=st)
+                                  workspace=ws, stream=st, epilogues=epilogues)
             if evs is not None:
                 evs[0][1].record(st)
             return
@@ -545,7 +635,8 @@ def run_gpu(args, rank, world):
     # --- e2e: the public API on host buffers: pinned activations copied in,
     # the step's GEMMs on the resident weights, the outputs copied back
     a_host = [A.pin_memory() for (_, A, _) in host]
-    y_host = [torch.empty(c.M, c.N, dtype=fx.act_dtype).pin_memory() for c in cases]
+    y_host = [torch.empty(c.M, c.N // 2 if e else c.N, dtype=fx.act_dtype).pin_memory()
+              for c, e in zip(cases, epilogues)]
     h2d = sum(a.numel() * a.element_size() for a in a_host)
     d2h = sum(y.numel() * y.element_size() for y in y_host)
     s0 = sets[0]
@@ -633,11 +724,21 @@ def run_gpu(args, rank, world):
     wcache = {}
     b2b = [back_to_back(fx, c, peaks, wcache, args.tune, dev) for c in
            {(c.M, c.N, c.K): c for c in cases}.values()] if len(cases) > 1 else []
-    sweep = None
-    if args.workload == "large" and not args.no_sweep:
+    if args.swiglu:
+        b2b += [back_to_back(fx, c, peaks, wcache, args.tune, dev, swiglu=True)
+                for c, e in zip(cases, epilogues) if e]
+    sweep = block = None
+    if (args.workload == "large" and not args.shape and not args.no_sweep and fmt == "int4"
+            and args.act == "bf16"):
         del sets, W_dev
         torch.cuda.empty_cache()
         sweep = [back_to_back(fx, c, peaks, wcache, args.tune, dev) for c in synthetic.SWEEP]
+        # the action-expert block (M = 50) as one grouped launch, plain and
+        # with the SwiGLU epilogue on its gate/up projection
+        ex = synthetic.EXPERT_M50
+        block = [grouped_back_to_back(w4, ex, [0] * len(ex), peaks, args.tune, dev),
+                 grouped_back_to_back(w4, ex, [1 if "gate_up" in c.name else 0 for c in ex],
+                                      peaks, args.tune, dev)]
     if w4.w4a16_get_device_error() != w4.W4A16_OK:
         raise RuntimeError("device error during the back-to-back GEMM timing")
 
@@ -645,10 +746,12 @@ def run_gpu(args, rank, world):
                warmup=args.warmup, ms_per_step=round(elapsed_ms / args.steps, 5),
                higher_is_better=True, scaling="weak", vs_baseline=None, dtype=args.act,
                data="synthetic",
-               config=dict(workload=args.workload, activations=args.act, weights=fmt,
+               config=dict(workload=args.workload if not args.shape else "shape " + args.shape,
+                           activations=args.act, weights=fmt,
                            shapes=[[c.M, c.N, c.K] for c in cases],
                            step=("one grouped W4A16 GEMM launch over all projections"
                                  if args.grouped else "one GEMM launch per projection") +
+                                (" (gate/up with the SwiGLU epilogue)" if any(epilogues) else "") +
                                 " on weights quantized at load (the quantize is timed apart, "
                                 "under kernels)",
                            l2="inputs rotate over %d copies (%.0f MB of weights and activations "
@@ -665,6 +768,8 @@ def run_gpu(args, rank, world):
                         d2h_bytes_per_step=int(d2h)))
     if b2b:
         out["gemm_back_to_back"] = b2b
+    if block is not None:
+        out["expert_block_grouped"] = block
     if sweep is not None:
         out["sweep"] = sweep
         out["sweep_roofline_frac"] = dict(
@@ -676,7 +781,7 @@ def run_gpu(args, rank, world):
 
 
 # ------------------------------------------------------------- CPU oracle
-def time_oracle(workload: str, budget_s: float, weights="int4", rows=1024):
+def time_oracle(workload, budget_s: float, weights="int4", rows=1024):
     """The oracle as it stands, on the host cores: each projection's weight
     quantized once by the oracle (load time, untimed), then the oracle's GEMM
     (dequantize + FP32 matmul) on the first `rows` rows of the activations,
@@ -687,7 +792,8 @@ def time_oracle(workload: str, budget_s: float, weights="int4", rows=1024):
     import oracle
     from weight_only_int4_rtn_gb300 import synthetic
 
-    cases = synthetic.WORKLOADS[workload]
+    cases = synthetic.WORKLOADS[workload] if isinstance(workload, str) else workload
+    name = workload if isinstance(workload, str) else cases[0].name
     prepared = []
     for c in cases:
         W, A, _ = synthetic.draw(c)
@@ -719,7 +825,7 @@ def time_oracle(workload: str, budget_s: float, weights="int4", rows=1024):
     dt = time.perf_counter() - t0
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
     sampled = any(mr < c.M for c, _, mr, _ in prepared)
-    sample = (f"{passes} pass(es) of {workload}: the oracle's "
+    sample = (f"{passes} pass(es) of {name}: the oracle's "
               + ({"int8": "INT8 ", "mxfp4": "MXFP4 ", "nvfp4": "NVFP4 "}.get(weights, ""))
               + "GEMM (dequantize + FP32 matmul) per projection"
               + (f" on the first {rows} rows of A" if sampled else "")
@@ -748,6 +854,11 @@ def main():
     ap.add_argument("--sr-seed", type=int, default=None,
                     help="quantize at load with seeded stochastic rounding (w4a16_quantize_sr) "
                          "instead of round to nearest")
+    ap.add_argument("--shape", default=None,
+                    help="M,N,K: one projection of this shape instead of the workload's")
+    ap.add_argument("--swiglu", action="store_true",
+                    help="the gate/up projection takes the SwiGLU epilogue: inside the grouped "
+                         "step, and back to back through w4a16_gemm_swiglu (INT4, bf16)")
     ap.add_argument("--no-sweep", action="store_true",
                     help="leave out the M in {1, 4, 16, 64} sweep of the default line")
     ap.add_argument("--no-tune", dest="tune", action="store_false", default=True,
@@ -767,11 +878,13 @@ def main():
             return 0
         # each step a bounded sample of the workload: about 1.2 s of oracle work
         t_budget = max(5.0, min(90.0, 1.2 * (args.steps + args.warmup)))
-        cb = time_oracle(args.workload, t_budget, args.weights)
+        cb = time_oracle(workload_cases(args), t_budget, args.weights)
         line = dict(metric=METRIC, value=cb["value"], unit="TFLOP/s", n_gpus=world,
                     steps=args.steps, warmup=args.warmup, ms_per_step=None, higher_is_better=True,
                     scaling="weak", vs_baseline=None, dtype="f32", data="synthetic",
-                    impl="reference", config=dict(workload=args.workload, weights=args.weights),
+                    impl="reference",
+                    config=dict(workload=args.workload if not args.shape else "shape " + args.shape,
+                                weights=args.weights),
                     cpu_baseline=cb,
                     e2e=dict(value=cb["value"], unit="TFLOP/s", h2d_bytes_per_step=0,
                              d2h_bytes_per_step=0))
@@ -788,7 +901,7 @@ def main():
     build()
     out = run_gpu(args, rank, world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = time_oracle(args.workload, args.cpu_budget, args.weights)
+        out["cpu_baseline"] = time_oracle(workload_cases(args), args.cpu_budget, args.weights)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
