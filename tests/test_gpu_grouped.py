@@ -48,8 +48,9 @@ def test_grouped_gemm_every_variant(w4, act):
     As = [A.cuda() for _, A, _ in drawn]
     bs = [None if b is None else b.cuda() for _, _, b in drawn]
     for v in range(w4.w4a16_variant_count()):
-        if not all(w4.w4a16_variant_eligible(v, c.M, c.N, c.K) for c in MIXED):
-            continue
+        if "csk" in w4.w4a16_variant_name(v) or not all(
+                w4.w4a16_variant_eligible(v, c.M, c.N, c.K) for c in MIXED):
+            continue   # cluster split-K runs single problems only
         Ys = w4.w4a16_gemm_grouped(As, [p for p, _ in q], [s for _, s in q], biases=bs, variant=v)
         assert w4.w4a16_get_device_error() == w4.W4A16_OK, w4.w4a16_variant_name(v)
         for c, Y, ref in zip(MIXED, Ys, refs):

@@ -22,9 +22,11 @@ pytestmark = pytest.mark.gpu
 
 def test_noalloc_matches_regular_entry_point_twice(w4):
     L = w4.lib()
-    # a stream-K shape: the variant for it needs scratch
+    # a stream-K variant for this shape, so that the call uses the scratch
+    # (the library's own choice for a shape may need none)
     case = synthetic.Case("noalloc_m16_n2048_k2048", 16, 2048, 2048, 41, bias=True)
     M, N, K = case.M, case.N, case.K
+    w4.w4a16_table_set(M, N, K, w4.variant_id("tc_a16_grp_sk"))
     assert w4.w4a16_gemm_workspace_bytes(M, N, K) > 0
     W, A, b = synthetic.draw(case)
     packed, scales = w4.w4a16_quantize(W.cuda())
@@ -45,6 +47,7 @@ def test_noalloc_matches_regular_entry_point_twice(w4):
         check_gemm_close(Y, y_regular.float().cpu().numpy(), what=f"noalloc call {call}")
         check_gemm_close(Y, y_ref, what=f"noalloc call {call} vs oracle")
     assert w4.w4a16_get_device_error() == w4.W4A16_OK
+    w4.w4a16_table_clear()
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch(w4):

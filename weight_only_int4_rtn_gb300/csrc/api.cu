@@ -88,6 +88,12 @@ bool device_info(DeviceInfo& out) {
   return true;
 }
 
+// The current device's SM count (the GB300 count without a device).
+int current_sms() {
+  DeviceInfo dev;
+  return device_info(dev) ? dev.num_sms : kDefaultSms;
+}
+
 // ------------------------------------------------------------ catalogue
 struct Variant {
   const char* name;
@@ -99,6 +105,7 @@ struct Variant {
                    // in steady state on GB300, for the selection rule
   double head_us = -1.0;   // launch-to-steady-state cost if not the common one
   double split_us = -1.0;  // split-tile fixup cost if not the common model's
+  int csk = 0;             // > 1: cluster split-K with clusters of up to csk CTAs
 };
 
 const Variant kVariants[] = {
@@ -133,6 +140,14 @@ const Variant kVariants[] = {
     {"tc_a32_deq2_sk_u2", {32, 2, false, 6, 2}, true, 1, 1.01},
     {"tc_a64_deq2_sk_u2", {64, 2, false, 4, 2}, true, 1, 1.08},
     {"tc_a64_deq2_dp_u2", {64, 2, false, 4, 2}, false, 1, 0.98},
+    // cluster split-K: a tile's K range over the CTAs of one cluster (at
+    // most 8), partials summed through distributed shared memory; for few
+    // tiles of long K
+    {"tc_a16_grp_csk", {16, 2, true, 16}, false, 1, 0.44, -1.0, 0.3, 8},
+    {"tc_a16_grp_csk_u2", {16, 2, true, 8, 2}, false, 1, 0.66, -1.0, 0.3, 8},
+    {"tc_a32_deq2_csk", {32, 2, false, 12}, false, 1, 0.48, -1.0, 0.3, 8},
+    {"tc_a64_deq2_csk", {64, 2, false, 8}, false, 1, 0.50, -1.0, 0.35, 8},
+    {"tc_a128_deq2_csk", {128, 2, false, 4}, false, 1, 0.65, -1.0, 0.5, 8},
     // CUDA-core streaming kernel for M <= 1, 2, 4, 8: unit_us is the time of
     // one unit on one worker (a warp; many warps share an SM)
     {"simt_m1_sk", {1, 1, true, 2, 1, kFmtInt4, true}, true, 1, 6.0, 2.0, 0.8},
@@ -223,6 +238,18 @@ GemmSchedule make_schedule(const Variant& v, int64_t M, int64_t N, int64_t K, in
   const int64_t tiles = gemm_tiles(v.cfg, M, N);
   const int64_t KB = K / kGroup / v.cfg.unit_groups;   // units per tile
   const int64_t units = tiles * KB;
+  if (v.csk > 1) {
+    // the largest power-of-two cluster (<= v.csk, <= KB) such that every
+    // tile's cluster is resident at once (tiles * cluster <= SMs); grid 0
+    // when no cluster of 2 or more fits
+    int S = 1;
+    while (2 * S <= v.csk && 2 * S <= KB && tiles * 2 * S <= num_sms) S *= 2;
+    s.cluster = S;
+    s.grid = S > 1 ? static_cast<int>(tiles * S) : 0;
+    s.dp_tiles = 0;
+    s.sk_units = 0;
+    return s;
+  }
   if (!v.stream_k) {
     s.grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
     s.dp_tiles = static_cast<int>(tiles);
@@ -254,6 +281,8 @@ GemmSchedule make_schedule(const Variant& v, int64_t M, int64_t N, int64_t K, in
   return s;
 }
 
+int current_sms();
+
 bool variant_ok(const Variant& v, int64_t M, int64_t N, int64_t K) {
   if (!shape_ok(M, N, K)) return false;
   if (v.cfg.simt && M > v.cfg.act_tile) return false;
@@ -261,6 +290,7 @@ bool variant_ok(const Variant& v, int64_t M, int64_t N, int64_t K) {
   const int64_t tiles = gemm_tiles(v.cfg, M, N);
   if (tiles * (K / kGroup) >= (1ll << 31)) return false;
   if ((K / kGroup) % v.cfg.unit_groups != 0) return false;
+  if (v.csk > 1 && make_schedule(v, M, N, K, current_sms()).cluster < 2) return false;
   return true;
 }
 
@@ -290,6 +320,9 @@ constexpr double kSplitUsPerCol = 0.051;
 
 double estimate_sched(const Variant& v, const GemmSchedule& s, int64_t K) {
   const int64_t KB = K / kGroup / v.cfg.unit_groups;
+  if (s.cluster > 1)
+    return (v.head_us >= 0.0 ? v.head_us : kHeadUs) +
+           static_cast<double>((KB + s.cluster - 1) / s.cluster) * v.unit_us + v.split_us;
   const int64_t dp_per_cta = (s.dp_tiles + s.grid - 1) / s.grid;
   const int64_t sk_per_cta = (s.sk_units + s.grid - 1) / s.grid;
   double t = (v.head_us >= 0.0 ? v.head_us : kHeadUs) +
@@ -433,7 +466,9 @@ int select_variant(int64_t M, int64_t N, int64_t K) {
 // SwiGLU epilogue: the variant select_variant gives for the shape, unless it
 // is a CUDA-core streaming variant (whose epilogue does not pair rows); then
 // the rule over the tcgen05 variants.
-bool swiglu_ok(int id) { return id >= 0 && id < kNumVariants && !kVariants[id].cfg.simt; }
+bool swiglu_ok(int id) {
+  return id >= 0 && id < kNumVariants && !kVariants[id].cfg.simt && kVariants[id].csk == 0;
+}
 
 int select_variant_swiglu(int64_t M, int64_t N, int64_t K) {
   const int tuned = table_get(kCatSwiglu, M, N, K);
@@ -617,7 +652,7 @@ GemmSchedule group_schedule(const Variant& v, const w4a16_gemm_problem& p, int c
 bool plan_for_variant(int id, const w4a16_gemm_problem* pr, int count, int sms, GroupPlan& plan,
                       bool forced) {
   const Variant& v = kVariants[id];
-  if (v.cfg.simt && count > 1) return false;   // single problems only
+  if ((v.cfg.simt || v.csk > 1) && count > 1) return false;   // single problems only
   for (int i = 0; i < count; ++i) {
     if (!variant_eligible(id, pr[i].M, pr[i].N, pr[i].K)) return false;
     if (pr[i].epilogue == W4A16_EPILOGUE_SWIGLU && !swiglu_ok(id)) return false;

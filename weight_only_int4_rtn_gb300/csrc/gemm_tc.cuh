@@ -137,6 +137,8 @@ struct Args {
   int dp_tiles;
   int sk_units;
   int act_3d;                  // activation map is 3-D: both 64-k halves in one copy
+  int csk;                     // cluster split-K: each tile's K range split over the
+                               // csk CTAs of one thread-block cluster (0: off)
   int sw;                      // this problem takes the SwiGLU epilogue (read by the
                                // instances compiled with it only)
   int prefetch_w;              // weights are not written by the previous kernel on
@@ -185,6 +187,17 @@ struct Sched {
     C = ctas;
     KB = a.KB;
     dp_tiles = a.dp_tiles;
+    if (a.csk > 1) {
+      // cluster split-K: cluster cta / csk owns tile cta / csk; its CTA of
+      // rank r runs that tile's units [r KB / csk, (r + 1) KB / csk)
+      const int t = cta / a.csk, r = cta - t * a.csk;
+      dp_tiles = 0;
+      dp_iters = 0;
+      u0 = t * KB + (r * KB) / a.csk;
+      u1 = t * KB + ((r + 1) * KB) / a.csk;
+      total = u1 - u0;
+      return;
+    }
     dp_iters = (dp_tiles > c) ? (dp_tiles - c + C - 1) / C : 0;
     u0 = static_cast<int>((static_cast<int64_t>(c) * a.sk_units) / C);
     u1 = static_cast<int>((static_cast<int64_t>(c + 1) * a.sk_units) / C);
@@ -496,6 +509,7 @@ struct Cfg {
   static_assert(kDB <= 8, "barrier arrays");
   static_assert(L * kRL <= 32, "barrier arrays");
   static_assert(!GRP || BA <= 64, "group mode keeps BA fp32 accumulators per thread");
+  static_assert(BA * kTileW * 4 <= STAGES * kStage, "cluster split-K partial fits the stages");
   static_assert(!GRP || L == 2, "group mode runs two lanes (the readout takes units in pairs)");
   // group mode: the pair ring replaces the unit ring for every waiter, so
   // it must be as deep as the stage rings and the accumulator buffers
@@ -560,9 +574,14 @@ __device__ __forceinline__ void swiglu_vals(float (&h)[K]) {
 // either to Y (whole tile: bias added, one rounding to the output type; or
 // the SwiGLU epilogue, swiglu_vals) or to this CTA's partial slot (fp32, no
 // bias; column m of the slot holds 128 rows).  Called by whole warps.
+// Cluster split-K: the CTA's partial tile, [BA][128] fp32 at the start of
+// the (by then drained) shared-memory stages.
+__device__ __forceinline__ float* csk_partial(uint8_t* smem) { return reinterpret_cast<float*>(smem); }
+
 template <int BA, int CNT, bool F16, bool SW>
 __device__ __forceinline__ void emit_cols(const Args& a, const Unit& u, int row, int col0,
-                                          const float (&v)[CNT], float bias_n, int cta) {
+                                          const float (&v)[CNT], float bias_n, int cta,
+                                          float* sp) {
   const int n0 = (u.tile % a.n_tiles) * kTileW;
   const int m0 = (u.tile / a.n_tiles) * BA;
   if (u.whole) {
@@ -590,6 +609,11 @@ __device__ __forceinline__ void emit_cols(const Args& a, const Unit& u, int row,
         if (m < a.M) a.Y[static_cast<int64_t>(m) * a.N + n] = act_from_float<F16>(v[j] + bias_n);
       }
     }
+  } else if (a.csk > 1) {
+    // the run's partial stays in this CTA's shared memory; the cluster sums
+    // the partials of the tile at exit
+#pragma unroll
+    for (int j = 0; j < CNT; ++j) sp[(col0 + j) * kTileW + row] = v[j];
   } else {
     float* slot = a.ws + (static_cast<int64_t>(cta) * 2 + u.slot) * (BA * kTileW) + row;
 #pragma unroll
@@ -768,6 +792,40 @@ __device__ void wide_fixup(const Args& a, const Shared* sh) {
       }
     }
   }
+}
+
+// Cluster split-K reduction, by every thread of every CTA of the cluster at
+// exit.  The csk CTAs of a cluster hold the partials of one tile (rank r:
+// the r-th K range) in their shared memory.  After a cluster barrier (every
+// CTA reaches it: all of the kernel's waits before it are bounded, and a CTA
+// whose wait ran out still comes here), CTA r sums the r-th slice of the
+// tile's 128 x BA values over the ranks in rank order, i.e. in k order (the
+// result does not depend on timing), reading its peers' partials through
+// distributed shared memory, adds the bias in fp32, rounds once and stores
+// Y.  A second cluster barrier keeps every CTA's shared memory alive until
+// its peers have read it.  A CTA whose kernel gave up (abort flag) stores
+// nothing: the error word already reports the launch as failed.
+template <int BA, bool F16>
+__device__ void csk_reduce(const Args& a, const Shared* sh, int cta, float* sp) {
+  ptx::cluster_sync();
+  const int S = a.csk;
+  const int t = cta / S, r = cta - t * S;
+  const int n0 = (t % a.n_tiles) * kTileW;
+  const int m0 = (t / a.n_tiles) * BA;
+  constexpr int kE = BA * kTileW;   // values of a tile, column-major ([BA][128])
+  const int e0 = (r * kE) / S, e1 = ((r + 1) * kE) / S;
+  const uint32_t base = ptx::smem_u32(sp);
+  const bool ok = *reinterpret_cast<const volatile int*>(&sh->abort_flag) == 0;
+  for (int e = e0 + static_cast<int>(threadIdx.x); ok && e < e1; e += static_cast<int>(blockDim.x)) {
+    const int col = e / kTileW, row = e - col * kTileW;
+    const int m = m0 + col, n = n0 + row;
+    if (m >= a.M || n >= a.N) continue;
+    float sum = 0.0f;
+    for (int q = 0; q < S; ++q) sum += ptx::ld_dsmem_f32(base + 4u * static_cast<uint32_t>(e), q);
+    if (a.bias != nullptr) sum += act_to_float<F16>(a.bias[n]);
+    a.Y[static_cast<int64_t>(m) * a.N + n] = act_from_float<F16>(sum);
+  }
+  ptx::cluster_sync();
 }
 
 template <int BA, int L, bool GRP, int STAGES, int UG, int WF, bool F16, int G, bool SW>
@@ -1198,7 +1256,7 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG, WF>::kThreads, 1)
         cur.next(seg, kb0, seg_left, a.dp_tiles);
         const int n = (seg.tile % a.n_tiles) * kTileW + row;
         bias_f = (a.bias != nullptr && n < a.N) ? act_to_float<F16>(a.bias[n]) : 0.0f;
-        if (!seg.whole) si = split_info(a, seg.sk_tile, ctas);
+        if (!seg.whole && a.csk <= 1) si = split_info(a, seg.sk_tile, ctas);
         first = true;
       };
       if (total > 0) open_run();
@@ -1216,8 +1274,8 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG, WF>::kThreads, 1)
       auto finish_unit = [&](int i) {
         first = false;
         if (--seg_left == 0) {
-          emit_cols<BA, BA, F16, SW>(a, seg, row, 0, acc, bias_f, cta);
-          if (!seg.whole)
+          emit_cols<BA, BA, F16, SW>(a, seg, row, 0, acc, bias_f, cta, csk_partial(smem));
+          if (!seg.whole && a.csk <= 1)
             ok = split_fixup<BA, F16, SW>(a, seg, si, sh, row, bias_f, nsync, wc, i + 1 == total);
           if (i + 1 < total) open_run();
         }
@@ -1342,12 +1400,12 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG, WF>::kThreads, 1)
 #pragma unroll
             for (int c = 0; c < C::kChunk; ++c) v[c] *= g_t;
           }
-          emit_cols<BA, C::kChunk, F16, SW>(a, u, row, c0, v, bias_f, cta);
+          emit_cols<BA, C::kChunk, F16, SW>(a, u, row, c0, v, bias_f, cta, csk_partial(smem));
         }
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&sh->dempty[db]);
-        if (!u.whole &&
+        if (!u.whole && a.csk <= 1 &&
             !split_fixup<BA, F16, SW>(a, u, split_info(a, u.sk_tile, ctas), sh, row, bias_f, nsync, wc,
                                   i + 1 == total))
           break;
@@ -1513,6 +1571,7 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG, WF>::kThreads, 1)
   ptx::tc_fence_after();
   if (warp == 1) ptx::tmem_dealloc(tmem, kTmemCols);
   if (sh->fixup_defer) wide_fixup<BA, F16, SW>(a, sh);
+  if (a.csk > 1) csk_reduce<BA, F16>(a, sh, cta, csk_partial(smem));
   if (threadIdx.x == 32) W4A16_TRACE_POINT(11);
 }
 
@@ -1588,6 +1647,7 @@ cudaError_t launch_instance(const GemmGroup& grp, bool use_pdl, cudaStream_t str
     a.dp_tiles = s.dp_tiles;
     a.sk_units = static_cast<int>(s.sk_units);
     a.act_3d = act_3d;
+    a.csk = s.cluster > 1 ? s.cluster : 0;
     a.sw = SW && p.swiglu ? 1 : 0;
     // two units per producer: deeper early copies sit ahead of the first
     // activation copy in the TMA queue and delay the start (measured)
@@ -1608,16 +1668,31 @@ cudaError_t launch_instance(const GemmGroup& grp, bool use_pdl, cudaStream_t str
   g.cta_start[grp.count] = start;
   g.count = grp.count;
 
+  // cluster split-K: one problem, its grid a whole number of clusters
+  const int cluster = grp.s[0].cluster > 1 ? grp.s[0].cluster : 0;
+  if (cluster > 0 && (grp.count != 1 || start % cluster != 0 || cluster > 8))
+    return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(start));
   cfg.blockDim = dim3(C::kThreads);
   cfg.dynamicSmemBytes = C::kSmem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (use_pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  if (cluster > 0) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = static_cast<unsigned>(cluster);
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = use_pdl ? 1 : 0;
+  cfg.numAttrs = na;
   return cudaLaunchKernelEx(&cfg, kernel, g);
 }
 

@@ -80,6 +80,11 @@ struct GemmSchedule {
   int dp_tiles;      // tiles 0..dp_tiles-1 run whole, tile t on CTA t % grid
   int64_t sk_units;  // the remaining tiles' (tile, k-block) units, split in
                      // contiguous balanced ranges over all CTAs
+  int cluster = 0;   // > 1: cluster split-K instead (dp_tiles = sk_units = 0):
+                     // grid = tiles * cluster, tile t's K range split over the
+                     // cluster CTAs t * cluster .. + cluster - 1 of one
+                     // thread-block cluster, summed through distributed
+                     // shared memory (no workspace)
 };
 
 struct GemmProblem {

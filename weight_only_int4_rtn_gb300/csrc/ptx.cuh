@@ -344,6 +344,23 @@ __device__ __forceinline__ uint32_t atom_add_release_gpu(uint32_t* p, uint32_t v
   return old;
 }
 
+// Thread-block cluster barrier: every thread of every CTA of the cluster
+// arrives (release) and waits (acquire) for all the others.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+
+// fp32 load from the shared memory of CTA `rank` of this cluster, at the
+// shared-memory address `saddr` of the same variable in this CTA.
+__device__ __forceinline__ float ld_dsmem_f32(uint32_t saddr, int rank) {
+  uint32_t remote;
+  float v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(saddr), "r"(rank));
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ void nanosleep(uint32_t ns) {
   asm volatile("nanosleep.u32 %0;" ::"r"(ns));
 }
