@@ -148,6 +148,11 @@ const Variant kVariants[] = {
     {"tc_a32_deq2_csk", {32, 2, false, 12}, false, 1, 0.48, -1.0, 0.3, 8},
     {"tc_a64_deq2_csk", {64, 2, false, 8}, false, 1, 0.50, -1.0, 0.35, 8},
     {"tc_a128_deq2_csk", {128, 2, false, 4}, false, 1, 0.65, -1.0, 0.5, 8},
+    // row-block CUDA-core kernel for M <= 1, 2, 4: unit_us is the time of one
+    // 128 x 128 unit per SM (all its CTAs together)
+    {"simt_m1_rb", {1, 1, true, 0, 1, kFmtInt4, true, true}, false, 1, 0.30, 2.0, 0.0},
+    {"simt_m2_rb", {2, 1, true, 0, 1, kFmtInt4, true, true}, false, 1, 0.36, 2.0, 0.0},
+    {"simt_m4_rb", {4, 1, true, 0, 1, kFmtInt4, true, true}, false, 1, 0.50, 2.0, 0.0},
     // CUDA-core streaming kernel for M <= 1, 2, 4, 8: unit_us is the time of
     // one unit on one worker (a warp; many warps share an SM)
     {"simt_m1_sk", {1, 1, true, 2, 1, kFmtInt4, true}, true, 1, 6.0, 2.0, 0.8},
@@ -215,6 +220,20 @@ bool shape_ok(int64_t M, int64_t N, int64_t K) {
 
 GemmSchedule make_schedule(const Variant& v, int64_t M, int64_t N, int64_t K, int num_sms) {
   GemmSchedule s{};
+  if (v.cfg.rb) {
+    // row blocks; K split over a cluster (up to 8 CTAs, each at least one
+    // group) until there are two CTAs of 8 warps per SM
+    const int64_t rows = gemv_rb_rows(v.cfg.act_tile);
+    const int64_t blocks = (N + rows - 1) / rows;
+    const int64_t KB = K / kGroup;
+    int S = 1;
+    while (2 * S <= 8 && 2 * S <= KB && blocks * S < 2 * num_sms) S *= 2;
+    s.grid = static_cast<int>(blocks * S);
+    s.dp_tiles = 0;
+    s.sk_units = 0;
+    s.cluster = S;
+    return s;
+  }
   if (v.cfg.simt) {
     // workers (warps) of the CUDA-core streaming kernel: every resident slot
     // (the warps of an SM share its issue slots, so units balance per SM,
@@ -318,8 +337,11 @@ constexpr double kHeadUs = 3.71;
 constexpr double kSplitUs = 2.44;
 constexpr double kSplitUsPerCol = 0.051;
 
-double estimate_sched(const Variant& v, const GemmSchedule& s, int64_t K) {
+double estimate_sched(const Variant& v, const GemmSchedule& s, int64_t K, int64_t N = 0,
+                      int num_sms = kDefaultSms) {
   const int64_t KB = K / kGroup / v.cfg.unit_groups;
+  if (v.cfg.rb)   // the weight's 128 x 128 units shared by the SMs
+    return v.head_us + static_cast<double>((N + kTileW - 1) / kTileW * KB) / num_sms * v.unit_us;
   if (s.cluster > 1)
     return (v.head_us >= 0.0 ? v.head_us : kHeadUs) +
            static_cast<double>((KB + s.cluster - 1) / s.cluster) * v.unit_us + v.split_us;
@@ -332,7 +354,7 @@ double estimate_sched(const Variant& v, const GemmSchedule& s, int64_t K) {
 }
 
 double estimate_us(const Variant& v, int64_t M, int64_t N, int64_t K, int num_sms) {
-  return estimate_sched(v, make_schedule(v, M, N, K, num_sms), K);
+  return estimate_sched(v, make_schedule(v, M, N, K, num_sms), K, N, num_sms);
 }
 
 int rule_variant(int64_t M, int64_t N, int64_t K, int num_sms) {
@@ -629,14 +651,14 @@ struct GroupPlan {
 GemmSchedule group_schedule(const Variant& v, const w4a16_gemm_problem& p, int ctas, double& est,
                             bool own_only) {
   GemmSchedule s = make_schedule(v, p.M, p.N, p.K, ctas);
-  est = estimate_sched(v, s, p.K);
+  est = estimate_sched(v, s, p.K, p.N, ctas);
   if (!own_only && v.stream_k && s.sk_units > 0) {
     const int64_t tiles = gemm_tiles(v.cfg, p.M, p.N);
     GemmSchedule d{};
     d.grid = static_cast<int>(tiles < ctas ? tiles : ctas);
     d.dp_tiles = static_cast<int>(tiles);
     d.sk_units = 0;
-    const double ed = estimate_sched(v, d, p.K);
+    const double ed = estimate_sched(v, d, p.K, p.N, ctas);
     if (ed < est) {
       s = d;
       est = ed;

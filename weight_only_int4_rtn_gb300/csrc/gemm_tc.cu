@@ -23,6 +23,11 @@ __global__ void wait_timeout_selftest_kernel(uint32_t* err, uint64_t timeout_ns)
 }  // namespace
 
 size_t gemm_smem_bytes(const GemmKernelConfig& c) {
+  if (c.rb) {
+    // static shared memory only (per-warp row totals)
+    return (c.simt && c.weight_format == kFmtInt4 &&
+            (c.act_tile == 1 || c.act_tile == 2 || c.act_tile == 4)) ? 4096 : 0;
+  }
   if (c.simt) return gemv_smem_bytes(c);
 #define W4A16_SMEM_CASE(BA, L, GRP, ST, UG)                                          \
   if (c.act_tile == BA && c.lanes == L && c.group_scale == GRP && c.stages == ST && \
@@ -63,6 +68,7 @@ cudaError_t launch_gemm_tc_group(const GemmKernelConfig& c, const GemmGroup& grp
                                  cudaStream_t stream) {
   static_assert(kMaxGemmGroup == kMaxGroup, "group size of the kernel arguments");
   if (grp.count < 1 || grp.count > kMaxGroup) return cudaErrorInvalidValue;
+  if (c.rb) return launch_gemv_rb(c, grp, use_pdl, stream);
   if (c.simt) return launch_gemv(c, grp, use_pdl, stream);
   bool any_sw = false;
   for (int i = 0; i < grp.count; ++i) any_sw = any_sw || grp.p[i].swiglu;

@@ -63,6 +63,8 @@ struct GemmKernelConfig {
                                  // kFmtNvfp4 (FP4 weights, dequant mode)
   bool simt = false;  // the CUDA-core streaming kernel (gemv.cu) for M <= act_tile
                       // (1, 2, 4 or 8), INT4 weights
+  bool rb = false;    // with simt: the row-block CUDA-core kernel (gemv_rb.cu) for
+                      // M <= act_tile (1, 2 or 4)
 };
 
 // The CUDA-core streaming kernel: every warp is a stream-K worker with two
@@ -195,6 +197,14 @@ cudaError_t launch_repack_rowmajor(const void* rowmajor, int64_t N, int64_t K, v
 // counts[0..3] on `stream`, then adds the pairs checked, the codes that
 // differ, the quotients that differ in the normal range and anywhere.
 cudaError_t launch_quotient_selftest(int mode, unsigned long long* counts, cudaStream_t stream);
+
+// The row-block CUDA-core kernel (gemv_rb.cu): one problem, INT4 weights, bf16
+// or fp16 activations, M <= act_tile (1, 2, 4); schedule grid = row blocks x
+// cluster (a K split over the CTAs of a cluster when cluster > 1).  Rows per
+// block for an act_tile.
+cudaError_t launch_gemv_rb(const GemmKernelConfig& c, const GemmGroup& grp, bool use_pdl,
+                           cudaStream_t stream);
+int gemv_rb_rows(int act_tile);
 
 // Failure-detection self test: one thread waits on an mbarrier nobody
 // arrives at, with a bounded wait; records a timeout in *error_word.
