@@ -250,7 +250,10 @@ def test_static_weights_prefetch_back_to_back(w4):
     data-parallel shape); a launch that used another launch's operands would
     miss the tolerance."""
     cases = [synthetic.Case("static_m16_n1024_k2048", 16, 1024, 2048, 31, bias=True),
-             synthetic.Case("static_m64_n256_k4096", 64, 256, 4096, 32)]
+             synthetic.Case("static_m64_n256_k4096", 64, 256, 4096, 32),
+             # the CUDA-core kernels for M <= 4 (ragged last row block)
+             synthetic.Case("static_m1_n2056_k2048", 1, 2056, 2048, 33, bias=True),
+             synthetic.Case("static_m3_n1032_k4096", 3, 1032, 4096, 34)]
     try:
         w4.w4a16_set_weights_static(True)
         assert w4.w4a16_weights_static()

@@ -149,10 +149,10 @@ const Variant kVariants[] = {
     {"tc_a64_deq2_csk", {64, 2, false, 8}, false, 1, 0.50, -1.0, 0.35, 8},
     {"tc_a128_deq2_csk", {128, 2, false, 4}, false, 1, 0.65, -1.0, 0.5, 8},
     // row-block CUDA-core kernel for M <= 1, 2, 4: unit_us is the time of one
-    // 128 x 128 unit per SM (all its CTAs together)
-    {"simt_m1_rb", {1, 1, true, 0, 1, kFmtInt4, true, true}, false, 1, 0.30, 2.0, 0.0},
-    {"simt_m2_rb", {2, 1, true, 0, 1, kFmtInt4, true, true}, false, 1, 0.36, 2.0, 0.0},
-    {"simt_m4_rb", {4, 1, true, 0, 1, kFmtInt4, true, true}, false, 1, 0.50, 2.0, 0.0},
+    // (row block, group) item of the busiest warp on a full SM (rb_cost)
+    {"simt_m1_rb", {1, 1, true, 0, 1, kFmtInt4, true, true}, false, 1, 1.29, 1.85, 0.0},
+    {"simt_m2_rb", {2, 1, true, 0, 1, kFmtInt4, true, true}, false, 1, 1.20, 1.85, 0.0},
+    {"simt_m4_rb", {4, 1, true, 0, 1, kFmtInt4, true, true}, false, 1, 1.80, 1.85, 0.0},
     // CUDA-core streaming kernel for M <= 1, 2, 4, 8: unit_us is the time of
     // one unit on one worker (a warp; many warps share an SM)
     {"simt_m1_sk", {1, 1, true, 2, 1, kFmtInt4, true}, true, 1, 6.0, 2.0, 0.8},
@@ -218,20 +218,68 @@ bool shape_ok(int64_t M, int64_t N, int64_t K) {
          N * K < (1ll << 40);
 }
 
+// Row-block kernel: the largest number of (row block, group) items one warp
+// runs under schedule s (persistent teams, or cluster waves over `slots`
+// resident CTAs).
+int64_t rb_items(const GemmSchedule& s, int64_t blocks, int64_t KB, int64_t slots) {
+  if (s.cluster > 1) {
+    const int64_t waves = (blocks * s.cluster + slots - 1) / slots;
+    const int64_t per = static_cast<int64_t>(s.cluster) * kRbWarpsPerCta;
+    return waves * ((KB + per - 1) / per);
+  }
+  const int64_t teams = static_cast<int64_t>(s.grid) * (kRbWarpsPerCta / s.team);
+  return (blocks + teams - 1) / teams * ((KB + s.team - 1) / s.team);
+}
+
+// Its cost in units of one item's time on a full SM (two CTAs of 8 warps):
+// the busiest warp's items, at half that time per item when no SM holds
+// two CTAs (the warps of one CTA alone share the SM's issue slots with
+// nobody), plus the cluster split's own cost (barriers, the distributed
+// shared-memory sum), measured on GB300 at about 1.3 items.
+double rb_cost(const GemmSchedule& s, int64_t blocks, int64_t KB, int64_t slots, int num_sms) {
+  const double load = s.grid <= num_sms ? 0.5 : 1.0;
+  return static_cast<double>(rb_items(s, blocks, KB, slots)) * load + (s.cluster > 1 ? 1.3 : 0.0);
+}
+
 GemmSchedule make_schedule(const Variant& v, int64_t M, int64_t N, int64_t K, int num_sms) {
   GemmSchedule s{};
   if (v.cfg.rb) {
-    // row blocks; K split over a cluster (up to 8 CTAs, each at least one
-    // group) until there are two CTAs of 8 warps per SM
-    const int64_t rows = gemv_rb_rows(v.cfg.act_tile);
-    const int64_t blocks = (N + rows - 1) / rows;
+    // Items are (row block, group) pairs.  Persistent: the resident CTAs
+    // (fewer when there are fewer teams' worth of row blocks), teams of WK
+    // warps, row blocks dealt round-robin to the teams.  Cluster split: one
+    // CTA-wide team per row block and cluster rank, in waves of the
+    // resident CTAs.  The smallest cost (rb_cost) wins; ties go to the
+    // persistent form, then to smaller teams.
+    const int64_t blocks = (N + gemv_rb_rows(v.cfg.act_tile) - 1) / gemv_rb_rows(v.cfg.act_tile);
     const int64_t KB = K / kGroup;
-    int S = 1;
-    while (2 * S <= 8 && 2 * S <= KB && blocks * S < 2 * num_sms) S *= 2;
-    s.grid = static_cast<int>(blocks * S);
+    const int64_t slots = static_cast<int64_t>(num_sms) * gemv_rb_ctas_per_sm(v.cfg.act_tile);
+    double best = -1.0;
+    GemmSchedule c{};
+    c.dp_tiles = 0;
+    c.sk_units = 0;
+    for (int wk = 1; wk <= kRbWarpsPerCta && KB >= wk; wk *= 2) {
+      const int64_t tpc = kRbWarpsPerCta / wk;
+      c.grid = static_cast<int>(std::min(slots, (blocks + tpc - 1) / tpc));
+      c.team = wk;
+      c.cluster = 1;
+      const double cost = rb_cost(c, blocks, KB, slots, num_sms);
+      if (best < 0.0 || cost < best) {
+        best = cost;
+        s = c;
+      }
+    }
+    for (int S = 2; S <= 8 && KB >= S * kRbWarpsPerCta; S *= 2) {
+      c.grid = static_cast<int>(blocks * S);
+      c.team = kRbWarpsPerCta;
+      c.cluster = S;
+      const double cost = rb_cost(c, blocks, KB, slots, num_sms);
+      if (cost < best) {
+        best = cost;
+        s = c;
+      }
+    }
     s.dp_tiles = 0;
     s.sk_units = 0;
-    s.cluster = S;
     return s;
   }
   if (v.cfg.simt) {
@@ -340,8 +388,12 @@ constexpr double kSplitUsPerCol = 0.051;
 double estimate_sched(const Variant& v, const GemmSchedule& s, int64_t K, int64_t N = 0,
                       int num_sms = kDefaultSms) {
   const int64_t KB = K / kGroup / v.cfg.unit_groups;
-  if (v.cfg.rb)   // the weight's 128 x 128 units shared by the SMs
-    return v.head_us + static_cast<double>((N + kTileW - 1) / kTileW * KB) / num_sms * v.unit_us;
+  if (v.cfg.rb) {
+    // unit_us: one (row block, group) item of the busiest warp on a full SM
+    const int64_t rows = gemv_rb_rows(v.cfg.act_tile);
+    const int64_t slots = static_cast<int64_t>(num_sms) * gemv_rb_ctas_per_sm(v.cfg.act_tile);
+    return v.head_us + rb_cost(s, (N + rows - 1) / rows, K / kGroup, slots, num_sms) * v.unit_us;
+  }
   if (s.cluster > 1)
     return (v.head_us >= 0.0 ? v.head_us : kHeadUs) +
            static_cast<double>((KB + s.cluster - 1) / s.cluster) * v.unit_us + v.split_us;

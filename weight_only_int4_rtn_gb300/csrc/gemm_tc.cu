@@ -23,11 +23,7 @@ __global__ void wait_timeout_selftest_kernel(uint32_t* err, uint64_t timeout_ns)
 }  // namespace
 
 size_t gemm_smem_bytes(const GemmKernelConfig& c) {
-  if (c.rb) {
-    // static shared memory only (per-warp row totals)
-    return (c.simt && c.weight_format == kFmtInt4 &&
-            (c.act_tile == 1 || c.act_tile == 2 || c.act_tile == 4)) ? 4096 : 0;
-  }
+  if (c.rb) return c.simt && c.weight_format == kFmtInt4 ? gemv_rb_smem_bytes(c.act_tile) : 0;
   if (c.simt) return gemv_smem_bytes(c);
 #define W4A16_SMEM_CASE(BA, L, GRP, ST, UG)                                          \
   if (c.act_tile == BA && c.lanes == L && c.group_scale == GRP && c.stages == ST && \

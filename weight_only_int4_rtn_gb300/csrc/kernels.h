@@ -87,6 +87,8 @@ struct GemmSchedule {
                      // cluster CTAs t * cluster .. + cluster - 1 of one
                      // thread-block cluster, summed through distributed
                      // shared memory (no workspace)
+  int team = 8;      // row-block kernel: warps splitting one row block's K
+                     // range (1, 2, 4, 8; 8 with a cluster split)
 };
 
 struct GemmProblem {
@@ -199,12 +201,16 @@ cudaError_t launch_repack_rowmajor(const void* rowmajor, int64_t N, int64_t K, v
 cudaError_t launch_quotient_selftest(int mode, unsigned long long* counts, cudaStream_t stream);
 
 // The row-block CUDA-core kernel (gemv_rb.cu): one problem, INT4 weights, bf16
-// or fp16 activations, M <= act_tile (1, 2, 4); schedule grid = row blocks x
-// cluster (a K split over the CTAs of a cluster when cluster > 1).  Rows per
-// block for an act_tile.
+// or fp16 activations, M <= act_tile (1, 2, 4).  Persistent (cluster <= 1):
+// any grid, teams of `team` warps walk row blocks round-robin.  Cluster
+// split (cluster > 1): grid = row blocks x cluster, team = 8.  Rows per block
+// and resident CTAs per SM for an act_tile.
 cudaError_t launch_gemv_rb(const GemmKernelConfig& c, const GemmGroup& grp, bool use_pdl,
                            cudaStream_t stream);
 int gemv_rb_rows(int act_tile);
+constexpr int kRbWarpsPerCta = 8;
+int gemv_rb_ctas_per_sm(int act_tile);
+size_t gemv_rb_smem_bytes(int act_tile);   // dynamic shared memory; 0: no such kernel
 
 // Failure-detection self test: one thread waits on an mbarrier nobody
 // arrives at, with a bounded wait; records a timeout in *error_word.
