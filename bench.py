@@ -376,6 +376,7 @@ def back_to_back(fx, c, peaks, wcache, tune, dev, swiglu=False):
         W = synthetic.draw_weight_only(c.seed, c.N, c.K, c.wdist).to(dev)
         wt = fx.new_weight(c.N, c.K)
         fx.quantize(W, wt)
+        torch.cuda.synchronize(dev)   # weights complete before any GEMM may read them early
         del W
         wcache[key] = wt
     wt = wcache[key]
@@ -430,6 +431,7 @@ def grouped_back_to_back(w4, cases, epilogues, peaks, tune, dev):
         w4.w4a16_tune_grouped(shapes)
     drawn = [synthetic.draw(c) for c in cases]
     q = w4.w4a16_quantize_grouped([W.to(dev) for W, _, _ in drawn])
+    torch.cuda.synchronize(dev)   # weights complete before any GEMM may read them early
     nb = sum(p.numel() + s.numel() * 2 for p, s in q)
     ncp = max(1, min(16, -(-3 * L2_BYTES // nb)))
     cps = [q] + [[(p.clone(), s.clone()) for p, s in q] for _ in range(ncp - 1)]
@@ -527,6 +529,10 @@ def run_gpu(args, rank, world):
                                         dtype=fx.act_dtype, device=dev)))
         sets.append(s)
     torch.cuda.synchronize(dev)
+    # inference: no kernel writes the weights between steps (they are
+    # quantized above, at load), so each GEMM may request its first codes
+    # and scales before the previous kernel on the stream has finished
+    w4.w4a16_set_weights_static(args.static_weights)
     ws_bytes = max(fx.workspace_bytes(c.M, c.N, c.K) for c in cases)
     if args.grouped:
         probs, _, _ = w4._gemm_problems([s["A"] for s in sets[0]],
@@ -758,6 +764,7 @@ def run_gpu(args, rank, world):
                               "> 3x L2)" % (copies, copies * in_bytes / 2**20),
                            selection=("tuned by measurement before timing" if args.tune
                                       else "cost-model rule"),
+                           weights_static=bool(args.static_weights),
                            parallelism=f"replicas x{world}"),
                gemm=dict(tflops=round(value, 3),
                          weight_gbs=round(job_rate(wbytes_step, args.steps, elapsed_ms, world) / 1e9, 1),
@@ -864,6 +871,9 @@ def main():
     ap.add_argument("--no-tune", dest="tune", action="store_false", default=True,
                     help="select kernels by the cost-model rule instead of tuning each "
                          "shape by measurement first")
+    ap.add_argument("--dynamic-weights", dest="static_weights", action="store_false", default=True,
+                    help="do not declare the weights static (w4a16_set_weights_static): every GEMM "
+                         "then waits for the previous kernel before its first weight copy")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

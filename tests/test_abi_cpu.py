@@ -111,7 +111,7 @@ def test_swiglu_argument_errors_before_any_launch(built_lib):
     L = w4.lib()
     names = [w4.w4a16_variant_name(i) for i in range(w4.w4a16_variant_count())]
     args = (16, 4, 256, 512, 16, 16, 128, None, 16, None, 0, None)
-    simt = [i for i, n in enumerate(names) if n.startswith("simt_")]
+    simt = [i for i, n in enumerate(names) if n.startswith(("simt_", "rb_"))]
     assert simt
     for v in simt:   # the streaming variants have no SwiGLU epilogue
         assert L.w4a16_gemm_swiglu_variant(v, *args) == w4.W4A16_ERR_UNSUPPORTED
@@ -132,10 +132,10 @@ def test_variant_catalogue_is_host_only(built_lib):
     assert w4.w4a16_variant_name(n) is None
     for i in range(n):
         # the CUDA-core streaming variants take M up to their own tile
-        m = int(names[i].split("_")[1][1:]) if names[i].startswith("simt_") else 16
+        m = int(names[i].split("_")[1][1:]) if names[i].startswith(("simt_", "rb_")) else 16
         assert w4.w4a16_variant_eligible(i, m, 256, 512)
         assert not w4.w4a16_variant_eligible(i, m, 256, 500)
-        assert not names[i].startswith("simt_") or not w4.w4a16_variant_eligible(i, m + 1, 256, 512)
+        assert not names[i].startswith(("simt_", "rb_")) or not w4.w4a16_variant_eligible(i, m + 1, 256, 512)
     for M in (1, 4, 16, 50, 64, 816, 8192):
         v = w4.w4a16_select_variant(M, 8192, 8192)
         assert 0 <= v < n

@@ -1,5 +1,5 @@
-"""The CUDA-core GEMM variants for tiny M (the stream-K workers
-simt_m{1,2,4,8}_sk and the row-block kernels simt_m{1,2,4}_rb)
+"""The streaming GEMM variants for tiny M (the CUDA-core stream-K workers
+simt_m{1,2,4,8}_sk and the row-block warp-MMA kernels rb_m{1,2,4,8})
 against the oracle's FP32 GEMM on identical packed operands: every M from 1
 to 8 on ragged, multi-tile and long-K shapes within |y - y_ref| <= 1e-2
 |y_ref| + 1e-2 rms(y_ref); bit-exact on integer-exact inputs; split tiles
@@ -19,7 +19,7 @@ NAN_BF16 = 0x7FC1
 
 
 def simt_variants(w4):
-    return [v for v in range(w4.w4a16_variant_count()) if w4.w4a16_variant_name(v).startswith("simt_")]
+    return [v for v in range(w4.w4a16_variant_count()) if w4.w4a16_variant_name(v).startswith(("simt_", "rb_"))]
 
 
 def reference(A, packed, scales, b, rows=None):
@@ -101,9 +101,9 @@ def test_simt_split_tiles_deterministic(w4):
             continue
         need = w4.w4a16_variant_workspace_bytes(v, case.M, case.N, case.K)
         # the stream-K workers split tiles through the workspace; the
-        # row-block variants (simt_m*_rb) split K inside a CTA and a cluster
-        # and need none
-        rowblock = w4.w4a16_variant_name(v).endswith("_rb")
+        # row-block variants (rb_m*) split K inside a CTA and a cluster and
+        # need none
+        rowblock = w4.w4a16_variant_name(v).startswith("rb_")
         assert need == 0 if rowblock else need > 8192
         ys = []
         for _ in range(2):

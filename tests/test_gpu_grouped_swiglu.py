@@ -41,7 +41,7 @@ def test_grouped_block_with_swiglu_every_variant(w4):
     ran = 0
     for v in range(w4.w4a16_variant_count()):
         name = w4.w4a16_variant_name(v)
-        if name.startswith("simt_") or "csk" in name or not all(
+        if name.startswith(("simt_", "rb_")) or "csk" in name or not all(
                 w4.w4a16_variant_eligible(v, c.M, c.N, c.K) for c in BLOCK):
             continue
         Ys = w4.w4a16_gemm_grouped(As, [p for p, _ in q], [s for _, s in q], biases=bs, variant=v,
@@ -55,7 +55,7 @@ def test_grouped_block_with_swiglu_every_variant(w4):
 
 def test_grouped_block_with_swiglu_tuned_plan(w4):
     v = w4.w4a16_tune_grouped([(c.M, c.N, c.K, e) for c, e in zip(BLOCK, EPI)])
-    assert not w4.w4a16_variant_name(v).startswith("simt_")
+    assert not w4.w4a16_variant_name(v).startswith(("simt_", "rb_"))
     drawn, q = _operands(w4, BLOCK)
     Ys = w4.w4a16_gemm_grouped([A.cuda() for _, A, _ in drawn], [p for p, _ in q], [s for _, s in q],
                                biases=[None if b is None else b.cuda() for _, _, b in drawn],

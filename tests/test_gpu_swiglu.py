@@ -66,7 +66,7 @@ def tc_variants(w4):
     # tcgen05 variants with a SwiGLU form: not the CUDA-core streaming ones,
     # not cluster split-K (its exit reduction stores plain outputs)
     return [v for v in range(w4.w4a16_variant_count())
-            if not w4.w4a16_variant_name(v).startswith("simt_")
+            if not w4.w4a16_variant_name(v).startswith(("simt_", "rb_"))
             and "csk" not in w4.w4a16_variant_name(v)]
 
 
@@ -104,7 +104,7 @@ def test_streaming_variants_are_rejected(w4):
     Ad, bd, packed, scales, _ = operands(w4, case)
     for v in range(w4.w4a16_variant_count()):
         name = w4.w4a16_variant_name(v)
-        if not (name.startswith("simt_") or "csk" in name):
+        if not (name.startswith(("simt_", "rb_")) or "csk" in name):
             continue
         with pytest.raises(w4.W4A16Error):
             w4.w4a16_gemm_swiglu(Ad[:1].contiguous(), packed, scales, variant=v)

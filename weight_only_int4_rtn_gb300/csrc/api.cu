@@ -148,11 +148,12 @@ const Variant kVariants[] = {
     {"tc_a32_deq2_csk", {32, 2, false, 12}, false, 1, 0.48, -1.0, 0.3, 8},
     {"tc_a64_deq2_csk", {64, 2, false, 8}, false, 1, 0.50, -1.0, 0.35, 8},
     {"tc_a128_deq2_csk", {128, 2, false, 4}, false, 1, 0.65, -1.0, 0.5, 8},
-    // row-block CUDA-core kernel for M <= 1, 2, 4: unit_us is the time of one
-    // (row block, group) item of the busiest warp on a full SM (rb_cost)
-    {"simt_m1_rb", {1, 1, true, 0, 1, kFmtInt4, true, true}, false, 1, 1.29, 1.85, 0.0},
-    {"simt_m2_rb", {2, 1, true, 0, 1, kFmtInt4, true, true}, false, 1, 1.20, 1.85, 0.0},
-    {"simt_m4_rb", {4, 1, true, 0, 1, kFmtInt4, true, true}, false, 1, 1.80, 1.85, 0.0},
+    // row-block warp-MMA kernel for M <= 1, 2, 4, 8: unit_us is the time of
+    // one (row block, group) item of the busiest warp on a full SM (rb_cost)
+    {"rb_m1", {1, 1, true, 0, 1, kFmtInt4, true, true}, false, 1, 1.12, 1.85, 0.0},
+    {"rb_m2", {2, 1, true, 0, 1, kFmtInt4, true, true}, false, 1, 1.30, 1.85, 0.0},
+    {"rb_m4", {4, 1, true, 0, 1, kFmtInt4, true, true}, false, 1, 1.56, 1.85, 0.0},
+    {"rb_m8", {8, 1, true, 0, 1, kFmtInt4, true, true}, false, 1, 1.98, 1.85, 0.0},
     // CUDA-core streaming kernel for M <= 1, 2, 4, 8: unit_us is the time of
     // one unit on one worker (a warp; many warps share an SM)
     {"simt_m1_sk", {1, 1, true, 2, 1, kFmtInt4, true}, true, 1, 6.0, 2.0, 0.8},
@@ -232,13 +233,14 @@ int64_t rb_items(const GemmSchedule& s, int64_t blocks, int64_t KB, int64_t slot
 }
 
 // Its cost in units of one item's time on a full SM (two CTAs of 8 warps):
-// the busiest warp's items, at half that time per item when no SM holds
-// two CTAs (the warps of one CTA alone share the SM's issue slots with
-// nobody), plus the cluster split's own cost (barriers, the distributed
-// shared-memory sum), measured on GB300 at about 1.3 items.
+// the busiest warp's items, at 0.65 of that time per item when no SM holds
+// two CTAs (the warps of one CTA share the SM's issue slots with nobody;
+// measured on GB300: 0.62), plus the cluster split's own cost (barriers,
+// the distributed shared-memory sum), measured at about 1.3 items a wave.
 double rb_cost(const GemmSchedule& s, int64_t blocks, int64_t KB, int64_t slots, int num_sms) {
-  const double load = s.grid <= num_sms ? 0.5 : 1.0;
-  return static_cast<double>(rb_items(s, blocks, KB, slots)) * load + (s.cluster > 1 ? 1.3 : 0.0);
+  const double load = s.grid <= num_sms ? 0.65 : 1.0;
+  const int64_t waves = s.cluster > 1 ? (blocks * s.cluster + slots - 1) / slots : 0;
+  return static_cast<double>(rb_items(s, blocks, KB, slots)) * load + 1.3 * static_cast<double>(waves);
 }
 
 GemmSchedule make_schedule(const Variant& v, int64_t M, int64_t N, int64_t K, int num_sms) {

@@ -1,19 +1,21 @@
-// W4A16 GEMV for M <= 4: a row-block CUDA-core kernel (sm_103a), bf16 or fp16
-// activations.
+// W4A16 GEMM for M <= 8: a row-block kernel with warp-level MMA (sm_103a),
+// bf16 or fp16 activations.
 //
 // "Kernel dispatch and Humming quantization in PhyAI", section "Humming makes
 // the separation useful": INT4 round-to-nearest weights, group 128 along K,
 // BF16 (or FP16) activations; the packed layout runs only through the kernels
-// that understand it.  At M <= 4 the GEMM does at most 8 flops per 0.52
+// that understand it.  At M <= 8 the GEMM does at most 16 flops per 0.52
 // bytes of codes and scales: it is bound by streaming the weight from HBM,
-// and the tensor-core path's fixed costs per 128 x 128 unit (the converted
-// operand's TMEM round trip, MMA issue, barrier hand-offs between roles)
-// are what limits it.  This kernel has no pipeline roles: every warp feeds
-// itself and converts its codes in registers.
+// and the tcgen05 path's fixed costs per 128 x 128 unit (the converted
+// operand's TMEM round trip, MMA issue and commit, barrier hand-offs between
+// roles) are what limits it there.  This kernel has no pipeline roles: every
+// warp feeds itself, converts its codes in registers and multiplies them
+// with synchronous warp MMAs (mma.sync m16n8k16, fp32 accumulators), whose
+// 8 columns take up to 8 activation rows at no extra cost.
 //
-// Work split.  An item is one row block (RB = 16 consecutive weight rows of
-// one 128-row storage tile) times one group of 128 codes along K: 1 KiB of
-// contiguous codes in the tiled storage, the 16 rows' scales, the group's
+// Work split.  An item is one row block (RB = 32 consecutive weight rows of
+// one 128-row storage tile) times one group of 128 codes along K: 2 KiB of
+// contiguous codes in the tiled storage, the 32 rows' scales, the group's
 // activations.  Persistent form: the grid is the resident CTAs (or fewer),
 // teams of WK warps (1, 2, 4, 8) take row blocks round-robin and split each
 // row block's K range into WK equal runs of groups; the host picks WK so
@@ -25,31 +27,31 @@
 // Streaming.  Each warp owns a ring of D shared-memory stages (one item
 // each) filled by non-tensor bulk copies (cp.async.bulk) that complete on a
 // per-stage mbarrier, so D items per warp are in flight without holding a
-// register: 16 warps x D KiB per SM cover the HBM latency.  With static
-// weights the first stages' codes and scales are requested before the wait
-// for the previous kernel (whose output may be A).  Waits are time-bounded:
-// a warp that gives up records the error, walks its remaining items without
-// waiting (so its team's barriers still match) and lets its copies in
-// flight land before it exits.
+// register.  With static weights the first stages' codes and scales are
+// requested before the wait for the previous kernel (whose output may be
+// A).  Waits are time-bounded: a warp that gives up records the error,
+// walks its remaining items without waiting (so its team's barriers still
+// match) and lets its copies in flight land before it exits.
 //
-// Arithmetic.  A lane owns a chunk of CH = 16 codes (8 bytes of a 64-byte
-// tile row) of RPL = 4 rows, r = lane / 8 + 4 j, and reads its activations
-// once per item for those rows.  One shift of a code word puts two
-// neighbouring nibbles at bits 12..15 and 16..19; one AND-XOR each places
-// them under the exponent of 2048 (bits 12..15) or 128 (bits 16..19) with
-// the nibble's sign bit flipped (n ^ 8 = q + 8), so a code of even k reads
-// 2056 + q and one of odd k reads 136 + q, exactly: twelve operations per
-// eight codes.  Products with a bf16 or fp16 activation are exact in fp32
-// (at most 12 + 11 significant bits), and per chunk
-//   sum_k q_k a_k = sum_k x_k a_k - 2056 sum_even a - 136 sum_odd a,
-// the two activation sums formed once per item and shared by the lane's
-// rows.  The item's partial times the fp32 scale goes to the row's total.
+// Arithmetic.  The row block is two 16-row MMA tiles (A: weight rows x k),
+// the activations are B (k x 8 columns, column m = activation row m).  A
+// lane (gq, tq) = (lane / 4, lane % 4) reads, of its rows gq and gq + 8, the
+// 32 codes k = 32 tq .. 32 tq + 31 with one 16-byte load per row.  One
+// shift and one AND-XOR turn nibbles s and s + 4 of a code word into two
+// 16-bit values x + q under the exponent whose unit is bit 0 (sign bit
+// flipped: n ^ 8 = q + 8), x = 136 for bf16 and 1032 for fp16, both exact;
+// each word gives the A fragments of two MMAs.  The MMA's k order within a
+// group is a permutation of the storage's; B takes the activations in the
+// same order (byte permutes of the 16-byte activation loads), so each
+// product is unchanged.  Products of x + q (at most 11 significant bits)
+// with an activation are exact in fp32.  An MMA of an all-ones A gives the
+// group's activation sums per column, and x times those is taken off before
+// the group's fp32 scale multiplies the partial into the row's total.
 //
-// Reduction.  Lanes of one row sum their totals by shuffles (fixed order);
-// a team's warps add theirs in k order through shared memory after a named
-// barrier; with a cluster the CTAs' sums are added in rank order; the bias
-// is added in fp32 and Y rounded once.  The result does not depend on
-// timing.
+// Reduction.  A team's warps add their totals in k order through shared
+// memory after a named barrier; with a cluster the CTAs' sums are added in
+// rank order; the bias is added in fp32 and Y rounded once.  The result
+// does not depend on timing.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -64,6 +66,8 @@ namespace w4a16 {
 namespace {
 
 constexpr int kRbWarps = kRbWarpsPerCta;
+constexpr int kRbRows = 32;       // rows per block: two 16-row MMA tiles
+constexpr int kRbCtasPerSm = 2;   // registers <= 128, shared memory <= 113 KB
 
 struct RbArgs {
   const uint16_t* A;       // [M, K] activation type
@@ -100,75 +104,28 @@ __device__ __forceinline__ uint16_t rb_out(float x) {
   }
 }
 
-// Activations of one chunk: CH values (CH / 2 words of two 16-bit values,
-// k even in the low half) to CH / 2 (even k, odd k) pairs.
-template <int CH, bool F16>
-__device__ __forceinline__ void rb_acts(const uint32_t (&w)[CH / 2], float2 (&a)[CH / 2]) {
-#pragma unroll
-  for (int i = 0; i < CH / 2; ++i) {
-    if constexpr (F16) {
-      a[i] = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
-    } else {
-      a[i] = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xFFFF0000u));
-    }
-  }
-}
-
-// A nibble at bits p..p+3 of v, as the float 2^(23-p) + (n ^ 8) = 2^(23-p)
-// + 8 + q: one AND-XOR puts it under the exponent whose unit is bit p, with
-// the sign bit of the two's-complement nibble flipped.
-template <int P>
-__device__ __forceinline__ float rb_nib(uint32_t v) {
-  constexpr uint32_t kMagic = (static_cast<uint32_t>(150 - P) << 23) | (8u << P);
-  return __uint_as_float(ptx::and_xor(v, 0xFu << P, kMagic));
-}
-template <int P>
-__device__ __forceinline__ constexpr float rb_off() {
-  return static_cast<float>((1u << (23 - P)) + 8u);
-}
-
-// The 8 codes of one word as exact (q_k, q_k+1) pairs, k even: nibbles 0..4
-// sit at bits 0, 4, 8, 12, 16 of w, nibbles 5..7 at bits 8, 12, 16 of w >>
-// 12 (one shift); one packed subtraction of the exponents' offsets per pair
-// is exact (x and its offset share a binade).
-__device__ __forceinline__ void rb_codes(uint32_t w, float2 (&q)[4]) {
-  const uint32_t v = w >> 12;
-  q[0] = __fadd2_rn(make_float2(rb_nib<0>(w), rb_nib<4>(w)), make_float2(-rb_off<0>(), -rb_off<4>()));
-  q[1] = __fadd2_rn(make_float2(rb_nib<8>(w), rb_nib<12>(w)), make_float2(-rb_off<8>(), -rb_off<12>()));
-  q[2] = __fadd2_rn(make_float2(rb_nib<16>(w), rb_nib<8>(v)), make_float2(-rb_off<16>(), -rb_off<8>()));
-  q[3] = __fadd2_rn(make_float2(rb_nib<12>(v), rb_nib<16>(v)), make_float2(-rb_off<12>(), -rb_off<16>()));
-}
-
-// MT: activation rows (M <= MT); CH: codes per lane chunk; RPL: rows per lane.
-template <int MT, int CH, int RPL>
+// MT: activation rows (M <= MT; the MMA's 8 columns).  One stage: the
+// item's codes, its rows' scales, MT activation rows of the group.
+template <int MT>
 struct RbCfg {
-  static constexpr int kLPR = kGroup / CH;           // lanes per row
-  static constexpr int kRowsPerPass = 32 / kLPR;     // rows one warp instruction covers
-  static constexpr int kRB = kRowsPerPass * RPL;     // rows per block
-  static constexpr int kWords = CH / 8;              // code words per lane-chunk
-  static_assert(kGroup % kRB == 0, "a row block sits inside one 128-row tile");
-  // one stage: the item's codes, its rows' scales, MT activation rows
-  static constexpr int kCodeBytes = kRB * 64;
+  static constexpr int kCodeBytes = kRbRows * 64;
   static constexpr int kScaleOff = kCodeBytes;
-  static constexpr int kActOff = kScaleOff + kRB * 2;
+  static constexpr int kActOff = kScaleOff + kRbRows * 2;
   static constexpr int kStage = kActOff + MT * kGroup * 2;
-  static constexpr int kDepth = MT <= 1 ? 5 : MT <= 2 ? 7 : 6;   // stages per warp
+  static constexpr int kDepth = MT <= 4 ? 3 : 2;   // stages per warp
   static constexpr int kBarOff = kRbWarps * kDepth * kStage;
   static constexpr int kSmem = kBarOff + kRbWarps * kDepth * 8;
   static_assert(kActOff % 16 == 0 && kStage % 16 == 0, "bulk-copy destinations 16-byte aligned");
+  static_assert(MT >= 1 && MT <= 8, "the MMA has 8 columns");
 };
-
-// Two CTAs of 8 warps per SM (registers <= 128, shared memory <= 113 KB each).
-constexpr int kRbCtasPerSm = 2;
 
 // Walks a warp's items for the copies: the row blocks of its team (rb = T,
 // T + TT, ...) and, in each, the warp's groups k0 .. k1 - 1, with the item's
 // copy sources and transaction bytes (stepped, not recomputed, inside a
 // row block).
-template <int RB, int MT>
 struct RbWalk {
   int rb, g;
-  const uint8_t* codes;      // RB x 64 bytes
+  const uint8_t* codes;      // kRbRows x 64 bytes
   const __half* scales;      // nv values
   const uint16_t* act;       // row 0's 128 values
   uint32_t scale_bytes, bytes;
@@ -177,14 +134,14 @@ struct RbWalk {
     rb = rb_;
     g = k0;
     if (rb >= a.NB) return;
-    const int r0 = rb * RB;
+    const int r0 = rb * kRbRows;
     const int tn = r0 / kTileW;
-    const int nv = a.N - r0 < RB ? a.N - r0 : RB;   // a multiple of 8
+    const int nv = a.N - r0 < kRbRows ? a.N - r0 : kRbRows;   // a multiple of 8
     codes = a.packed + ((static_cast<int64_t>(tn) * a.KB + k0) * kTileW + (r0 - tn * kTileW)) * 64;
     scales = a.scales + static_cast<int64_t>(k0) * a.N + r0;
     act = a.A + static_cast<int64_t>(k0) * kGroup;
     scale_bytes = 2u * static_cast<uint32_t>(nv);
-    bytes = RB * 64 + scale_bytes + static_cast<uint32_t>(a.M) * kGroup * 2;
+    bytes = kRbRows * 64 + scale_bytes + static_cast<uint32_t>(a.M) * kGroup * 2;
   }
   __device__ void next(const RbArgs& a, int k0, int k1, int TT) {
     if (++g == k1) {
@@ -203,24 +160,49 @@ __device__ __forceinline__ uint32_t lds_u16(uint32_t saddr) {
   return v;
 }
 
-template <int MT, int CH, int RPL, bool F16>
+// D += A B for one m16n8k16 tile (A row-major 16 x 16, B column-major 16 x
+// 8, fp32 accumulators), bf16 or fp16 operands.
+template <bool F16>
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  if constexpr (F16) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  }
+}
+
+// Nibbles s and s + 4 of a code word as two 16-bit values x + q (low half:
+// nibble s), x = 136 (bf16) or 1032 (fp16).
+template <bool F16>
+__device__ __forceinline__ uint32_t rb_pair16(uint32_t w, int s) {
+  return ptx::and_xor(w >> (4 * s), 0x000F000Fu, F16 ? 0x64086408u : 0x43084308u);
+}
+
+template <int MT, bool F16>
 __global__ void __launch_bounds__(kRbWarps * 32, kRbCtasPerSm)
     gemv_rb_kernel(const __grid_constant__ RbArgs g) {
-  using C = RbCfg<MT, CH, RPL>;
-  constexpr int W = C::kWords;
+  using C = RbCfg<MT>;
   constexpr int D = C::kDepth;
   extern __shared__ __align__(128) uint8_t smem[];
   // per warp, per row-block parity: its rows' totals (a team's flush)
-  __shared__ float tbuf[kRbWarps][2][C::kRB][MT];
-  __shared__ float csum[C::kRB][MT];   // cluster split: the CTA's totals
+  __shared__ float tbuf[kRbWarps][2][kRbRows][MT];
+  __shared__ float csum[kRbRows][MT];   // cluster split: the CTA's totals
   __shared__ int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gq = lane >> 2, tq = lane & 3;        // MMA fragment row group, column pair
   const int WK = g.team, S = g.cluster;
   const int tpc = kRbWarps / WK;                  // teams per CTA
   const int team = warp / WK, wt = warp - team * WK;
-  const int c = lane % C::kLPR;                   // the lane's chunk
-  const int rl = lane / C::kLPR;                  // the lane's first row in a block
 
   // the team's first row block and stride; with a cluster split the CTA is
   // one team on one row block and its rank takes a share of K
@@ -250,13 +232,12 @@ __global__ void __launch_bounds__(kRbWarps * 32, kRbCtasPerSm)
 
   // an item's copies, issued by lane 0: weights (codes and the valid rows'
   // scales) and activations (the M rows' 128 values)
-  using Walk = RbWalk<C::kRB, MT>;
-  auto issue_w = [&](const Walk& it, uint8_t* st, uint64_t* bar) {
+  auto issue_w = [&](const RbWalk& it, uint8_t* st, uint64_t* bar) {
     ptx::mbar_arrive_expect_tx(bar, it.bytes);
     ptx::bulk_g2s(st, it.codes, C::kCodeBytes, bar);
     ptx::bulk_g2s(st + C::kScaleOff, it.scales, it.scale_bytes, bar);
   };
-  auto issue_a = [&](const Walk& it, uint8_t* st, uint64_t* bar) {
+  auto issue_a = [&](const RbWalk& it, uint8_t* st, uint64_t* bar) {
     if constexpr (MT == 1) {
       ptx::bulk_g2s(st + C::kActOff, it.act, kGroup * 2, bar);
     } else {
@@ -267,13 +248,13 @@ __global__ void __launch_bounds__(kRbWarps * 32, kRbCtasPerSm)
 
   // (the launch guarantees KB >= team x cluster: no warp's range is empty)
   const int first = k1 > k0 ? T : g.NB;
-  Walk pre;
+  RbWalk pre;
   pre.start(g, first, k0);
   // the first D items; with static weights their codes and scales are
   // requested before the wait for the previous kernel
   int issued = 0;
   if (lane == 0 && g.static_w) {
-    Walk q = pre;
+    RbWalk q = pre;
     for (int s = 0; s < D && q.valid(g.NB); ++s, q.next(g, k0, k1, TT))
       issue_w(q, ring + s * C::kStage, &full[s]);
   }
@@ -286,94 +267,94 @@ __global__ void __launch_bounds__(kRbWarps * 32, kRbCtasPerSm)
     }
   }
 
-  float acc[RPL][MT];
-#pragma unroll
-  for (int j = 0; j < RPL; ++j)
-#pragma unroll
-    for (int m = 0; m < MT; ++m) acc[j][m] = 0.0f;
+  // the lane's totals of the block's two 16-row tiles: rows gq, gq + 8 of
+  // tile tau, columns (activation rows) 2 tq, 2 tq + 1
+  float acc[2][4] = {};
 
+  // One item.  Code word j of a row (k = 32 tq + 8 j ..) gives the A
+  // fragments of MMAs 2 j + h, h = 0, 1: fragment columns (2 tq, 2 tq + 1)
+  // <- k = 32 tq + 8 j + 2 h + (0, 4), columns (2 tq + 8, 2 tq + 9) <- + (1,
+  // 5); B's fragment rows take the same k from the activations.
   auto compute = [&](uint32_t st) {
-    uint32_t cw[RPL][W];
-    float sc[RPL];
+    constexpr uint32_t kOne = F16 ? 0x3C003C00u : 0x3F803F80u;
+    constexpr float kOff = F16 ? 1032.0f : 136.0f;
+    const int mrow = gq < MT ? gq : MT - 1;   // columns >= M are never stored
+    uint32_t u[16];
 #pragma unroll
-    for (int j = 0; j < RPL; ++j) {
-      const int r = rl + C::kRowsPerPass * j;
-      const uint2 v = ptx::lds64(st + r * 64 + c * (CH / 2));
-      cw[j][0] = v.x;
-      cw[j][1] = v.y;
-      sc[j] = __half2float(__ushort_as_half(static_cast<uint16_t>(lds_u16(st + C::kScaleOff + 2 * r))));
+    for (int i = 0; i < 4; ++i) {
+      const uint4 v = ptx::lds128(st + C::kActOff + mrow * kGroup * 2 + 64 * tq + 16 * i);
+      u[4 * i] = v.x;
+      u[4 * i + 1] = v.y;
+      u[4 * i + 2] = v.z;
+      u[4 * i + 3] = v.w;
     }
-    float2 a[MT][CH / 2];
+    uint32_t b[8][2];
 #pragma unroll
-    for (int m = 0; m < MT; ++m) {
-      uint32_t aw[CH / 2];
+    for (int j = 0; j < 4; ++j)
 #pragma unroll
-      for (int q = 0; q < CH / 8; ++q) {
-        // rows m >= M were not copied: their values are never stored
-        const uint4 v = ptx::lds128(st + C::kActOff + m * kGroup * 2 + c * CH * 2 + 16 * q);
-        aw[4 * q] = v.x;
-        aw[4 * q + 1] = v.y;
-        aw[4 * q + 2] = v.z;
-        aw[4 * q + 3] = v.w;
+      for (int h = 0; h < 2; ++h) {
+        b[2 * j + h][0] = ptx::prmt(u[4 * j + h], u[4 * j + h + 2], 0x5410u);
+        b[2 * j + h][1] = ptx::prmt(u[4 * j + h], u[4 * j + h + 2], 0x7632u);
       }
-      rb_acts<CH, F16>(aw, a[m]);
-    }
+    // the group's activation sums: column 2 tq in sum[0], 2 tq + 1 in sum[1]
+    float sum[4] = {};
 #pragma unroll
-    for (int j = 0; j < RPL; ++j) {
-      float2 p[MT];
+    for (int mu = 0; mu < 8; ++mu) mma16816<F16>(sum, kOne, kOne, kOne, kOne, b[mu][0], b[mu][1]);
 #pragma unroll
-      for (int m = 0; m < MT; ++m) p[m] = make_float2(0.0f, 0.0f);
+    for (int tau = 0; tau < 2; ++tau) {
+      const int r = 16 * tau + gq;
+      const uint4 w0 = ptx::lds128(st + r * 64 + 16 * tq);
+      const uint4 w1 = ptx::lds128(st + (r + 8) * 64 + 16 * tq);
+      const uint32_t W0[4] = {w0.x, w0.y, w0.z, w0.w};
+      const uint32_t W1[4] = {w1.x, w1.y, w1.z, w1.w};
+      float d[4] = {};
 #pragma unroll
-      for (int wi = 0; wi < W; ++wi) {
-        float2 q[4];
-        rb_codes(cw[j][wi], q);
+      for (int j = 0; j < 4; ++j)
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-          for (int m = 0; m < MT; ++m) p[m] = __ffma2_rn(q[i], a[m][4 * wi + i], p[m]);
-      }
-#pragma unroll
-      for (int m = 0; m < MT; ++m) acc[j][m] = fmaf(sc[j], p[m].x + p[m].y, acc[j][m]);
+        for (int h = 0; h < 2; ++h)
+          mma16816<F16>(d, rb_pair16<F16>(W0[j], 2 * h), rb_pair16<F16>(W1[j], 2 * h),
+                        rb_pair16<F16>(W0[j], 2 * h + 1), rb_pair16<F16>(W1[j], 2 * h + 1),
+                        b[2 * j + h][0], b[2 * j + h][1]);
+      const float s0 = __half2float(__ushort_as_half(static_cast<uint16_t>(lds_u16(st + C::kScaleOff + 2 * r))));
+      const float s1 =
+          __half2float(__ushort_as_half(static_cast<uint16_t>(lds_u16(st + C::kScaleOff + 2 * (r + 8)))));
+      acc[tau][0] = fmaf(s0, fmaf(-kOff, sum[0], d[0]), acc[tau][0]);
+      acc[tau][1] = fmaf(s0, fmaf(-kOff, sum[1], d[1]), acc[tau][1]);
+      acc[tau][2] = fmaf(s1, fmaf(-kOff, sum[0], d[2]), acc[tau][2]);
+      acc[tau][3] = fmaf(s1, fmaf(-kOff, sum[1], d[3]), acc[tau][3]);
     }
   };
 
-  // The row block's totals: the chunk lanes of a row in a fixed order, then
-  // the team's warps in k order; stored to Y (bias added in fp32, one
-  // rounding), or with a cluster split left in csum for the cluster sum.
+  // The row block's totals: with a team of one and no cluster straight to Y
+  // (bias added in fp32, one rounding); else through shared memory, the
+  // team's warps in k order, into Y or (cluster split) csum.
   int nflush = 0;
   auto flush = [&](int rb) {
-#pragma unroll
-    for (int j = 0; j < RPL; ++j)
-#pragma unroll
-      for (int m = 0; m < MT; ++m)
-#pragma unroll
-        for (int o = 1; o < C::kLPR; o <<= 1) acc[j][m] += __shfl_xor_sync(0xFFFFFFFFu, acc[j][m], o);
-    const int r0 = rb * C::kRB;
+    const int r0 = rb * kRbRows;
     if (WK == 1 && S == 1) {
-      if (c == 0) {
 #pragma unroll
-        for (int j = 0; j < RPL; ++j) {
-          const int n = r0 + rl + C::kRowsPerPass * j;
+      for (int tau = 0; tau < 2; ++tau)
 #pragma unroll
-          for (int m = 0; m < MT; ++m) {
-            if (n < g.N && m < g.M) {
-              float t = acc[j][m];
-              if (g.bias != nullptr) t += rb_act<F16>(g.bias[n]);
-              g.Y[static_cast<int64_t>(m) * g.N + n] = rb_out<F16>(t);
-            }
+        for (int e = 0; e < 4; ++e) {
+          const int n = r0 + 16 * tau + gq + (e >= 2 ? 8 : 0);
+          const int m = 2 * tq + (e & 1);
+          if (m < g.M && n < g.N) {
+            float t = acc[tau][e];
+            if (g.bias != nullptr) t += rb_act<F16>(g.bias[n]);
+            g.Y[static_cast<int64_t>(m) * g.N + n] = rb_out<F16>(t);
           }
         }
-      }
     } else {
-      if (c == 0) {
 #pragma unroll
-        for (int j = 0; j < RPL; ++j)
+      for (int tau = 0; tau < 2; ++tau)
 #pragma unroll
-          for (int m = 0; m < MT; ++m) tbuf[warp][nflush & 1][rl + C::kRowsPerPass * j][m] = acc[j][m];
-      }
+        for (int e = 0; e < 4; ++e) {
+          const int m = 2 * tq + (e & 1);
+          if (m < MT) tbuf[warp][nflush & 1][16 * tau + gq + (e >= 2 ? 8 : 0)][m] = acc[tau][e];
+        }
       ptx::named_barrier_sync(1 + team, WK * 32);
       if (wt == 0) {
-        for (int e = lane; e < C::kRB * MT; e += 32) {
+        for (int e = lane; e < kRbRows * MT; e += 32) {
           const int row = e / MT, m = e - row * MT;
           float t = 0.0f;
           for (int w = 0; w < WK; ++w) t += tbuf[team * WK + w][nflush & 1][row][m];
@@ -390,9 +371,9 @@ __global__ void __launch_bounds__(kRbWarps * 32, kRbCtasPerSm)
       }
     }
 #pragma unroll
-    for (int j = 0; j < RPL; ++j)
+    for (int tau = 0; tau < 2; ++tau)
 #pragma unroll
-      for (int m = 0; m < MT; ++m) acc[j][m] = 0.0f;
+      for (int e = 0; e < 4; ++e) acc[tau][e] = 0.0f;
     ++nflush;
   };
 
@@ -452,8 +433,8 @@ __global__ void __launch_bounds__(kRbWarps * 32, kRbCtasPerSm)
     // CTAs of the cluster in rank (k) order; rank q stores rows q, q + S, ...
     ptx::cluster_sync();
     const uint32_t base = ptx::smem_u32(&csum[0][0]);
-    const int r0 = T * C::kRB;
-    for (int e = threadIdx.x; e < C::kRB * MT; e += blockDim.x) {
+    const int r0 = T * kRbRows;
+    for (int e = threadIdx.x; e < kRbRows * MT; e += blockDim.x) {
       const int row = e / MT, m = e - row * MT;
       if (row % S != rank) continue;
       const int n = r0 + row;
@@ -467,10 +448,10 @@ __global__ void __launch_bounds__(kRbWarps * 32, kRbCtasPerSm)
   }
 }
 
-template <int MT, int CH, int RPL, bool F16>
+template <int MT, bool F16>
 cudaError_t launch_rb(const GemmProblem& p, const GemmSchedule& s, bool use_pdl, cudaStream_t stream) {
-  using C = RbCfg<MT, CH, RPL>;
-  const int64_t blocks = (p.N + C::kRB - 1) / C::kRB;
+  using C = RbCfg<MT>;
+  const int64_t blocks = (p.N + kRbRows - 1) / kRbRows;
   const int S = s.cluster > 1 ? s.cluster : 1;
   const int WK = s.team;
   const int64_t KB = p.K / kGroup;
@@ -495,7 +476,7 @@ cudaError_t launch_rb(const GemmProblem& p, const GemmSchedule& s, bool use_pdl,
   g.static_w = p.weights_static ? 1 : 0;
   g.err = p.error_word;
   g.timeout_ns = p.timeout_ns;
-  auto kernel = gemv_rb_kernel<MT, CH, RPL, F16>;
+  auto kernel = gemv_rb_kernel<MT, F16>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -533,7 +514,8 @@ cudaError_t launch_rb(const GemmProblem& p, const GemmSchedule& s, bool use_pdl,
 }  // namespace
 
 int gemv_rb_rows(int act_tile) {
-  return act_tile <= 1 ? RbCfg<1, 16, 8>::kRB : RbCfg<4, 16, 4>::kRB;
+  (void)act_tile;
+  return kRbRows;
 }
 
 int gemv_rb_ctas_per_sm(int act_tile) {
@@ -543,9 +525,10 @@ int gemv_rb_ctas_per_sm(int act_tile) {
 
 size_t gemv_rb_smem_bytes(int act_tile) {
   switch (act_tile) {
-    case 1: return RbCfg<1, 16, 8>::kSmem;
-    case 2: return RbCfg<2, 16, 4>::kSmem;
-    case 4: return RbCfg<4, 16, 4>::kSmem;
+    case 1: return RbCfg<1>::kSmem;
+    case 2: return RbCfg<2>::kSmem;
+    case 4: return RbCfg<4>::kSmem;
+    case 8: return RbCfg<8>::kSmem;
     default: return 0;
   }
 }
@@ -558,12 +541,10 @@ cudaError_t launch_gemv_rb(const GemmKernelConfig& c, const GemmGroup& grp, bool
   if (p.swiglu) return cudaErrorInvalidValue;   // the fused epilogue is the tcgen05 path's
   const bool f16 = p.act_f16;
   switch (c.act_tile) {
-    case 1: return f16 ? launch_rb<1, 16, 8, true>(p, s, use_pdl, stream)
-                       : launch_rb<1, 16, 8, false>(p, s, use_pdl, stream);
-    case 2: return f16 ? launch_rb<2, 16, 4, true>(p, s, use_pdl, stream)
-                       : launch_rb<2, 16, 4, false>(p, s, use_pdl, stream);
-    case 4: return f16 ? launch_rb<4, 16, 4, true>(p, s, use_pdl, stream)
-                       : launch_rb<4, 16, 4, false>(p, s, use_pdl, stream);
+    case 1: return f16 ? launch_rb<1, true>(p, s, use_pdl, stream) : launch_rb<1, false>(p, s, use_pdl, stream);
+    case 2: return f16 ? launch_rb<2, true>(p, s, use_pdl, stream) : launch_rb<2, false>(p, s, use_pdl, stream);
+    case 4: return f16 ? launch_rb<4, true>(p, s, use_pdl, stream) : launch_rb<4, false>(p, s, use_pdl, stream);
+    case 8: return f16 ? launch_rb<8, true>(p, s, use_pdl, stream) : launch_rb<8, false>(p, s, use_pdl, stream);
     default: return cudaErrorInvalidConfiguration;
   }
 }
