@@ -166,14 +166,12 @@ template <bool F16>
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
   if constexpr (F16) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
         "{%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
   } else {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
         "{%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
@@ -296,32 +294,47 @@ __global__ void __launch_bounds__(kRbWarps * 32, kRbCtasPerSm)
         b[2 * j + h][0] = ptx::prmt(u[4 * j + h], u[4 * j + h + 2], 0x5410u);
         b[2 * j + h][1] = ptx::prmt(u[4 * j + h], u[4 * j + h + 2], 0x7632u);
       }
-    // the group's activation sums: column 2 tq in sum[0], 2 tq + 1 in sum[1]
-    float sum[4] = {};
+    // the group's activation sums (column 2 tq in sum[0], 2 tq + 1 in
+    // sum[1]); the MMAs run as independent accumulation chains (two for the
+    // sums, one per tile and h), added at the end
+    float sa[4] = {}, sb[4] = {};
 #pragma unroll
-    for (int mu = 0; mu < 8; ++mu) mma16816<F16>(sum, kOne, kOne, kOne, kOne, b[mu][0], b[mu][1]);
+    for (int mu = 0; mu < 8; mu += 2) {
+      mma16816<F16>(sa, kOne, kOne, kOne, kOne, b[mu][0], b[mu][1]);
+      mma16816<F16>(sb, kOne, kOne, kOne, kOne, b[mu + 1][0], b[mu + 1][1]);
+    }
+    uint32_t W[2][2][4];   // [tile][row gq, gq + 8][word]
+#pragma unroll
+    for (int tau = 0; tau < 2; ++tau)
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const uint4 v = ptx::lds128(st + (16 * tau + 8 * half + gq) * 64 + 16 * tq);
+        W[tau][half][0] = v.x;
+        W[tau][half][1] = v.y;
+        W[tau][half][2] = v.z;
+        W[tau][half][3] = v.w;
+      }
+    float d[2][2][4] = {};   // [tile][h]
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int tau = 0; tau < 2; ++tau)
+          mma16816<F16>(d[tau][h], rb_pair16<F16>(W[tau][0][j], 2 * h), rb_pair16<F16>(W[tau][1][j], 2 * h),
+                        rb_pair16<F16>(W[tau][0][j], 2 * h + 1), rb_pair16<F16>(W[tau][1][j], 2 * h + 1),
+                        b[2 * j + h][0], b[2 * j + h][1]);
+    const float sum0 = sa[0] + sb[0], sum1 = sa[1] + sb[1];
 #pragma unroll
     for (int tau = 0; tau < 2; ++tau) {
       const int r = 16 * tau + gq;
-      const uint4 w0 = ptx::lds128(st + r * 64 + 16 * tq);
-      const uint4 w1 = ptx::lds128(st + (r + 8) * 64 + 16 * tq);
-      const uint32_t W0[4] = {w0.x, w0.y, w0.z, w0.w};
-      const uint32_t W1[4] = {w1.x, w1.y, w1.z, w1.w};
-      float d[4] = {};
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-          mma16816<F16>(d, rb_pair16<F16>(W0[j], 2 * h), rb_pair16<F16>(W1[j], 2 * h),
-                        rb_pair16<F16>(W0[j], 2 * h + 1), rb_pair16<F16>(W1[j], 2 * h + 1),
-                        b[2 * j + h][0], b[2 * j + h][1]);
       const float s0 = __half2float(__ushort_as_half(static_cast<uint16_t>(lds_u16(st + C::kScaleOff + 2 * r))));
       const float s1 =
           __half2float(__ushort_as_half(static_cast<uint16_t>(lds_u16(st + C::kScaleOff + 2 * (r + 8)))));
-      acc[tau][0] = fmaf(s0, fmaf(-kOff, sum[0], d[0]), acc[tau][0]);
-      acc[tau][1] = fmaf(s0, fmaf(-kOff, sum[1], d[1]), acc[tau][1]);
-      acc[tau][2] = fmaf(s1, fmaf(-kOff, sum[0], d[2]), acc[tau][2]);
-      acc[tau][3] = fmaf(s1, fmaf(-kOff, sum[1], d[3]), acc[tau][3]);
+      acc[tau][0] = fmaf(s0, fmaf(-kOff, sum0, d[tau][0][0] + d[tau][1][0]), acc[tau][0]);
+      acc[tau][1] = fmaf(s0, fmaf(-kOff, sum1, d[tau][0][1] + d[tau][1][1]), acc[tau][1]);
+      acc[tau][2] = fmaf(s1, fmaf(-kOff, sum0, d[tau][0][2] + d[tau][1][2]), acc[tau][2]);
+      acc[tau][3] = fmaf(s1, fmaf(-kOff, sum1, d[tau][0][3] + d[tau][1][3]), acc[tau][3]);
     }
   };
 
