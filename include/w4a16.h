@@ -200,10 +200,11 @@ int w4a16_gemm_f16(const void* A_f16, int64_t M, int64_t N, int64_t K, const voi
  *   Y[m, f] = bf16( silu(y[m, 2f + 1]) * y[m, 2f] ),  silu(g) = g / (1 + e^-g),
  * computed in fp32 (expf), one rounding.  Y is [M, N/2] bf16.  Shape limits,
  * packed layout, alignment and workspace rules are w4a16_gemm's; workspace
- * bytes from w4a16_gemm_swiglu_workspace_bytes.  The variant is the one
- * w4a16_select_variant gives unless that is a CUDA-core streaming variant
- * (simt_*), whose epilogue has no SwiGLU form: then the rule's best tcgen05
- * variant.  1 launch on `stream`.
+ * bytes from w4a16_gemm_swiglu_workspace_bytes.  The variant is the SwiGLU
+ * table's (w4a16_tune_swiglu), else the one w4a16_select_variant gives unless
+ * that is a streaming variant for M <= 8 (simt_*, rb_*) or a cluster split-K
+ * variant (*_csk), whose epilogues have no SwiGLU form: then the rule's best
+ * tcgen05 variant that has one.  1 launch on `stream`.
  */
 int w4a16_gemm_swiglu(const void* A_bf16, int64_t M, int64_t N, int64_t K, const void* packed,
                       const void* scales, int group, const void* bias_bf16_or_null, void* Y_bf16,
@@ -213,7 +214,8 @@ int w4a16_gemm_swiglu(const void* A_bf16, int64_t M, int64_t N, int64_t K, const
 size_t w4a16_gemm_swiglu_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
 /* w4a16_gemm_swiglu with an explicit variant; W4A16_ERR_UNSUPPORTED for a
- * CUDA-core streaming variant or a bad id, W4A16_ERR_NO_VARIANT if the
+ * streaming (simt_*, rb_*) or cluster split-K (*_csk) variant or a bad id,
+ * W4A16_ERR_NO_VARIANT if the
  * variant cannot run the shape.  Otherwise the same contract. */
 int w4a16_gemm_swiglu_variant(int variant, const void* A_bf16, int64_t M, int64_t N, int64_t K,
                               const void* packed, const void* scales, int group,
@@ -226,7 +228,12 @@ int w4a16_gemm_swiglu_variant(int variant, const void* A_bf16, int64_t M, int64_
  * is filled by measurement (w4a16_tune), in the spirit of the memoized,
  * autotuned kernel choice of "Kernel dispatch and Humming quantization in
  * PhyAI", section "Keep selection work out of repeated inference".  A shape
- * with no entry uses a fixed rule; both only ever choose GPU variants. */
+ * with no entry uses a fixed rule; both only ever choose GPU variants.
+ * Families: tc_* the tcgen05/TMEM GEMM (group or dequant mode, whole-tile,
+ * stream-K or cluster split-K (*_csk) schedules); rb_m1, rb_m2, rb_m4, rb_m8
+ * the row-block warp-MMA kernel for M <= 1, 2, 4, 8; simt_m*_sk the CUDA-core
+ * stream-K workers for M <= 1, 2, 4, 8.  The streaming and cluster split-K
+ * variants run single problems only and have no SwiGLU form. */
 
 /* Number of variants in the catalogue; ids are 0 .. count-1. */
 int w4a16_variant_count(void);
