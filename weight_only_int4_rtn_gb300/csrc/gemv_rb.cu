@@ -104,15 +104,21 @@ __device__ __forceinline__ uint16_t rb_out(float x) {
   }
 }
 
-// MT: activation rows (M <= MT; the MMA's 8 columns).  One stage: the
-// item's codes, its rows' scales, MT activation rows of the group.
+// MT: activation rows (M <= MT; the MMA's 8 columns).  An item holds up to
+// UG groups of one row block (2 for M <= 4; 1 for M = 8, whose activation
+// rows fill the shared memory).  One stage: the item's codes (2 KiB per
+// group), its rows' scales (64 B per group), MT activation rows of the
+// item's groups (contiguous in A: 256 B per group).
 template <int MT>
 struct RbCfg {
-  static constexpr int kCodeBytes = kRbRows * 64;
-  static constexpr int kScaleOff = kCodeBytes;
-  static constexpr int kActOff = kScaleOff + kRbRows * 2;
-  static constexpr int kStage = kActOff + MT * kGroup * 2;
-  static constexpr int kDepth = MT <= 4 ? 3 : 2;   // stages per warp
+  static constexpr int kUG = MT <= 4 ? 2 : 1;
+  static constexpr int kCodeBytes = kRbRows * 64;                 // one group
+  static constexpr int kScaleOff = kUG * kCodeBytes;
+  static constexpr int kScaleBytes = kRbRows * 2;                 // one group
+  static constexpr int kActOff = kScaleOff + kUG * kScaleBytes;
+  static constexpr int kActRow = kUG * kGroup * 2;                // one activation row
+  static constexpr int kStage = kActOff + MT * kActRow;
+  static constexpr int kDepth = 2;                                // stages per warp
   static constexpr int kBarOff = kRbWarps * kDepth * kStage;
   static constexpr int kSmem = kBarOff + kRbWarps * kDepth * 8;
   static_assert(kActOff % 16 == 0 && kStage % 16 == 0, "bulk-copy destinations 16-byte aligned");
@@ -120,19 +126,24 @@ struct RbCfg {
 };
 
 // Walks a warp's items for the copies: the row blocks of its team (rb = T,
-// T + TT, ...) and, in each, the warp's groups k0 .. k1 - 1, with the item's
-// copy sources and transaction bytes (stepped, not recomputed, inside a
-// row block).
+// T + TT, ...) and, in each, the warp's groups k0 .. k1 - 1 in items of up
+// to UG groups, with the item's copy sources and transaction bytes
+// (stepped, not recomputed, inside a row block).
+template <int UG>
 struct RbWalk {
-  int rb, g;
-  const uint8_t* codes;      // kRbRows x 64 bytes
-  const __half* scales;      // nv values
-  const uint16_t* act;       // row 0's 128 values
-  uint32_t scale_bytes, bytes;
+  int rb, g, ng;             // row block, first group, groups in the item
+  const uint8_t* codes;      // the first group's kRbRows x 64 bytes
+  const __half* scales;      // the first group's nv values
+  const uint16_t* act;       // row 0's values of the item's groups
+  uint32_t scale_bytes;      // one group's
   __device__ bool valid(int NB) const { return rb < NB; }
-  __device__ void start(const RbArgs& a, int rb_, int k0) {
+  __device__ uint32_t bytes(int M) const {
+    return static_cast<uint32_t>(ng) * (kRbRows * 64 + scale_bytes + static_cast<uint32_t>(M) * kGroup * 2);
+  }
+  __device__ void start(const RbArgs& a, int rb_, int k0, int k1) {
     rb = rb_;
     g = k0;
+    ng = k1 - k0 < UG ? k1 - k0 : UG;
     if (rb >= a.NB) return;
     const int r0 = rb * kRbRows;
     const int tn = r0 / kTileW;
@@ -141,15 +152,16 @@ struct RbWalk {
     scales = a.scales + static_cast<int64_t>(k0) * a.N + r0;
     act = a.A + static_cast<int64_t>(k0) * kGroup;
     scale_bytes = 2u * static_cast<uint32_t>(nv);
-    bytes = kRbRows * 64 + scale_bytes + static_cast<uint32_t>(a.M) * kGroup * 2;
   }
   __device__ void next(const RbArgs& a, int k0, int k1, int TT) {
-    if (++g == k1) {
-      start(a, rb + TT, k0);
+    g += ng;
+    if (g >= k1) {
+      start(a, rb + TT, k0, k1);
     } else {
-      codes += kTileW * 64;
-      scales += a.N;
-      act += kGroup;
+      codes += static_cast<int64_t>(ng) * kTileW * 64;
+      scales += static_cast<int64_t>(ng) * a.N;
+      act += ng * kGroup;
+      ng = k1 - g < UG ? k1 - g : UG;
     }
   }
 };
@@ -228,31 +240,39 @@ __global__ void __launch_bounds__(kRbWarps * 32, kRbCtasPerSm)
   __syncthreads();
   const WaitCtx wc{g.err, g.timeout_ns, &abort_flag};
 
-  // an item's copies, issued by lane 0: weights (codes and the valid rows'
-  // scales) and activations (the M rows' 128 values)
-  auto issue_w = [&](const RbWalk& it, uint8_t* st, uint64_t* bar) {
-    ptx::mbar_arrive_expect_tx(bar, it.bytes);
-    ptx::bulk_g2s(st, it.codes, C::kCodeBytes, bar);
-    ptx::bulk_g2s(st + C::kScaleOff, it.scales, it.scale_bytes, bar);
+  // an item's copies, issued by lane 0: weights (each group's codes and the
+  // valid rows' scales) and activations (each of the M rows' values of the
+  // item's groups, one contiguous run)
+  constexpr int UG = C::kUG;
+  using Walk = RbWalk<UG>;
+  auto issue_w = [&](const Walk& it, uint8_t* st, uint64_t* bar) {
+    ptx::mbar_arrive_expect_tx(bar, it.bytes(g.M));
+    for (int gi = 0; gi < it.ng; ++gi) {
+      ptx::bulk_g2s(st + gi * C::kCodeBytes, it.codes + static_cast<int64_t>(gi) * kTileW * 64, C::kCodeBytes,
+                    bar);
+      ptx::bulk_g2s(st + C::kScaleOff + gi * C::kScaleBytes, it.scales + static_cast<int64_t>(gi) * g.N,
+                    it.scale_bytes, bar);
+    }
   };
-  auto issue_a = [&](const RbWalk& it, uint8_t* st, uint64_t* bar) {
+  auto issue_a = [&](const Walk& it, uint8_t* st, uint64_t* bar) {
+    const uint32_t bytes = static_cast<uint32_t>(it.ng) * kGroup * 2;
     if constexpr (MT == 1) {
-      ptx::bulk_g2s(st + C::kActOff, it.act, kGroup * 2, bar);
+      ptx::bulk_g2s(st + C::kActOff, it.act, bytes, bar);
     } else {
       for (int m = 0; m < g.M; ++m)
-        ptx::bulk_g2s(st + C::kActOff + m * kGroup * 2, it.act + static_cast<int64_t>(m) * g.K, kGroup * 2, bar);
+        ptx::bulk_g2s(st + C::kActOff + m * C::kActRow, it.act + static_cast<int64_t>(m) * g.K, bytes, bar);
     }
   };
 
   // (the launch guarantees KB >= team x cluster: no warp's range is empty)
   const int first = k1 > k0 ? T : g.NB;
-  RbWalk pre;
-  pre.start(g, first, k0);
+  Walk pre;
+  pre.start(g, first, k0, k1);
   // the first D items; with static weights their codes and scales are
   // requested before the wait for the previous kernel
   int issued = 0;
   if (lane == 0 && g.static_w) {
-    RbWalk q = pre;
+    Walk q = pre;
     for (int s = 0; s < D && q.valid(g.NB); ++s, q.next(g, k0, k1, TT))
       issue_w(q, ring + s * C::kStage, &full[s]);
   }
@@ -273,14 +293,14 @@ __global__ void __launch_bounds__(kRbWarps * 32, kRbCtasPerSm)
   // fragments of MMAs 2 j + h, h = 0, 1: fragment columns (2 tq, 2 tq + 1)
   // <- k = 32 tq + 8 j + 2 h + (0, 4), columns (2 tq + 8, 2 tq + 9) <- + (1,
   // 5); B's fragment rows take the same k from the activations.
-  auto compute = [&](uint32_t st) {
+  auto compute_group = [&](uint32_t st, int gi) {
     constexpr uint32_t kOne = F16 ? 0x3C003C00u : 0x3F803F80u;
     constexpr float kOff = F16 ? 1032.0f : 136.0f;
     const int mrow = gq < MT ? gq : MT - 1;   // columns >= M are never stored
     uint32_t u[16];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const uint4 v = ptx::lds128(st + C::kActOff + mrow * kGroup * 2 + 64 * tq + 16 * i);
+      const uint4 v = ptx::lds128(st + C::kActOff + mrow * C::kActRow + gi * kGroup * 2 + 64 * tq + 16 * i);
       u[4 * i] = v.x;
       u[4 * i + 1] = v.y;
       u[4 * i + 2] = v.z;
@@ -308,7 +328,7 @@ __global__ void __launch_bounds__(kRbWarps * 32, kRbCtasPerSm)
     for (int tau = 0; tau < 2; ++tau)
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
-        const uint4 v = ptx::lds128(st + (16 * tau + 8 * half + gq) * 64 + 16 * tq);
+        const uint4 v = ptx::lds128(st + gi * C::kCodeBytes + (16 * tau + 8 * half + gq) * 64 + 16 * tq);
         W[tau][half][0] = v.x;
         W[tau][half][1] = v.y;
         W[tau][half][2] = v.z;
@@ -328,9 +348,9 @@ __global__ void __launch_bounds__(kRbWarps * 32, kRbCtasPerSm)
 #pragma unroll
     for (int tau = 0; tau < 2; ++tau) {
       const int r = 16 * tau + gq;
-      const float s0 = __half2float(__ushort_as_half(static_cast<uint16_t>(lds_u16(st + C::kScaleOff + 2 * r))));
+      const float s0 = __half2float(__ushort_as_half(static_cast<uint16_t>(lds_u16(st + C::kScaleOff + gi * C::kScaleBytes + 2 * r))));
       const float s1 =
-          __half2float(__ushort_as_half(static_cast<uint16_t>(lds_u16(st + C::kScaleOff + 2 * (r + 8)))));
+          __half2float(__ushort_as_half(static_cast<uint16_t>(lds_u16(st + C::kScaleOff + gi * C::kScaleBytes + 2 * (r + 8)))));
       acc[tau][0] = fmaf(s0, fmaf(-kOff, sum0, d[tau][0][0] + d[tau][1][0]), acc[tau][0]);
       acc[tau][1] = fmaf(s0, fmaf(-kOff, sum1, d[tau][0][1] + d[tau][1][1]), acc[tau][1]);
       acc[tau][2] = fmaf(s1, fmaf(-kOff, sum0, d[tau][0][2] + d[tau][1][2]), acc[tau][2]);
@@ -397,7 +417,8 @@ __global__ void __launch_bounds__(kRbWarps * 32, kRbCtasPerSm)
   int waited = 0;   // items whose copies have landed
   const uint32_t ring_u32 = ptx::smem_u32(ring);
   uint32_t st = ring_u32;
-  const int per_block = k1 - k0;
+  const int per_block = (k1 - k0 + UG - 1) / UG;   // items per row block
+  const int last_ng = k1 - k0 - (per_block - 1) * UG;  // groups in a row block's last item
   int left = per_block;   // items left in the current row block
 #pragma unroll 1
   for (int rb = first; rb < g.NB;) {
@@ -407,7 +428,8 @@ __global__ void __launch_bounds__(kRbWarps * 32, kRbCtasPerSm)
       else
         ok = false;
     }
-    compute(st);
+    compute_group(st, 0);
+    if (UG > 1 && (left > 1 || last_ng > 1)) compute_group(st, 1);
     if (ok && pre.valid(g.NB)) {
       // the lanes' reads of the stage have returned (their values are
       // consumed above): the copy may overwrite it
