@@ -250,6 +250,17 @@ size_t w4a16_variant_workspace_bytes(int variant, int64_t M, int64_t N, int64_t 
 /* The variant w4a16_gemm uses for this shape (table entry, else the rule). */
 int w4a16_select_variant(int64_t M, int64_t N, int64_t K);
 
+/* The launch the library would make for `variant` on this shape, on a GPU
+ * of num_sms SMs (0: the current device's, or 152 when there is none).
+ * Host-only (no launch, no device memory).  out[5] (caller-owned):
+ *   out[0] grid (CTAs), out[1] whole tiles run data-parallel, out[2]
+ *   stream-K (tile, unit) pairs, out[3] cluster size (CTAs of one thread-
+ *   block cluster sharing a tile's or a row block's K range; 0 or 1: none),
+ *   out[4] warps per team of the row-block kernel (rb_*; 0 otherwise).
+ * W4A16_ERR_INVALID_ARG for a null out or a negative num_sms,
+ * W4A16_ERR_NO_VARIANT if the variant cannot run the shape. */
+int w4a16_variant_schedule(int variant, int64_t M, int64_t N, int64_t K, int num_sms, int* out);
+
 /* w4a16_gemm with an explicit variant (tests, tuning).  Same contract. */
 int w4a16_gemm_variant(int variant, const void* A_bf16, int64_t M, int64_t N, int64_t K,
                        const void* packed, const void* scales, int group,

@@ -293,3 +293,35 @@ def test_grouped_epilogue_argument_errors(built_lib):
     assert L.w4a16_gemm_grouped(P, 2, 128, 0, -1, None, 0, None) == w4.W4A16_ERR_UNSUPPORTED
     P[1] = w4.GemmProblem(16, 16, 16, None, 16, 4, 256, 512, 1)
     assert L.w4a16_gemm_grouped(P, 2, 128, 1, -1, None, 0, None) == w4.W4A16_ERR_UNSUPPORTED  # fp16
+
+
+def test_row_block_schedule_forms(built_lib):
+    """The row-block kernel's launch form chosen by the host cost model (on a
+    152-SM GB300): the busiest SM's group-items at 16 per unit of time with
+    two busy CTAs and 8 / 0.65 with one, the cluster split at 1.3 items a
+    wave.  Each team size and the cluster form is the choice for some
+    shape."""
+    rb1 = w4.variant_id("rb_m1")
+    sched = lambda N, K: w4.w4a16_variant_schedule(rb1, 1, N, K, 152)
+    # K/128 groups bound the team: one group (team 1) up to eight (team 8)
+    assert sched(4096, 128)["team"] == 1 and sched(4096, 128)["grid"] == 16
+    assert sched(4096, 256)["team"] == 2 and sched(4096, 256)["grid"] == 32
+    assert sched(4096, 512)["team"] == 4 and sched(4096, 512)["grid"] == 64
+    assert sched(4096, 1024) == dict(grid=128, dp_tiles=0, sk_units=0, cluster=1, team=8)
+    # the metric's sweep shapes: the measured-best forms
+    assert sched(8192, 8192) == dict(grid=256, dp_tiles=0, sk_units=0, cluster=1, team=8)
+    assert sched(16384, 2048) == dict(grid=256, dp_tiles=0, sk_units=0, cluster=1, team=4)
+    assert sched(4096, 4096) == dict(grid=128, dp_tiles=0, sk_units=0, cluster=1, team=8)
+    assert w4.w4a16_variant_workspace_bytes(rb1, 1, 8192, 8192) == 0
+    # few row blocks, long K: a cluster K split (grid = row blocks x cluster)
+    assert sched(2048, 16384) == dict(grid=256, dp_tiles=0, sk_units=0, cluster=4, team=8)
+    assert sched(256, 4096) == dict(grid=32, dp_tiles=0, sk_units=0, cluster=4, team=8)
+    assert sched(256, 16384) == dict(grid=64, dp_tiles=0, sk_units=0, cluster=8, team=8)
+    # a tcgen05 variant reports no team; argument errors
+    tc = w4.variant_id("tc_a16_grp_sk")
+    assert w4.w4a16_variant_schedule(tc, 16, 8192, 8192, 152)["team"] == 0
+    out = (ctypes.c_int * 5)()
+    L = w4.lib()
+    assert L.w4a16_variant_schedule(rb1, 2, 4096, 1024, 152, out) == w4.W4A16_ERR_NO_VARIANT
+    assert L.w4a16_variant_schedule(rb1, 1, 4096, 1024, -1, out) == w4.W4A16_ERR_INVALID_ARG
+    assert L.w4a16_variant_schedule(rb1, 1, 4096, 1024, 152, None) == w4.W4A16_ERR_INVALID_ARG

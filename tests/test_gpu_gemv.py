@@ -163,3 +163,35 @@ def test_simt_graph_capture(w4):
     torch.cuda.synchronize()
     assert torch.equal(Y.view(torch.int16), y_e.view(torch.int16))
     assert w4.w4a16_get_device_error() == w4.W4A16_OK
+
+
+# shapes whose row-block launch takes each form (team of 1, 2, 4 or 8 warps;
+# cluster K split), the last row block ragged (N = 32 k + 8)
+FORM_SHAPES = [(4104, 128), (4104, 256), (4104, 512), (4104, 1024), (264, 4096), (264, 16384),
+               (16392, 2048)]
+
+
+@pytest.mark.parametrize("M,variant", [(1, "rb_m1"), (3, "rb_m4"), (8, "rb_m8")])
+def test_row_block_every_form(w4, M, variant):
+    """Every launch form of the row-block kernel against the oracle: the
+    forms are the host's choice for these shapes on this GPU, and together
+    they cover teams of 1, 2, 4, 8 warps and the cluster split,
+    bit-identical across repeats."""
+    v = w4.variant_id(variant)
+    forms = set()
+    for i, (N, K) in enumerate(FORM_SHAPES):
+        sch = w4.w4a16_variant_schedule(v, M, N, K)
+        forms.add("cluster" if sch["cluster"] > 1 else "team%d" % sch["team"])
+        assert w4.w4a16_variant_workspace_bytes(v, M, N, K) == 0
+        case = synthetic.Case(f"form_m{M}_{N}x{K}", M, N, K, 70 + i, bias=(i % 2 == 0))
+        W, A, b = synthetic.draw(case)
+        packed, scales = w4.w4a16_quantize(W.cuda())
+        y_ref = reference(A, packed, scales, b)
+        bd = None if b is None else b.cuda()
+        Y = w4.w4a16_gemm(A.cuda(), packed, scales, bias=bd, variant=v)
+        Y2 = w4.w4a16_gemm(A.cuda(), packed, scales, bias=bd, variant=v)
+        torch.cuda.synchronize()
+        assert w4.w4a16_get_device_error() == w4.W4A16_OK
+        check_gemm_close(Y, y_ref, what=f"{variant} {N}x{K} {sch}")
+        assert torch.equal(Y.view(torch.int16), Y2.view(torch.int16))
+    assert forms == {"team1", "team2", "team4", "team8", "cluster"}, forms

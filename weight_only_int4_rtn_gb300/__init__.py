@@ -107,6 +107,8 @@ SIGNATURES = [
     ("w4a16_variant_eligible", ctypes.c_int, [ctypes.c_int, _c_int64, _c_int64, _c_int64]),
     ("w4a16_variant_workspace_bytes", _c_size, [ctypes.c_int, _c_int64, _c_int64, _c_int64]),
     ("w4a16_select_variant", ctypes.c_int, [_c_int64, _c_int64, _c_int64]),
+    ("w4a16_variant_schedule", ctypes.c_int,
+     [ctypes.c_int, _c_int64, _c_int64, _c_int64, ctypes.c_int, ctypes.POINTER(ctypes.c_int)]),
     ("w4a16_gemm_variant", ctypes.c_int,
      [ctypes.c_int, _vp, _c_int64, _c_int64, _c_int64, _vp, _vp, ctypes.c_int, _vp, _vp, _vp,
       _c_size, _vp]),
@@ -754,6 +756,14 @@ def w4a16_variant_workspace_bytes(variant: int, M: int, N: int, K: int) -> int:
 
 def w4a16_select_variant(M: int, N: int, K: int) -> int:
     return lib().w4a16_select_variant(M, N, K)
+
+
+def w4a16_variant_schedule(variant: int, M: int, N: int, K: int, num_sms: int = 0) -> dict:
+    """The launch the library would make for `variant` on this shape (host
+    only): grid, dp_tiles, sk_units, cluster, team (row-block kernel)."""
+    out = (ctypes.c_int * 5)()
+    _check(lib().w4a16_variant_schedule(variant, M, N, K, num_sms, out), "w4a16_variant_schedule")
+    return dict(grid=out[0], dp_tiles=out[1], sk_units=out[2], cluster=out[3], team=out[4])
 
 
 def variant_id(name: str) -> int:

@@ -219,28 +219,41 @@ bool shape_ok(int64_t M, int64_t N, int64_t K) {
          N * K < (1ll << 40);
 }
 
-// Row-block kernel: the largest number of (row block, group) items one warp
-// runs under schedule s (persistent teams, or cluster waves over `slots`
-// resident CTAs).
-int64_t rb_items(const GemmSchedule& s, int64_t blocks, int64_t KB, int64_t slots) {
+// Row-block kernel: the cost of schedule s in units of one group-item's time
+// on a full SM (two CTAs of 8 warps), fitted to GB300 measurements.
+// Persistent form: CTA c runs on SM c mod num_sms; an SM with two busy CTAs
+// works through 16 group-items per unit of time, one with a single busy CTA
+// through 8 / 0.65 (measured: 8 / 0.62); the cost is the busiest SM's.
+// Cluster form: waves of the resident CTAs, each wave's warps running their
+// share of a row block's K range, plus the cluster's own cost (barriers, the
+// distributed shared-memory sum), about 1.3 items a wave.
+double rb_cost(const GemmSchedule& s, int64_t blocks, int64_t KB, int64_t slots, int num_sms) {
   if (s.cluster > 1) {
     const int64_t waves = (blocks * s.cluster + slots - 1) / slots;
     const int64_t per = static_cast<int64_t>(s.cluster) * kRbWarpsPerCta;
-    return waves * ((KB + per - 1) / per);
+    const double load = s.grid <= num_sms ? 0.65 : 1.0;
+    return static_cast<double>(waves * ((KB + per - 1) / per)) * load + 1.3 * static_cast<double>(waves);
   }
-  const int64_t teams = static_cast<int64_t>(s.grid) * (kRbWarpsPerCta / s.team);
-  return (blocks + teams - 1) / teams * ((KB + s.team - 1) / s.team);
-}
-
-// Its cost in units of one item's time on a full SM (two CTAs of 8 warps):
-// the busiest warp's items, at 0.65 of that time per item when no SM holds
-// two CTAs (the warps of one CTA share the SM's issue slots with nobody;
-// measured on GB300: 0.62), plus the cluster split's own cost (barriers,
-// the distributed shared-memory sum), measured at about 1.3 items a wave.
-double rb_cost(const GemmSchedule& s, int64_t blocks, int64_t KB, int64_t slots, int num_sms) {
-  const double load = s.grid <= num_sms ? 0.65 : 1.0;
-  const int64_t waves = s.cluster > 1 ? (blocks * s.cluster + slots - 1) / slots : 0;
-  return static_cast<double>(rb_items(s, blocks, KB, slots)) * load + 1.3 * static_cast<double>(waves);
+  const double thr1 = kRbWarpsPerCta / 0.65, thr2 = 2.0 * kRbWarpsPerCta;
+  std::vector<double> load(static_cast<size_t>(num_sms), 0.0);
+  std::vector<int> busy(static_cast<size_t>(num_sms), 0);
+  const int tpc = kRbWarpsPerCta / s.team;
+  const int64_t TT = static_cast<int64_t>(s.grid) * tpc;
+  for (int c = 0; c < s.grid; ++c) {
+    bool any = false;
+    for (int j = 0; j < tpc; ++j) {
+      const int64_t t = static_cast<int64_t>(c) * tpc + j;
+      if (t >= blocks) break;
+      load[static_cast<size_t>(c % num_sms)] += static_cast<double>(((blocks - 1 - t) / TT + 1) * KB);
+      any = true;
+    }
+    if (any) ++busy[static_cast<size_t>(c % num_sms)];
+  }
+  double worst = 0.0;
+  for (int i = 0; i < num_sms; ++i)
+    if (busy[static_cast<size_t>(i)] > 0)
+      worst = std::max(worst, load[static_cast<size_t>(i)] / (busy[static_cast<size_t>(i)] >= 2 ? thr2 : thr1));
+  return worst;
 }
 
 GemmSchedule make_schedule(const Variant& v, int64_t M, int64_t N, int64_t K, int num_sms) {
@@ -249,9 +262,9 @@ GemmSchedule make_schedule(const Variant& v, int64_t M, int64_t N, int64_t K, in
     // Items are (row block, group) pairs.  Persistent: the resident CTAs
     // (fewer when there are fewer teams' worth of row blocks), teams of WK
     // warps, row blocks dealt round-robin to the teams.  Cluster split: one
-    // CTA-wide team per row block and cluster rank, in waves of the
-    // resident CTAs.  The smallest cost (rb_cost) wins; ties go to the
-    // persistent form, then to smaller teams.
+    // CTA-wide team per row block and cluster rank, in waves of the resident
+    // CTAs.  The smallest cost (rb_cost) wins; ties go to the persistent
+    // form, then to smaller teams.
     const int64_t blocks = (N + gemv_rb_rows(v.cfg.act_tile) - 1) / gemv_rb_rows(v.cfg.act_tile);
     const int64_t KB = K / kGroup;
     const int64_t slots = static_cast<int64_t>(num_sms) * gemv_rb_ctas_per_sm(v.cfg.act_tile);
@@ -280,8 +293,6 @@ GemmSchedule make_schedule(const Variant& v, int64_t M, int64_t N, int64_t K, in
         s = c;
       }
     }
-    s.dp_tiles = 0;
-    s.sk_units = 0;
     return s;
   }
   if (v.cfg.simt) {
@@ -1261,6 +1272,20 @@ size_t w4a16_variant_workspace_bytes(int variant, int64_t M, int64_t N, int64_t 
 }
 
 int w4a16_select_variant(int64_t M, int64_t N, int64_t K) { return select_variant(M, N, K); }
+
+int w4a16_variant_schedule(int variant, int64_t M, int64_t N, int64_t K, int num_sms, int* out) {
+  if (out == nullptr || num_sms < 0) return W4A16_ERR_INVALID_ARG;
+  if (!variant_eligible(variant, M, N, K)) return W4A16_ERR_NO_VARIANT;
+  const int sms = std::min(num_sms > 0 ? num_sms : current_sms(), kMaxGrid);
+  const Variant& v = kVariants[variant];
+  const GemmSchedule s = make_schedule(v, M, N, K, sms);
+  out[0] = s.grid;
+  out[1] = s.dp_tiles;
+  out[2] = static_cast<int>(std::min<int64_t>(s.sk_units, 0x7FFFFFFF));
+  out[3] = s.cluster;
+  out[4] = v.cfg.rb ? s.team : 0;
+  return W4A16_OK;
+}
 
 }  // extern "C"
 
