@@ -24,7 +24,7 @@ exceed 3x the L2 size, so each step streams its inputs from HBM.  SM clocks
 and throttle reasons are sampled during the timed region (NVML, read only).
 The e2e figure is the same steps through the public API with the
 activations copied in from pinned host memory and the outputs copied back,
-every step.
+every step, pipelined over copy-in, compute and copy-out streams.
 
 --impl reference times the CPU oracle (test infrastructure, never the
 product path) on a bounded sample of the same workload, in the same unit.
@@ -638,34 +638,63 @@ def run_gpu(args, rank, world):
             q_us.append(time_graph_us(dev, gq, qreps))
     del gq
 
-    # --- e2e: the public API on host buffers: pinned activations copied in,
-    # the step's GEMMs on the resident weights, the outputs copied back
+    # --- e2e: the public API on host buffers, every step: the step's
+    # activations copied in from pinned host memory, its GEMMs on the
+    # resident weights, its outputs copied back to pinned host memory.  The
+    # steps are pipelined over three streams (copy in, compute, copy out)
+    # with two device buffers for A and Y: step i's copies overlap the GEMMs
+    # of steps i - 1 and i + 1, and a buffer is reused only after the copy
+    # that last read it has finished.  The timed region runs from the first
+    # copy in to the last copy out.
     a_host = [A.pin_memory() for (_, A, _) in host]
     y_host = [torch.empty(c.M, c.N // 2 if e else c.N, dtype=fx.act_dtype).pin_memory()
               for c, e in zip(cases, epilogues)]
     h2d = sum(a.numel() * a.element_size() for a in a_host)
     d2h = sum(y.numel() * y.element_size() for y in y_host)
-    s0 = sets[0]
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    bufs = [[dict(A=torch.empty_like(s["A"]), Y=torch.empty_like(s["Y"])) for s in sets[0]] for _ in range(2)]
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_gemm = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
 
-    def e2e_step():
-        for j in range(len(cases)):
-            s0[j]["A"].copy_(a_host[j], non_blocking=True)
-        step(0, stream)
-        for j in range(len(cases)):
-            y_host[j].copy_(s0[j]["Y"], non_blocking=True)
+    def e2e_step(i):
+        b = i % 2
+        wset = sets[i % copies]
+        s_in.wait_event(ev_gemm[b])              # A[b]'s last GEMM is done
+        with torch.cuda.stream(s_in):
+            for j in range(len(cases)):
+                bufs[b][j]["A"].copy_(a_host[j], non_blocking=True)
+        ev_in[b].record(s_in)
+        stream.wait_event(ev_in[b])
+        stream.wait_event(ev_out[b])              # Y[b]'s last copy out is done
+        if args.grouped:
+            w4.w4a16_gemm_grouped([x["A"] for x in bufs[b]], [s["wt"]["packed"] for s in wset],
+                                  [s["wt"]["scales"] for s in wset], Ys=[x["Y"] for x in bufs[b]],
+                                  workspace=ws, stream=stream, epilogues=epilogues)
+        else:
+            for j, s in enumerate(wset):
+                fx.gemm(bufs[b][j]["A"], s["wt"], bufs[b][j]["Y"], ws, stream)
+        ev_gemm[b].record(stream)
+        s_out.wait_event(ev_gemm[b])
+        with torch.cuda.stream(s_out):
+            for j in range(len(cases)):
+                y_host[j].copy_(bufs[b][j]["Y"], non_blocking=True)
+        ev_out[b].record(s_out)
 
-    for _ in range(2):
-        e2e_step()
+    for i in range(2):
+        e2e_step(i)
     torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
-    e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    e1.record(stream)
+    e0.record(s_in)
+    for i in range(args.steps):
+        e2e_step(i)
+    e1.record(s_out)
     torch.cuda.synchronize(dev)
     barrier()
     e2e_ms = e0.elapsed_time(e1)
+    if w4.w4a16_get_device_error() != w4.W4A16_OK:
+        raise RuntimeError("device error during the end-to-end steps")
 
     elapsed_ms, e2e_ms = max_over_ranks([elapsed_ms, e2e_ms], world, dev)
     flops_step = sum(gemm_flops(c.M, c.N, c.K) for c in cases)
@@ -772,7 +801,10 @@ def run_gpu(args, rank, world):
                kernels=kernels, roofline=roofline, clocks=clk.summary(),
                gpu_launches=int(launches),
                e2e=dict(value=round(e2e_value, 3), unit="TFLOP/s", h2d_bytes_per_step=int(h2d),
-                        d2h_bytes_per_step=int(d2h)))
+                        d2h_bytes_per_step=int(d2h),
+                        pipeline="copy in, GEMM and copy out on three streams, two device "
+                                 "buffers for A and Y: step i's copies overlap the GEMMs of "
+                                 "its neighbours"))
     if b2b:
         out["gemm_back_to_back"] = b2b
     if block is not None:
