@@ -344,18 +344,21 @@ def graph_of(dev, fn, n):
     return g
 
 
-def time_graph_us(dev, g, reps):
-    """Device time per call of a replayed graph of `reps` calls (CUDA events
-    on the current stream, after one untimed replay)."""
+def time_graph_us(dev, g, reps, trials=20):
+    """Device time per call of a replayed graph of `reps` calls: the median
+    over `trials` replays, each between CUDA events on the current stream,
+    after one untimed replay."""
     import torch
     stream = torch.cuda.current_stream(dev)
     g.replay()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    g.replay()
-    e1.record(stream)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(trials)]
+    for e0, e1 in evs:
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
     torch.cuda.synchronize(dev)
-    return e0.elapsed_time(e1) / reps * 1e3
+    return statistics.median(e0.elapsed_time(e1) for e0, e1 in evs) / reps * 1e3
 
 
 def back_to_back(fx, c, peaks, wcache, tune, dev, swiglu=False):
