@@ -144,6 +144,10 @@ struct Args {
   int prefetch_w;              // weights are not written by the previous kernel on
                                // the stream: the codes and scales of this many
                                // first units go out before the dependency wait
+  int tail_tile0;              // dequant mode: tiles from this one on are the last
+                               // activation tile, whose MMAs run tail_n columns
+                               // (M rounded up to 16 there) instead of BA
+  int tail_n;
   const __half* scales;        // [K/128, N]; the group-mode readout reads its scales here
   const float* out_scale;      // NVFP4: the tensor scale g, applied to the fp32 sums
   const uint16_t* bias;        // [N] activation type (bf16 or fp16 bits)
@@ -1157,10 +1161,14 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG, WF>::kThreads, 1)
               if (gi == 0) W4A16_TRACE_UNIT(4, i);
               const uint32_t a_tmem = tmem + as * kAStageCols;
               const uint64_t bdesc = ptx::smem_desc_sw128(b0 + 2 * gi * C::kActBox);
+              // the last activation tile: only its columns that hold rows
+              const uint32_t id = u.tile >= a.tail_tile0
+                                      ? ptx::idesc_f16kind_f32(kTileW, a.tail_n, F16 ? 0u : 1u)
+                                      : idesc;
 #pragma unroll
               for (int kk = 0; kk < kUnitK / 16; ++kk) {
                 const uint32_t boff = ((kk >> 2) * C::kActBox + (kk & 3) * 32) >> 4;
-                ptx::mma_f16kind_tmem_a(d_tmem, a_tmem + kk * 8, bdesc + boff, idesc,
+                ptx::mma_f16kind_tmem_a(d_tmem, a_tmem + kk * 8, bdesc + boff, id,
                                         (kk > 0 || have) ? 1u : 0u);
               }
               have = true;
@@ -1386,8 +1394,11 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG, WF>::kThreads, 1)
         const bool has0 = L == 1 || i > i_first || (i_first & 1) == 0;
         const bool has1 = L == 2 && (i > i_first || (i_first & 1) == 1);
         const uint32_t buf = lane_base + C::kDCol + db * L * BA;
+        // columns past the last activation row were not computed (M-tail)
+        const int mcols = min(BA, a.M - (u.tile / a.n_tiles) * BA);
 #pragma unroll 1
         for (int c0 = 0; c0 < BA; c0 += C::kChunk) {
+          if (c0 >= mcols) break;
           float v[C::kChunk];
           load_cols<C::kChunk>(buf + (has0 ? 0 : BA) + c0, v);
           if (has0 && has1) {
@@ -1652,6 +1663,15 @@ cudaError_t launch_instance(const GemmGroup& grp, bool use_pdl, cudaStream_t str
     // two units per producer: deeper early copies sit ahead of the first
     // activation copy in the TMA queue and delay the start (measured)
     a.prefetch_w = p.weights_static ? 4 : 0;
+    {
+      // M-tail (dequant mode): the last activation tile's MMAs cover its
+      // rows rounded up to 16 (a valid kind::f16 N for 128-row MMAs)
+      const int m_tiles = static_cast<int>((p.M + BA - 1) / BA);
+      const int rows = static_cast<int>(p.M) - (m_tiles - 1) * BA;
+      const int tn = (rows + 15) / 16 * 16;
+      a.tail_n = tn < BA ? tn : BA;
+      a.tail_tile0 = (!GRP && tn < BA) ? (m_tiles - 1) * a.n_tiles : 0x7FFFFFFF;
+    }
     a.scales = static_cast<const __half*>(p.scales);
     a.out_scale = p.tensor_scale;
     a.bias = static_cast<const uint16_t*>(p.bias);
