@@ -956,6 +956,14 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG, WF>::kThreads, 1)
   Sched sched;
   sched.init(a, cta, ctas);
   const int total = sched.total;
+#ifdef W4A16_TRACE
+  if (threadIdx.x == 0 && trace_cta != nullptr) {
+    // profiling builds: the CTA's problem, units and dp tiles next to its times
+    trace_cta[blockIdx.x * 16 + 12] = static_cast<unsigned long long>(prob);
+    trace_cta[blockIdx.x * 16 + 13] = static_cast<unsigned long long>(total);
+    trace_cta[blockIdx.x * 16 + 14] = static_cast<unsigned long long>(sched.dp_iters);
+  }
+#endif
   // Every role but the producers waits for the previous kernel on the stream
   // here (its outputs may be this kernel's inputs); the producers wait in
   // their own branch, after any early weight copies.
