@@ -17,6 +17,10 @@ SHAPES = [
     synthetic.Case("m1_ragged_n", 1, 264, 384, 11, bias=True),
     synthetic.Case("m50_ragged", 50, 520, 640, 12, "t4", bias=True),
     synthetic.Case("m300_multi_tile", 300, 384, 1024, 14, bias=True),
+    # the row-block kernel's fp16 MMAs with several activation columns: teams
+    # (2056 rows, ragged) and a cluster K split (few rows, long K)
+    synthetic.Case("m7_n2056", 7, 2056, 2048, 19, bias=True),
+    synthetic.Case("m3_long_k", 3, 264, 16384, 20, "t4"),
 ]
 
 
@@ -96,3 +100,32 @@ def test_workloads_f16_default_variant(w4, case):
     Y = w4.w4a16_gemm(A.cuda(), packed, scales)
     assert w4.w4a16_get_device_error() == w4.W4A16_OK
     check_gemm_close(Y, reference(A, packed, scales, b), what=case.name + " f16")
+
+
+def test_integer_exact_f16_small_m(w4):
+    # as test_integer_exact_f16 at M = 5: the streaming variants for M <= 8
+    # (the row-block kernel's fp16 MMAs on 1032 + q, less 1032 x the
+    # activation sums) return the exact sum rounded once to fp16
+    rng = np.random.default_rng(33)
+    M, N, K = 5, 264, 1024
+    codes = rng.integers(-3, 4, size=(N, K))
+    codes[:, ::128] = 7
+    e = rng.integers(-3, 0, size=(N, K // 128))
+    x = (codes * np.repeat(2.0 ** e, 128, axis=1)).astype(np.float32)
+    a = rng.integers(-2, 3, size=(M, K)).astype(np.float32)
+    W = synthetic.to_bf16(x).cuda()
+    A = synthetic.to_f16(a)
+    packed, scales = w4.w4a16_quantize(W)
+    exact = a.astype(np.float64) @ x.astype(np.float64).T
+    assert np.all(exact == np.round(exact * 8) / 8) and np.abs(exact).max() < 4096
+    expected = bits(synthetic.to_f16(exact.astype(np.float32)))
+    ran = 0
+    for v in range(w4.w4a16_variant_count()):
+        name = w4.w4a16_variant_name(v)
+        if not name.startswith(("simt_", "rb_")) or not w4.w4a16_variant_eligible(v, M, N, K):
+            continue
+        Y = w4.w4a16_gemm(A.cuda(), packed, scales, variant=v)
+        torch.cuda.synchronize()
+        assert np.array_equal(bits(Y), expected), name
+        ran += 1
+    assert ran >= 2
