@@ -149,11 +149,11 @@ const Variant kVariants[] = {
     {"tc_a64_deq2_csk", {64, 2, false, 8}, false, 1, 0.50, -1.0, 0.35, 8},
     {"tc_a128_deq2_csk", {128, 2, false, 4}, false, 1, 0.65, -1.0, 0.5, 8},
     // row-block warp-MMA kernel for M <= 1, 2, 4, 8: unit_us is the time of
-    // one (row block, group) item of the busiest warp on a full SM (rb_cost)
-    {"rb_m1", {1, 1, true, 0, 1, kFmtInt4, true, true}, false, 1, 1.12, 1.85, 0.0},
-    {"rb_m2", {2, 1, true, 0, 1, kFmtInt4, true, true}, false, 1, 1.30, 1.85, 0.0},
-    {"rb_m4", {4, 1, true, 0, 1, kFmtInt4, true, true}, false, 1, 1.56, 1.85, 0.0},
-    {"rb_m8", {8, 1, true, 0, 1, kFmtInt4, true, true}, false, 1, 1.98, 1.85, 0.0},
+    // one (row block, group) item per warp on a full SM (rb_cost)
+    {"rb_m1", {1, 1, true, 0, 1, kFmtInt4, true, true}, false, 1, 1.07, 1.85, 0.0},
+    {"rb_m2", {2, 1, true, 0, 1, kFmtInt4, true, true}, false, 1, 1.20, 1.85, 0.0},
+    {"rb_m4", {4, 1, true, 0, 1, kFmtInt4, true, true}, false, 1, 1.33, 1.85, 0.0},
+    {"rb_m8", {8, 1, true, 0, 1, kFmtInt4, true, true}, false, 1, 2.16, 1.85, 0.0},
     // CUDA-core streaming kernel for M <= 1, 2, 4, 8: unit_us is the time of
     // one unit on one worker (a warp; many warps share an SM)
     {"simt_m1_sk", {1, 1, true, 2, 1, kFmtInt4, true}, true, 1, 6.0, 2.0, 0.8},
@@ -402,7 +402,7 @@ double estimate_sched(const Variant& v, const GemmSchedule& s, int64_t K, int64_
                       int num_sms = kDefaultSms) {
   const int64_t KB = K / kGroup / v.cfg.unit_groups;
   if (v.cfg.rb) {
-    // unit_us: one (row block, group) item of the busiest warp on a full SM
+    // unit_us: one (row block, group) item per warp on a full SM
     const int64_t rows = gemv_rb_rows(v.cfg.act_tile);
     const int64_t slots = static_cast<int64_t>(num_sms) * gemv_rb_ctas_per_sm(v.cfg.act_tile);
     return v.head_us + rb_cost(s, (N + rows - 1) / rows, K / kGroup, slots, num_sms) * v.unit_us;

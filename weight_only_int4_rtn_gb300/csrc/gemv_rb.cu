@@ -14,20 +14,20 @@
 // 8 columns take up to 8 activation rows at no extra cost.
 //
 // Work split.  An item is one row block (RB = 32 consecutive weight rows of
-// one 128-row storage tile) times one group of 128 codes along K: 2 KiB of
-// contiguous codes in the tiled storage, the 32 rows' scales, the group's
-// activations.  Persistent form: the grid is the resident CTAs (or fewer),
-// teams of WK warps (1, 2, 4, 8) take row blocks round-robin and split each
-// row block's K range into WK equal runs of groups; the host picks WK so
-// that the busiest warp has the fewest items.  Cluster form, for shapes
-// with few row blocks and long K: one CTA-wide team per (row block, cluster
-// rank), the K range split over the S CTAs of a thread-block cluster and
-// summed through distributed shared memory.
+// one 128-row storage tile) times up to two groups of 128 codes along K (one
+// for M = 8): 2 KiB of contiguous codes per group in the tiled storage, the
+// 32 rows' scales, the groups' activations.  Persistent form: the grid is
+// the resident CTAs (or fewer), teams of WK warps (1, 2, 4, 8) take row
+// blocks round-robin and split each row block's K range into WK equal runs
+// of groups; the host picks WK so that the busiest SM has the least work.
+// Cluster form, for shapes with few row blocks and long K: one CTA-wide team
+// per (row block, cluster rank), the K range split over the S CTAs of a
+// thread-block cluster and summed through distributed shared memory.
 //
-// Streaming.  Each warp owns a ring of D shared-memory stages (one item
+// Streaming.  Each warp owns a ring of two shared-memory stages (one item
 // each) filled by non-tensor bulk copies (cp.async.bulk) that complete on a
-// per-stage mbarrier, so D items per warp are in flight without holding a
-// register.  With static weights the first stages' codes and scales are
+// per-stage mbarrier, so the next item is in flight while one is computed,
+// without holding a register.  With static weights the first stages' codes and scales are
 // requested before the wait for the previous kernel (whose output may be
 // A).  Waits are time-bounded: a warp that gives up records the error,
 // walks its remaining items without waiting (so its team's barriers still
