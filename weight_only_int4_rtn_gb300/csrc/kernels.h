@@ -61,10 +61,11 @@ struct GemmKernelConfig {
                         // codes, scales and activations per unit
   int weight_format = kFmtInt4;  // kFmtInt4 (W4A16), kFmtInt8 (W8A16), kFmtMxfp4,
                                  // kFmtNvfp4 (FP4 weights, dequant mode)
-  bool simt = false;  // the CUDA-core streaming kernel (gemv.cu) for M <= act_tile
-                      // (1, 2, 4 or 8), INT4 weights
-  bool rb = false;    // with simt: the row-block warp-MMA kernel (gemv_rb.cu) for
-                      // M <= act_tile (1, 2, 4 or 8)
+  bool simt = false;  // a streaming kernel without tcgen05 pipeline roles for M <=
+                      // act_tile, INT4 weights: the CUDA-core stream-K workers
+                      // (gemv.cu, act_tile 1, 2, 4 or 8), or with rb:
+  bool rb = false;    // the row-block warp-MMA kernel (gemv_rb.cu, act_tile 1, 2,
+                      // 4 or 8)
 };
 
 // The CUDA-core streaming kernel: every warp is a stream-K worker with two
