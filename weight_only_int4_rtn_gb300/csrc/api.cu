@@ -153,7 +153,7 @@ const Variant kVariants[] = {
     {"rb_m1", {1, 1, true, 0, 1, kFmtInt4, true, true}, false, 1, 1.07, 1.85, 0.0},
     {"rb_m2", {2, 1, true, 0, 1, kFmtInt4, true, true}, false, 1, 1.20, 1.85, 0.0},
     {"rb_m4", {4, 1, true, 0, 1, kFmtInt4, true, true}, false, 1, 1.33, 1.85, 0.0},
-    {"rb_m8", {8, 1, true, 0, 1, kFmtInt4, true, true}, false, 1, 2.16, 1.85, 0.0},
+    {"rb_m8", {8, 1, true, 0, 1, kFmtInt4, true, true}, false, 1, 1.58, 1.85, 0.0},
     // CUDA-core streaming kernel for M <= 1, 2, 4, 8: unit_us is the time of
     // one unit on one worker (a warp; many warps share an SM)
     {"simt_m1_sk", {1, 1, true, 2, 1, kFmtInt4, true}, true, 1, 6.0, 2.0, 0.8},

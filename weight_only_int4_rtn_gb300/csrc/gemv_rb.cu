@@ -25,11 +25,15 @@
 // thread-block cluster and summed through distributed shared memory.
 //
 // Streaming.  Each warp owns a ring of two shared-memory stages (one item
-// each) filled by non-tensor bulk copies (cp.async.bulk) that complete on a
-// per-stage mbarrier, so the next item is in flight while one is computed,
-// without holding a register.  With static weights the first stages' codes and scales are
-// requested before the wait for the previous kernel (whose output may be
-// A).  Waits are time-bounded: a warp that gives up records the error,
+// each) whose copies complete on a per-stage mbarrier, so the next item is
+// in flight while one is computed, without holding a register: the codes
+// and scales by non-tensor bulk copies (cp.async.bulk), the activations by
+// one bulk copy per row for M <= 2 and by one tensor copy per group for all
+// rows for M <= 4 and 8 (each copy instruction costs the issuing warp time,
+// and per-row copies made M = 8 the slowest form).  With static weights the
+// first stages' codes and scales are requested before the wait for the
+// previous kernel (whose output may be A).  Waits are time-bounded: a warp
+// that gives up records the error,
 // walks its remaining items without waiting (so its team's barriers still
 // match) and lets its copies in flight land before it exits.
 //
@@ -61,6 +65,7 @@
 #include "kernels.h"
 #include "ptx.cuh"
 #include "waits.cuh"
+#include "warp_mma.cuh"
 
 namespace w4a16 {
 namespace {
@@ -70,6 +75,7 @@ constexpr int kRbRows = 32;       // rows per block: two 16-row MMA tiles
 constexpr int kRbCtasPerSm = 2;   // registers <= 128, shared memory <= 113 KB
 
 struct RbArgs {
+  CUtensorMap amap;        // M >= 4: A as [M][K], boxes of 136 values x MT rows
   const uint16_t* A;       // [M, K] activation type
   const uint8_t* packed;   // tiled codes
   const __half* scales;    // [K/128, N]
@@ -86,42 +92,39 @@ struct RbArgs {
   uint64_t timeout_ns;     // limit of one wait
 };
 
-template <bool F16>
-__device__ __forceinline__ float rb_act(uint16_t b) {
-  if constexpr (F16) {
-    return __half2float(__ushort_as_half(b));
-  } else {
-    return __uint_as_float(static_cast<uint32_t>(b) << 16);
-  }
-}
-
-template <bool F16>
-__device__ __forceinline__ uint16_t rb_out(float x) {
-  if constexpr (F16) {
-    return __half_as_ushort(__float2half_rn(x));
-  } else {
-    return __bfloat16_as_ushort(__float2bfloat16_rn(x));
-  }
-}
-
 // MT: activation rows (M <= MT; the MMA's 8 columns).  An item holds up to
 // UG groups of one row block (2 for M <= 4; 1 for M = 8, whose activation
-// rows fill the shared memory).  One stage: the item's codes (2 KiB per
-// group), its rows' scales (64 B per group), MT activation rows of the
-// item's groups (contiguous in A: 256 B per group).
+// rows fill the shared memory).  One stage holds the item's codes (2 KiB per
+// group), its rows' scales (64 B per group) and MT activation rows of the
+// item's groups.  M <= 2: the codes, the scales, then each activation row's
+// UG groups (contiguous in A: 256 B per group), padded by 16 B for M = 2.
+// M <= 4 and 8 (kTensor): per group, the activations as one tensor copy of
+// MT rows x 136 values (272-byte rows: the lanes' 16-byte loads of
+// different rows fall in different bank groups; rows >= M and values past K
+// are zero) followed by the group's scales, then the codes.
 template <int MT>
 struct RbCfg {
+  static constexpr bool kTensor = MT >= 4;
   static constexpr int kUG = MT <= 4 ? 2 : 1;
   static constexpr int kCodeBytes = kRbRows * 64;                 // one group
-  static constexpr int kScaleOff = kUG * kCodeBytes;
   static constexpr int kScaleBytes = kRbRows * 2;                 // one group
-  static constexpr int kActOff = kScaleOff + kUG * kScaleBytes;
-  static constexpr int kActRow = kUG * kGroup * 2;                // one activation row
-  static constexpr int kStage = kActOff + MT * kActRow;
+  static constexpr int kActRow = kTensor ? 272 : kUG * kGroup * 2 + (MT > 1 ? 16 : 0);
+  static constexpr int kActBox = MT * 272;                        // one group's tensor copy
+  static constexpr int kGrpBytes = (kActBox + kScaleBytes + 127) / 128 * 128;
+  static constexpr int kCodeOff = kTensor ? kUG * kGrpBytes : 0;
+  static constexpr int kScaleOff = kTensor ? kActBox : kUG * kCodeBytes;
+  static constexpr int kScaleStride = kTensor ? kGrpBytes : kScaleBytes;
+  static constexpr int kActOff = kTensor ? 0 : kScaleOff + kUG * kScaleBytes;
+  static constexpr int kActGroup = kTensor ? kGrpBytes : kGroup * 2;   // to group gi's values
+  static constexpr int kStage =
+      kTensor ? (kCodeOff + kUG * kCodeBytes + 127) / 128 * 128 : kActOff + MT * kActRow;
   static constexpr int kDepth = 2;                                // stages per warp
   static constexpr int kBarOff = kRbWarps * kDepth * kStage;
-  static constexpr int kSmem = kBarOff + kRbWarps * kDepth * 8;
-  static_assert(kActOff % 16 == 0 && kStage % 16 == 0, "bulk-copy destinations 16-byte aligned");
+  static constexpr int kSmem = kBarOff + kRbWarps * kDepth * 8 + 128;   // + alignment of the base
+  static_assert(kActOff % 16 == 0 && kCodeOff % 16 == 0 && kStage % 16 == 0,
+                "bulk-copy destinations 16-byte aligned");
+  static_assert(!kTensor || (kGrpBytes % 128 == 0 && kStage % 128 == 0),
+                "tensor-copy destinations 128-byte aligned");
   static_assert(MT >= 1 && MT <= 8, "the MMA has 8 columns");
 };
 
@@ -137,8 +140,9 @@ struct RbWalk {
   const uint16_t* act;       // row 0's values of the item's groups
   uint32_t scale_bytes;      // one group's
   __device__ bool valid(int NB) const { return rb < NB; }
-  __device__ uint32_t bytes(int M) const {
-    return static_cast<uint32_t>(ng) * (kRbRows * 64 + scale_bytes + static_cast<uint32_t>(M) * kGroup * 2);
+  // the item's transaction bytes, given one group's activation bytes
+  __device__ uint32_t bytes(uint32_t act_group) const {
+    return static_cast<uint32_t>(ng) * (kRbRows * 64 + scale_bytes + act_group);
   }
   __device__ void start(const RbArgs& a, int rb_, int k0, int k1) {
     rb = rb_;
@@ -166,43 +170,14 @@ struct RbWalk {
   }
 };
 
-__device__ __forceinline__ uint32_t lds_u16(uint32_t saddr) {
-  uint16_t v;
-  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(saddr));
-  return v;
-}
-
-// D += A B for one m16n8k16 tile (A row-major 16 x 16, B column-major 16 x
-// 8, fp32 accumulators), bf16 or fp16 operands.
-template <bool F16>
-__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1) {
-  if constexpr (F16) {
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-  } else {
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-  }
-}
-
-// Nibbles s and s + 4 of a code word as two 16-bit values x + q (low half:
-// nibble s), x = 136 (bf16) or 1032 (fp16).
-template <bool F16>
-__device__ __forceinline__ uint32_t rb_pair16(uint32_t w, int s) {
-  return ptx::and_xor(w >> (4 * s), 0x000F000Fu, F16 ? 0x64086408u : 0x43084308u);
-}
-
 template <int MT, bool F16>
 __global__ void __launch_bounds__(kRbWarps * 32, kRbCtasPerSm)
     gemv_rb_kernel(const __grid_constant__ RbArgs g) {
   using C = RbCfg<MT>;
   constexpr int D = C::kDepth;
-  extern __shared__ __align__(128) uint8_t smem[];
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
+                                             ~static_cast<uintptr_t>(127));
   // per warp, per row-block parity: its rows' totals (a team's flush)
   __shared__ float tbuf[kRbWarps][2][kRbRows][MT];
   __shared__ float csum[kRbRows][MT];   // cluster split: the CTA's totals
@@ -232,7 +207,10 @@ __global__ void __launch_bounds__(kRbWarps * 32, kRbCtasPerSm)
 
   uint8_t* ring = smem + warp * D * C::kStage;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBarOff) + warp * D;
-  if (threadIdx.x == 0) abort_flag = 0;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    if constexpr (C::kTensor) ptx::prefetch_tmap(&g.amap);
+  }
   if (lane == 0) {
     for (int s = 0; s < D; ++s) ptx::mbar_init(&full[s], 1);
     ptx::fence_mbar_init();
@@ -246,17 +224,21 @@ __global__ void __launch_bounds__(kRbWarps * 32, kRbCtasPerSm)
   constexpr int UG = C::kUG;
   using Walk = RbWalk<UG>;
   auto issue_w = [&](const Walk& it, uint8_t* st, uint64_t* bar) {
-    ptx::mbar_arrive_expect_tx(bar, it.bytes(g.M));
+    ptx::mbar_arrive_expect_tx(
+        bar, it.bytes(C::kTensor ? static_cast<uint32_t>(C::kActBox) : static_cast<uint32_t>(g.M) * kGroup * 2));
     for (int gi = 0; gi < it.ng; ++gi) {
-      ptx::bulk_g2s(st + gi * C::kCodeBytes, it.codes + static_cast<int64_t>(gi) * kTileW * 64, C::kCodeBytes,
-                    bar);
-      ptx::bulk_g2s(st + C::kScaleOff + gi * C::kScaleBytes, it.scales + static_cast<int64_t>(gi) * g.N,
+      ptx::bulk_g2s(st + C::kCodeOff + gi * C::kCodeBytes, it.codes + static_cast<int64_t>(gi) * kTileW * 64,
+                    C::kCodeBytes, bar);
+      ptx::bulk_g2s(st + C::kScaleOff + gi * C::kScaleStride, it.scales + static_cast<int64_t>(gi) * g.N,
                     it.scale_bytes, bar);
     }
   };
   auto issue_a = [&](const Walk& it, uint8_t* st, uint64_t* bar) {
     const uint32_t bytes = static_cast<uint32_t>(it.ng) * kGroup * 2;
-    if constexpr (MT == 1) {
+    if constexpr (C::kTensor) {
+      for (int gi = 0; gi < it.ng; ++gi)
+        ptx::tma_load_2d(st + gi * C::kGrpBytes, &g.amap, bar, (it.g + gi) * kGroup, 0);
+    } else if constexpr (MT == 1) {
       ptx::bulk_g2s(st + C::kActOff, it.act, bytes, bar);
     } else {
       for (int m = 0; m < g.M; ++m)
@@ -294,13 +276,13 @@ __global__ void __launch_bounds__(kRbWarps * 32, kRbCtasPerSm)
   // <- k = 32 tq + 8 j + 2 h + (0, 4), columns (2 tq + 8, 2 tq + 9) <- + (1,
   // 5); B's fragment rows take the same k from the activations.
   auto compute_group = [&](uint32_t st, int gi) {
-    constexpr uint32_t kOne = F16 ? 0x3C003C00u : 0x3F803F80u;
-    constexpr float kOff = F16 ? 1032.0f : 136.0f;
+    constexpr uint32_t kOne = wmma16::CodeOffset<F16>::kOnes;
+    constexpr float kOff = wmma16::CodeOffset<F16>::kOff;
     const int mrow = gq < MT ? gq : MT - 1;   // columns >= M are never stored
     uint32_t u[16];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const uint4 v = ptx::lds128(st + C::kActOff + mrow * C::kActRow + gi * kGroup * 2 + 64 * tq + 16 * i);
+      const uint4 v = ptx::lds128(st + C::kActOff + mrow * C::kActRow + gi * C::kActGroup + 64 * tq + 16 * i);
       u[4 * i] = v.x;
       u[4 * i + 1] = v.y;
       u[4 * i + 2] = v.z;
@@ -320,15 +302,16 @@ __global__ void __launch_bounds__(kRbWarps * 32, kRbCtasPerSm)
     float sa[4] = {}, sb[4] = {};
 #pragma unroll
     for (int mu = 0; mu < 8; mu += 2) {
-      mma16816<F16>(sa, kOne, kOne, kOne, kOne, b[mu][0], b[mu][1]);
-      mma16816<F16>(sb, kOne, kOne, kOne, kOne, b[mu + 1][0], b[mu + 1][1]);
+      wmma16::mma16816<F16>(sa, kOne, kOne, kOne, kOne, b[mu][0], b[mu][1]);
+      wmma16::mma16816<F16>(sb, kOne, kOne, kOne, kOne, b[mu + 1][0], b[mu + 1][1]);
     }
     uint32_t W[2][2][4];   // [tile][row gq, gq + 8][word]
 #pragma unroll
     for (int tau = 0; tau < 2; ++tau)
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
-        const uint4 v = ptx::lds128(st + gi * C::kCodeBytes + (16 * tau + 8 * half + gq) * 64 + 16 * tq);
+        const uint4 v =
+            ptx::lds128(st + C::kCodeOff + gi * C::kCodeBytes + (16 * tau + 8 * half + gq) * 64 + 16 * tq);
         W[tau][half][0] = v.x;
         W[tau][half][1] = v.y;
         W[tau][half][2] = v.z;
@@ -341,16 +324,17 @@ __global__ void __launch_bounds__(kRbWarps * 32, kRbCtasPerSm)
       for (int h = 0; h < 2; ++h)
 #pragma unroll
         for (int tau = 0; tau < 2; ++tau)
-          mma16816<F16>(d[tau][h], rb_pair16<F16>(W[tau][0][j], 2 * h), rb_pair16<F16>(W[tau][1][j], 2 * h),
-                        rb_pair16<F16>(W[tau][0][j], 2 * h + 1), rb_pair16<F16>(W[tau][1][j], 2 * h + 1),
-                        b[2 * j + h][0], b[2 * j + h][1]);
+          wmma16::mma16816<F16>(d[tau][h], wmma16::code_pair16<F16>(W[tau][0][j], 2 * h),
+                                wmma16::code_pair16<F16>(W[tau][1][j], 2 * h),
+                                wmma16::code_pair16<F16>(W[tau][0][j], 2 * h + 1),
+                                wmma16::code_pair16<F16>(W[tau][1][j], 2 * h + 1), b[2 * j + h][0],
+                                b[2 * j + h][1]);
     const float sum0 = sa[0] + sb[0], sum1 = sa[1] + sb[1];
 #pragma unroll
     for (int tau = 0; tau < 2; ++tau) {
       const int r = 16 * tau + gq;
-      const float s0 = __half2float(__ushort_as_half(static_cast<uint16_t>(lds_u16(st + C::kScaleOff + gi * C::kScaleBytes + 2 * r))));
-      const float s1 =
-          __half2float(__ushort_as_half(static_cast<uint16_t>(lds_u16(st + C::kScaleOff + gi * C::kScaleBytes + 2 * (r + 8)))));
+      const float s0 = wmma16::lds_scale(st + C::kScaleOff + gi * C::kScaleStride + 2 * r);
+      const float s1 = wmma16::lds_scale(st + C::kScaleOff + gi * C::kScaleStride + 2 * (r + 8));
       acc[tau][0] = fmaf(s0, fmaf(-kOff, sum0, d[tau][0][0] + d[tau][1][0]), acc[tau][0]);
       acc[tau][1] = fmaf(s0, fmaf(-kOff, sum1, d[tau][0][1] + d[tau][1][1]), acc[tau][1]);
       acc[tau][2] = fmaf(s1, fmaf(-kOff, sum0, d[tau][0][2] + d[tau][1][2]), acc[tau][2]);
@@ -373,8 +357,8 @@ __global__ void __launch_bounds__(kRbWarps * 32, kRbCtasPerSm)
           const int m = 2 * tq + (e & 1);
           if (m < g.M && n < g.N) {
             float t = acc[tau][e];
-            if (g.bias != nullptr) t += rb_act<F16>(g.bias[n]);
-            g.Y[static_cast<int64_t>(m) * g.N + n] = rb_out<F16>(t);
+            if (g.bias != nullptr) t += wmma16::act_to_f32<F16>(g.bias[n]);
+            g.Y[static_cast<int64_t>(m) * g.N + n] = wmma16::f32_to_out<F16>(t);
           }
         }
     } else {
@@ -396,8 +380,8 @@ __global__ void __launch_bounds__(kRbWarps * 32, kRbCtasPerSm)
           } else {
             const int n = r0 + row;
             if (n < g.N && m < g.M) {
-              if (g.bias != nullptr) t += rb_act<F16>(g.bias[n]);
-              g.Y[static_cast<int64_t>(m) * g.N + n] = rb_out<F16>(t);
+              if (g.bias != nullptr) t += wmma16::act_to_f32<F16>(g.bias[n]);
+              g.Y[static_cast<int64_t>(m) * g.N + n] = wmma16::f32_to_out<F16>(t);
             }
           }
         }
@@ -476,8 +460,8 @@ __global__ void __launch_bounds__(kRbWarps * 32, kRbCtasPerSm)
       if (n >= g.N || m >= g.M) continue;
       float t = 0.0f;
       for (int q = 0; q < S; ++q) t += ptx::ld_dsmem_f32(base + 4u * static_cast<uint32_t>(e), q);
-      if (g.bias != nullptr) t += rb_act<F16>(g.bias[n]);
-      g.Y[static_cast<int64_t>(m) * g.N + n] = rb_out<F16>(t);
+      if (g.bias != nullptr) t += wmma16::act_to_f32<F16>(g.bias[n]);
+      g.Y[static_cast<int64_t>(m) * g.N + n] = wmma16::f32_to_out<F16>(t);
     }
     ptx::cluster_sync();   // every CTA's sums stay alive until read
   }
@@ -511,6 +495,15 @@ cudaError_t launch_rb(const GemmProblem& p, const GemmSchedule& s, bool use_pdl,
   g.static_w = p.weights_static ? 1 : 0;
   g.err = p.error_word;
   g.timeout_ns = p.timeout_ns;
+  if constexpr (C::kTensor) {
+    // A as [M][K]: a box of 136 values (one group and 8 more, which keep the
+    // rows 272 bytes apart in shared memory) by MT rows, zero past K and M
+    constexpr CUtensorMapDataType kActType =
+        F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    if (encode_tmap_2d(&g.amap, kActType, p.A, p.K, p.M, p.K * 2, C::kActRow / 2, MT,
+                       CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
   auto kernel = gemv_rb_kernel<MT, F16>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
