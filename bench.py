@@ -687,6 +687,25 @@ def run_gpu(args, rank, world):
     for i in range(2):
         e2e_step(i)
     torch.cuda.synchronize(dev)
+
+    # the host link alone, outside the timed region: one step's copies in,
+    # then its copies out, each direction by itself (median of 3)
+    def copies_ms(fn, st):
+        ts = []
+        for _ in range(3):
+            c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            c0.record(st)
+            with torch.cuda.stream(st):
+                fn()
+            c1.record(st)
+            torch.cuda.synchronize(dev)
+            ts.append(c0.elapsed_time(c1))
+        return statistics.median(ts)
+
+    t_in = copies_ms(lambda: [bufs[0][j]["A"].copy_(a_host[j], non_blocking=True) for j in range(len(cases))],
+                     s_in)
+    t_out = copies_ms(lambda: [y_host[j].copy_(bufs[0][j]["Y"], non_blocking=True) for j in range(len(cases))],
+                      s_out)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     e0.record(s_in)
@@ -807,7 +826,12 @@ def run_gpu(args, rank, world):
                         d2h_bytes_per_step=int(d2h),
                         pipeline="copy in, GEMM and copy out on three streams, two device "
                                  "buffers for A and Y: step i's copies overlap the GEMMs of "
-                                 "its neighbours"))
+                                 "its neighbours",
+                        link=dict(h2d_gbs=round(h2d / (t_in * 1e-3) / 1e9, 1),
+                                  d2h_gbs=round(d2h / (t_out * 1e-3) / 1e9, 1),
+                                  h2d_ms=round(t_in, 4), d2h_ms=round(t_out, 4),
+                                  note="one step's copies, each direction alone, outside the "
+                                       "timed region")))
     if b2b:
         out["gemm_back_to_back"] = b2b
     if block is not None:
