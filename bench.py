@@ -706,6 +706,30 @@ def run_gpu(args, rank, world):
                      s_in)
     t_out = copies_ms(lambda: [y_host[j].copy_(bufs[0][j]["Y"], non_blocking=True) for j in range(len(cases))],
                       s_out)
+
+    def both_ms():
+        # a step's copies in and out at once, on their two streams
+        ts = []
+        cur = torch.cuda.current_stream(dev)
+        for _ in range(3):
+            c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            c0.record(cur)
+            for st, fn in ((s_in, lambda: [bufs[0][j]["A"].copy_(a_host[j], non_blocking=True)
+                                           for j in range(len(cases))]),
+                           (s_out, lambda: [y_host[j].copy_(bufs[1][j]["Y"], non_blocking=True)
+                                            for j in range(len(cases))])):
+                st.wait_event(c0)
+                with torch.cuda.stream(st):
+                    fn()
+                done = torch.cuda.Event()
+                done.record(st)
+                cur.wait_event(done)
+            c1.record(cur)
+            torch.cuda.synchronize(dev)
+            ts.append(c0.elapsed_time(c1))
+        return statistics.median(ts)
+
+    t_both = both_ms()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     e0.record(s_in)
@@ -830,8 +854,10 @@ def run_gpu(args, rank, world):
                         link=dict(h2d_gbs=round(h2d / (t_in * 1e-3) / 1e9, 1),
                                   d2h_gbs=round(d2h / (t_out * 1e-3) / 1e9, 1),
                                   h2d_ms=round(t_in, 4), d2h_ms=round(t_out, 4),
-                                  note="one step's copies, each direction alone, outside the "
-                                       "timed region")))
+                                  both_ms=round(t_both, 4),
+                                  note="one step's copies outside the timed region: each "
+                                       "direction alone, then both at once (both_ms: the "
+                                       "shortest step the link allows)")))
     if b2b:
         out["gemm_back_to_back"] = b2b
     if block is not None:
