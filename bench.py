@@ -507,6 +507,17 @@ def run_gpu(args, rank, world):
     if any(epilogues) and (not args.grouped or fmt != "int4" or args.act != "bf16"):
         raise SystemExit("--swiglu: INT4 weights, bf16 activations, grouped step")
     shapes = [(c.M, c.N, c.K, e) for c, e in zip(cases, epilogues)]
+    if args.variant is not None:
+        # one catalogue variant for every projection of the step, set in the
+        # library's table (no tuning): to time or profile that kernel
+        vid = w4.variant_id(args.variant)
+        if fmt != "int4" or args.grouped or any(epilogues):
+            raise SystemExit("--variant: INT4 weights, one launch per projection, no epilogue")
+        for c in cases:
+            if not w4.w4a16_variant_eligible(vid, c.M, c.N, c.K):
+                raise SystemExit(f"--variant {args.variant} is not eligible for {c.M}x{c.N}x{c.K}")
+            w4.w4a16_table_set(c.M, c.N, c.K, vid)
+        args.tune = False
     if args.tune:
         if args.grouped:
             w4.w4a16_tune_grouped(shapes, act=fx.act_dtype)
@@ -784,8 +795,11 @@ def run_gpu(args, rank, world):
     else:
         bound, peak, unit = "hbm", peaks["hbm_gbs"], "GB/s"
         achieved = bytes_step / (dom_ms * 1e-3) / 1e9
-    tkey = args.workload + ("_grouped" if args.grouped else "") + \
-        ("" if fmt == "int4" else "_" + fmt) + ("_f16" if args.act == "f16" else "")
+    # the recorded traffic is keyed by workload (or --shape) and, when one
+    # was forced, the variant: another workload's figure never applies
+    tkey = ("shape_" + args.shape.replace(",", "x") if args.shape else args.workload) + \
+        ("_grouped" if args.grouped else "") + ("" if fmt == "int4" else "_" + fmt) + \
+        ("_f16" if args.act == "f16" else "") + ("_" + args.variant if args.variant else "")
     traffic = dram_traffic(fx.gname, tkey)
     roofline = dict(bound=bound, achieved=round(achieved, 2), peak=peak, unit=unit,
                     frac=round(achieved / peak, 4),
@@ -837,7 +851,8 @@ def run_gpu(args, rank, world):
                                 "under kernels)",
                            l2="inputs rotate over %d copies (%.0f MB of weights and activations "
                               "> 3x L2)" % (copies, copies * in_bytes / 2**20),
-                           selection=("tuned by measurement before timing" if args.tune
+                           selection=(f"forced: {args.variant}" if args.variant is not None
+                                      else "tuned by measurement before timing" if args.tune
                                       else "cost-model rule"),
                            weights_static=bool(args.static_weights),
                            parallelism=f"replicas x{world}"),
@@ -948,6 +963,9 @@ def main():
                          "instead of round to nearest")
     ap.add_argument("--shape", default=None,
                     help="M,N,K: one projection of this shape instead of the workload's")
+    ap.add_argument("--variant", default=None,
+                    help="INT4: run every projection of the step with this catalogue variant "
+                         "(set in the library's table; no tuning)")
     ap.add_argument("--swiglu", action="store_true",
                     help="the gate/up projection takes the SwiGLU epilogue: inside the grouped "
                          "step, and back to back through w4a16_gemm_swiglu (INT4, bf16)")
