@@ -50,7 +50,12 @@
 // product is unchanged.  Products of x + q (at most 11 significant bits)
 // with an activation are exact in fp32.  An MMA of an all-ones A gives the
 // group's activation sums per column, and x times those is taken off before
-// the group's fp32 scale multiplies the partial into the row's total.
+// the group's fp32 scale multiplies the partial into the row's total.  With
+// fp16 activations the 10-bit mantissa also holds a nibble at bits 4-7: the
+// MMAs of a word split into a class of nibbles 0, 2, 4, 6 (1032 + q) and one
+// of nibbles 1, 3, 5, 7 (1152 + 16 q under 0x6480, exact), so one shift by 8
+// per word serves both, and the second class's partial, less 1152 times its
+// activation sum, is scaled by 1/16 (exact) before the group scale.
 //
 // Reduction.  A team's warps add their totals in k order through shared
 // memory after a named barrier; with a cluster the CTAs' sums are added in
@@ -293,8 +298,14 @@ __global__ void __launch_bounds__(kRbWarps * 32, kRbCtasPerSm)
     for (int j = 0; j < 4; ++j)
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        b[2 * j + h][0] = ptx::prmt(u[4 * j + h], u[4 * j + h + 2], 0x5410u);
-        b[2 * j + h][1] = ptx::prmt(u[4 * j + h], u[4 * j + h + 2], 0x7632u);
+        if constexpr (F16) {
+          // class h of word j: k = k0 + h + (0, 4) and k0 + h + (2, 6)
+          b[2 * j + h][0] = ptx::prmt(u[4 * j], u[4 * j + 2], h ? 0x7632u : 0x5410u);
+          b[2 * j + h][1] = ptx::prmt(u[4 * j + 1], u[4 * j + 3], h ? 0x7632u : 0x5410u);
+        } else {
+          b[2 * j + h][0] = ptx::prmt(u[4 * j + h], u[4 * j + h + 2], 0x5410u);
+          b[2 * j + h][1] = ptx::prmt(u[4 * j + h], u[4 * j + h + 2], 0x7632u);
+        }
       }
     // the group's activation sums (column 2 tq in sum[0], 2 tq + 1 in
     // sum[1]); the MMAs run as independent accumulation chains (two for the
@@ -318,27 +329,70 @@ __global__ void __launch_bounds__(kRbWarps * 32, kRbCtasPerSm)
         W[tau][half][3] = v.w;
       }
     float d[2][2][4] = {};   // [tile][h]
+    if constexpr (F16) {
+      // fp16 (10 mantissa bits): nibbles s and s + 4 as 1032 + q (class 0,
+      // bits 0-3 of each half) or 16 (72 + q) = 1152 + 16 q (class 1, bits
+      // 4-7 under 0x6480), so one shift by 8 serves nibbles 2, 3, 6, 7;
+      // class 1's products are exact and its partial is scaled by 1/16
+      constexpr uint32_t kLoMask = 0x000F000Fu, kHiMask = 0x00F000F0u;
+      constexpr uint32_t kLoMagic = 0x64086408u, kHiMagic = 0x64806480u;
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-#pragma unroll
-      for (int h = 0; h < 2; ++h)
+      for (int j = 0; j < 4; ++j) {
+        uint32_t w[2][2], w8[2][2];
 #pragma unroll
         for (int tau = 0; tau < 2; ++tau)
-          wmma16::mma16816<F16>(d[tau][h], wmma16::code_pair16<F16>(W[tau][0][j], 2 * h),
-                                wmma16::code_pair16<F16>(W[tau][1][j], 2 * h),
-                                wmma16::code_pair16<F16>(W[tau][0][j], 2 * h + 1),
-                                wmma16::code_pair16<F16>(W[tau][1][j], 2 * h + 1), b[2 * j + h][0],
-                                b[2 * j + h][1]);
-    const float sum0 = sa[0] + sb[0], sum1 = sa[1] + sb[1];
 #pragma unroll
-    for (int tau = 0; tau < 2; ++tau) {
-      const int r = 16 * tau + gq;
-      const float s0 = wmma16::lds_scale(st + C::kScaleOff + gi * C::kScaleStride + 2 * r);
-      const float s1 = wmma16::lds_scale(st + C::kScaleOff + gi * C::kScaleStride + 2 * (r + 8));
-      acc[tau][0] = fmaf(s0, fmaf(-kOff, sum0, d[tau][0][0] + d[tau][1][0]), acc[tau][0]);
-      acc[tau][1] = fmaf(s0, fmaf(-kOff, sum1, d[tau][0][1] + d[tau][1][1]), acc[tau][1]);
-      acc[tau][2] = fmaf(s1, fmaf(-kOff, sum0, d[tau][0][2] + d[tau][1][2]), acc[tau][2]);
-      acc[tau][3] = fmaf(s1, fmaf(-kOff, sum1, d[tau][0][3] + d[tau][1][3]), acc[tau][3]);
+          for (int half = 0; half < 2; ++half) {
+            w[tau][half] = W[tau][half][j];
+            w8[tau][half] = W[tau][half][j] >> 8;
+          }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t mask = h ? kHiMask : kLoMask, magic = h ? kHiMagic : kLoMagic;
+#pragma unroll
+          for (int tau = 0; tau < 2; ++tau)
+            wmma16::mma16816<F16>(d[tau][h], ptx::and_xor(w[tau][0], mask, magic),
+                                  ptx::and_xor(w[tau][1], mask, magic),
+                                  ptx::and_xor(w8[tau][0], mask, magic),
+                                  ptx::and_xor(w8[tau][1], mask, magic), b[2 * j + h][0],
+                                  b[2 * j + h][1]);
+        }
+      }
+#pragma unroll
+      for (int tau = 0; tau < 2; ++tau) {
+        const int r = 16 * tau + gq;
+        const float s0 = wmma16::lds_scale(st + C::kScaleOff + gi * C::kScaleStride + 2 * r);
+        const float s1 = wmma16::lds_scale(st + C::kScaleOff + gi * C::kScaleStride + 2 * (r + 8));
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float q = fmaf(0.0625f, fmaf(-1152.0f, sb[e & 1], d[tau][1][e]),
+                               fmaf(-1032.0f, sa[e & 1], d[tau][0][e]));
+          acc[tau][e] = fmaf(e < 2 ? s0 : s1, q, acc[tau][e]);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int tau = 0; tau < 2; ++tau)
+            wmma16::mma16816<F16>(d[tau][h], wmma16::code_pair16<F16>(W[tau][0][j], 2 * h),
+                                  wmma16::code_pair16<F16>(W[tau][1][j], 2 * h),
+                                  wmma16::code_pair16<F16>(W[tau][0][j], 2 * h + 1),
+                                  wmma16::code_pair16<F16>(W[tau][1][j], 2 * h + 1), b[2 * j + h][0],
+                                  b[2 * j + h][1]);
+      const float sum0 = sa[0] + sb[0], sum1 = sa[1] + sb[1];
+#pragma unroll
+      for (int tau = 0; tau < 2; ++tau) {
+        const int r = 16 * tau + gq;
+        const float s0 = wmma16::lds_scale(st + C::kScaleOff + gi * C::kScaleStride + 2 * r);
+        const float s1 = wmma16::lds_scale(st + C::kScaleOff + gi * C::kScaleStride + 2 * (r + 8));
+        acc[tau][0] = fmaf(s0, fmaf(-kOff, sum0, d[tau][0][0] + d[tau][1][0]), acc[tau][0]);
+        acc[tau][1] = fmaf(s0, fmaf(-kOff, sum1, d[tau][0][1] + d[tau][1][1]), acc[tau][1]);
+        acc[tau][2] = fmaf(s1, fmaf(-kOff, sum0, d[tau][0][2] + d[tau][1][2]), acc[tau][2]);
+        acc[tau][3] = fmaf(s1, fmaf(-kOff, sum1, d[tau][0][3] + d[tau][1][3]), acc[tau][3]);
+      }
     }
   };
 
