@@ -299,7 +299,7 @@ def test_row_block_schedule_forms(built_lib):
     """The row-block kernel's launch form chosen by the host cost model (on a
     152-SM GB300): the busiest SM's group-items at 16 per unit of time with
     two busy CTAs and 8 / 0.65 with one, the cluster split at 1.3 items a
-    wave.  Each team size and the cluster form is the choice for some
+    wave (items at 1.4 when its clusters put two CTAs on an SM).  Each team size and the cluster form is the choice for some
     shape."""
     rb1 = w4.variant_id("rb_m1")
     sched = lambda N, K: w4.w4a16_variant_schedule(rb1, 1, N, K, 152)
@@ -314,7 +314,8 @@ def test_row_block_schedule_forms(built_lib):
     assert sched(4096, 4096) == dict(grid=128, dp_tiles=0, sk_units=0, cluster=1, team=8)
     assert w4.w4a16_variant_workspace_bytes(rb1, 1, 8192, 8192) == 0
     # few row blocks, long K: a cluster K split (grid = row blocks x cluster)
-    assert sched(2048, 16384) == dict(grid=256, dp_tiles=0, sk_units=0, cluster=4, team=8)
+    # (a split of 2 on 128 CTAs: measured 7.7 us against 8.2 us for 4 on 256)
+    assert sched(2048, 16384) == dict(grid=128, dp_tiles=0, sk_units=0, cluster=2, team=8)
     assert sched(256, 4096) == dict(grid=32, dp_tiles=0, sk_units=0, cluster=4, team=8)
     assert sched(256, 16384) == dict(grid=64, dp_tiles=0, sk_units=0, cluster=8, team=8)
     # a tcgen05 variant reports no team; argument errors

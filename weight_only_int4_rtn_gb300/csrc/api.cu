@@ -226,12 +226,14 @@ bool shape_ok(int64_t M, int64_t N, int64_t K) {
 // through 8 / 0.65 (measured: 8 / 0.62); the cost is the busiest SM's.
 // Cluster form: waves of the resident CTAs, each wave's warps running their
 // share of a row block's K range, plus the cluster's own cost (barriers, the
-// distributed shared-memory sum), about 1.3 items a wave.
+// distributed shared-memory sum), about 1.3 items a wave.  Clusters that put
+// two CTAs on an SM run each item at 1.4 (measured: 2048 x 16384 at M = 1
+// and 4, a split of 4 on 256 CTAs 6-7% slower than a split of 2 on 128).
 double rb_cost(const GemmSchedule& s, int64_t blocks, int64_t KB, int64_t slots, int num_sms) {
   if (s.cluster > 1) {
     const int64_t waves = (blocks * s.cluster + slots - 1) / slots;
     const int64_t per = static_cast<int64_t>(s.cluster) * kRbWarpsPerCta;
-    const double load = s.grid <= num_sms ? 0.65 : 1.0;
+    const double load = s.grid <= num_sms ? 0.65 : 1.4;
     return static_cast<double>(waves * ((KB + per - 1) / per)) * load + 1.3 * static_cast<double>(waves);
   }
   const double thr1 = kRbWarpsPerCta / 0.65, thr2 = 2.0 * kRbWarpsPerCta;
