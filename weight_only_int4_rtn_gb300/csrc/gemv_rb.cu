@@ -33,9 +33,9 @@
 // and per-row copies made M = 8 the slowest form).  With static weights the
 // first stages' codes and scales are requested before the wait for the
 // previous kernel (whose output may be A).  Waits are time-bounded: a warp
-// that gives up records the error,
-// walks its remaining items without waiting (so its team's barriers still
-// match) and lets its copies in flight land before it exits.
+// that gives up records the error, walks its remaining items without
+// waiting (so its team's barriers still match) and lets its copies in
+// flight land before it exits.
 //
 // Arithmetic.  The row block is two 16-row MMA tiles (A: weight rows x k),
 // the activations are B (k x 8 columns, column m = activation row m).  A
@@ -224,8 +224,9 @@ __global__ void __launch_bounds__(kRbWarps * 32, kRbCtasPerSm)
   const WaitCtx wc{g.err, g.timeout_ns, &abort_flag};
 
   // an item's copies, issued by lane 0: weights (each group's codes and the
-  // valid rows' scales) and activations (each of the M rows' values of the
-  // item's groups, one contiguous run)
+  // valid rows' scales) and activations (M <= 2: each of the M rows' values
+  // of the item's groups, one contiguous run; else one tensor copy of MT
+  // rows per group)
   constexpr int UG = C::kUG;
   using Walk = RbWalk<UG>;
   auto issue_w = [&](const Walk& it, uint8_t* st, uint64_t* bar) {
