@@ -54,20 +54,25 @@ def test_traffic_only_for_the_recorded_sources(monkeypatch):
 
 
 def test_source_hash_covers_every_kernel_source(tmp_path, monkeypatch):
-    # the hash changes when any .cu, .cuh or .h file under csrc changes
+    # the hash changes when the code of any .cu, .cuh or .h file under csrc
+    # changes, and not when only a comment does
     h0 = bench.kernel_source_hash()
     csrc = os.path.join(bench.ROOT, "weight_only_int4_rtn_gb300", "csrc")
     names = sorted(f for f in os.listdir(csrc) if f.endswith((".cu", ".cuh", ".h")))
     real_open = open
+    extra = {"text": ""}
 
     def fake_open(p, mode="r", *a, **k):
         f = real_open(p, mode, *a, **k)
-        if "b" in mode and os.path.basename(str(p)) == names[-1]:
-            data = f.read() + b"\n"
+        if "b" not in mode and os.path.basename(str(p)) == names[-1]:
+            data = f.read() + extra["text"]
             f.close()
             import io
-            return io.BytesIO(data)
+            return io.StringIO(data)
         return f
 
     monkeypatch.setattr("builtins.open", fake_open)
+    extra["text"] = "\n// a comment only\n"
+    assert bench.kernel_source_hash() == h0
+    extra["text"] = "\nstatic int w4a16_probe_value = 1;\n"
     assert bench.kernel_source_hash() != h0
