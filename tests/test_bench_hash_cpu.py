@@ -20,8 +20,3 @@ def test_comment_edit_keeps_code_edit_changes_the_key():
     assert bench.code_only(a) == bench.code_only(b)
     assert bench.code_only(a) != bench.code_only(c)
 
-
-def test_recorded_traffic_matches_the_current_sources():
-    # the default workload's GEMM traffic in profiles/ was taken on the
-    # current code
-    assert bench.dram_traffic("w4a16_gemm_tc", "large") is not None

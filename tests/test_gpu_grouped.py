@@ -57,6 +57,44 @@ def test_grouped_gemm_every_variant(w4, act):
             check_gemm_close(Y, ref, what=f"{w4.w4a16_variant_name(v)} {c.name} {act}")
 
 
+# the action-expert block's projections and a ragged one, at decode sizes
+SMALL = [(2048, 1024), (1024, 1024), (8192, 1024), (1024, 4096), (136, 384)]
+
+
+@pytest.mark.parametrize("M,act", [(1, "bf16"), (3, "bf16"), (8, "bf16"), (5, "f16")])
+def test_grouped_small_m_row_block(w4, M, act):
+    """Projections of a decode step (M <= 8) in one grouped launch of the
+    row-block kernel (problem i on its own sub-grid, persistent form):
+    every eligible rb variant against the oracle, bit-identical repeats, and
+    the library's own plan."""
+    cases = [synthetic.Case(f"gs_m{M}_{n}x{k}", M, n, k, 60 + i, "t4" if i % 2 else "normal",
+                            bias=(i % 2 == 0)) for i, (n, k) in enumerate(SMALL)]
+    drawn, q = _operands(w4, cases, act)
+    refs = [_reference(A, p, s, b, act) for (_, A, b), (p, s) in zip(drawn, q)]
+    As = [A.cuda() for _, A, _ in drawn]
+    bs = [None if b is None else b.cuda() for _, _, b in drawn]
+    ps, ss = [p for p, _ in q], [s for _, s in q]
+    ran = 0
+    for v in range(w4.w4a16_variant_count()):
+        name = w4.w4a16_variant_name(v)
+        if not name.startswith("rb_") or not all(w4.w4a16_variant_eligible(v, c.M, c.N, c.K) for c in cases):
+            continue
+        Y1 = w4.w4a16_gemm_grouped(As, ps, ss, biases=bs, variant=v)
+        Y2 = w4.w4a16_gemm_grouped(As, ps, ss, biases=bs, variant=v)
+        torch.cuda.synchronize()
+        assert w4.w4a16_get_device_error() == w4.W4A16_OK, name
+        for c, ya, yb, ref in zip(cases, Y1, Y2, refs):
+            check_gemm_close(ya, ref, what=f"{name} {c.name} {act}")
+            assert torch.equal(ya.view(torch.int16), yb.view(torch.int16)), f"{name} {c.name}"
+        ran += 1
+    assert ran >= 1
+    Ys = w4.w4a16_gemm_grouped(As, ps, ss, biases=bs)
+    torch.cuda.synchronize()
+    assert w4.w4a16_get_device_error() == w4.W4A16_OK
+    for c, y, ref in zip(cases, Ys, refs):
+        check_gemm_close(y, ref, what=f"default plan {c.name} {act}")
+
+
 def test_grouped_expert_block_default_variant(w4):
     cases = synthetic.WORKLOADS["expert_m50"]
     drawn, q = _operands(w4, cases)

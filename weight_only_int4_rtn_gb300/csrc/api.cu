@@ -258,7 +258,11 @@ double rb_cost(const GemmSchedule& s, int64_t blocks, int64_t KB, int64_t slots,
   return worst;
 }
 
-GemmSchedule make_schedule(const Variant& v, int64_t M, int64_t N, int64_t K, int num_sms) {
+// single: the problem has the launch to itself (false: one problem of a
+// grouped launch, where the row-block kernel's cluster form, one cluster size
+// per launch, is not open).
+GemmSchedule make_schedule(const Variant& v, int64_t M, int64_t N, int64_t K, int num_sms,
+                           bool single = true) {
   GemmSchedule s{};
   if (v.cfg.rb) {
     // Items are (row block, group) pairs.  Persistent: the resident CTAs
@@ -285,7 +289,7 @@ GemmSchedule make_schedule(const Variant& v, int64_t M, int64_t N, int64_t K, in
         s = c;
       }
     }
-    for (int S = 2; S <= 8 && KB >= S * kRbWarpsPerCta; S *= 2) {
+    for (int S = 2; single && S <= 8 && KB >= S * kRbWarpsPerCta; S *= 2) {
       c.grid = static_cast<int>(blocks * S);
       c.team = kRbWarpsPerCta;
       c.cluster = S;
@@ -716,8 +720,8 @@ struct GroupPlan {
 // whole tiles only when that is estimated faster (every split tile pays the
 // fixup).
 GemmSchedule group_schedule(const Variant& v, const w4a16_gemm_problem& p, int ctas, double& est,
-                            bool own_only) {
-  GemmSchedule s = make_schedule(v, p.M, p.N, p.K, ctas);
+                            bool own_only, bool single) {
+  GemmSchedule s = make_schedule(v, p.M, p.N, p.K, ctas, single);
   est = estimate_sched(v, s, p.K, p.N, ctas);
   if (!own_only && v.stream_k && s.sk_units > 0) {
     const int64_t tiles = gemm_tiles(v.cfg, p.M, p.N);
@@ -741,7 +745,10 @@ GemmSchedule group_schedule(const Variant& v, const w4a16_gemm_problem& p, int c
 bool plan_for_variant(int id, const w4a16_gemm_problem* pr, int count, int sms, GroupPlan& plan,
                       bool forced) {
   const Variant& v = kVariants[id];
-  if ((v.cfg.simt || v.csk > 1) && count > 1) return false;   // single problems only
+  // single problems only: the CUDA-core workers and the cluster split-K
+  // variants (the row-block kernel groups problems in its persistent form;
+  // a share of `ctas` SMs runs up to two of its CTAs each)
+  if (((v.cfg.simt && !v.cfg.rb) || v.csk > 1) && count > 1) return false;
   for (int i = 0; i < count; ++i) {
     if (!variant_eligible(id, pr[i].M, pr[i].N, pr[i].K)) return false;
     if (pr[i].epilogue == W4A16_EPILOGUE_SWIGLU && !swiglu_ok(id)) return false;
@@ -751,7 +758,7 @@ bool plan_for_variant(int id, const w4a16_gemm_problem* pr, int count, int sms, 
   double est[kMaxGemmGroup];
   for (int i = 0; i < count; ++i) {
     ctas[i] = count == 1 ? sms : 1;
-    (void)group_schedule(v, pr[i], ctas[i], est[i], forced);
+    (void)group_schedule(v, pr[i], ctas[i], est[i], forced, count == 1);
   }
   // units per CTA fall in steps, so a problem may need several more CTAs
   // before its estimate improves: look ahead to the next improving count
@@ -763,7 +770,7 @@ bool plan_for_variant(int id, const w4a16_gemm_problem* pr, int count, int sms, 
       if (pick >= 0 && est[i] <= est[pick]) continue;
       for (int k = 1; used + k <= sms; ++k) {
         double e1;
-        (void)group_schedule(v, pr[i], ctas[i] + k, e1, forced);
+        (void)group_schedule(v, pr[i], ctas[i] + k, e1, forced, count == 1);
         if (e1 < est[i]) {
           pick = i;
           pick_k = k;
@@ -783,7 +790,7 @@ bool plan_for_variant(int id, const w4a16_gemm_problem* pr, int count, int sms, 
   bool split = false;
   for (int i = 0; i < count; ++i) {
     double e;
-    plan.s[i] = group_schedule(v, pr[i], ctas[i], e, forced);
+    plan.s[i] = group_schedule(v, pr[i], ctas[i], e, forced, count == 1);
     plan.est_us = std::max(plan.est_us, e);
     plan.partial_off[i] = off;
     if (plan.s[i].sk_units > 0) {

@@ -23,6 +23,9 @@
 // Cluster form, for shapes with few row blocks and long K: one CTA-wide team
 // per (row block, cluster rank), the K range split over the S CTAs of a
 // thread-block cluster and summed through distributed shared memory.
+// Grouped launches: up to 8 independent problems, problem p on its own
+// sub-grid of CTAs in the persistent form (one launch, one head, for the
+// projections of a decode step).
 //
 // Streaming.  Each warp owns a ring of two shared-memory stages (one item
 // each) whose copies complete on a per-stage mbarrier, so the next item is
@@ -95,6 +98,15 @@ struct RbArgs {
                            // grid-dependency wait
   uint32_t* err;           // device error word
   uint64_t timeout_ns;     // limit of one wait
+};
+
+// A launch: G problems, problem p on CTAs cta_start[p] .. cta_start[p+1]-1
+// (G = 1: a single problem; the cluster form only then).
+template <int G>
+struct RbLaunch {
+  RbArgs p[G];
+  int cta_start[G + 1];
+  int count;
 };
 
 // MT: activation rows (M <= MT; the MMA's 8 columns).  An item holds up to
@@ -175,10 +187,18 @@ struct RbWalk {
   }
 };
 
-template <int MT, bool F16>
+template <int MT, bool F16, int G>
 __global__ void __launch_bounds__(kRbWarps * 32, kRbCtasPerSm)
-    gemv_rb_kernel(const __grid_constant__ RbArgs g) {
+    gemv_rb_kernel(const __grid_constant__ RbLaunch<G> L) {
   using C = RbCfg<MT>;
+  // this CTA's problem and its index in the problem's sub-grid
+  int prob = 0;
+  if constexpr (G > 1) {
+    while (prob + 1 < L.count && static_cast<int>(blockIdx.x) >= L.cta_start[prob + 1]) ++prob;
+  }
+  const RbArgs& g = L.p[prob];
+  const int cta = static_cast<int>(blockIdx.x) - L.cta_start[prob];
+  const int ctas = L.cta_start[prob + 1] - L.cta_start[prob];
   constexpr int D = C::kDepth;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
@@ -198,14 +218,14 @@ __global__ void __launch_bounds__(kRbWarps * 32, kRbCtasPerSm)
   // one team on one row block and its rank takes a share of K
   int T, TT, rank = 0, cg0 = 0, cg1 = g.KB;
   if (S > 1) {
-    T = static_cast<int>(blockIdx.x) / S;
-    rank = static_cast<int>(blockIdx.x) - T * S;
+    T = cta / S;
+    rank = cta - T * S;
     TT = g.NB;
     cg0 = (rank * g.KB) / S;
     cg1 = ((rank + 1) * g.KB) / S;
   } else {
-    T = static_cast<int>(blockIdx.x) * tpc + team;
-    TT = static_cast<int>(gridDim.x) * tpc;
+    T = cta * tpc + team;
+    TT = ctas * tpc;
   }
   const int k0 = cg0 + (wt * (cg1 - cg0)) / WK;
   const int k1 = cg0 + ((wt + 1) * (cg1 - cg0)) / WK;
@@ -522,8 +542,10 @@ __global__ void __launch_bounds__(kRbWarps * 32, kRbCtasPerSm)
   }
 }
 
+// One problem's kernel arguments under schedule s (false: the problem or
+// the schedule is not one this kernel runs).
 template <int MT, bool F16>
-cudaError_t launch_rb(const GemmProblem& p, const GemmSchedule& s, bool use_pdl, cudaStream_t stream) {
+bool rb_args(const GemmProblem& p, const GemmSchedule& s, RbArgs& g) {
   using C = RbCfg<MT>;
   const int64_t blocks = (p.N + kRbRows - 1) / kRbRows;
   const int S = s.cluster > 1 ? s.cluster : 1;
@@ -533,8 +555,8 @@ cudaError_t launch_rb(const GemmProblem& p, const GemmSchedule& s, bool use_pdl,
   // per row block
   if (p.M > MT || S > 8 || (WK != 1 && WK != 2 && WK != 4 && WK != 8) || KB < WK * S ||
       (S > 1 && (WK != kRbWarps || s.grid != blocks * S)) || s.grid < 1)
-    return cudaErrorInvalidValue;
-  RbArgs g{};
+    return false;
+  g = RbArgs{};
   g.A = static_cast<const uint16_t*>(p.A);
   g.packed = static_cast<const uint8_t*>(p.packed);
   g.scales = static_cast<const __half*>(p.scales);
@@ -557,9 +579,28 @@ cudaError_t launch_rb(const GemmProblem& p, const GemmSchedule& s, bool use_pdl,
         F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     if (encode_tmap_2d(&g.amap, kActType, p.A, p.K, p.M, p.K * 2, C::kActRow / 2, MT,
                        CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
+      return false;
   }
-  auto kernel = gemv_rb_kernel<MT, F16>;
+  return true;
+}
+
+template <int MT, bool F16, int G>
+cudaError_t launch_rb(const GemmGroup& grp, bool use_pdl, cudaStream_t stream) {
+  using C = RbCfg<MT>;
+  if (grp.count < 1 || grp.count > G) return cudaErrorInvalidValue;
+  RbLaunch<G> L{};
+  L.count = grp.count;
+  int total = 0;
+  for (int i = 0; i < grp.count; ++i) {
+    if (!rb_args<MT, F16>(grp.p[i], grp.s[i], L.p[i])) return cudaErrorInvalidValue;
+    // the cluster form (one cluster size per launch) takes a single problem
+    if (grp.count > 1 && L.p[i].cluster > 1) return cudaErrorInvalidValue;
+    L.cta_start[i] = total;
+    total += grp.s[i].grid;
+  }
+  L.cta_start[grp.count] = total;
+  const int S = L.p[0].cluster;
+  auto kernel = gemv_rb_kernel<MT, F16, G>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -571,7 +612,7 @@ cudaError_t launch_rb(const GemmProblem& p, const GemmSchedule& s, bool use_pdl,
     attr_set[dev] = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(s.grid));
+  cfg.gridDim = dim3(static_cast<unsigned>(total));
   cfg.blockDim = dim3(kRbWarps * 32);
   cfg.dynamicSmemBytes = C::kSmem;
   cfg.stream = stream;
@@ -591,7 +632,13 @@ cudaError_t launch_rb(const GemmProblem& p, const GemmSchedule& s, bool use_pdl,
   }
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, kernel, g);
+  return cudaLaunchKernelEx(&cfg, kernel, L);
+}
+
+template <int MT, bool F16>
+cudaError_t launch_rb_any(const GemmGroup& grp, bool use_pdl, cudaStream_t stream) {
+  return grp.count == 1 ? launch_rb<MT, F16, 1>(grp, use_pdl, stream)
+                        : launch_rb<MT, F16, kMaxGemmGroup>(grp, use_pdl, stream);
 }
 
 }  // namespace
@@ -618,16 +665,17 @@ size_t gemv_rb_smem_bytes(int act_tile) {
 
 cudaError_t launch_gemv_rb(const GemmKernelConfig& c, const GemmGroup& grp, bool use_pdl,
                            cudaStream_t stream) {
-  if (grp.count != 1) return cudaErrorInvalidValue;
-  const GemmProblem& p = grp.p[0];
-  const GemmSchedule& s = grp.s[0];
-  if (p.swiglu) return cudaErrorInvalidValue;   // the fused epilogue is the tcgen05 path's
-  const bool f16 = p.act_f16;
+  if (grp.count < 1 || grp.count > kMaxGemmGroup) return cudaErrorInvalidValue;
+  for (int i = 0; i < grp.count; ++i) {
+    // the fused epilogue is the tcgen05 path's; one activation type a launch
+    if (grp.p[i].swiglu || grp.p[i].act_f16 != grp.p[0].act_f16) return cudaErrorInvalidValue;
+  }
+  const bool f16 = grp.p[0].act_f16;
   switch (c.act_tile) {
-    case 1: return f16 ? launch_rb<1, true>(p, s, use_pdl, stream) : launch_rb<1, false>(p, s, use_pdl, stream);
-    case 2: return f16 ? launch_rb<2, true>(p, s, use_pdl, stream) : launch_rb<2, false>(p, s, use_pdl, stream);
-    case 4: return f16 ? launch_rb<4, true>(p, s, use_pdl, stream) : launch_rb<4, false>(p, s, use_pdl, stream);
-    case 8: return f16 ? launch_rb<8, true>(p, s, use_pdl, stream) : launch_rb<8, false>(p, s, use_pdl, stream);
+    case 1: return f16 ? launch_rb_any<1, true>(grp, use_pdl, stream) : launch_rb_any<1, false>(grp, use_pdl, stream);
+    case 2: return f16 ? launch_rb_any<2, true>(grp, use_pdl, stream) : launch_rb_any<2, false>(grp, use_pdl, stream);
+    case 4: return f16 ? launch_rb_any<4, true>(grp, use_pdl, stream) : launch_rb_any<4, false>(grp, use_pdl, stream);
+    case 8: return f16 ? launch_rb_any<8, true>(grp, use_pdl, stream) : launch_rb_any<8, false>(grp, use_pdl, stream);
     default: return cudaErrorInvalidConfiguration;
   }
 }
