@@ -458,8 +458,9 @@ def grouped_back_to_back(w4, cases, epilogues, peaks, tune, dev):
 
     from weight_only_int4_rtn_gb300 import synthetic
     shapes = [(c.M, c.N, c.K, e) for c, e in zip(cases, epilogues)]
+    vname = None
     if tune:
-        w4.w4a16_tune_grouped(shapes)
+        vname = w4.w4a16_variant_name(w4.w4a16_tune_grouped(shapes))
     drawn = [synthetic.draw(c) for c in cases]
     q = w4.w4a16_quantize_grouped([W.to(dev) for W, _, _ in drawn])
     torch.cuda.synchronize(dev)   # weights complete before any GEMM may read them early
@@ -490,7 +491,7 @@ def grouped_back_to_back(w4, cases, epilogues, peaks, tune, dev):
     t_tc = flops / (peaks["bf16_tflops"] * 1e12) * 1e6
     return dict(shapes=[[c.M, c.N, c.K] for c in cases], epilogues=["swiglu" if e else "none"
                                                                     for e in epilogues],
-                us=round(us, 3), gbs=round(byts / (us * 1e-6) / 1e9, 1),
+                variant=vname, us=round(us, 3), gbs=round(byts / (us * 1e-6) / 1e9, 1),
                 tflops=round(flops / (us * 1e-6) / 1e12, 2),
                 bound="hbm" if t_hbm >= t_tc else "tensor",
                 roofline_frac=round(max(t_hbm, t_tc) / us, 4), weight_copies=ncp)
@@ -862,6 +863,12 @@ def run_gpu(args, rank, world):
         block = [grouped_back_to_back(w4, ex, [0] * len(ex), peaks, args.tune, dev),
                  grouped_back_to_back(w4, ex, [1 if "gate_up" in c.name else 0 for c in ex],
                                       peaks, args.tune, dev)]
+        # the same projections at decode sizes (M = 1 and 4): one grouped
+        # launch, whose plan may take the row-block kernel
+        import dataclasses
+        for m in (1, 4):
+            dec = [dataclasses.replace(c, M=m, name=c.name.replace("m50", f"m{m}")) for c in ex]
+            block.append(grouped_back_to_back(w4, dec, [0] * len(dec), peaks, args.tune, dev))
     if w4.w4a16_get_device_error() != w4.W4A16_OK:
         raise RuntimeError("device error during the back-to-back GEMM timing")
 
