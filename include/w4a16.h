@@ -232,8 +232,10 @@ int w4a16_gemm_swiglu_variant(int variant, const void* A_bf16, int64_t M, int64_
  * Families: tc_* the tcgen05/TMEM GEMM (group or dequant mode, whole-tile,
  * stream-K or cluster split-K (*_csk) schedules); rb_m1, rb_m2, rb_m4, rb_m8
  * the row-block warp-MMA kernel for M <= 1, 2, 4, 8; simt_m*_sk the CUDA-core
- * stream-K workers for M <= 1, 2, 4, 8.  The streaming and cluster split-K
- * variants run single problems only and have no SwiGLU form. */
+ * stream-K workers for M <= 1, 2, 4, 8.  None of the streaming and cluster
+ * split-K variants has a SwiGLU form; the CUDA-core workers and the cluster
+ * split-K variants run single problems only, the row-block kernel also
+ * grouped launches (in its persistent form). */
 
 /* Number of variants in the catalogue; ids are 0 .. count-1. */
 int w4a16_variant_count(void);
@@ -391,8 +393,9 @@ size_t w4a16_gemm_grouped_workspace_bytes(const w4a16_gemm_problem* problems, in
  * only: W4A16_ERR_UNSUPPORTED with act_f16, an odd N or another epilogue
  * value), so an MLP block's gate/up projection runs in the same launch as
  * its other projections.  One variant serves the whole group (variant = -1:
- * chosen by the library).  Argument errors of any problem are returned
- * before anything is launched. */
+ * chosen by the library; at M <= 8 without epilogues the plan may take the
+ * row-block kernel, each problem on its own sub-grid).  Argument errors of
+ * any problem are returned before anything is launched. */
 int w4a16_gemm_grouped(const w4a16_gemm_problem* problems, int count, int group, int act_f16,
                        int variant, void* workspace, size_t workspace_bytes, void* stream);
 
