@@ -175,6 +175,8 @@ const Variant kVariants8[] = {
     {"w8_tc_a128_deq_dp", {128, 1, false, 4, 1, 8}, false, 1, 0.78},
     {"w8_tc_a256_deq_sk", {256, 1, false, 2, 1, 8}, true, 1, 1.36},
     {"w8_tc_a256_deq_dp", {256, 1, false, 2, 1, 8}, false, 1, 1.49},
+    // split rings (stages = 2 activation stages + 32 x 4 code stages)
+    {"w8_tc_a256_deq_w4_sk", {256, 1, false, 130, 1, 8}, true, 1, 1.3},
 };
 constexpr int kNumVariants8 = static_cast<int>(sizeof(kVariants8) / sizeof(kVariants8[0]));
 

@@ -318,7 +318,10 @@ __device__ __forceinline__ int sk_owner(int u, int C, int sk_units) {
 }
 
 struct Shared {
-  uint64_t full[16];          // a shared-memory stage's copies landed
+  uint64_t full[16];          // a shared-memory stage's copies landed (split
+                              // rings: the activation stage's)
+  uint64_t wfull[16];         // split rings: a code stage's copies landed
+  uint64_t wempty[16];        // split rings: the dequant read a code stage
   uint64_t afull[kMaxAStages];   // a TMEM weight stage is written (it is free
                                  // again when its unit's MMAs completed)
   uint64_t unit_done[32];     // per lane a ring: a unit's MMAs completed
@@ -481,8 +484,27 @@ struct Cfg {
   static constexpr int kSOff = kWOff + UG * kWB;
   static constexpr int kStageRaw = UG * (2 * kActBox + kWB + kSB);
   static constexpr int kStage = (kStageRaw + 1023) / 1024 * 1024;
+  // STAGES >= 32 (dequant mode, one lane, INT8): split rings.  The codes and
+  // scales take a ring of their own, STAGES / 32 stages deep, released as
+  // soon as the dequant has read a unit's codes, and the activations one of
+  // STAGES % 32 stages, released by the unit's MMAs: where the combined
+  // stages are few (8-bit codes beside a 256-wide activation tile), the
+  // dequant runs further ahead of the MMAs.
+  static constexpr int kCodeStages = STAGES / 32;
+  static constexpr bool kSplit = kCodeStages > 0;
+  static constexpr int kActStages = STAGES % 32;
+  static constexpr int kActStage = (2 * UG * kActBox + 1023) / 1024 * 1024;
+  static constexpr int kCodeStage = (UG * (kWB + kSB) + 1023) / 1024 * 1024;
+  static constexpr int kActStride = kSplit ? kActStage : kStage;  // act stage to stage
+  static constexpr int kWStride = kSplit ? kCodeStage : kStage;   // code stage to stage
+  static constexpr int kWBase = kSplit ? kActStages * kActStage : kWOff;   // code stage 0
+  static constexpr int kSRel = kSplit ? UG * kWB : kSOff - kWOff;  // scales after the codes
+  static constexpr int kRing = kSplit ? kActStages * kActStage + kCodeStages * kCodeStage
+                                      : STAGES * kStage;
+  static constexpr uint32_t kTxAct = 2 * UG * kActBox;
+  static constexpr uint32_t kTxCode = UG * (kWB + kSB);
   static constexpr int kThreads = 32 * kWarps;                    // 16 warps: <= 128 registers
-  static constexpr int kSL = STAGES / L;                          // shared-memory stages per lane
+  static constexpr int kSL = kActStages / L;                      // shared-memory stages per lane
   // TMEM: kAS weight stages of 64 columns, then the accumulators.  The
   // narrowest group-mode tile needs few accumulator columns, so it takes
   // three weight stages per lane (the dequant runs further ahead).
@@ -499,7 +521,7 @@ struct Cfg {
   static constexpr int kDL = GRP ? kDB / L : kDB;                 // buffers a lane cycles through
   static constexpr int kRL = kSL > kAL ? kSL : kAL;               // unit_done ring per lane
   static constexpr int kChunk = BA < (GRP ? 16 : 32) ? BA : (GRP ? 16 : 32);
-  static constexpr size_t kSmem = static_cast<size_t>(STAGES) * kStage + 1024 + sizeof(Shared) +
+  static constexpr size_t kSmem = static_cast<size_t>(kRing) + 1024 + sizeof(Shared) +
                                   (GRP ? kScaleRing * UG * kTileW * 2 : 0);
   static constexpr uint32_t kTx = kStageRaw;
   static_assert(BA % 16 == 0 && BA >= 16 && BA <= 256, "tcgen05 N for M=128");
@@ -508,12 +530,16 @@ struct Cfg {
   static_assert(WF == kFmtInt4 || WF == kFmtInt8 || wf_fp4(WF), "weight format");
   static_assert(!wf_fp4(WF) || !GRP, "FP4 weights run in dequant mode (block scales inside a group)");
   static_assert(kAS % L == 0 && kAS <= kMaxAStages, "TMEM weight stages split over the lanes");
-  static_assert(STAGES % L == 0 && STAGES <= 16, "stages split over the lanes");
+  static_assert(kActStages % L == 0 && kActStages >= 1 && kActStages <= 16, "stages split over the lanes");
+  static_assert(!kSplit || (!GRP && L == 1 && WF == kFmtInt8 && kCodeStages % 2 == 0 &&
+                            kCodeStages <= 16),
+                "split rings: dequant mode, one lane, INT8, an even code ring (the two dequant "
+                "warpgroups alternate units)");
   static_assert(kDB >= 1 && kDL >= 1 && (!GRP || kDB % L == 0), "accumulators split over the lanes");
   static_assert(kDB <= 8, "barrier arrays");
   static_assert(L * kRL <= 32, "barrier arrays");
   static_assert(!GRP || BA <= 64, "group mode keeps BA fp32 accumulators per thread");
-  static_assert(BA * kTileW * 4 <= STAGES * kStage, "cluster split-K partial fits the stages");
+  static_assert(BA * kTileW * 4 <= kRing, "cluster split-K partial fits the stages");
   static_assert(!GRP || L == 2, "group mode runs two lanes (the readout takes units in pairs)");
   // group mode: the pair ring replaces the unit ring for every waiter, so
   // it must be as deep as the stage rings and the accumulator buffers
@@ -856,20 +882,22 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG, WF>::kThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  Shared* sh = reinterpret_cast<Shared*>(smem + STAGES * C::kStage);
+  Shared* sh = reinterpret_cast<Shared*>(smem + C::kRing);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
+  // activation boxes of a stage; codes and scales of a stage (split rings:
+  // of a code stage)
   auto act_box = [&](int stage, int box) -> uint8_t* {
-    return smem + stage * C::kStage + box * C::kActBox;
+    return smem + stage * C::kActStride + box * C::kActBox;
   };
-  auto w_tile = [&](int stage) -> uint8_t* { return smem + stage * C::kStage + C::kWOff; };
+  auto w_tile = [&](int stage) -> uint8_t* { return smem + C::kWBase + stage * C::kWStride; };
   auto s_tile = [&](int stage, int gi) -> __half* {
-    return reinterpret_cast<__half*>(smem + stage * C::kStage + C::kSOff + gi * C::kSB);
+    return reinterpret_cast<__half*>(w_tile(stage) + C::kSRel + gi * C::kSB);
   };
   // FP4: block-scale bytes of group gi of a stage, [block][128 rows]
   auto s_bytes = [&](int stage, int gi) -> const uint8_t* {
-    return smem + stage * C::kStage + C::kSOff + gi * C::kSB;
+    return w_tile(stage) + C::kSRel + gi * C::kSB;
   };
   // Resources of unit i (lane p, index j in the lane): the lanes own
   // interleaved shared-memory stages, TMEM weight stages and accumulators.
@@ -881,6 +909,8 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG, WF>::kThreads, 1)
   // TMEM weight stages go round per group: group jg of lane p's groups
   // (jg = UG * j + gi for group gi of the lane's unit j).
   auto gstage_of = [&](int p, int jg) -> int { return p + L * (jg % AL); };
+  // split rings (one lane): the code stage of unit i
+  auto wstage_of = [&](int i) -> int { return C::kSplit ? i % (C::kCodeStages > 0 ? C::kCodeStages : 1) : 0; };
   // Completion of unit i's MMAs.  Group mode: the pair ring (lane 0's and
   // lane 1's j-th units complete together, one arrival each); one lane:
   // the unit ring.
@@ -909,8 +939,11 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG, WF>::kThreads, 1)
     // of them in turn costs several hundred cycles of the launch's head)
     const int t = static_cast<int>(threadIdx.x);
     bool init = true;
-    if (t < STAGES) {
+    if (t < C::kActStages) {
       ptx::mbar_init(&sh->full[t], 1);
+    } else if (C::kSplit && t >= 224 && t < 224 + C::kCodeStages) {
+      ptx::mbar_init(&sh->wfull[t - 224], 1);
+      ptx::mbar_init(&sh->wempty[t - 224], 4);   // the 4 warps of a dequant warpgroup
     } else if (t >= 32 && t < 32 + L * RL) {
       ptx::mbar_init(&sh->unit_done[t - 32], 1);
     } else if (t >= 64 && t < 64 + C::kAS) {
@@ -1002,7 +1035,11 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG, WF>::kThreads, 1)
           const int m0 = mt * BA;
           const int wrow0 = tn * a.KB * UG * kTileW;
           const int sx = tn * kTileW;
-          for (int i = i0 + ((i0 & 1) != mine ? 1 : 0); i < i0 + len && i < limit; i += 2) {
+          // split rings: one producer walks every unit (warp 0 the codes,
+          // warp 2 the activations); else even units from warp 0, odd from 2
+          constexpr int kStep = C::kSplit ? 1 : 2;
+          for (int i = i0 + (!C::kSplit && (i0 & 1) != mine ? 1 : 0); i < i0 + len && i < limit;
+               i += kStep) {
             const int g0 = (kb0 + i - i0) * UG;   // the unit's first group
             if (!fn(i, m0, wrow0 + g0 * kTileW, sx, g0)) return false;
           }
@@ -1026,6 +1063,75 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG, WF>::kThreads, 1)
             ptx::tma_load_2d(act_box(stage, b), tm_act, &sh->full[stage], g0 * kUnitK + 64 * b, m0);
         }
       };
+      if constexpr (C::kSplit) {
+        if (warp == 0) {
+          // codes and scales of every unit into the code ring; with static
+          // weights the whole ring is requested before the dependency wait
+          auto issue_c = [&](int i, int wrow, int sx, int g0) {
+            const int ws = wstage_of(i);
+            ptx::mbar_arrive_expect_tx(&sh->wfull[ws], C::kTxCode);
+            ptx::tma_load_2d(w_tile(ws), tm_w, &sh->wfull[ws], 0, wrow);
+            ptx::tma_load_2d(s_tile(ws, 0), tm_s, &sh->wfull[ws], sx, g0 * wf_blocks(WF));
+          };
+          const int npre = a.prefetch_w > 0 ? C::kCodeStages : 0;
+          if (npre > 0) {
+            walk(npre, [&](int i, int, int wrow, int sx, int g0) {
+              issue_c(i, wrow, sx, g0);
+              issued = i;
+              return true;
+            });
+          }
+          ptx::grid_dependency_wait();
+          ptx::grid_launch_dependents();
+          walk(total, [&](int i, int, int wrow, int sx, int g0) {
+            if (i < npre) return true;
+            // the stage's previous unit (i - kCodeStages) was read by the dequant
+            if (i >= C::kCodeStages &&
+                !wait_one(&sh->wempty[wstage_of(i)], static_cast<uint32_t>((i / C::kCodeStages) - 1) & 1u,
+                          wc))
+              return false;
+            issue_c(i, wrow, sx, g0);
+            W4A16_TRACE_UNIT(0, i);
+            issued = i;
+            return true;
+          });
+          if (*reinterpret_cast<volatile int*>(&sh->abort_flag)) {
+            // this producer's copies still in flight land before the CTA exits
+            for (int i = issued; i >= 0 && i > issued - C::kCodeStages; --i) {
+              const uint64_t t0 = ptx::globaltimer_ns();
+              while (!ptx::mbar_try_wait(&sh->wfull[wstage_of(i)],
+                                         static_cast<uint32_t>(i / C::kCodeStages) & 1u)) {
+                if (ptx::globaltimer_ns() - t0 > a.timeout_ns) break;
+              }
+            }
+          }
+        } else {
+          // activations of every unit into the activation ring; a stage is
+          // free once the MMAs of its previous unit completed
+          ptx::grid_dependency_wait();
+          ptx::grid_launch_dependents();
+          walk(total, [&](int i, int m0, int, int, int g0) {
+            const int stage = stage_of(i);
+            if (i >= C::kActStages &&
+                !wait_one(done_bar(i - C::kActStages), done_parity(i - C::kActStages), wc))
+              return false;
+            ptx::mbar_arrive_expect_tx(&sh->full[stage], C::kTxAct);
+            issue_a(stage, m0, g0);
+            if (i <= 1) W4A16_TRACE_POINT(3);
+            issued = i;
+            return true;
+          });
+          if (*reinterpret_cast<volatile int*>(&sh->abort_flag)) {
+            for (int i = issued; i >= 0 && i > issued - C::kActStages; --i) {
+              const uint64_t t0 = ptx::globaltimer_ns();
+              while (!ptx::mbar_try_wait(&sh->full[stage_of(i)],
+                                         static_cast<uint32_t>(i / C::kActStages) & 1u)) {
+                if (ptx::globaltimer_ns() - t0 > a.timeout_ns) break;
+              }
+            }
+          }
+        }
+      } else {
       // a shallow prefetch: the copies of one TMA unit run in order, so every
       // early weight copy sits ahead of the first activation copy
       const int npre = a.prefetch_w < STAGES ? a.prefetch_w : STAGES;
@@ -1065,6 +1171,7 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG, WF>::kThreads, 1)
           }
         }
       }
+      }
     }
   } else if (warp == 1 || (L == 2 && warp == kMmaWarp2)) {
     // ------------------------------------------------------- MMA issuers
@@ -1082,7 +1189,7 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG, WF>::kThreads, 1)
         for (int j = 0; j < nj && ok; ++j) {
           const int stage = mine + 2 * (j % SL);
           const int dl = j % DL;
-          const uint32_t b0 = smem0 + stage * C::kStage;
+          const uint32_t b0 = smem0 + stage * C::kActStride;
 #pragma unroll
           for (int gi = 0; gi < UG; ++gi) {
             const int jg = UG * j + gi;
@@ -1144,10 +1251,15 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG, WF>::kThreads, 1)
           lane_split<L>(i, p, j);
           if (p == mine) {
             const int stage = stage_of(i);
-            const uint32_t b0 = smem0 + stage * C::kStage;
+            const uint32_t b0 = smem0 + stage * C::kActStride;
             const uint32_t d_tmem = tmem + C::kDCol + (db * L + mine) * BA;
             W4A16_TRACE_UNIT(8, i);
             bool ok = true;
+            // split rings: the activations have a barrier of their own (the
+            // dequant's arrival covers only the codes)
+            if constexpr (C::kSplit) {
+              if (!wait_one(&sh->full[stage], static_cast<uint32_t>(j / SL) & 1u, wc)) break;
+            }
 #pragma unroll
             for (int gi = 0; gi < UG; ++gi) {
               const int jg = UG * j + gi;
@@ -1448,8 +1560,9 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG, WF>::kThreads, 1)
     for (int i = wg; i < total; i += 2) {
       int p, j;
       lane_split<L>(i, p, j);
-      const int stage = stage_of(i);
-      if constexpr (L == 1 && (STAGES & 1) != 0) {
+      // the stage holding unit i's codes (split rings: its code stage)
+      const int stage = C::kSplit ? wstage_of(i) : stage_of(i);
+      if constexpr (!C::kSplit && L == 1 && (STAGES & 1) != 0) {
         // With an odd stage count the uses of one stage alternate between
         // the two warpgroups, so this warpgroup did not see the stage's
         // previous phase (unit i - STAGES, the other warpgroup's), and a
@@ -1459,7 +1572,11 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG, WF>::kThreads, 1)
         if (i >= STAGES && !wait_warp(done_bar(i - STAGES), done_parity(i - STAGES), wc)) break;
       }
       if (threadIdx.x == 32 * kDequantWarp0) W4A16_TRACE_UNIT(25, i);
-      if (!wait_warp(&sh->full[stage], (j / SL) & 1, wc)) break;
+      if constexpr (C::kSplit) {
+        if (!wait_warp(&sh->wfull[stage], static_cast<uint32_t>(i / C::kCodeStages) & 1u, wc)) break;
+      } else {
+        if (!wait_warp(&sh->full[stage], (j / SL) & 1, wc)) break;
+      }
       if (i == 0 && threadIdx.x == 32 * kDequantWarp0) W4A16_TRACE_POINT(6);
       if (threadIdx.x == 32 * kDequantWarp0) W4A16_TRACE_UNIT(1, i);
       bool ok = true;
@@ -1467,7 +1584,7 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG, WF>::kThreads, 1)
       uint32_t words[UG][4 * kChunks];
 #pragma unroll
       for (int gi = 0; gi < UG; ++gi) {
-        const uint32_t wrow = wrow0 + stage * C::kStage + gi * C::kWB;
+        const uint32_t wrow = wrow0 + stage * C::kWStride + gi * C::kWB;
 #pragma unroll
         for (int q = 0; q < kChunks; ++q) {
           const uint4 v = ptx::lds128(wrow + ((q ^ swz) << 4));
@@ -1476,6 +1593,15 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG, WF>::kThreads, 1)
           words[gi][4 * q + 2] = v.z;
           words[gi][4 * q + 3] = v.w;
         }
+      }
+      // split rings: the row's scales too, then the code stage goes back to
+      // the producer (the values are in registers)
+      __half sv[UG];
+      if constexpr (C::kSplit) {
+#pragma unroll
+        for (int gi = 0; gi < UG; ++gi) sv[gi] = s_tile(stage, gi)[row];
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&sh->wempty[stage]);
       }
       if (threadIdx.x == 32 * kDequantWarp0) W4A16_TRACE_UNIT(16, i);
 #pragma unroll
@@ -1502,7 +1628,7 @@ __global__ void __launch_bounds__(Cfg<BA, L, GRP, STAGES, UG, WF>::kThreads, 1)
         if constexpr (wf_fp4(WF)) {
           // the block scales are read per block below
         } else if constexpr (!GRP && WF == kFmtInt8) {
-          s_w8 = __half2float(s_tile(stage, gi)[row]);
+          s_w8 = __half2float(C::kSplit ? sv[gi] : s_tile(stage, gi)[row]);
         } else if constexpr (!GRP) {
           if constexpr (F16) {
             // fp16 operand: fp16_rn(q * s) is one fused multiply-add (q and
@@ -1749,7 +1875,8 @@ cudaError_t launch_instance(const GemmGroup& grp, bool use_pdl, cudaStream_t str
   X(32, 2, true, 8, 1)          \
   X(64, 2, false, 6, 1)         \
   X(128, 1, false, 4, 1)        \
-  X(256, 1, false, 2, 1)
+  X(256, 1, false, 2, 1)        \
+  X(256, 1, false, 130, 1)
 
 // FP4 weights (MXFP4 or NVFP4, bf16 activations, single problems; dequant
 // mode only): {act_tile, lanes, group_scale, stages, unit_groups}.
