@@ -973,7 +973,7 @@ def time_oracle(workload, budget_s: float, weights="int4", rows=1024):
               + (f" on the first {rows} rows of A" if sampled else "")
               + "; weights quantized once by the oracle beforehand (load time, untimed)")
     return dict(value=round(flops / dt / 1e12, 6), unit="TFLOP/s", cores=cores, kind="oracle",
-                sample=sample, seconds=round(dt, 2))
+                sample=sample, seconds=round(dt, 2), passes=passes)
 
 
 def main():
@@ -1027,8 +1027,11 @@ def main():
         # each step a bounded sample of the workload: about 1.2 s of oracle work
         t_budget = max(5.0, min(90.0, 1.2 * (args.steps + args.warmup)))
         cb = time_oracle(workload_cases(args), t_budget, args.weights)
+        # a step of this arm is one sampled pass of the oracle (see the sample)
         line = dict(metric=METRIC, value=cb["value"], unit="TFLOP/s", n_gpus=world,
-                    steps=args.steps, warmup=args.warmup, ms_per_step=None, higher_is_better=True,
+                    steps=args.steps, warmup=args.warmup,
+                    ms_per_step=round(cb["seconds"] * 1e3 / max(cb["passes"], 1), 3),
+                    higher_is_better=True,
                     scaling="weak", vs_baseline=None, dtype="f32", data="synthetic",
                     impl="reference",
                     config=dict(workload=args.workload if not args.shape else "shape " + args.shape,
