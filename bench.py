@@ -391,7 +391,7 @@ def time_graph_us(dev, g, reps, trials=20):
 
 def back_to_back(fx, c, peaks, wcache, tune, dev, swiglu=False):
     """One GEMM shape alone: a CUDA graph of back-to-back launches on weight
-    copies that rotate through more than 3x L2 (SURVEY's timing method), no
+    copies that rotate through more than 3x L2 (every launch reads from HBM), no
     other kernel in between, against the roofline of the shape.  swiglu: the
     same weights through w4a16_gemm_swiglu (rows read as interleaved up/gate
     pairs, Y of [M, N/2]), its variant chosen by its own tuner."""
