@@ -202,7 +202,7 @@ int w4a16_gemm_f16(const void* A_f16, int64_t M, int64_t N, int64_t K, const voi
  * packed layout, alignment and workspace rules are w4a16_gemm's; workspace
  * bytes from w4a16_gemm_swiglu_workspace_bytes.  The variant is the SwiGLU
  * table's (w4a16_tune_swiglu), else the one w4a16_select_variant gives unless
- * that is a streaming variant for M <= 8 (simt_*, rb_*) or a cluster split-K
+ * that is a streaming variant for M <= 16 (simt_*, rb_*) or a cluster split-K
  * variant (*_csk), whose epilogues have no SwiGLU form: then the rule's best
  * tcgen05 variant that has one.  1 launch on `stream`.
  */
@@ -230,8 +230,8 @@ int w4a16_gemm_swiglu_variant(int variant, const void* A_bf16, int64_t M, int64_
  * PhyAI", section "Keep selection work out of repeated inference".  A shape
  * with no entry uses a fixed rule; both only ever choose GPU variants.
  * Families: tc_* the tcgen05/TMEM GEMM (group or dequant mode, whole-tile,
- * stream-K or cluster split-K (*_csk) schedules); rb_m1, rb_m2, rb_m4, rb_m8
- * the row-block warp-MMA kernel for M <= 1, 2, 4, 8; simt_m*_sk the CUDA-core
+ * stream-K or cluster split-K (*_csk) schedules); rb_m1, rb_m2, rb_m4, rb_m8,
+ * rb_m16 the row-block warp-MMA kernel for M <= 1, 2, 4, 8, 16; simt_m*_sk the CUDA-core
  * stream-K workers for M <= 1, 2, 4, 8.  None of the streaming and cluster
  * split-K variants has a SwiGLU form; the CUDA-core workers and the cluster
  * split-K variants run single problems only, the row-block kernel also
@@ -393,7 +393,7 @@ size_t w4a16_gemm_grouped_workspace_bytes(const w4a16_gemm_problem* problems, in
  * only: W4A16_ERR_UNSUPPORTED with act_f16, an odd N or another epilogue
  * value), so an MLP block's gate/up projection runs in the same launch as
  * its other projections.  One variant serves the whole group (variant = -1:
- * chosen by the library; at M <= 8 without epilogues the plan may take the
+ * chosen by the library; at M <= 16 without epilogues the plan may take the
  * row-block kernel, each problem on its own sub-grid).  Argument errors of
  * any problem are returned before anything is launched. */
 int w4a16_gemm_grouped(const w4a16_gemm_problem* problems, int count, int group, int act_f16,

@@ -102,12 +102,13 @@ def test_workloads_f16_default_variant(w4, case):
     check_gemm_close(Y, reference(A, packed, scales, b), what=case.name + " f16")
 
 
-@pytest.mark.parametrize("M", [1, 3, 5])
+@pytest.mark.parametrize("M", [1, 3, 5, 12, 16])
 def test_integer_exact_f16_small_m(w4, M):
-    # as test_integer_exact_f16 at M = 1, 3, 5: the streaming variants for
-    # M <= 8 (the row-block kernel's fp16 MMAs on 1032 + q and 1152 + 16 q,
-    # less their offsets times the activation sums, the second class scaled
-    # by 1/16) return the exact sum rounded once to fp16
+    # as test_integer_exact_f16 at M = 1, 3, 5, 12, 16: the streaming
+    # variants for M <= 16 (the row-block kernel's fp16 MMAs on 1032 + q and
+    # 1152 + 16 q, less their offsets times the activation sums, the second
+    # class scaled by 1/16; two column tiles above M = 8) return the exact
+    # sum rounded once to fp16
     rng = np.random.default_rng(33 + M)
     N, K = 264, 1024
     codes = rng.integers(-3, 4, size=(N, K))
@@ -130,4 +131,4 @@ def test_integer_exact_f16_small_m(w4, M):
         torch.cuda.synchronize()
         assert np.array_equal(bits(Y), expected), name
         ran += 1
-    assert ran >= (4 if M <= 2 else 2)
+    assert ran >= (4 if M <= 2 else 2 if M <= 8 else 1)

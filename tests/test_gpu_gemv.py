@@ -1,8 +1,8 @@
-"""The streaming GEMM variants for tiny M (the CUDA-core stream-K workers
-simt_m{1,2,4,8}_sk and the row-block warp-MMA kernels rb_m{1,2,4,8})
-against the oracle's FP32 GEMM on identical packed operands: every M from 1
-to 8 on ragged, multi-tile and long-K shapes within |y - y_ref| <= 1e-2
-|y_ref| + 1e-2 rms(y_ref); bit-exact on integer-exact inputs; split tiles
+"""The streaming GEMM variants for small M (the CUDA-core stream-K workers
+simt_m{1,2,4,8}_sk and the row-block warp-MMA kernels rb_m{1,2,4,8,16})
+against the oracle's FP32 GEMM on identical packed operands: M from 1 to 16
+on ragged, multi-tile and long-K shapes within |y - y_ref| <= 1e-2 |y_ref|
++ 1e-2 rms(y_ref); bit-exact on integer-exact inputs; split tiles
 bit-identical across runs with NaN-filled partial slots."""
 
 import numpy as np
@@ -31,7 +31,7 @@ def reference(A, packed, scales, b, rows=None):
 
 SHAPES = [synthetic.Case(f"m{m}_{n}x{k}", m, n, k, 40 + m + k // 128, "t4" if m % 2 else "normal",
                          bias=(m % 3 != 0))
-          for m in (1, 2, 3, 4, 5, 7, 8)
+          for m in (1, 2, 3, 4, 5, 7, 8, 9, 12, 16)
           for (n, k) in ((264, 384), (2048, 4096), (136, 16384))]
 
 
@@ -68,7 +68,7 @@ def test_simt_integer_exact(w4):
     # offset corrections and every partial sum are exact in fp32, so Y is the
     # exact sum rounded once to bf16
     rng = np.random.default_rng(35)
-    M, N, K = 8, 384, 2048
+    M, N, K = 16, 384, 2048
     codes = rng.integers(-7, 8, size=(N, K))
     codes[:, ::128] = 7
     e = rng.integers(-3, 0, size=(N, K // 128))
@@ -118,10 +118,10 @@ def test_simt_split_tiles_deterministic(w4):
         assert torch.equal(ys[0].view(torch.int16), ys[1].view(torch.int16)), w4.w4a16_variant_name(v)
 
 
-@pytest.mark.parametrize("case", [c for c in synthetic.WORKLOADS["sweep"] if c.M <= 8],
+@pytest.mark.parametrize("case", [c for c in synthetic.WORKLOADS["sweep"] if c.M <= 16],
                          ids=lambda c: c.name)
 def test_simt_sweep_shapes(w4, case):
-    # the sweep's M <= 8 shapes through every eligible streaming variant,
+    # the sweep's M <= 16 shapes through every eligible streaming variant,
     # all rows against the oracle
     W, A, b = synthetic.draw(case)
     packed, scales = w4.w4a16_quantize(W.cuda())
@@ -171,7 +171,8 @@ FORM_SHAPES = [(4104, 128), (4104, 256), (4104, 512), (4104, 1024), (264, 4096),
                (16392, 2048)]
 
 
-@pytest.mark.parametrize("M,variant", [(1, "rb_m1"), (3, "rb_m4"), (8, "rb_m8")])
+@pytest.mark.parametrize("M,variant", [(1, "rb_m1"), (3, "rb_m4"), (8, "rb_m8"), (11, "rb_m16"),
+                                       (16, "rb_m16")])
 def test_row_block_every_form(w4, M, variant):
     """Every launch form of the row-block kernel against the oracle: the
     forms are the host's choice for these shapes on this GPU, and together

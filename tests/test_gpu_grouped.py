@@ -61,9 +61,10 @@ def test_grouped_gemm_every_variant(w4, act):
 SMALL = [(2048, 1024), (1024, 1024), (8192, 1024), (1024, 4096), (136, 384)]
 
 
-@pytest.mark.parametrize("M,act", [(1, "bf16"), (3, "bf16"), (8, "bf16"), (5, "f16")])
+@pytest.mark.parametrize("M,act", [(1, "bf16"), (3, "bf16"), (8, "bf16"), (16, "bf16"), (5, "f16"),
+                                   (13, "f16")])
 def test_grouped_small_m_row_block(w4, M, act):
-    """Projections of a decode step (M <= 8) in one grouped launch of the
+    """Projections of a decode step (M <= 16) in one grouped launch of the
     row-block kernel (problem i on its own sub-grid, persistent form):
     every eligible rb variant against the oracle, bit-identical repeats, and
     the library's own plan."""

@@ -148,12 +148,13 @@ const Variant kVariants[] = {
     {"tc_a32_deq2_csk", {32, 2, false, 12}, false, 1, 0.48, -1.0, 0.3, 8},
     {"tc_a64_deq2_csk", {64, 2, false, 8}, false, 1, 0.50, -1.0, 0.35, 8},
     {"tc_a128_deq2_csk", {128, 2, false, 4}, false, 1, 0.65, -1.0, 0.5, 8},
-    // row-block warp-MMA kernel for M <= 1, 2, 4, 8: unit_us is the time of
-    // one (row block, group) item per warp on a full SM (rb_cost)
+    // row-block warp-MMA kernel for M <= 1, 2, 4, 8, 16: unit_us is the time
+    // of one (row block, group) item per warp on a full SM (rb_cost)
     {"rb_m1", {1, 1, true, 0, 1, kFmtInt4, true, true}, false, 1, 1.07, 1.85, 0.0},
     {"rb_m2", {2, 1, true, 0, 1, kFmtInt4, true, true}, false, 1, 1.20, 1.85, 0.0},
     {"rb_m4", {4, 1, true, 0, 1, kFmtInt4, true, true}, false, 1, 1.33, 1.85, 0.0},
     {"rb_m8", {8, 1, true, 0, 1, kFmtInt4, true, true}, false, 1, 1.58, 1.85, 0.0},
+    {"rb_m16", {16, 1, true, 0, 1, kFmtInt4, true, true}, false, 1, 2.30, 1.85, 0.0},
     // CUDA-core streaming kernel for M <= 1, 2, 4, 8: unit_us is the time of
     // one unit on one worker (a warp; many warps share an SM)
     {"simt_m1_sk", {1, 1, true, 2, 1, kFmtInt4, true}, true, 1, 6.0, 2.0, 0.8},
@@ -222,7 +223,8 @@ bool shape_ok(int64_t M, int64_t N, int64_t K) {
 }
 
 // Row-block kernel: the cost of schedule s in units of one group-item's time
-// on a full SM (two CTAs of 8 warps), fitted to GB300 measurements.
+// on a full SM (two CTAs of 8 warps; one for M <= 16, whose CTA takes an SM),
+// fitted to GB300 measurements.
 // Persistent form: CTA c runs on SM c mod num_sms; an SM with two busy CTAs
 // works through 16 group-items per unit of time, one with a single busy CTA
 // through 8 / 0.65 (measured: 8 / 0.62); the cost is the busiest SM's.
@@ -230,12 +232,13 @@ bool shape_ok(int64_t M, int64_t N, int64_t K) {
 // share of a row block's K range, plus the cluster's own cost (barriers, the
 // distributed shared-memory sum), about 1.3 items a wave.  Clusters that put
 // two CTAs on an SM run each item at 1.4 (measured: 2048 x 16384 at M = 1
-// and 4, a split of 4 on 256 CTAs 6-7% slower than a split of 2 on 128).
+// and 4, a split of 4 on 256 CTAs 6-7% slower than a split of 2 on 128);
+// with one CTA an SM the CTAs beyond the SMs form further waves instead.
 double rb_cost(const GemmSchedule& s, int64_t blocks, int64_t KB, int64_t slots, int num_sms) {
   if (s.cluster > 1) {
     const int64_t waves = (blocks * s.cluster + slots - 1) / slots;
     const int64_t per = static_cast<int64_t>(s.cluster) * kRbWarpsPerCta;
-    const double load = s.grid <= num_sms ? 0.65 : 1.4;
+    const double load = s.grid <= num_sms || slots <= num_sms ? 0.65 : 1.4;
     return static_cast<double>(waves * ((KB + per - 1) / per)) * load + 1.3 * static_cast<double>(waves);
   }
   const double thr1 = kRbWarpsPerCta / 0.65, thr2 = 2.0 * kRbWarpsPerCta;

@@ -1,17 +1,19 @@
-// W4A16 GEMM for M <= 8: a row-block kernel with warp-level MMA (sm_103a),
+// W4A16 GEMM for M <= 16: a row-block kernel with warp-level MMA (sm_103a),
 // bf16 or fp16 activations.
 //
 // "Kernel dispatch and Humming quantization in PhyAI", section "Humming makes
 // the separation useful": INT4 round-to-nearest weights, group 128 along K,
 // BF16 (or FP16) activations; the packed layout runs only through the kernels
-// that understand it.  At M <= 8 the GEMM does at most 16 flops per 0.52
+// that understand it.  At M <= 16 the GEMM does at most 32 flops per 0.52
 // bytes of codes and scales: it is bound by streaming the weight from HBM,
 // and the tcgen05 path's fixed costs per 128 x 128 unit (the converted
 // operand's TMEM round trip, MMA issue and commit, barrier hand-offs between
 // roles) are what limits it there.  This kernel has no pipeline roles: every
 // warp feeds itself, converts its codes in registers and multiplies them
 // with synchronous warp MMAs (mma.sync m16n8k16, fp32 accumulators), whose
-// 8 columns take up to 8 activation rows at no extra cost.
+// 8 columns take up to 8 activation rows at no extra cost; for M = 9 .. 16
+// each converted code fragment feeds two MMAs (activation rows 0-7 and
+// 8-15), so the conversion, the kernel's main cost, is shared by 16 rows.
 //
 // Work split.  An item is one row block (RB = 32 consecutive weight rows of
 // one 128-row storage tile) times up to two groups of 128 codes along K (one
@@ -27,8 +29,9 @@
 // sub-grid of CTAs in the persistent form (one launch, one head, for the
 // projections of a decode step).
 //
-// Streaming.  Each warp owns a ring of two shared-memory stages (one item
-// each) whose copies complete on a per-stage mbarrier, so the next item is
+// Streaming.  Each warp owns a ring of two shared-memory stages (three for
+// M <= 16, whose CTA has an SM to itself) of one item each, whose copies
+// complete on a per-stage mbarrier, so the next item is
 // in flight while one is computed, without holding a register: the codes
 // and scales by non-tensor bulk copies (cp.async.bulk), the activations by
 // one bulk copy per row for M <= 2 and by one tensor copy per group for all
@@ -53,7 +56,10 @@
 // product is unchanged.  Products of x + q (at most 11 significant bits)
 // with an activation are exact in fp32.  An MMA of an all-ones A gives the
 // group's activation sums per column, and x times those is taken off before
-// the group's fp32 scale multiplies the partial into the row's total.  With
+// the group's fp32 scale multiplies the partial into the row's total (for
+// M <= 16 one MMA of the activations as A, rows gq and gq + 8 = activation
+// rows gq and 8 + gq, against an all-ones B gives the sums of all 16 rows;
+// each lane fetches its columns' sums from the lanes that hold them).  With
 // fp16 activations the 10-bit mantissa also holds a nibble at bits 4-7: the
 // MMAs of a word split into a class of nibbles 0, 2, 4, 6 (1032 + q) and one
 // of nibbles 1, 3, 5, 7 (1152 + 16 q under 0x6480, exact), so one shift by 8
@@ -80,7 +86,6 @@ namespace {
 
 constexpr int kRbWarps = kRbWarpsPerCta;
 constexpr int kRbRows = 32;       // rows per block: two 16-row MMA tiles
-constexpr int kRbCtasPerSm = 2;   // registers <= 128, shared memory <= 113 KB
 
 struct RbArgs {
   CUtensorMap amap;        // M >= 4: A as [M][K], boxes of 136 values x MT rows
@@ -109,14 +114,14 @@ struct RbLaunch {
   int count;
 };
 
-// MT: activation rows (M <= MT; the MMA's 8 columns).  An item holds up to
-// UG groups of one row block (2 for M <= 4; 1 for M = 8, whose activation
-// rows fill the shared memory).  One stage holds the item's codes (2 KiB per
+// MT: activation rows (M <= MT; the MMA's 8 columns, twice for MT = 16).
+// An item holds up to UG groups of one row block (2 for M <= 4; 1 for
+// M = 8 and 16, whose activation rows fill the shared memory).  One stage holds the item's codes (2 KiB per
 // group), its rows' scales (64 B per group) and MT activation rows of the
 // item's groups.  M <= 2: the codes, the scales, then each activation row's
 // UG groups (contiguous in A: 256 B per group), padded by 16 B for M = 2.
-// M <= 4 and 8 (kTensor): per group, the activations as one tensor copy of
-// MT rows x 136 values (272-byte rows: the lanes' 16-byte loads of
+// M <= 4, 8 and 16 (kTensor): per group, the activations as one tensor copy
+// of MT rows x 136 values (272-byte rows: the lanes' 16-byte loads of
 // different rows fall in different bank groups; rows >= M and values past K
 // are zero) followed by the group's scales, then the codes.
 template <int MT>
@@ -135,14 +140,22 @@ struct RbCfg {
   static constexpr int kActGroup = kTensor ? kGrpBytes : kGroup * 2;   // to group gi's values
   static constexpr int kStage =
       kTensor ? (kCodeOff + kUG * kCodeBytes + 127) / 128 * 128 : kActOff + MT * kActRow;
-  static constexpr int kDepth = 2;                                // stages per warp
+  static constexpr int kNT = MT > 8 ? 2 : 1;                      // MMA column tiles
+  // Two CTAs an SM (registers <= 128, shared memory <= 113 KB) with two
+  // stages a warp; MT = 16 (32 KB of team totals, 6.5 KB stages): one CTA
+  // an SM with three stages a warp, so that as many code bytes are in flight
+  static constexpr int kCtasPerSm = MT > 8 ? 1 : 2;
+  static constexpr int kDepth = MT > 8 ? 3 : 2;                   // stages per warp
   static constexpr int kBarOff = kRbWarps * kDepth * kStage;
   static constexpr int kSmem = kBarOff + kRbWarps * kDepth * 8 + 128;   // + alignment of the base
+  static constexpr int kStatic = kRbWarps * 2 * kRbRows * MT * 4 + kRbRows * MT * 4 + 16;
   static_assert(kActOff % 16 == 0 && kCodeOff % 16 == 0 && kStage % 16 == 0,
                 "bulk-copy destinations 16-byte aligned");
   static_assert(!kTensor || (kGrpBytes % 128 == 0 && kStage % 128 == 0),
                 "tensor-copy destinations 128-byte aligned");
-  static_assert(MT >= 1 && MT <= 8, "the MMA has 8 columns");
+  static_assert(MT == 1 || MT == 2 || MT == 4 || MT == 8 || MT == 16,
+                "the MMA has 8 columns, taken once or twice");
+  static_assert(kCtasPerSm * (kSmem + kStatic + 1024) <= 228 * 1024, "shared memory of an SM");
 };
 
 // Walks a warp's items for the copies: the row blocks of its team (rb = T,
@@ -188,9 +201,10 @@ struct RbWalk {
 };
 
 template <int MT, bool F16, int G>
-__global__ void __launch_bounds__(kRbWarps * 32, kRbCtasPerSm)
+__global__ void __launch_bounds__(kRbWarps * 32, RbCfg<MT>::kCtasPerSm)
     gemv_rb_kernel(const __grid_constant__ RbLaunch<G> L) {
   using C = RbCfg<MT>;
+  constexpr int NT = C::kNT;
   // this CTA's problem and its index in the problem's sub-grid
   int prob = 0;
   if constexpr (G > 1) {
@@ -294,8 +308,8 @@ __global__ void __launch_bounds__(kRbWarps * 32, kRbCtasPerSm)
   }
 
   // the lane's totals of the block's two 16-row tiles: rows gq, gq + 8 of
-  // tile tau, columns (activation rows) 2 tq, 2 tq + 1
-  float acc[2][4] = {};
+  // tile tau, columns (activation rows) 8 nt + 2 tq, 8 nt + 2 tq + 1
+  float acc[2][NT][4] = {};
 
   // One item.  Code word j of a row (k = 32 tq + 8 j ..) gives the A
   // fragments of MMAs 2 j + h, h = 0, 1: fragment columns (2 tq, 2 tq + 1)
@@ -304,38 +318,71 @@ __global__ void __launch_bounds__(kRbWarps * 32, kRbCtasPerSm)
   auto compute_group = [&](uint32_t st, int gi) {
     constexpr uint32_t kOne = wmma16::CodeOffset<F16>::kOnes;
     constexpr float kOff = wmma16::CodeOffset<F16>::kOff;
-    const int mrow = gq < MT ? gq : MT - 1;   // columns >= M are never stored
-    uint32_t u[16];
+    // B fragments of column tile nt: activation row 8 nt + gq (for MT < 8
+    // rows >= MT repeat row MT - 1: columns >= M are never stored)
+    uint32_t b[NT][8][2];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint4 v = ptx::lds128(st + C::kActOff + mrow * C::kActRow + gi * C::kActGroup + 64 * tq + 16 * i);
-      u[4 * i] = v.x;
-      u[4 * i + 1] = v.y;
-      u[4 * i + 2] = v.z;
-      u[4 * i + 3] = v.w;
-    }
-    uint32_t b[8][2];
+    for (int nt = 0; nt < NT; ++nt) {
+      const int mrow = NT > 1 ? 8 * nt + gq : (gq < MT ? gq : MT - 1);
+      uint32_t u[16];
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        if constexpr (F16) {
-          // class h of word j: k = k0 + h + (0, 4) and k0 + h + (2, 6)
-          b[2 * j + h][0] = ptx::prmt(u[4 * j], u[4 * j + 2], h ? 0x7632u : 0x5410u);
-          b[2 * j + h][1] = ptx::prmt(u[4 * j + 1], u[4 * j + 3], h ? 0x7632u : 0x5410u);
-        } else {
-          b[2 * j + h][0] = ptx::prmt(u[4 * j + h], u[4 * j + h + 2], 0x5410u);
-          b[2 * j + h][1] = ptx::prmt(u[4 * j + h], u[4 * j + h + 2], 0x7632u);
-        }
+      for (int i = 0; i < 4; ++i) {
+        const uint4 v =
+            ptx::lds128(st + C::kActOff + mrow * C::kActRow + gi * C::kActGroup + 64 * tq + 16 * i);
+        u[4 * i] = v.x;
+        u[4 * i + 1] = v.y;
+        u[4 * i + 2] = v.z;
+        u[4 * i + 3] = v.w;
       }
-    // the group's activation sums (column 2 tq in sum[0], 2 tq + 1 in
-    // sum[1]); the MMAs run as independent accumulation chains (two for the
-    // sums, one per tile and h), added at the end
-    float sa[4] = {}, sb[4] = {};
 #pragma unroll
-    for (int mu = 0; mu < 8; mu += 2) {
-      wmma16::mma16816<F16>(sa, kOne, kOne, kOne, kOne, b[mu][0], b[mu][1]);
-      wmma16::mma16816<F16>(sb, kOne, kOne, kOne, kOne, b[mu + 1][0], b[mu + 1][1]);
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          if constexpr (F16) {
+            // class h of word j: k = k0 + h + (0, 4) and k0 + h + (2, 6)
+            b[nt][2 * j + h][0] = ptx::prmt(u[4 * j], u[4 * j + 2], h ? 0x7632u : 0x5410u);
+            b[nt][2 * j + h][1] = ptx::prmt(u[4 * j + 1], u[4 * j + 3], h ? 0x7632u : 0x5410u);
+          } else {
+            b[nt][2 * j + h][0] = ptx::prmt(u[4 * j + h], u[4 * j + h + 2], 0x5410u);
+            b[nt][2 * j + h][1] = ptx::prmt(u[4 * j + h], u[4 * j + h + 2], 0x7632u);
+          }
+        }
+    }
+    // the group's activation sums over the k of class h (the MMAs 2 j + h)
+    // for the lane's columns: sum[h][nt][c] for column 8 nt + 2 tq + c; the
+    // MMAs run as independent accumulation chains, added at the end
+    float sum[2][NT][2];
+    if constexpr (NT == 1) {
+      float sa[4] = {}, sb[4] = {};
+#pragma unroll
+      for (int mu = 0; mu < 8; mu += 2) {
+        wmma16::mma16816<F16>(sa, kOne, kOne, kOne, kOne, b[0][mu][0], b[0][mu][1]);
+        wmma16::mma16816<F16>(sb, kOne, kOne, kOne, kOne, b[0][mu + 1][0], b[0][mu + 1][1]);
+      }
+      sum[0][0][0] = sa[0];
+      sum[0][0][1] = sa[1];
+      sum[1][0][0] = sb[0];
+      sum[1][0][1] = sb[1];
+    } else {
+      // the activations as A (row gq: activation row gq, row gq + 8:
+      // activation row 8 + gq), all-ones B: every column holds the row sums;
+      // activation row 8 nt + 2 tq + c is row 2 tq + c (+ 8) of lane
+      // 4 (2 tq + c)
+      float sa[4] = {}, sb[4] = {};
+#pragma unroll
+      for (int mu = 0; mu < 8; mu += 2) {
+        wmma16::mma16816<F16>(sa, b[0][mu][0], b[1][mu][0], b[0][mu][1], b[1][mu][1], kOne, kOne);
+        wmma16::mma16816<F16>(sb, b[0][mu + 1][0], b[1][mu + 1][0], b[0][mu + 1][1], b[1][mu + 1][1],
+                              kOne, kOne);
+      }
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int src = 4 * (2 * tq + c);
+          sum[0][nt][c] = __shfl_sync(0xFFFFFFFFu, sa[2 * nt], src);
+          sum[1][nt][c] = __shfl_sync(0xFFFFFFFFu, sb[2 * nt], src);
+        }
     }
     uint32_t W[2][2][4];   // [tile][row gq, gq + 8][word]
 #pragma unroll
@@ -349,7 +396,7 @@ __global__ void __launch_bounds__(kRbWarps * 32, kRbCtasPerSm)
         W[tau][half][2] = v.z;
         W[tau][half][3] = v.w;
       }
-    float d[2][2][4] = {};   // [tile][h]
+    float d[2][2][NT][4] = {};   // [tile][h][column tile]
     if constexpr (F16) {
       // fp16 (10 mantissa bits): nibbles s and s + 4 as 1032 + q (class 0,
       // bits 0-3 of each half) or 16 (72 + q) = 1152 + 16 q (class 1, bits
@@ -371,12 +418,15 @@ __global__ void __launch_bounds__(kRbWarps * 32, kRbCtasPerSm)
         for (int h = 0; h < 2; ++h) {
           const uint32_t mask = h ? kHiMask : kLoMask, magic = h ? kHiMagic : kLoMagic;
 #pragma unroll
-          for (int tau = 0; tau < 2; ++tau)
-            wmma16::mma16816<F16>(d[tau][h], ptx::and_xor(w[tau][0], mask, magic),
-                                  ptx::and_xor(w[tau][1], mask, magic),
-                                  ptx::and_xor(w8[tau][0], mask, magic),
-                                  ptx::and_xor(w8[tau][1], mask, magic), b[2 * j + h][0],
-                                  b[2 * j + h][1]);
+          for (int tau = 0; tau < 2; ++tau) {
+            const uint32_t a0 = ptx::and_xor(w[tau][0], mask, magic);
+            const uint32_t a1 = ptx::and_xor(w[tau][1], mask, magic);
+            const uint32_t a2 = ptx::and_xor(w8[tau][0], mask, magic);
+            const uint32_t a3 = ptx::and_xor(w8[tau][1], mask, magic);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+              wmma16::mma16816<F16>(d[tau][h][nt], a0, a1, a2, a3, b[nt][2 * j + h][0], b[nt][2 * j + h][1]);
+          }
         }
       }
 #pragma unroll
@@ -385,11 +435,13 @@ __global__ void __launch_bounds__(kRbWarps * 32, kRbCtasPerSm)
         const float s0 = wmma16::lds_scale(st + C::kScaleOff + gi * C::kScaleStride + 2 * r);
         const float s1 = wmma16::lds_scale(st + C::kScaleOff + gi * C::kScaleStride + 2 * (r + 8));
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float q = fmaf(0.0625f, fmaf(-1152.0f, sb[e & 1], d[tau][1][e]),
-                               fmaf(-1032.0f, sa[e & 1], d[tau][0][e]));
-          acc[tau][e] = fmaf(e < 2 ? s0 : s1, q, acc[tau][e]);
-        }
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float q = fmaf(0.0625f, fmaf(-1152.0f, sum[1][nt][e & 1], d[tau][1][nt][e]),
+                                 fmaf(-1032.0f, sum[0][nt][e & 1], d[tau][0][nt][e]));
+            acc[tau][nt][e] = fmaf(e < 2 ? s0 : s1, q, acc[tau][nt][e]);
+          }
       }
     } else {
 #pragma unroll
@@ -397,22 +449,28 @@ __global__ void __launch_bounds__(kRbWarps * 32, kRbCtasPerSm)
 #pragma unroll
         for (int h = 0; h < 2; ++h)
 #pragma unroll
-          for (int tau = 0; tau < 2; ++tau)
-            wmma16::mma16816<F16>(d[tau][h], wmma16::code_pair16<F16>(W[tau][0][j], 2 * h),
-                                  wmma16::code_pair16<F16>(W[tau][1][j], 2 * h),
-                                  wmma16::code_pair16<F16>(W[tau][0][j], 2 * h + 1),
-                                  wmma16::code_pair16<F16>(W[tau][1][j], 2 * h + 1), b[2 * j + h][0],
-                                  b[2 * j + h][1]);
-      const float sum0 = sa[0] + sb[0], sum1 = sa[1] + sb[1];
+          for (int tau = 0; tau < 2; ++tau) {
+            const uint32_t a0 = wmma16::code_pair16<F16>(W[tau][0][j], 2 * h);
+            const uint32_t a1 = wmma16::code_pair16<F16>(W[tau][1][j], 2 * h);
+            const uint32_t a2 = wmma16::code_pair16<F16>(W[tau][0][j], 2 * h + 1);
+            const uint32_t a3 = wmma16::code_pair16<F16>(W[tau][1][j], 2 * h + 1);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+              wmma16::mma16816<F16>(d[tau][h][nt], a0, a1, a2, a3, b[nt][2 * j + h][0], b[nt][2 * j + h][1]);
+          }
 #pragma unroll
       for (int tau = 0; tau < 2; ++tau) {
         const int r = 16 * tau + gq;
         const float s0 = wmma16::lds_scale(st + C::kScaleOff + gi * C::kScaleStride + 2 * r);
         const float s1 = wmma16::lds_scale(st + C::kScaleOff + gi * C::kScaleStride + 2 * (r + 8));
-        acc[tau][0] = fmaf(s0, fmaf(-kOff, sum0, d[tau][0][0] + d[tau][1][0]), acc[tau][0]);
-        acc[tau][1] = fmaf(s0, fmaf(-kOff, sum1, d[tau][0][1] + d[tau][1][1]), acc[tau][1]);
-        acc[tau][2] = fmaf(s1, fmaf(-kOff, sum0, d[tau][0][2] + d[tau][1][2]), acc[tau][2]);
-        acc[tau][3] = fmaf(s1, fmaf(-kOff, sum1, d[tau][0][3] + d[tau][1][3]), acc[tau][3]);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const float sum0 = sum[0][nt][0] + sum[1][nt][0], sum1 = sum[0][nt][1] + sum[1][nt][1];
+          acc[tau][nt][0] = fmaf(s0, fmaf(-kOff, sum0, d[tau][0][nt][0] + d[tau][1][nt][0]), acc[tau][nt][0]);
+          acc[tau][nt][1] = fmaf(s0, fmaf(-kOff, sum1, d[tau][0][nt][1] + d[tau][1][nt][1]), acc[tau][nt][1]);
+          acc[tau][nt][2] = fmaf(s1, fmaf(-kOff, sum0, d[tau][0][nt][2] + d[tau][1][nt][2]), acc[tau][nt][2]);
+          acc[tau][nt][3] = fmaf(s1, fmaf(-kOff, sum1, d[tau][0][nt][3] + d[tau][1][nt][3]), acc[tau][nt][3]);
+        }
       }
     }
   };
@@ -427,23 +485,27 @@ __global__ void __launch_bounds__(kRbWarps * 32, kRbCtasPerSm)
 #pragma unroll
       for (int tau = 0; tau < 2; ++tau)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int n = r0 + 16 * tau + gq + (e >= 2 ? 8 : 0);
-          const int m = 2 * tq + (e & 1);
-          if (m < g.M && n < g.N) {
-            float t = acc[tau][e];
-            if (g.bias != nullptr) t += wmma16::act_to_f32<F16>(g.bias[n]);
-            g.Y[static_cast<int64_t>(m) * g.N + n] = wmma16::f32_to_out<F16>(t);
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int n = r0 + 16 * tau + gq + (e >= 2 ? 8 : 0);
+            const int m = 8 * nt + 2 * tq + (e & 1);
+            if (m < g.M && n < g.N) {
+              float t = acc[tau][nt][e];
+              if (g.bias != nullptr) t += wmma16::act_to_f32<F16>(g.bias[n]);
+              g.Y[static_cast<int64_t>(m) * g.N + n] = wmma16::f32_to_out<F16>(t);
+            }
           }
-        }
     } else {
 #pragma unroll
       for (int tau = 0; tau < 2; ++tau)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int m = 2 * tq + (e & 1);
-          if (m < MT) tbuf[warp][nflush & 1][16 * tau + gq + (e >= 2 ? 8 : 0)][m] = acc[tau][e];
-        }
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int m = 8 * nt + 2 * tq + (e & 1);
+            if (m < MT) tbuf[warp][nflush & 1][16 * tau + gq + (e >= 2 ? 8 : 0)][m] = acc[tau][nt][e];
+          }
       ptx::named_barrier_sync(1 + team, WK * 32);
       if (wt == 0) {
         for (int e = lane; e < kRbRows * MT; e += 32) {
@@ -465,7 +527,9 @@ __global__ void __launch_bounds__(kRbWarps * 32, kRbCtasPerSm)
 #pragma unroll
     for (int tau = 0; tau < 2; ++tau)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) acc[tau][e] = 0.0f;
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[tau][nt][e] = 0.0f;
     ++nflush;
   };
 
@@ -649,8 +713,7 @@ int gemv_rb_rows(int act_tile) {
 }
 
 int gemv_rb_ctas_per_sm(int act_tile) {
-  (void)act_tile;
-  return kRbCtasPerSm;
+  return act_tile > 8 ? RbCfg<16>::kCtasPerSm : RbCfg<8>::kCtasPerSm;
 }
 
 size_t gemv_rb_smem_bytes(int act_tile) {
@@ -659,6 +722,7 @@ size_t gemv_rb_smem_bytes(int act_tile) {
     case 2: return RbCfg<2>::kSmem;
     case 4: return RbCfg<4>::kSmem;
     case 8: return RbCfg<8>::kSmem;
+    case 16: return RbCfg<16>::kSmem;
     default: return 0;
   }
 }
@@ -676,6 +740,7 @@ cudaError_t launch_gemv_rb(const GemmKernelConfig& c, const GemmGroup& grp, bool
     case 2: return f16 ? launch_rb_any<2, true>(grp, use_pdl, stream) : launch_rb_any<2, false>(grp, use_pdl, stream);
     case 4: return f16 ? launch_rb_any<4, true>(grp, use_pdl, stream) : launch_rb_any<4, false>(grp, use_pdl, stream);
     case 8: return f16 ? launch_rb_any<8, true>(grp, use_pdl, stream) : launch_rb_any<8, false>(grp, use_pdl, stream);
+    case 16: return f16 ? launch_rb_any<16, true>(grp, use_pdl, stream) : launch_rb_any<16, false>(grp, use_pdl, stream);
     default: return cudaErrorInvalidConfiguration;
   }
 }

@@ -65,7 +65,7 @@ struct GemmKernelConfig {
                       // act_tile, INT4 weights: the CUDA-core stream-K workers
                       // (gemv.cu, act_tile 1, 2, 4 or 8), or with rb:
   bool rb = false;    // the row-block warp-MMA kernel (gemv_rb.cu, act_tile 1, 2,
-                      // 4 or 8)
+                      // 4, 8 or 16)
 };
 
 // The CUDA-core streaming kernel: every warp is a stream-K worker with two
@@ -201,8 +201,8 @@ cudaError_t launch_repack_rowmajor(const void* rowmajor, int64_t N, int64_t K, v
 // differ, the quotients that differ in the normal range and anywhere.
 cudaError_t launch_quotient_selftest(int mode, unsigned long long* counts, cudaStream_t stream);
 
-// The row-block warp-MMA kernel (gemv_rb.cu): one problem, INT4 weights, bf16
-// or fp16 activations, M <= act_tile (1, 2, 4, 8).  Persistent (cluster <= 1):
+// The row-block warp-MMA kernel (gemv_rb.cu): INT4 weights, bf16 or fp16
+// activations, M <= act_tile (1, 2, 4, 8, 16), one problem or a group.  Persistent (cluster <= 1):
 // any grid, teams of `team` warps walk row blocks round-robin.  Cluster
 // split (cluster > 1): grid = row blocks x cluster, team = 8.  Rows per block
 // and resident CTAs per SM for an act_tile.
