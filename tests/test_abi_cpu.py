@@ -326,3 +326,21 @@ def test_row_block_schedule_forms(built_lib):
     assert L.w4a16_variant_schedule(rb1, 2, 4096, 1024, 152, out) == w4.W4A16_ERR_NO_VARIANT
     assert L.w4a16_variant_schedule(rb1, 1, 4096, 1024, -1, out) == w4.W4A16_ERR_INVALID_ARG
     assert L.w4a16_variant_schedule(rb1, 1, 4096, 1024, 152, None) == w4.W4A16_ERR_INVALID_ARG
+
+
+def test_row_block_two_column_tiles(built_lib):
+    """rb_m16 (two MMA column tiles, one CTA of 8 warps per SM): persistent
+    grids stay within the SMs, few row blocks with long K take the cluster
+    split, and the rule leaves the sweep's M = 16 shapes, where it measured
+    slower than the tcgen05 kernel, to the tcgen05 variants."""
+    rb16 = w4.variant_id("rb_m16")
+    assert w4.w4a16_variant_eligible(rb16, 16, 8192, 8192)
+    assert not w4.w4a16_variant_eligible(rb16, 17, 8192, 8192)
+    for N, K in ((8192, 8192), (16384, 2048), (28672, 4096), (4104, 1024)):
+        s = w4.w4a16_variant_schedule(rb16, 16, N, K, 152)
+        assert s["cluster"] == 1 and 1 <= s["grid"] <= 152, (N, K, s)
+    assert w4.w4a16_variant_schedule(rb16, 16, 264, 16384, 152) == dict(
+        grid=72, dp_tiles=0, sk_units=0, cluster=8, team=8)
+    for N, K in ((16384, 2048), (2048, 16384), (8192, 8192)):
+        name = w4.w4a16_variant_name(w4.w4a16_select_variant(16, N, K))
+        assert name.startswith("tc_"), (N, K, name)

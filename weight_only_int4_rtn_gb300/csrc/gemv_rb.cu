@@ -142,8 +142,9 @@ struct RbCfg {
       kTensor ? (kCodeOff + kUG * kCodeBytes + 127) / 128 * 128 : kActOff + MT * kActRow;
   static constexpr int kNT = MT > 8 ? 2 : 1;                      // MMA column tiles
   // Two CTAs an SM (registers <= 128, shared memory <= 113 KB) with two
-  // stages a warp; MT = 16 (32 KB of team totals, 6.5 KB stages): one CTA
-  // an SM with three stages a warp, so that as many code bytes are in flight
+  // stages a warp; MT = 16 (32 KB of team totals, 6.5 KB stages, about 165
+  // registers): one CTA an SM with three stages a warp (48 KiB of codes in
+  // flight per SM against 64 KiB with two CTAs)
   static constexpr int kCtasPerSm = MT > 8 ? 1 : 2;
   static constexpr int kDepth = MT > 8 ? 3 : 2;                   // stages per warp
   static constexpr int kBarOff = kRbWarps * kDepth * kStage;
