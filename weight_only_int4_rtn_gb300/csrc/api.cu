@@ -64,11 +64,45 @@ struct DeviceInfo {
   bool ready = false;
   int num_sms = 0;
   uint32_t* error_word = nullptr;
+  // clusters of 2, 4, 8 CTAs that each need a whole SM (every tcgen05 GEMM
+  // instance) the GPU holds at once; -1: unknown
+  int whole_sm_clusters[3] = {-1, -1, -1};
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mutex;
 
-// Current device's SM count and error-word address (looked up once).
+// Never launched: the occupancy query's stand-in for a CTA that needs a
+// whole SM (512 threads, more than half of the shared memory).
+__global__ void whole_sm_cta_kernel() {}
+constexpr int kWholeSmSmem = 200 * 1024;
+
+// Clusters of `cluster` whole-SM CTAs resident at once on the current device
+// (a cluster's CTAs share one GPC, so this can be below SMs / cluster).
+int query_whole_sm_clusters(int cluster) {
+  if (cudaFuncSetAttribute(whole_sm_cta_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kWholeSmSmem) != cudaSuccess)
+    return -1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(cluster));
+  cfg.blockDim = dim3(512);
+  cfg.dynamicSmemBytes = kWholeSmSmem;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = static_cast<unsigned>(cluster);
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, whole_sm_cta_kernel, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return -1;
+  }
+  return n;
+}
+
+// Current device's SM count, error-word address and whole-SM cluster
+// capacity (looked up once).
 bool device_info(DeviceInfo& out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
@@ -82,10 +116,25 @@ bool device_info(DeviceInfo& out) {
     if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return false;
     d.num_sms = sms;
     d.error_word = static_cast<uint32_t*>(p);
+    // host-side queries (no stream work); relaxed capture mode so that a
+    // first call inside a stream capture leaves the capture intact
+    cudaStreamCaptureMode mode = cudaStreamCaptureModeRelaxed;
+    const bool swapped = cudaThreadExchangeStreamCaptureMode(&mode) == cudaSuccess;
+    for (int i = 0; i < 3; ++i) d.whole_sm_clusters[i] = query_whole_sm_clusters(2 << i);
+    if (swapped) (void)cudaThreadExchangeStreamCaptureMode(&mode);
     d.ready = true;
   }
   out = d;
   return true;
+}
+
+// Clusters of `cluster` (2, 4 or 8) whole-SM CTAs the current device holds
+// at once; -1 without a device.
+int resident_whole_sm_clusters(int cluster) {
+  DeviceInfo dev;
+  if (!device_info(dev)) return -1;
+  const int i = cluster == 2 ? 0 : cluster == 4 ? 1 : cluster == 8 ? 2 : -1;
+  return i < 0 ? -1 : dev.whole_sm_clusters[i];
 }
 
 // The current device's SM count (the GB300 count without a device).
@@ -331,10 +380,17 @@ GemmSchedule make_schedule(const Variant& v, int64_t M, int64_t N, int64_t K, in
   const int64_t units = tiles * KB;
   if (v.csk > 1) {
     // the largest power-of-two cluster (<= v.csk, <= KB) such that every
-    // tile's cluster is resident at once (tiles * cluster <= SMs); grid 0
-    // when no cluster of 2 or more fits
+    // tile's cluster is resident at once: tiles * cluster <= SMs and, on a
+    // device, tiles <= the clusters of that size it holds at once (a
+    // cluster's CTAs share one GPC: on GB300 16 tiles in clusters of 8 ran
+    // in two waves, 2048 x 16384 at M = 16 in 21.8 us against 11.1 us for
+    // 1024 x 16384); grid 0 when no cluster of 2 or more fits
+    const auto resident = [&](int S2) {
+      const int r = resident_whole_sm_clusters(S2);
+      return r < 0 || tiles <= r;
+    };
     int S = 1;
-    while (2 * S <= v.csk && 2 * S <= KB && tiles * 2 * S <= num_sms) S *= 2;
+    while (2 * S <= v.csk && 2 * S <= KB && tiles * 2 * S <= num_sms && resident(2 * S)) S *= 2;
     s.cluster = S;
     s.grid = S > 1 ? static_cast<int>(tiles * S) : 0;
     s.dp_tiles = 0;
