@@ -181,9 +181,9 @@ const Variant kVariants[] = {
     {"tc_a64_deq2_dp", {64, 2, false, 8}, false, 1, 0.47},
     {"tc_a128_deq2_dp", {128, 2, false, 4}, false, 1, 0.70},
     // units of two groups (one 16 KiB copy of codes per unit)
-    {"tc_a16_grp_sk_u2", {16, 2, true, 8, 2}, true, 1, 0.76},
-    {"tc_a16_grp_sk8_u2", {16, 2, true, 8, 2}, true, 8, 0.61},
-    {"tc_a16_grp_dp_u2", {16, 2, true, 8, 2}, false, 1, 0.66},
+    {"tc_a16_grp_sk_u2", {16, 2, true, 8, 2}, true, 1, 0.84},
+    {"tc_a16_grp_sk8_u2", {16, 2, true, 8, 2}, true, 8, 0.73},
+    {"tc_a16_grp_dp_u2", {16, 2, true, 8, 2}, false, 1, 0.76},
     {"tc_a16_deq2_sk_u2", {16, 2, false, 8, 2}, true, 1, 0.92},
     {"tc_a16_deq2_dp_u2", {16, 2, false, 8, 2}, false, 1, 0.86},
     {"tc_a32_deq2_sk_u2", {32, 2, false, 6, 2}, true, 1, 1.01},
@@ -193,7 +193,7 @@ const Variant kVariants[] = {
     // most 8), partials summed through distributed shared memory; for few
     // tiles of long K
     {"tc_a16_grp_csk", {16, 2, true, 16}, false, 1, 0.44, -1.0, 0.3, 8},
-    {"tc_a16_grp_csk_u2", {16, 2, true, 8, 2}, false, 1, 0.66, -1.0, 0.3, 8},
+    {"tc_a16_grp_csk_u2", {16, 2, true, 8, 2}, false, 1, 0.80, -1.0, 0.3, 8},
     {"tc_a32_deq2_csk", {32, 2, false, 12}, false, 1, 0.48, -1.0, 0.3, 8},
     {"tc_a64_deq2_csk", {64, 2, false, 8}, false, 1, 0.50, -1.0, 0.35, 8},
     {"tc_a128_deq2_csk", {128, 2, false, 4}, false, 1, 0.65, -1.0, 0.5, 8},
@@ -202,7 +202,7 @@ const Variant kVariants[] = {
     {"rb_m1", {1, 1, true, 0, 1, kFmtInt4, true, true}, false, 1, 1.07, 1.85, 0.0},
     {"rb_m2", {2, 1, true, 0, 1, kFmtInt4, true, true}, false, 1, 1.20, 1.85, 0.0},
     {"rb_m4", {4, 1, true, 0, 1, kFmtInt4, true, true}, false, 1, 1.33, 1.85, 0.0},
-    {"rb_m8", {8, 1, true, 0, 1, kFmtInt4, true, true}, false, 1, 1.58, 1.85, 0.0},
+    {"rb_m8", {8, 1, true, 0, 1, kFmtInt4, true, true}, false, 1, 1.45, 1.85, 0.0},
     {"rb_m16", {16, 1, true, 0, 1, kFmtInt4, true, true}, false, 1, 2.30, 1.85, 0.0},
     // CUDA-core streaming kernel for M <= 1, 2, 4, 8: unit_us is the time of
     // one unit on one worker (a warp; many warps share an SM)
@@ -464,6 +464,11 @@ bool variantf4_eligible(int id, int64_t M, int64_t N, int64_t K) {
 constexpr double kHeadUs = 3.71;
 constexpr double kSplitUs = 2.44;
 constexpr double kSplitUsPerCol = 0.051;
+// a split tile's last contributor sums the others' partials: each
+// contributor beyond two lengthens that tail (fitted, with the unit times
+// of the two-group and row-block variants, to 60 shapes at M = 1 .. 816:
+// mean regret of the rule 1.65% -> 0.73%, worst 35% -> 12%)
+constexpr double kSplitUsPerContributor = 0.2;
 
 double estimate_sched(const Variant& v, const GemmSchedule& s, int64_t K, int64_t N = 0,
                       int num_sms = kDefaultSms) {
@@ -481,7 +486,13 @@ double estimate_sched(const Variant& v, const GemmSchedule& s, int64_t K, int64_
   const int64_t sk_per_cta = (s.sk_units + s.grid - 1) / s.grid;
   double t = (v.head_us >= 0.0 ? v.head_us : kHeadUs) +
              static_cast<double>(dp_per_cta * KB + sk_per_cta) * v.unit_us;
-  if (s.sk_units > 0) t += v.split_us >= 0.0 ? v.split_us : kSplitUs + kSplitUsPerCol * v.cfg.act_tile;
+  if (s.sk_units > 0) {
+    t += v.split_us >= 0.0 ? v.split_us : kSplitUs + kSplitUsPerCol * v.cfg.act_tile;
+    if (!v.cfg.simt && sk_per_cta > 0 && sk_per_cta < KB) {
+      const int64_t contributors = (KB + sk_per_cta - 1) / sk_per_cta;
+      if (contributors > 2) t += kSplitUsPerContributor * static_cast<double>(contributors - 2);
+    }
+  }
   return t;
 }
 
