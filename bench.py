@@ -976,6 +976,71 @@ def time_oracle(workload, budget_s: float, weights="int4", rows=1024):
                 sample=sample, seconds=round(dt, 2), passes=passes)
 
 
+# the shapes on which the selection rule is checked against measurement: the
+# metric's M range on the sweep's and the workloads' weight shapes
+REGRET_NK = [(16384, 2048), (2048, 16384), (8192, 8192), (4096, 4096), (2048, 8192),
+             (28672, 4096), (1024, 4096), (4096, 14336)]
+REGRET_SHAPES = ([(m, n, k) for m in (1, 2, 4, 8, 16, 32, 64) for n, k in REGRET_NK] +
+                 [(m, n, k) for m in (50, 128, 256, 816)
+                  for n, k in ((8192, 8192), (2048, 2048), (32768, 2048), (1024, 4096))])
+
+
+def rule_regret(dev, trials=10):
+    """Every eligible INT4 (bf16) variant timed back to back on each shape of
+    REGRET_SHAPES (weights static, copies rotating past 3x L2): the variant
+    the library's cost-model rule selects on this device against the fastest
+    measured one.  The measured, memoized choice ("Kernel dispatch and
+    Humming quantization in PhyAI", section "Keep selection work out of
+    repeated inference") is the tuners'; this checks the rule that shapes
+    without a table entry take."""
+    import torch
+    import weight_only_int4_rtn_gb300 as w4
+    from weight_only_int4_rtn_gb300 import synthetic
+    w4.w4a16_set_weights_static(True)
+    rows = []
+    for (M, N, K) in REGRET_SHAPES:
+        case = synthetic.Case("regret", M, N, K, 3)
+        W = synthetic.draw_weight_only(case.seed, N, K, case.wdist).to(dev)
+        packed, scales = w4.w4a16_quantize(W)
+        torch.cuda.synchronize(dev)
+        del W
+        _, A, _ = synthetic.draw(case)
+        A = A.to(dev)
+        Y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        nb = packed.numel() + scales.numel() * 2
+        ncp = max(1, min(16, -(-3 * L2_BYTES // nb)))
+        cps = [(packed, scales)] + [(packed.clone(), scales.clone()) for _ in range(ncp - 1)]
+        reps = max(8, 2 * ncp)
+        times = {}
+        for v in range(w4.w4a16_variant_count()):
+            if not w4.w4a16_variant_eligible(v, M, N, K):
+                continue
+            ws = torch.zeros(max(w4.w4a16_variant_workspace_bytes(v, M, N, K), 256),
+                             dtype=torch.uint8, device=dev)
+
+            def one(i, st=None, v=v, ws=ws):
+                w4.w4a16_gemm(A, cps[i % ncp][0], cps[i % ncp][1], Y=Y, workspace=ws, variant=v,
+                              stream=st)
+            for i in range(2):
+                one(i)
+            g = graph_of(dev, one, reps)
+            times[w4.w4a16_variant_name(v)] = time_graph_us(dev, g, reps, trials)
+            del g
+        if w4.w4a16_get_device_error() != w4.W4A16_OK:
+            raise RuntimeError("device error while timing the variants")
+        pick = w4.w4a16_variant_name(w4.w4a16_select_variant(M, N, K))
+        best = min(times, key=times.get)
+        rows.append(dict(shape=[M, N, K], rule=pick, rule_us=round(times[pick], 3), best=best,
+                         best_us=round(times[best], 3),
+                         regret=round(times[pick] / times[best] - 1.0, 4)))
+        del cps, packed, scales
+    regrets = [r["regret"] for r in rows]
+    return dict(metric="selection rule regret (rule's variant / fastest variant - 1)",
+                unit="fraction", shapes=len(rows), mean=round(sum(regrets) / len(regrets), 4),
+                worst=max(regrets), above_5pct=sum(1 for x in regrets if x > 0.05),
+                kernel_sources=kernel_source_hash(), rows=rows)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -1014,6 +1079,9 @@ def main():
                          "then waits for the previous kernel before its first weight copy")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--rule-regret", action="store_true",
+                    help="instead of the step: time every eligible INT4 variant on a grid of "
+                         "72 shapes and report the selection rule's regret (one JSON line)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -1050,6 +1118,11 @@ def main():
 
     from __graft_entry__ import build
     build()
+    if args.rule_regret:
+        import torch
+        if rank == 0:
+            print(json.dumps(rule_regret(torch.device("cuda", 0))), flush=True)
+        return 0
     out = run_gpu(args, rank, world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = time_oracle(workload_cases(args), args.cpu_budget, args.weights)

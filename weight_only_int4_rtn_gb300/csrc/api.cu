@@ -466,7 +466,7 @@ constexpr double kSplitUs = 2.44;
 constexpr double kSplitUsPerCol = 0.051;
 // a split tile's last contributor sums the others' partials: each
 // contributor beyond two lengthens that tail (fitted, with the unit times
-// of the two-group and row-block variants, to 60 shapes at M = 1 .. 816:
+// of the two-group and row-block variants, to 72 shapes at M = 1 .. 816:
 // mean regret of the rule 1.65% -> 0.73%, worst 35% -> 12%)
 constexpr double kSplitUsPerContributor = 0.2;
 
